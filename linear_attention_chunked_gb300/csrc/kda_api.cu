@@ -1,0 +1,306 @@
+// Host side of the C ABI declared in include/kda.h: validation, workspace layout, launches.
+// No entry point allocates memory or synchronises the device (kda_read_device_status excepted,
+// which exists to synchronise).
+#include <mutex>
+
+#include "kda_internal.cuh"
+
+using namespace kda;
+
+namespace {
+
+constexpr size_t SMEM_INTRA_FWD = (4 * CH * LDP + 3 * CH * LDA + CH + GEMM_SCRATCH) * 4;
+constexpr size_t SMEM_CHAIN = (D * (SLICE + 1) + CH * (SLICE + 1) + GEMM_SCRATCH) * 4;
+constexpr size_t SMEM_BWD_GEMMS = GEMM_SCRATCH * 4;
+constexpr size_t SMEM_BWD_INTRA = (4 * CH * LDP + 3 * CH * LDA + 3 * CH + NTHR) * 4;
+constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
+
+std::mutex g_mu;
+bool g_ready[128];
+
+// Once per device: check it is an sm_103 part and raise the dynamic shared memory limits.
+kda_status setup_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev < 0 || dev >= 128) return KDA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ready[dev]) return KDA_OK;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
+    struct { const void* f; size_t smem; } attrs[] = {
+        {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd, SMEM_CHAIN},
+        {(const void*)k_chain_bwd, SMEM_CHAIN},     {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
+        {(const void*)k_bwd_intra, SMEM_BWD_INTRA}, {(const void*)k_walk, SMEM_WALK},
+    };
+    for (auto& a : attrs)
+        if (cudaFuncSetAttribute(a.f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(a.smem)) !=
+            cudaSuccess)
+            return KDA_ERR_CUDA;
+    g_ready[dev] = true;
+    return KDA_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+kda_status check_problem(const kda_problem* p) {
+    if (!p) return KDA_ERR_INVALID_ARG;
+    if (p->d != D) return KDA_ERR_UNSUPPORTED;
+    if (p->H < 1 || p->H > 65535 || p->N < 1 || p->T < 0 || p->T > INT32_MAX)
+        return KDA_ERR_INVALID_ARG;
+    if (p->gate != KDA_GATE_G && p->gate != KDA_GATE_RAW) return KDA_ERR_INVALID_ARG;
+    if (p->l2norm != 0 && p->l2norm != 1) return KDA_ERR_INVALID_ARG;
+    if (!p->cu_seqlens || (reinterpret_cast<uintptr_t>(p->cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
+    if (!(p->l2_eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+// Required pointers must be non-null and 16-byte aligned; optional ones only aligned.
+bool req(const void* ptr) { return ptr && aligned16(ptr); }
+bool opt(const void* ptr) { return !ptr || aligned16(ptr); }
+
+kda_status check_inputs(const kda_problem* p, const void* q, const void* k, const void* v,
+                        const void* beta, const float* g, const float* A_log,
+                        const float* dt_bias) {
+    if (p->T > 0 && !(req(q) && req(k) && req(v) && req(g) && opt(beta) && beta))
+        return KDA_ERR_INVALID_ARG;
+    if (p->gate == KDA_GATE_RAW && !(req(A_log) && req(dt_bias))) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+Params make_params(const kda_problem* pr, const Layout& L, void* ws) {
+    Params p{};
+    p.T = pr->T;
+    p.N = pr->N;
+    p.H = pr->H;
+    p.gate_raw = pr->gate == KDA_GATE_RAW;
+    p.l2n = pr->l2norm;
+    p.scale = pr->scale;
+    p.eps = pr->l2_eps;
+    p.cu = pr->cu_seqlens;
+    p.maxC = L.maxC;
+    char* w = static_cast<char*>(ws);
+    p.status = reinterpret_cast<int*>(w + L.status);
+    p.nchunks = reinterpret_cast<int*>(w + L.nchunks);
+    p.doc_off = reinterpret_cast<int*>(w + L.doc_off);
+    p.chunk_tab = reinterpret_cast<int4*>(w + L.chunk_tab);
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
+    p.gam = f(L.gam);
+    p.W = f(L.W);
+    p.U = f(L.U);
+    p.Qg = f(L.Qg);
+    p.Kb = f(L.Kb);
+    p.Aqk = f(L.Aqk);
+    p.Akk = f(L.Akk);
+    p.Minv = f(L.Minv);
+    return p;
+}
+
+void set_bwd_regions(Params& p, const Layout& L, void* ws) {
+    char* w = static_cast<char*>(ws);
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
+    p.dS1 = f(L.dS1);
+    p.dDelta = f(L.dDelta);
+    p.dR = f(L.dR);
+    p.P = f(L.P);
+    p.dQg = f(L.dQg);
+    p.dKb = f(L.dKb);
+    p.dAqk = f(L.dAqk);
+    p.dM = f(L.dM);
+    p.rsum = f(L.rsum);
+    p.pdA = f(L.pdA);
+    p.pddt = f(L.pddt);
+}
+
+void set_inputs(Params& p, const void* q, const void* k, const void* v, const void* beta,
+                const float* g, const float* A_log, const float* dt_bias) {
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.beta = static_cast<const __nv_bfloat16*>(beta);
+    p.g = g;
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+}
+
+kda_status launched() {
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// plan + intra-chunk products (shared by every op)
+kda_status run_prologue(const Params& p, cudaStream_t st) {
+    k_plan<<<1, NTHR, 0, st>>>(p);
+    if (p.maxC > 0) k_intra_fwd<<<dim3(unsigned(p.maxC), p.H), NTHR, SMEM_INTRA_FWD, st>>>(p);
+    return launched();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, bad size, H < 1)";
+        case KDA_ERR_UNSUPPORTED: return "unsupported (head dim must be 128; device must be sm_103)";
+        case KDA_ERR_WORKSPACE: return "workspace or saved buffer too small";
+        case KDA_ERR_CUDA: return "CUDA runtime error";
+        case KDA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+        case KDA_ERR_DEVICE_CHECK: return "device-side validation failed (malformed cu_seqlens)";
+    }
+    return "unknown status";
+}
+
+kda_status kda_workspace_size(const kda_problem* p, int op, size_t* ws_bytes, size_t* saved_bytes) {
+    if (kda_status s = check_problem(p)) return s;
+    const Layout L = make_layout(p->T, p->N, p->H);
+    size_t ws = 0;
+    switch (op) {
+        case KDA_OP_FWD: ws = L.ws_fwd; break;
+        case KDA_OP_BWD_SAVED: ws = L.ws_bwd_saved; break;
+        case KDA_OP_BWD_REPLAY: ws = L.ws_bwd_replay; break;
+        case KDA_OP_FRAGMENT: ws = L.ws_frag; break;
+        case KDA_OP_WALK: ws = 0; break;
+        default: return KDA_ERR_INVALID_ARG;
+    }
+    if (ws_bytes) *ws_bytes = ws;
+    if (saved_bytes) *saved_bytes = L.saved_bytes;
+    return KDA_OK;
+}
+
+kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const void* v,
+                   const void* beta, const float* g_or_a, const float* A_log,
+                   const float* dt_bias, const float* h0, void* o, float* ht, void* saved,
+                   void* ws, size_t ws_bytes, kda_stream_t stream) {
+    if (kda_status s = check_problem(pr)) return s;
+    if (kda_status s = check_inputs(pr, q, k, v, beta, g_or_a, A_log, dt_bias)) return s;
+    if ((pr->T > 0 && !req(o)) || !opt(h0) || !opt(ht) || !opt(saved) || !req(ws))
+        return KDA_ERR_INVALID_ARG;
+    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    if (ws_bytes < L.ws_fwd) return KDA_ERR_WORKSPACE;
+    if (kda_status s = setup_device()) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Params p = make_params(pr, L, ws);
+    set_inputs(p, q, k, v, beta, g_or_a, A_log, dt_bias);
+    p.h0 = h0;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.ht = ht;
+    if (saved) {
+        p.sS = reinterpret_cast<float*>(static_cast<char*>(saved) + L.sv_S);
+        p.sDelta = reinterpret_cast<float*>(static_cast<char*>(saved) + L.sv_Delta);
+    }
+    if (kda_status s = run_prologue(p, st)) return s;
+    k_chain_fwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FWD_OUT);
+    return launched();
+}
+
+kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const void* v,
+                   const void* beta, const float* g_or_a, const float* A_log,
+                   const float* dt_bias, const float* h0, const void* dO, const float* dht,
+                   const void* saved, void* dq, void* dk, void* dv, void* dbeta, float* dg_or_da,
+                   float* dA_log, float* ddt_bias, float* dh0, void* ws, size_t ws_bytes,
+                   kda_stream_t stream) {
+    if (kda_status s = check_problem(pr)) return s;
+    if (kda_status s = check_inputs(pr, q, k, v, beta, g_or_a, A_log, dt_bias)) return s;
+    if (pr->T > 0 && !(req(dO) && req(dq) && req(dk) && req(dv) && req(dbeta) && req(dg_or_da)))
+        return KDA_ERR_INVALID_ARG;
+    if (pr->gate == KDA_GATE_RAW && !(req(dA_log) && req(ddt_bias))) return KDA_ERR_INVALID_ARG;
+    if (!opt(h0) || !opt(dht) || !opt(dh0) || !opt(saved) || !req(ws)) return KDA_ERR_INVALID_ARG;
+    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    if (ws_bytes < (saved ? L.ws_bwd_saved : L.ws_bwd_replay)) return KDA_ERR_WORKSPACE;
+    if (kda_status s = setup_device()) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Params p = make_params(pr, L, ws);
+    set_bwd_regions(p, L, ws);
+    set_inputs(p, q, k, v, beta, g_or_a, A_log, dt_bias);
+    p.h0 = h0;
+    p.dht = dht;
+    p.dO = static_cast<const __nv_bfloat16*>(dO);
+    p.dq = static_cast<__nv_bfloat16*>(dq);
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.dbeta = static_cast<__nv_bfloat16*>(dbeta);
+    p.dg = dg_or_da;
+    p.dA_log = dA_log;
+    p.ddt_bias = ddt_bias;
+    p.dh0 = dh0;
+    char* sv = saved ? static_cast<char*>(const_cast<void*>(saved))
+                     : static_cast<char*>(ws) + L.replay;
+    p.sS = reinterpret_cast<float*>(sv + L.sv_S);
+    p.sDelta = reinterpret_cast<float*>(sv + L.sv_Delta);
+    if (kda_status s = run_prologue(p, st)) return s;
+    if (!saved) {
+        // checkpoint replay: recompute the per-chunk states and write vectors
+        Params r = p;
+        r.o = nullptr;
+        r.ht = nullptr;
+        k_chain_fwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(r, CHAIN_FWD_OUT);
+    }
+    k_chain_bwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_BWD);
+    if (L.maxC > 0) {
+        const dim3 grid(unsigned(L.maxC), pr->H);
+        k_bwd_gemms<<<grid, NTHR, SMEM_BWD_GEMMS, st>>>(p);
+        k_bwd_intra<<<grid, NTHR, SMEM_BWD_INTRA, st>>>(p);
+    }
+    if (p.gate_raw) k_param_reduce<<<pr->H, D, 0, st>>>(p);
+    return launched();
+}
+
+kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, const void* k,
+                                const void* v, const void* beta, const float* g_or_a,
+                                const float* A_log, const float* dt_bias, const void* dO,
+                                float* M, float* B_or_C, void* ws, size_t ws_bytes,
+                                kda_stream_t stream) {
+    if (kda_status s = check_problem(pr)) return s;
+    if (kda_status s = check_inputs(pr, q, k, v, beta, g_or_a, A_log, dt_bias)) return s;
+    if (mode != KDA_FRAG_FWD && mode != KDA_FRAG_BWD) return KDA_ERR_INVALID_ARG;
+    if (!req(B_or_C) || !req(ws)) return KDA_ERR_INVALID_ARG;
+    if (mode == KDA_FRAG_FWD && !req(M)) return KDA_ERR_INVALID_ARG;
+    if (mode == KDA_FRAG_BWD && pr->T > 0 && !req(dO)) return KDA_ERR_INVALID_ARG;
+    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    if (ws_bytes < L.ws_frag) return KDA_ERR_WORKSPACE;
+    if (kda_status s = setup_device()) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Params p = make_params(pr, L, ws);
+    set_inputs(p, q, k, v, beta, g_or_a, A_log, dt_bias);
+    p.dO = static_cast<const __nv_bfloat16*>(dO);
+    p.fragM = M;
+    p.fragB = B_or_C;
+    if (kda_status s = run_prologue(p, st)) return s;
+    if (mode == KDA_FRAG_FWD)
+        k_chain_fwd<<<dim3(pr->N, pr->H, 2 * NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FRAG_MB);
+    else
+        k_chain_bwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FRAG_C);
+    return launched();
+}
+
+kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int32_t H,
+                             const float* M, const float* B, const float* S0, int reverse,
+                             float* S_in, float* S_final, kda_stream_t stream) {
+    if (N < 1 || H < 1 || F < 0 || !doc_frag || (reinterpret_cast<uintptr_t>(doc_frag) & 3u))
+        return KDA_ERR_INVALID_ARG;
+    if (reverse != 0 && reverse != 1) return KDA_ERR_INVALID_ARG;
+    if (F > 0 && !(req(M) && req(B) && req(S_in))) return KDA_ERR_INVALID_ARG;
+    if (!opt(S0) || !opt(S_final)) return KDA_ERR_INVALID_ARG;
+    if (kda_status s = setup_device()) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, H, M, B, S0, reverse, S_in,
+                                                         S_final);
+    return launched();
+}
+
+kda_status kda_read_device_status(void* ws, int* device_status, kda_stream_t stream) {
+    if (!req(ws) || !device_status) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    *device_status = v;
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,198 @@
+// Internal definitions shared by the CUDA translation units of the KDA library.
+//
+// Chunked evaluation (chunk C = 64 tokens, restarted at every document start; rows past the end
+// of a document are zero-padded: q = k = v = 0, beta = 0, g = 0).  Per chunk and head, with
+// gam = in-chunk inclusive cumsum of g and gL = gam[63] (per channel):
+//   E[r,s,c] = exp(gam[r,c] - gam[s,c])
+//   Akk[r,s] = sum_c k_rc k_sc E[r,s,c] (s < r)        Aqk[r,s] = sum_c q_rc k_sc E[r,s,c] (s <= r)
+//   Minv = (I + diag(beta) Akk)^-1,  W = Minv diag(beta) (K * e^gam),  U = Minv diag(beta) V
+//   Delta = U - W S,  O = (Q * e^gam) S + Aqk Delta,  S <- e^gL * S + (K * e^(gL - gam))^T Delta
+// This is the WY / UT form of the delta rule with per-channel gates (Yang et al. 2024, "Gated
+// Delta Networks" and "Gated Linear Attention"), applied here to the KDA recurrence.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int D = 128;       // head dim (keys = values = 128)
+constexpr int CH = 64;       // chunk length
+constexpr int NTHR = 256;    // threads per block of the chunk kernels
+constexpr int SLICE = 32;    // value columns per block of the state-recurrence kernels
+constexpr int NSLICE = D / SLICE;
+constexpr int LDP = D + 1;   // padded row stride (floats) of [64 x 128] shared tiles
+constexpr int LDA = CH + 1;  // padded row stride of [64 x 64] shared tiles
+
+// Byte offsets of every region of the workspace / saved buffers.  Everything is derived from
+// (T, N, H) only, so one allocation serves every pack with the same sizes.
+struct Layout {
+    int64_t T;
+    int N, H;
+    int64_t maxC;  // upper bound of the chunk count: ceil(T/64) + N
+    // workspace
+    size_t status, nchunks, doc_off, chunk_tab;
+    size_t gam, W, U, Qg, Kb, Aqk, Akk, Minv;           // per (chunk, head) intra products
+    size_t dS1, dDelta, dR, P, dQg, dKb, dAqk, dM, rsum; // backward intermediates
+    size_t pdA, pddt;                                   // per (chunk, head) parameter partials
+    size_t replay;                                      // saved set recomputed in replay mode
+    size_t ws_fwd, ws_bwd_saved, ws_bwd_replay, ws_frag;
+    // saved set
+    size_t sv_S, sv_Delta, saved_bytes;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline Layout make_layout(int64_t T, int N, int H) {
+    Layout L{};
+    L.T = T;
+    L.N = N;
+    L.H = H;
+    L.maxC = (T + CH - 1) / CH + N;
+    const size_t CHd = size_t(L.maxC) * H;  // chunk-head pairs
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+    L.status = take(256);
+    L.nchunks = take(sizeof(int));
+    L.doc_off = take(sizeof(int) * size_t(N + 1));
+    L.chunk_tab = take(sizeof(int4) * size_t(L.maxC));
+    L.gam = take(CHd * CH * D * 4);
+    L.W = take(CHd * CH * D * 4);
+    L.U = take(CHd * CH * D * 4);
+    L.Qg = take(CHd * CH * D * 4);
+    L.Kb = take(CHd * CH * D * 4);
+    L.Aqk = take(CHd * CH * CH * 4);
+    L.Akk = take(CHd * CH * CH * 4);
+    L.Minv = take(CHd * CH * CH * 4);
+    L.ws_fwd = o;
+    L.ws_frag = o;
+    L.dS1 = take(CHd * D * D * 4);
+    L.dDelta = take(CHd * CH * D * 4);
+    L.dR = take(CHd * CH * D * 4);
+    L.P = take(CHd * CH * D * 4);
+    L.dQg = take(CHd * CH * D * 4);
+    L.dKb = take(CHd * CH * D * 4);
+    L.dAqk = take(CHd * CH * CH * 4);
+    L.dM = take(CHd * CH * CH * 4);
+    L.rsum = take(CHd * D * 4);
+    L.pdA = take(CHd * 4);
+    L.pddt = take(CHd * D * 4);
+    L.ws_bwd_saved = o;
+    // saved set
+    size_t s = 0;
+    L.sv_S = 0;
+    s = align256(CHd * D * D * 4);
+    L.sv_Delta = s;
+    s = align256(s + CHd * CH * D * 4);
+    L.saved_bytes = s;
+    L.replay = take(L.saved_bytes);
+    L.ws_bwd_replay = o;
+    return L;
+}
+
+// Everything a kernel needs, passed by value.
+struct Params {
+    int64_t T;
+    int N, H;
+    int gate_raw, l2n;
+    float scale, eps;
+    const int* cu;
+    const __nv_bfloat16 *q, *k, *v, *beta, *dO;
+    const float *g, *A_log, *dt_bias, *h0, *dht;
+    __nv_bfloat16 *o, *dq, *dk, *dv, *dbeta;
+    float *ht, *dg, *dA_log, *ddt_bias, *dh0;
+    // workspace regions
+    int* status;
+    int* nchunks;
+    int* doc_off;
+    int4* chunk_tab;  // {doc, first token, length, chunk index within the doc}
+    float *gam, *W, *U, *Qg, *Kb, *Aqk, *Akk, *Minv;
+    float *dS1, *dDelta, *dR, *P, *dQg, *dKb, *dAqk, *dM, *rsum, *pdA, *pddt;
+    // saved set (per chunk-head states and write vectors)
+    float *sS, *sDelta;
+    // fragment summary outputs
+    float *fragM, *fragB;
+    int64_t maxC;
+};
+
+__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// softplus(x) = log(1 + e^x); for x > 20 the correction log1p(e^-x) < 2.1e-9 is below fp32
+// resolution of x and is dropped.
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide fp32 product acc += sum_k A(m,k) B(k,n) over an M x N tile by 256 threads.
+// Thread (tx, ty) owns rows ty + TY*i and columns tx + TX*j.  Operands are read through the
+// loader functors la(m,k), lb(k,n) into shared tiles of KT rows.  Starts and ends with a barrier.
+template <int M, int N, int RM, int RN, class LA, class LB>
+__device__ __forceinline__ void block_gemm(float (&acc)[RM][RN], LA la, LB lb, int K, float* sA,
+                                           float* sB) {
+    constexpr int TX = N / RN, TY = M / RM, KT = 16;
+    static_assert(TX * TY == NTHR, "tile shape must use 256 threads");
+    const int tid = threadIdx.x, tx = tid % TX, ty = tid / TX;
+    for (int k0 = 0; k0 < K; k0 += KT) {
+        __syncthreads();
+        for (int i = tid; i < KT * M; i += NTHR) {
+            int kk = i / M, m = i % M;
+            sA[kk * M + m] = (k0 + kk < K) ? la(m, k0 + kk) : 0.f;
+        }
+        for (int i = tid; i < KT * N; i += NTHR) {
+            int kk = i / N, n = i % N;
+            sB[kk * N + n] = (k0 + kk < K) ? lb(k0 + kk, n) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int kk = 0; kk < KT; ++kk) {
+            float a[RM], b[RN];
+#pragma unroll
+            for (int i = 0; i < RM; ++i) a[i] = sA[kk * M + ty + TY * i];
+#pragma unroll
+            for (int j = 0; j < RN; ++j) b[j] = sB[kk * N + tx + TX * j];
+#pragma unroll
+            for (int i = 0; i < RM; ++i)
+#pragma unroll
+                for (int j = 0; j < RN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+    }
+    __syncthreads();
+}
+
+template <int RM, int RN>
+__device__ __forceinline__ void zero_acc(float (&acc)[RM][RN]) {
+#pragma unroll
+    for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
+}
+
+// Scratch for block_gemm: KT x (M + N) floats, M + N <= 256.
+constexpr int GEMM_SCRATCH = 16 * 256;
+
+// ---- kernels (defined in the .cu files) ----
+__global__ void k_plan(Params p);
+__global__ void k_intra_fwd(Params p);
+__global__ void k_chain_fwd(Params p, int mode);
+__global__ void k_chain_bwd(Params p, int mode);
+__global__ void k_bwd_gemms(Params p);
+__global__ void k_bwd_intra(Params p);
+__global__ void k_param_reduce(Params p);
+__global__ void k_walk(int N, const int* doc_frag, int H, const float* M, const float* B,
+                       const float* S0, int reverse, float* S_in, float* S_final);
+
+// chain modes
+constexpr int CHAIN_FWD_OUT = 0;   // forward: o, ht, optional saved set
+constexpr int CHAIN_FRAG_MB = 1;   // fragment summary: augmented state [M | B]
+constexpr int CHAIN_BWD = 0;       // backward: dS1, dDelta, dh0
+constexpr int CHAIN_FRAG_C = 1;    // fragment summary backward: C only
+
+}  // namespace kda

@@ -1,0 +1,228 @@
+"""ctypes binding of the C ABI in include/kda.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  PyTorch supplies device memory
+and the current stream; all arithmetic runs in the CUDA kernels of libkda_gb300.so.  If that
+library has not been built this module raises -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+D = 128
+CHUNK = 64
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE = 0, 1, 2, 3
+KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE_CHECK = 4, 5, 6
+KDA_GATE_G, KDA_GATE_RAW = 0, 1
+KDA_OP_FWD, KDA_OP_BWD_SAVED, KDA_OP_BWD_REPLAY, KDA_OP_FRAGMENT, KDA_OP_WALK = 0, 1, 2, 3, 4
+KDA_FRAG_FWD, KDA_FRAG_BWD = 0, 1
+
+EXPORTS = ("kda_workspace_size", "kda_fwd", "kda_bwd", "kda_fragment_summary",
+           "kda_transfer_walk", "kda_read_device_status", "kda_status_string")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {kda_status_string(status)} (status {status})")
+
+
+class kda_problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("gate", ctypes.c_int32), ("l2norm", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
+                ("cu_seqlens", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Loads libkda_gb300.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library {path} is missing: run "
+                                   "`python -m linear_attention_chunked_gb300.build` first")
+            L = ctypes.CDLL(path)
+            P, I, S, V = ctypes.POINTER(kda_problem), ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+            L.kda_workspace_size.argtypes = [P, I, ctypes.POINTER(S), ctypes.POINTER(S)]
+            L.kda_fwd.argtypes = [P] + [V] * 11 + [V, S, V]
+            L.kda_bwd.argtypes = [P] + [V] * 19 + [V, S, V]
+            L.kda_fragment_summary.argtypes = [P, I] + [V] * 10 + [V, S, V]
+            L.kda_transfer_walk.argtypes = [ctypes.c_int32, V, ctypes.c_int32, ctypes.c_int32,
+                                            V, V, V, I, V, V, V]
+            L.kda_read_device_status.argtypes = [V, ctypes.POINTER(I), V]
+            L.kda_status_string.argtypes = [I]
+            L.kda_status_string.restype = ctypes.c_char_p
+            for name in EXPORTS[:-1]:
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != KDA_OK:
+        raise KdaError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _gate(gate):
+    if gate in ("g", KDA_GATE_G):
+        return KDA_GATE_G
+    if gate in ("raw", KDA_GATE_RAW):
+        return KDA_GATE_RAW
+    raise ValueError(f"gate must be 'g' or 'raw', got {gate!r}")
+
+
+def make_problem(T, N, H, cu_seqlens=None, *, gate="g", l2norm=False, scale=1.0, eps=1e-6,
+                 d=D):
+    return kda_problem(int(T), int(N), int(H), int(d), _gate(gate), int(bool(l2norm)),
+                       float(scale), float(eps),
+                       None if cu_seqlens is None else cu_seqlens.data_ptr())
+
+
+def kda_workspace_size(T, N, H, op, **kw):
+    """Returns (workspace bytes, saved-set bytes) of op for (T, N, H)."""
+    pr = make_problem(T, N, H, **kw)
+    if pr.cu_seqlens is None:
+        pr.cu_seqlens = 16  # size queries never read it; any aligned non-null value passes
+    ws, sv = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("kda_workspace_size",
+           lib().kda_workspace_size(ctypes.byref(pr), int(op), ctypes.byref(ws), ctypes.byref(sv)))
+    return ws.value, sv.value
+
+
+def _empty_bytes(n, device):
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
+def _shape(q, cu_seqlens):
+    T, H, d = q.shape
+    return T, cu_seqlens.numel() - 1, H, d
+
+
+def kda_fwd(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=None, h0=None,
+            l2norm=False, scale=1.0, eps=1e-6, save=True, o=None, ht=None, saved=None, ws=None):
+    """Forward.  Returns (o, ht, saved) -- saved is None when save=False."""
+    T, N, H, d = _shape(q, cu_seqlens)
+    dev = q.device
+    pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d)
+    ws_b, sv_b = kda_workspace_size(T, N, H, KDA_OP_FWD)
+    if ws is None:
+        ws = _empty_bytes(ws_b, dev)
+    if save and saved is None:
+        saved = _empty_bytes(sv_b, dev)
+    if not save:
+        saved = None
+    if o is None:
+        o = torch.empty_like(q)
+    if ht is None:
+        ht = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().kda_fwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_or_a),
+                           _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o), _ptr(ht), _ptr(saved),
+                           _ptr(ws), ws.numel(), _stream(dev))
+    _check("kda_fwd", st)
+    return o, ht, saved
+
+
+def kda_bwd(q, k, v, beta, g_or_a, cu_seqlens, dO, *, saved=None, gate="g", A_log=None,
+            dt_bias=None, h0=None, dht=None, l2norm=False, scale=1.0, eps=1e-6, want_dh0=True,
+            out=None, ws=None):
+    """Backward (saved=None: checkpoint replay).  Returns a dict of gradients."""
+    T, N, H, d = _shape(q, cu_seqlens)
+    dev = q.device
+    g_ = _gate(gate)
+    pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d)
+    op = KDA_OP_BWD_SAVED if saved is not None else KDA_OP_BWD_REPLAY
+    ws_b, _ = kda_workspace_size(T, N, H, op)
+    if ws is None:
+        ws = _empty_bytes(ws_b, dev)
+    if out is None:
+        out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                   dbeta=torch.empty_like(beta), dg=torch.empty_like(g_or_a))
+        if g_ == KDA_GATE_RAW:
+            out["dA_log"] = torch.empty((H,), dtype=torch.float32, device=dev)
+            out["ddt_bias"] = torch.empty((H, d), dtype=torch.float32, device=dev)
+        if want_dh0:
+            out["dh0"] = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().kda_bwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_or_a),
+                           _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(dO), _ptr(dht), _ptr(saved),
+                           _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dbeta"]),
+                           _ptr(out["dg"]), _ptr(out.get("dA_log")), _ptr(out.get("ddt_bias")),
+                           _ptr(out.get("dh0")), _ptr(ws), ws.numel(), _stream(dev))
+    _check("kda_bwd", st)
+    return out
+
+
+def kda_fragment_summary(q, k, v, beta, g_or_a, frag_cu, *, mode=KDA_FRAG_FWD, dO=None,
+                         gate="g", A_log=None, dt_bias=None, l2norm=False, scale=1.0, eps=1e-6,
+                         M=None, B_or_C=None, ws=None):
+    """mode KDA_FRAG_FWD -> (M, B); mode KDA_FRAG_BWD -> C.  Fragments = documents of frag_cu."""
+    T, F, H, d = _shape(q, frag_cu)
+    dev = q.device
+    pr = make_problem(T, F, H, frag_cu, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d)
+    ws_b, _ = kda_workspace_size(T, F, H, KDA_OP_FRAGMENT)
+    if ws is None:
+        ws = _empty_bytes(ws_b, dev)
+    if mode == KDA_FRAG_FWD and M is None:
+        M = torch.empty((F, H, d, d), dtype=torch.float32, device=dev)
+    if B_or_C is None:
+        B_or_C = torch.empty((F, H, d, d), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().kda_fragment_summary(ctypes.byref(pr), int(mode), _ptr(q), _ptr(k), _ptr(v),
+                                        _ptr(beta), _ptr(g_or_a), _ptr(A_log), _ptr(dt_bias),
+                                        _ptr(dO), _ptr(M), _ptr(B_or_C), _ptr(ws), ws.numel(),
+                                        _stream(dev))
+    _check("kda_fragment_summary", st)
+    return (M, B_or_C) if mode == KDA_FRAG_FWD else B_or_C
+
+
+def kda_transfer_walk(doc_frag, M, B, S0=None, *, reverse=False, S_in=None, S_final=None):
+    """Returns (S_in [F,H,d,d], S_final [N,H,d,d])."""
+    F, H, d, _ = M.shape
+    N = doc_frag.numel() - 1
+    dev = M.device
+    if S_in is None:
+        S_in = torch.empty_like(M)
+    if S_final is None:
+        S_final = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().kda_transfer_walk(N, _ptr(doc_frag), F, H, _ptr(M), _ptr(B), _ptr(S0),
+                                     int(bool(reverse)), _ptr(S_in), _ptr(S_final), _stream(dev))
+    _check("kda_transfer_walk", st)
+    return S_in, S_final
+
+
+def kda_read_device_status(ws) -> int:
+    v = ctypes.c_int(0)
+    with torch.cuda.device(ws.device):
+        _check("kda_read_device_status",
+               lib().kda_read_device_status(_ptr(ws), ctypes.byref(v), _stream(ws.device)))
+    return v.value

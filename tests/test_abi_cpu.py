@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function
+declared in include/kda.h, answers size queries, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_chunked_gb300 import build, kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kda.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(kda_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 7, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/kda.h but not exported"
+    assert set(kda.EXPORTS) <= set(names)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert kda.kda_status_string(s)
+    assert "unknown" in kda.kda_status_string(99)
+
+
+def test_workspace_sizes_depend_on_T_N_H_only(lib):
+    a = kda.kda_workspace_size(3548, 2, 4, kda.KDA_OP_FWD)
+    b = kda.kda_workspace_size(3548, 2, 4, kda.KDA_OP_FWD, gate="raw", l2norm=True)
+    assert a == b and a[0] > 0 and a[1] > 0
+    fwd, saved = a
+    bs, _ = kda.kda_workspace_size(3548, 2, 4, kda.KDA_OP_BWD_SAVED)
+    br, _ = kda.kda_workspace_size(3548, 2, 4, kda.KDA_OP_BWD_REPLAY)
+    assert fwd <= bs < br and br >= bs + saved
+    assert kda.kda_workspace_size(3548, 2, 4, kda.KDA_OP_WALK)[0] == 0
+    # grows with T
+    assert kda.kda_workspace_size(7096, 2, 4, kda.KDA_OP_FWD)[0] > fwd
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("H", 0, kda.KDA_ERR_INVALID_ARG),
+    ("H", -3, kda.KDA_ERR_INVALID_ARG),
+    ("N", 0, kda.KDA_ERR_INVALID_ARG),
+    ("T", -1, kda.KDA_ERR_INVALID_ARG),
+    ("d", 64, kda.KDA_ERR_UNSUPPORTED),
+    ("gate", 7, kda.KDA_ERR_INVALID_ARG),
+    ("l2norm", 2, kda.KDA_ERR_INVALID_ARG),
+])
+def test_problem_validation(lib, field, value, status):
+    pr = kda.make_problem(128, 1, 2)
+    pr.cu_seqlens = 256
+    setattr(pr, field, value)
+    ws = ctypes.c_size_t(0)
+    assert lib.kda_workspace_size(ctypes.byref(pr), 0, ctypes.byref(ws), None) == status
+    # the compute entry points validate before any CUDA call
+    z = ctypes.c_void_p(0)
+    assert lib.kda_fwd(ctypes.byref(pr), *([z] * 11), z, 0, z) == status
+
+
+def test_pointer_validation(lib):
+    pr = kda.make_problem(128, 1, 2)
+    pr.cu_seqlens = 256
+    z = ctypes.c_void_p(0)
+    a = ctypes.c_void_p(4096)
+    mis = ctypes.c_void_p(4098)  # not 16-byte aligned
+    # null q
+    assert lib.kda_fwd(ctypes.byref(pr), z, a, a, a, a, z, z, z, a, z, z, a, 1 << 40, z) == \
+        kda.KDA_ERR_INVALID_ARG
+    # misaligned k
+    assert lib.kda_fwd(ctypes.byref(pr), a, mis, a, a, a, z, z, z, a, z, z, a, 1 << 40, z) == \
+        kda.KDA_ERR_INVALID_ARG
+    # raw gate needs A_log and dt_bias
+    pr.gate = kda.KDA_GATE_RAW
+    assert lib.kda_fwd(ctypes.byref(pr), a, a, a, a, a, z, z, z, a, z, z, a, 1 << 40, z) == \
+        kda.KDA_ERR_INVALID_ARG
+    # workspace too small
+    pr.gate = kda.KDA_GATE_G
+    assert lib.kda_fwd(ctypes.byref(pr), a, a, a, a, a, z, z, z, a, z, z, a, 16, z) == \
+        kda.KDA_ERR_WORKSPACE
+    # cu_seqlens null
+    pr.cu_seqlens = None
+    assert lib.kda_fwd(ctypes.byref(pr), a, a, a, a, a, z, z, z, a, z, z, a, 1 << 40, z) == \
+        kda.KDA_ERR_INVALID_ARG
+    # walk: N < 1, H < 1, bad reverse flag
+    assert lib.kda_transfer_walk(0, a, 1, 1, a, a, z, 0, a, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_transfer_walk(1, a, 1, 0, a, a, z, 0, a, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_transfer_walk(1, a, 1, 1, a, a, z, 2, a, z, z) == kda.KDA_ERR_INVALID_ARG
+    # fragment summary: bad mode
+    assert lib.kda_fragment_summary(ctypes.byref(kda.make_problem(128, 1, 2, None)), 5,
+                                    *([a] * 10), a, 1 << 40, z) == kda.KDA_ERR_INVALID_ARG

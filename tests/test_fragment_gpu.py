@@ -1,0 +1,98 @@
+"""GPU parity of the fragment path: fragment summaries (M, B, C), the transfer walk in both
+directions, and the documents finished fragment by fragment, against the unfragmented oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import TOL, assert_within, compare, f64, oracle_fwd_bwd, rel_err, to_dev
+from linear_attention_chunked_gb300 import inputs, kda
+
+pytestmark = pytest.mark.gpu
+
+
+def _split(lens, nfrag):
+    frag, doc_frag = [], [0]
+    for L in lens:
+        pieces = inputs.fragment_lens(L, nfrag)
+        frag += pieces
+        doc_frag.append(doc_frag[-1] + len(pieces))
+    return frag, doc_frag
+
+
+def run_fragment_path(inp, lens, nfrag, *, gate, l2norm, h0=None, dht=None):
+    """fwd + saved bwd of the documents via summaries, walks and per-fragment finishing."""
+    frag, doc_frag = _split(lens, nfrag)
+    d = to_dev(inp)
+    fcu = inputs.cu_from_lens(frag).cuda()
+    dfr = torch.tensor(doc_frag, dtype=torch.int32, device="cuda")
+    args = (d["q"], d["k"], d["v"], d["beta"], d["g"], fcu)
+    kw = dict(gate=gate, A_log=d["A_log"], dt_bias=d["dt_bias"], l2norm=l2norm)
+    M, B = kda.kda_fragment_summary(*args, mode=kda.KDA_FRAG_FWD, **kw)
+    h0d = None if h0 is None else torch.as_tensor(h0).float().cuda()
+    dhtd = None if dht is None else torch.as_tensor(dht).float().cuda()
+    S_in, S_fin = kda.kda_transfer_walk(dfr, M, B, h0d)
+    o, _, saved = kda.kda_fwd(*args, h0=S_in, **kw)
+    C = kda.kda_fragment_summary(*args, mode=kda.KDA_FRAG_BWD, dO=d["dO"], **kw)
+    dS_end, dh0 = kda.kda_transfer_walk(dfr, M, C, dhtd, reverse=True)
+    g = kda.kda_bwd(*args, d["dO"], saved=saved, h0=S_in, dht=dS_end, **kw)
+    torch.cuda.synchronize()
+    out = dict(o=o, ht=S_fin, dh0=dh0, M=M, B=B, C=C)
+    out.update({k: v for k, v in g.items() if k != "dh0"})
+    return {k: v.float().cpu().numpy() for k, v in out.items()}, frag
+
+
+@pytest.mark.parametrize("gate,l2norm", [("g", False), ("raw", True)])
+def test_fragment_path_small(gate, l2norm):
+    lens = [300, 77, 129]
+    inp = inputs.make_inputs(lens, 2, gate=gate, l2norm=l2norm, gdiv=64.0, seed=11)
+    rng = np.random.default_rng(3)
+    h0 = rng.standard_normal((3, 2, 128, 128)).astype(np.float32) * 0.1
+    dht = rng.standard_normal((3, 2, 128, 128)).astype(np.float32) * 0.1
+    gpu, frag = run_fragment_path(inp, lens, 4, gate=gate, l2norm=l2norm, h0=h0, dht=dht)
+    ref = oracle_fwd_bwd(inp, gate=gate, l2norm=l2norm, h0=h0, dht=dht)
+    errs = compare(gpu, ref)
+    print({k: f"{v:.2e}" for k, v in errs.items()})
+    assert_within(errs, label=f"fragments {gate}")
+    # the summaries themselves against the oracle's fragment algebra
+    raw = gate == "raw"
+    oargs = [f64(inp[n]) for n in ("q", "k", "v", "beta", "g")]
+    okw = dict(raw=raw, l2norm=l2norm, A_log=f64(inp["A_log"]) if raw else None,
+               dt_bias=f64(inp["dt_bias"]) if raw else None)
+    fcu = inputs.cu_from_lens(frag).numpy()
+    M, B = oracle.fragment_summary(*oargs, fcu, **okw)
+    C = oracle.fragment_summary(*oargs, fcu, mode=1, dO=f64(inp["dO"]), **okw)
+    for name, r in (("M", M), ("B", B), ("C", C)):
+        e = rel_err(gpu[name], r)
+        assert e < 1e-3, (name, e)
+
+
+def test_walk_covers_every_column_slice():
+    # every column of every S_in must be written: prefill with NaN and check none is left
+    F, H = 5, 3
+    gen = torch.Generator("cpu").manual_seed(0)
+    M = (torch.randn((F, H, 128, 128), generator=gen) * 0.05).cuda()
+    B = torch.randn((F, H, 128, 128), generator=gen).cuda()
+    dfr = torch.tensor([0, 2, 5], dtype=torch.int32, device="cuda")
+    for rev in (False, True):
+        S_in = torch.full((F, H, 128, 128), float("nan"), device="cuda")
+        S_fin = torch.full((2, H, 128, 128), float("nan"), device="cuda")
+        kda.kda_transfer_walk(dfr, M, B, None, reverse=rev, S_in=S_in, S_final=S_fin)
+        torch.cuda.synchronize()
+        assert not torch.isnan(S_in).any() and not torch.isnan(S_fin).any()
+        S_ref, fin_ref = oracle.transfer_walk([0, 2, 5], M.double().cpu().numpy(),
+                                              B.double().cpu().numpy(), None, reverse=rev)
+        assert rel_err(S_in.cpu().numpy(), S_ref) < 1e-5
+        assert rel_err(S_fin.cpu().numpy(), fin_ref) < 1e-5
+
+
+@pytest.mark.slow
+def test_longpack_sampled_heads():
+    w = inputs.WORKLOADS["longpack"]
+    inp = inputs.workload_inputs("longpack")
+    gpu, _ = run_fragment_path(inp, w.lens, w.fragments, gate=w.gate, l2norm=w.l2norm)
+    heads = [0, 9]
+    ref = oracle_fwd_bwd(inp, gate=w.gate, l2norm=w.l2norm, heads=heads)
+    errs = compare(gpu, ref, heads=heads)
+    print("longpack", {k: f"{v:.2e}" for k, v in errs.items()})
+    assert_within(errs, label="longpack")

@@ -30,8 +30,11 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The library allocates nothing,
  *    keeps no pointer after a call returns, and never synchronises the device: every call only
  *    enqueues kernels on `stream` (NULL = the legacy default stream).
- *  - Layouts are dense row-major ("THD"): q, k, v, o, dO, dq, dk, dv are bf16 [T, H, 128];
- *    beta, dbeta are bf16 [T, H]; g / a and dg / da are fp32 [T, H, 128]; A_log is fp32 [H];
+ *  - Layouts are dense row-major ("THD"): q, k, v, dO are bf16 [T, H, 128]; beta is bf16 [T, H];
+ *    o, dq, dk, dv [T, H, 128] and dbeta [T, H] are fp32 when kda_problem.out_fp32 = 1, else bf16
+ *    (the outputs are heavy-tailed: bf16 storage alone puts max|err|/rms(ref) of o near 4e-2 on
+ *    the raw-gate workloads, so fp32 is the parity-grade choice);
+ *    g / a and dg / da are fp32 [T, H, 128]; A_log is fp32 [H];
  *    dt_bias, ddt_bias are fp32 [H, 128]; h0, ht, dht, dh0 are fp32 [N, H, 128, 128] indexed
  *    [key][value]; cu_seqlens is int32 [N + 1] on the device with cu_seqlens[0] = 0,
  *    non-decreasing, cu_seqlens[N] = T.  Empty documents are allowed (their ht = h0).
@@ -93,6 +96,7 @@ typedef struct kda_problem {
     int32_t d;                  /* head dim; must be 128 */
     int32_t gate;               /* kda_gate_form */
     int32_t l2norm;             /* 0: q, k used as given; 1: fused q/sqrt(|q|^2+eps), same for k */
+    int32_t out_fp32;           /* 1: o, dq, dk, dv, dbeta are fp32; 0: they are bf16 */
     float scale;                /* output scale (1 for the plain recurrence) */
     float l2_eps;               /* eps of the fused L2 norm (1e-6) */
     const int32_t* cu_seqlens;  /* device int32 [N+1] */
@@ -104,7 +108,7 @@ typedef struct kda_problem {
  * allocation serves every pack with the same T, N, H.  Either output pointer may be NULL. */
 kda_status kda_workspace_size(const kda_problem* p, int op, size_t* ws_bytes, size_t* saved_bytes);
 
-/* Forward.  Writes o (bf16 [T,H,128]), ht (fp32 [N,H,128,128], nullable) and, when `saved` is
+/* Forward.  Writes o ([T,H,128], fp32 or bf16 per out_fp32), ht (fp32 [N,H,128,128], nullable) and, when `saved` is
  * non-NULL, the saved forward set (per-chunk states and chunk write vectors) for kda_bwd.
  * h0 (nullable = zero initial state).  A_log / dt_bias are read only in raw gate form.
  * Source: the chunked KDA training package page (PR #8909), summary (forward pass, gate forms,
@@ -116,8 +120,8 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
 
 /* Backward of L = sum(o * dO) + sum(ht * dht) for the same inputs as kda_fwd.
  * saved: the set written by kda_fwd for exactly these inputs, or NULL to recompute the forward
- * (checkpoint replay).  dht nullable (zero).  Outputs: dq, dk, dv bf16 [T,H,128]; dbeta bf16
- * [T,H]; dg_or_da fp32 [T,H,128] = dL/dg in g form, dL/da in raw form; in raw form also dA_log
+ * (checkpoint replay).  dht nullable (zero).  Outputs: dq, dk, dv [T,H,128] and dbeta [T,H]
+ * (fp32 or bf16 per out_fp32); dg_or_da fp32 [T,H,128] = dL/dg in g form, dL/da in raw form; in raw form also dA_log
  * fp32 [H] and ddt_bias fp32 [H,128] (ignored, may be NULL, in g form); dh0 fp32
  * [N,H,128,128] nullable.  Source: the chunked KDA training package page (PR #8909), summary
  * (backward path saved / replay) and first commit message (gate gradient dg, dA_log, dt_bias). */

@@ -52,6 +52,7 @@ kda_status check_problem(const kda_problem* p) {
         return KDA_ERR_INVALID_ARG;
     if (p->gate != KDA_GATE_G && p->gate != KDA_GATE_RAW) return KDA_ERR_INVALID_ARG;
     if (p->l2norm != 0 && p->l2norm != 1) return KDA_ERR_INVALID_ARG;
+    if (p->out_fp32 != 0 && p->out_fp32 != 1) return KDA_ERR_INVALID_ARG;
     if (!p->cu_seqlens || (reinterpret_cast<uintptr_t>(p->cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
     if (!(p->l2_eps >= 0.f)) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
@@ -77,6 +78,7 @@ Params make_params(const kda_problem* pr, const Layout& L, void* ws) {
     p.H = pr->H;
     p.gate_raw = pr->gate == KDA_GATE_RAW;
     p.l2n = pr->l2norm;
+    p.out_fp32 = pr->out_fp32;
     p.scale = pr->scale;
     p.eps = pr->l2_eps;
     p.cu = pr->cu_seqlens;
@@ -185,7 +187,7 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     Params p = make_params(pr, L, ws);
     set_inputs(p, q, k, v, beta, g_or_a, A_log, dt_bias);
     p.h0 = h0;
-    p.o = static_cast<__nv_bfloat16*>(o);
+    p.o = o;
     p.ht = ht;
     if (saved) {
         p.sS = reinterpret_cast<float*>(static_cast<char*>(saved) + L.sv_S);
@@ -218,10 +220,10 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
     p.h0 = h0;
     p.dht = dht;
     p.dO = static_cast<const __nv_bfloat16*>(dO);
-    p.dq = static_cast<__nv_bfloat16*>(dq);
-    p.dk = static_cast<__nv_bfloat16*>(dk);
-    p.dv = static_cast<__nv_bfloat16*>(dv);
-    p.dbeta = static_cast<__nv_bfloat16*>(dbeta);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dbeta = dbeta;
     p.dg = dg_or_da;
     p.dA_log = dA_log;
     p.ddt_bias = ddt_bias;
@@ -286,7 +288,7 @@ kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int3
     if (!opt(S0) || !opt(S_final)) return KDA_ERR_INVALID_ARG;
     if (kda_status s = setup_device()) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, H, M, B, S0, reverse, S_in,
+    k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, F, H, M, B, S0, reverse, S_in,
                                                          S_final);
     return launched();
 }

@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
             const float vv = r < L ? bf2f(p.v[(size_t(t0 + r) * p.H + h) * D + c]) : 0.f;
             const float dRv = dRp[r * D + c];
             dbp += dRv * vv - kv * er * Pv;
-            if (r < L) p.dv[(size_t(t0 + r) * p.H + h) * D + c] = __float2bfloat16_rn(br * dRv);
+            if (r < L) store_out(p.dv, (size_t(t0 + r) * p.H + h) * D + c, br * dRv, p.out_fp32);
         }
         for (int s = lane; s < r; s += 32) dbp += sAkk[r * LDA + s] * dMp[r * CH + s];
         dbp = warp_sum(dbp);
@@ -340,10 +340,10 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
                     dq = (dq - sq[r * LDP + c] * pq) * srq[r];
                     dk = (dk - sk[r * LDP + c] * pk) * srk[r];
                 }
-                p.dq[base + c] = __float2bfloat16_rn(dq);
-                p.dk[base + c] = __float2bfloat16_rn(dk);
+                store_out(p.dq, base + c, dq, p.out_fp32);
+                store_out(p.dk, base + c, dk, p.out_fp32);
             }
-            if (lane == 0) p.dbeta[size_t(t0 + r) * p.H + h] = __float2bfloat16_rn(dbp);
+            if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, dbp, p.out_fp32);
         }
     }
     __syncthreads();

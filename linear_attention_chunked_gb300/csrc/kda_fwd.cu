@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(NTHR) k_chain_fwd(Params p, int mode) {
                 for (int j = 0; j < 4; ++j) {
                     const int r = ty + 32 * i, jj = tx + 8 * j;
                     if (r < L)
-                        p.o[(size_t(t0 + r) * p.H + h) * D + col0 + jj] =
-                            __float2bfloat16_rn(p.scale * acc[i][j]);
+                        store_out(p.o, (size_t(t0 + r) * p.H + h) * D + col0 + jj,
+                                  p.scale * acc[i][j], p.out_fp32);
                 }
         }
         // S = e^gL S + Kb^T Delta   (128 x 32)

@@ -97,12 +97,12 @@ inline Layout make_layout(int64_t T, int N, int H) {
 struct Params {
     int64_t T;
     int N, H;
-    int gate_raw, l2n;
+    int gate_raw, l2n, out_fp32;
     float scale, eps;
     const int* cu;
     const __nv_bfloat16 *q, *k, *v, *beta, *dO;
     const float *g, *A_log, *dt_bias, *h0, *dht;
-    __nv_bfloat16 *o, *dq, *dk, *dv, *dbeta;
+    void *o, *dq, *dk, *dv, *dbeta;  // fp32 or bf16 per out_fp32
     float *ht, *dg, *dA_log, *ddt_bias, *dh0;
     // workspace regions
     int* status;
@@ -119,6 +119,12 @@ struct Params {
 };
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Stores an output element in the caller's chosen precision.
+__device__ __forceinline__ void store_out(void* base, size_t i, float v, int fp32) {
+    if (fp32) static_cast<float*>(base)[i] = v;
+    else static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+}
 
 // softplus(x) = log(1 + e^x); for x > 20 the correction log1p(e^-x) < 2.1e-9 is below fp32
 // resolution of x and is dropped.
@@ -186,7 +192,7 @@ __global__ void k_chain_bwd(Params p, int mode);
 __global__ void k_bwd_gemms(Params p);
 __global__ void k_bwd_intra(Params p);
 __global__ void k_param_reduce(Params p);
-__global__ void k_walk(int N, const int* doc_frag, int H, const float* M, const float* B,
+__global__ void k_walk(int N, const int* doc_frag, int F, int H, const float* M, const float* B,
                        const float* S0, int reverse, float* S_in, float* S_final);
 
 // chain modes

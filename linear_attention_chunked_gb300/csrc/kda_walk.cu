@@ -5,8 +5,9 @@ namespace kda {
 
 // One block per (document, head, 32-column slice of the state).  FP32 products with FP32
 // accumulation (exact to fp32 rounding; the walk is at most a few 128^3 products per document).
-// Documents whose fragment range is malformed (decreasing or outside [0, F]) are skipped.
-__global__ void __launch_bounds__(NTHR) k_walk(int N, const int* doc_frag, int H, const float* M,
+// Documents whose fragment range is malformed (decreasing or outside [0, F], F the host-given
+// fragment count that sizes M, B and S_in) are skipped.
+__global__ void __launch_bounds__(NTHR) k_walk(int N, const int* doc_frag, int F, int H, const float* M,
                                                const float* B, const float* S0, int reverse,
                                                float* S_in, float* S_final) {
     constexpr int LS = SLICE + 1;
@@ -15,7 +16,7 @@ __global__ void __launch_bounds__(NTHR) k_walk(int N, const int* doc_frag, int H
     float* cur = sm;
     float* gs = cur + D * LS;
     const int tid = threadIdx.x;
-    const int f0 = doc_frag[n], f1 = doc_frag[n + 1], F = doc_frag[N];
+    const int f0 = doc_frag[n], f1 = doc_frag[n + 1];
     if (f1 < f0 || f0 < 0 || f1 > F) return;
     const size_t dh = (size_t(n) * H + h) * D * D;
     for (int i = tid; i < D * SLICE; i += NTHR) {

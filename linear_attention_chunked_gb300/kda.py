@@ -36,7 +36,7 @@ class KdaError(RuntimeError):
 class kda_problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("d", ctypes.c_int32), ("gate", ctypes.c_int32), ("l2norm", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
+                ("out_fp32", ctypes.c_int32), ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
                 ("cu_seqlens", ctypes.c_void_p)]
 
 
@@ -100,9 +100,11 @@ def _gate(gate):
 
 
 def make_problem(T, N, H, cu_seqlens=None, *, gate="g", l2norm=False, scale=1.0, eps=1e-6,
-                 d=D):
+                 d=D, out_dtype=torch.float32):
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     return kda_problem(int(T), int(N), int(H), int(d), _gate(gate), int(bool(l2norm)),
-                       float(scale), float(eps),
+                       int(out_dtype == torch.float32), float(scale), float(eps),
                        None if cu_seqlens is None else cu_seqlens.data_ptr())
 
 
@@ -127,11 +129,13 @@ def _shape(q, cu_seqlens):
 
 
 def kda_fwd(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=None, h0=None,
-            l2norm=False, scale=1.0, eps=1e-6, save=True, o=None, ht=None, saved=None, ws=None):
+            l2norm=False, scale=1.0, eps=1e-6, save=True, out_dtype=torch.float32, o=None, ht=None,
+            saved=None, ws=None):
     """Forward.  Returns (o, ht, saved) -- saved is None when save=False."""
     T, N, H, d = _shape(q, cu_seqlens)
     dev = q.device
-    pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d)
+    pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d,
+                      out_dtype=out_dtype)
     ws_b, sv_b = kda_workspace_size(T, N, H, KDA_OP_FWD)
     if ws is None:
         ws = _empty_bytes(ws_b, dev)
@@ -140,7 +144,7 @@ def kda_fwd(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=
     if not save:
         saved = None
     if o is None:
-        o = torch.empty_like(q)
+        o = torch.empty(q.shape, dtype=out_dtype, device=dev)
     if ht is None:
         ht = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -153,19 +157,22 @@ def kda_fwd(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=
 
 def kda_bwd(q, k, v, beta, g_or_a, cu_seqlens, dO, *, saved=None, gate="g", A_log=None,
             dt_bias=None, h0=None, dht=None, l2norm=False, scale=1.0, eps=1e-6, want_dh0=True,
-            out=None, ws=None):
+            out_dtype=torch.float32, out=None, ws=None):
     """Backward (saved=None: checkpoint replay).  Returns a dict of gradients."""
     T, N, H, d = _shape(q, cu_seqlens)
     dev = q.device
     g_ = _gate(gate)
-    pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d)
+    pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d,
+                      out_dtype=out_dtype)
     op = KDA_OP_BWD_SAVED if saved is not None else KDA_OP_BWD_REPLAY
     ws_b, _ = kda_workspace_size(T, N, H, op)
     if ws is None:
         ws = _empty_bytes(ws_b, dev)
     if out is None:
-        out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
-                   dbeta=torch.empty_like(beta), dg=torch.empty_like(g_or_a))
+        od = dict(dtype=out_dtype, device=dev)
+        out = dict(dq=torch.empty(q.shape, **od), dk=torch.empty(k.shape, **od),
+                   dv=torch.empty(v.shape, **od), dbeta=torch.empty(beta.shape, **od),
+                   dg=torch.empty_like(g_or_a))
         if g_ == KDA_GATE_RAW:
             out["dA_log"] = torch.empty((H,), dtype=torch.float32, device=dev)
             out["ddt_bias"] = torch.empty((H, d), dtype=torch.float32, device=dev)

@@ -26,18 +26,20 @@ def to_dev(inp, device="cuda"):
     return {k: (v.to(device) if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
-def gpu_fwd_bwd(inp, *, gate, l2norm, h0=None, dht=None, saved_mode=True, want_bwd=True):
+def gpu_fwd_bwd(inp, *, gate, l2norm, h0=None, dht=None, saved_mode=True, want_bwd=True,
+                out_dtype=torch.float32):
     d = to_dev(inp)
     h0d = None if h0 is None else torch.as_tensor(h0, dtype=torch.float32).cuda()
     dhtd = None if dht is None else torch.as_tensor(dht, dtype=torch.float32).cuda()
     o, ht, saved = kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["cu_seqlens"],
                                gate=gate, A_log=d["A_log"], dt_bias=d["dt_bias"], h0=h0d,
-                               l2norm=l2norm, save=saved_mode)
+                               l2norm=l2norm, save=saved_mode, out_dtype=out_dtype)
     out = dict(o=o, ht=ht)
     if want_bwd:
         g = kda.kda_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["cu_seqlens"], d["dO"],
                         saved=saved if saved_mode else None, gate=gate, A_log=d["A_log"],
-                        dt_bias=d["dt_bias"], h0=h0d, dht=dhtd, l2norm=l2norm)
+                        dt_bias=d["dt_bias"], h0=h0d, dht=dhtd, l2norm=l2norm,
+                        out_dtype=out_dtype)
         out.update(g)
     torch.cuda.synchronize()
     return {k: v.float().cpu().numpy() for k, v in out.items()}

@@ -58,6 +58,7 @@ def test_workspace_sizes_depend_on_T_N_H_only(lib):
     ("d", 64, kda.KDA_ERR_UNSUPPORTED),
     ("gate", 7, kda.KDA_ERR_INVALID_ARG),
     ("l2norm", 2, kda.KDA_ERR_INVALID_ARG),
+    ("out_fp32", 3, kda.KDA_ERR_INVALID_ARG),
 ])
 def test_problem_validation(lib, field, value, status):
     pr = kda.make_problem(128, 1, 2)
@@ -99,5 +100,7 @@ def test_pointer_validation(lib):
     assert lib.kda_transfer_walk(1, a, 1, 0, a, a, z, 0, a, z, z) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_transfer_walk(1, a, 1, 1, a, a, z, 2, a, z, z) == kda.KDA_ERR_INVALID_ARG
     # fragment summary: bad mode
-    assert lib.kda_fragment_summary(ctypes.byref(kda.make_problem(128, 1, 2, None)), 5,
-                                    *([a] * 10), a, 1 << 40, z) == kda.KDA_ERR_INVALID_ARG
+    pf = kda.make_problem(128, 1, 2)
+    pf.cu_seqlens = 256
+    assert lib.kda_fragment_summary(ctypes.byref(pf), 5, *([a] * 10), a, 1 << 40, z) == \
+        kda.KDA_ERR_INVALID_ARG

@@ -62,9 +62,12 @@ def test_fragment_path_small(gate, l2norm):
     fcu = inputs.cu_from_lens(frag).numpy()
     M, B = oracle.fragment_summary(*oargs, fcu, **okw)
     C = oracle.fragment_summary(*oargs, fcu, mode=1, dO=f64(inp["dO"]), **okw)
-    for name, r in (("M", M), ("B", B), ("C", C)):
-        e = rel_err(gpu[name], r)
-        assert e < 1e-3, (name, e)
+    # B and C are states: the final-state bound.  M is a transition product whose entries span
+    # many orders of magnitude (a few slow channels near 1, the rest decayed towards 0), so it is
+    # scored against its largest entry; its effect on states is covered by ht / dh0 above.
+    errs = {"B": rel_err(gpu["B"], B), "C": rel_err(gpu["C"], C),
+            "M": float(np.max(np.abs(gpu["M"] - M)) / np.max(np.abs(M)))}
+    assert errs["B"] < TOL["ht"] and errs["C"] < TOL["ht"] and errs["M"] < 1e-4, errs
 
 
 def test_walk_covers_every_column_slice():

@@ -128,3 +128,15 @@ def test_host_validation_on_device():
     with pytest.raises(kda.KdaError) as e:
         kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["cu_seqlens"], gate="raw")
     assert e.value.status == kda.KDA_ERR_INVALID_ARG
+
+
+def test_bf16_outputs_within_rounding_of_fp32_outputs():
+    # bf16 outputs are the fp32 outputs rounded to nearest: within half a bf16 ulp elementwise
+    inp, gate, l2n = _small("raw_fast", seed=6)
+    a = gpu_fwd_bwd(inp, gate=gate, l2norm=l2n, out_dtype=torch.float32)
+    b = gpu_fwd_bwd(inp, gate=gate, l2norm=l2n, out_dtype=torch.bfloat16)
+    for k in ("o", "dq", "dk", "dv", "dbeta"):
+        want = torch.tensor(a[k]).bfloat16().float().numpy()
+        assert np.array_equal(b[k], want), k
+    for k in ("ht", "dg", "dA_log", "ddt_bias", "dh0"):
+        assert np.array_equal(a[k], b[k]), k

@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""KDA fwd+bwd throughput on GB300: one JSON line on rank 0.
+
+A step is one pass of the whole hot path over one batch: kda_fwd (writing the saved set) followed
+by kda_bwd (saved mode) on the 4doc workload (16384 tokens in documents of 8192/4096/3072/1024,
+64 heads, d = 128, raw gate, no fused L2 norm), inputs already resident in HBM.  Timing: W warm-up
+steps, then K steps bracketed by a barrier and torch.cuda.synchronize(), CUDA events on the
+launching stream, max over ranks.  The inputs are larger than L2 (q, k, v, a, dO ~2.1 GB), so no
+flush is needed between steps.
+
+Also reported: per-kernel device time (CUDA events around each launch, a second pass of K
+steps), the dominant kernel's roofline position, an end-to-end number through the public API
+with host buffers (pinned H2D of every input and D2H of the parameter gradients inside every
+step), SM clocks sampled during the timed region, and the FP64 oracle timed on the host cores on
+a bounded sample of the same workload.
+
+--impl reference times the oracle (the reference arm for this build) on the same workload,
+metric and unit, each step a bounded sample (a subset of heads), scaled to the full workload.
+Multi-GPU (torchrun, one process per GPU): every rank runs its own copy of the workload (the
+path shards by heads / documents with no exchange), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "4doc"
+PAGES_MS = 4.2789  # 4doc:raw:off:saved fwd+bwd on GB300 (sm_103a), the chunked KDA package page
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic bytes per kernel launch (method inputs and outputs a kernel must touch; workspace
+# intermediates excluded), per token-head, with this library's I/O formats: q, k, v, dO bf16;
+# beta bf16; gate fp32; o, dq, dk, dv, dbeta fp32 (parity-grade outputs)
+
+
+def alg_bytes_per_token_head(kernel):
+    qkv, beta, gate, dO = 3 * 256, 2, 512, 256
+    o, dqkv, dbeta, dg = 512, 3 * 512, 4, 512
+    table = {
+        "k_intra_fwd": qkv + beta + gate,                    # reads the chunk inputs
+        "k_chain_fwd": o,                                    # writes o
+        "k_chain_bwd": dO,                                   # reads dO
+        "k_bwd_gemms": dO,                                   # reads dO
+        "k_bwd_intra": qkv + beta + gate + dqkv + dbeta + dg,  # reads inputs, writes grads
+    }
+    return table.get(kernel)
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it is for the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    from linear_attention_chunked_gb300 import build as b
+    sha = b.source_digest()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#"):
+            k, w, s, byts = parts[:4]
+            if k == kernel and w == workload and s == sha:
+                return float(byts)
+    return None
+
+
+# ---------------------------------------------------------------------------------------------
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the FP64 oracle on the host cores, bounded sample per step."""
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from harness import oracle_fwd_bwd
+    from linear_attention_chunked_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    inp = inputs.workload_inputs(args.workload)
+    oracle.build()
+    heads = [0]
+    cores = min(os.cpu_count() or 1, w.N * len(heads))
+    for _ in range(args.warmup):
+        oracle_fwd_bwd(inp, gate=w.gate, l2norm=w.l2norm, heads=heads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_fwd_bwd(inp, gate=w.gate, l2norm=w.l2norm, heads=heads)
+    dt = (time.perf_counter() - t0) / args.steps
+    full_s = dt * w.H / len(heads)  # seconds per full-workload step
+    value = w.T / full_s
+    line = {
+        "impl": "reference", "metric": f"KDA fwd+bwd tokens/s (H={w.H},d=128)",
+        "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": full_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.row}:saved", "T": w.T, "H": w.H, "docs": list(w.lens)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"head {heads} of {w.H} per step, fwd+bwd token by token, "
+                                   f"scaled by {w.H}/{len(heads)}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, inp):
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from harness import oracle_fwd_bwd
+    oracle.build()
+    heads = list(range(4))
+    cores = min(os.cpu_count() or 1, w.N * len(heads))
+    t0 = time.perf_counter()
+    oracle_fwd_bwd(inp, gate=w.gate, l2norm=w.l2norm, heads=heads)
+    dt = time.perf_counter() - t0
+    value = w.T * len(heads) / w.H / dt
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"heads {heads} of {w.H} (fwd+bwd, FP64 token by token), {dt:.1f} s, "
+                      f"scaled to {w.H} heads"}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from linear_attention_chunked_gb300 import inputs, kda
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    w = inputs.WORKLOADS[args.workload]
+    cpu_inp = inputs.workload_inputs(args.workload)
+    inp = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in cpu_inp.items()}
+    T, N, H = w.T, w.N, w.H
+    wsf, svb = kda.kda_workspace_size(T, N, H, kda.KDA_OP_FWD)
+    wsb, _ = kda.kda_workspace_size(T, N, H, kda.KDA_OP_BWD_SAVED)
+    ws = torch.empty(max(wsf, wsb), dtype=torch.uint8, device=dev)
+    saved = torch.empty(svb, dtype=torch.uint8, device=dev)
+    f32 = torch.float32
+    o = torch.empty((T, H, 128), dtype=f32, device=dev)
+    ht = torch.empty((N, H, 128, 128), dtype=f32, device=dev)
+    grads = dict(dq=torch.empty((T, H, 128), dtype=f32, device=dev),
+                 dk=torch.empty((T, H, 128), dtype=f32, device=dev),
+                 dv=torch.empty((T, H, 128), dtype=f32, device=dev),
+                 dbeta=torch.empty((T, H), dtype=f32, device=dev),
+                 dg=torch.empty((T, H, 128), dtype=f32, device=dev))
+    if w.gate == "raw":
+        grads["dA_log"] = torch.empty((H,), dtype=f32, device=dev)
+        grads["ddt_bias"] = torch.empty((H, 128), dtype=f32, device=dev)
+    kw = dict(gate=w.gate, l2norm=w.l2norm)
+
+    def step(x):
+        a = (x["q"], x["k"], x["v"], x["beta"], x["g"], x["cu_seqlens"])
+        kda.kda_fwd(*a, A_log=x["A_log"], dt_bias=x["dt_bias"], o=o, ht=ht, saved=saved, ws=ws,
+                    **kw)
+        kda.kda_bwd(*a, x["dO"], saved=saved, A_log=x["A_log"], dt_bias=x["dt_bias"],
+                    want_dh0=False, out=grads, ws=ws, **kw)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step(inp)
+    torch.cuda.synchronize()
+
+    # ---- timed region ----
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = kda.kda_launch_counter()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(inp)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ck = clocks.stop()
+    launches = kda.kda_launch_counter() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1e3)
+
+    # ---- per-kernel device time (second pass, CUDA events around every launch) ----
+    kda.kda_profile_enable(True)
+    for _ in range(args.steps):
+        step(inp)
+    torch.cuda.synchronize()
+    kda.kda_profile_enable(False)
+    prof = kda.kda_profile_collect()
+    kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+               for k, v in prof.items() if v[1]}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+    hbm, bf16, src = load_peaks()
+    per_th = alg_bytes_per_token_head(dom)
+    roof = None
+    if per_th is not None:
+        launch_ms = kernels[dom]["ms_per_step"] / kernels[dom]["launches_per_step"]
+        byts = per_th * T * H
+        achieved = byts / (launch_ms / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": src,
+                "alg_bytes_per_launch": byts, "launch_ms": launch_ms,
+                "traffic": traffic_for(dom, args.workload)}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in cpu_inp.items()}
+        res_host = {k: torch.empty(grads[k].shape, dtype=f32).pin_memory()
+                    for k in ("dA_log", "ddt_bias") if k in grads}
+        if not res_host:
+            res_host = {"ht": torch.empty(ht.shape, dtype=f32).pin_memory()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if torch.is_tensor(v))
+        d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+
+        def e2e_step():
+            for k_, v_ in host.items():
+                if torch.is_tensor(v_):
+                    inp[k_].copy_(v_, non_blocking=True)
+            step(inp)
+            for k_, v_ in res_host.items():
+                v_.copy_(grads[k_] if k_ in grads else ht, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = a0.elapsed_time(a1) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * T / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, cpu_inp)
+
+    if rank == 0:
+        line = {
+            "metric": f"KDA fwd+bwd tokens/s (H={H},d=128)", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": (value / world) / (T / (PAGES_MS / 1e3)),
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{w.row}:saved", "T": T, "H": H, "docs": list(w.lens),
+                       "d": 128, "chunk": 64, "outputs": "fp32",
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "clocks": ck,
+            "gpu_launches": launches,
+            "kernels": kernels,
+            "roofline": roof,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -166,6 +166,17 @@ kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int3
  * *device_status receives a kda_status value (KDA_OK when no device-side error happened). */
 kda_status kda_read_device_status(void* ws, int* device_status, kda_stream_t stream);
 
+/* Instrumentation (no effect on results).  Every kernel launch is counted; while profiling is
+ * enabled each launch is also bracketed by CUDA events recorded on its stream.
+ * kda_profile_collect waits for the recorded events and returns, per kernel kind (index <
+ * kda_kernel_count()), the summed device milliseconds and launch counts since the last collect;
+ * either array may be NULL. */
+kda_status kda_profile_enable(int enable);
+kda_status kda_profile_collect(double* ms_per_kind, uint64_t* launches_per_kind);
+int kda_kernel_count(void);
+const char* kda_kernel_name(int kind);
+uint64_t kda_launch_counter(void);
+
 /* Human-readable text of a status; never NULL. */
 const char* kda_status_string(kda_status s);
 

@@ -64,6 +64,18 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
+
+def source_digest() -> str:
+    """Short digest of the CUDA sources and the ABI header (ties profiles to the code they measured)."""
+    import hashlib
+    h = hashlib.sha256()
+    for path in sorted(_deps()):
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))

@@ -133,8 +133,14 @@ kda_status launched() {
 
 // plan + intra-chunk products (shared by every op)
 kda_status run_prologue(const Params& p, cudaStream_t st) {
-    k_plan<<<1, NTHR, 0, st>>>(p);
-    if (p.maxC > 0) k_intra_fwd<<<dim3(unsigned(p.maxC), p.H), NTHR, SMEM_INTRA_FWD, st>>>(p);
+    {
+        ProfScope ps(KK_PLAN, st);
+        k_plan<<<1, NTHR, 0, st>>>(p);
+    }
+    if (p.maxC > 0) {
+        ProfScope ps(KK_INTRA_FWD, st);
+        k_intra_fwd<<<dim3(unsigned(p.maxC), p.H), NTHR, SMEM_INTRA_FWD, st>>>(p);
+    }
     return launched();
 }
 
@@ -194,7 +200,10 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
         p.sDelta = reinterpret_cast<float*>(static_cast<char*>(saved) + L.sv_Delta);
     }
     if (kda_status s = run_prologue(p, st)) return s;
-    k_chain_fwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FWD_OUT);
+    {
+        ProfScope ps(KK_CHAIN_FWD, st);
+        k_chain_fwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FWD_OUT);
+    }
     return launched();
 }
 
@@ -238,15 +247,26 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         Params r = p;
         r.o = nullptr;
         r.ht = nullptr;
+        ProfScope ps(KK_CHAIN_FWD, st);
         k_chain_fwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(r, CHAIN_FWD_OUT);
     }
-    k_chain_bwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_BWD);
+    {
+        ProfScope ps(KK_CHAIN_BWD, st);
+        k_chain_bwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_BWD);
+    }
     if (L.maxC > 0) {
         const dim3 grid(unsigned(L.maxC), pr->H);
-        k_bwd_gemms<<<grid, NTHR, SMEM_BWD_GEMMS, st>>>(p);
+        {
+            ProfScope ps(KK_BWD_GEMMS, st);
+            k_bwd_gemms<<<grid, NTHR, SMEM_BWD_GEMMS, st>>>(p);
+        }
+        ProfScope ps(KK_BWD_INTRA, st);
         k_bwd_intra<<<grid, NTHR, SMEM_BWD_INTRA, st>>>(p);
     }
-    if (p.gate_raw) k_param_reduce<<<pr->H, D, 0, st>>>(p);
+    if (p.gate_raw) {
+        ProfScope ps(KK_PARAM_REDUCE, st);
+        k_param_reduce<<<pr->H, D, 0, st>>>(p);
+    }
     return launched();
 }
 
@@ -271,10 +291,13 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     p.fragM = M;
     p.fragB = B_or_C;
     if (kda_status s = run_prologue(p, st)) return s;
-    if (mode == KDA_FRAG_FWD)
+    if (mode == KDA_FRAG_FWD) {
+        ProfScope ps(KK_CHAIN_FWD, st);
         k_chain_fwd<<<dim3(pr->N, pr->H, 2 * NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FRAG_MB);
-    else
+    } else {
+        ProfScope ps(KK_CHAIN_BWD, st);
         k_chain_bwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FRAG_C);
+    }
     return launched();
 }
 
@@ -288,8 +311,11 @@ kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int3
     if (!opt(S0) || !opt(S_final)) return KDA_ERR_INVALID_ARG;
     if (kda_status s = setup_device()) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, F, H, M, B, S0, reverse, S_in,
-                                                         S_final);
+    {
+        ProfScope ps(KK_WALK, st);
+        k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, F, H, M, B, S0, reverse,
+                                                             S_in, S_final);
+    }
     return launched();
 }
 

@@ -195,6 +195,23 @@ __global__ void k_param_reduce(Params p);
 __global__ void k_walk(int N, const int* doc_frag, int F, int H, const float* M, const float* B,
                        const float* S0, int reverse, float* S_in, float* S_final);
 
+// Launch accounting: every kernel launch of the library sits inside a ProfScope, which counts it
+// and, while profiling is enabled (kda_profile_enable), brackets it with CUDA events on its stream.
+enum KernelKind {
+    KK_PLAN, KK_INTRA_FWD, KK_CHAIN_FWD, KK_CHAIN_BWD, KK_BWD_GEMMS, KK_BWD_INTRA,
+    KK_PARAM_REDUCE, KK_WALK, KK_COUNT
+};
+const char* kernel_name(int kind);
+class ProfScope {
+  public:
+    ProfScope(int kind, cudaStream_t st);
+    ~ProfScope();
+  private:
+    int kind_;
+    cudaStream_t st_;
+    cudaEvent_t a_, b_;
+};
+
 // chain modes
 constexpr int CHAIN_FWD_OUT = 0;   // forward: o, ht, optional saved set
 constexpr int CHAIN_FRAG_MB = 1;   // fragment summary: augmented state [M | B]

@@ -24,7 +24,9 @@ KDA_OP_FWD, KDA_OP_BWD_SAVED, KDA_OP_BWD_REPLAY, KDA_OP_FRAGMENT, KDA_OP_WALK = 
 KDA_FRAG_FWD, KDA_FRAG_BWD = 0, 1
 
 EXPORTS = ("kda_workspace_size", "kda_fwd", "kda_bwd", "kda_fragment_summary",
-           "kda_transfer_walk", "kda_read_device_status", "kda_status_string")
+           "kda_transfer_walk", "kda_read_device_status", "kda_profile_enable",
+           "kda_profile_collect", "kda_kernel_count", "kda_kernel_name", "kda_launch_counter",
+           "kda_status_string")
 
 
 class KdaError(RuntimeError):
@@ -66,9 +68,18 @@ def lib():
             L.kda_transfer_walk.argtypes = [ctypes.c_int32, V, ctypes.c_int32, ctypes.c_int32,
                                             V, V, V, I, V, V, V]
             L.kda_read_device_status.argtypes = [V, ctypes.POINTER(I), V]
+            L.kda_profile_enable.argtypes = [I]
+            L.kda_profile_collect.argtypes = [V, V]
+            L.kda_kernel_count.argtypes = []
+            L.kda_kernel_name.argtypes = [I]
+            L.kda_kernel_name.restype = ctypes.c_char_p
+            L.kda_launch_counter.argtypes = []
+            L.kda_launch_counter.restype = ctypes.c_uint64
             L.kda_status_string.argtypes = [I]
             L.kda_status_string.restype = ctypes.c_char_p
-            for name in EXPORTS[:-1]:
+            for name in ("kda_workspace_size", "kda_fwd", "kda_bwd", "kda_fragment_summary",
+                         "kda_transfer_walk", "kda_read_device_status", "kda_profile_enable",
+                         "kda_profile_collect", "kda_kernel_count"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -233,3 +244,20 @@ def kda_read_device_status(ws) -> int:
         _check("kda_read_device_status",
                lib().kda_read_device_status(_ptr(ws), ctypes.byref(v), _stream(ws.device)))
     return v.value
+
+
+def kda_profile_enable(enable=True):
+    _check("kda_profile_enable", lib().kda_profile_enable(int(bool(enable))))
+
+
+def kda_profile_collect():
+    """{kernel name: (summed device ms, launches)} since the last collect (waits for events)."""
+    n = lib().kda_kernel_count()
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_uint64 * n)()
+    _check("kda_profile_collect", lib().kda_profile_collect(ms, cnt))
+    return {lib().kda_kernel_name(i).decode(): (ms[i], cnt[i]) for i in range(n)}
+
+
+def kda_launch_counter() -> int:
+    return int(lib().kda_launch_counter())

@@ -9,9 +9,10 @@ using namespace kda;
 
 namespace {
 
-constexpr size_t SMEM_INTRA_FWD = (4 * CH * LDP + 3 * CH * LDA + CH + GEMM_SCRATCH) * 4;
-constexpr size_t SMEM_CHAIN = (D * (SLICE + 1) + CH * (SLICE + 1) + GEMM_SCRATCH) * 4;
-constexpr size_t SMEM_BWD_GEMMS = GEMM_SCRATCH * 4;
+const size_t SMEM_INTRA_FWD = intra_smem_bytes();
+const size_t SMEM_CHAIN_FWD = chain_fwd_smem_bytes();
+const size_t SMEM_CHAIN_BWD = chain_bwd_smem_bytes();
+const size_t SMEM_BWD_GEMMS = bwd_gemm_smem_bytes();
 constexpr size_t SMEM_BWD_INTRA = (4 * CH * LDP + 3 * CH * LDA + 3 * CH + NTHR) * 4;
 constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
 
@@ -31,8 +32,8 @@ kda_status setup_device() {
         return KDA_ERR_CUDA;
     if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
     struct { const void* f; size_t smem; } attrs[] = {
-        {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd, SMEM_CHAIN},
-        {(const void*)k_chain_bwd, SMEM_CHAIN},     {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
+        {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd, SMEM_CHAIN_FWD},
+        {(const void*)k_chain_bwd, SMEM_CHAIN_BWD}, {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
         {(const void*)k_bwd_intra, SMEM_BWD_INTRA}, {(const void*)k_walk, SMEM_WALK},
     };
     for (auto& a : attrs)
@@ -89,14 +90,21 @@ Params make_params(const kda_problem* pr, const Layout& L, void* ws) {
     p.doc_off = reinterpret_cast<int*>(w + L.doc_off);
     p.chunk_tab = reinterpret_cast<int4*>(w + L.chunk_tab);
     auto f = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
-    p.gam = f(L.gam);
-    p.W = f(L.W);
+    auto b = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(w + off); };
+    p.Wh = b(L.Wh);
+    p.Wl = b(L.Wl);
+    p.Qh = b(L.Qh);
+    p.Ql = b(L.Ql);
+    p.Kh = b(L.Kh);
+    p.Kl = b(L.Kl);
+    p.Ah = b(L.Ah);
+    p.Al = b(L.Al);
+    p.Mh = b(L.Mh);
+    p.Ml = b(L.Ml);
     p.U = f(L.U);
-    p.Qg = f(L.Qg);
-    p.Kb = f(L.Kb);
-    p.Aqk = f(L.Aqk);
     p.Akk = f(L.Akk);
-    p.Minv = f(L.Minv);
+    p.gam = f(L.gam);
+    p.eGL = f(L.eGL);
     return p;
 }
 
@@ -202,7 +210,7 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     if (kda_status s = run_prologue(p, st)) return s;
     {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FWD_OUT);
+        k_chain_fwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD, st>>>(p, CHAIN_FWD_OUT);
     }
     return launched();
 }
@@ -248,11 +256,11 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         r.o = nullptr;
         r.ht = nullptr;
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(r, CHAIN_FWD_OUT);
+        k_chain_fwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD, st>>>(r, CHAIN_FWD_OUT);
     }
     {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_BWD);
+        k_chain_bwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD, st>>>(p, CHAIN_BWD);
     }
     if (L.maxC > 0) {
         const dim3 grid(unsigned(L.maxC), pr->H);
@@ -293,10 +301,10 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     if (kda_status s = run_prologue(p, st)) return s;
     if (mode == KDA_FRAG_FWD) {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd<<<dim3(pr->N, pr->H, 2 * NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FRAG_MB);
+        k_chain_fwd<<<dim3(pr->N, pr->H, 2 * NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD, st>>>(p, CHAIN_FRAG_MB);
     } else {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd<<<dim3(pr->N, pr->H, NSLICE), NTHR, SMEM_CHAIN, st>>>(p, CHAIN_FRAG_C);
+        k_chain_bwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD, st>>>(p, CHAIN_FRAG_C);
     }
     return launched();
 }

@@ -37,282 +37,261 @@ __global__ void k_plan(Params p) {
     }
 }
 
-// Intra-chunk products of one (chunk, head): gam, Akk, Aqk, Minv, W, U, Qg, Kb.
-// Shared: q, k, gam, scratch [64 x 129] fp32; Akk, Aqk, Minv [64 x 65]; beta; gemm scratch.
-__global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
-    const int ci = blockIdx.x, h = blockIdx.y;
-    if (ci >= *p.nchunks) return;
-    const int4 info = p.chunk_tab[ci];
-    const int t0 = info.y, L = info.z;
-    extern __shared__ float sm[];
-    float* sq = sm;
-    float* sk = sq + CH * LDP;
-    float* sg = sk + CH * LDP;
-    float* sb = sg + CH * LDP;
-    float* sAkk = sb + CH * LDP;
-    float* sAqk = sAkk + CH * LDA;
-    float* sMi = sAqk + CH * LDA;
-    float* sbeta = sMi + CH * LDA;
-    float* gs = sbeta + CH;
-    const int tid = threadIdx.x;
-    const size_t chd = size_t(ci) * p.H + h;
+namespace {
 
-    // 1. loads (zero-padded past the document end), gate
-    for (int i = tid; i < CH * D; i += NTHR) {
-        const int r = i / D, c = i % D;
-        float qv = 0.f, kv = 0.f, gv = 0.f;
-        if (r < L) {
-            const size_t off = (size_t(t0 + r) * p.H + h) * D + c;
-            qv = bf2f(p.q[off]);
-            kv = bf2f(p.k[off]);
-            const float x = p.g[off];
-            gv = p.gate_raw ? -expf(p.A_log[h]) * softplus_f(x + p.dt_bias[h * D + c]) : x;
-        }
-        sq[r * LDP + c] = qv;
-        sk[r * LDP + c] = kv;
-        sg[r * LDP + c] = gv;
-    }
-    if (tid < CH) sbeta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
-    __syncthreads();
+constexpr int LB = 136;   // row stride (bf16) of [64][128] operand tiles
+constexpr int LB64 = 72;  // row stride (bf16) of [rows][64] tiles
+constexpr int LU = 68;    // row stride (fp32) of the U half tile
 
-    // 2. fused L2 norm of q and k over the 128 channels of the head (warp per row)
-    if (p.l2n) {
-        const int w = tid / 32, lane = tid % 32;
-        for (int r = w; r < CH; r += NTHR / 32) {
-            float a = 0.f, b = 0.f;
-            for (int c = lane; c < D; c += 32) {
-                float x = sq[r * LDP + c], y = sk[r * LDP + c];
-                a = fmaf(x, x, a);
-                b = fmaf(y, y, b);
-            }
-            a = warp_sum(a);
-            b = warp_sum(b);
-            const float ra = 1.f / sqrtf(a + p.eps), rb = 1.f / sqrtf(b + p.eps);
-            for (int c = lane; c < D; c += 32) {
-                sq[r * LDP + c] *= ra;
-                sk[r * LDP + c] *= rb;
-            }
-        }
-    }
-    // 3. in-chunk inclusive cumsum of the gate (thread per channel)
-    if (tid < D) {
-        float run = 0.f;
-        for (int r = 0; r < CH; ++r) {
-            run += sg[r * LDP + tid];
-            sg[r * LDP + tid] = run;
-        }
-    }
-    __syncthreads();
+struct ChainFwdSmem {
+    __nv_bfloat16 S[2][D * LB64];   // state S [key][64 values] (hi, lo)
+    __nv_bfloat16 Dl[2][CH * LB64]; // Delta [token][64 values] (hi, lo)
+    __nv_bfloat16 W[2][CH * LB];    // W [token][key]
+    __nv_bfloat16 Q[2][CH * LB];    // Qg [token][key]
+    __nv_bfloat16 K[2][CH * LB];    // Kb [token][key]
+    __nv_bfloat16 A[2][CH * LB64];  // Aqk [token][token]
+    float U[CH * LU];               // U [token][64 values]
+    float eGL[D];                   // e^gL per key
+};
 
-    // 4. Akk (strictly lower) and Aqk (lower incl. diagonal) with exact exponent differences
-    for (int i = tid; i < CH * CH; i += NTHR) {
-        const int r = i / CH, s = i % CH;
-        float akk = 0.f, aqk = 0.f;
-        if (s <= r) {
-            for (int c = 0; c < D; ++c) {
-                const float e = expf(sg[r * LDP + c] - sg[s * LDP + c]);
-                const float ks = sk[s * LDP + c] * e;
-                akk = fmaf(sk[r * LDP + c], ks, akk);
-                aqk = fmaf(sq[r * LDP + c], ks, aqk);
-            }
-        }
-        sAkk[r * LDA + s] = s < r ? akk : 0.f;
-        sAqk[r * LDA + s] = aqk;
-    }
-    __syncthreads();
+}  // namespace
 
-    // 5. Minv = (I + diag(beta) Akk)^-1 by forward substitution, one column per thread
-    if (tid < CH) {
-        const int c = tid;
-        for (int r = 0; r < CH; ++r) {
-            float val = (r == c) ? 1.f : 0.f;
-            if (r > c) {
-                float acc = 0.f;
-                for (int s = c; s < r; ++s) acc = fmaf(sAkk[r * LDA + s], sMi[s * LDA + c], acc);
-                val = -sbeta[r] * acc;
-            }
-            sMi[r * LDA + c] = val;
-        }
-    }
-    // scratch = beta * K * e^gam
-    for (int i = tid; i < CH * D; i += NTHR) {
-        const int r = i / D, c = i % D;
-        sb[r * LDP + c] = sbeta[r] * sk[r * LDP + c] * expf(sg[r * LDP + c]);
-    }
-    __syncthreads();
+size_t chain_fwd_smem_bytes() { return sizeof(ChainFwdSmem); }
 
-    // 6. W = Minv (beta K e^gam), then U = Minv (beta V)
-    constexpr int TX = D / 8;  // block_gemm<64,128,4,8> thread map
-    const int tx = tid % TX, ty = tid / TX;
-    {
-        float acc[4][8];
-        zero_acc(acc);
-        block_gemm<CH, D, 4, 8>(acc, [&](int m, int kk) { return sMi[m * LDA + kk]; },
-                                [&](int kk, int n) { return sb[kk * LDP + n]; }, CH, gs, gs + 16 * CH);
-        float* W = p.W + chd * CH * D;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) W[(ty + 16 * i) * D + tx + TX * j] = acc[i][j];
-    }
-    for (int i = tid; i < CH * D; i += NTHR) {
-        const int r = i / D, c = i % D;
-        sb[r * LDP + c] = r < L ? sbeta[r] * bf2f(p.v[(size_t(t0 + r) * p.H + h) * D + c]) : 0.f;
-    }
-    {
-        float acc[4][8];
-        zero_acc(acc);
-        block_gemm<CH, D, 4, 8>(acc, [&](int m, int kk) { return sMi[m * LDA + kk]; },
-                                [&](int kk, int n) { return sb[kk * LDP + n]; }, CH, gs, gs + 16 * CH);
-        float* U = p.U + chd * CH * D;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) U[(ty + 16 * i) * D + tx + TX * j] = acc[i][j];
-    }
-
-    // 7. elementwise products and the small matrices
-    {
-        float* gam = p.gam + chd * CH * D;
-        float* Qg = p.Qg + chd * CH * D;
-        float* Kb = p.Kb + chd * CH * D;
-        for (int i = tid; i < CH * D; i += NTHR) {
-            const int r = i / D, c = i % D;
-            const float g = sg[r * LDP + c], gl = sg[(CH - 1) * LDP + c];
-            gam[i] = g;
-            Qg[i] = sq[r * LDP + c] * expf(g);
-            Kb[i] = sk[r * LDP + c] * expf(gl - g);
-        }
-        float* Aqk = p.Aqk + chd * CH * CH;
-        float* Akk = p.Akk + chd * CH * CH;
-        float* Mi = p.Minv + chd * CH * CH;
-        for (int i = tid; i < CH * CH; i += NTHR) {
-            const int r = i / CH, s = i % CH;
-            Aqk[i] = sAqk[r * LDA + s];
-            Akk[i] = sAkk[r * LDA + s];
-            Mi[i] = sMi[r * LDA + s];
-        }
-    }
-}
-
-// Inter-chunk state recurrence of one (document, head, 32-column value slice).
-// mode CHAIN_FWD_OUT: S from h0; per chunk save S (and Delta) when p.sS is set, write o; ht.
-// mode CHAIN_FRAG_MB: blockIdx.z < NSLICE evolves X = I with zero values (-> M), the rest
-//                     evolves Y = 0 with the chunk values (-> B); no output.
-__global__ void __launch_bounds__(NTHR) k_chain_fwd(Params p, int mode) {
-    constexpr int LS = SLICE + 1;
-    const int n = blockIdx.x, h = blockIdx.y, sl = blockIdx.z;
-    const bool fragX = (mode == CHAIN_FRAG_MB) && sl < NSLICE;
-    const int col0 = (sl % NSLICE) * SLICE;
-    extern __shared__ float sm[];
-    float* sS = sm;            // [128][33]
-    float* sD = sS + D * LS;   // [64][33]
-    float* gs = sD + CH * LS;
-    const int tid = threadIdx.x;
+// Inter-chunk state recurrence of one (document, head, 64-column value half) on tensor cores.
+// Warp w keeps keys 32w..32w+31 of the FP32 state in registers; per chunk:
+//   A: Delta = U - W S            (warp w: tokens 16w..16w+15)
+//   C: O = Qg S + Aqk Delta       (output; forward mode only)
+//   D: S = e^gL * S + Kb^T Delta  (warp w: its 32 keys)
+// Operands of chunk c+1 are prefetched with cp.async as soon as their buffer is consumed.
+// mode CHAIN_FWD_OUT: S from h0; writes o, ht and (when p.sS) the saved S_c and Delta_c.
+// mode CHAIN_FRAG_MB: blockIdx.z in 0..3: halves 0,1 evolve X = I with zero values (-> M),
+//                     halves 2,3 evolve Y = 0 with the chunk values (-> B).
+__global__ void __launch_bounds__(128) k_chain_fwd(Params p, int mode) {
+    const int n = blockIdx.x, h = blockIdx.y, hv = blockIdx.z;
+    const bool fwd = mode == CHAIN_FWD_OUT;
+    const bool fragX = !fwd && hv < 2;
+    const int col0 = (hv & 1) * 64;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    ChainFwdSmem& sm = *reinterpret_cast<ChainFwdSmem*>(smraw);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
 
-    for (int i = tid; i < D * SLICE; i += NTHR) {
-        const int r = i / SLICE, j = i % SLICE;
-        float v0 = 0.f;
-        if (mode == CHAIN_FRAG_MB) v0 = (fragX && r == col0 + j) ? 1.f : 0.f;
-        else if (p.h0) v0 = p.h0[dh + size_t(r) * D + col0 + j];
-        sS[r * LS + j] = v0;
-    }
-    __syncthreads();
+    float Sv[2][8][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = 32 * w + 16 * mt + g + 8 * (e >> 1);
+                const int val = col0 + 8 * nt + 2 * t + (e & 1);
+                float v0 = 0.f;
+                if (!fwd) v0 = (fragX && key == val) ? 1.f : 0.f;
+                else if (p.h0) v0 = p.h0[dh + size_t(key) * D + val];
+                Sv[mt][nt][e] = v0;
+            }
+    auto store_S = [&]() {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int key = 32 * w + 16 * mt + g + 8 * hf, col = 8 * nt + 2 * t;
+                    uint32_t hi, lo;
+                    split2(Sv[mt][nt][2 * hf], Sv[mt][nt][2 * hf + 1], hi, lo);
+                    *reinterpret_cast<uint32_t*>(&sm.S[0][key * LB64 + col]) = hi;
+                    *reinterpret_cast<uint32_t*>(&sm.S[1][key * LB64 + col]) = lo;
+                }
+    };
+    auto issue_WU = [&](int ci) {
+        if (ci < c1) {
+            const size_t chd = size_t(ci) * p.H + h;
+            cp_tile_bf16(sm.W[0], LB, p.Wh + chd * CH * D, D, CH, D, tid, 128);
+            cp_tile_bf16(sm.W[1], LB, p.Wl + chd * CH * D, D, CH, D, tid, 128);
+            if (!fragX) cp_tile_f32(sm.U, LU, p.U + chd * CH * D + col0, D, CH, 64, tid, 128);
+        }
+        cp_commit();
+    };
+    auto issue_QA = [&](int ci) {
+        if (ci < c1 && fwd && p.o) {
+            const size_t chd = size_t(ci) * p.H + h;
+            cp_tile_bf16(sm.Q[0], LB, p.Qh + chd * CH * D, D, CH, D, tid, 128);
+            cp_tile_bf16(sm.Q[1], LB, p.Ql + chd * CH * D, D, CH, D, tid, 128);
+            cp_tile_bf16(sm.A[0], LB64, p.Ah + chd * CH * CH, CH, CH, CH, tid, 128);
+            cp_tile_bf16(sm.A[1], LB64, p.Al + chd * CH * CH, CH, CH, CH, tid, 128);
+        }
+        cp_commit();
+    };
+    auto issue_K = [&](int ci) {
+        if (ci < c1) {
+            const size_t chd = size_t(ci) * p.H + h;
+            cp_tile_bf16(sm.K[0], LB, p.Kh + chd * CH * D, D, CH, D, tid, 128);
+            cp_tile_bf16(sm.K[1], LB, p.Kl + chd * CH * D, D, CH, D, tid, 128);
+            cp_tile_f32(sm.eGL, D, p.eGL + chd * D, D, 1, D, tid, 128);
+        }
+        cp_commit();
+    };
+    issue_WU(c0);
+    issue_QA(c0);
+    issue_K(c0);
+    store_S();
 
     for (int ci = c0; ci < c1; ++ci) {
         const int4 info = p.chunk_tab[ci];
         const int t0 = info.y, L = info.z;
         const size_t chd = size_t(ci) * p.H + h;
-        const float* W = p.W + chd * CH * D;
-        const float* U = p.U + chd * CH * D;
-        const float* Qg = p.Qg + chd * CH * D;
-        const float* Kb = p.Kb + chd * CH * D;
-        const float* Aqk = p.Aqk + chd * CH * CH;
-        const float* gam = p.gam + chd * CH * D;
-        if (mode == CHAIN_FWD_OUT && p.sS) {
+        if (fwd && p.sS) {  // saved state at the chunk start
             float* dst = p.sS + chd * D * D;
-            for (int i = tid; i < D * SLICE; i += NTHR) {
-                const int r = i / SLICE, j = i % SLICE;
-                dst[size_t(r) * D + col0 + j] = sS[r * LS + j];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int key = 32 * w + 16 * mt + g + 8 * hf, val = col0 + 8 * nt + 2 * t;
+                        *reinterpret_cast<float2*>(dst + size_t(key) * D + val) =
+                            make_float2(Sv[mt][nt][2 * hf], Sv[mt][nt][2 * hf + 1]);
+                    }
+        }
+        // ---- A: Delta = U - W S ----
+        cp_wait<2>();
+        __syncthreads();
+        float dl[8][4] = {};
+#pragma unroll 2
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t ah[4], al[4];
+            ldsm4(ah, a_addr(sm.W[0], LB, 16 * w, 16 * ks, lane));
+            ldsm4(al, a_addr(sm.W[1], LB, 16 * w, 16 * ks, lane));
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bh[4], bl[4];
+                ldsm4t(bh, bk_addr(sm.S[0], LB64, 16 * ks, 16 * np, lane));
+                ldsm4t(bl, bk_addr(sm.S[1], LB64, 16 * ks, 16 * np, lane));
+                mma_x3(dl[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
+                mma_x3(dl[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
             }
         }
-        // Delta = U - W S   (64 x 32)
-        {
-            float acc[2][4];
-            zero_acc(acc);
-            block_gemm<CH, SLICE, 2, 4>(acc, [&](int m, int kk) { return W[m * D + kk]; },
-                                        [&](int kk, int nn) { return sS[kk * LS + nn]; }, D, gs,
-                                        gs + 16 * CH);
-            const int tx = tid % 8, ty = tid / 8;
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+        for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = ty + 32 * i, jj = tx + 8 * j;
-                    const float u = fragX ? 0.f : U[r * D + col0 + jj];
-                    sD[r * LS + jj] = u - acc[i][j];
+            for (int hf = 0; hf < 2; ++hf) {
+                const int row = 16 * w + g + 8 * hf, col = 8 * nt + 2 * t;
+                float d0 = -dl[nt][2 * hf], d1 = -dl[nt][2 * hf + 1];
+                if (!fragX) {
+                    d0 += sm.U[row * LU + col];
+                    d1 += sm.U[row * LU + col + 1];
+                }
+                dl[nt][2 * hf] = d0;
+                dl[nt][2 * hf + 1] = d1;
+                uint32_t hi, lo;
+                split2(d0, d1, hi, lo);
+                *reinterpret_cast<uint32_t*>(&sm.Dl[0][row * LB64 + col]) = hi;
+                *reinterpret_cast<uint32_t*>(&sm.Dl[1][row * LB64 + col]) = lo;
+                if (fwd && p.sDelta)
+                    *reinterpret_cast<float2*>(p.sDelta + chd * CH * D + row * D + col0 + col) =
+                        make_float2(d0, d1);
+            }
+        __syncthreads();
+        issue_WU(ci + 1);
+        // ---- C: O = Qg S + Aqk Delta ----
+        cp_wait<2>();
+        __syncthreads();
+        if (fwd && p.o) {
+            float acc[8][4] = {};
+#pragma unroll 2
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t ah[4], al[4];
+                ldsm4(ah, a_addr(sm.Q[0], LB, 16 * w, 16 * ks, lane));
+                ldsm4(al, a_addr(sm.Q[1], LB, 16 * w, 16 * ks, lane));
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bh[4], bl[4];
+                    ldsm4t(bh, bk_addr(sm.S[0], LB64, 16 * ks, 16 * np, lane));
+                    ldsm4t(bl, bk_addr(sm.S[1], LB64, 16 * ks, 16 * np, lane));
+                    mma_x3(acc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
+                    mma_x3(acc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+                }
+            }
+            for (int ks = 0; ks <= w; ++ks) {  // Aqk is lower triangular
+                uint32_t ah[4], al[4];
+                ldsm4(ah, a_addr(sm.A[0], LB64, 16 * w, 16 * ks, lane));
+                ldsm4(al, a_addr(sm.A[1], LB64, 16 * w, 16 * ks, lane));
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bh[4], bl[4];
+                    ldsm4t(bh, bk_addr(sm.Dl[0], LB64, 16 * ks, 16 * np, lane));
+                    ldsm4t(bl, bk_addr(sm.Dl[1], LB64, 16 * ks, 16 * np, lane));
+                    mma_x3(acc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
+                    mma_x3(acc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int row = 16 * w + g + 8 * hf, col = col0 + 8 * nt + 2 * t;
+                    if (row < L) {
+                        const size_t off = (size_t(t0 + row) * p.H + h) * D + col;
+                        store_out(p.o, off, p.scale * acc[nt][2 * hf], p.out_fp32);
+                        store_out(p.o, off + 1, p.scale * acc[nt][2 * hf + 1], p.out_fp32);
+                    }
                 }
         }
         __syncthreads();
-        if (mode == CHAIN_FWD_OUT) {
-            if (p.sDelta) {
-                float* dst = p.sDelta + chd * CH * D;
-                for (int i = tid; i < CH * SLICE; i += NTHR) {
-                    const int r = i / SLICE, j = i % SLICE;
-                    dst[r * D + col0 + j] = sD[r * LS + j];
+        issue_QA(ci + 1);
+        // ---- D: S = e^gL * S + Kb^T Delta ----
+        cp_wait<2>();
+        __syncthreads();
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float eg = sm.eGL[32 * w + 16 * mt + g + 8 * (e >> 1)];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) Sv[mt][nt][e] *= eg;
+            }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t ah[2][4], al[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                ldsm4t(ah[mt], at_addr(sm.K[0], LB, 32 * w + 16 * mt, 16 * ks, lane));
+                ldsm4t(al[mt], at_addr(sm.K[1], LB, 32 * w + 16 * mt, 16 * ks, lane));
+            }
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bh[4], bl[4];
+                ldsm4t(bh, bk_addr(sm.Dl[0], LB64, 16 * ks, 16 * np, lane));
+                ldsm4t(bl, bk_addr(sm.Dl[1], LB64, 16 * ks, 16 * np, lane));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    mma_x3(Sv[mt][2 * np], ah[mt], al[mt], bh[0], bh[1], bl[0], bl[1]);
+                    mma_x3(Sv[mt][2 * np + 1], ah[mt], al[mt], bh[2], bh[3], bl[2], bl[3]);
                 }
             }
         }
-        if (mode == CHAIN_FWD_OUT && p.o) {
-            // O = Qg S + Aqk Delta
-            float acc[2][4];
-            zero_acc(acc);
-            block_gemm<CH, SLICE, 2, 4>(acc, [&](int m, int kk) { return Qg[m * D + kk]; },
-                                        [&](int kk, int nn) { return sS[kk * LS + nn]; }, D, gs,
-                                        gs + 16 * CH);
-            block_gemm<CH, SLICE, 2, 4>(acc, [&](int m, int kk) { return Aqk[m * CH + kk]; },
-                                        [&](int kk, int nn) { return sD[kk * LS + nn]; }, CH, gs,
-                                        gs + 16 * CH);
-            const int tx = tid % 8, ty = tid / 8;
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = ty + 32 * i, jj = tx + 8 * j;
-                    if (r < L)
-                        store_out(p.o, (size_t(t0 + r) * p.H + h) * D + col0 + jj,
-                                  p.scale * acc[i][j], p.out_fp32);
-                }
-        }
-        // S = e^gL S + Kb^T Delta   (128 x 32)
-        {
-            float acc[4][4];
-            zero_acc(acc);
-            block_gemm<D, SLICE, 4, 4>(acc, [&](int m, int kk) { return Kb[kk * D + m]; },
-                                       [&](int kk, int nn) { return sD[kk * LS + nn]; }, CH, gs,
-                                       gs + 16 * D);
-            const int tx = tid % 8, ty = tid / 8;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = ty + 32 * i, jj = tx + 8 * j;
-                    const float e = expf(gam[(CH - 1) * D + r]);
-                    sS[r * LS + jj] = fmaf(e, sS[r * LS + jj], acc[i][j]);
-                }
-        }
         __syncthreads();
+        issue_K(ci + 1);
+        store_S();
     }
-    float* out = nullptr;
-    if (mode == CHAIN_FWD_OUT) out = p.ht ? p.ht + dh : nullptr;
-    else out = (fragX ? p.fragM : p.fragB) + dh;
-    if (out)
-        for (int i = tid; i < D * SLICE; i += NTHR) {
-            const int r = i / SLICE, j = i % SLICE;
-            out[size_t(r) * D + col0 + j] = sS[r * LS + j];
-        }
+    cp_wait<0>();
+    float* out = fwd ? p.ht : (fragX ? p.fragM : p.fragB);
+    if (out) {
+        out += dh;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int key = 32 * w + 16 * mt + g + 8 * hf, val = col0 + 8 * nt + 2 * t;
+                    *reinterpret_cast<float2*>(out + size_t(key) * D + val) =
+                        make_float2(Sv[mt][nt][2 * hf], Sv[mt][nt][2 * hf + 1]);
+                }
+    }
 }
 
 }  // namespace kda

@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include "../../include/kda.h"
+#include "kda_mma.cuh"
 
 namespace kda {
 
@@ -29,16 +30,20 @@ constexpr int LDA = CH + 1;  // padded row stride of [64 x 64] shared tiles
 
 // Byte offsets of every region of the workspace / saved buffers.  Everything is derived from
 // (T, N, H) only, so one allocation serves every pack with the same sizes.
+//
+// Per (chunk, head) the intra-chunk stage writes the operands of the state recurrence: the MMA
+// operands W, Qg = Q e^gam, Kb = K e^(gL - gam), Aqk and Minv as bf16 hi/lo planes (hi + lo carries
+// ~16 significant bits), U as fp32 (accumulator initialiser), Akk and gam as fp32, and e^gL.
 struct Layout {
     int64_t T;
     int N, H;
     int64_t maxC;  // upper bound of the chunk count: ceil(T/64) + N
     // workspace
     size_t status, nchunks, doc_off, chunk_tab;
-    size_t gam, W, U, Qg, Kb, Aqk, Akk, Minv;           // per (chunk, head) intra products
-    size_t dS1, dDelta, dR, P, dQg, dKb, dAqk, dM, rsum; // backward intermediates
-    size_t pdA, pddt;                                   // per (chunk, head) parameter partials
-    size_t replay;                                      // saved set recomputed in replay mode
+    size_t Wh, Wl, Qh, Ql, Kh, Kl, Ah, Al, Mh, Ml, U, Akk, gam, eGL;  // intra products
+    size_t dS1, dDelta, dR, P, dQg, dKb, dAqk, dM, rsum;              // backward intermediates
+    size_t pdA, pddt;                                                 // parameter partials
+    size_t replay;                                                    // saved set (replay mode)
     size_t ws_fwd, ws_bwd_saved, ws_bwd_replay, ws_frag;
     // saved set
     size_t sv_S, sv_Delta, saved_bytes;
@@ -59,34 +64,41 @@ inline Layout make_layout(int64_t T, int N, int H) {
     L.nchunks = take(sizeof(int));
     L.doc_off = take(sizeof(int) * size_t(N + 1));
     L.chunk_tab = take(sizeof(int4) * size_t(L.maxC));
-    L.gam = take(CHd * CH * D * 4);
-    L.W = take(CHd * CH * D * 4);
-    L.U = take(CHd * CH * D * 4);
-    L.Qg = take(CHd * CH * D * 4);
-    L.Kb = take(CHd * CH * D * 4);
-    L.Aqk = take(CHd * CH * CH * 4);
-    L.Akk = take(CHd * CH * CH * 4);
-    L.Minv = take(CHd * CH * CH * 4);
+    const size_t tileD = CHd * CH * D, tileC = CHd * CH * CH;
+    L.Wh = take(tileD * 2);
+    L.Wl = take(tileD * 2);
+    L.Qh = take(tileD * 2);
+    L.Ql = take(tileD * 2);
+    L.Kh = take(tileD * 2);
+    L.Kl = take(tileD * 2);
+    L.Ah = take(tileC * 2);
+    L.Al = take(tileC * 2);
+    L.Mh = take(tileC * 2);
+    L.Ml = take(tileC * 2);
+    L.U = take(tileD * 4);
+    L.Akk = take(tileC * 4);
+    L.gam = take(tileD * 4);
+    L.eGL = take(CHd * D * 4);
     L.ws_fwd = o;
     L.ws_frag = o;
     L.dS1 = take(CHd * D * D * 4);
-    L.dDelta = take(CHd * CH * D * 4);
-    L.dR = take(CHd * CH * D * 4);
-    L.P = take(CHd * CH * D * 4);
-    L.dQg = take(CHd * CH * D * 4);
-    L.dKb = take(CHd * CH * D * 4);
-    L.dAqk = take(CHd * CH * CH * 4);
-    L.dM = take(CHd * CH * CH * 4);
+    L.dDelta = take(tileD * 4);
+    L.dR = take(tileD * 4);
+    L.P = take(tileD * 4);
+    L.dQg = take(tileD * 4);
+    L.dKb = take(tileD * 4);
+    L.dAqk = take(tileC * 4);
+    L.dM = take(tileC * 4);
     L.rsum = take(CHd * D * 4);
     L.pdA = take(CHd * 4);
     L.pddt = take(CHd * D * 4);
     L.ws_bwd_saved = o;
-    // saved set
+    // saved set: per-chunk start states S_c (fp32 [128][128]) and write vectors Delta_c
     size_t s = 0;
     L.sv_S = 0;
     s = align256(CHd * D * D * 4);
     L.sv_Delta = s;
-    s = align256(s + CHd * CH * D * 4);
+    s = align256(s + tileD * 4);
     L.saved_bytes = s;
     L.replay = take(L.saved_bytes);
     L.ws_bwd_replay = o;
@@ -109,7 +121,8 @@ struct Params {
     int* nchunks;
     int* doc_off;
     int4* chunk_tab;  // {doc, first token, length, chunk index within the doc}
-    float *gam, *W, *U, *Qg, *Kb, *Aqk, *Akk, *Minv;
+    __nv_bfloat16 *Wh, *Wl, *Qh, *Ql, *Kh, *Kl, *Ah, *Al, *Mh, *Ml;
+    float *U, *Akk, *gam, *eGL;
     float *dS1, *dDelta, *dR, *P, *dQg, *dKb, *dAqk, *dM, *rsum, *pdA, *pddt;
     // saved set (per chunk-head states and write vectors)
     float *sS, *sDelta;
@@ -184,7 +197,13 @@ __device__ __forceinline__ void zero_acc(float (&acc)[RM][RN]) {
 // Scratch for block_gemm: KT x (M + N) floats, M + N <= 256.
 constexpr int GEMM_SCRATCH = 16 * 256;
 
-// ---- kernels (defined in the .cu files) ----
+// ---- kernels (defined in the .cu files) and their dynamic shared memory ----
+size_t intra_smem_bytes();
+size_t chain_fwd_smem_bytes();
+size_t chain_bwd_smem_bytes();
+size_t bwd_gemm_smem_bytes();
+constexpr int CHAIN_THREADS = 128;  // 4 warps per state-recurrence block
+constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences
 __global__ void k_plan(Params p);
 __global__ void k_intra_fwd(Params p);
 __global__ void k_chain_fwd(Params p, int mode);

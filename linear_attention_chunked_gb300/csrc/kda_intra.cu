@@ -1,0 +1,308 @@
+// Intra-chunk stage of the forward: per (chunk, head) the gate cumsum, the fused L2 norm, the
+// 64x64 matrices Akk (strictly lower, the KK^T part of the delta rule) and Aqk (lower incl. the
+// diagonal), the UT / WY inverse Minv = (I + diag(beta) Akk)^-1, W = Minv diag(beta)(K e^gam),
+// U = Minv diag(beta) V, and the operands Qg = Q e^gam, Kb = K e^(gL - gam) of the recurrence.
+//
+// Exponent differences (secondary chunking into four 16-row sub-chunks, after Gated Linear
+// Attention): for rows r of sub-chunk i and columns s of an earlier sub-chunk j the factor
+// exp(gam_r - gam_s) is split at the last row e_j of sub-chunk j into exp(gam_r - gam_ej) and
+// exp(gam_ej - gam_s); with a decaying gate both are <= 1, so the product runs on tensor cores
+// without overflow at any decay rate.  Inside a sub-chunk (the diagonal 16x16 blocks) the factor
+// is formed elementwise in FP32.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int LB = 136;  // row stride (bf16 elements) of [rows][128] MMA operand tiles
+
+struct IntraSmem {
+    float q[CH * LDP], k[CH * LDP], gam[CH * LDP];
+    float Akk[CH * LDA], Aqk[CH * LDA], Mi[CH * LDA];
+    float beta[CH];
+    union {
+        struct {
+            __nv_bfloat16 Ks[3][2][16 * LB];  // B operands of the off-diagonal blocks (hi, lo)
+            float T[3][16 * 17];              // blockwise inverse scratch
+        } a;
+        struct {
+            __nv_bfloat16 bKg[2][CH * LB];  // beta K e^gam (hi, lo)
+            __nv_bfloat16 v[CH * LB];       // V (exact in bf16)
+        } b;
+    } u;
+};
+
+// off-diagonal sub-chunk pairs (i, j), i > j, one per warp
+__constant__ int2 kPairs[6] = {{1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
+
+__device__ __forceinline__ int tri_row(int pi) {  // row of the pi-th entry of a lower triangle
+    int r = int((sqrtf(8.f * pi + 1.f) - 1.f) * 0.5f);
+    while ((r + 1) * (r + 2) / 2 <= pi) ++r;
+    while (r * (r + 1) / 2 > pi) --r;
+    return r;
+}
+
+}  // namespace
+
+size_t intra_smem_bytes() { return sizeof(IntraSmem); }
+
+__global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
+    const int ci = blockIdx.x, h = blockIdx.y;
+    if (ci >= *p.nchunks) return;
+    const int4 info = p.chunk_tab[ci];
+    const int t0 = info.y, L = info.z;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    IntraSmem& S = *reinterpret_cast<IntraSmem*>(smraw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const size_t chd = size_t(ci) * p.H + h;
+
+    // 1. loads (zero rows past the document end), gate, beta; clear the 64x64 accumulators
+    for (int i = tid; i < CH * D; i += NTHR) {
+        const int r = i / D, c = i % D;
+        float qv = 0.f, kv = 0.f, gv = 0.f;
+        if (r < L) {
+            const size_t off = (size_t(t0 + r) * p.H + h) * D + c;
+            qv = bf2f(p.q[off]);
+            kv = bf2f(p.k[off]);
+            const float x = p.g[off];
+            gv = p.gate_raw ? -expf(p.A_log[h]) * softplus_f(x + p.dt_bias[h * D + c]) : x;
+        }
+        S.q[r * LDP + c] = qv;
+        S.k[r * LDP + c] = kv;
+        S.gam[r * LDP + c] = gv;
+    }
+    for (int i = tid; i < CH * LDA; i += NTHR) {
+        S.Akk[i] = 0.f;
+        S.Aqk[i] = 0.f;
+        S.Mi[i] = 0.f;
+    }
+    if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
+    __syncthreads();
+
+    // 2. fused L2 norm (warp per row)
+    if (p.l2n) {
+        for (int r = warp; r < CH; r += NTHR / 32) {
+            float a = 0.f, b = 0.f;
+            for (int c = lane; c < D; c += 32) {
+                const float x = S.q[r * LDP + c], y = S.k[r * LDP + c];
+                a = fmaf(x, x, a);
+                b = fmaf(y, y, b);
+            }
+            a = warp_sum(a);
+            b = warp_sum(b);
+            const float ra = 1.f / sqrtf(a + p.eps), rb = 1.f / sqrtf(b + p.eps);
+            for (int c = lane; c < D; c += 32) {
+                S.q[r * LDP + c] *= ra;
+                S.k[r * LDP + c] *= rb;
+            }
+        }
+    }
+    // 3. in-chunk inclusive cumsum (thread per channel)
+    if (tid < D) {
+        float run = 0.f;
+        for (int r = 0; r < CH; ++r) {
+            run += S.gam[r * LDP + tid];
+            S.gam[r * LDP + tid] = run;
+        }
+    }
+    __syncthreads();
+
+    // 4a. diagonal 16x16 blocks, elementwise exact exponent differences
+    for (int idx = tid; idx < 4 * 136; idx += NTHR) {
+        const int b = idx / 136, pi = idx % 136;
+        const int rl = tri_row(pi), sl = pi - rl * (rl + 1) / 2;
+        const int r = 16 * b + rl, s = 16 * b + sl;
+        float akk = 0.f, aqk = 0.f;
+        const float* gr = S.gam + r * LDP;
+        const float* gs = S.gam + s * LDP;
+        const float* kr = S.k + r * LDP;
+        const float* ks = S.k + s * LDP;
+        const float* qr = S.q + r * LDP;
+#pragma unroll 4
+        for (int c = 0; c < D; ++c) {
+            const float kse = ks[c] * __expf(gr[c] - gs[c]);
+            akk = fmaf(kr[c], kse, akk);
+            aqk = fmaf(qr[c], kse, aqk);
+        }
+        if (s < r) S.Akk[r * LDA + s] = akk;
+        S.Aqk[r * LDA + s] = aqk;
+    }
+    // 4b. B operands Ks_j[sl][c] = k[16j+sl][c] exp(gam[16j+15][c] - gam[16j+sl][c]), j = 0..2
+    for (int idx = tid; idx < 3 * 16 * D; idx += NTHR) {
+        const int j = idx / (16 * D), rem = idx % (16 * D), sl = rem / D, c = rem % D;
+        const int s = 16 * j + sl, e = 16 * j + 15;
+        const float x = S.k[s * LDP + c] * __expf(S.gam[e * LDP + c] - S.gam[s * LDP + c]);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        S.u.a.Ks[j][0][sl * LB + c] = hi;
+        S.u.a.Ks[j][1][sl * LB + c] = __float2bfloat16_rn(x - __bfloat162float(hi));
+    }
+    __syncthreads();
+    // 4c. off-diagonal blocks on tensor cores: warp w < 6 takes the pair (i, j)
+    if (warp < 6) {
+        const int i = kPairs[warp].x, j = kPairs[warp].y, e = 16 * j + 15;
+        float accQ[2][4] = {}, accK[2][4] = {};
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t qh[4], ql[4], kh[4], kl[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int row = 16 * i + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
+                const float e0 = __expf(S.gam[row * LDP + col] - S.gam[e * LDP + col]);
+                const float e1 = __expf(S.gam[row * LDP + col + 1] - S.gam[e * LDP + col + 1]);
+                split2(S.q[row * LDP + col] * e0, S.q[row * LDP + col + 1] * e1, qh[rr], ql[rr]);
+                split2(S.k[row * LDP + col] * e0, S.k[row * LDP + col + 1] * e1, kh[rr], kl[rr]);
+            }
+            uint32_t bh[4], bl[4];
+            ldsm4(bh, bn_addr(S.u.a.Ks[j][0], LB, 16 * ks, 0, lane));
+            ldsm4(bl, bn_addr(S.u.a.Ks[j][1], LB, 16 * ks, 0, lane));
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                mma_x3(accQ[nt], qh, ql, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
+                mma_x3(accK[nt], kh, kl, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const int row = 16 * i + g + 8 * (e4 >> 1), col = 16 * j + 8 * nt + 2 * t + (e4 & 1);
+                S.Aqk[row * LDA + col] = accQ[nt][e4];
+                S.Akk[row * LDA + col] = accK[nt][e4];
+            }
+    }
+    __syncthreads();
+
+    // 5. Minv = (I + diag(beta) Akk)^-1, blockwise: 16x16 diagonal inverses by substitution, then
+    //    X_ij = -D_i sum_{l=j}^{i-1} diag(beta_i) Akk_il X_lj by increasing block distance
+    if (tid < 64) {
+        const int b = tid >> 4, cl = tid & 15, c = 16 * b + cl;
+        for (int rl = 0; rl < 16; ++rl) {
+            const int r = 16 * b + rl;
+            float val = (rl == cl) ? 1.f : 0.f;
+            if (rl > cl) {
+                float acc = 0.f;
+                for (int sl = cl; sl < rl; ++sl)
+                    acc = fmaf(S.Akk[r * LDA + 16 * b + sl], S.Mi[(16 * b + sl) * LDA + c], acc);
+                val = -S.beta[r] * acc;
+            }
+            S.Mi[r * LDA + c] = val;
+        }
+    }
+    __syncthreads();
+    for (int dist = 1; dist < 4; ++dist) {
+        const int nb = 4 - dist;
+        for (int idx = tid; idx < nb * 256; idx += NTHR) {
+            const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
+            const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
+            float acc = 0.f;
+            for (int l = 16 * jb; l < 16 * ib; ++l) acc = fmaf(S.Akk[r * LDA + l], S.Mi[l * LDA + c], acc);
+            S.u.a.T[b][rl * 17 + cl] = S.beta[r] * acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < nb * 256; idx += NTHR) {
+            const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
+            const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
+            float acc = 0.f;
+            for (int sl = 0; sl < 16; ++sl)
+                acc = fmaf(S.Mi[r * LDA + 16 * ib + sl], S.u.a.T[b][sl * 17 + cl], acc);
+            S.Mi[r * LDA + c] = -acc;
+        }
+        __syncthreads();
+    }
+
+    // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
+    for (int i = tid; i < CH * D; i += NTHR) {
+        const int r = i / D, c = i % D;
+        const float x = S.beta[r] * S.k[r * LDP + c] * __expf(S.gam[r * LDP + c]);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        S.u.b.bKg[0][r * LB + c] = hi;
+        S.u.b.bKg[1][r * LB + c] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        S.u.b.v[r * LB + c] =
+            r < L ? p.v[(size_t(t0 + r) * p.H + h) * D + c] : __float2bfloat16_rn(0.f);
+    }
+    __syncthreads();
+    {
+        const int mt = warp & 3, nh = warp >> 2;
+        float accW[8][4] = {}, accU[8][4] = {};
+        for (int ks = 0; ks <= mt; ++ks) {  // Minv is lower triangular
+            uint32_t mh[4], ml[4], bh_[4], bl_[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int row = 16 * mt + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
+                const float m0 = S.Mi[row * LDA + col], m1 = S.Mi[row * LDA + col + 1];
+                split2(m0, m1, mh[rr], ml[rr]);
+                split2(m0 * S.beta[col], m1 * S.beta[col + 1], bh_[rr], bl_[rr]);
+            }
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t kh[4], kl[4], vv[4];
+                const int n0 = 64 * nh + 16 * np;
+                ldsm4t(kh, bk_addr(S.u.b.bKg[0], LB, 16 * ks, n0, lane));
+                ldsm4t(kl, bk_addr(S.u.b.bKg[1], LB, 16 * ks, n0, lane));
+                ldsm4t(vv, bk_addr(S.u.b.v, LB, 16 * ks, n0, lane));
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    mma_x3(accW[2 * np + hh], mh, ml, kh[2 * hh], kh[2 * hh + 1], kl[2 * hh],
+                           kl[2 * hh + 1]);
+                    mma_x2(accU[2 * np + hh], bh_, bl_, vv[2 * hh], vv[2 * hh + 1]);
+                }
+            }
+        }
+        __nv_bfloat16* Wh = p.Wh + chd * CH * D;
+        __nv_bfloat16* Wl = p.Wl + chd * CH * D;
+        float* U = p.U + chd * CH * D;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int row = 16 * mt + g + 8 * hf, col = 64 * nh + 8 * nt + 2 * t;
+                uint32_t hi, lo;
+                split2(accW[nt][2 * hf], accW[nt][2 * hf + 1], hi, lo);
+                *reinterpret_cast<uint32_t*>(Wh + row * D + col) = hi;
+                *reinterpret_cast<uint32_t*>(Wl + row * D + col) = lo;
+                *reinterpret_cast<float2*>(U + row * D + col) =
+                    make_float2(accU[nt][2 * hf], accU[nt][2 * hf + 1]);
+            }
+    }
+
+    // 7. elementwise operands and the small matrices
+    {
+        __nv_bfloat16* Qh = p.Qh + chd * CH * D;
+        __nv_bfloat16* Ql = p.Ql + chd * CH * D;
+        __nv_bfloat16* Kh = p.Kh + chd * CH * D;
+        __nv_bfloat16* Kl = p.Kl + chd * CH * D;
+        float* gam = p.gam + chd * CH * D;
+        for (int i = tid; i < CH * D / 2; i += NTHR) {
+            const int r = (2 * i) / D, c = (2 * i) % D;
+            const float g0 = S.gam[r * LDP + c], g1 = S.gam[r * LDP + c + 1];
+            const float gl0 = S.gam[(CH - 1) * LDP + c], gl1 = S.gam[(CH - 1) * LDP + c + 1];
+            uint32_t hi, lo;
+            split2(S.q[r * LDP + c] * __expf(g0), S.q[r * LDP + c + 1] * __expf(g1), hi, lo);
+            reinterpret_cast<uint32_t*>(Qh)[i] = hi;
+            reinterpret_cast<uint32_t*>(Ql)[i] = lo;
+            split2(S.k[r * LDP + c] * __expf(gl0 - g0), S.k[r * LDP + c + 1] * __expf(gl1 - g1), hi, lo);
+            reinterpret_cast<uint32_t*>(Kh)[i] = hi;
+            reinterpret_cast<uint32_t*>(Kl)[i] = lo;
+            reinterpret_cast<float2*>(gam)[i] = make_float2(g0, g1);
+        }
+        __nv_bfloat16* Ah = p.Ah + chd * CH * CH;
+        __nv_bfloat16* Al = p.Al + chd * CH * CH;
+        __nv_bfloat16* Mh = p.Mh + chd * CH * CH;
+        __nv_bfloat16* Ml = p.Ml + chd * CH * CH;
+        float* Akk = p.Akk + chd * CH * CH;
+        for (int i = tid; i < CH * CH / 2; i += NTHR) {
+            const int r = (2 * i) / CH, s = (2 * i) % CH;
+            uint32_t hi, lo;
+            split2(S.Aqk[r * LDA + s], S.Aqk[r * LDA + s + 1], hi, lo);
+            reinterpret_cast<uint32_t*>(Ah)[i] = hi;
+            reinterpret_cast<uint32_t*>(Al)[i] = lo;
+            split2(S.Mi[r * LDA + s], S.Mi[r * LDA + s + 1], hi, lo);
+            reinterpret_cast<uint32_t*>(Mh)[i] = hi;
+            reinterpret_cast<uint32_t*>(Ml)[i] = lo;
+            reinterpret_cast<float2*>(Akk)[i] = make_float2(S.Akk[r * LDA + s], S.Akk[r * LDA + s + 1]);
+        }
+        if (tid < D) p.eGL[chd * D + tid] = __expf(S.gam[(CH - 1) * LDP + tid]);
+    }
+}
+
+}  // namespace kda

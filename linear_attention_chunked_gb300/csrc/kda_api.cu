@@ -13,7 +13,7 @@ const size_t SMEM_INTRA_FWD = intra_smem_bytes();
 const size_t SMEM_CHAIN_FWD = chain_fwd_smem_bytes();
 const size_t SMEM_CHAIN_BWD = chain_bwd_smem_bytes();
 const size_t SMEM_BWD_GEMMS = bwd_gemm_smem_bytes();
-constexpr size_t SMEM_BWD_INTRA = (4 * CH * LDP + 3 * CH * LDA + 3 * CH + NTHR) * 4;
+const size_t SMEM_BWD_INTRA = bwd_intra_smem_bytes();
 constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
 
 std::mutex g_mu;

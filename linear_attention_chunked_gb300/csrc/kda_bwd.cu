@@ -40,15 +40,19 @@ struct BwdGemmSmem {
     __nv_bfloat16 Dl[2][CH * LB];    // Delta (hi, lo)
 };
 
-// fp32 [rows][128] global tile -> bf16 hi/lo shared tiles with row stride LB
+// dense fp32 [ROWS][128] global tile -> bf16 hi/lo shared tiles with row stride LB (all loads of
+// a thread issued first)
+template <int ROWS>
 __device__ __forceinline__ void split_tile(__nv_bfloat16* hi, __nv_bfloat16* lo, const float* g,
-                                           int rows, int tid, int nthr) {
-    for (int i = tid; i < rows * D / 4; i += nthr) {
-        const int r = (4 * i) / D, c = (4 * i) % D;
-        const float4 v = reinterpret_cast<const float4*>(g)[i];
+                                           int tid) {
+    float4 v[ROWS / 8];
+    load_tile_f32<ROWS>(v, g, tid);
+#pragma unroll
+    for (int k = 0; k < ROWS / 8; ++k) {
+        const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;
         uint32_t h0, l0, h1, l1;
-        split2(v.x, v.y, h0, l0);
-        split2(v.z, v.w, h1, l1);
+        split2(v[k].x, v[k].y, h0, l0);
+        split2(v[k].z, v[k].w, h1, l1);
         *reinterpret_cast<uint2*>(hi + r * LB + c) = make_uint2(h0, h1);
         *reinterpret_cast<uint2*>(lo + r * LB + c) = make_uint2(l0, l1);
     }
@@ -284,9 +288,9 @@ __global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
         cp16z(sm.O + r * LB + c, p.dO + (row * p.H + h) * D + c, ok);
     }
     cp_commit();
-    split_tile(sm.X[0], sm.X[1], p.dDelta + chd * CH * D, CH, tid, NTHR);
-    split_tile(sm.S[0], sm.S[1], S0, D, tid, NTHR);
-    split_tile(sm.Dl[0], sm.Dl[1], Dl, CH, tid, NTHR);
+    split_tile<CH>(sm.X[0], sm.X[1], p.dDelta + chd * CH * D, tid);
+    split_tile<D>(sm.S[0], sm.S[1], S0, tid);
+    split_tile<CH>(sm.Dl[0], sm.Dl[1], Dl, tid);
     cp_wait<0>();
     __syncthreads();
 
@@ -387,13 +391,35 @@ __global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
             }
     }
     __syncthreads();
-    // dKb = Delta dS1^T  [64 tok x 128 key]; rsum from the fp32 states
-    split_tile(sm.S[0], sm.S[1], dS1, D, tid, NTHR);
-    for (int i = w; i < D; i += NTHR / 32) {
-        float a = 0.f;
-        for (int j = lane; j < D; j += 32) a = fmaf(S0[i * D + j], dS1[i * D + j], a);
-        a = warp_sum(a);
-        if (lane == 0) p.rsum[chd * D + i] = a;
+    // dKb = Delta dS1^T  [64 tok x 128 key]; rsum = rowsum(S0 * dS1) with S0 taken from its
+    // staged hi + lo parts (16 significant bits) before the tile is replaced by dS1
+    {
+        float4 v[16];
+        load_tile_f32<D>(v, dS1, tid);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;  // warp w + 8k owns row r
+            float a = 0.f;
+            const float x[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float s0 = __bfloat162float(sm.S[0][r * LB + c + j]) +
+                                 __bfloat162float(sm.S[1][r * LB + c + j]);
+                a = fmaf(s0, x[j], a);
+            }
+            a = warp_sum(a);
+            if (lane == 0) p.rsum[chd * D + r] = a;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;
+            uint32_t h0, l0, h1, l1;
+            split2(v[k].x, v[k].y, h0, l0);
+            split2(v[k].z, v[k].w, h1, l1);
+            *reinterpret_cast<uint2*>(&sm.S[0][r * LB + c]) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(&sm.S[1][r * LB + c]) = make_uint2(l0, l1);
+        }
     }
     __syncthreads();
     {
@@ -423,51 +449,67 @@ __global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
     }
 }
 
-// Intra-chunk gradients of one (chunk, head): dq, dk, dv, dbeta, dg / da and the partial sums
-// of dA_log / ddt_bias.  Warp w owns rows w, w+8, ...; lane owns channels lane + 32 m.
+namespace {
+
+struct BwdIntraSmem {
+    float q[CH * LDP], k[CH * LDP], gam[CH * LDP];  // normalised q, k; in-chunk cumsum of g
+    float dQ[CH * LDP], dK[CH * LDP], dG[CH * LDP];  // accumulators of dq^, dk^, dgam
+    float beta[CH], rq[CH], rk[CH];
+    float red[NTHR];
+};
+
+}  // namespace
+
+size_t bwd_intra_smem_bytes() { return sizeof(BwdIntraSmem); }
+
+// Intra-chunk gradients of one (chunk, head): dq, dk, dv, dbeta, dg / da and the partials of
+// dA_log / ddt_bias.  The contractions through the exponent differences,
+//   aq_r = sum_{s<r} dAqk[r,s] k_s E[r,s]     ak_r = sum_{s<r} dAkk[r,s] k_s E[r,s]
+//   b_s  = sum_{r>s} (dAqk[r,s] q_r + dAkk[r,s] k_r) E[r,s]     (E = exp(gam_r - gam_s))
+// feed dq += aq, dk += ak + b, dgam += q aq + k ak - k b.  Across sub-chunks they run on tensor
+// cores: for destination rows of sub-chunk i the factor is split at the first row of i (both parts
+// <= 1), for destination columns of sub-chunk j at its last row.  Inside a sub-chunk they are formed
+// elementwise.  The r == s terms of Aqk (no gate dependence) enter dq and dk only.
 __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
     const int ci = blockIdx.x, h = blockIdx.y;
     if (ci >= *p.nchunks) return;
     const int4 info = p.chunk_tab[ci];
     const int t0 = info.y, L = info.z;
-    extern __shared__ float sm[];
-    float* sq = sm;
-    float* sk = sq + CH * LDP;
-    float* sg = sk + CH * LDP;
-    float* sdg = sg + CH * LDP;
-    float* sdAqk = sdg + CH * LDP;
-    float* sdAkk = sdAqk + CH * LDA;
-    float* sAkk = sdAkk + CH * LDA;
-    float* sbeta = sAkk + CH * LDA;
-    float* srq = sbeta + CH;
-    float* srk = srq + CH;
-    float* red = srk + CH;  // [NTHR]
-    const int tid = threadIdx.x, w = tid / 32, lane = tid % 32;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    BwdIntraSmem& S = *reinterpret_cast<BwdIntraSmem*>(smraw);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const size_t chd = size_t(ci) * p.H + h;
+    const float* dQg = p.dQg + chd * CH * D;
+    const float* Pp = p.P + chd * CH * D;
+    const float* dKb = p.dKb + chd * CH * D;
+    const float* dR = p.dR + chd * CH * D;
+    const float* dAqk = p.dAqk + chd * CH * CH;
+    const float* dM = p.dM + chd * CH * CH;
+    const float* Akk = p.Akk + chd * CH * CH;
 
-    for (int i = tid; i < CH * D; i += NTHR) {
-        const int r = i / D, c = i % D;
-        float qv = 0.f, kv = 0.f;
-        if (r < L) {
-            const size_t off = (size_t(t0 + r) * p.H + h) * D + c;
-            qv = bf2f(p.q[off]);
-            kv = bf2f(p.k[off]);
-        }
-        sq[r * LDP + c] = qv;
-        sk[r * LDP + c] = kv;
-    }
-    if (tid < CH) sbeta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
+    // 1. inputs
+    load_rows_bf16(S.q, LDP, p.q, t0, L, p.H, h, tid);
+    load_rows_bf16(S.k, LDP, p.k, t0, L, p.H, h, tid);
     {
-        const float* gam = p.gam + chd * CH * D;
-        for (int i = tid; i < CH * D; i += NTHR) sg[(i / D) * LDP + i % D] = gam[i];
+        float4 v[8];
+        load_tile_f32<CH>(v, p.gam + chd * CH * D, tid);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;
+            S.gam[r * LDP + c] = v[k].x;
+            S.gam[r * LDP + c + 1] = v[k].y;
+            S.gam[r * LDP + c + 2] = v[k].z;
+            S.gam[r * LDP + c + 3] = v[k].w;
+        }
     }
+    if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
     __syncthreads();
     for (int r = w; r < CH; r += NTHR / 32) {
         float ra = 1.f, rb = 1.f;
         if (p.l2n) {
             float a = 0.f, b = 0.f;
             for (int c = lane; c < D; c += 32) {
-                float x = sq[r * LDP + c], y = sk[r * LDP + c];
+                const float x = S.q[r * LDP + c], y = S.k[r * LDP + c];
                 a = fmaf(x, x, a);
                 b = fmaf(y, y, b);
             }
@@ -476,149 +518,294 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
             ra = 1.f / sqrtf(a + p.eps);
             rb = 1.f / sqrtf(b + p.eps);
             for (int c = lane; c < D; c += 32) {
-                sq[r * LDP + c] *= ra;
-                sk[r * LDP + c] *= rb;
+                S.q[r * LDP + c] *= ra;
+                S.k[r * LDP + c] *= rb;
             }
         }
         if (lane == 0) {
-            srq[r] = ra;
-            srk[r] = rb;
-        }
-    }
-    {
-        const float* dAqk = p.dAqk + chd * CH * CH;
-        const float* dM = p.dM + chd * CH * CH;
-        const float* Akk = p.Akk + chd * CH * CH;
-        for (int i = tid; i < CH * CH; i += NTHR) {
-            const int r = i / CH, s = i % CH;
-            sdAqk[r * LDA + s] = dAqk[i];
-            sdAkk[r * LDA + s] = sbeta[r] * dM[i];
-            sAkk[r * LDA + s] = Akk[i];
+            S.rq[r] = ra;
+            S.rk[r] = rb;
         }
     }
     __syncthreads();
 
-    const float* dQgp = p.dQg + chd * CH * D;
-    const float* Pp = p.P + chd * CH * D;
-    const float* dKbp = p.dKb + chd * CH * D;
-    const float* dRp = p.dR + chd * CH * D;
-    const float* dMp = p.dM + chd * CH * CH;
-    for (int r = w; r < CH; r += NTHR / 32) {
-        const float br = sbeta[r];
-        float dqh[4], dkh[4], dbp = 0.f;
+    // 2. elementwise terms through Qg, Kg, Kb and the diagonal of Aqk
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        float4 vq[4], vp[4], vb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + NTHR * (k + 4 * half);
+            vq[k] = reinterpret_cast<const float4*>(dQg)[i];
+            vp[k] = reinterpret_cast<const float4*>(Pp)[i];
+            vb[k] = reinterpret_cast<const float4*>(dKb)[i];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + NTHR * (k + 4 * half), r = i >> 5, c0 = (i & 31) * 4;
+            const float dgn = dAqk[r * CH + r], br = S.beta[r];
+            const float aq[4] = {vq[k].x, vq[k].y, vq[k].z, vq[k].w};
+            const float ap[4] = {vp[k].x, vp[k].y, vp[k].z, vp[k].w};
+            const float ab[4] = {vb[k].x, vb[k].y, vb[k].z, vb[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = c0 + j;
+                const float gv = S.gam[r * LDP + c], gl = S.gam[(CH - 1) * LDP + c];
+                const float er = __expf(gv), eb = __expf(gl - gv);
+                const float qv = S.q[r * LDP + c], kv = S.k[r * LDP + c];
+                const float dqg = aq[j], dkg = -br * ap[j], dkb = ab[j];
+                S.dQ[r * LDP + c] = fmaf(dqg, er, dgn * kv);
+                S.dK[r * LDP + c] = fmaf(dkg, er, fmaf(dkb, eb, dgn * qv));
+                S.dG[r * LDP + c] = (dqg * qv + dkg * kv) * er - dkb * kv * eb;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 3. contractions across sub-chunks on tensor cores; warp w owns channels 16w..16w+15
+    {
+        auto a_frag = [&](const float* src, bool tr, bool kk, int m0, int k0, uint32_t (&hi)[4],
+                          uint32_t (&lo)[4]) {
+            // element (m, kx) of the A operand: src[m][kx] (tr = false) or src[kx][m] (tr = true);
+            // kk: the source is dM and the operand is dAkk = beta_row * dM
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int m = m0 + g + 8 * (rr & 1), kx = k0 + 2 * t + 8 * (rr >> 1);
+                float x0, x1;
+                if (!tr) {
+                    x0 = src[m * CH + kx];
+                    x1 = src[m * CH + kx + 1];
+                    if (kk) { x0 *= S.beta[m]; x1 *= S.beta[m]; }
+                } else {
+                    x0 = src[kx * CH + m];
+                    x1 = src[(kx + 1) * CH + m];
+                    if (kk) { x0 *= S.beta[kx]; x1 *= S.beta[kx + 1]; }
+                }
+                split2(x0, x1, hi[rr], lo[rr]);
+            }
+        };
+        // "as row": destination sub-chunk i = 1..3, reference row 16 i
+        for (int i = 1; i < 4; ++i) {
+            const int ref = 16 * i;
+            float aq[2][4] = {}, ak[2][4] = {};
+            for (int ks = 0; ks < i; ++ks) {
+                uint32_t qh[4], ql[4], kh[4], kl[4];
+                a_frag(dAqk, false, false, 16 * i, 16 * ks, qh, ql);
+                a_frag(dM, false, true, 16 * i, 16 * ks, kh, kl);
+#pragma unroll
+                for (int nn = 0; nn < 2; ++nn) {
+                    const int c = 16 * w + 8 * nn + g;
+                    uint32_t bh[2], bl[2];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int s0 = 16 * ks + 2 * t + 8 * hf;
+                        const float gr = S.gam[ref * LDP + c];
+                        const float x0 = S.k[s0 * LDP + c] * __expf(gr - S.gam[s0 * LDP + c]);
+                        const float x1 = S.k[(s0 + 1) * LDP + c] * __expf(gr - S.gam[(s0 + 1) * LDP + c]);
+                        split2(x0, x1, bh[hf], bl[hf]);
+                    }
+                    mma_x3(aq[nn], qh, ql, bh[0], bh[1], bl[0], bl[1]);
+                    mma_x3(ak[nn], kh, kl, bh[0], bh[1], bl[0], bl[1]);
+                }
+            }
+#pragma unroll
+            for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 16 * i + g + 8 * (e >> 1), c = 16 * w + 8 * nn + 2 * t + (e & 1);
+                    const float sc = __expf(S.gam[r * LDP + c] - S.gam[ref * LDP + c]);
+                    const float vq = aq[nn][e] * sc, vk = ak[nn][e] * sc;
+                    S.dQ[r * LDP + c] += vq;
+                    S.dK[r * LDP + c] += vk;
+                    S.dG[r * LDP + c] += S.q[r * LDP + c] * vq + S.k[r * LDP + c] * vk;
+                }
+        }
+        // "as column": destination sub-chunk j = 0..2, reference row 16 j + 15
+        for (int j = 0; j < 3; ++j) {
+            const int ref = 16 * j + 15;
+            float bacc[2][4] = {};
+            for (int ks = j + 1; ks < 4; ++ks) {
+                uint32_t qh[4], ql[4], kh[4], kl[4];
+                a_frag(dAqk, true, false, 16 * j, 16 * ks, qh, ql);
+                a_frag(dM, true, true, 16 * j, 16 * ks, kh, kl);
+#pragma unroll
+                for (int nn = 0; nn < 2; ++nn) {
+                    const int c = 16 * w + 8 * nn + g;
+                    uint32_t qbh[2], qbl[2], kbh[2], kbl[2];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int r0 = 16 * ks + 2 * t + 8 * hf;
+                        const float gr = S.gam[ref * LDP + c];
+                        const float e0 = __expf(S.gam[r0 * LDP + c] - gr);
+                        const float e1 = __expf(S.gam[(r0 + 1) * LDP + c] - gr);
+                        split2(S.q[r0 * LDP + c] * e0, S.q[(r0 + 1) * LDP + c] * e1, qbh[hf], qbl[hf]);
+                        split2(S.k[r0 * LDP + c] * e0, S.k[(r0 + 1) * LDP + c] * e1, kbh[hf], kbl[hf]);
+                    }
+                    mma_x3(bacc[nn], qh, ql, qbh[0], qbh[1], qbl[0], qbl[1]);
+                    mma_x3(bacc[nn], kh, kl, kbh[0], kbh[1], kbl[0], kbl[1]);
+                }
+            }
+#pragma unroll
+            for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = 16 * j + g + 8 * (e >> 1), c = 16 * w + 8 * nn + 2 * t + (e & 1);
+                    const float vb = bacc[nn][e] * __expf(S.gam[ref * LDP + c] - S.gam[s * LDP + c]);
+                    S.dK[s * LDP + c] += vb;
+                    S.dG[s * LDP + c] -= S.k[s * LDP + c] * vb;
+                }
+        }
+    }
+    __syncthreads();
+
+    // 4. inside each sub-chunk, elementwise: thread per (sub-chunk, channel)
+    for (int task = tid; task < 4 * D; task += NTHR) {
+        const int b = task / D, c = task % D, base = 16 * b;
+        float aq[16], ak[16], bb[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) aq[x] = ak[x] = bb[x] = 0.f;
+#pragma unroll
+        for (int rl = 1; rl < 16; ++rl) {
+            const int r = base + rl;
+            const float gr = S.gam[r * LDP + c], qr = S.q[r * LDP + c], kr = S.k[r * LDP + c];
+            const float br = S.beta[r];
+#pragma unroll
+            for (int sl = 0; sl < rl; ++sl) {
+                const int s = base + sl;
+                const float E = __expf(gr - S.gam[s * LDP + c]);
+                const float da = dAqk[r * CH + s], dk = br * dM[r * CH + s];
+                const float ks = S.k[s * LDP + c] * E;
+                aq[rl] = fmaf(da, ks, aq[rl]);
+                ak[rl] = fmaf(dk, ks, ak[rl]);
+                bb[sl] = fmaf(fmaf(da, qr, dk * kr), E, bb[sl]);
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            const int r = base + x;
+            const float qv = S.q[r * LDP + c], kv = S.k[r * LDP + c];
+            S.dQ[r * LDP + c] += aq[x];
+            S.dK[r * LDP + c] += ak[x] + bb[x];
+            S.dG[r * LDP + c] += qv * aq[x] + kv * (ak[x] - bb[x]);
+        }
+    }
+    __syncthreads();
+
+    // 5. chunk-end gate term dgL = e^gL rowsum(S0 * dS1) + sum_r dKb * Kb, then the reverse
+    //    cumsum over the chunk; two threads per channel (rows 0-31 / 32-63), fixed order
+    {
+        const int c = tid & (D - 1), half = tid >> 7, r0 = 32 * half;
+        const float gl = S.gam[(CH - 1) * LDP + c];
+        float part = 0.f;
+#pragma unroll 8
+        for (int r = r0; r < r0 + 32; ++r)
+            part = fmaf(dKb[r * D + c], S.k[r * LDP + c] * __expf(gl - S.gam[r * LDP + c]), part);
+        float suf = 0.f;  // suffix sums inside the half
+        for (int r = r0 + 31; r >= r0; --r) {
+            suf += S.dG[r * LDP + c];
+            S.dG[r * LDP + c] = suf;
+        }
+        S.red[tid] = part;
+        __syncthreads();
+        const float dgl = __expf(gl) * p.rsum[chd * D + c] + (S.red[c] + S.red[c + D]);
+        // rows of the lower half also receive the whole upper half; every row receives dgL
+        const float carry = half == 0 ? S.dG[32 * LDP + c] : 0.f;
+        __syncthreads();
+        for (int r = r0; r < r0 + 32; ++r) S.dG[r * LDP + c] += carry + dgl;
+    }
+    __syncthreads();
+
+    // 6. per row: L2-norm backward, dq, dk, dv, dbeta (warp per row)
+    for (int r = w; r < L; r += NTHR / 32) {
+        const size_t base = (size_t(t0 + r) * p.H + h) * D;
+        const float br = S.beta[r];
+        float dq[4], dk[4], pq = 0.f, pk = 0.f, db = 0.f;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int c = lane + 32 * m;
-            const float g = sg[r * LDP + c], gl = sg[(CH - 1) * LDP + c];
-            const float er = expf(g), eb = expf(gl - g);
-            const float qv = sq[r * LDP + c], kv = sk[r * LDP + c];
-            const float dQg = dQgp[r * D + c], Pv = Pp[r * D + c], dKb = dKbp[r * D + c];
-            const float dKg = -br * Pv;
-            float dq = dQg * er;
-            float dk = fmaf(dKg, er, dKb * eb);
-            float dgam = dQg * qv * er + dKg * kv * er - dKb * kv * eb;
-            float aq = 0.f, ak = 0.f, bq = 0.f, bk = 0.f;
-            for (int s = 0; s < r; ++s) {
-                const float E = expf(g - sg[s * LDP + c]);
-                const float ks = sk[s * LDP + c] * E;
-                aq = fmaf(sdAqk[r * LDA + s], ks, aq);
-                ak = fmaf(sdAkk[r * LDA + s], ks, ak);
-            }
-            for (int r2 = r + 1; r2 < CH; ++r2) {
-                const float E = expf(sg[r2 * LDP + c] - g);
-                bq = fmaf(sdAqk[r2 * LDA + r], sq[r2 * LDP + c] * E, bq);
-                bk = fmaf(sdAkk[r2 * LDA + r], sk[r2 * LDP + c] * E, bk);
-            }
-            const float diag = sdAqk[r * LDA + r];
-            dq += aq + diag * kv;
-            dk += ak + bq + bk + diag * qv;
-            dgam += qv * aq + kv * ak - kv * (bq + bk);
-            sdg[r * LDP + c] = dgam;
-            dqh[m] = dq;
-            dkh[m] = dk;
-            // dbeta pieces: dR.v - Kg.P
-            const float vv = r < L ? bf2f(p.v[(size_t(t0 + r) * p.H + h) * D + c]) : 0.f;
-            const float dRv = dRp[r * D + c];
-            dbp += dRv * vv - kv * er * Pv;
-            if (r < L) store_out(p.dv, (size_t(t0 + r) * p.H + h) * D + c, br * dRv, p.out_fp32);
+            dq[m] = S.dQ[r * LDP + c];
+            dk[m] = S.dK[r * LDP + c];
+            pq = fmaf(S.q[r * LDP + c], dq[m], pq);
+            pk = fmaf(S.k[r * LDP + c], dk[m], pk);
+            const float dRv = dR[r * D + c];
+            const float kg = S.k[r * LDP + c] * __expf(S.gam[r * LDP + c]);
+            db = fmaf(dRv, bf2f(p.v[base + c]), db);
+            db = fmaf(-kg, Pp[r * D + c], db);
+            store_out(p.dv, base + c, br * dRv, p.out_fp32);
         }
-        for (int s = lane; s < r; s += 32) dbp += sAkk[r * LDA + s] * dMp[r * CH + s];
-        dbp = warp_sum(dbp);
-        float pq = 0.f, pk = 0.f;
+        for (int s = lane; s < r; s += 32) db = fmaf(Akk[r * CH + s], dM[r * CH + s], db);
+        db = warp_sum(db);
         if (p.l2n) {
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                pq += sq[r * LDP + lane + 32 * m] * dqh[m];
-                pk += sk[r * LDP + lane + 32 * m] * dkh[m];
-            }
             pq = warp_sum(pq);
             pk = warp_sum(pk);
         }
-        if (r < L) {
-            const size_t base = (size_t(t0 + r) * p.H + h) * D;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int c = lane + 32 * m;
-                float dq = dqh[m], dk = dkh[m];
-                if (p.l2n) {
-                    dq = (dq - sq[r * LDP + c] * pq) * srq[r];
-                    dk = (dk - sk[r * LDP + c] * pk) * srk[r];
-                }
-                store_out(p.dq, base + c, dq, p.out_fp32);
-                store_out(p.dk, base + c, dk, p.out_fp32);
+        for (int m = 0; m < 4; ++m) {
+            const int c = lane + 32 * m;
+            float vq = dq[m], vk = dk[m];
+            if (p.l2n) {
+                vq = (vq - S.q[r * LDP + c] * pq) * S.rq[r];
+                vk = (vk - S.k[r * LDP + c] * pk) * S.rk[r];
             }
-            if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, dbp, p.out_fp32);
+            store_out(p.dq, base + c, vq, p.out_fp32);
+            store_out(p.dk, base + c, vk, p.out_fp32);
         }
+        if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, db, p.out_fp32);
     }
-    __syncthreads();
-    // chunk-end gate term, then reverse cumsum over the chunk (thread per channel)
-    if (tid < D) {
-        const int c = tid;
-        const float gl = sg[(CH - 1) * LDP + c];
-        float dgl = expf(gl) * p.rsum[chd * D + c];
-        for (int r = 0; r < CH; ++r)
-            dgl = fmaf(dKbp[r * D + c], sk[r * LDP + c] * expf(gl - sg[r * LDP + c]), dgl);
-        sdg[(CH - 1) * LDP + c] += dgl;
-        float run = 0.f;
-        for (int r = CH - 1; r >= 0; --r) {
-            run += sdg[r * LDP + c];
-            sdg[r * LDP + c] = run;
-        }
-    }
-    __syncthreads();
+
+    __syncthreads();  // step 7 reuses dQ / dK as scratch
+    // 7. gate gradient: g form writes dg; raw form writes da and the parameter partials
     if (!p.gate_raw) {
-        for (int i = tid; i < CH * D; i += NTHR) {
+        for (int i = tid; i < L * D; i += NTHR) {
             const int r = i / D, c = i % D;
-            if (r < L) p.dg[(size_t(t0 + r) * p.H + h) * D + c] = sdg[r * LDP + c];
+            p.dg[(size_t(t0 + r) * p.H + h) * D + c] = S.dG[r * LDP + c];
         }
         return;
     }
-    // raw gate: da = dg * (-exp(A_log)) * sigmoid(a + dt_bias); partials of dA_log and ddt_bias
     const float eA = expf(p.A_log[h]);
+    {
+        // da elementwise (all threads, batched loads); dg * g -> dQ, da -> dK for the reductions
+        float4 av[8];
+        load_rows_f32(av, p.g, t0, L, p.H, h, tid);
+        const int c4 = (tid & 31) * 4;
+        const float4 db = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
+        const float b4[4] = {db.x, db.y, db.z, db.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int r = (tid + NTHR * k) >> 5;
+            const float a4[4] = {av[k].x, av[k].y, av[k].z, av[k].w};
+            float da4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float x = a4[j] + b4[j], dg = S.dG[r * LDP + c4 + j];
+                const bool ok = r < L;
+                da4[j] = ok ? dg * (-eA) * sigmoid_f(x) : 0.f;
+                S.dQ[r * LDP + c4 + j] = ok ? dg * (-eA * softplus_f(x)) : 0.f;
+                S.dK[r * LDP + c4 + j] = da4[j];
+            }
+            if (r < L)
+                *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
+                    make_float4(da4[0], da4[1], da4[2], da4[3]);
+        }
+    }
+    __syncthreads();
     float pa = 0.f;
     if (tid < D) {
         const int c = tid;
-        const float db = p.dt_bias[h * D + c];
         float pd = 0.f;
-        for (int r = 0; r < L; ++r) {
-            const size_t off = (size_t(t0 + r) * p.H + h) * D + c;
-            const float x = p.g[off] + db;
-            const float dg = sdg[r * LDP + c];
-            const float gv = -eA * softplus_f(x);
-            const float da = dg * (-eA) * sigmoid_f(x);
-            p.dg[off] = da;
-            pd += da;
-            pa = fmaf(dg, gv, pa);
+        for (int r = 0; r < CH; ++r) {
+            pd += S.dK[r * LDP + c];
+            pa += S.dQ[r * LDP + c];
         }
         p.pddt[chd * D + c] = pd;
     }
-    red[tid] = pa;
+    S.red[tid] = pa;
     __syncthreads();
-    for (int s = NTHR / 2; s > 0; s >>= 1) {
-        if (tid < s) red[tid] += red[tid + s];
+    for (int s2 = NTHR / 2; s2 > 0; s2 >>= 1) {
+        if (tid < s2) S.red[tid] += S.red[tid + s2];
         __syncthreads();
     }
-    if (tid == 0) p.pdA[chd] = red[0];
+    if (tid == 0) p.pdA[chd] = S.red[0];
 }
 
 // Fixed-order sums of the per-chunk partials: dA_log[h], ddt_bias[h, :].

@@ -186,6 +186,51 @@ __device__ __forceinline__ void block_gemm(float (&acc)[RM][RN], LA la, LB lb, i
     __syncthreads();
 }
 
+// ---- batched tile loads (every global load of a thread is issued before its first use) ----
+
+// [64][128] rows t0.. of head h of a [T, H, 128] bf16 tensor -> fp32 shared [64][ld]; rows >= L
+// read as zero.  256 threads.
+__device__ __forceinline__ void load_rows_bf16(float* s, int ld, const __nv_bfloat16* g, int t0,
+                                               int L, int H, int h, int tid) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+        v[k] = r < L ? *reinterpret_cast<const uint4*>(g + (size_t(t0 + r) * H + h) * D + c8)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            s[r * ld + c8 + 2 * j] = f.x;
+            s[r * ld + c8 + 2 * j + 1] = f.y;
+        }
+    }
+}
+
+// [64][128] rows t0.. of head h of a [T, H, 128] fp32 tensor -> registers (8 float4 per thread,
+// element index i = tid + 256 k -> row i / 32, column 4 (i % 32)); rows >= L read as zero.
+__device__ __forceinline__ void load_rows_f32(float4 (&v)[8], const float* g, int t0, int L, int H,
+                                              int h, int tid) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = tid + NTHR * k, r = i >> 5, c4 = (i & 31) * 4;
+        v[k] = r < L ? *reinterpret_cast<const float4*>(g + (size_t(t0 + r) * H + h) * D + c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Dense [ROWS][128] fp32 tile -> registers, same element mapping (ROWS / 8 float4 per thread).
+template <int ROWS>
+__device__ __forceinline__ void load_tile_f32(float4 (&v)[ROWS / 8], const float* g, int tid) {
+#pragma unroll
+    for (int k = 0; k < ROWS / 8; ++k) v[k] = reinterpret_cast<const float4*>(g)[tid + NTHR * k];
+}
+
 template <int RM, int RN>
 __device__ __forceinline__ void zero_acc(float (&acc)[RM][RN]) {
 #pragma unroll
@@ -202,6 +247,7 @@ size_t intra_smem_bytes();
 size_t chain_fwd_smem_bytes();
 size_t chain_bwd_smem_bytes();
 size_t bwd_gemm_smem_bytes();
+size_t bwd_intra_smem_bytes();
 constexpr int CHAIN_THREADS = 128;  // 4 warps per state-recurrence block
 constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences
 __global__ void k_plan(Params p);

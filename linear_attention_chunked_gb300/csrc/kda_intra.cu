@@ -58,19 +58,30 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
     const size_t chd = size_t(ci) * p.H + h;
 
     // 1. loads (zero rows past the document end), gate, beta; clear the 64x64 accumulators
-    for (int i = tid; i < CH * D; i += NTHR) {
-        const int r = i / D, c = i % D;
-        float qv = 0.f, kv = 0.f, gv = 0.f;
-        if (r < L) {
-            const size_t off = (size_t(t0 + r) * p.H + h) * D + c;
-            qv = bf2f(p.q[off]);
-            kv = bf2f(p.k[off]);
-            const float x = p.g[off];
-            gv = p.gate_raw ? -expf(p.A_log[h]) * softplus_f(x + p.dt_bias[h * D + c]) : x;
+    load_rows_bf16(S.q, LDP, p.q, t0, L, p.H, h, tid);
+    load_rows_bf16(S.k, LDP, p.k, t0, L, p.H, h, tid);
+    {
+        float4 gv[8];
+        load_rows_f32(gv, p.g, t0, L, p.H, h, tid);
+        const int c4 = (tid & 31) * 4;  // the same 4 channels for every k
+        float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
+        float eA = 0.f;
+        if (p.gate_raw) {
+            db = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
+            eA = expf(p.A_log[h]);
         }
-        S.q[r * LDP + c] = qv;
-        S.k[r * LDP + c] = kv;
-        S.gam[r * LDP + c] = gv;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int r = (tid + NTHR * k) >> 5;
+            float x[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+            const float b4[4] = {db.x, db.y, db.z, db.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float val = x[j];
+                if (p.gate_raw) val = r < L ? -eA * softplus_f(val + b4[j]) : 0.f;
+                S.gam[r * LDP + c4 + j] = val;
+            }
+        }
     }
     for (int i = tid; i < CH * LDA; i += NTHR) {
         S.Akk[i] = 0.f;
@@ -176,49 +187,71 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
     //    X_ij = -D_i sum_{l=j}^{i-1} diag(beta_i) Akk_il X_lj by increasing block distance
     if (tid < 64) {
         const int b = tid >> 4, cl = tid & 15, c = 16 * b + cl;
+        float x[16];
+#pragma unroll
         for (int rl = 0; rl < 16; ++rl) {
             const int r = 16 * b + rl;
-            float val = (rl == cl) ? 1.f : 0.f;
-            if (rl > cl) {
-                float acc = 0.f;
-                for (int sl = cl; sl < rl; ++sl)
-                    acc = fmaf(S.Akk[r * LDA + 16 * b + sl], S.Mi[(16 * b + sl) * LDA + c], acc);
-                val = -S.beta[r] * acc;
-            }
-            S.Mi[r * LDA + c] = val;
+            float acc = 0.f;
+#pragma unroll
+            for (int sl = 0; sl < rl; ++sl) acc = fmaf(S.Akk[r * LDA + 16 * b + sl], x[sl], acc);
+            x[rl] = (rl == cl) ? 1.f : -S.beta[r] * acc;
         }
+#pragma unroll
+        for (int rl = 0; rl < 16; ++rl) S.Mi[(16 * b + rl) * LDA + c] = x[rl];
     }
     __syncthreads();
+#pragma unroll
     for (int dist = 1; dist < 4; ++dist) {
         const int nb = 4 - dist;
         for (int idx = tid; idx < nb * 256; idx += NTHR) {
             const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
             const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
-            float acc = 0.f;
-            for (int l = 16 * jb; l < 16 * ib; ++l) acc = fmaf(S.Akk[r * LDA + l], S.Mi[l * LDA + c], acc);
-            S.u.a.T[b][rl * 17 + cl] = S.beta[r] * acc;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int l = 0; l < 16 * dist; l += 2) {
+                a0 = fmaf(S.Akk[r * LDA + 16 * jb + l], S.Mi[(16 * jb + l) * LDA + c], a0);
+                a1 = fmaf(S.Akk[r * LDA + 16 * jb + l + 1], S.Mi[(16 * jb + l + 1) * LDA + c], a1);
+            }
+            S.u.a.T[b][rl * 17 + cl] = S.beta[r] * (a0 + a1);
         }
         __syncthreads();
         for (int idx = tid; idx < nb * 256; idx += NTHR) {
             const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
             const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
-            float acc = 0.f;
-            for (int sl = 0; sl < 16; ++sl)
-                acc = fmaf(S.Mi[r * LDA + 16 * ib + sl], S.u.a.T[b][sl * 17 + cl], acc);
-            S.Mi[r * LDA + c] = -acc;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int sl = 0; sl < 16; sl += 2) {
+                a0 = fmaf(S.Mi[r * LDA + 16 * ib + sl], S.u.a.T[b][sl * 17 + cl], a0);
+                a1 = fmaf(S.Mi[r * LDA + 16 * ib + sl + 1], S.u.a.T[b][(sl + 1) * 17 + cl], a1);
+            }
+            S.Mi[r * LDA + c] = -(a0 + a1);
         }
         __syncthreads();
     }
 
     // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
-    for (int i = tid; i < CH * D; i += NTHR) {
-        const int r = i / D, c = i % D;
-        const float x = S.beta[r] * S.k[r * LDP + c] * __expf(S.gam[r * LDP + c]);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-        S.u.b.bKg[0][r * LB + c] = hi;
-        S.u.b.bKg[1][r * LB + c] = __float2bfloat16_rn(x - __bfloat162float(hi));
-        S.u.b.v[r * LB + c] =
-            r < L ? p.v[(size_t(t0 + r) * p.H + h) * D + c] : __float2bfloat16_rn(0.f);
+    {
+        uint4 vv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+            vv[k] = r < L ? *reinterpret_cast<const uint4*>(p.v + (size_t(t0 + r) * p.H + h) * D + c8)
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int i = tid; i < CH * D / 2; i += NTHR) {
+            const int r = (2 * i) / D, c = (2 * i) % D;
+            const float x0 = S.beta[r] * S.k[r * LDP + c] * __expf(S.gam[r * LDP + c]);
+            const float x1 = S.beta[r] * S.k[r * LDP + c + 1] * __expf(S.gam[r * LDP + c + 1]);
+            uint32_t hi, lo;
+            split2(x0, x1, hi, lo);
+            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
+            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+            *reinterpret_cast<uint4*>(&S.u.b.v[r * LB + c8]) = vv[k];
+        }
     }
     __syncthreads();
     {

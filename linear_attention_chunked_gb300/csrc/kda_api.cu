@@ -89,23 +89,30 @@ Params make_params(const kda_problem* pr, const Layout& L, void* ws) {
     p.nchunks = reinterpret_cast<int*>(w + L.nchunks);
     p.doc_off = reinterpret_cast<int*>(w + L.doc_off);
     p.chunk_tab = reinterpret_cast<int4*>(w + L.chunk_tab);
-    auto f = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
-    auto b = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(w + off); };
-    p.Wh = b(L.Wh);
-    p.Wl = b(L.Wl);
-    p.Qh = b(L.Qh);
-    p.Ql = b(L.Ql);
-    p.Kh = b(L.Kh);
-    p.Kl = b(L.Kl);
-    p.Ah = b(L.Ah);
-    p.Al = b(L.Al);
-    p.Mh = b(L.Mh);
-    p.Ml = b(L.Ml);
-    p.U = f(L.U);
-    p.Akk = f(L.Akk);
-    p.gam = f(L.gam);
-    p.eGL = f(L.eGL);
     return p;
+}
+
+// Points the intra-chunk products and (optionally) the states at a saved-set image at `base`.
+void set_saved(Params& p, const Layout& L, char* base, bool states) {
+    const IntraRecord R = make_intra_record(size_t(L.maxC) * L.H);
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
+    auto b = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(base + off); };
+    p.Wh = b(R.Wh);
+    p.Wl = b(R.Wl);
+    p.Qh = b(R.Qh);
+    p.Ql = b(R.Ql);
+    p.Kh = b(R.Kh);
+    p.Kl = b(R.Kl);
+    p.Ah = b(R.Ah);
+    p.Al = b(R.Al);
+    p.Mh = b(R.Mh);
+    p.Ml = b(R.Ml);
+    p.U = f(R.U);
+    p.Akk = f(R.Akk);
+    p.gam = f(R.gam);
+    p.eGL = f(R.eGL);
+    p.sS = states ? f(L.sv_S) : nullptr;
+    p.sDelta = states ? f(L.sv_Delta) : nullptr;
 }
 
 void set_bwd_regions(Params& p, const Layout& L, void* ws) {
@@ -147,7 +154,7 @@ kda_status run_prologue(const Params& p, cudaStream_t st) {
     }
     if (p.maxC > 0) {
         ProfScope ps(KK_INTRA_FWD, st);
-        k_intra_fwd<<<dim3(unsigned(p.maxC), p.H), NTHR, SMEM_INTRA_FWD, st>>>(p);
+        k_intra_fwd<<<dim3(unsigned(p.maxC), p.H), INTRA_THREADS, SMEM_INTRA_FWD, st>>>(p);
     }
     return launched();
 }
@@ -203,10 +210,8 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     p.h0 = h0;
     p.o = o;
     p.ht = ht;
-    if (saved) {
-        p.sS = reinterpret_cast<float*>(static_cast<char*>(saved) + L.sv_S);
-        p.sDelta = reinterpret_cast<float*>(static_cast<char*>(saved) + L.sv_Delta);
-    }
+    if (saved) set_saved(p, L, static_cast<char*>(saved), true);
+    else set_saved(p, L, static_cast<char*>(ws) + L.intra_ws, false);
     if (kda_status s = run_prologue(p, st)) return s;
     {
         ProfScope ps(KK_CHAIN_FWD, st);
@@ -247,11 +252,14 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
     p.dh0 = dh0;
     char* sv = saved ? static_cast<char*>(const_cast<void*>(saved))
                      : static_cast<char*>(ws) + L.replay;
-    p.sS = reinterpret_cast<float*>(sv + L.sv_S);
-    p.sDelta = reinterpret_cast<float*>(sv + L.sv_Delta);
-    if (kda_status s = run_prologue(p, st)) return s;
-    if (!saved) {
-        // checkpoint replay: recompute the per-chunk states and write vectors
+    set_saved(p, L, sv, true);
+    if (saved) {
+        // the saved set already holds the intra products and states: only the chunk plan
+        ProfScope ps(KK_PLAN, st);
+        k_plan<<<1, NTHR, 0, st>>>(p);
+    } else {
+        // checkpoint replay: recompute the intra products, the states and the write vectors
+        if (kda_status s = run_prologue(p, st)) return s;
         Params r = p;
         r.o = nullptr;
         r.ht = nullptr;
@@ -269,7 +277,7 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
             k_bwd_gemms<<<grid, NTHR, SMEM_BWD_GEMMS, st>>>(p);
         }
         ProfScope ps(KK_BWD_INTRA, st);
-        k_bwd_intra<<<grid, NTHR, SMEM_BWD_INTRA, st>>>(p);
+        k_bwd_intra<<<grid, BI_THREADS, SMEM_BWD_INTRA, st>>>(p);
     }
     if (p.gate_raw) {
         ProfScope ps(KK_PARAM_REDUCE, st);
@@ -298,6 +306,7 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     p.dO = static_cast<const __nv_bfloat16*>(dO);
     p.fragM = M;
     p.fragB = B_or_C;
+    set_saved(p, L, static_cast<char*>(ws) + L.intra_ws, false);
     if (kda_status s = run_prologue(p, st)) return s;
     if (mode == KDA_FRAG_FWD) {
         ProfScope ps(KK_CHAIN_FWD, st);

@@ -451,11 +451,15 @@ __global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
 
 namespace {
 
+constexpr int LAS = 68;  // row stride (fp32) of the staged 64x64 gradient matrices
+
 struct BwdIntraSmem {
-    float q[CH * LDP], k[CH * LDP], gam[CH * LDP];  // normalised q, k; in-chunk cumsum of g
+    float gam[CH * LDP];                             // in-chunk cumsum of g
     float dQ[CH * LDP], dK[CH * LDP], dG[CH * LDP];  // accumulators of dq^, dk^, dgam
+    __nv_bfloat16 qb[CH * LB], kb[CH * LB];          // q, k as given (bf16); q^ = q * rq
+    float dA[CH * LAS], dAk[CH * LAS];               // dAqk and dAkk = beta_r dM
     float beta[CH], rq[CH], rk[CH];
-    float red[NTHR];
+    float red[2 * BI_THREADS];
 };
 
 }  // namespace
@@ -469,8 +473,9 @@ size_t bwd_intra_smem_bytes() { return sizeof(BwdIntraSmem); }
 // feed dq += aq, dk += ak + b, dgam += q aq + k ak - k b.  Across sub-chunks they run on tensor
 // cores: for destination rows of sub-chunk i the factor is split at the first row of i (both parts
 // <= 1), for destination columns of sub-chunk j at its last row.  Inside a sub-chunk they are formed
-// elementwise.  The r == s terms of Aqk (no gate dependence) enter dq and dk only.
-__global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
+// elementwise.  The r == s terms of Aqk (no gate dependence) enter dq and dk only.  512 threads.
+__global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
+    constexpr int BT = BI_THREADS, NW = BT / 32;
     const int ci = blockIdx.x, h = blockIdx.y;
     if (ci >= *p.nchunks) return;
     const int4 info = p.chunk_tab[ci];
@@ -478,6 +483,8 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
     extern __shared__ __align__(16) unsigned char smraw[];
     BwdIntraSmem& S = *reinterpret_cast<BwdIntraSmem*>(smraw);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    auto Qv = [&](int r, int c) { return __bfloat162float(S.qb[r * LB + c]) * S.rq[r]; };
+    auto Kv = [&](int r, int c) { return __bfloat162float(S.kb[r * LB + c]) * S.rk[r]; };
     const size_t chd = size_t(ci) * p.H + h;
     const float* dQg = p.dQg + chd * CH * D;
     const float* Pp = p.P + chd * CH * D;
@@ -487,29 +494,55 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
     const float* dM = p.dM + chd * CH * CH;
     const float* Akk = p.Akk + chd * CH * CH;
 
-    // 1. inputs
-    load_rows_bf16(S.q, LDP, p.q, t0, L, p.H, h, tid);
-    load_rows_bf16(S.k, LDP, p.k, t0, L, p.H, h, tid);
+    // 1. inputs: q, k (bf16 rows, zero past the end), gam, beta, dAqk, dAkk; per-row L2 scales
     {
-        float4 v[8];
-        load_tile_f32<CH>(v, p.gam + chd * CH * D, tid);
+        uint4 vq[2], vk[2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;
-            S.gam[r * LDP + c] = v[k].x;
-            S.gam[r * LDP + c + 1] = v[k].y;
-            S.gam[r * LDP + c + 2] = v[k].z;
-            S.gam[r * LDP + c + 3] = v[k].w;
+        for (int k4 = 0; k4 < 2; ++k4) {
+            const int i = tid + BT * k4, r = i >> 4, c8 = (i & 15) * 8;
+            const size_t off = (size_t(t0 + r) * p.H + h) * D + c8;
+            vq[k4] = r < L ? *reinterpret_cast<const uint4*>(p.q + off) : make_uint4(0u, 0u, 0u, 0u);
+            vk[k4] = r < L ? *reinterpret_cast<const uint4*>(p.k + off) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float4 v[4], va[2], vm[2];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) v[k4] = reinterpret_cast<const float4*>(p.gam + chd * CH * D)[tid + BT * k4];
+#pragma unroll
+        for (int k4 = 0; k4 < 2; ++k4) {
+            va[k4] = reinterpret_cast<const float4*>(dAqk)[tid + BT * k4];
+            vm[k4] = reinterpret_cast<const float4*>(dM)[tid + BT * k4];
+        }
+        if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
+#pragma unroll
+        for (int k4 = 0; k4 < 2; ++k4) {
+            const int i = tid + BT * k4, r = i >> 4, c8 = (i & 15) * 8;
+            *reinterpret_cast<uint4*>(&S.qb[r * LB + c8]) = vq[k4];
+            *reinterpret_cast<uint4*>(&S.kb[r * LB + c8]) = vk[k4];
+        }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int i = tid + BT * k4, r = i >> 5, c = (i & 31) * 4;
+            S.gam[r * LDP + c] = v[k4].x;
+            S.gam[r * LDP + c + 1] = v[k4].y;
+            S.gam[r * LDP + c + 2] = v[k4].z;
+            S.gam[r * LDP + c + 3] = v[k4].w;
+        }
+        __syncthreads();  // beta
+#pragma unroll
+        for (int k4 = 0; k4 < 2; ++k4) {
+            const int i = tid + BT * k4, r = i >> 4, c = (i & 15) * 4;
+            *reinterpret_cast<float4*>(&S.dA[r * LAS + c]) = va[k4];
+            const float br = S.beta[r];
+            *reinterpret_cast<float4*>(&S.dAk[r * LAS + c]) =
+                make_float4(br * vm[k4].x, br * vm[k4].y, br * vm[k4].z, br * vm[k4].w);
         }
     }
-    if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
-    __syncthreads();
-    for (int r = w; r < CH; r += NTHR / 32) {
+    for (int r = w; r < CH; r += NW) {
         float ra = 1.f, rb = 1.f;
         if (p.l2n) {
             float a = 0.f, b = 0.f;
             for (int c = lane; c < D; c += 32) {
-                const float x = S.q[r * LDP + c], y = S.k[r * LDP + c];
+                const float x = __bfloat162float(S.qb[r * LB + c]), y = __bfloat162float(S.kb[r * LB + c]);
                 a = fmaf(x, x, a);
                 b = fmaf(y, y, b);
             }
@@ -517,10 +550,6 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
             b = warp_sum(b);
             ra = 1.f / sqrtf(a + p.eps);
             rb = 1.f / sqrtf(b + p.eps);
-            for (int c = lane; c < D; c += 32) {
-                S.q[r * LDP + c] *= ra;
-                S.k[r * LDP + c] *= rb;
-            }
         }
         if (lane == 0) {
             S.rq[r] = ra;
@@ -530,20 +559,19 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
     __syncthreads();
 
     // 2. elementwise terms through Qg, Kg, Kb and the diagonal of Aqk
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
+    {
         float4 vq[4], vp[4], vb[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int i = tid + NTHR * (k + 4 * half);
+            const int i = tid + BT * k;
             vq[k] = reinterpret_cast<const float4*>(dQg)[i];
             vp[k] = reinterpret_cast<const float4*>(Pp)[i];
             vb[k] = reinterpret_cast<const float4*>(dKb)[i];
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int i = tid + NTHR * (k + 4 * half), r = i >> 5, c0 = (i & 31) * 4;
-            const float dgn = dAqk[r * CH + r], br = S.beta[r];
+            const int i = tid + BT * k, r = i >> 5, c0 = (i & 31) * 4;
+            const float dgn = S.dA[r * LAS + r], br = S.beta[r];
             const float aq[4] = {vq[k].x, vq[k].y, vq[k].z, vq[k].w};
             const float ap[4] = {vp[k].x, vp[k].y, vp[k].z, vp[k].w};
             const float ab[4] = {vb[k].x, vb[k].y, vb[k].z, vb[k].w};
@@ -552,7 +580,7 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
                 const int c = c0 + j;
                 const float gv = S.gam[r * LDP + c], gl = S.gam[(CH - 1) * LDP + c];
                 const float er = __expf(gv), eb = __expf(gl - gv);
-                const float qv = S.q[r * LDP + c], kv = S.k[r * LDP + c];
+                const float qv = Qv(r, c), kv = Kv(r, c);
                 const float dqg = aq[j], dkg = -br * ap[j], dkb = ab[j];
                 S.dQ[r * LDP + c] = fmaf(dqg, er, dgn * kv);
                 S.dK[r * LDP + c] = fmaf(dkg, er, fmaf(dkb, eb, dgn * qv));
@@ -562,161 +590,142 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
     }
     __syncthreads();
 
-    // 3. contractions across sub-chunks on tensor cores; warp w owns channels 16w..16w+15
+    // 3. contractions across sub-chunks on tensor cores; warp w owns channels 8w..8w+7
     {
-        auto a_frag = [&](const float* src, bool tr, bool kk, int m0, int k0, uint32_t (&hi)[4],
+        const int c = 8 * w + g;  // B-fragment column of this lane
+        auto a_frag = [&](const float* src, bool tr, int m0, int k0, uint32_t (&hi)[4],
                           uint32_t (&lo)[4]) {
-            // element (m, kx) of the A operand: src[m][kx] (tr = false) or src[kx][m] (tr = true);
-            // kk: the source is dM and the operand is dAkk = beta_row * dM
+            // element (m, kx) of the A operand: src[m][kx] (tr = false) or src[kx][m] (tr = true)
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const int m = m0 + g + 8 * (rr & 1), kx = k0 + 2 * t + 8 * (rr >> 1);
-                float x0, x1;
-                if (!tr) {
-                    x0 = src[m * CH + kx];
-                    x1 = src[m * CH + kx + 1];
-                    if (kk) { x0 *= S.beta[m]; x1 *= S.beta[m]; }
-                } else {
-                    x0 = src[kx * CH + m];
-                    x1 = src[(kx + 1) * CH + m];
-                    if (kk) { x0 *= S.beta[kx]; x1 *= S.beta[kx + 1]; }
-                }
+                const float x0 = tr ? src[kx * LAS + m] : src[m * LAS + kx];
+                const float x1 = tr ? src[(kx + 1) * LAS + m] : src[m * LAS + kx + 1];
                 split2(x0, x1, hi[rr], lo[rr]);
             }
         };
         // "as row": destination sub-chunk i = 1..3, reference row 16 i
         for (int i = 1; i < 4; ++i) {
             const int ref = 16 * i;
-            float aq[2][4] = {}, ak[2][4] = {};
+            const float gr = S.gam[ref * LDP + c];
+            float aq[4] = {}, ak[4] = {};
             for (int ks = 0; ks < i; ++ks) {
-                uint32_t qh[4], ql[4], kh[4], kl[4];
-                a_frag(dAqk, false, false, 16 * i, 16 * ks, qh, ql);
-                a_frag(dM, false, true, 16 * i, 16 * ks, kh, kl);
+                uint32_t qh[4], ql[4], kh[4], kl[4], bh[2], bl[2];
+                a_frag(S.dA, false, 16 * i, 16 * ks, qh, ql);
+                a_frag(S.dAk, false, 16 * i, 16 * ks, kh, kl);
 #pragma unroll
-                for (int nn = 0; nn < 2; ++nn) {
-                    const int c = 16 * w + 8 * nn + g;
-                    uint32_t bh[2], bl[2];
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int s0 = 16 * ks + 2 * t + 8 * hf;
-                        const float gr = S.gam[ref * LDP + c];
-                        const float x0 = S.k[s0 * LDP + c] * __expf(gr - S.gam[s0 * LDP + c]);
-                        const float x1 = S.k[(s0 + 1) * LDP + c] * __expf(gr - S.gam[(s0 + 1) * LDP + c]);
-                        split2(x0, x1, bh[hf], bl[hf]);
-                    }
-                    mma_x3(aq[nn], qh, ql, bh[0], bh[1], bl[0], bl[1]);
-                    mma_x3(ak[nn], kh, kl, bh[0], bh[1], bl[0], bl[1]);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int s0 = 16 * ks + 2 * t + 8 * hf;
+                    const float x0 = Kv(s0, c) * __expf(gr - S.gam[s0 * LDP + c]);
+                    const float x1 = Kv(s0 + 1, c) * __expf(gr - S.gam[(s0 + 1) * LDP + c]);
+                    split2(x0, x1, bh[hf], bl[hf]);
                 }
+                mma_x3(aq, qh, ql, bh[0], bh[1], bl[0], bl[1]);
+                mma_x3(ak, kh, kl, bh[0], bh[1], bl[0], bl[1]);
             }
 #pragma unroll
-            for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = 16 * i + g + 8 * (e >> 1), c = 16 * w + 8 * nn + 2 * t + (e & 1);
-                    const float sc = __expf(S.gam[r * LDP + c] - S.gam[ref * LDP + c]);
-                    const float vq = aq[nn][e] * sc, vk = ak[nn][e] * sc;
-                    S.dQ[r * LDP + c] += vq;
-                    S.dK[r * LDP + c] += vk;
-                    S.dG[r * LDP + c] += S.q[r * LDP + c] * vq + S.k[r * LDP + c] * vk;
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int r = 16 * i + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
+                const float sc = __expf(S.gam[r * LDP + cc] - S.gam[ref * LDP + cc]);
+                const float vq = aq[e] * sc, vk = ak[e] * sc;
+                S.dQ[r * LDP + cc] += vq;
+                S.dK[r * LDP + cc] += vk;
+                S.dG[r * LDP + cc] += Qv(r, cc) * vq + Kv(r, cc) * vk;
+            }
         }
         // "as column": destination sub-chunk j = 0..2, reference row 16 j + 15
         for (int j = 0; j < 3; ++j) {
             const int ref = 16 * j + 15;
-            float bacc[2][4] = {};
+            const float gr = S.gam[ref * LDP + c];
+            float bacc[4] = {};
             for (int ks = j + 1; ks < 4; ++ks) {
-                uint32_t qh[4], ql[4], kh[4], kl[4];
-                a_frag(dAqk, true, false, 16 * j, 16 * ks, qh, ql);
-                a_frag(dM, true, true, 16 * j, 16 * ks, kh, kl);
+                uint32_t qh[4], ql[4], kh[4], kl[4], qbh[2], qbl[2], kbh[2], kbl[2];
+                a_frag(S.dA, true, 16 * j, 16 * ks, qh, ql);
+                a_frag(S.dAk, true, 16 * j, 16 * ks, kh, kl);
 #pragma unroll
-                for (int nn = 0; nn < 2; ++nn) {
-                    const int c = 16 * w + 8 * nn + g;
-                    uint32_t qbh[2], qbl[2], kbh[2], kbl[2];
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int r0 = 16 * ks + 2 * t + 8 * hf;
-                        const float gr = S.gam[ref * LDP + c];
-                        const float e0 = __expf(S.gam[r0 * LDP + c] - gr);
-                        const float e1 = __expf(S.gam[(r0 + 1) * LDP + c] - gr);
-                        split2(S.q[r0 * LDP + c] * e0, S.q[(r0 + 1) * LDP + c] * e1, qbh[hf], qbl[hf]);
-                        split2(S.k[r0 * LDP + c] * e0, S.k[(r0 + 1) * LDP + c] * e1, kbh[hf], kbl[hf]);
-                    }
-                    mma_x3(bacc[nn], qh, ql, qbh[0], qbh[1], qbl[0], qbl[1]);
-                    mma_x3(bacc[nn], kh, kl, kbh[0], kbh[1], kbl[0], kbl[1]);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int r0 = 16 * ks + 2 * t + 8 * hf;
+                    const float e0 = __expf(S.gam[r0 * LDP + c] - gr);
+                    const float e1 = __expf(S.gam[(r0 + 1) * LDP + c] - gr);
+                    split2(Qv(r0, c) * e0, Qv(r0 + 1, c) * e1, qbh[hf], qbl[hf]);
+                    split2(Kv(r0, c) * e0, Kv(r0 + 1, c) * e1, kbh[hf], kbl[hf]);
                 }
+                mma_x3(bacc, qh, ql, qbh[0], qbh[1], qbl[0], qbl[1]);
+                mma_x3(bacc, kh, kl, kbh[0], kbh[1], kbl[0], kbl[1]);
             }
 #pragma unroll
-            for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int s = 16 * j + g + 8 * (e >> 1), c = 16 * w + 8 * nn + 2 * t + (e & 1);
-                    const float vb = bacc[nn][e] * __expf(S.gam[ref * LDP + c] - S.gam[s * LDP + c]);
-                    S.dK[s * LDP + c] += vb;
-                    S.dG[s * LDP + c] -= S.k[s * LDP + c] * vb;
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int sr = 16 * j + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
+                const float vb = bacc[e] * __expf(S.gam[ref * LDP + cc] - S.gam[sr * LDP + cc]);
+                S.dK[sr * LDP + cc] += vb;
+                S.dG[sr * LDP + cc] -= Kv(sr, cc) * vb;
+            }
         }
     }
     __syncthreads();
 
-    // 4. inside each sub-chunk, elementwise: thread per (sub-chunk, channel)
-    for (int task = tid; task < 4 * D; task += NTHR) {
-        const int b = task / D, c = task % D, base = 16 * b;
-        float aq[16], ak[16], bb[16];
+    // 4. inside each sub-chunk, elementwise: one thread per (sub-chunk, channel); the column's 16
+    //    values of gam, q^, k^ are held in registers
+    {
+        const int b = tid / D, c = tid % D, base = 16 * b;
+        float gv[16], qv[16], kv[16], aq[16], ak[16], bb[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) aq[x] = ak[x] = bb[x] = 0.f;
+        for (int x = 0; x < 16; ++x) {
+            gv[x] = S.gam[(base + x) * LDP + c];
+            qv[x] = Qv(base + x, c);
+            kv[x] = Kv(base + x, c);
+            aq[x] = ak[x] = bb[x] = 0.f;
+        }
 #pragma unroll
         for (int rl = 1; rl < 16; ++rl) {
             const int r = base + rl;
-            const float gr = S.gam[r * LDP + c], qr = S.q[r * LDP + c], kr = S.k[r * LDP + c];
-            const float br = S.beta[r];
 #pragma unroll
             for (int sl = 0; sl < rl; ++sl) {
-                const int s = base + sl;
-                const float E = __expf(gr - S.gam[s * LDP + c]);
-                const float da = dAqk[r * CH + s], dk = br * dM[r * CH + s];
-                const float ks = S.k[s * LDP + c] * E;
+                const float E = __expf(gv[rl] - gv[sl]);
+                const float da = S.dA[r * LAS + base + sl], dk = S.dAk[r * LAS + base + sl];
+                const float ks = kv[sl] * E;
                 aq[rl] = fmaf(da, ks, aq[rl]);
                 ak[rl] = fmaf(dk, ks, ak[rl]);
-                bb[sl] = fmaf(fmaf(da, qr, dk * kr), E, bb[sl]);
+                bb[sl] = fmaf(fmaf(da, qv[rl], dk * kv[rl]), E, bb[sl]);
             }
         }
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
             const int r = base + x;
-            const float qv = S.q[r * LDP + c], kv = S.k[r * LDP + c];
             S.dQ[r * LDP + c] += aq[x];
             S.dK[r * LDP + c] += ak[x] + bb[x];
-            S.dG[r * LDP + c] += qv * aq[x] + kv * (ak[x] - bb[x]);
+            S.dG[r * LDP + c] += qv[x] * aq[x] + kv[x] * (ak[x] - bb[x]);
         }
     }
     __syncthreads();
 
     // 5. chunk-end gate term dgL = e^gL rowsum(S0 * dS1) + sum_r dKb * Kb, then the reverse
-    //    cumsum over the chunk; two threads per channel (rows 0-31 / 32-63), fixed order
+    //    cumsum over the chunk; four threads per channel (16 rows each), fixed order
     {
-        const int c = tid & (D - 1), half = tid >> 7, r0 = 32 * half;
+        const int c = tid & (D - 1), qu = tid >> 7, r0 = 16 * qu;
         const float gl = S.gam[(CH - 1) * LDP + c];
         float part = 0.f;
-#pragma unroll 8
-        for (int r = r0; r < r0 + 32; ++r)
-            part = fmaf(dKb[r * D + c], S.k[r * LDP + c] * __expf(gl - S.gam[r * LDP + c]), part);
-        float suf = 0.f;  // suffix sums inside the half
-        for (int r = r0 + 31; r >= r0; --r) {
+#pragma unroll
+        for (int r = r0; r < r0 + 16; ++r)
+            part = fmaf(dKb[r * D + c], Kv(r, c) * __expf(gl - S.gam[r * LDP + c]), part);
+        float suf = 0.f;  // suffix sums inside the quarter
+        for (int r = r0 + 15; r >= r0; --r) {
             suf += S.dG[r * LDP + c];
             S.dG[r * LDP + c] = suf;
         }
         S.red[tid] = part;
+        S.red[BT + tid] = suf;  // quarter total
         __syncthreads();
-        const float dgl = __expf(gl) * p.rsum[chd * D + c] + (S.red[c] + S.red[c + D]);
-        // rows of the lower half also receive the whole upper half; every row receives dgL
-        const float carry = half == 0 ? S.dG[32 * LDP + c] : 0.f;
-        __syncthreads();
-        for (int r = r0; r < r0 + 32; ++r) S.dG[r * LDP + c] += carry + dgl;
+        const float dgl = __expf(gl) * p.rsum[chd * D + c] +
+                          ((S.red[c] + S.red[D + c]) + (S.red[2 * D + c] + S.red[3 * D + c]));
+        float carry = 0.f;  // totals of the later quarters
+        for (int q2 = qu + 1; q2 < 4; ++q2) carry += S.red[BT + q2 * D + c];
+        for (int r = r0; r < r0 + 16; ++r) S.dG[r * LDP + c] += carry + dgl;
     }
     __syncthreads();
 
     // 6. per row: L2-norm backward, dq, dk, dv, dbeta (warp per row)
-    for (int r = w; r < L; r += NTHR / 32) {
+    for (int r = w; r < L; r += NW) {
         const size_t base = (size_t(t0 + r) * p.H + h) * D;
         const float br = S.beta[r];
         float dq[4], dk[4], pq = 0.f, pk = 0.f, db = 0.f;
@@ -725,15 +734,16 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
             const int c = lane + 32 * m;
             dq[m] = S.dQ[r * LDP + c];
             dk[m] = S.dK[r * LDP + c];
-            pq = fmaf(S.q[r * LDP + c], dq[m], pq);
-            pk = fmaf(S.k[r * LDP + c], dk[m], pk);
+            const float qv = Qv(r, c), kv = Kv(r, c);
+            pq = fmaf(qv, dq[m], pq);
+            pk = fmaf(kv, dk[m], pk);
             const float dRv = dR[r * D + c];
-            const float kg = S.k[r * LDP + c] * __expf(S.gam[r * LDP + c]);
+            const float kg = kv * __expf(S.gam[r * LDP + c]);
             db = fmaf(dRv, bf2f(p.v[base + c]), db);
             db = fmaf(-kg, Pp[r * D + c], db);
             store_out(p.dv, base + c, br * dRv, p.out_fp32);
         }
-        for (int s = lane; s < r; s += 32) db = fmaf(Akk[r * CH + s], dM[r * CH + s], db);
+        for (int s2 = lane; s2 < r; s2 += 32) db = fmaf(Akk[r * CH + s2], dM[r * CH + s2], db);
         db = warp_sum(db);
         if (p.l2n) {
             pq = warp_sum(pq);
@@ -744,44 +754,56 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
             const int c = lane + 32 * m;
             float vq = dq[m], vk = dk[m];
             if (p.l2n) {
-                vq = (vq - S.q[r * LDP + c] * pq) * S.rq[r];
-                vk = (vk - S.k[r * LDP + c] * pk) * S.rk[r];
+                vq = (vq - Qv(r, c) * pq) * S.rq[r];
+                vk = (vk - Kv(r, c) * pk) * S.rk[r];
             }
             store_out(p.dq, base + c, vq, p.out_fp32);
             store_out(p.dk, base + c, vk, p.out_fp32);
         }
         if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, db, p.out_fp32);
     }
-
     __syncthreads();  // step 7 reuses dQ / dK as scratch
-    // 7. gate gradient: g form writes dg; raw form writes da and the parameter partials
+
+    // 7. gate gradient: g form writes dg; raw form writes da and the parameter partials.
+    //    In raw form the token's gate g_r is recovered from the stored cumsum, g_r = gam_r -
+    //    gam_{r-1}, and dg/da = -exp(A_log) sigmoid(a + dt_bias).
     if (!p.gate_raw) {
-        for (int i = tid; i < L * D; i += NTHR) {
-            const int r = i / D, c = i % D;
-            p.dg[(size_t(t0 + r) * p.H + h) * D + c] = S.dG[r * LDP + c];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
+            if (r < L)
+                *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
+                    make_float4(S.dG[r * LDP + c4], S.dG[r * LDP + c4 + 1], S.dG[r * LDP + c4 + 2],
+                                S.dG[r * LDP + c4 + 3]);
         }
         return;
     }
     const float eA = expf(p.A_log[h]);
     {
-        // da elementwise (all threads, batched loads); dg * g -> dQ, da -> dK for the reductions
-        float4 av[8];
-        load_rows_f32(av, p.g, t0, L, p.H, h, tid);
-        const int c4 = (tid & 31) * 4;
-        const float4 db = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
-        const float b4[4] = {db.x, db.y, db.z, db.w};
+        float4 av[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int r = (tid + NTHR * k) >> 5;
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
+            av[k] = r < L ? *reinterpret_cast<const float4*>(p.g + (size_t(t0 + r) * p.H + h) * D + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const int c4 = (tid & 31) * 4;
+        const float4 dtb = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
+        const float b4[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = (tid + BT * k) >> 5;
             const float a4[4] = {av[k].x, av[k].y, av[k].z, av[k].w};
             float da4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float x = a4[j] + b4[j], dg = S.dG[r * LDP + c4 + j];
+                const int c = c4 + j;
                 const bool ok = r < L;
-                da4[j] = ok ? dg * (-eA) * sigmoid_f(x) : 0.f;
-                S.dQ[r * LDP + c4 + j] = ok ? dg * (-eA * softplus_f(x)) : 0.f;
-                S.dK[r * LDP + c4 + j] = da4[j];
+                const float x = a4[j] + b4[j], dg = S.dG[r * LDP + c];
+                const float gv = S.gam[r * LDP + c] - (r > 0 ? S.gam[(r - 1) * LDP + c] : 0.f);
+                da4[j] = ok ? dg * (-eA) * __frcp_rn(1.f + __expf(-x)) : 0.f;
+                S.dQ[r * LDP + c] = ok ? dg * gv : 0.f;
+                S.dK[r * LDP + c] = da4[j];
             }
             if (r < L)
                 *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
@@ -789,19 +811,26 @@ __global__ void __launch_bounds__(NTHR) k_bwd_intra(Params p) {
         }
     }
     __syncthreads();
-    float pa = 0.f;
-    if (tid < D) {
-        const int c = tid;
-        float pd = 0.f;
-        for (int r = 0; r < CH; ++r) {
+    {
+        // column sums over the 64 rows: four threads per channel (16 rows each), fixed order
+        const int c = tid & (D - 1), qu = tid >> 7;
+        float pd = 0.f, pa = 0.f;
+        for (int r = 16 * qu; r < 16 * qu + 16; ++r) {
             pd += S.dK[r * LDP + c];
             pa += S.dQ[r * LDP + c];
         }
-        p.pddt[chd * D + c] = pd;
+        S.red[tid] = pd;
+        S.red[BT + tid] = pa;
     }
-    S.red[tid] = pa;
     __syncthreads();
-    for (int s2 = NTHR / 2; s2 > 0; s2 >>= 1) {
+    if (tid < D) {
+        const int c = tid;
+        p.pddt[chd * D + c] = (S.red[c] + S.red[D + c]) + (S.red[2 * D + c] + S.red[3 * D + c]);
+        const float pa = (S.red[BT + c] + S.red[BT + D + c]) + (S.red[BT + 2 * D + c] + S.red[BT + 3 * D + c]);
+        S.red[c] = pa;
+    }
+    __syncthreads();
+    for (int s2 = D / 2; s2 > 0; s2 >>= 1) {
         if (tid < s2) S.red[tid] += S.red[tid + s2];
         __syncthreads();
     }

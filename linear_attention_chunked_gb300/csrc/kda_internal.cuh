@@ -40,10 +40,10 @@ struct Layout {
     int64_t maxC;  // upper bound of the chunk count: ceil(T/64) + N
     // workspace
     size_t status, nchunks, doc_off, chunk_tab;
-    size_t Wh, Wl, Qh, Ql, Kh, Kl, Ah, Al, Mh, Ml, U, Akk, gam, eGL;  // intra products
     size_t dS1, dDelta, dR, P, dQg, dKb, dAqk, dM, rsum;              // backward intermediates
     size_t pdA, pddt;                                                 // parameter partials
-    size_t replay;                                                    // saved set (replay mode)
+    size_t replay;    // replay copy of the saved set
+    size_t intra_ws;  // intra products of a forward without saved set / of fragment summaries
     size_t ws_fwd, ws_bwd_saved, ws_bwd_replay, ws_frag;
     // saved set
     size_t sv_S, sv_Delta, saved_bytes;
@@ -51,6 +51,38 @@ struct Layout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Offsets inside one "record" of the intra-chunk products (relative to its base).
+struct IntraRecord {
+    size_t Wh, Wl, Qh, Ql, Kh, Kl, Ah, Al, Mh, Ml, U, Akk, gam, eGL, bytes;
+};
+
+inline IntraRecord make_intra_record(size_t CHd) {
+    IntraRecord R{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+    const size_t tileD = CHd * CH * D, tileC = CHd * CH * CH;
+    R.Wh = take(tileD * 2);
+    R.Wl = take(tileD * 2);
+    R.Qh = take(tileD * 2);
+    R.Ql = take(tileD * 2);
+    R.Kh = take(tileD * 2);
+    R.Kl = take(tileD * 2);
+    R.Ah = take(tileC * 2);
+    R.Al = take(tileC * 2);
+    R.Mh = take(tileC * 2);
+    R.Ml = take(tileC * 2);
+    R.U = take(tileD * 4);
+    R.Akk = take(tileC * 4);
+    R.gam = take(tileD * 4);
+    R.eGL = take(CHd * D * 4);
+    R.bytes = o;
+    return R;
+}
+
+// The saved forward set = [intra-chunk products | per-chunk start states S_c | write vectors
+// Delta_c].  The workspace holds the chunk plan, the backward intermediates, and a private copy of
+// the intra products (forward without a saved set, fragment summaries) or of the whole saved set
+// (checkpoint replay).
 inline Layout make_layout(int64_t T, int N, int H) {
     Layout L{};
     L.T = T;
@@ -58,29 +90,24 @@ inline Layout make_layout(int64_t T, int N, int H) {
     L.H = H;
     L.maxC = (T + CH - 1) / CH + N;
     const size_t CHd = size_t(L.maxC) * H;  // chunk-head pairs
+    const size_t tileD = CHd * CH * D, tileC = CHd * CH * CH;
+    const IntraRecord R = make_intra_record(CHd);
+    // saved set
+    L.sv_S = R.bytes;
+    L.sv_Delta = align256(L.sv_S + CHd * D * D * 4);
+    L.saved_bytes = align256(L.sv_Delta + tileD * 4);
+    // workspace: header | backward intermediates | replay copy of the saved set.  The forward
+    // without a saved set and the fragment summaries keep their intra products right after the
+    // header instead (they need no backward intermediates).
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(256);
     L.nchunks = take(sizeof(int));
     L.doc_off = take(sizeof(int) * size_t(N + 1));
     L.chunk_tab = take(sizeof(int4) * size_t(L.maxC));
-    const size_t tileD = CHd * CH * D, tileC = CHd * CH * CH;
-    L.Wh = take(tileD * 2);
-    L.Wl = take(tileD * 2);
-    L.Qh = take(tileD * 2);
-    L.Ql = take(tileD * 2);
-    L.Kh = take(tileD * 2);
-    L.Kl = take(tileD * 2);
-    L.Ah = take(tileC * 2);
-    L.Al = take(tileC * 2);
-    L.Mh = take(tileC * 2);
-    L.Ml = take(tileC * 2);
-    L.U = take(tileD * 4);
-    L.Akk = take(tileC * 4);
-    L.gam = take(tileD * 4);
-    L.eGL = take(CHd * D * 4);
-    L.ws_fwd = o;
-    L.ws_frag = o;
+    L.intra_ws = o;
+    L.ws_fwd = o + R.bytes;
+    L.ws_frag = o + R.bytes;
     L.dS1 = take(CHd * D * D * 4);
     L.dDelta = take(tileD * 4);
     L.dR = take(tileD * 4);
@@ -93,13 +120,6 @@ inline Layout make_layout(int64_t T, int N, int H) {
     L.pdA = take(CHd * 4);
     L.pddt = take(CHd * D * 4);
     L.ws_bwd_saved = o;
-    // saved set: per-chunk start states S_c (fp32 [128][128]) and write vectors Delta_c
-    size_t s = 0;
-    L.sv_S = 0;
-    s = align256(CHd * D * D * 4);
-    L.sv_Delta = s;
-    s = align256(s + tileD * 4);
-    L.saved_bytes = s;
     L.replay = take(L.saved_bytes);
     L.ws_bwd_replay = o;
     return L;
@@ -249,6 +269,8 @@ size_t chain_bwd_smem_bytes();
 size_t bwd_gemm_smem_bytes();
 size_t bwd_intra_smem_bytes();
 constexpr int CHAIN_THREADS = 128;  // 4 warps per state-recurrence block
+constexpr int BI_THREADS = 512;     // threads of the backward intra-chunk kernel
+constexpr int INTRA_THREADS = 512;  // threads of the forward intra-chunk kernel
 constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences
 __global__ void k_plan(Params p);
 __global__ void k_intra_fwd(Params p);

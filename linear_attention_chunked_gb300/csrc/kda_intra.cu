@@ -47,7 +47,8 @@ __device__ __forceinline__ int tri_row(int pi) {  // row of the pi-th entry of a
 
 size_t intra_smem_bytes() { return sizeof(IntraSmem); }
 
-__global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
+__global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
+    constexpr int BT = INTRA_THREADS, NW = BT / 32;
     const int ci = blockIdx.x, h = blockIdx.y;
     if (ci >= *p.nchunks) return;
     const int4 info = p.chunk_tab[ci];
@@ -58,11 +59,22 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
     const size_t chd = size_t(ci) * p.H + h;
 
     // 1. loads (zero rows past the document end), gate, beta; clear the 64x64 accumulators
-    load_rows_bf16(S.q, LDP, p.q, t0, L, p.H, h, tid);
-    load_rows_bf16(S.k, LDP, p.k, t0, L, p.H, h, tid);
     {
-        float4 gv[8];
-        load_rows_f32(gv, p.g, t0, L, p.H, h, tid);
+        uint4 vq[2], vk[2];
+        float4 gv[4];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
+            const size_t off = (size_t(t0 + r) * p.H + h) * D + c8;
+            vq[k] = r < L ? *reinterpret_cast<const uint4*>(p.q + off) : make_uint4(0u, 0u, 0u, 0u);
+            vk[k] = r < L ? *reinterpret_cast<const uint4*>(p.k + off) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
+            gv[k] = r < L ? *reinterpret_cast<const float4*>(p.g + (size_t(t0 + r) * p.H + h) * D + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         const int c4 = (tid & 31) * 4;  // the same 4 channels for every k
         float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
         float eA = 0.f;
@@ -70,10 +82,25 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
             db = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
             eA = expf(p.A_log[h]);
         }
+        if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int r = (tid + NTHR * k) >> 5;
-            float x[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
+            const __nv_bfloat162* bq = reinterpret_cast<const __nv_bfloat162*>(&vq[k]);
+            const __nv_bfloat162* bk = reinterpret_cast<const __nv_bfloat162*>(&vk[k]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 fq = __bfloat1622float2(bq[j]), fk = __bfloat1622float2(bk[j]);
+                S.q[r * LDP + c8 + 2 * j] = fq.x;
+                S.q[r * LDP + c8 + 2 * j + 1] = fq.y;
+                S.k[r * LDP + c8 + 2 * j] = fk.x;
+                S.k[r * LDP + c8 + 2 * j + 1] = fk.y;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = (tid + BT * k) >> 5;
+            const float x[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
             const float b4[4] = {db.x, db.y, db.z, db.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -83,17 +110,16 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
             }
         }
     }
-    for (int i = tid; i < CH * LDA; i += NTHR) {
+    for (int i = tid; i < CH * LDA; i += BT) {
         S.Akk[i] = 0.f;
         S.Aqk[i] = 0.f;
         S.Mi[i] = 0.f;
     }
-    if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
     __syncthreads();
 
     // 2. fused L2 norm (warp per row)
     if (p.l2n) {
-        for (int r = warp; r < CH; r += NTHR / 32) {
+        for (int r = warp; r < CH; r += NW) {
             float a = 0.f, b = 0.f;
             for (int c = lane; c < D; c += 32) {
                 const float x = S.q[r * LDP + c], y = S.k[r * LDP + c];
@@ -109,18 +135,27 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
             }
         }
     }
-    // 3. in-chunk inclusive cumsum (thread per channel)
-    if (tid < D) {
+    // 3. in-chunk inclusive cumsum: four threads per channel (16 rows each), then carries
+    {
+        const int c = tid & (D - 1), qu = tid >> 7, r0 = 16 * qu;
         float run = 0.f;
-        for (int r = 0; r < CH; ++r) {
-            run += S.gam[r * LDP + tid];
-            S.gam[r * LDP + tid] = run;
+#pragma unroll
+        for (int r = r0; r < r0 + 16; ++r) {
+            run += S.gam[r * LDP + c];
+            S.gam[r * LDP + c] = run;
         }
+        __syncthreads();
+        float carry = 0.f;
+        for (int q2 = 0; q2 < qu; ++q2) carry += S.gam[(16 * q2 + 15) * LDP + c];
+        __syncthreads();
+        if (qu > 0)
+#pragma unroll
+            for (int r = r0; r < r0 + 16; ++r) S.gam[r * LDP + c] += carry;
     }
     __syncthreads();
 
     // 4a. diagonal 16x16 blocks, elementwise exact exponent differences
-    for (int idx = tid; idx < 4 * 136; idx += NTHR) {
+    for (int idx = tid; idx < 4 * 136; idx += BT) {
         const int b = idx / 136, pi = idx % 136;
         const int rl = tri_row(pi), sl = pi - rl * (rl + 1) / 2;
         const int r = 16 * b + rl, s = 16 * b + sl;
@@ -140,7 +175,7 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
         S.Aqk[r * LDA + s] = aqk;
     }
     // 4b. B operands Ks_j[sl][c] = k[16j+sl][c] exp(gam[16j+15][c] - gam[16j+sl][c]), j = 0..2
-    for (int idx = tid; idx < 3 * 16 * D; idx += NTHR) {
+    for (int idx = tid; idx < 3 * 16 * D; idx += BT) {
         const int j = idx / (16 * D), rem = idx % (16 * D), sl = rem / D, c = rem % D;
         const int s = 16 * j + sl, e = 16 * j + 15;
         const float x = S.k[s * LDP + c] * __expf(S.gam[e * LDP + c] - S.gam[s * LDP + c]);
@@ -149,10 +184,11 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
         S.u.a.Ks[j][1][sl * LB + c] = __float2bfloat16_rn(x - __bfloat162float(hi));
     }
     __syncthreads();
-    // 4c. off-diagonal blocks on tensor cores: warp w < 6 takes the pair (i, j)
-    if (warp < 6) {
-        const int i = kPairs[warp].x, j = kPairs[warp].y, e = 16 * j + 15;
-        float accQ[2][4] = {}, accK[2][4] = {};
+    // 4c. off-diagonal blocks on tensor cores: warp w < 12 takes pair w / 2, n-tile w % 2
+    if (warp < 12) {
+        const int pr = warp >> 1, nt = warp & 1;
+        const int i = kPairs[pr].x, j = kPairs[pr].y, e = 16 * j + 15;
+        float accQ[4] = {}, accK[4] = {};
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t qh[4], ql[4], kh[4], kl[4];
 #pragma unroll
@@ -166,20 +202,15 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
             uint32_t bh[4], bl[4];
             ldsm4(bh, bn_addr(S.u.a.Ks[j][0], LB, 16 * ks, 0, lane));
             ldsm4(bl, bn_addr(S.u.a.Ks[j][1], LB, 16 * ks, 0, lane));
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                mma_x3(accQ[nt], qh, ql, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
-                mma_x3(accK[nt], kh, kl, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
-            }
+            mma_x3(accQ, qh, ql, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
+            mma_x3(accK, kh, kl, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                const int row = 16 * i + g + 8 * (e4 >> 1), col = 16 * j + 8 * nt + 2 * t + (e4 & 1);
-                S.Aqk[row * LDA + col] = accQ[nt][e4];
-                S.Akk[row * LDA + col] = accK[nt][e4];
-            }
+        for (int e4 = 0; e4 < 4; ++e4) {
+            const int row = 16 * i + g + 8 * (e4 >> 1), col = 16 * j + 8 * nt + 2 * t + (e4 & 1);
+            S.Aqk[row * LDA + col] = accQ[e4];
+            S.Akk[row * LDA + col] = accK[e4];
+        }
     }
     __syncthreads();
 
@@ -203,7 +234,7 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
 #pragma unroll
     for (int dist = 1; dist < 4; ++dist) {
         const int nb = 4 - dist;
-        for (int idx = tid; idx < nb * 256; idx += NTHR) {
+        for (int idx = tid; idx < nb * 256; idx += BT) {
             const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
             const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
             float a0 = 0.f, a1 = 0.f;
@@ -215,7 +246,7 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
             S.u.a.T[b][rl * 17 + cl] = S.beta[r] * (a0 + a1);
         }
         __syncthreads();
-        for (int idx = tid; idx < nb * 256; idx += NTHR) {
+        for (int idx = tid; idx < nb * 256; idx += BT) {
             const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
             const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
             float a0 = 0.f, a1 = 0.f;
@@ -231,14 +262,14 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
 
     // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
     {
-        uint4 vv[4];
+        uint4 vv[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
             vv[k] = r < L ? *reinterpret_cast<const uint4*>(p.v + (size_t(t0 + r) * p.H + h) * D + c8)
                           : make_uint4(0u, 0u, 0u, 0u);
         }
-        for (int i = tid; i < CH * D / 2; i += NTHR) {
+        for (int i = tid; i < CH * D / 2; i += BT) {
             const int r = (2 * i) / D, c = (2 * i) % D;
             const float x0 = S.beta[r] * S.k[r * LDP + c] * __expf(S.gam[r * LDP + c]);
             const float x1 = S.beta[r] * S.k[r * LDP + c + 1] * __expf(S.gam[r * LDP + c + 1]);
@@ -248,15 +279,15 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
             *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
             *reinterpret_cast<uint4*>(&S.u.b.v[r * LB + c8]) = vv[k];
         }
     }
     __syncthreads();
     {
-        const int mt = warp & 3, nh = warp >> 2;
-        float accW[8][4] = {}, accU[8][4] = {};
+        const int mt = warp & 3, nq = warp >> 2;  // rows 16 mt.., columns 32 nq..
+        float accW[4][4] = {}, accU[4][4] = {};
         for (int ks = 0; ks <= mt; ++ks) {  // Minv is lower triangular
             uint32_t mh[4], ml[4], bh_[4], bl_[4];
 #pragma unroll
@@ -267,9 +298,9 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
                 split2(m0 * S.beta[col], m1 * S.beta[col + 1], bh_[rr], bl_[rr]);
             }
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
+            for (int np = 0; np < 2; ++np) {
                 uint32_t kh[4], kl[4], vv[4];
-                const int n0 = 64 * nh + 16 * np;
+                const int n0 = 32 * nq + 16 * np;
                 ldsm4t(kh, bk_addr(S.u.b.bKg[0], LB, 16 * ks, n0, lane));
                 ldsm4t(kl, bk_addr(S.u.b.bKg[1], LB, 16 * ks, n0, lane));
                 ldsm4t(vv, bk_addr(S.u.b.v, LB, 16 * ks, n0, lane));
@@ -285,10 +316,10 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
         __nv_bfloat16* Wl = p.Wl + chd * CH * D;
         float* U = p.U + chd * CH * D;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const int row = 16 * mt + g + 8 * hf, col = 64 * nh + 8 * nt + 2 * t;
+                const int row = 16 * mt + g + 8 * hf, col = 32 * nq + 8 * nt + 2 * t;
                 uint32_t hi, lo;
                 split2(accW[nt][2 * hf], accW[nt][2 * hf + 1], hi, lo);
                 *reinterpret_cast<uint32_t*>(Wh + row * D + col) = hi;
@@ -305,7 +336,7 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
         __nv_bfloat16* Kh = p.Kh + chd * CH * D;
         __nv_bfloat16* Kl = p.Kl + chd * CH * D;
         float* gam = p.gam + chd * CH * D;
-        for (int i = tid; i < CH * D / 2; i += NTHR) {
+        for (int i = tid; i < CH * D / 2; i += BT) {
             const int r = (2 * i) / D, c = (2 * i) % D;
             const float g0 = S.gam[r * LDP + c], g1 = S.gam[r * LDP + c + 1];
             const float gl0 = S.gam[(CH - 1) * LDP + c], gl1 = S.gam[(CH - 1) * LDP + c + 1];
@@ -323,7 +354,7 @@ __global__ void __launch_bounds__(NTHR) k_intra_fwd(Params p) {
         __nv_bfloat16* Mh = p.Mh + chd * CH * CH;
         __nv_bfloat16* Ml = p.Ml + chd * CH * CH;
         float* Akk = p.Akk + chd * CH * CH;
-        for (int i = tid; i < CH * CH / 2; i += NTHR) {
+        for (int i = tid; i < CH * CH / 2; i += BT) {
             const int r = (2 * i) / CH, s = (2 * i) % CH;
             uint32_t hi, lo;
             split2(S.Aqk[r * LDA + s], S.Aqk[r * LDA + s + 1], hi, lo);

@@ -64,40 +64,43 @@ size_t chain_bwd_smem_bytes() { return sizeof(ChainBwdSmem); }
 size_t bwd_gemm_smem_bytes() { return sizeof(BwdGemmSmem); }
 
 // Reverse state recurrence of one (document, head, 64-column value half) on tensor cores.
-// Warp w keeps keys 32w..32w+31 of the FP32 gradient dS in registers; per chunk, going back:
-//   A': dDelta = scale Aqk^T dO + Kb dS1     (warp w: tokens 16w..16w+15)
+// Eight warps: warp w = (wq, wn), wq = w % 4 (row group), wn = w / 4 (32-column quarter).  Warp w
+// keeps keys 32 wq.. x columns 32 wn.. of the FP32 gradient dS in registers; per chunk, going back:
+//   A': dDelta = scale Aqk^T dO + Kb dS1     (tokens 16 wq..16 wq+15)
 //   D': dS0 = e^gL * dS1 + scale Qg^T dO - W^T dDelta
 // mode CHAIN_BWD: dS from dht; per chunk writes dS1 and dDelta for the per-chunk kernels; dh0.
 // mode CHAIN_FRAG_C: dS from zero; writes C (= dS at the fragment start) to fragB.
-__global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
+__global__ void __launch_bounds__(CHAIN_THREADS) k_chain_bwd(Params p, int mode) {
+    constexpr int BT = CHAIN_THREADS;
     const int n = blockIdx.x, h = blockIdx.y, hv = blockIdx.z;
     const bool bwd = mode == CHAIN_BWD;
     const int col0 = hv * 64;
     extern __shared__ __align__(16) unsigned char smraw[];
     ChainBwdSmem& sm = *reinterpret_cast<ChainBwdSmem*>(smraw);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int wq = w & 3, wn = w >> 2, cq = 32 * wn;
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
 
-    float dS[2][8][4];
+    float dS[2][4][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int key = 32 * w + 16 * mt + g + 8 * (e >> 1);
-                const int val = col0 + 8 * nt + 2 * t + (e & 1);
+                const int key = 32 * wq + 16 * mt + g + 8 * (e >> 1);
+                const int val = col0 + cq + 8 * nt + 2 * t + (e & 1);
                 dS[mt][nt][e] = (bwd && p.dht) ? p.dht[dh + size_t(key) * D + val] : 0.f;
             }
     auto store_dS = [&]() {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const int key = 32 * w + 16 * mt + g + 8 * hf, col = 8 * nt + 2 * t;
+                    const int key = 32 * wq + 16 * mt + g + 8 * hf, col = cq + 8 * nt + 2 * t;
                     uint32_t hi, lo;
                     split2(dS[mt][nt][2 * hf], dS[mt][nt][2 * hf + 1], hi, lo);
                     *reinterpret_cast<uint32_t*>(&sm.dS[0][key * LB64 + col]) = hi;
@@ -109,12 +112,12 @@ __global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
         if (ci >= c0) {
             const int4 info = p.chunk_tab[ci];
             const size_t chd = size_t(ci) * p.H + h;
-            cp_tile_bf16(sm.A[0], LB64, p.Ah + chd * CH * CH, CH, CH, CH, tid, 128);
-            cp_tile_bf16(sm.A[1], LB64, p.Al + chd * CH * CH, CH, CH, CH, tid, 128);
-            cp_tile_bf16(sm.K[0], LB, p.Kh + chd * CH * D, D, CH, D, tid, 128);
-            cp_tile_bf16(sm.K[1], LB, p.Kl + chd * CH * D, D, CH, D, tid, 128);
+            cp_tile_bf16(sm.A[0], LB64, p.Ah + chd * CH * CH, CH, CH, CH, tid, BT);
+            cp_tile_bf16(sm.A[1], LB64, p.Al + chd * CH * CH, CH, CH, CH, tid, BT);
+            cp_tile_bf16(sm.K[0], LB, p.Kh + chd * CH * D, D, CH, D, tid, BT);
+            cp_tile_bf16(sm.K[1], LB, p.Kl + chd * CH * D, D, CH, D, tid, BT);
             __nv_bfloat16* dst = sm.dO[(c1 - 1 - ci) & 1];
-            for (int i = tid; i < CH * 8; i += 128) {
+            for (int i = tid; i < CH * 8; i += BT) {
                 const int r = i >> 3, c = (i & 7) * 8;
                 const bool ok = r < info.z;
                 const size_t row = size_t(info.y + (ok ? r : 0));
@@ -126,11 +129,11 @@ __global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
     auto issue_Y = [&](int ci) {
         if (ci >= c0) {
             const size_t chd = size_t(ci) * p.H + h;
-            cp_tile_bf16(sm.Q[0], LB, p.Qh + chd * CH * D, D, CH, D, tid, 128);
-            cp_tile_bf16(sm.Q[1], LB, p.Ql + chd * CH * D, D, CH, D, tid, 128);
-            cp_tile_bf16(sm.W[0], LB, p.Wh + chd * CH * D, D, CH, D, tid, 128);
-            cp_tile_bf16(sm.W[1], LB, p.Wl + chd * CH * D, D, CH, D, tid, 128);
-            cp_tile_f32(sm.eGL, D, p.eGL + chd * D, D, 1, D, tid, 128);
+            cp_tile_bf16(sm.Q[0], LB, p.Qh + chd * CH * D, D, CH, D, tid, BT);
+            cp_tile_bf16(sm.Q[1], LB, p.Ql + chd * CH * D, D, CH, D, tid, BT);
+            cp_tile_bf16(sm.W[0], LB, p.Wh + chd * CH * D, D, CH, D, tid, BT);
+            cp_tile_bf16(sm.W[1], LB, p.Wl + chd * CH * D, D, CH, D, tid, BT);
+            cp_tile_f32(sm.eGL, D, p.eGL + chd * D, D, 1, D, tid, BT);
         }
         cp_commit();
     };
@@ -146,10 +149,11 @@ __global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
+                for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        const int key = 32 * w + 16 * mt + g + 8 * hf, val = col0 + 8 * nt + 2 * t;
+                        const int key = 32 * wq + 16 * mt + g + 8 * hf;
+                        const int val = col0 + cq + 8 * nt + 2 * t;
                         *reinterpret_cast<float2*>(dst + size_t(key) * D + val) =
                             make_float2(dS[mt][nt][2 * hf], dS[mt][nt][2 * hf + 1]);
                     }
@@ -158,15 +162,15 @@ __global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
         cp_wait<1>();
         __syncthreads();
         {
-            float a1[8][4] = {}, a2[8][4] = {};
-            for (int ks = w; ks < 4; ++ks) {  // Aqk^T is upper triangular
+            float a1[4][4] = {}, a2[4][4] = {};
+            for (int ks = wq; ks < 4; ++ks) {  // Aqk^T is upper triangular
                 uint32_t ah[4], al[4];
-                ldsm4t(ah, at_addr(sm.A[0], LB64, 16 * w, 16 * ks, lane));
-                ldsm4t(al, at_addr(sm.A[1], LB64, 16 * w, 16 * ks, lane));
+                ldsm4t(ah, at_addr(sm.A[0], LB64, 16 * wq, 16 * ks, lane));
+                ldsm4t(al, at_addr(sm.A[1], LB64, 16 * wq, 16 * ks, lane));
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
+                for (int np = 0; np < 2; ++np) {
                     uint32_t b[4];
-                    ldsm4t(b, bk_addr(sdO, LB64, 16 * ks, 16 * np, lane));
+                    ldsm4t(b, bk_addr(sdO, LB64, 16 * ks, cq + 16 * np, lane));
                     mma_x2(a1[2 * np], ah, al, b[0], b[1]);
                     mma_x2(a1[2 * np + 1], ah, al, b[2], b[3]);
                 }
@@ -174,22 +178,22 @@ __global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
 #pragma unroll 2
             for (int ks = 0; ks < 8; ++ks) {
                 uint32_t ah[4], al[4];
-                ldsm4(ah, a_addr(sm.K[0], LB, 16 * w, 16 * ks, lane));
-                ldsm4(al, a_addr(sm.K[1], LB, 16 * w, 16 * ks, lane));
+                ldsm4(ah, a_addr(sm.K[0], LB, 16 * wq, 16 * ks, lane));
+                ldsm4(al, a_addr(sm.K[1], LB, 16 * wq, 16 * ks, lane));
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
+                for (int np = 0; np < 2; ++np) {
                     uint32_t bh[4], bl[4];
-                    ldsm4t(bh, bk_addr(sm.dS[0], LB64, 16 * ks, 16 * np, lane));
-                    ldsm4t(bl, bk_addr(sm.dS[1], LB64, 16 * ks, 16 * np, lane));
+                    ldsm4t(bh, bk_addr(sm.dS[0], LB64, 16 * ks, cq + 16 * np, lane));
+                    ldsm4t(bl, bk_addr(sm.dS[1], LB64, 16 * ks, cq + 16 * np, lane));
                     mma_x3(a2[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
                     mma_x3(a2[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
                 }
             }
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const int row = 16 * w + g + 8 * hf, col = 8 * nt + 2 * t;
+                    const int row = 16 * wq + g + 8 * hf, col = cq + 8 * nt + 2 * t;
                     const float d0 = fmaf(p.scale, a1[nt][2 * hf], a2[nt][2 * hf]);
                     const float d1 = fmaf(p.scale, a1[nt][2 * hf + 1], a2[nt][2 * hf + 1]);
                     uint32_t hi, lo;
@@ -210,36 +214,43 @@ __global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float eg = sm.eGL[32 * w + 16 * mt + g + 8 * (e >> 1)];
+                const float eg = sm.eGL[32 * wq + 16 * mt + g + 8 * (e >> 1)];
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) dS[mt][nt][e] *= eg;
+                for (int nt = 0; nt < 4; ++nt) dS[mt][nt][e] *= eg;
             }
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            float tq[8][4] = {};
+        {
+            float tq[2][4][4] = {};
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                uint32_t qh[4], ql[4], wh[4], wl[4];
-                ldsm4t(qh, at_addr(sm.Q[0], LB, 32 * w + 16 * mt, 16 * ks, lane));
-                ldsm4t(ql, at_addr(sm.Q[1], LB, 32 * w + 16 * mt, 16 * ks, lane));
-                ldsm4t(wh, at_addr(sm.W[0], LB, 32 * w + 16 * mt, 16 * ks, lane));
-                ldsm4t(wl, at_addr(sm.W[1], LB, 32 * w + 16 * mt, 16 * ks, lane));
+                uint32_t qh[2][4], ql[2][4], wh[2][4], wl[2][4];
 #pragma unroll
-                for (int np = 0; np < 4; ++np) {
+                for (int mt = 0; mt < 2; ++mt) {
+                    ldsm4t(qh[mt], at_addr(sm.Q[0], LB, 32 * wq + 16 * mt, 16 * ks, lane));
+                    ldsm4t(ql[mt], at_addr(sm.Q[1], LB, 32 * wq + 16 * mt, 16 * ks, lane));
+                    ldsm4t(wh[mt], at_addr(sm.W[0], LB, 32 * wq + 16 * mt, 16 * ks, lane));
+                    ldsm4t(wl[mt], at_addr(sm.W[1], LB, 32 * wq + 16 * mt, 16 * ks, lane));
+                }
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
                     uint32_t b[4], xh[4], xl[4];
-                    ldsm4t(b, bk_addr(sdO, LB64, 16 * ks, 16 * np, lane));
-                    ldsm4t(xh, bk_addr(sm.X[0], LB64, 16 * ks, 16 * np, lane));
-                    ldsm4t(xl, bk_addr(sm.X[1], LB64, 16 * ks, 16 * np, lane));
-                    mma_x2(tq[2 * np], qh, ql, b[0], b[1]);
-                    mma_x2(tq[2 * np + 1], qh, ql, b[2], b[3]);
-                    mma_x3(dS[mt][2 * np], wh, wl, xh[0], xh[1], xl[0], xl[1]);
-                    mma_x3(dS[mt][2 * np + 1], wh, wl, xh[2], xh[3], xl[2], xl[3]);
+                    ldsm4t(b, bk_addr(sdO, LB64, 16 * ks, cq + 16 * np, lane));
+                    ldsm4t(xh, bk_addr(sm.X[0], LB64, 16 * ks, cq + 16 * np, lane));
+                    ldsm4t(xl, bk_addr(sm.X[1], LB64, 16 * ks, cq + 16 * np, lane));
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        mma_x2(tq[mt][2 * np], qh[mt], ql[mt], b[0], b[1]);
+                        mma_x2(tq[mt][2 * np + 1], qh[mt], ql[mt], b[2], b[3]);
+                        mma_x3(dS[mt][2 * np], wh[mt], wl[mt], xh[0], xh[1], xl[0], xl[1]);
+                        mma_x3(dS[mt][2 * np + 1], wh[mt], wl[mt], xh[2], xh[3], xl[2], xl[3]);
+                    }
                 }
             }
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) dS[mt][nt][e] = fmaf(p.scale, tq[nt][e], dS[mt][nt][e]);
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dS[mt][nt][e] = fmaf(p.scale, tq[mt][nt][e], dS[mt][nt][e]);
         }
         __syncthreads();
         issue_Y(ci - 1);
@@ -252,10 +263,11 @@ __global__ void __launch_bounds__(128) k_chain_bwd(Params p, int mode) {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const int key = 32 * w + 16 * mt + g + 8 * hf, val = col0 + 8 * nt + 2 * t;
+                    const int key = 32 * wq + 16 * mt + g + 8 * hf;
+                    const int val = col0 + cq + 8 * nt + 2 * t;
                     *reinterpret_cast<float2*>(out + size_t(key) * D + val) =
                         make_float2(dS[mt][nt][2 * hf], dS[mt][nt][2 * hf + 1]);
                 }

@@ -268,7 +268,7 @@ size_t chain_fwd_smem_bytes();
 size_t chain_bwd_smem_bytes();
 size_t bwd_gemm_smem_bytes();
 size_t bwd_intra_smem_bytes();
-constexpr int CHAIN_THREADS = 128;  // 4 warps per state-recurrence block
+constexpr int CHAIN_THREADS = 256;  // 8 warps per state-recurrence block
 constexpr int BI_THREADS = 512;     // threads of the backward intra-chunk kernel
 constexpr int INTRA_THREADS = 512;  // threads of the forward intra-chunk kernel
 constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences

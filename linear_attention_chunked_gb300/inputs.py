@@ -13,6 +13,7 @@ Workloads (documents packed back to back, head dim 128, chunk 64):
   1doc      16384 tokens, 64 heads, g form, g = logsigmoid(N(0,1))/8, fused L2 norm of raw
             q,k ~ N(0,1)
   4doc      8192/4096/3072/1024 tokens, 64 heads, raw form as R2, unit q,k
+  4doc-h16  the same with 16 heads (profiling case)
   longpack  120000/70000/40000/19856 tokens, 16 heads, g form /16, unit q,k; 8 fragments per doc
 In every workload v, dO ~ N(0,1), beta = sigmoid(N(0,1)), zero initial state.
 """
@@ -58,6 +59,8 @@ WORKLOADS = {
                        A_log_range=(math.log(8.0), math.log(32.0))),
     "1doc": Workload("1doc", (16384,), 64, "g", True, 8.0),
     "4doc": Workload("4doc", (8192, 4096, 3072, 1024), 64, "raw", False),
+    # 4doc with 16 heads: the profiling case (inputs still larger than L2, a quarter of the units)
+    "4doc-h16": Workload("4doc-h16", (8192, 4096, 3072, 1024), 16, "raw", False),
     "longpack": Workload("longpack", (120000, 70000, 40000, 19856), 16, "g", False, 16.0,
                          fragments=8),
 }

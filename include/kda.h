@@ -67,7 +67,8 @@ typedef enum kda_status {
     KDA_ERR_WORKSPACE = 3,    /* workspace (or saved buffer) smaller than the size query says */
     KDA_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch error) */
     KDA_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (reported via device status) */
-    KDA_ERR_DEVICE_CHECK = 6  /* device-side validation failed (e.g. malformed cu_seqlens) */
+    KDA_ERR_DEVICE_CHECK = 6, /* device-side validation failed (e.g. malformed cu_seqlens) */
+    KDA_ERR_TOO_LARGE = 7     /* problem needs more scratch than kda_fwd_static_ws holds */
 } kda_status;
 
 typedef enum kda_gate_form {
@@ -117,6 +118,30 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
                    const void* beta, const float* g_or_a, const float* A_log,
                    const float* dt_bias, const float* h0, void* o, float* ht, void* saved,
                    void* ws, size_t ws_bytes, kda_stream_t stream);
+
+/* Allocation-free forward for callers that cannot allocate device memory themselves -- e.g. code
+ * that runs where the framework owns every device allocation and offers no workspace (a plugin
+ * or op inside a host runtime), or code that must not grow the memory footprint behind the
+ * caller's allocator.  It computes exactly what kda_fwd computes with saved == NULL (o and,
+ * when non-NULL, ht), but its scratch lives in one static device array inside this library:
+ * KDA_STATIC_WS_BYTES (64 MiB) on every GPU that loads the library, held until the process exits.
+ * The pages describe no such entry point; it has no counterpart there.
+ *  - Problems whose kda_fwd workspace (kda_workspace_size, KDA_OP_FWD) exceeds
+ *    KDA_STATIC_WS_BYTES are rejected with KDA_ERR_TOO_LARGE before anything is launched
+ *    (roughly: (ceil(T/64) + N) * H <= 300 (chunk, head) pairs, e.g. 4096 tokens x 4 heads).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *    that device current; make that first call before any stream capture.  It allocates nothing:
+ *    no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - Every call shares the one array, which keeps the previous call's contents (nothing in it
+ *    needs to start at zero).  Calls that may overlap on the GPU -- on different streams, or from
+ *    several host threads -- race on it; serialise them on one stream.
+ *  - Device status (malformed cu_seqlens) is not readable through kda_read_device_status, which
+ *    needs the workspace pointer; the outputs are then left unwritten. */
+#define KDA_STATIC_WS_BYTES ((size_t)64 << 20)
+kda_status kda_fwd_static_ws(const kda_problem* p, const void* q, const void* k, const void* v,
+                             const void* beta, const float* g_or_a, const float* A_log,
+                             const float* dt_bias, const float* h0, void* o, float* ht,
+                             kda_stream_t stream);
 
 /* Backward of L = sum(o * dO) + sum(ht * dht) for the same inputs as kda_fwd.
  * saved: the set written by kda_fwd for exactly these inputs, or NULL to recompute the forward

@@ -159,6 +159,12 @@ kda_status run_prologue(const Params& p, cudaStream_t st) {
     return launched();
 }
 
+// Scratch of the allocation-free forward (kda_fwd_static_ws): one static array per device that
+// loads this library.  Host code must not use the symbol as an address; the device address is
+// looked up once per device with cudaGetSymbolAddress.
+__device__ __align__(256) unsigned char g_static_ws[KDA_STATIC_WS_BYTES];
+void* g_static_ws_ptr[128];
+
 }  // namespace
 
 extern "C" {
@@ -172,6 +178,8 @@ const char* kda_status_string(kda_status s) {
         case KDA_ERR_CUDA: return "CUDA runtime error";
         case KDA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
         case KDA_ERR_DEVICE_CHECK: return "device-side validation failed (malformed cu_seqlens)";
+        case KDA_ERR_TOO_LARGE:
+            return "problem needs more scratch than the allocation-free forward holds (KDA_STATIC_WS_BYTES)";
     }
     return "unknown status";
 }
@@ -218,6 +226,30 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
         k_chain_fwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD, st>>>(p, CHAIN_FWD_OUT);
     }
     return launched();
+}
+
+kda_status kda_fwd_static_ws(const kda_problem* pr, const void* q, const void* k, const void* v,
+                             const void* beta, const float* g_or_a, const float* A_log,
+                             const float* dt_bias, const float* h0, void* o, float* ht,
+                             kda_stream_t stream) {
+    if (kda_status s = check_problem(pr)) return s;
+    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    if (L.ws_fwd > KDA_STATIC_WS_BYTES) return KDA_ERR_TOO_LARGE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev < 0 || dev >= 128) return KDA_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_static_ws_ptr[dev]) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return KDA_ERR_CUDA;
+            g_static_ws_ptr[dev] = ptr;
+        }
+        ws = g_static_ws_ptr[dev];
+    }
+    return kda_fwd(pr, q, k, v, beta, g_or_a, A_log, dt_bias, h0, o, ht, nullptr, ws,
+                   KDA_STATIC_WS_BYTES, stream);
 }
 
 kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const void* v,

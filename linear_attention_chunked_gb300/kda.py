@@ -18,12 +18,13 @@ D = 128
 CHUNK = 64
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE = 0, 1, 2, 3
-KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE_CHECK = 4, 5, 6
+KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE_CHECK, KDA_ERR_TOO_LARGE = 4, 5, 6, 7
+KDA_STATIC_WS_BYTES = 64 << 20
 KDA_GATE_G, KDA_GATE_RAW = 0, 1
 KDA_OP_FWD, KDA_OP_BWD_SAVED, KDA_OP_BWD_REPLAY, KDA_OP_FRAGMENT, KDA_OP_WALK = 0, 1, 2, 3, 4
 KDA_FRAG_FWD, KDA_FRAG_BWD = 0, 1
 
-EXPORTS = ("kda_workspace_size", "kda_fwd", "kda_bwd", "kda_fragment_summary",
+EXPORTS = ("kda_workspace_size", "kda_fwd", "kda_fwd_static_ws", "kda_bwd", "kda_fragment_summary",
            "kda_transfer_walk", "kda_read_device_status", "kda_profile_enable",
            "kda_profile_collect", "kda_kernel_count", "kda_kernel_name", "kda_launch_counter",
            "kda_status_string")
@@ -63,6 +64,7 @@ def lib():
             P, I, S, V = ctypes.POINTER(kda_problem), ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
             L.kda_workspace_size.argtypes = [P, I, ctypes.POINTER(S), ctypes.POINTER(S)]
             L.kda_fwd.argtypes = [P] + [V] * 11 + [V, S, V]
+            L.kda_fwd_static_ws.argtypes = [P] + [V] * 10 + [V]
             L.kda_bwd.argtypes = [P] + [V] * 19 + [V, S, V]
             L.kda_fragment_summary.argtypes = [P, I] + [V] * 10 + [V, S, V]
             L.kda_transfer_walk.argtypes = [ctypes.c_int32, V, ctypes.c_int32, ctypes.c_int32,
@@ -77,7 +79,7 @@ def lib():
             L.kda_launch_counter.restype = ctypes.c_uint64
             L.kda_status_string.argtypes = [I]
             L.kda_status_string.restype = ctypes.c_char_p
-            for name in ("kda_workspace_size", "kda_fwd", "kda_bwd", "kda_fragment_summary",
+            for name in ("kda_workspace_size", "kda_fwd", "kda_fwd_static_ws", "kda_bwd", "kda_fragment_summary",
                          "kda_transfer_walk", "kda_read_device_status", "kda_profile_enable",
                          "kda_profile_collect", "kda_kernel_count"):
                 getattr(L, name).restype = ctypes.c_int
@@ -164,6 +166,28 @@ def kda_fwd(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=
                            _ptr(ws), ws.numel(), _stream(dev))
     _check("kda_fwd", st)
     return o, ht, saved
+
+
+def kda_fwd_static_ws(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=None,
+                      h0=None, l2norm=False, scale=1.0, eps=1e-6, out_dtype=torch.float32,
+                      o=None, ht=None):
+    """Forward through the allocation-free entry point (its scratch is a static device array of
+    the library).  Returns (o, ht).  The output tensors are the caller's (allocated here when not
+    given, as any caller would); the library itself allocates nothing."""
+    T, N, H, d = _shape(q, cu_seqlens)
+    dev = q.device
+    pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d,
+                      out_dtype=out_dtype)
+    if o is None:
+        o = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    if ht is None:
+        ht = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().kda_fwd_static_ws(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                     _ptr(g_or_a), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(o),
+                                     _ptr(ht), _stream(dev))
+    _check("kda_fwd_static_ws", st)
+    return o, ht
 
 
 def kda_bwd(q, k, v, beta, g_or_a, cu_seqlens, dO, *, saved=None, gate="g", A_log=None,

@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true", help="skip the per-kernel event pass")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-configuration rows")
     return ap.parse_args()
 
 
@@ -54,6 +55,22 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def reduce_max_ms(ms, world, device):
+    """Max over ranks of a per-rank time (the slowest rank sets the step time)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, max_ms):
+    """Whole-job tokens/s: every rank processes its own batch (weak scaling)."""
+    return world * tokens_per_rank / (max_ms / 1e3)
 
 
 def load_peaks():
@@ -148,6 +165,91 @@ def traffic_for(kernel, workload):
             if k == kernel and w == workload and s == sha:
                 return float(byts)
     return None
+
+
+# ---------------------------------------------------------------------------------------------
+# per-configuration rows: fwd and fwd+bwd ms (median of 5 samples, each 5 back-to-back calls / 5)
+
+ROWS = [("m2", "saved"), ("R2", "saved"), ("R2fast", "saved"), ("1doc", "saved"),
+        ("4doc", "saved"), ("4doc", "replay"), ("longpack", "saved")]
+
+
+def _time_calls(fn, samples=5, calls=5):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(samples):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(calls):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b) / calls)
+    return statistics.median(out)
+
+
+def run_rows(dev):
+    import torch
+    from linear_attention_chunked_gb300 import inputs, kda
+    rows = {}
+    for name, mode in ROWS:
+        w = inputs.WORKLOADS[name]
+        x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inputs.workload_inputs(name).items()}
+        kw = dict(gate=w.gate, A_log=x["A_log"], dt_bias=x["dt_bias"], l2norm=w.l2norm)
+        if w.fragments:
+            frag, doc_frag = [], [0]
+            for L in w.lens:
+                pieces = inputs.fragment_lens(L, w.fragments)
+                frag += pieces
+                doc_frag.append(doc_frag[-1] + len(pieces))
+            fcu = inputs.cu_from_lens(frag).to(dev)
+            dfr = torch.tensor(doc_frag, dtype=torch.int32, device=dev)
+            a = (x["q"], x["k"], x["v"], x["beta"], x["g"], fcu)
+            T, F, H = w.T, len(frag), w.H
+            wsf, svb = kda.kda_workspace_size(T, F, H, kda.KDA_OP_FWD)
+            wsb, _ = kda.kda_workspace_size(T, F, H, kda.KDA_OP_BWD_SAVED)
+            ws = torch.empty(max(wsf, wsb), dtype=torch.uint8, device=dev)
+            saved = torch.empty(svb, dtype=torch.uint8, device=dev)
+            st = {}
+
+            def fwd():
+                M, B = kda.kda_fragment_summary(*a, mode=kda.KDA_FRAG_FWD, ws=ws, **kw)
+                S_in, S_fin = kda.kda_transfer_walk(dfr, M, B)
+                o, _, _ = kda.kda_fwd(*a, h0=S_in, saved=saved, ws=ws, **kw)
+                st.update(M=M, S_in=S_in)
+
+            def fwd_bwd():
+                fwd()
+                C = kda.kda_fragment_summary(*a, mode=kda.KDA_FRAG_BWD, dO=x["dO"], ws=ws, **kw)
+                dS_end, dh0 = kda.kda_transfer_walk(dfr, st["M"], C, reverse=True)
+                kda.kda_bwd(*a, x["dO"], saved=saved, h0=st["S_in"], dht=dS_end, want_dh0=False,
+                            ws=ws, **kw)
+        else:
+            a = (x["q"], x["k"], x["v"], x["beta"], x["g"], x["cu_seqlens"])
+            T, N, H = w.T, w.N, w.H
+            replay = mode == "replay"
+            wsf, svb = kda.kda_workspace_size(T, N, H, kda.KDA_OP_FWD)
+            wsb, _ = kda.kda_workspace_size(T, N, H, kda.KDA_OP_BWD_REPLAY if replay else
+                                            kda.KDA_OP_BWD_SAVED)
+            ws = torch.empty(max(wsf, wsb), dtype=torch.uint8, device=dev)
+            saved = None if replay else torch.empty(svb, dtype=torch.uint8, device=dev)
+
+            def fwd():
+                kda.kda_fwd(*a, saved=saved, save=not replay, ws=ws, **kw)
+
+            def fwd_bwd():
+                fwd()
+                kda.kda_bwd(*a, x["dO"], saved=saved, want_dh0=False, ws=ws, **kw)
+        f_ms = _time_calls(fwd)
+        fb_ms = _time_calls(fwd_bwd)
+        rows[f"{w.row}:{mode}"] = {"T": w.T, "H": w.H, "fwd_ms": round(f_ms, 4),
+                                   "fwd_bwd_ms": round(fb_ms, 4),
+                                   "fwd_bwd_tokens_per_s": round(w.T / (fb_ms / 1e3))}
+        del x, ws, saved
+        torch.cuda.empty_cache()
+    return rows
 
 
 # ---------------------------------------------------------------------------------------------
@@ -276,34 +378,31 @@ def main():
     barrier()
     ck = clocks.stop()
     launches = kda.kda_launch_counter() - launches0
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms / 1e3)
+    ms = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dev)
+    value = job_throughput(T, world, ms)
 
     # ---- per-kernel device time (second pass, CUDA events around every launch) ----
-    kda.kda_profile_enable(True)
-    for _ in range(args.steps):
-        step(inp)
-    torch.cuda.synchronize()
-    kda.kda_profile_enable(False)
-    prof = kda.kda_profile_collect()
-    kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
-               for k, v in prof.items() if v[1]}
-    dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
-    hbm, bf16, src = load_peaks()
-    per_th = alg_bytes_per_token_head(dom)
-    roof = None
-    if per_th is not None:
-        launch_ms = kernels[dom]["ms_per_step"] / kernels[dom]["launches_per_step"]
-        byts = per_th * T * H
-        achieved = byts / (launch_ms / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "peak_source": src,
-                "alg_bytes_per_launch": byts, "launch_ms": launch_ms,
-                "traffic": traffic_for(dom, args.workload)}
+    kernels, roof = {}, None
+    if not args.no_profile:
+        kda.kda_profile_enable(True)
+        for _ in range(args.steps):
+            step(inp)
+        torch.cuda.synchronize()
+        kda.kda_profile_enable(False)
+        prof = kda.kda_profile_collect()
+        kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                   for k, v in prof.items() if v[1]}
+        dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+        hbm, bf16, src = load_peaks()
+        per_th = alg_bytes_per_token_head(dom)
+        if per_th is not None:
+            launch_ms = kernels[dom]["ms_per_step"] / kernels[dom]["launches_per_step"]
+            byts = per_th * T * H
+            achieved = byts / (launch_ms / 1e3) / 1e9
+            roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
+                    "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
+                    "alg_bytes_per_launch": byts, "launch_ms": launch_ms,
+                    "traffic": traffic_for(dom, args.workload)}
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -334,13 +433,13 @@ def main():
         a1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = a0.elapsed_time(a1) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * T / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+        ems = reduce_max_ms(a0.elapsed_time(a1) / args.steps, world, dev)
+        e2e = {"value": job_throughput(T, world, ems), "unit": "tokens/s", "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = run_rows(dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -363,6 +462,7 @@ def main():
             "roofline": roof,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "rows": rows,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

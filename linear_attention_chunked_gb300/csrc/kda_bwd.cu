@@ -58,6 +58,9 @@ __device__ __forceinline__ void split_tile(__nv_bfloat16* hi, __nv_bfloat16* lo,
     }
 }
 
+static_assert(sizeof(ChainBwdSmem) <= 232448, "chain shared memory above the opt-in limit");
+static_assert(sizeof(BwdGemmSmem) <= 232448, "backward GEMM shared memory above the opt-in limit");
+
 }  // namespace
 
 size_t chain_bwd_smem_bytes() { return sizeof(ChainBwdSmem); }
@@ -471,8 +474,12 @@ struct BwdIntraSmem {
     __nv_bfloat16 qb[CH * LB], kb[CH * LB];          // q, k as given (bf16); q^ = q * rq
     float dA[CH * LAS], dAk[CH * LAS];               // dAqk and dAkk = beta_r dM
     float beta[CH], rq[CH], rk[CH];
-    float red[2 * BI_THREADS];
+    union {
+        uint4 Af[24][2][32];         // split A fragments of dAqk / dAkk (fragment order), step 3
+        float red[2 * BI_THREADS];   // reduction scratch, steps 5 and 7
+    };
 };
+static_assert(sizeof(BwdIntraSmem) <= 232448, "backward intra shared memory above the opt-in limit");
 
 }  // namespace
 
@@ -583,21 +590,60 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int i = tid + BT * k, r = i >> 5, c0 = (i & 31) * 4;
-            const float dgn = S.dA[r * LAS + r], br = S.beta[r];
+            const float dgn = S.dA[r * LAS + r], br = S.beta[r], rqr = S.rq[r], rkr = S.rk[r];
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LDP + c0]);
+            const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LDP + c0]);
+            const uint2 qb2 = *reinterpret_cast<const uint2*>(&S.qb[r * LB + c0]);
+            const uint2 kb2 = *reinterpret_cast<const uint2*>(&S.kb[r * LB + c0]);
+            __nv_bfloat162 qa, qb_, ka, kb_;
+            memcpy(&qa, &qb2.x, 4);
+            memcpy(&qb_, &qb2.y, 4);
+            memcpy(&ka, &kb2.x, 4);
+            memcpy(&kb_, &kb2.y, 4);
+            const float2 q01 = __bfloat1622float2(qa), q23 = __bfloat1622float2(qb_);
+            const float2 k01 = __bfloat1622float2(ka), k23 = __bfloat1622float2(kb_);
+            const float gvv[4] = {g4.x, g4.y, g4.z, g4.w}, glv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float qv4[4] = {q01.x * rqr, q01.y * rqr, q23.x * rqr, q23.y * rqr};
+            const float kv4[4] = {k01.x * rkr, k01.y * rkr, k23.x * rkr, k23.y * rkr};
             const float aq[4] = {vq[k].x, vq[k].y, vq[k].z, vq[k].w};
             const float ap[4] = {vp[k].x, vp[k].y, vp[k].z, vp[k].w};
             const float ab[4] = {vb[k].x, vb[k].y, vb[k].z, vb[k].w};
+            float oq[4], ok[4], og[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int c = c0 + j;
-                const float gv = S.gam[r * LDP + c], gl = S.gam[(CH - 1) * LDP + c];
-                const float er = __expf(gv), eb = __expf(gl - gv);
-                const float qv = Qv(r, c), kv = Kv(r, c);
+                const float er = __expf(gvv[j]), eb = __expf(glv[j] - gvv[j]);
+                const float qv = qv4[j], kv = kv4[j];
                 const float dqg = aq[j], dkg = -br * ap[j], dkb = ab[j];
-                S.dQ[r * LDP + c] = fmaf(dqg, er, dgn * kv);
-                S.dK[r * LDP + c] = fmaf(dkg, er, fmaf(dkb, eb, dgn * qv));
-                S.dG[r * LDP + c] = (dqg * qv + dkg * kv) * er - dkb * kv * eb;
+                oq[j] = fmaf(dqg, er, dgn * kv);
+                ok[j] = fmaf(dkg, er, fmaf(dkb, eb, dgn * qv));
+                og[j] = (dqg * qv + dkg * kv) * er - dkb * kv * eb;
             }
+            *reinterpret_cast<float4*>(&S.dQ[r * LDP + c0]) = make_float4(oq[0], oq[1], oq[2], oq[3]);
+            *reinterpret_cast<float4*>(&S.dK[r * LDP + c0]) = make_float4(ok[0], ok[1], ok[2], ok[3]);
+            *reinterpret_cast<float4*>(&S.dG[r * LDP + c0]) = make_float4(og[0], og[1], og[2], og[3]);
+        }
+    }
+    // split A fragments of dAqk and dAkk, built once: 12 "as row" (i, ks<i) and 12 "as column"
+    // (j, ks>j) fragments, index = 2 * pair + (0: dAqk, 1: dAkk)
+    {
+        constexpr int2 kRow[6] = {{1, 0}, {2, 0}, {2, 1}, {3, 0}, {3, 1}, {3, 2}};
+        constexpr int2 kCol[6] = {{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}, {2, 3}};
+        for (int f = w; f < 24; f += NW) {
+            const bool col = f >= 12;
+            const int pi = (f % 12) >> 1, src = f & 1;
+            const float* A = src ? S.dAk : S.dA;
+            const int m0 = 16 * (col ? kCol[pi].x : kRow[pi].x);
+            const int k0 = 16 * (col ? kCol[pi].y : kRow[pi].y);
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int m = m0 + g + 8 * (rr & 1), kx = k0 + 2 * t + 8 * (rr >> 1);
+                const float x0 = col ? A[kx * LAS + m] : A[m * LAS + kx];
+                const float x1 = col ? A[(kx + 1) * LAS + m] : A[m * LAS + kx + 1];
+                split2(x0, x1, hi[rr], lo[rr]);
+            }
+            S.Af[f][0][lane] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            S.Af[f][1][lane] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
     }
     __syncthreads();
@@ -605,26 +651,21 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
     // 3. contractions across sub-chunks on tensor cores; warp w owns channels 8w..8w+7
     {
         const int c = 8 * w + g;  // B-fragment column of this lane
-        auto a_frag = [&](const float* src, bool tr, int m0, int k0, uint32_t (&hi)[4],
-                          uint32_t (&lo)[4]) {
-            // element (m, kx) of the A operand: src[m][kx] (tr = false) or src[kx][m] (tr = true)
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const int m = m0 + g + 8 * (rr & 1), kx = k0 + 2 * t + 8 * (rr >> 1);
-                const float x0 = tr ? src[kx * LAS + m] : src[m * LAS + kx];
-                const float x1 = tr ? src[(kx + 1) * LAS + m] : src[m * LAS + kx + 1];
-                split2(x0, x1, hi[rr], lo[rr]);
-            }
+        auto afrag = [&](int f, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+            const uint4 h4 = S.Af[f][0][lane], l4 = S.Af[f][1][lane];
+            hi[0] = h4.x; hi[1] = h4.y; hi[2] = h4.z; hi[3] = h4.w;
+            lo[0] = l4.x; lo[1] = l4.y; lo[2] = l4.z; lo[3] = l4.w;
         };
         // "as row": destination sub-chunk i = 1..3, reference row 16 i
+        int pair = 0;
         for (int i = 1; i < 4; ++i) {
             const int ref = 16 * i;
             const float gr = S.gam[ref * LDP + c];
             float aq[4] = {}, ak[4] = {};
-            for (int ks = 0; ks < i; ++ks) {
+            for (int ks = 0; ks < i; ++ks, ++pair) {
                 uint32_t qh[4], ql[4], kh[4], kl[4], bh[2], bl[2];
-                a_frag(S.dA, false, 16 * i, 16 * ks, qh, ql);
-                a_frag(S.dAk, false, 16 * i, 16 * ks, kh, kl);
+                afrag(2 * pair, qh, ql);
+                afrag(2 * pair + 1, kh, kl);
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int s0 = 16 * ks + 2 * t + 8 * hf;
@@ -646,14 +687,15 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
             }
         }
         // "as column": destination sub-chunk j = 0..2, reference row 16 j + 15
+        pair = 6;
         for (int j = 0; j < 3; ++j) {
             const int ref = 16 * j + 15;
             const float gr = S.gam[ref * LDP + c];
             float bacc[4] = {};
-            for (int ks = j + 1; ks < 4; ++ks) {
+            for (int ks = j + 1; ks < 4; ++ks, ++pair) {
                 uint32_t qh[4], ql[4], kh[4], kl[4], qbh[2], qbl[2], kbh[2], kbl[2];
-                a_frag(S.dA, true, 16 * j, 16 * ks, qh, ql);
-                a_frag(S.dAk, true, 16 * j, 16 * ks, kh, kl);
+                afrag(2 * pair, qh, ql);
+                afrag(2 * pair + 1, kh, kl);
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int r0 = 16 * ks + 2 * t + 8 * hf;

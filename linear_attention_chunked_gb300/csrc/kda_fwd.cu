@@ -54,6 +54,8 @@ struct ChainFwdSmem {
     float eGL[D];                   // e^gL per key
 };
 
+static_assert(sizeof(ChainFwdSmem) <= 232448, "chain shared memory above the opt-in limit");
+
 }  // namespace
 
 size_t chain_fwd_smem_bytes() { return sizeof(ChainFwdSmem); }

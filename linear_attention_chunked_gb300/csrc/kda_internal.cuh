@@ -25,7 +25,8 @@ constexpr int CH = 64;       // chunk length
 constexpr int NTHR = 256;    // threads per block of the chunk kernels
 constexpr int SLICE = 32;    // value columns per block of the state-recurrence kernels
 constexpr int NSLICE = D / SLICE;
-constexpr int LDP = D + 1;   // padded row stride (floats) of [64 x 128] shared tiles
+constexpr int LDP = D + 4;   // row stride (floats) of [64 x 128] shared tiles: 16-byte aligned rows,
+                             // conflict-free float4 access for row-varying lanes
 constexpr int LDA = CH + 1;  // padded row stride of [64 x 64] shared tiles
 
 // Byte offsets of every region of the workspace / saved buffers.  Everything is derived from
@@ -159,9 +160,20 @@ __device__ __forceinline__ void store_out(void* base, size_t i, float v, int fp3
     else static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
 }
 
-// softplus(x) = log(1 + e^x); for x > 20 the correction log1p(e^-x) < 2.1e-9 is below fp32
-// resolution of x and is dropped.
-__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(u), u = e^-|x| in (0, 1].  log1p(u) is taken as
+// 2 atanh(z) with z = u / (2 + u) in (0, 1/3]: 2 (z + z^3/3 + ... + z^13/13) has relative
+// truncation error below (1/3)^14 / 15 < 1e-7, i.e. FP32-accurate without the library log1p.
+__device__ __forceinline__ float softplus_f(float x) {
+    const float u = __expf(-fabsf(x));
+    const float z = __fdividef(u, 2.f + u), z2 = z * z;
+    float pz = fmaf(z2, 1.f / 13.f, 1.f / 11.f);
+    pz = fmaf(z2, pz, 1.f / 9.f);
+    pz = fmaf(z2, pz, 1.f / 7.f);
+    pz = fmaf(z2, pz, 1.f / 5.f);
+    pz = fmaf(z2, pz, 1.f / 3.f);
+    pz = fmaf(z2, pz, 1.f);
+    return fmaxf(x, 0.f) + 2.f * z * pz;
+}
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -25,6 +25,7 @@ struct IntraSmem {
         struct {
             __nv_bfloat16 Ks[3][2][16 * LB];  // B operands of the off-diagonal blocks (hi, lo)
             float T[3][16 * 17];              // blockwise inverse scratch
+            float P[6][16 * 32];              // partial off-diagonal sums of the K-split warps
         } a;
         struct {
             __nv_bfloat16 bKg[2][CH * LB];  // beta K e^gam (hi, lo)
@@ -42,6 +43,8 @@ __device__ __forceinline__ int tri_row(int pi) {  // row of the pi-th entry of a
     while (r * (r + 1) / 2 > pi) --r;
     return r;
 }
+
+static_assert(sizeof(IntraSmem) <= 232448, "intra shared memory above the opt-in limit");
 
 }  // namespace
 
@@ -88,26 +91,32 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
             const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
             const __nv_bfloat162* bq = reinterpret_cast<const __nv_bfloat162*>(&vq[k]);
             const __nv_bfloat162* bk = reinterpret_cast<const __nv_bfloat162*>(&vk[k]);
+            float fq[8], fk[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float2 fq = __bfloat1622float2(bq[j]), fk = __bfloat1622float2(bk[j]);
-                S.q[r * LDP + c8 + 2 * j] = fq.x;
-                S.q[r * LDP + c8 + 2 * j + 1] = fq.y;
-                S.k[r * LDP + c8 + 2 * j] = fk.x;
-                S.k[r * LDP + c8 + 2 * j + 1] = fk.y;
+                const float2 a = __bfloat1622float2(bq[j]), b = __bfloat1622float2(bk[j]);
+                fq[2 * j] = a.x;
+                fq[2 * j + 1] = a.y;
+                fk[2 * j] = b.x;
+                fk[2 * j + 1] = b.y;
             }
+            float4* dq = reinterpret_cast<float4*>(&S.q[r * LDP + c8]);
+            float4* dk = reinterpret_cast<float4*>(&S.k[r * LDP + c8]);
+            dq[0] = make_float4(fq[0], fq[1], fq[2], fq[3]);
+            dq[1] = make_float4(fq[4], fq[5], fq[6], fq[7]);
+            dk[0] = make_float4(fk[0], fk[1], fk[2], fk[3]);
+            dk[1] = make_float4(fk[4], fk[5], fk[6], fk[7]);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
-            const float x[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
+            float x[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
             const float b4[4] = {db.x, db.y, db.z, db.w};
+            if (p.gate_raw) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float val = x[j];
-                if (p.gate_raw) val = r < L ? -eA * softplus_f(val + b4[j]) : 0.f;
-                S.gam[r * LDP + c4 + j] = val;
+                for (int j = 0; j < 4; ++j) x[j] = r < L ? -eA * softplus_f(x[j] + b4[j]) : 0.f;
             }
+            *reinterpret_cast<float4*>(&S.gam[r * LDP + c4]) = make_float4(x[0], x[1], x[2], x[3]);
         }
     }
     for (int i = tid; i < CH * LDA; i += BT) {
@@ -159,18 +168,28 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
         const int b = idx / 136, pi = idx % 136;
         const int rl = tri_row(pi), sl = pi - rl * (rl + 1) / 2;
         const int r = 16 * b + rl, s = 16 * b + sl;
-        float akk = 0.f, aqk = 0.f;
-        const float* gr = S.gam + r * LDP;
-        const float* gs = S.gam + s * LDP;
-        const float* kr = S.k + r * LDP;
-        const float* ks = S.k + s * LDP;
-        const float* qr = S.q + r * LDP;
-#pragma unroll 4
-        for (int c = 0; c < D; ++c) {
-            const float kse = ks[c] * __expf(gr[c] - gs[c]);
-            akk = fmaf(kr[c], kse, akk);
-            aqk = fmaf(qr[c], kse, aqk);
+        float akk = 0.f, aqk = 0.f, akk2 = 0.f, aqk2 = 0.f;
+        const float4* gr = reinterpret_cast<const float4*>(S.gam + r * LDP);
+        const float4* gs = reinterpret_cast<const float4*>(S.gam + s * LDP);
+        const float4* kr = reinterpret_cast<const float4*>(S.k + r * LDP);
+        const float4* ks = reinterpret_cast<const float4*>(S.k + s * LDP);
+        const float4* qr = reinterpret_cast<const float4*>(S.q + r * LDP);
+#pragma unroll 2
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+            const float4 a = gr[c4], b = gs[c4], ksv = ks[c4], krv = kr[c4], qrv = qr[c4];
+            const float e0 = ksv.x * __expf(a.x - b.x), e1 = ksv.y * __expf(a.y - b.y);
+            const float e2 = ksv.z * __expf(a.z - b.z), e3 = ksv.w * __expf(a.w - b.w);
+            akk = fmaf(krv.x, e0, akk);
+            aqk = fmaf(qrv.x, e0, aqk);
+            akk2 = fmaf(krv.y, e1, akk2);
+            aqk2 = fmaf(qrv.y, e1, aqk2);
+            akk = fmaf(krv.z, e2, akk);
+            aqk = fmaf(qrv.z, e2, aqk);
+            akk2 = fmaf(krv.w, e3, akk2);
+            aqk2 = fmaf(qrv.w, e3, aqk2);
         }
+        akk += akk2;
+        aqk += aqk2;
         if (s < r) S.Akk[r * LDA + s] = akk;
         S.Aqk[r * LDA + s] = aqk;
     }
@@ -184,32 +203,56 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
         S.u.a.Ks[j][1][sl * LB + c] = __float2bfloat16_rn(x - __bfloat162float(hi));
     }
     __syncthreads();
-    // 4c. off-diagonal blocks on tensor cores: warp w < 12 takes pair w / 2, n-tile w % 2
+    // 4c. off-diagonal blocks on tensor cores: warp w < 12 takes pair w / 2 and half w % 2 of the
+    //     128 channels (k-steps); the two halves are added in a fixed order
     if (warp < 12) {
-        const int pr = warp >> 1, nt = warp & 1;
+        const int pr = warp >> 1, kh = warp & 1;
         const int i = kPairs[pr].x, j = kPairs[pr].y, e = 16 * j + 15;
-        float accQ[4] = {}, accK[4] = {};
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t qh[4], ql[4], kh[4], kl[4];
+        float accQ[2][4] = {}, accK[2][4] = {};
+#pragma unroll 2
+        for (int ks = 4 * kh; ks < 4 * kh + 4; ++ks) {
+            uint32_t qh[4], ql[4], kh4[4], kl[4];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const int row = 16 * i + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
-                const float e0 = __expf(S.gam[row * LDP + col] - S.gam[e * LDP + col]);
-                const float e1 = __expf(S.gam[row * LDP + col + 1] - S.gam[e * LDP + col + 1]);
-                split2(S.q[row * LDP + col] * e0, S.q[row * LDP + col + 1] * e1, qh[rr], ql[rr]);
-                split2(S.k[row * LDP + col] * e0, S.k[row * LDP + col + 1] * e1, kh[rr], kl[rr]);
+                const float2 gr = *reinterpret_cast<const float2*>(&S.gam[row * LDP + col]);
+                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LDP + col]);
+                const float2 qv = *reinterpret_cast<const float2*>(&S.q[row * LDP + col]);
+                const float2 kv = *reinterpret_cast<const float2*>(&S.k[row * LDP + col]);
+                const float e0 = __expf(gr.x - ge.x), e1 = __expf(gr.y - ge.y);
+                split2(qv.x * e0, qv.y * e1, qh[rr], ql[rr]);
+                split2(kv.x * e0, kv.y * e1, kh4[rr], kl[rr]);
             }
             uint32_t bh[4], bl[4];
             ldsm4(bh, bn_addr(S.u.a.Ks[j][0], LB, 16 * ks, 0, lane));
             ldsm4(bl, bn_addr(S.u.a.Ks[j][1], LB, 16 * ks, 0, lane));
-            mma_x3(accQ, qh, ql, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
-            mma_x3(accK, kh, kl, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
-        }
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-            const int row = 16 * i + g + 8 * (e4 >> 1), col = 16 * j + 8 * nt + 2 * t + (e4 & 1);
-            S.Aqk[row * LDA + col] = accQ[e4];
-            S.Akk[row * LDA + col] = accK[e4];
+            for (int nt = 0; nt < 2; ++nt) {
+                mma_x3(accQ[nt], qh, ql, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
+                mma_x3(accK[nt], kh4, kl, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
+            }
+        }
+        float* part = S.u.a.P[pr];  // upper half's partial [2 n-tiles][2 (Q, K)][4] per lane
+        if (kh == 1) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    part[((nt * 2 + 0) * 4 + e4) * 32 + lane] = accQ[nt][e4];
+                    part[((nt * 2 + 1) * 4 + e4) * 32 + lane] = accK[nt][e4];
+                }
+        }
+        __syncwarp();
+        named_barrier_sync(1 + pr, 64);  // the two warps of this pair
+        if (kh == 0) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int row = 16 * i + g + 8 * (e4 >> 1), col = 16 * j + 8 * nt + 2 * t + (e4 & 1);
+                    S.Aqk[row * LDA + col] = accQ[nt][e4] + part[((nt * 2 + 0) * 4 + e4) * 32 + lane];
+                    S.Akk[row * LDA + col] = accK[nt][e4] + part[((nt * 2 + 1) * 4 + e4) * 32 + lane];
+                }
         }
     }
     __syncthreads();
@@ -271,8 +314,10 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
         }
         for (int i = tid; i < CH * D / 2; i += BT) {
             const int r = (2 * i) / D, c = (2 * i) % D;
-            const float x0 = S.beta[r] * S.k[r * LDP + c] * __expf(S.gam[r * LDP + c]);
-            const float x1 = S.beta[r] * S.k[r * LDP + c + 1] * __expf(S.gam[r * LDP + c + 1]);
+            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
+            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
+            const float x0 = S.beta[r] * kv.x * __expf(gv.x);
+            const float x1 = S.beta[r] * kv.y * __expf(gv.y);
             uint32_t hi, lo;
             split2(x0, x1, hi, lo);
             *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
@@ -338,13 +383,16 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
         float* gam = p.gam + chd * CH * D;
         for (int i = tid; i < CH * D / 2; i += BT) {
             const int r = (2 * i) / D, c = (2 * i) % D;
-            const float g0 = S.gam[r * LDP + c], g1 = S.gam[r * LDP + c + 1];
-            const float gl0 = S.gam[(CH - 1) * LDP + c], gl1 = S.gam[(CH - 1) * LDP + c + 1];
+            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
+            const float2 gl = *reinterpret_cast<const float2*>(&S.gam[(CH - 1) * LDP + c]);
+            const float2 qv = *reinterpret_cast<const float2*>(&S.q[r * LDP + c]);
+            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
+            const float g0 = gv.x, g1 = gv.y;
             uint32_t hi, lo;
-            split2(S.q[r * LDP + c] * __expf(g0), S.q[r * LDP + c + 1] * __expf(g1), hi, lo);
+            split2(qv.x * __expf(g0), qv.y * __expf(g1), hi, lo);
             reinterpret_cast<uint32_t*>(Qh)[i] = hi;
             reinterpret_cast<uint32_t*>(Ql)[i] = lo;
-            split2(S.k[r * LDP + c] * __expf(gl0 - g0), S.k[r * LDP + c + 1] * __expf(gl1 - g1), hi, lo);
+            split2(kv.x * __expf(gl.x - g0), kv.y * __expf(gl.y - g1), hi, lo);
             reinterpret_cast<uint32_t*>(Kh)[i] = hi;
             reinterpret_cast<uint32_t*>(Kl)[i] = lo;
             reinterpret_cast<float2*>(gam)[i] = make_float2(g0, g1);

@@ -106,6 +106,12 @@ __device__ __forceinline__ const __nv_bfloat16* bk_addr(const __nv_bfloat16* bas
     return base + (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * ld + n0 + 8 * (lane >> 4);
 }
 
+// Barrier over `count` threads (a multiple of 32) on hardware barrier `id` (1..15; 0 is the
+// block-wide barrier of __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---- cp.async (16-byte, L2-cached) ----
 __device__ __forceinline__ void cp16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));

@@ -49,7 +49,7 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 kda_status check_problem(const kda_problem* p) {
     if (!p) return KDA_ERR_INVALID_ARG;
     if (p->d != D) return KDA_ERR_UNSUPPORTED;
-    if (p->H < 1 || p->H > 65535 || p->N < 1 || p->T < 0 || p->T > INT32_MAX)
+    if (p->H < 1 || p->H > 65535 || p->N < 1 || p->N > 65535 || p->T < 0 || p->T > INT32_MAX)
         return KDA_ERR_INVALID_ARG;
     if (p->gate != KDA_GATE_G && p->gate != KDA_GATE_RAW) return KDA_ERR_INVALID_ARG;
     if (p->l2norm != 0 && p->l2norm != 1) return KDA_ERR_INVALID_ARG;
@@ -111,15 +111,15 @@ void set_saved(Params& p, const Layout& L, char* base, bool states) {
     p.Akk = f(R.Akk);
     p.gam = f(R.gam);
     p.eGL = f(R.eGL);
-    p.sS = states ? f(L.sv_S) : nullptr;
-    p.sDelta = states ? f(L.sv_Delta) : nullptr;
+    p.sS = states ? b(L.sv_S) : nullptr;
+    p.sDelta = states ? b(L.sv_Delta) : nullptr;
 }
 
 void set_bwd_regions(Params& p, const Layout& L, void* ws) {
     char* w = static_cast<char*>(ws);
     auto f = [&](size_t off) { return reinterpret_cast<float*>(w + off); };
-    p.dS1 = f(L.dS1);
-    p.dDelta = f(L.dDelta);
+    p.dS1 = reinterpret_cast<__nv_bfloat16*>(w + L.dS1);
+    p.dDelta = reinterpret_cast<__nv_bfloat16*>(w + L.dDelta);
     p.dR = f(L.dR);
     p.P = f(L.P);
     p.dQg = f(L.dQg);

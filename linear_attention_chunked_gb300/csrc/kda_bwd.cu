@@ -40,24 +40,6 @@ struct BwdGemmSmem {
     __nv_bfloat16 Dl[2][CH * LB];    // Delta (hi, lo)
 };
 
-// dense fp32 [ROWS][128] global tile -> bf16 hi/lo shared tiles with row stride LB (all loads of
-// a thread issued first)
-template <int ROWS>
-__device__ __forceinline__ void split_tile(__nv_bfloat16* hi, __nv_bfloat16* lo, const float* g,
-                                           int tid) {
-    float4 v[ROWS / 8];
-    load_tile_f32<ROWS>(v, g, tid);
-#pragma unroll
-    for (int k = 0; k < ROWS / 8; ++k) {
-        const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;
-        uint32_t h0, l0, h1, l1;
-        split2(v[k].x, v[k].y, h0, l0);
-        split2(v[k].z, v[k].w, h1, l1);
-        *reinterpret_cast<uint2*>(hi + r * LB + c) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(lo + r * LB + c) = make_uint2(l0, l1);
-    }
-}
-
 static_assert(sizeof(ChainBwdSmem) <= 232448, "chain shared memory above the opt-in limit");
 static_assert(sizeof(BwdGemmSmem) <= 232448, "backward GEMM shared memory above the opt-in limit");
 
@@ -96,6 +78,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain_bwd(Params p, int mode)
                 const int val = col0 + cq + 8 * nt + 2 * t + (e & 1);
                 dS[mt][nt][e] = (bwd && p.dht) ? p.dht[dh + size_t(key) * D + val] : 0.f;
             }
+    // writes dS's hi / lo split to shared memory (B operand of the next step)
     auto store_dS = [&]() {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
@@ -147,23 +130,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain_bwd(Params p, int mode)
     for (int ci = c1 - 1; ci >= c0; --ci) {
         const size_t chd = size_t(ci) * p.H + h;
         const __nv_bfloat16* sdO = sm.dO[(c1 - 1 - ci) & 1];
-        if (bwd) {  // gradient at the chunk end
-            float* dst = p.dS1 + chd * D * D;
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int key = 32 * wq + 16 * mt + g + 8 * hf;
-                        const int val = col0 + cq + 8 * nt + 2 * t;
-                        *reinterpret_cast<float2*>(dst + size_t(key) * D + val) =
-                            make_float2(dS[mt][nt][2 * hf], dS[mt][nt][2 * hf + 1]);
-                    }
-        }
         // ---- A': dDelta = scale Aqk^T dO + Kb dS1 ----
         cp_wait<1>();
         __syncthreads();
+        if (bwd) {  // gradient at the end of this chunk: the split in shared memory
+            __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + col0;
+            st_tile_bf16(dst, D, sm.dS[0], LB64, D, 64, tid, BT);
+            st_tile_bf16(dst + D * D, D, sm.dS[1], LB64, D, 64, tid, BT);
+        }
         {
             float a1[4][4] = {}, a2[4][4] = {};
             for (int ks = wq; ks < 4; ++ks) {  // Aqk^T is upper triangular
@@ -203,13 +177,16 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain_bwd(Params p, int mode)
                     split2(-d0, -d1, hi, lo);
                     *reinterpret_cast<uint32_t*>(&sm.X[0][row * LB64 + col]) = hi;
                     *reinterpret_cast<uint32_t*>(&sm.X[1][row * LB64 + col]) = lo;
-                    if (bwd)
-                        *reinterpret_cast<float2*>(p.dDelta + chd * CH * D + row * D + col0 + col) =
-                            make_float2(d0, d1);
+
                 }
         }
         __syncthreads();
         issue_X(ci - 1);
+        if (bwd) {  // planes of +dDelta (shared memory holds -dDelta; the split of -x is -split(x))
+            __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + col0;
+            st_tile_bf16(dst, D, sm.X[0], LB64, CH, 64, tid, BT, 0x80008000u);
+            st_tile_bf16(dst + CH * D, D, sm.X[1], LB64, CH, 64, tid, BT, 0x80008000u);
+        }
         // ---- D': dS0 = e^gL dS1 + scale Qg^T dO - W^T dDelta ----
         cp_wait<1>();
         __syncthreads();
@@ -289,13 +266,21 @@ __global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
     BwdGemmSmem& sm = *reinterpret_cast<BwdGemmSmem*>(smraw);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const size_t chd = size_t(ci) * p.H + h;
-    const float* S0 = p.sS + chd * D * D;
-    const float* dS1 = p.dS1 + chd * D * D;
-    const float* Dl = p.sDelta + chd * CH * D;
+    const __nv_bfloat16* S0 = p.sS + chd * 2 * D * D;
+    const __nv_bfloat16* dS1 = p.dS1 + chd * 2 * D * D;
+    const __nv_bfloat16* Dl = p.sDelta + chd * 2 * CH * D;
+    const __nv_bfloat16* dDl = p.dDelta + chd * 2 * CH * D;
     const int mt = w & 3, nh = w >> 2;
 
+    // every operand arrives as bf16 (hi / lo planes): one batch of cp.async
     cp_tile_bf16(sm.M[0], LB64, p.Mh + chd * CH * CH, CH, CH, CH, tid, NTHR);
     cp_tile_bf16(sm.M[1], LB64, p.Ml + chd * CH * CH, CH, CH, CH, tid, NTHR);
+    cp_tile_bf16(sm.X[0], LB, dDl, D, CH, D, tid, NTHR);
+    cp_tile_bf16(sm.X[1], LB, dDl + CH * D, D, CH, D, tid, NTHR);
+    cp_tile_bf16(sm.S[0], LB, S0, D, D, D, tid, NTHR);
+    cp_tile_bf16(sm.S[1], LB, S0 + D * D, D, D, D, tid, NTHR);
+    cp_tile_bf16(sm.Dl[0], LB, Dl, D, CH, D, tid, NTHR);
+    cp_tile_bf16(sm.Dl[1], LB, Dl + CH * D, D, CH, D, tid, NTHR);
     for (int i = tid; i < CH * 16; i += NTHR) {
         const int r = i >> 4, c = (i & 15) * 8;
         const bool ok = r < L;
@@ -303,9 +288,6 @@ __global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
         cp16z(sm.O + r * LB + c, p.dO + (row * p.H + h) * D + c, ok);
     }
     cp_commit();
-    split_tile<CH>(sm.X[0], sm.X[1], p.dDelta + chd * CH * D, tid);
-    split_tile<D>(sm.S[0], sm.S[1], S0, tid);
-    split_tile<CH>(sm.Dl[0], sm.Dl[1], Dl, tid);
     cp_wait<0>();
     __syncthreads();
 
@@ -406,34 +388,41 @@ __global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
             }
     }
     __syncthreads();
-    // dKb = Delta dS1^T  [64 tok x 128 key]; rsum = rowsum(S0 * dS1) with S0 taken from its
-    // staged hi + lo parts (16 significant bits) before the tile is replaced by dS1
+    // dKb = Delta dS1^T  [64 tok x 128 key]; rsum = rowsum(S0 * dS1) from the hi + lo parts of
+    // both (16 significant bits), taken before the staged S0 is replaced by dS1
     {
-        float4 v[16];
-        load_tile_f32<D>(v, dS1, tid);
+        uint4 vh[8], vl[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;  // warp w + 8k owns row r
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+            vh[k] = *reinterpret_cast<const uint4*>(dS1 + r * D + c8);
+            vl[k] = *reinterpret_cast<const uint4*>(dS1 + D * D + r * D + c8);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;  // 16 lanes per row
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&vh[k]);
+            const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&vl[k]);
+            const __nv_bfloat162* sh = reinterpret_cast<const __nv_bfloat162*>(&sm.S[0][r * LB + c8]);
+            const __nv_bfloat162* sl = reinterpret_cast<const __nv_bfloat162*>(&sm.S[1][r * LB + c8]);
             float a = 0.f;
-            const float x[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float s0 = __bfloat162float(sm.S[0][r * LB + c + j]) +
-                                 __bfloat162float(sm.S[1][r * LB + c + j]);
-                a = fmaf(s0, x[j], a);
+                const float2 d0 = __bfloat1622float2(h2[j]), d1 = __bfloat1622float2(l2[j]);
+                const float2 s0 = __bfloat1622float2(sh[j]), s1 = __bfloat1622float2(sl[j]);
+                a = fmaf(s0.x + s1.x, d0.x + d1.x, a);
+                a = fmaf(s0.y + s1.y, d0.y + d1.y, a);
             }
-            a = warp_sum(a);
-            if (lane == 0) p.rsum[chd * D + r] = a;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if ((lane & 15) == 0) p.rsum[chd * D + r] = a;
         }
         __syncthreads();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int i = tid + NTHR * k, r = i >> 5, c = (i & 31) * 4;
-            uint32_t h0, l0, h1, l1;
-            split2(v[k].x, v[k].y, h0, l0);
-            split2(v[k].z, v[k].w, h1, l1);
-            *reinterpret_cast<uint2*>(&sm.S[0][r * LB + c]) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2*>(&sm.S[1][r * LB + c]) = make_uint2(l0, l1);
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
+            *reinterpret_cast<uint4*>(&sm.S[0][r * LB + c8]) = vh[k];
+            *reinterpret_cast<uint4*>(&sm.S[1][r * LB + c8]) = vl[k];
         }
     }
     __syncthreads();
@@ -474,6 +463,7 @@ struct BwdIntraSmem {
     __nv_bfloat16 qb[CH * LB], kb[CH * LB];          // q, k as given (bf16); q^ = q * rq
     float dA[CH * LAS], dAk[CH * LAS];               // dAqk and dAkk = beta_r dM
     float beta[CH], rq[CH], rk[CH];
+    float dbp[CH];  // per-row dbeta, accumulated in steps 1-2 in a fixed order
     union {
         uint4 Af[24][2][32];         // split A fragments of dAqk / dAkk (fragment order), step 3
         float red[2 * BI_THREADS];   // reduction scratch, steps 5 and 7
@@ -523,13 +513,23 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
             vq[k4] = r < L ? *reinterpret_cast<const uint4*>(p.q + off) : make_uint4(0u, 0u, 0u, 0u);
             vk[k4] = r < L ? *reinterpret_cast<const uint4*>(p.k + off) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float4 v[4], va[2], vm[2];
+        float4 v[4], va[2], vm[2], vak[2];
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) v[k4] = reinterpret_cast<const float4*>(p.gam + chd * CH * D)[tid + BT * k4];
 #pragma unroll
         for (int k4 = 0; k4 < 2; ++k4) {
             va[k4] = reinterpret_cast<const float4*>(dAqk)[tid + BT * k4];
             vm[k4] = reinterpret_cast<const float4*>(dM)[tid + BT * k4];
+            vak[k4] = reinterpret_cast<const float4*>(Akk)[tid + BT * k4];
+        }
+        // dbeta_r <- sum_{s<r} Akk[r,s] dM[r,s] (dM is zero for s >= r): 16 lanes per row
+#pragma unroll
+        for (int k4 = 0; k4 < 2; ++k4) {
+            const int i = tid + BT * k4, r = i >> 4;
+            float a = vak[k4].x * vm[k4].x + vak[k4].y * vm[k4].y + vak[k4].z * vm[k4].z + vak[k4].w * vm[k4].w;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if ((i & 15) == 0) S.dbp[r] = a;
         }
         if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
 #pragma unroll
@@ -577,38 +577,49 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
     }
     __syncthreads();
 
-    // 2. elementwise terms through Qg, Kg, Kb and the diagonal of Aqk
-    {
-        float4 vq[4], vp[4], vb[4];
+    // 2. elementwise terms through Qg, Kg, Kb and the diagonal of Aqk; dv = beta dR; dbeta_r +=
+    //    dR_r . v_r - Kg_r . P_r (one warp per row, fixed-order warp sums)
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        float4 vq[2], vp[2], vb[2], vr[2];
+        uint2 vv[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = tid + BT * k;
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + BT * (2 * half + k), r = i >> 5, c0 = (i & 31) * 4;
             vq[k] = reinterpret_cast<const float4*>(dQg)[i];
             vp[k] = reinterpret_cast<const float4*>(Pp)[i];
             vb[k] = reinterpret_cast<const float4*>(dKb)[i];
+            vr[k] = reinterpret_cast<const float4*>(dR)[i];
+            vv[k] = r < L ? *reinterpret_cast<const uint2*>(p.v + (size_t(t0 + r) * p.H + h) * D + c0)
+                          : make_uint2(0u, 0u);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = tid + BT * k, r = i >> 5, c0 = (i & 31) * 4;
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + BT * (2 * half + k), r = i >> 5, c0 = (i & 31) * 4;
             const float dgn = S.dA[r * LAS + r], br = S.beta[r], rqr = S.rq[r], rkr = S.rk[r];
             const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LDP + c0]);
             const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LDP + c0]);
             const uint2 qb2 = *reinterpret_cast<const uint2*>(&S.qb[r * LB + c0]);
             const uint2 kb2 = *reinterpret_cast<const uint2*>(&S.kb[r * LB + c0]);
-            __nv_bfloat162 qa, qb_, ka, kb_;
+            __nv_bfloat162 qa, qb_, ka, kb_, va_, vb_;
             memcpy(&qa, &qb2.x, 4);
             memcpy(&qb_, &qb2.y, 4);
             memcpy(&ka, &kb2.x, 4);
             memcpy(&kb_, &kb2.y, 4);
+            memcpy(&va_, &vv[k].x, 4);
+            memcpy(&vb_, &vv[k].y, 4);
             const float2 q01 = __bfloat1622float2(qa), q23 = __bfloat1622float2(qb_);
             const float2 k01 = __bfloat1622float2(ka), k23 = __bfloat1622float2(kb_);
+            const float2 v01 = __bfloat1622float2(va_), v23 = __bfloat1622float2(vb_);
             const float gvv[4] = {g4.x, g4.y, g4.z, g4.w}, glv[4] = {l4.x, l4.y, l4.z, l4.w};
             const float qv4[4] = {q01.x * rqr, q01.y * rqr, q23.x * rqr, q23.y * rqr};
             const float kv4[4] = {k01.x * rkr, k01.y * rkr, k23.x * rkr, k23.y * rkr};
+            const float vvv[4] = {v01.x, v01.y, v23.x, v23.y};
             const float aq[4] = {vq[k].x, vq[k].y, vq[k].z, vq[k].w};
             const float ap[4] = {vp[k].x, vp[k].y, vp[k].z, vp[k].w};
             const float ab[4] = {vb[k].x, vb[k].y, vb[k].z, vb[k].w};
-            float oq[4], ok[4], og[4];
+            const float ar[4] = {vr[k].x, vr[k].y, vr[k].z, vr[k].w};
+            float oq[4], ok[4], og[4], db = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float er = __expf(gvv[j]), eb = __expf(glv[j] - gvv[j]);
@@ -617,10 +628,17 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
                 oq[j] = fmaf(dqg, er, dgn * kv);
                 ok[j] = fmaf(dkg, er, fmaf(dkb, eb, dgn * qv));
                 og[j] = (dqg * qv + dkg * kv) * er - dkb * kv * eb;
+                db = fmaf(ar[j], vvv[j], db);
+                db = fmaf(-kv * er, ap[j], db);
             }
             *reinterpret_cast<float4*>(&S.dQ[r * LDP + c0]) = make_float4(oq[0], oq[1], oq[2], oq[3]);
             *reinterpret_cast<float4*>(&S.dK[r * LDP + c0]) = make_float4(ok[0], ok[1], ok[2], ok[3]);
             *reinterpret_cast<float4*>(&S.dG[r * LDP + c0]) = make_float4(og[0], og[1], og[2], og[3]);
+            if (r < L)
+                store_out4(p.dv, (size_t(t0 + r) * p.H + h) * D + c0,
+                           make_float4(br * ar[0], br * ar[1], br * ar[2], br * ar[3]), p.out_fp32);
+            db = warp_sum(db);
+            if (lane == 0) S.dbp[r] += db;
         }
     }
     // split A fragments of dAqk and dAkk, built once: 12 "as row" (i, ks<i) and 12 "as column"
@@ -719,23 +737,33 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
     __syncthreads();
 
     // 4. inside each sub-chunk, elementwise: one thread per (sub-chunk, channel); the column's 16
-    //    values of gam, q^, k^ are held in registers
+    //    values of gam, q^, k^ are held in registers, and exp(gam_r - gam_s) is the running product
+    //    of the per-token decay factors exp(gam_x - gam_{x-1}), s < x <= r (each <= 1)
     {
         const int b = tid / D, c = tid % D, base = 16 * b;
-        float gv[16], qv[16], kv[16], aq[16], ak[16], bb[16];
+        float qv[16], kv[16], ed[16], aq[16], ak[16], bb[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-            gv[x] = S.gam[(base + x) * LDP + c];
             qv[x] = Qv(base + x, c);
             kv[x] = Kv(base + x, c);
             aq[x] = ak[x] = bb[x] = 0.f;
         }
+        {
+            float prev = S.gam[base * LDP + c];
 #pragma unroll
-        for (int rl = 1; rl < 16; ++rl) {
-            const int r = base + rl;
+            for (int x = 1; x < 16; ++x) {
+                const float cur = S.gam[(base + x) * LDP + c];
+                ed[x] = __expf(cur - prev);
+                prev = cur;
+            }
+        }
 #pragma unroll
-            for (int sl = 0; sl < rl; ++sl) {
-                const float E = __expf(gv[rl] - gv[sl]);
+        for (int sl = 0; sl < 15; ++sl) {
+            float E = 1.f;
+#pragma unroll
+            for (int rl = sl + 1; rl < 16; ++rl) {
+                E *= ed[rl];
+                const int r = base + rl;
                 const float da = S.dA[r * LAS + base + sl], dk = S.dAk[r * LAS + base + sl];
                 const float ks = kv[sl] * E;
                 aq[rl] = fmaf(da, ks, aq[rl]);
@@ -778,43 +806,33 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
     }
     __syncthreads();
 
-    // 6. per row: L2-norm backward, dq, dk, dv, dbeta (warp per row)
+    // 6. per row: L2-norm backward and the dq, dk, dbeta outputs (warp per row, 4 channels per lane)
     for (int r = w; r < L; r += NW) {
         const size_t base = (size_t(t0 + r) * p.H + h) * D;
-        const float br = S.beta[r];
-        float dq[4], dk[4], pq = 0.f, pk = 0.f, db = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int c = lane + 32 * m;
-            dq[m] = S.dQ[r * LDP + c];
-            dk[m] = S.dK[r * LDP + c];
-            const float qv = Qv(r, c), kv = Kv(r, c);
-            pq = fmaf(qv, dq[m], pq);
-            pk = fmaf(kv, dk[m], pk);
-            const float dRv = dR[r * D + c];
-            const float kg = kv * __expf(S.gam[r * LDP + c]);
-            db = fmaf(dRv, bf2f(p.v[base + c]), db);
-            db = fmaf(-kg, Pp[r * D + c], db);
-            store_out(p.dv, base + c, br * dRv, p.out_fp32);
-        }
-        for (int s2 = lane; s2 < r; s2 += 32) db = fmaf(Akk[r * CH + s2], dM[r * CH + s2], db);
-        db = warp_sum(db);
+        const int c0 = 4 * lane;
+        const float4 dq4 = *reinterpret_cast<const float4*>(&S.dQ[r * LDP + c0]);
+        const float4 dk4 = *reinterpret_cast<const float4*>(&S.dK[r * LDP + c0]);
+        float dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w}, dk[4] = {dk4.x, dk4.y, dk4.z, dk4.w};
         if (p.l2n) {
+            float qv[4], kv[4], pq = 0.f, pk = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                qv[j] = Qv(r, c0 + j);
+                kv[j] = Kv(r, c0 + j);
+                pq = fmaf(qv[j], dq[j], pq);
+                pk = fmaf(kv[j], dk[j], pk);
+            }
             pq = warp_sum(pq);
             pk = warp_sum(pk);
-        }
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int c = lane + 32 * m;
-            float vq = dq[m], vk = dk[m];
-            if (p.l2n) {
-                vq = (vq - Qv(r, c) * pq) * S.rq[r];
-                vk = (vk - Kv(r, c) * pk) * S.rk[r];
+            for (int j = 0; j < 4; ++j) {
+                dq[j] = (dq[j] - qv[j] * pq) * S.rq[r];
+                dk[j] = (dk[j] - kv[j] * pk) * S.rk[r];
             }
-            store_out(p.dq, base + c, vq, p.out_fp32);
-            store_out(p.dk, base + c, vk, p.out_fp32);
         }
-        if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, db, p.out_fp32);
+        store_out4(p.dq, base + c0, make_float4(dq[0], dq[1], dq[2], dq[3]), p.out_fp32);
+        store_out4(p.dk, base + c0, make_float4(dk[0], dk[1], dk[2], dk[3]), p.out_fp32);
+        if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, S.dbp[r], p.out_fp32);
     }
     __syncthreads();  // step 7 reuses dQ / dK as scratch
 

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain_fwd(Params p, int mode)
                 else if (p.h0) v0 = p.h0[dh + size_t(key) * D + val];
                 Sv[mt][nt][e] = v0;
             }
+    // writes the state's hi / lo split to shared memory (B operand of the next chunk)
     auto store_S = [&]() {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
@@ -149,23 +150,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain_fwd(Params p, int mode)
         const int4 info = p.chunk_tab[ci];
         const int t0 = info.y, L = info.z;
         const size_t chd = size_t(ci) * p.H + h;
-        if (fwd && p.sS) {  // saved state at the chunk start
-            float* dst = p.sS + chd * D * D;
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int key = 32 * wq + 16 * mt + g + 8 * hf;
-                        const int val = col0 + cq + 8 * nt + 2 * t;
-                        *reinterpret_cast<float2*>(dst + size_t(key) * D + val) =
-                            make_float2(Sv[mt][nt][2 * hf], Sv[mt][nt][2 * hf + 1]);
-                    }
-        }
         // ---- A: Delta = U - W S ----
         cp_wait<2>();
         __syncthreads();
+        if (fwd && p.sS) {  // saved start state of this chunk: the split in shared memory
+            __nv_bfloat16* dst = p.sS + chd * 2 * D * D + col0;
+            st_tile_bf16(dst, D, sm.S[0], LB64, D, 64, tid, BT);
+            st_tile_bf16(dst + D * D, D, sm.S[1], LB64, D, 64, tid, BT);
+        }
         float dl[4][4] = {};
 #pragma unroll 2
         for (int ks = 0; ks < 8; ++ks) {
@@ -195,12 +187,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS) k_chain_fwd(Params p, int mode)
                 split2(d0, d1, hi, lo);
                 *reinterpret_cast<uint32_t*>(&sm.Dl[0][row * LB64 + col]) = hi;
                 *reinterpret_cast<uint32_t*>(&sm.Dl[1][row * LB64 + col]) = lo;
-                if (fwd && p.sDelta)
-                    *reinterpret_cast<float2*>(p.sDelta + chd * CH * D + row * D + col0 + col) =
-                        make_float2(d0, d1);
+
             }
         __syncthreads();
         issue_WU(ci + 1);
+        if (fwd && p.sDelta) {  // saved write vectors of this chunk
+            __nv_bfloat16* dst = p.sDelta + chd * 2 * CH * D + col0;
+            st_tile_bf16(dst, D, sm.Dl[0], LB64, CH, 64, tid, BT);
+            st_tile_bf16(dst + CH * D, D, sm.Dl[1], LB64, CH, 64, tid, BT);
+        }
         // ---- C: O = Qg S + Aqk Delta ----
         cp_wait<2>();
         __syncthreads();

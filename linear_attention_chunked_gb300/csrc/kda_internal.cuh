@@ -15,7 +15,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kda.h"
+#include "kda.h"  // include/ is on the include path (build.py)
 #include "kda_mma.cuh"
 
 namespace kda {
@@ -144,15 +144,32 @@ struct Params {
     int4* chunk_tab;  // {doc, first token, length, chunk index within the doc}
     __nv_bfloat16 *Wh, *Wl, *Qh, *Ql, *Kh, *Kl, *Ah, *Al, *Mh, *Ml;
     float *U, *Akk, *gam, *eGL;
-    float *dS1, *dDelta, *dR, *P, *dQg, *dKb, *dAqk, *dM, *rsum, *pdA, *pddt;
-    // saved set (per chunk-head states and write vectors)
-    float *sS, *sDelta;
+    // per (chunk, head) chunk-end gradient dS1 [2][128][128] and dDelta [2][64][128]: bf16 hi/lo
+    // planes (plane 0 = hi, plane 1 = lo), i.e. the split the per-chunk GEMMs consume
+    __nv_bfloat16 *dS1, *dDelta;
+    float *dR, *P, *dQg, *dKb, *dAqk, *dM, *rsum, *pdA, *pddt;
+    // saved set: chunk-start states S_c [2][128][128] and write vectors Delta_c [2][64][128] as
+    // bf16 hi/lo planes
+    __nv_bfloat16 *sS, *sDelta;
     // fragment summary outputs
     float *fragM, *fragB;
     int64_t maxC;
 };
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Stores four consecutive output elements (index i, a multiple of 4) in the chosen precision.
+__device__ __forceinline__ void store_out4(void* base, size_t i, float4 v, int fp32) {
+    if (fp32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(base) + i) = v;
+    } else {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        memcpy(&u.x, &a, 4);
+        memcpy(&u.y, &b, 4);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(base) + i) = u;
+    }
+}
 
 // Stores an output element in the caller's chosen precision.
 __device__ __forceinline__ void store_out(void* base, size_t i, float v, int fp32) {

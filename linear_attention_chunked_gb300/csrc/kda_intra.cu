@@ -163,11 +163,12 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
     }
     __syncthreads();
 
-    // 4a. diagonal 16x16 blocks, elementwise exact exponent differences
-    for (int idx = tid; idx < 4 * 136; idx += BT) {
-        const int b = idx / 136, pi = idx % 136;
+    // 4a. diagonal 8x8 blocks, elementwise exact exponent differences (the lower-left 8x8
+    //     quadrant of each 16-row sub-chunk runs on tensor cores in 4c)
+    for (int idx = tid; idx < 8 * 36; idx += BT) {
+        const int b = idx / 36, pi = idx % 36;
         const int rl = tri_row(pi), sl = pi - rl * (rl + 1) / 2;
-        const int r = 16 * b + rl, s = 16 * b + sl;
+        const int r = 8 * b + rl, s = 8 * b + sl;
         float akk = 0.f, aqk = 0.f, akk2 = 0.f, aqk2 = 0.f;
         const float4* gr = reinterpret_cast<const float4*>(S.gam + r * LDP);
         const float4* gs = reinterpret_cast<const float4*>(S.gam + s * LDP);
@@ -204,8 +205,45 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
     }
     __syncthreads();
     // 4c. off-diagonal blocks on tensor cores: warp w < 12 takes pair w / 2 and half w % 2 of the
-    //     128 channels (k-steps); the two halves are added in a fixed order
-    if (warp < 12) {
+    //     128 channels (k-steps); the two halves are added in a fixed order.  Warps 12..15 take the
+    //     lower-left 8x8 quadrant of sub-chunk b = w - 12 (rows 16b+8.., columns 16b..16b+7),
+    //     split at the quadrant boundary e = 16b+7 so both factors are <= 1.
+    if (warp >= 12) {
+        const int b = warp - 12, e = 16 * b + 7;
+        float accQ[4] = {}, accK[4] = {};
+#pragma unroll 2
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t qh[4] = {}, ql[4] = {}, kh4[4] = {}, kl[4] = {};
+#pragma unroll
+            for (int rr = 1; rr < 4; rr += 2) {  // rows 16b + 8 + g; rows 16b + g stay zero
+                const int row = 16 * b + 8 + g, col = 16 * ks + 2 * t + 8 * (rr >> 1);
+                const float2 gr = *reinterpret_cast<const float2*>(&S.gam[row * LDP + col]);
+                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LDP + col]);
+                const float2 qv = *reinterpret_cast<const float2*>(&S.q[row * LDP + col]);
+                const float2 kv = *reinterpret_cast<const float2*>(&S.k[row * LDP + col]);
+                const float e0 = __expf(gr.x - ge.x), e1 = __expf(gr.y - ge.y);
+                split2(qv.x * e0, qv.y * e1, qh[rr], ql[rr]);
+                split2(kv.x * e0, kv.y * e1, kh4[rr], kl[rr]);
+            }
+            uint32_t bh[2], bl[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {  // B[k = channel][n = s]: k[s][c] exp(gam_e - gam_s)
+                const int sr = 16 * b + g, c = 16 * ks + 2 * t + 8 * hf;
+                const float2 gs = *reinterpret_cast<const float2*>(&S.gam[sr * LDP + c]);
+                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LDP + c]);
+                const float2 kv = *reinterpret_cast<const float2*>(&S.k[sr * LDP + c]);
+                split2(kv.x * __expf(ge.x - gs.x), kv.y * __expf(ge.y - gs.y), bh[hf], bl[hf]);
+            }
+            mma_x3(accQ, qh, ql, bh[0], bh[1], bl[0], bl[1]);
+            mma_x3(accK, kh4, kl, bh[0], bh[1], bl[0], bl[1]);
+        }
+#pragma unroll
+        for (int e4 = 2; e4 < 4; ++e4) {
+            const int row = 16 * b + 8 + g, col = 16 * b + 2 * t + (e4 & 1);
+            S.Aqk[row * LDA + col] = accQ[e4];
+            S.Akk[row * LDA + col] = accK[e4];
+        }
+    } else {
         const int pr = warp >> 1, kh = warp & 1;
         const int i = kPairs[pr].x, j = kPairs[pr].y, e = 16 * j + 15;
         float accQ[2][4] = {}, accK[2][4] = {};

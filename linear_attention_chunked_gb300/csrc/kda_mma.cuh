@@ -147,4 +147,21 @@ __device__ __forceinline__ void cp_tile_f32(float* s, int ld, const float* g, in
     }
 }
 
+// Copies a [rows][cols] bf16 shared tile (row stride sld) to a dense global tile (row stride gld)
+// with 16-byte accesses by the whole block; flip = 0x80008000 negates every element.
+__device__ __forceinline__ void st_tile_bf16(__nv_bfloat16* g, int gld, const __nv_bfloat16* s,
+                                             int sld, int rows, int cols, int tid, int nthr,
+                                             uint32_t flip = 0u) {
+    const int per_row = cols / 8;
+    for (int i = tid; i < rows * per_row; i += nthr) {
+        const int r = i / per_row, c = (i % per_row) * 8;
+        uint4 v = *reinterpret_cast<const uint4*>(s + r * sld + c);
+        v.x ^= flip;
+        v.y ^= flip;
+        v.z ^= flip;
+        v.w ^= flip;
+        *reinterpret_cast<uint4*>(g + size_t(r) * gld + c) = v;
+    }
+}
+
 }  // namespace kda

@@ -143,7 +143,7 @@ def alg_bytes_per_token_head(kernel):
     o, dqkv, dbeta, dg = 512, 3 * 512, 4, 512
     table = {
         "k_intra_fwd": qkv + beta + gate,                    # reads the chunk inputs
-        "k_chain_fwd": o,                                    # writes o
+        "k_chain_fwd_tc": o,                                 # writes o
         "k_chain_bwd": dO,                                   # reads dO
         "k_bwd_gemms": dO,                                   # reads dO
         "k_bwd_intra": qkv + beta + gate + dqkv + dbeta + dg,  # reads inputs, writes grads

@@ -10,7 +10,7 @@ using namespace kda;
 namespace {
 
 const size_t SMEM_INTRA_FWD = intra_smem_bytes();
-const size_t SMEM_CHAIN_FWD = chain_fwd_smem_bytes();
+const size_t SMEM_CHAIN_FWD_TC = chain_fwd_tc_smem_bytes();
 const size_t SMEM_CHAIN_BWD = chain_bwd_smem_bytes();
 const size_t SMEM_BWD_GEMMS = bwd_gemm_smem_bytes();
 const size_t SMEM_BWD_INTRA = bwd_intra_smem_bytes();
@@ -32,7 +32,7 @@ kda_status setup_device() {
         return KDA_ERR_CUDA;
     if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
     struct { const void* f; size_t smem; } attrs[] = {
-        {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd, SMEM_CHAIN_FWD},
+        {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd_tc, SMEM_CHAIN_FWD_TC},
         {(const void*)k_chain_bwd, SMEM_CHAIN_BWD}, {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
         {(const void*)k_bwd_intra, SMEM_BWD_INTRA}, {(const void*)k_walk, SMEM_WALK},
     };
@@ -142,6 +142,58 @@ void set_inputs(Params& p, const void* q, const void* k, const void* v, const vo
     p.dt_bias = dt_bias;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time libcuda dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Tensor maps over the intra-chunk record that p points at (3-D: [tile][64 rows][columns], 128-byte
+// swizzle, 64 x 64 boxes).  The W, Qg, Kb planes are consecutive runs of CHd tiles, as are the two
+// Aqk planes.
+kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return KDA_ERR_CUDA;
+    const size_t CHd = size_t(L.maxC) * L.H;
+    if (6 * CHd > size_t(INT32_MAX)) return KDA_ERR_UNSUPPORTED;
+    const IntraRecord R = make_intra_record(CHd);
+    const size_t t128 = size_t(CH) * D * 2, t64 = size_t(CH) * CH * 2;
+    if (R.Kl + CHd * t128 - R.Wh != 6 * CHd * t128 || R.Al + CHd * t64 - R.Ah != 2 * CHd * t64)
+        return KDA_ERR_UNSUPPORTED;  // planes not contiguous (layout changed)
+    tm->zWh = 0;
+    tm->zWl = int((R.Wl - R.Wh) / t128);
+    tm->zQh = int((R.Qh - R.Wh) / t128);
+    tm->zQl = int((R.Ql - R.Wh) / t128);
+    tm->zKh = int((R.Kh - R.Wh) / t128);
+    tm->zKl = int((R.Kl - R.Wh) / t128);
+    tm->zAh = 0;
+    tm->zAl = int((R.Al - R.Ah) / t64);
+    const cuuint32_t box[3] = {64, 64, 1}, es[3] = {1, 1, 1};
+    const cuuint64_t d128[3] = {D, CH, 6 * CHd}, s128[2] = {D * 2, t128};
+    const cuuint64_t d64[3] = {CH, CH, 2 * CHd}, s64[2] = {CH * 2, t64};
+    if (enc(&tm->m128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.Wh, d128, s128, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&tm->m64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.Ah, d64, s64, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status launched() {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -220,10 +272,13 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     p.ht = ht;
     if (saved) set_saved(p, L, static_cast<char*>(saved), true);
     else set_saved(p, L, static_cast<char*>(ws) + L.intra_ws, false);
+    TcMaps tm;
+    if (kda_status s = make_tc_maps(p, L, &tm)) return s;
     if (kda_status s = run_prologue(p, st)) return s;
     {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD, st>>>(p, CHAIN_FWD_OUT);
+        k_chain_fwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
+            p, CHAIN_FWD_OUT, tm);
     }
     return launched();
 }
@@ -291,12 +346,15 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         k_plan<<<1, NTHR, 0, st>>>(p);
     } else {
         // checkpoint replay: recompute the intra products, the states and the write vectors
+        TcMaps tm;
+        if (kda_status s = make_tc_maps(p, L, &tm)) return s;
         if (kda_status s = run_prologue(p, st)) return s;
         Params r = p;
         r.o = nullptr;
         r.ht = nullptr;
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD, st>>>(r, CHAIN_FWD_OUT);
+        k_chain_fwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
+            r, CHAIN_FWD_OUT, tm);
     }
     {
         ProfScope ps(KK_CHAIN_BWD, st);
@@ -339,10 +397,13 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     p.fragM = M;
     p.fragB = B_or_C;
     set_saved(p, L, static_cast<char*>(ws) + L.intra_ws, false);
+    TcMaps tm;
+    if (kda_status s = make_tc_maps(p, L, &tm)) return s;
     if (kda_status s = run_prologue(p, st)) return s;
     if (mode == KDA_FRAG_FWD) {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd<<<dim3(pr->N, pr->H, 2 * NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD, st>>>(p, CHAIN_FRAG_MB);
+        k_chain_fwd_tc<<<dim3(pr->N, pr->H, 2 * NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
+            p, CHAIN_FRAG_MB, tm);
     } else {
         ProfScope ps(KK_CHAIN_BWD, st);
         k_chain_bwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD, st>>>(p, CHAIN_FRAG_C);

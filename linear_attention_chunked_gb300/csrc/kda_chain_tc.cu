@@ -1,0 +1,361 @@
+// Inter-chunk state recurrence of the forward pass on tcgen05 tensor cores (TMEM accumulators,
+// TMA-fed operands).  Per (document, head, 64-column value half) and chunk, with the FP32 state S
+// held in registers (thread = one key row x 32 value columns):
+//   MMA1  D1 = [W; Qg] S                 M = 128 (64 W rows, 64 Qg rows), N = 64, K = 128 keys
+//         Delta = U - D1[0:64]           (threads of TMEM lanes 0..63)
+//   MMA2  D2 = Kb^T Delta                M = 128 keys, N = 64, K = 64 tokens
+//   MMA3  D1 += [*; Aqk] Delta           rows 64..127: O = Qg S + Aqk Delta
+//         S  = e^gL * S + D2             (every thread, its own row)
+// Every product is split into bf16 hi/lo terms (a_hi b_lo + a_lo b_hi + a_hi b_hi, FP32 accumulate
+// in TMEM), which keeps ~16 significant bits per operand.  Rows 0..63 of the MMA3 A operand are
+// whatever precedes the hi / lo Aqk tiles (zeros / the hi tile): they only touch D1 rows whose W S
+// values were already consumed.
+#include "kda_internal.cuh"
+#include "kda_tc.cuh"
+
+namespace kda {
+
+namespace {
+
+// Shared-memory image, byte offsets from a 1024-byte aligned base.  Operand tiles are 128-byte
+// swizzled (see kda_tc.cuh); "plane" 0 = hi, 1 = lo.
+constexpr int OFF_KT = 0;        // Kb as MN-major A: [plane][2 key blocks][64 tokens][128 B]  32 KB
+constexpr int OFF_A1 = 32768;    // [W; Qg] K-major: [plane][2 key blocks][128 rows][128 B]    64 KB
+constexpr int OFF_S = 98304;     // S as MN-major B: [plane][128 keys][128 B]                  32 KB
+constexpr int OFF_PAD = 131072;  // 8 KB of zeros: rows 0..63 of the hi MMA3 operand
+constexpr int OFF_AQ = 139264;   // Aqk K-major: [plane][64 tokens][128 B]                     16 KB
+constexpr int OFF_DL = 155648;   // Delta as MN-major B: [plane][64 tokens][128 B]             16 KB
+constexpr int OFF_BAR = 172032;  // mbarriers, TMEM base address, abort flag
+constexpr size_t CHAIN_TC_SMEM = OFF_BAR + 128 + 1024;  // + alignment slack of the base
+
+static_assert(CHAIN_TC_SMEM <= 232448, "tcgen05 chain shared memory above the opt-in limit");
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+    return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                            ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 32 values -> packed bf16 hi / lo pairs
+__device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&h)[16],
+                                        uint32_t (&l)[16]) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) split2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+}
+// 128-byte-swizzled tile row `row`, 32 values starting at column c0 (multiple of 8)
+__device__ __forceinline__ void st_sw128(unsigned char* tile, int row, int c0,
+                                         const uint32_t (&x)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int chunk = ((c0 >> 3) + j) ^ (row & 7);
+        *reinterpret_cast<uint4*>(tile + row * 128 + chunk * 16) =
+            make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    }
+}
+// 32 consecutive bf16 in global memory (64 bytes, 16-byte aligned)
+__device__ __forceinline__ void st_g32(__nv_bfloat16* dst, const uint32_t (&x)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        reinterpret_cast<uint4*>(dst)[j] = make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+}
+
+}  // namespace
+
+size_t chain_fwd_tc_smem_bytes() { return CHAIN_TC_SMEM; }
+
+// Grid (documents, heads, 2 value halves) for CHAIN_FWD_OUT; (documents, heads, 4) for
+// CHAIN_FRAG_MB (z = 0, 1: X = I with zero values -> M; z = 2, 3: Y = 0 with the values -> B).
+// 256 threads: warp w reads TMEM lanes 32 (w % 4).. and value columns 32 (w / 4).. of the half.
+// Thread 0 issues the TMA loads and the MMAs.  Operands of chunk c+1 are loaded as soon as the
+// MMA that reads their buffer has completed.
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+    k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm) {
+    const int n = blockIdx.x, h = blockIdx.y, hv = blockIdx.z;
+    const bool fwd = mode == CHAIN_FWD_OUT;
+    const bool fragX = !fwd && hv < 2;
+    const bool want_o = fwd && p.o != nullptr;
+    const int col0 = (hv & 1) * 64;
+    extern __shared__ unsigned char smraw[];
+    unsigned char* sm = align1024(smraw);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // A1 in, K in, MMA1 done, MMA2 done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + 36);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int qd = w & 3, cc = 32 * (w >> 2);
+    const int row = 32 * qd + lane;  // accumulator row (key for S / D2, token for D1)
+    const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
+    const size_t dh = (size_t(n) * p.H + h) * D * D;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tc::mbar_init(&bar[i], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::tma_prefetch_map(&tm.m128);
+        tc::tma_prefetch_map(&tm.m64);
+    }
+    if (w == 0) tc::tmem_alloc(tslot, 128);
+    for (int i = tid; i < 8192 / 16; i += CHAIN_THREADS)
+        reinterpret_cast<uint4*>(sm + OFF_PAD)[i] = make_uint4(0u, 0u, 0u, 0u);
+
+    float Sr[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int val = col0 + cc + j;
+        float v0 = 0.f;
+        if (!fwd) v0 = (fragX && row == val) ? 1.f : 0.f;
+        else if (p.h0) v0 = p.h0[dh + size_t(row) * D + val];
+        Sr[j] = v0;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t taddr = *tslot;
+    const uint32_t tD1 = taddr + (uint32_t(32 * qd) << 16), tD2 = tD1 + 64;
+
+    const uint32_t ID1 = tc::idesc_bf16(128, 64, false, true);  // K-major A, MN-major B
+    const uint32_t ID2 = tc::idesc_bf16(128, 64, true, true);   // MN-major A and B
+    const uint32_t sA1 = smem_u32(sm + OFF_A1), sS = smem_u32(sm + OFF_S);
+    const uint32_t sKt = smem_u32(sm + OFF_KT), sPad = smem_u32(sm + OFF_PAD);
+    const uint32_t sDl = smem_u32(sm + OFF_DL);
+
+    const uint32_t bytesA1 = want_o ? 65536u : 32768u, bytesK = want_o ? 49152u : 32768u;
+    auto load_A1 = [&](int ci) {
+        const int chd = ci * p.H + h;
+        tc::mbar_expect_tx(&bar[0], bytesA1);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_3d(sm + OFF_A1 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWh + chd, &bar[0]);
+            tma_load_3d(sm + OFF_A1 + 32768 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWl + chd, &bar[0]);
+            if (want_o) {
+                tma_load_3d(sm + OFF_A1 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0, tm.zQh + chd, &bar[0]);
+                tma_load_3d(sm + OFF_A1 + 32768 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0,
+                            tm.zQl + chd, &bar[0]);
+            }
+        }
+    };
+    auto load_K = [&](int ci) {
+        const int chd = ci * p.H + h;
+        tc::mbar_expect_tx(&bar[1], bytesK);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + OFF_KT + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[1]);
+            tma_load_3d(sm + OFF_KT + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[1]);
+        }
+        if (want_o) {
+            tma_load_3d(sm + OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[1]);
+            tma_load_3d(sm + OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[1]);
+        }
+    };
+    // per-thread operands of the next chunk, fetched one chunk ahead: its U row (lanes 0..63),
+    // e^gL of this thread's key, its chunk-table entry
+    float Un[32];
+    float egn = 0.f;
+    int4 infon = make_int4(0, 0, 0, 0);
+    auto fetch_next = [&](int ci) {
+        if (ci >= c1) return;
+        const size_t chd = size_t(ci) * p.H + h;
+        if (qd < 2 && !fragX) {
+            const float4* src = reinterpret_cast<const float4*>(p.U + chd * CH * D + size_t(row) * D + col0 + cc);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 u4 = src[j];
+                Un[4 * j] = u4.x;
+                Un[4 * j + 1] = u4.y;
+                Un[4 * j + 2] = u4.z;
+                Un[4 * j + 3] = u4.w;
+            }
+        }
+        egn = p.eGL[chd * D + row];
+        infon = p.chunk_tab[ci];
+    };
+#pragma unroll
+    for (int j = 0; j < 32; ++j) Un[j] = 0.f;
+    fetch_next(c0);
+
+    // phase parity of the loads in flight, -1 = none (thread 0's bookkeeping for an early exit)
+    int pendA = -1, pendK = -1;
+    if (tid == 0 && c0 < c1) {
+        load_A1(c0);
+        load_K(c0);
+        pendA = pendK = 0;
+    }
+
+    for (int ci = c0; ci < c1; ++ci) {
+        const uint32_t ph = uint32_t(ci - c0) & 1u;
+        const size_t chd = size_t(ci) * p.H + h;
+        uint32_t sh[16], sl[16];
+        split32(Sr, sh, sl);
+        st_sw128(sm + OFF_S, row, cc, sh);
+        st_sw128(sm + OFF_S + 16384, row, cc, sl);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (*abort_flag) break;
+
+        // ---- MMA1: D1 = [W; Qg] S ----
+        if (tid == 0) {
+            if (tc::mbar_wait(&bar[0], ph)) {
+                pendA = -1;
+                tc::fence_after_sync();
+                const uint64_t dAh = tc::sdesc(sA1, 16, 1024), dAl = tc::sdesc(sA1 + 32768, 16, 1024);
+                const uint64_t dSh = tc::sdesc(sS, 1024, 1024), dSl = tc::sdesc(sS + 16384, 1024, 1024);
+                const uint64_t ta[3] = {dAh, dAl, dAh}, tb[3] = {dSl, dSh, dSh};
+                uint32_t acc = 0;
+#pragma unroll
+                for (int tm3 = 0; tm3 < 3; ++tm3)
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        tc::mma(taddr, ta[tm3] + uint64_t(((s >> 2) * 16384 + (s & 3) * 32) >> 4),
+                                tb[tm3] + uint64_t((s * 2048) >> 4), ID1, acc);
+                        acc = 1;
+                    }
+            } else {
+                *abort_flag = 1;
+            }
+            tc::mma_commit(&bar[2]);
+        }
+        __syncwarp();
+        // while MMA1 runs: the saved start state, this chunk's U row and e^gL
+        if (fwd && p.sS) {
+            __nv_bfloat16* dst = p.sS + chd * 2 * D * D + size_t(row) * D + col0 + cc;
+            st_g32(dst, sh);
+            st_g32(dst + D * D, sl);
+        }
+        const float eg = egn;
+        const int4 info = infon;
+        if (!tc::mbar_wait(&bar[2], ph)) *abort_flag = 1;
+        tc::fence_after_sync();
+        if (tid == 0 && ci + 1 < c1 && !*abort_flag) {
+            load_A1(ci + 1);
+            pendA = int(ph ^ 1u);
+        }
+        __syncwarp();
+
+        // ---- Delta = U - W S (lanes 0..63) ----
+        if (qd < 2) {
+            float v[32];
+            tc::tmem_ld32(tD1 + cc, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = Un[j] - v[j];
+            uint32_t dhh[16], dll[16];
+            split32(v, dhh, dll);
+            st_sw128(sm + OFF_DL, row, cc, dhh);
+            st_sw128(sm + OFF_DL + 8192, row, cc, dll);
+            if (fwd && p.sDelta) {
+                __nv_bfloat16* dst = p.sDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
+                st_g32(dst, dhh);
+                st_g32(dst + CH * D, dll);
+            }
+        }
+        fetch_next(ci + 1);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (*abort_flag) break;
+
+        // ---- MMA2: D2 = Kb^T Delta;  MMA3: D1 += [*; Aqk] Delta ----
+        if (tid == 0) {
+            if (tc::mbar_wait(&bar[1], ph)) {
+                pendK = -1;
+                tc::fence_after_sync();
+                const uint64_t dKh = tc::sdesc(sKt, 8192, 1024), dKl = tc::sdesc(sKt + 16384, 8192, 1024);
+                const uint64_t dDh = tc::sdesc(sDl, 1024, 1024), dDl = tc::sdesc(sDl + 8192, 1024, 1024);
+                const uint64_t ka[3] = {dKh, dKl, dKh}, db[3] = {dDl, dDh, dDh};
+                uint32_t acc = 0;
+#pragma unroll
+                for (int tm3 = 0; tm3 < 3; ++tm3)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        tc::mma(taddr + 64, ka[tm3] + uint64_t((s * 2048) >> 4),
+                                db[tm3] + uint64_t((s * 2048) >> 4), ID2, acc);
+                        acc = 1;
+                    }
+                if (want_o) {
+                    const uint64_t dQh = tc::sdesc(sPad, 16, 1024), dQl = tc::sdesc(sPad + 8192, 16, 1024);
+                    const uint64_t qa[3] = {dQh, dQl, dQh};
+#pragma unroll
+                    for (int tm3 = 0; tm3 < 3; ++tm3)
+#pragma unroll
+                        for (int s = 0; s < 4; ++s)
+                            tc::mma(taddr, qa[tm3] + uint64_t((s * 32) >> 4),
+                                    db[tm3] + uint64_t((s * 2048) >> 4), ID1, 1u);
+                }
+            } else {
+                *abort_flag = 1;
+            }
+            tc::mma_commit(&bar[3]);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
+        tc::fence_after_sync();
+        if (tid == 0 && ci + 1 < c1 && !*abort_flag) {
+            load_K(ci + 1);
+            pendK = int(ph ^ 1u);
+        }
+        __syncwarp();
+
+        // ---- S = e^gL * S + Kb^T Delta;  O rows (lanes 64..127) ----
+        {
+            float v[32];
+            tc::tmem_ld32(tD2 + cc, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) Sr[j] = fmaf(eg, Sr[j], v[j]);
+        }
+        if (want_o && qd >= 2) {
+            float v[32];
+            tc::tmem_ld32(tD1 + cc, v);
+            const int t = row - 64;
+            if (t < info.z) {
+                const size_t off = (size_t(info.y + t) * p.H + h) * D + col0 + cc;
+                if (p.out_fp32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + off);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(p.scale * v[4 * j], p.scale * v[4 * j + 1],
+                                             p.scale * v[4 * j + 2], p.scale * v[4 * j + 3]);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + off);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(pack2(p.scale * v[8 * j], p.scale * v[8 * j + 1]),
+                                            pack2(p.scale * v[8 * j + 2], p.scale * v[8 * j + 3]),
+                                            pack2(p.scale * v[8 * j + 4], p.scale * v[8 * j + 5]),
+                                            pack2(p.scale * v[8 * j + 6], p.scale * v[8 * j + 7]));
+                }
+            }
+        }
+    }
+
+    if (*abort_flag) {
+        // after a timed-out wait: let the loads still in flight land (bounded), report, stop
+        if (tid == 0) {
+            if (pendA >= 0) tc::mbar_wait(&bar[0], uint32_t(pendA), 100000000ull);
+            if (pendK >= 0) tc::mbar_wait(&bar[1], uint32_t(pendK), 100000000ull);
+            p.status[0] = KDA_ERR_TIMEOUT;
+        }
+    } else {
+        float* out = fwd ? p.ht : (fragX ? p.fragM : p.fragB);
+        if (out) {
+            float4* dst = reinterpret_cast<float4*>(out + dh + size_t(row) * D + col0 + cc);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(Sr[4 * j], Sr[4 * j + 1], Sr[4 * j + 2], Sr[4 * j + 3]);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (w == 0) tc::tmem_dealloc(taddr, 128);
+}
+
+}  // namespace kda

@@ -11,6 +11,7 @@
 // Delta Networks" and "Gated Linear Attention"), applied here to the KDA recurrence.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -291,9 +292,18 @@ __device__ __forceinline__ void zero_acc(float (&acc)[RM][RN]) {
 // Scratch for block_gemm: KT x (M + N) floats, M + N <= 256.
 constexpr int GEMM_SCRATCH = 16 * 256;
 
+// TMA tensor maps of the state-recurrence operands, built on the host for each call over the
+// intra-chunk record: every plane is a run of (chunk, head) tiles, tile index = plane start +
+// chunk * H + head.
+struct TcMaps {
+    CUtensorMap m128;  // W, Qg, Kb hi / lo planes as [tile][64 rows][128 bf16]
+    CUtensorMap m64;   // Aqk hi / lo planes as [tile][64 rows][64 bf16]
+    int zWh, zWl, zQh, zQl, zKh, zKl, zAh, zAl;  // first tile of each plane
+};
+
 // ---- kernels (defined in the .cu files) and their dynamic shared memory ----
 size_t intra_smem_bytes();
-size_t chain_fwd_smem_bytes();
+size_t chain_fwd_tc_smem_bytes();
 size_t chain_bwd_smem_bytes();
 size_t bwd_gemm_smem_bytes();
 size_t bwd_intra_smem_bytes();
@@ -303,7 +313,7 @@ constexpr int INTRA_THREADS = 512;  // threads of the forward intra-chunk kernel
 constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences
 __global__ void k_plan(Params p);
 __global__ void k_intra_fwd(Params p);
-__global__ void k_chain_fwd(Params p, int mode);
+__global__ void k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
 __global__ void k_chain_bwd(Params p, int mode);
 __global__ void k_bwd_gemms(Params p);
 __global__ void k_bwd_intra(Params p);

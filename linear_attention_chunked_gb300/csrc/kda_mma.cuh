@@ -40,9 +40,10 @@ __device__ __forceinline__ uint32_t pack2(float x0, float x1) {
     return bits(__floats2bfloat162_rn(x0, x1));
 }
 
+// Not volatile: a pure register operation, so the compiler may interleave independent MMAs.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

@@ -11,7 +11,7 @@ namespace {
 
 const size_t SMEM_INTRA_FWD = intra_smem_bytes();
 const size_t SMEM_CHAIN_FWD_TC = chain_fwd_tc_smem_bytes();
-const size_t SMEM_CHAIN_BWD = chain_bwd_smem_bytes();
+const size_t SMEM_CHAIN_BWD_TC = chain_bwd_tc_smem_bytes();
 const size_t SMEM_BWD_GEMMS = bwd_gemm_smem_bytes();
 const size_t SMEM_BWD_INTRA = bwd_intra_smem_bytes();
 constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
@@ -33,7 +33,7 @@ kda_status setup_device() {
     if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
     struct { const void* f; size_t smem; } attrs[] = {
         {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd_tc, SMEM_CHAIN_FWD_TC},
-        {(const void*)k_chain_bwd, SMEM_CHAIN_BWD}, {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
+        {(const void*)k_chain_bwd_tc, SMEM_CHAIN_BWD_TC}, {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
         {(const void*)k_bwd_intra, SMEM_BWD_INTRA}, {(const void*)k_walk, SMEM_WALK},
     };
     for (auto& a : attrs)
@@ -194,6 +194,22 @@ kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
     return KDA_OK;
 }
 
+// Tensor map of dO [T][H][128] bf16: boxes of 64 values x 1 head x 64 tokens (128-byte swizzle);
+// tokens at or past T read as zero.
+kda_status make_dO_map(const void* dO, int64_t T, int H, TcMaps* tm) {
+    if (T <= 0) return KDA_OK;  // no chunks: the map is never used
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return KDA_ERR_CUDA;
+    const cuuint32_t box[3] = {64, 1, 64}, es[3] = {1, 1, 1};
+    const cuuint64_t dims[3] = {D, cuuint64_t(H), cuuint64_t(T)};
+    const cuuint64_t strides[2] = {D * 2, cuuint64_t(H) * D * 2};
+    if (enc(&tm->mdO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(dO), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status launched() {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -272,7 +288,7 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     p.ht = ht;
     if (saved) set_saved(p, L, static_cast<char*>(saved), true);
     else set_saved(p, L, static_cast<char*>(ws) + L.intra_ws, false);
-    TcMaps tm;
+    TcMaps tm{};
     if (kda_status s = make_tc_maps(p, L, &tm)) return s;
     if (kda_status s = run_prologue(p, st)) return s;
     {
@@ -340,14 +356,15 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
     char* sv = saved ? static_cast<char*>(const_cast<void*>(saved))
                      : static_cast<char*>(ws) + L.replay;
     set_saved(p, L, sv, true);
+    TcMaps tm{};
+    if (kda_status s = make_tc_maps(p, L, &tm)) return s;
+    if (kda_status s = make_dO_map(dO, pr->T, pr->H, &tm)) return s;
     if (saved) {
         // the saved set already holds the intra products and states: only the chunk plan
         ProfScope ps(KK_PLAN, st);
         k_plan<<<1, NTHR, 0, st>>>(p);
     } else {
         // checkpoint replay: recompute the intra products, the states and the write vectors
-        TcMaps tm;
-        if (kda_status s = make_tc_maps(p, L, &tm)) return s;
         if (kda_status s = run_prologue(p, st)) return s;
         Params r = p;
         r.o = nullptr;
@@ -358,7 +375,8 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
     }
     {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD, st>>>(p, CHAIN_BWD);
+        k_chain_bwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
+            p, CHAIN_BWD, tm);
     }
     if (L.maxC > 0) {
         const dim3 grid(unsigned(L.maxC), pr->H);
@@ -397,8 +415,10 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     p.fragM = M;
     p.fragB = B_or_C;
     set_saved(p, L, static_cast<char*>(ws) + L.intra_ws, false);
-    TcMaps tm;
+    TcMaps tm{};
     if (kda_status s = make_tc_maps(p, L, &tm)) return s;
+    if (mode == KDA_FRAG_BWD)
+        if (kda_status s = make_dO_map(dO, pr->T, pr->H, &tm)) return s;
     if (kda_status s = run_prologue(p, st)) return s;
     if (mode == KDA_FRAG_FWD) {
         ProfScope ps(KK_CHAIN_FWD, st);
@@ -406,7 +426,8 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
             p, CHAIN_FRAG_MB, tm);
     } else {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD, st>>>(p, CHAIN_FRAG_C);
+        k_chain_bwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
+            p, CHAIN_FRAG_C, tm);
     }
     return launched();
 }

@@ -1,5 +1,5 @@
-// Backward-side kernels: reverse state recurrence, per-chunk gradient products, intra-chunk
-// gradients, deterministic parameter reduction.
+// Backward-side per-chunk kernels: gradient products, intra-chunk gradients, deterministic
+// parameter reduction (the reverse state recurrence is in the tcgen05 recurrence file).
 //
 // Per chunk (adjoint of the forward lines in kda_internal.cuh), with dS1 the gradient at the
 // chunk-end state and dO already multiplied by the output scale:
@@ -20,17 +20,6 @@ namespace {
 constexpr int LB = 136;   // row stride (bf16) of [rows][128] tiles
 constexpr int LB64 = 72;  // row stride (bf16) of [rows][64] tiles
 
-struct ChainBwdSmem {
-    __nv_bfloat16 dS[2][D * LB64];   // dS [key][64 values] (hi, lo)
-    __nv_bfloat16 X[2][CH * LB64];   // -dDelta [token][64 values] (hi, lo)
-    __nv_bfloat16 A[2][CH * LB64];   // Aqk [token][token]
-    __nv_bfloat16 K[2][CH * LB];     // Kb [token][key]
-    __nv_bfloat16 Q[2][CH * LB];     // Qg [token][key]
-    __nv_bfloat16 W[2][CH * LB];     // W [token][key]
-    __nv_bfloat16 dO[2][CH * LB64];  // dO [token][64 values], double buffered (exact bf16)
-    float eGL[D];
-};
-
 struct BwdGemmSmem {
     __nv_bfloat16 M[2][CH * LB64];   // Minv (hi, lo)
     __nv_bfloat16 X[2][CH * LB];     // dDelta (hi, lo)
@@ -40,219 +29,11 @@ struct BwdGemmSmem {
     __nv_bfloat16 Dl[2][CH * LB];    // Delta (hi, lo)
 };
 
-static_assert(sizeof(ChainBwdSmem) <= 232448, "chain shared memory above the opt-in limit");
 static_assert(sizeof(BwdGemmSmem) <= 232448, "backward GEMM shared memory above the opt-in limit");
 
 }  // namespace
 
-size_t chain_bwd_smem_bytes() { return sizeof(ChainBwdSmem); }
 size_t bwd_gemm_smem_bytes() { return sizeof(BwdGemmSmem); }
-
-// Reverse state recurrence of one (document, head, 64-column value half) on tensor cores.
-// Eight warps: warp w = (wq, wn), wq = w % 4 (row group), wn = w / 4 (32-column quarter).  Warp w
-// keeps keys 32 wq.. x columns 32 wn.. of the FP32 gradient dS in registers; per chunk, going back:
-//   A': dDelta = scale Aqk^T dO + Kb dS1     (tokens 16 wq..16 wq+15)
-//   D': dS0 = e^gL * dS1 + scale Qg^T dO - W^T dDelta
-// mode CHAIN_BWD: dS from dht; per chunk writes dS1 and dDelta for the per-chunk kernels; dh0.
-// mode CHAIN_FRAG_C: dS from zero; writes C (= dS at the fragment start) to fragB.
-__global__ void __launch_bounds__(CHAIN_THREADS) k_chain_bwd(Params p, int mode) {
-    constexpr int BT = CHAIN_THREADS;
-    const int n = blockIdx.x, h = blockIdx.y, hv = blockIdx.z;
-    const bool bwd = mode == CHAIN_BWD;
-    const int col0 = hv * 64;
-    extern __shared__ __align__(16) unsigned char smraw[];
-    ChainBwdSmem& sm = *reinterpret_cast<ChainBwdSmem*>(smraw);
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int wq = w & 3, wn = w >> 2, cq = 32 * wn;
-    const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
-    const size_t dh = (size_t(n) * p.H + h) * D * D;
-
-    float dS[2][4][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = 32 * wq + 16 * mt + g + 8 * (e >> 1);
-                const int val = col0 + cq + 8 * nt + 2 * t + (e & 1);
-                dS[mt][nt][e] = (bwd && p.dht) ? p.dht[dh + size_t(key) * D + val] : 0.f;
-            }
-    // writes dS's hi / lo split to shared memory (B operand of the next step)
-    auto store_dS = [&]() {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int key = 32 * wq + 16 * mt + g + 8 * hf, col = cq + 8 * nt + 2 * t;
-                    uint32_t hi, lo;
-                    split2(dS[mt][nt][2 * hf], dS[mt][nt][2 * hf + 1], hi, lo);
-                    *reinterpret_cast<uint32_t*>(&sm.dS[0][key * LB64 + col]) = hi;
-                    *reinterpret_cast<uint32_t*>(&sm.dS[1][key * LB64 + col]) = lo;
-                }
-    };
-    // group X(ci): Aqk, Kb, dO(ci) -> dO buffer (c1-1-ci)&1 ; group Y(ci): Qg, W, e^gL
-    auto issue_X = [&](int ci) {
-        if (ci >= c0) {
-            const int4 info = p.chunk_tab[ci];
-            const size_t chd = size_t(ci) * p.H + h;
-            cp_tile_bf16(sm.A[0], LB64, p.Ah + chd * CH * CH, CH, CH, CH, tid, BT);
-            cp_tile_bf16(sm.A[1], LB64, p.Al + chd * CH * CH, CH, CH, CH, tid, BT);
-            cp_tile_bf16(sm.K[0], LB, p.Kh + chd * CH * D, D, CH, D, tid, BT);
-            cp_tile_bf16(sm.K[1], LB, p.Kl + chd * CH * D, D, CH, D, tid, BT);
-            __nv_bfloat16* dst = sm.dO[(c1 - 1 - ci) & 1];
-            for (int i = tid; i < CH * 8; i += BT) {
-                const int r = i >> 3, c = (i & 7) * 8;
-                const bool ok = r < info.z;
-                const size_t row = size_t(info.y + (ok ? r : 0));
-                cp16z(dst + r * LB64 + c, p.dO + (row * p.H + h) * D + col0 + c, ok);
-            }
-        }
-        cp_commit();
-    };
-    auto issue_Y = [&](int ci) {
-        if (ci >= c0) {
-            const size_t chd = size_t(ci) * p.H + h;
-            cp_tile_bf16(sm.Q[0], LB, p.Qh + chd * CH * D, D, CH, D, tid, BT);
-            cp_tile_bf16(sm.Q[1], LB, p.Ql + chd * CH * D, D, CH, D, tid, BT);
-            cp_tile_bf16(sm.W[0], LB, p.Wh + chd * CH * D, D, CH, D, tid, BT);
-            cp_tile_bf16(sm.W[1], LB, p.Wl + chd * CH * D, D, CH, D, tid, BT);
-            cp_tile_f32(sm.eGL, D, p.eGL + chd * D, D, 1, D, tid, BT);
-        }
-        cp_commit();
-    };
-    issue_X(c1 - 1);
-    issue_Y(c1 - 1);
-    store_dS();
-
-    for (int ci = c1 - 1; ci >= c0; --ci) {
-        const size_t chd = size_t(ci) * p.H + h;
-        const __nv_bfloat16* sdO = sm.dO[(c1 - 1 - ci) & 1];
-        // ---- A': dDelta = scale Aqk^T dO + Kb dS1 ----
-        cp_wait<1>();
-        __syncthreads();
-        if (bwd) {  // gradient at the end of this chunk: the split in shared memory
-            __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + col0;
-            st_tile_bf16(dst, D, sm.dS[0], LB64, D, 64, tid, BT);
-            st_tile_bf16(dst + D * D, D, sm.dS[1], LB64, D, 64, tid, BT);
-        }
-        {
-            float a1[4][4] = {}, a2[4][4] = {};
-            for (int ks = wq; ks < 4; ++ks) {  // Aqk^T is upper triangular
-                uint32_t ah[4], al[4];
-                ldsm4t(ah, at_addr(sm.A[0], LB64, 16 * wq, 16 * ks, lane));
-                ldsm4t(al, at_addr(sm.A[1], LB64, 16 * wq, 16 * ks, lane));
-#pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t b[4];
-                    ldsm4t(b, bk_addr(sdO, LB64, 16 * ks, cq + 16 * np, lane));
-                    mma_x2(a1[2 * np], ah, al, b[0], b[1]);
-                    mma_x2(a1[2 * np + 1], ah, al, b[2], b[3]);
-                }
-            }
-#pragma unroll 2
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t ah[4], al[4];
-                ldsm4(ah, a_addr(sm.K[0], LB, 16 * wq, 16 * ks, lane));
-                ldsm4(al, a_addr(sm.K[1], LB, 16 * wq, 16 * ks, lane));
-#pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t bh[4], bl[4];
-                    ldsm4t(bh, bk_addr(sm.dS[0], LB64, 16 * ks, cq + 16 * np, lane));
-                    ldsm4t(bl, bk_addr(sm.dS[1], LB64, 16 * ks, cq + 16 * np, lane));
-                    mma_x3(a2[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                    mma_x3(a2[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int row = 16 * wq + g + 8 * hf, col = cq + 8 * nt + 2 * t;
-                    const float d0 = fmaf(p.scale, a1[nt][2 * hf], a2[nt][2 * hf]);
-                    const float d1 = fmaf(p.scale, a1[nt][2 * hf + 1], a2[nt][2 * hf + 1]);
-                    uint32_t hi, lo;
-                    split2(-d0, -d1, hi, lo);
-                    *reinterpret_cast<uint32_t*>(&sm.X[0][row * LB64 + col]) = hi;
-                    *reinterpret_cast<uint32_t*>(&sm.X[1][row * LB64 + col]) = lo;
-
-                }
-        }
-        __syncthreads();
-        issue_X(ci - 1);
-        if (bwd) {  // planes of +dDelta (shared memory holds -dDelta; the split of -x is -split(x))
-            __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + col0;
-            st_tile_bf16(dst, D, sm.X[0], LB64, CH, 64, tid, BT, 0x80008000u);
-            st_tile_bf16(dst + CH * D, D, sm.X[1], LB64, CH, 64, tid, BT, 0x80008000u);
-        }
-        // ---- D': dS0 = e^gL dS1 + scale Qg^T dO - W^T dDelta ----
-        cp_wait<1>();
-        __syncthreads();
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float eg = sm.eGL[32 * wq + 16 * mt + g + 8 * (e >> 1)];
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) dS[mt][nt][e] *= eg;
-            }
-        {
-            float tq[2][4][4] = {};
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                uint32_t qh[2][4], ql[2][4], wh[2][4], wl[2][4];
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    ldsm4t(qh[mt], at_addr(sm.Q[0], LB, 32 * wq + 16 * mt, 16 * ks, lane));
-                    ldsm4t(ql[mt], at_addr(sm.Q[1], LB, 32 * wq + 16 * mt, 16 * ks, lane));
-                    ldsm4t(wh[mt], at_addr(sm.W[0], LB, 32 * wq + 16 * mt, 16 * ks, lane));
-                    ldsm4t(wl[mt], at_addr(sm.W[1], LB, 32 * wq + 16 * mt, 16 * ks, lane));
-                }
-#pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t b[4], xh[4], xl[4];
-                    ldsm4t(b, bk_addr(sdO, LB64, 16 * ks, cq + 16 * np, lane));
-                    ldsm4t(xh, bk_addr(sm.X[0], LB64, 16 * ks, cq + 16 * np, lane));
-                    ldsm4t(xl, bk_addr(sm.X[1], LB64, 16 * ks, cq + 16 * np, lane));
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        mma_x2(tq[mt][2 * np], qh[mt], ql[mt], b[0], b[1]);
-                        mma_x2(tq[mt][2 * np + 1], qh[mt], ql[mt], b[2], b[3]);
-                        mma_x3(dS[mt][2 * np], wh[mt], wl[mt], xh[0], xh[1], xl[0], xl[1]);
-                        mma_x3(dS[mt][2 * np + 1], wh[mt], wl[mt], xh[2], xh[3], xl[2], xl[3]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) dS[mt][nt][e] = fmaf(p.scale, tq[mt][nt][e], dS[mt][nt][e]);
-        }
-        __syncthreads();
-        issue_Y(ci - 1);
-        store_dS();
-    }
-    cp_wait<0>();
-    float* out = bwd ? p.dh0 : p.fragB;
-    if (out) {
-        out += dh;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int key = 32 * wq + 16 * mt + g + 8 * hf;
-                    const int val = col0 + cq + 8 * nt + 2 * t;
-                    *reinterpret_cast<float2*>(out + size_t(key) * D + val) =
-                        make_float2(dS[mt][nt][2 * hf], dS[mt][nt][2 * hf + 1]);
-                }
-    }
-}
 
 // Per-chunk gradient products that need the chunk's states (tensor cores, 8 warps):
 //   dR = Minv^T dDelta, P = dR S0^T, dQg = dO S0^T, dAqk = tril(dO Delta^T),

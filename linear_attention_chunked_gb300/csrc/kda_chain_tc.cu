@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         for (int i = 0; i < 4; ++i) tc::mbar_init(&bar[i], 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
-        tc::tma_prefetch_map(&tm.m128);
-        tc::tma_prefetch_map(&tm.m64);
+        if (c0 < c1) {
+            tc::tma_prefetch_map(&tm.m128);
+            tc::tma_prefetch_map(&tm.m64);
+        }
     }
     if (w == 0) tc::tmem_alloc(tslot, 128);
     for (int i = tid; i < 8192 / 16; i += CHAIN_THREADS)
@@ -356,6 +358,287 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     tc::fence_before_sync();
     __syncthreads();
     if (w == 0) tc::tmem_dealloc(taddr, 128);
+}
+
+
+// ------------------------------------------------------------------------------------------------
+// Backward state recurrence (reverse over the chunks of a document), same machinery.  Per chunk,
+// with dS = dS1 (gradient at the chunk end) in registers:
+//   MMA-A  DA = Kb dS1 (M = 128: rows 64..127 unused), DT = Aqk^T dO (dO exact bf16: two terms)
+//          dDelta = scale DT + DA                           (lanes 0..63)
+//   MMA-D  DQ = Qg^T dO,  DW = W^T dDelta                   (M = 128 keys)
+//          dS0 = e^gL * dS1 + scale DQ - DW                 (every thread, its own key row)
+// mode CHAIN_BWD: dS from dht; writes the dS1 and dDelta planes of every chunk and dh0.
+// mode CHAIN_FRAG_C: dS from zero; writes only the fragment-start gradient C (into p.fragB).
+namespace {
+
+constexpr int B_OFF_KB = 0;        // Kb K-major [plane][2 key blocks][64 tokens][128 B]     32 KB
+constexpr int B_OFF_QG = 32768;    // Qg MN-major [plane][2 key blocks][64 tokens][128 B]    32 KB
+constexpr int B_OFF_W = 65536;     // W MN-major, same layout                                32 KB
+constexpr int B_OFF_AQ = 98304;    // Aqk as MN-major A of Aqk^T: [plane][64 t][128 B]       16 KB
+constexpr int B_OFF_DO = 114688;   // dO MN-major B: [64 tokens][128 B]                        8 KB
+constexpr int B_OFF_DS = 122880;   // dS1 MN-major B: [plane][128 keys][128 B]               32 KB
+constexpr int B_OFF_DD = 155648;   // dDelta MN-major B: [plane][64 tokens][128 B]           16 KB
+constexpr int B_OFF_BAR = 172032;  // mbarriers, TMEM base address, abort flag
+constexpr size_t CHAIN_BWD_TC_SMEM = B_OFF_BAR + 128 + 1024;
+
+static_assert(CHAIN_BWD_TC_SMEM <= 232448, "tcgen05 chain shared memory above the opt-in limit");
+
+}  // namespace
+
+size_t chain_bwd_tc_smem_bytes() { return CHAIN_BWD_TC_SMEM; }
+
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+    k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm) {
+    const int n = blockIdx.x, h = blockIdx.y, hv = blockIdx.z;
+    const bool bwd = mode == CHAIN_BWD;
+    const int col0 = hv * 64;
+    extern __shared__ unsigned char smraw[];
+    unsigned char* sm = align1024(smraw);
+    // barriers: 0 Kb+Aqk in, 1 dO in, 2 Qg+W in, 3 MMA-A done, 4 MMA-D done
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + B_OFF_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_OFF_BAR + 48);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 52);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int qd = w & 3, cc = 32 * (w >> 2);
+    const int row = 32 * qd + lane;
+    const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
+    const size_t dh = (size_t(n) * p.H + h) * D * D;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        if (c0 < c1) {
+            tc::tma_prefetch_map(&tm.m128);
+            tc::tma_prefetch_map(&tm.m64);
+            tc::tma_prefetch_map(&tm.mdO);
+        }
+    }
+    if (w == 0) tc::tmem_alloc(tslot, 256);
+
+    float dSr[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        dSr[j] = (bwd && p.dht) ? p.dht[dh + size_t(row) * D + col0 + cc + j] : 0.f;
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t taddr = *tslot;
+    const uint32_t tl = taddr + (uint32_t(32 * qd) << 16);
+    const uint32_t tDA = tl, tDT = tl + 64, tDQ = tl + 128, tDW = tl + 192;
+
+    const uint32_t IDA1 = tc::idesc_bf16(128, 64, false, true);  // Kb K-major, dS1 MN-major
+    const uint32_t IDMN = tc::idesc_bf16(128, 64, true, true);   // MN-major A and B
+    const uint32_t sKb = smem_u32(sm + B_OFF_KB), sQg = smem_u32(sm + B_OFF_QG);
+    const uint32_t sW = smem_u32(sm + B_OFF_W), sAq = smem_u32(sm + B_OFF_AQ);
+    const uint32_t sdO = smem_u32(sm + B_OFF_DO), sdS = smem_u32(sm + B_OFF_DS);
+    const uint32_t sdD = smem_u32(sm + B_OFF_DD);
+
+    auto load_KA = [&](int ci) {
+        const int chd = ci * p.H + h;
+        tc::mbar_expect_tx(&bar[0], 49152u);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + B_OFF_KB + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[0]);
+            tma_load_3d(sm + B_OFF_KB + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[0]);
+        }
+        tma_load_3d(sm + B_OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[0]);
+        tma_load_3d(sm + B_OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[0]);
+    };
+    auto load_O = [&](int t0) {
+        tc::mbar_expect_tx(&bar[1], 8192u);
+        tma_load_3d(sm + B_OFF_DO, &tm.mdO, col0, h, t0, &bar[1]);
+    };
+    auto load_QW = [&](int ci) {
+        const int chd = ci * p.H + h;
+        tc::mbar_expect_tx(&bar[2], 65536u);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + B_OFF_QG + b * 8192, &tm.m128, 64 * b, 0, tm.zQh + chd, &bar[2]);
+            tma_load_3d(sm + B_OFF_QG + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zQl + chd, &bar[2]);
+            tma_load_3d(sm + B_OFF_W + b * 8192, &tm.m128, 64 * b, 0, tm.zWh + chd, &bar[2]);
+            tma_load_3d(sm + B_OFF_W + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zWl + chd, &bar[2]);
+        }
+    };
+    // next chunk's e^gL of this thread's key and first token, fetched one chunk ahead
+    float egn = 0.f;
+    int t0n = 0;
+    auto fetch_next = [&](int ci) {
+        if (ci >= c0) {
+            egn = p.eGL[(size_t(ci) * p.H + h) * D + row];
+            if (tid == 0) t0n = p.chunk_tab[ci].y;
+        }
+    };
+    fetch_next(c1 - 1);
+    int pend[3] = {-1, -1, -1};  // phase parity of the loads in flight per barrier (thread 0)
+    if (tid == 0 && c0 < c1) {
+        load_KA(c1 - 1);
+        load_O(t0n);
+        load_QW(c1 - 1);
+        pend[0] = pend[1] = pend[2] = 0;
+    }
+
+    for (int ci = c1 - 1; ci >= c0; --ci) {
+        const uint32_t ph = uint32_t(c1 - 1 - ci) & 1u;
+        const size_t chd = size_t(ci) * p.H + h;
+        {   // dS1 operand (+ its saved planes)
+            uint32_t hh[16], ll[16];
+            split32(dSr, hh, ll);
+            st_sw128(sm + B_OFF_DS, row, cc, hh);
+            st_sw128(sm + B_OFF_DS + 16384, row, cc, ll);
+            if (bwd) {
+                __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + size_t(row) * D + col0 + cc;
+                st_g32(dst, hh);
+                st_g32(dst + D * D, ll);
+            }
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (*abort_flag) break;
+
+        // ---- MMA-A: DA = Kb dS1, DT = Aqk^T dO ----
+        if (tid == 0) {
+            if (tc::mbar_wait(&bar[0], ph) && tc::mbar_wait(&bar[1], ph)) {
+                pend[0] = pend[1] = -1;
+                tc::fence_after_sync();
+                const uint64_t kh = tc::sdesc(sKb, 16, 1024), kl = tc::sdesc(sKb + 16384, 16, 1024);
+                const uint64_t dh_ = tc::sdesc(sdS, 1024, 1024), dl_ = tc::sdesc(sdS + 16384, 1024, 1024);
+                const uint64_t ta[3] = {kh, kl, kh}, tb[3] = {dl_, dh_, dh_};
+                uint32_t acc = 0;
+#pragma unroll
+                for (int t3 = 0; t3 < 3; ++t3)
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        tc::mma(taddr, ta[t3] + uint64_t(((s >> 2) * 8192 + (s & 3) * 32) >> 4),
+                                tb[t3] + uint64_t((s * 2048) >> 4), IDA1, acc);
+                        acc = 1;
+                    }
+                const uint64_t ah = tc::sdesc(sAq, 8192, 1024), al = tc::sdesc(sAq + 8192, 8192, 1024);
+                const uint64_t bo = tc::sdesc(sdO, 1024, 1024);
+                acc = 0;
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        tc::mma(taddr + 64, (t2 ? ah : al) + uint64_t((s * 2048) >> 4),
+                                bo + uint64_t((s * 2048) >> 4), IDMN, acc);
+                        acc = 1;
+                    }
+            } else {
+                *abort_flag = 1;
+            }
+            tc::mma_commit(&bar[3]);
+        }
+        __syncwarp();
+        const float eg = egn;
+        if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
+        tc::fence_after_sync();
+        if (tid == 0 && ci > c0 && !*abort_flag) {
+            load_KA(ci - 1);
+            pend[0] = int(ph ^ 1u);
+        }
+        __syncwarp();
+
+        // ---- dDelta = scale DT + DA (lanes 0..63) ----
+        if (qd < 2) {
+            float a[32], t[32];
+            tc::tmem_ld32(tDA + cc, a);
+            tc::tmem_ld32(tDT + cc, t);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = fmaf(p.scale, t[j], a[j]);
+            uint32_t hh[16], ll[16];
+            split32(a, hh, ll);
+            st_sw128(sm + B_OFF_DD, row, cc, hh);
+            st_sw128(sm + B_OFF_DD + 8192, row, cc, ll);
+            if (bwd) {
+                __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
+                st_g32(dst, hh);
+                st_g32(dst + CH * D, ll);
+            }
+        }
+        fetch_next(ci - 1);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (*abort_flag) break;
+
+        // ---- MMA-D: DQ = Qg^T dO, DW = W^T dDelta ----
+        if (tid == 0) {
+            if (tc::mbar_wait(&bar[2], ph)) {
+                pend[2] = -1;
+                tc::fence_after_sync();
+                const uint64_t qh = tc::sdesc(sQg, 8192, 1024), ql = tc::sdesc(sQg + 16384, 8192, 1024);
+                const uint64_t bo = tc::sdesc(sdO, 1024, 1024);
+                uint32_t acc = 0;
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        tc::mma(taddr + 128, (t2 ? qh : ql) + uint64_t((s * 2048) >> 4),
+                                bo + uint64_t((s * 2048) >> 4), IDMN, acc);
+                        acc = 1;
+                    }
+                const uint64_t wh = tc::sdesc(sW, 8192, 1024), wl = tc::sdesc(sW + 16384, 8192, 1024);
+                const uint64_t xh = tc::sdesc(sdD, 1024, 1024), xl = tc::sdesc(sdD + 8192, 1024, 1024);
+                const uint64_t ta[3] = {wh, wl, wh}, tb[3] = {xl, xh, xh};
+                acc = 0;
+#pragma unroll
+                for (int t3 = 0; t3 < 3; ++t3)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        tc::mma(taddr + 192, ta[t3] + uint64_t((s * 2048) >> 4),
+                                tb[t3] + uint64_t((s * 2048) >> 4), IDMN, acc);
+                        acc = 1;
+                    }
+            } else {
+                *abort_flag = 1;
+            }
+            tc::mma_commit(&bar[4]);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(&bar[4], ph)) *abort_flag = 1;
+        tc::fence_after_sync();
+        if (tid == 0 && ci > c0 && !*abort_flag) {
+            load_O(t0n);
+            load_QW(ci - 1);
+            pend[1] = pend[2] = int(ph ^ 1u);
+        }
+        __syncwarp();
+
+        // ---- dS0 = e^gL * dS1 + scale DQ - DW ----
+        {
+            float q[32], x[32];
+            tc::tmem_ld32(tDQ + cc, q);
+            tc::tmem_ld32(tDW + cc, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dSr[j] = fmaf(eg, dSr[j], fmaf(p.scale, q[j], -x[j]));
+        }
+    }
+
+    if (*abort_flag) {
+        if (tid == 0) {
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+                if (pend[i] >= 0) tc::mbar_wait(&bar[i], uint32_t(pend[i]), 100000000ull);
+            p.status[0] = KDA_ERR_TIMEOUT;
+        }
+    } else {
+        float* out = bwd ? p.dh0 : p.fragB;
+        if (out) {
+            float4* dst = reinterpret_cast<float4*>(out + dh + size_t(row) * D + col0 + cc);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(dSr[4 * j], dSr[4 * j + 1], dSr[4 * j + 2], dSr[4 * j + 3]);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (w == 0) tc::tmem_dealloc(taddr, 256);
 }
 
 }  // namespace kda

@@ -298,13 +298,14 @@ constexpr int GEMM_SCRATCH = 16 * 256;
 struct TcMaps {
     CUtensorMap m128;  // W, Qg, Kb hi / lo planes as [tile][64 rows][128 bf16]
     CUtensorMap m64;   // Aqk hi / lo planes as [tile][64 rows][64 bf16]
+    CUtensorMap mdO;   // dO [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens} (backward)
     int zWh, zWl, zQh, zQl, zKh, zKl, zAh, zAl;  // first tile of each plane
 };
 
 // ---- kernels (defined in the .cu files) and their dynamic shared memory ----
 size_t intra_smem_bytes();
 size_t chain_fwd_tc_smem_bytes();
-size_t chain_bwd_smem_bytes();
+size_t chain_bwd_tc_smem_bytes();
 size_t bwd_gemm_smem_bytes();
 size_t bwd_intra_smem_bytes();
 constexpr int CHAIN_THREADS = 256;  // 8 warps per state-recurrence block
@@ -314,7 +315,7 @@ constexpr int NHALF = 2;            // value halves (64 columns) per head in the
 __global__ void k_plan(Params p);
 __global__ void k_intra_fwd(Params p);
 __global__ void k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
-__global__ void k_chain_bwd(Params p, int mode);
+__global__ void k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
 __global__ void k_bwd_gemms(Params p);
 __global__ void k_bwd_intra(Params p);
 __global__ void k_param_reduce(Params p);

@@ -190,7 +190,13 @@ def _time_calls(fn, samples=5, calls=5):
     return statistics.median(out)
 
 
-def run_rows(dev):
+# per token-head: method inputs and outputs (q, k, v, beta, gate, o; + dO, dq, dk, dv, dbeta, dg)
+# and FLOPs of the chunked method with 64-token chunks, head dim 128
+BYTES_FWD, BYTES_FWD_BWD = 1538, 4358
+FLOP_FWD, FLOP_FWD_BWD = 180224, 540672
+
+
+def run_rows(dev, hbm_gbs, bf16_tflops):
     import torch
     from linear_attention_chunked_gb300 import inputs, kda
     rows = {}
@@ -244,9 +250,16 @@ def run_rows(dev):
                 kda.kda_bwd(*a, x["dO"], saved=saved, want_dh0=False, ws=ws, **kw)
         f_ms = _time_calls(fwd)
         fb_ms = _time_calls(fwd_bwd)
-        rows[f"{w.row}:{mode}"] = {"T": w.T, "H": w.H, "fwd_ms": round(f_ms, 4),
-                                   "fwd_bwd_ms": round(fb_ms, 4),
-                                   "fwd_bwd_tokens_per_s": round(w.T / (fb_ms / 1e3))}
+        # roofline position of the row: algorithmic bytes and FLOPs per token-head (method I/O and
+        # chunked-method FLOPs; replay adds one forward's FLOPs) against the measured peaks
+        th = w.T * w.H
+        fb_flop = FLOP_FWD_BWD + (FLOP_FWD if mode == "replay" else 0)
+        rows[f"{w.row}:{mode}"] = {
+            "T": w.T, "H": w.H, "fwd_ms": round(f_ms, 4), "fwd_bwd_ms": round(fb_ms, 4),
+            "fwd_bwd_tokens_per_s": round(w.T / (fb_ms / 1e3)),
+            "fwd_byte_frac": round(th * BYTES_FWD / (f_ms * 1e6) / hbm_gbs, 4),
+            "fwd_bwd_byte_frac": round(th * BYTES_FWD_BWD / (fb_ms * 1e6) / hbm_gbs, 4),
+            "fwd_bwd_flop_frac": round(th * fb_flop / (fb_ms * 1e9) / bf16_tflops, 4)}
         del x, ws, saved
         torch.cuda.empty_cache()
     return rows
@@ -383,6 +396,7 @@ def main():
 
     # ---- per-kernel device time (second pass, CUDA events around every launch) ----
     kernels, roof = {}, None
+    hbm, bf16, src = load_peaks()
     if not args.no_profile:
         kda.kda_profile_enable(True)
         for _ in range(args.steps):
@@ -393,7 +407,6 @@ def main():
         kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                    for k, v in prof.items() if v[1]}
         dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
-        hbm, bf16, src = load_peaks()
         per_th = alg_bytes_per_token_head(dom)
         if per_th is not None:
             launch_ms = kernels[dom]["ms_per_step"] / kernels[dom]["launches_per_step"]
@@ -439,7 +452,7 @@ def main():
 
     rows = None
     if rank == 0 and not args.no_rows:
-        rows = run_rows(dev)
+        rows = run_rows(dev, hbm, bf16)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -450,7 +463,8 @@ def main():
             "metric": f"KDA fwd+bwd tokens/s (H={H},d=128)", "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": (value / world) / (T / (PAGES_MS / 1e3)),
+            "vs_baseline": ((value / world) / (T / (PAGES_MS / 1e3))
+                            if args.workload == "4doc" else None),
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"{w.row}:saved", "T": T, "H": H, "docs": list(w.lens),
                        "d": 128, "chunk": 64, "outputs": "fp32",

@@ -18,6 +18,7 @@ constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
 
 std::mutex g_mu;
 bool g_ready[128];
+int g_sms[128];  // multiprocessor count per device (persistent grids)
 
 // Once per device: check it is an sm_103 part and raise the dynamic shared memory limits.
 kda_status setup_device() {
@@ -31,6 +32,9 @@ kda_status setup_device() {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (major != 10 || minor != 3) return KDA_ERR_UNSUPPORTED;
+    if (cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        g_sms[dev] < 1)
+        return KDA_ERR_CUDA;
     struct { const void* f; size_t smem; } attrs[] = {
         {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd_tc, SMEM_CHAIN_FWD_TC},
         {(const void*)k_chain_bwd_tc, SMEM_CHAIN_BWD_TC}, {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
@@ -222,7 +226,11 @@ kda_status run_prologue(const Params& p, cudaStream_t st) {
     }
     if (p.maxC > 0) {
         ProfScope ps(KK_INTRA_FWD, st);
-        k_intra_fwd<<<dim3(unsigned(p.maxC), p.H), INTRA_THREADS, SMEM_INTRA_FWD, st>>>(p);
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const long long items = p.maxC * p.H;
+        const unsigned grid = unsigned(items < g_sms[dev] ? items : g_sms[dev]);
+        k_intra_fwd<<<grid, INTRA_THREADS, SMEM_INTRA_FWD, st>>>(p);
     }
     return launched();
 }

@@ -29,9 +29,9 @@ struct IntraSmem {
         } a;
         struct {
             __nv_bfloat16 bKg[2][CH * LB];  // beta K e^gam (hi, lo)
-            __nv_bfloat16 v[CH * LB];       // V (exact in bf16)
         } b;
     } u;
+    __nv_bfloat16 v[CH * LB];  // V (exact in bf16)
 };
 
 // off-diagonal sub-chunk pairs (i, j), i > j, one per warp
@@ -50,47 +50,77 @@ static_assert(sizeof(IntraSmem) <= 232448, "intra shared memory above the opt-in
 
 size_t intra_smem_bytes() { return sizeof(IntraSmem); }
 
-__global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
+// Persistent: one block per SM walks the (chunk, head) items item = chunk * H + head; the raw
+// inputs of its next item are loaded into registers while the current one is computed.
+__global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     constexpr int BT = INTRA_THREADS, NW = BT / 32;
-    const int ci = blockIdx.x, h = blockIdx.y;
-    if (ci >= *p.nchunks) return;
-    const int4 info = p.chunk_tab[ci];
-    const int t0 = info.y, L = info.z;
     extern __shared__ __align__(16) unsigned char smraw[];
     IntraSmem& S = *reinterpret_cast<IntraSmem*>(smraw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const size_t chd = size_t(ci) * p.H + h;
+    const int items = *p.nchunks * p.H;
+    const int c4t = (tid & 31) * 4;  // the gate channels of this thread (every k below)
 
-    // 1. loads (zero rows past the document end), gate, beta; clear the 64x64 accumulators
-    {
-        uint4 vq[2], vk[2];
-        float4 gv[4];
+    // raw inputs of the next item (rows past the document end read as zero): q, k, gate, beta in
+    // registers; v goes to its shared tile with cp.async once the current item no longer needs it
+    uint4 pq[2], pk[2];
+    float4 pg[4], pdb = make_float4(0.f, 0.f, 0.f, 0.f);
+    float pb = 0.f, peA = 0.f;
+    int nT0 = 0, nL = 0, nh = 0;  // first token, length and head of the next item
+    int4 tab_ahead = make_int4(0, 0, 0, 0);  // chunk-table entry of the item after the next
+    auto fetch = [&](int item, int4 inf) {
+        const int hh = item % p.H;
+        const int T0 = inf.y, Ln = inf.z;
+        nT0 = T0;
+        nL = Ln;
+        nh = hh;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
-            const size_t off = (size_t(t0 + r) * p.H + h) * D + c8;
-            vq[k] = r < L ? *reinterpret_cast<const uint4*>(p.q + off) : make_uint4(0u, 0u, 0u, 0u);
-            vk[k] = r < L ? *reinterpret_cast<const uint4*>(p.k + off) : make_uint4(0u, 0u, 0u, 0u);
+            const size_t off = (size_t(T0 + r) * p.H + hh) * D + c8;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            pq[k] = r < Ln ? *reinterpret_cast<const uint4*>(p.q + off) : z;
+            pk[k] = r < Ln ? *reinterpret_cast<const uint4*>(p.k + off) : z;
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
-            gv[k] = r < L ? *reinterpret_cast<const float4*>(p.g + (size_t(t0 + r) * p.H + h) * D + c4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int r = (tid + BT * k) >> 5;
+            pg[k] = r < Ln ? *reinterpret_cast<const float4*>(p.g + (size_t(T0 + r) * p.H + hh) * D + c4t)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const int c4 = (tid & 31) * 4;  // the same 4 channels for every k
-        float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
-        float eA = 0.f;
+        if (tid < CH) pb = tid < Ln ? bf2f(p.beta[size_t(T0 + tid) * p.H + hh]) : 0.f;
         if (p.gate_raw) {
-            db = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
-            eA = expf(p.A_log[h]);
+            pdb = *reinterpret_cast<const float4*>(p.dt_bias + hh * D + c4t);
+            peA = p.A_log[hh];
         }
-        if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
+        const int after = item + int(gridDim.x);
+        if (after < items) tab_ahead = p.chunk_tab[after / p.H];
+    };
+    auto fetch_v = [&]() {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
-            const __nv_bfloat162* bq = reinterpret_cast<const __nv_bfloat162*>(&vq[k]);
-            const __nv_bfloat162* bk = reinterpret_cast<const __nv_bfloat162*>(&vk[k]);
+            const bool ok = r < nL;
+            cp16z(&S.v[r * LB + c8], p.v + (size_t(nT0 + (ok ? r : 0)) * p.H + nh) * D + c8, ok);
+        }
+        cp_commit();
+    };
+    if (int(blockIdx.x) < items) {
+        fetch(blockIdx.x, p.chunk_tab[blockIdx.x / p.H]);
+        fetch_v();
+    }
+
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int L = nL;  // this item's length (its fetch was the latest one)
+    const size_t chd = size_t(item);
+
+    // 1. inputs (fetched one item ahead) to shared memory, gate, beta; clear the 64x64 accumulators
+    {
+        if (tid < CH) S.beta[tid] = pb;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
+            const __nv_bfloat162* bq = reinterpret_cast<const __nv_bfloat162*>(&pq[k]);
+            const __nv_bfloat162* bk = reinterpret_cast<const __nv_bfloat162*>(&pk[k]);
             float fq[8], fk[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -107,16 +137,17 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
             dk[0] = make_float4(fk[0], fk[1], fk[2], fk[3]);
             dk[1] = make_float4(fk[4], fk[5], fk[6], fk[7]);
         }
+        const float eA = p.gate_raw ? expf(peA) : 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
-            float x[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
-            const float b4[4] = {db.x, db.y, db.z, db.w};
+            float x[4] = {pg[k].x, pg[k].y, pg[k].z, pg[k].w};
+            const float b4[4] = {pdb.x, pdb.y, pdb.z, pdb.w};
             if (p.gate_raw) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) x[j] = r < L ? -eA * softplus_f(x[j] + b4[j]) : 0.f;
             }
-            *reinterpret_cast<float4*>(&S.gam[r * LDP + c4]) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(&S.gam[r * LDP + c4t]) = make_float4(x[0], x[1], x[2], x[3]);
         }
     }
     for (int i = tid; i < CH * LDA; i += BT) {
@@ -125,6 +156,7 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
         S.Mi[i] = 0.f;
     }
     __syncthreads();
+    const bool more = item + int(gridDim.x) < items;
 
     // 2. fused L2 norm (warp per row)
     if (p.l2n) {
@@ -295,6 +327,8 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
     }
     __syncthreads();
 
+    if (more) fetch(item + gridDim.x, tab_ahead);  // lands during Minv, W / U and the stores
+
     // 5. Minv = (I + diag(beta) Akk)^-1, blockwise: 16x16 diagonal inverses by substitution, then
     //    X_ij = -D_i sum_{l=j}^{i-1} diag(beta_i) Akk_il X_lj by increasing block distance
     if (tid < 64) {
@@ -341,31 +375,19 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
         __syncthreads();
     }
 
+    cp_wait<0>();  // this item's v tile (copied during the previous item's last phase)
+
     // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
-    {
-        uint4 vv[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
-            vv[k] = r < L ? *reinterpret_cast<const uint4*>(p.v + (size_t(t0 + r) * p.H + h) * D + c8)
-                          : make_uint4(0u, 0u, 0u, 0u);
-        }
-        for (int i = tid; i < CH * D / 2; i += BT) {
-            const int r = (2 * i) / D, c = (2 * i) % D;
-            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
-            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
-            const float x0 = S.beta[r] * kv.x * __expf(gv.x);
-            const float x1 = S.beta[r] * kv.y * __expf(gv.y);
-            uint32_t hi, lo;
-            split2(x0, x1, hi, lo);
-            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
-            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
-        }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
-            *reinterpret_cast<uint4*>(&S.u.b.v[r * LB + c8]) = vv[k];
-        }
+    for (int i = tid; i < CH * D / 2; i += BT) {
+        const int r = (2 * i) / D, c = (2 * i) % D;
+        const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
+        const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
+        const float x0 = S.beta[r] * kv.x * __expf(gv.x);
+        const float x1 = S.beta[r] * kv.y * __expf(gv.y);
+        uint32_t hi, lo;
+        split2(x0, x1, hi, lo);
+        *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
+        *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
     }
     __syncthreads();
     {
@@ -386,7 +408,7 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
                 const int n0 = 32 * nq + 16 * np;
                 ldsm4t(kh, bk_addr(S.u.b.bKg[0], LB, 16 * ks, n0, lane));
                 ldsm4t(kl, bk_addr(S.u.b.bKg[1], LB, 16 * ks, n0, lane));
-                ldsm4t(vv, bk_addr(S.u.b.v, LB, 16 * ks, n0, lane));
+                ldsm4t(vv, bk_addr(S.v, LB, 16 * ks, n0, lane));
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     mma_x3(accW[2 * np + hh], mh, ml, kh[2 * hh], kh[2 * hh + 1], kl[2 * hh],
@@ -412,7 +434,8 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
             }
     }
 
-    // 7. elementwise operands and the small matrices
+    // 7. elementwise operands and the small matrices (eight consecutive elements per thread:
+    //    16-byte stores of every plane)
     {
         __nv_bfloat16* Qh = p.Qh + chd * CH * D;
         __nv_bfloat16* Ql = p.Ql + chd * CH * D;
@@ -452,6 +475,9 @@ __global__ void __launch_bounds__(INTRA_THREADS) k_intra_fwd(Params p) {
             reinterpret_cast<float2*>(Akk)[i] = make_float2(S.Akk[r * LDA + s], S.Akk[r * LDA + s + 1]);
         }
         if (tid < D) p.eGL[chd * D + tid] = __expf(S.gam[(CH - 1) * LDP + tid]);
+    }
+    __syncthreads();  // the next item overwrites the shared tiles
+    if (more) fetch_v();
     }
 }
 

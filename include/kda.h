@@ -93,7 +93,8 @@ typedef enum kda_frag_mode {
 typedef struct kda_problem {
     int64_t T;                  /* total packed tokens, >= 0 */
     int32_t N;                  /* documents (or fragments), 1 .. 65535 */
-    int32_t H;                  /* heads, 1 .. 65535 */
+    int32_t H;                  /* heads, 1 .. 65535; N * H * 4 above INT32_MAX is
+                                   KDA_ERR_UNSUPPORTED (one-dimensional recurrence grids) */
     int32_t d;                  /* head dim; must be 128 */
     int32_t gate;               /* kda_gate_form */
     int32_t l2norm;             /* 0: q, k used as given; 1: fused q/sqrt(|q|^2+eps), same for k */

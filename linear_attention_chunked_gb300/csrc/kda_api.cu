@@ -55,6 +55,7 @@ kda_status check_problem(const kda_problem* p) {
     if (p->d != D) return KDA_ERR_UNSUPPORTED;
     if (p->H < 1 || p->H > 65535 || p->N < 1 || p->N > 65535 || p->T < 0 || p->T > INT32_MAX)
         return KDA_ERR_INVALID_ARG;
+    if (int64_t(p->N) * p->H * 2 * NHALF > INT32_MAX) return KDA_ERR_UNSUPPORTED;  // 1-D grids
     if (p->gate != KDA_GATE_G && p->gate != KDA_GATE_RAW) return KDA_ERR_INVALID_ARG;
     if (p->l2norm != 0 && p->l2norm != 1) return KDA_ERR_INVALID_ARG;
     if (p->out_fp32 != 0 && p->out_fp32 != 1) return KDA_ERR_INVALID_ARG;
@@ -92,6 +93,7 @@ Params make_params(const kda_problem* pr, const Layout& L, void* ws) {
     p.status = reinterpret_cast<int*>(w + L.status);
     p.nchunks = reinterpret_cast<int*>(w + L.nchunks);
     p.doc_off = reinterpret_cast<int*>(w + L.doc_off);
+    p.doc_order = reinterpret_cast<int*>(w + L.doc_order);
     p.chunk_tab = reinterpret_cast<int4*>(w + L.chunk_tab);
     return p;
 }
@@ -301,7 +303,7 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     if (kda_status s = run_prologue(p, st)) return s;
     {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
+        k_chain_fwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
             p, CHAIN_FWD_OUT, tm);
     }
     return launched();
@@ -378,12 +380,12 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         r.o = nullptr;
         r.ht = nullptr;
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
+        k_chain_fwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
             r, CHAIN_FWD_OUT, tm);
     }
     {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
+        k_chain_bwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
             p, CHAIN_BWD, tm);
     }
     if (L.maxC > 0) {
@@ -430,11 +432,11 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     if (kda_status s = run_prologue(p, st)) return s;
     if (mode == KDA_FRAG_FWD) {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd_tc<<<dim3(pr->N, pr->H, 2 * NHALF), CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
+        k_chain_fwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * 2 * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
             p, CHAIN_FRAG_MB, tm);
     } else {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd_tc<<<dim3(pr->N, pr->H, NHALF), CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
+        k_chain_bwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
             p, CHAIN_FRAG_C, tm);
     }
     return launched();

@@ -246,8 +246,11 @@ struct BwdIntraSmem {
     float beta[CH], rq[CH], rk[CH];
     float dbp[CH];  // per-row dbeta, accumulated in steps 1-2 in a fixed order
     union {
-        uint4 Af[24][2][32];         // split A fragments of dAqk / dAkk (fragment order), step 3
-        float red[2 * BI_THREADS];   // reduction scratch, steps 5 and 7
+        uint4 Af[24][2][32];  // split A fragments of dAqk / dAkk (fragment order), step 3
+        struct {
+            float red[2 * BI_THREADS + 32];  // reduction scratch, steps 5 and 7
+            float kbp[16 * D];               // per-warp partials of sum_r dKb * Kb (step 2 -> 5)
+        };
     };
 };
 static_assert(sizeof(BwdIntraSmem) <= 232448, "backward intra shared memory above the opt-in limit");
@@ -360,6 +363,7 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
 
     // 2. elementwise terms through Qg, Kg, Kb and the diagonal of Aqk; dv = beta dR; dbeta_r +=
     //    dR_r . v_r - Kg_r . P_r (one warp per row, fixed-order warp sums)
+    float kbp[4] = {0.f, 0.f, 0.f, 0.f};  // sum over this thread's rows of dKb * Kb, its 4 channels
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
         float4 vq[2], vp[2], vb[2], vr[2];
@@ -408,6 +412,7 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
                 const float dqg = aq[j], dkg = -br * ap[j], dkb = ab[j];
                 oq[j] = fmaf(dqg, er, dgn * kv);
                 ok[j] = fmaf(dkg, er, fmaf(dkb, eb, dgn * qv));
+                kbp[j] = fmaf(dkb, kv * eb, kbp[j]);
                 og[j] = (dqg * qv + dkg * kv) * er - dkb * kv * eb;
                 db = fmaf(ar[j], vvv[j], db);
                 db = fmaf(-kv * er, ap[j], db);
@@ -562,25 +567,34 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
     }
     __syncthreads();
 
+    // raw gate input of step 7, loaded here so its latency hides behind steps 5 and 6
+    float4 av[4];
+    if (p.gate_raw) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
+            av[k] = r < L ? *reinterpret_cast<const float4*>(p.g + (size_t(t0 + r) * p.H + h) * D + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+
     // 5. chunk-end gate term dgL = e^gL rowsum(S0 * dS1) + sum_r dKb * Kb, then the reverse
     //    cumsum over the chunk; four threads per channel (16 rows each), fixed order
     {
         const int c = tid & (D - 1), qu = tid >> 7, r0 = 16 * qu;
         const float gl = S.gam[(CH - 1) * LDP + c];
-        float part = 0.f;
-#pragma unroll
-        for (int r = r0; r < r0 + 16; ++r)
-            part = fmaf(dKb[r * D + c], Kv(r, c) * __expf(gl - S.gam[r * LDP + c]), part);
+        *reinterpret_cast<float4*>(&S.kbp[w * D + 4 * lane]) = make_float4(kbp[0], kbp[1], kbp[2], kbp[3]);
         float suf = 0.f;  // suffix sums inside the quarter
         for (int r = r0 + 15; r >= r0; --r) {
             suf += S.dG[r * LDP + c];
             S.dG[r * LDP + c] = suf;
         }
-        S.red[tid] = part;
         S.red[BT + tid] = suf;  // quarter total
         __syncthreads();
-        const float dgl = __expf(gl) * p.rsum[chd * D + c] +
-                          ((S.red[c] + S.red[D + c]) + (S.red[2 * D + c] + S.red[3 * D + c]));
+        float part = 0.f;  // sum over the 16 warps' row sets, fixed order
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) part += S.kbp[ww * D + c];
+        const float dgl = __expf(gl) * p.rsum[chd * D + c] + part;
         float carry = 0.f;  // totals of the later quarters
         for (int q2 = qu + 1; q2 < 4; ++q2) carry += S.red[BT + q2 * D + c];
         for (int r = r0; r < r0 + 16; ++r) S.dG[r * LDP + c] += carry + dgl;
@@ -633,13 +647,6 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
     }
     const float eA = expf(p.A_log[h]);
     {
-        float4 av[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
-            av[k] = r < L ? *reinterpret_cast<const float4*>(p.g + (size_t(t0 + r) * p.H + h) * D + c4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
         const int c4 = (tid & 31) * 4;
         const float4 dtb = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
         const float b4[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
@@ -676,18 +683,16 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
         S.red[BT + tid] = pa;
     }
     __syncthreads();
-    if (tid < D) {
+    if (tid < D) {  // warps 0..3: one channel per thread, then a fixed-order sum of the channels
         const int c = tid;
         p.pddt[chd * D + c] = (S.red[c] + S.red[D + c]) + (S.red[2 * D + c] + S.red[3 * D + c]);
-        const float pa = (S.red[BT + c] + S.red[BT + D + c]) + (S.red[BT + 2 * D + c] + S.red[BT + 3 * D + c]);
-        S.red[c] = pa;
+        float pa = (S.red[BT + c] + S.red[BT + D + c]) + (S.red[BT + 2 * D + c] + S.red[BT + 3 * D + c]);
+        pa = warp_sum(pa);
+        if (lane == 0) S.red[2 * BT + w] = pa;
     }
     __syncthreads();
-    for (int s2 = D / 2; s2 > 0; s2 >>= 1) {
-        if (tid < s2) S.red[tid] += S.red[tid + s2];
-        __syncthreads();
-    }
-    if (tid == 0) p.pdA[chd] = S.red[0];
+    if (tid == 0)
+        p.pdA[chd] = (S.red[2 * BT] + S.red[2 * BT + 1]) + (S.red[2 * BT + 2] + S.red[2 * BT + 3]);
 }
 
 // Fixed-order sums of the per-chunk partials: dA_log[h], ddt_bias[h, :].

@@ -71,14 +71,18 @@ __device__ __forceinline__ void st_g32(__nv_bfloat16* dst, const uint32_t (&x)[1
 
 size_t chain_fwd_tc_smem_bytes() { return CHAIN_TC_SMEM; }
 
-// Grid (documents, heads, 2 value halves) for CHAIN_FWD_OUT; (documents, heads, 4) for
-// CHAIN_FRAG_MB (z = 0, 1: X = I with zero values -> M; z = 2, 3: Y = 0 with the values -> B).
+// Grid N x H x 2 value halves for CHAIN_FWD_OUT; N x H x 4 parts for CHAIN_FRAG_MB (parts 0, 1:
+// X = I with zero values -> M; parts 2, 3: Y = 0 with the values -> B).
 // 256 threads: warp w reads TMEM lanes 32 (w % 4).. and value columns 32 (w / 4).. of the half.
 // Thread 0 issues the TMA loads and the MMAs.  Operands of chunk c+1 are loaded as soon as the
 // MMA that reads their buffer has completed.
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm) {
-    const int n = blockIdx.x, h = blockIdx.y, hv = blockIdx.z;
+    // block = (document rank, head, value part): longest documents first, the parts of one
+    // (document, head) adjacent so their shared operand tiles are read from L2 together
+    const int nparts = mode == CHAIN_FWD_OUT ? NHALF : 2 * NHALF;
+    const int hv = int(blockIdx.x % unsigned(nparts)), rest = int(blockIdx.x / unsigned(nparts));
+    const int h = rest % p.H, n = p.doc_order[rest / p.H];
     const bool fwd = mode == CHAIN_FWD_OUT;
     const bool fragX = !fwd && hv < 2;
     const bool want_o = fwd && p.o != nullptr;
@@ -244,22 +248,16 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         __syncwarp();
 
         // ---- Delta = U - W S (lanes 0..63) ----
+        uint32_t dhh[16], dll[16];
         if (qd < 2) {
             float v[32];
             tc::tmem_ld32(tD1 + cc, v);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = Un[j] - v[j];
-            uint32_t dhh[16], dll[16];
             split32(v, dhh, dll);
             st_sw128(sm + OFF_DL, row, cc, dhh);
             st_sw128(sm + OFF_DL + 8192, row, cc, dll);
-            if (fwd && p.sDelta) {
-                __nv_bfloat16* dst = p.sDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
-                st_g32(dst, dhh);
-                st_g32(dst + CH * D, dll);
-            }
         }
-        fetch_next(ci + 1);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
@@ -299,6 +297,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::mma_commit(&bar[3]);
         }
         __syncwarp();
+        // while MMA2 / MMA3 run: the saved write vectors and the next chunk's per-thread operands
+        if (qd < 2 && fwd && p.sDelta) {
+            __nv_bfloat16* dst = p.sDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
+            st_g32(dst, dhh);
+            st_g32(dst + CH * D, dll);
+        }
+        fetch_next(ci + 1);
         if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
         tc::fence_after_sync();
         if (tid == 0 && ci + 1 < c1 && !*abort_flag) {
@@ -390,7 +395,8 @@ size_t chain_bwd_tc_smem_bytes() { return CHAIN_BWD_TC_SMEM; }
 
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm) {
-    const int n = blockIdx.x, h = blockIdx.y, hv = blockIdx.z;
+    const int hv = int(blockIdx.x % unsigned(NHALF)), rest = int(blockIdx.x / unsigned(NHALF));
+    const int h = rest % p.H, n = p.doc_order[rest / p.H];
     const bool bwd = mode == CHAIN_BWD;
     const int col0 = hv * 64;
     extern __shared__ unsigned char smraw[];
@@ -483,17 +489,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     for (int ci = c1 - 1; ci >= c0; --ci) {
         const uint32_t ph = uint32_t(c1 - 1 - ci) & 1u;
         const size_t chd = size_t(ci) * p.H + h;
-        {   // dS1 operand (+ its saved planes)
-            uint32_t hh[16], ll[16];
-            split32(dSr, hh, ll);
-            st_sw128(sm + B_OFF_DS, row, cc, hh);
-            st_sw128(sm + B_OFF_DS + 16384, row, cc, ll);
-            if (bwd) {
-                __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + size_t(row) * D + col0 + cc;
-                st_g32(dst, hh);
-                st_g32(dst + D * D, ll);
-            }
-        }
+        uint32_t sh_[16], sl_[16];  // dS1 operand split (its saved planes are written below)
+        split32(dSr, sh_, sl_);
+        st_sw128(sm + B_OFF_DS, row, cc, sh_);
+        st_sw128(sm + B_OFF_DS + 16384, row, cc, sl_);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
@@ -534,6 +533,11 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::mma_commit(&bar[3]);
         }
         __syncwarp();
+        if (bwd) {  // while MMA-A runs: the saved gradient at the chunk end
+            __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + size_t(row) * D + col0 + cc;
+            st_g32(dst, sh_);
+            st_g32(dst + D * D, sl_);
+        }
         const float eg = egn;
         if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
         tc::fence_after_sync();
@@ -544,23 +548,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         __syncwarp();
 
         // ---- dDelta = scale DT + DA (lanes 0..63) ----
+        uint32_t xh[16], xl[16];
         if (qd < 2) {
             float a[32], t[32];
             tc::tmem_ld32(tDA + cc, a);
             tc::tmem_ld32(tDT + cc, t);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] = fmaf(p.scale, t[j], a[j]);
-            uint32_t hh[16], ll[16];
-            split32(a, hh, ll);
-            st_sw128(sm + B_OFF_DD, row, cc, hh);
-            st_sw128(sm + B_OFF_DD + 8192, row, cc, ll);
-            if (bwd) {
-                __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
-                st_g32(dst, hh);
-                st_g32(dst + CH * D, ll);
-            }
+            split32(a, xh, xl);
+            st_sw128(sm + B_OFF_DD, row, cc, xh);
+            st_sw128(sm + B_OFF_DD + 8192, row, cc, xl);
         }
-        fetch_next(ci - 1);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
@@ -584,8 +582,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                         acc = 1;
                     }
                 const uint64_t wh = tc::sdesc(sW, 8192, 1024), wl = tc::sdesc(sW + 16384, 8192, 1024);
-                const uint64_t xh = tc::sdesc(sdD, 1024, 1024), xl = tc::sdesc(sdD + 8192, 1024, 1024);
-                const uint64_t ta[3] = {wh, wl, wh}, tb[3] = {xl, xh, xh};
+                const uint64_t dxh = tc::sdesc(sdD, 1024, 1024), dxl = tc::sdesc(sdD + 8192, 1024, 1024);
+                const uint64_t ta[3] = {wh, wl, wh}, tb[3] = {dxl, dxh, dxh};
                 acc = 0;
 #pragma unroll
                 for (int t3 = 0; t3 < 3; ++t3)
@@ -601,6 +599,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::mma_commit(&bar[4]);
         }
         __syncwarp();
+        // while MMA-D runs: the saved write-vector gradient and the next chunk's per-thread operands
+        if (qd < 2 && bwd) {
+            __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
+            st_g32(dst, xh);
+            st_g32(dst + CH * D, xl);
+        }
+        fetch_next(ci - 1);
         if (!tc::mbar_wait(&bar[4], ph)) *abort_flag = 1;
         tc::fence_after_sync();
         if (tid == 0 && ci > c0 && !*abort_flag) {

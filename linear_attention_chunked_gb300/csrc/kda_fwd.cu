@@ -27,7 +27,24 @@ __global__ void k_plan(Params p) {
     __syncthreads();
     if (bad) {
         for (int n = threadIdx.x; n <= p.N; n += blockDim.x) p.doc_off[n] = 0;
+        for (int n = threadIdx.x; n < p.N; n += blockDim.x) p.doc_order[n] = n;
         return;
+    }
+    // the state recurrences launch their blocks longest document first (ties in index order);
+    // above MAX_SORT documents the order stays the identity
+    constexpr int MAX_SORT = 1024;
+    __shared__ int ncs[MAX_SORT];
+    if (p.N > MAX_SORT) {
+        for (int i = threadIdx.x; i < p.N; i += blockDim.x) p.doc_order[i] = i;
+    } else {
+        for (int i = threadIdx.x; i < p.N; i += blockDim.x) ncs[i] = p.doc_off[i + 1] - p.doc_off[i];
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.N; i += blockDim.x) {
+            const int ni = ncs[i];
+            int rank = 0;
+            for (int j = 0; j < p.N; ++j) rank += (ncs[j] > ni) || (ncs[j] == ni && j < i);
+            p.doc_order[rank] = i;
+        }
     }
     for (int n = 0; n < p.N; ++n) {
         const int a = p.cu[n], len = p.cu[n + 1] - a, off = p.doc_off[n];

@@ -41,7 +41,7 @@ struct Layout {
     int N, H;
     int64_t maxC;  // upper bound of the chunk count: ceil(T/64) + N
     // workspace
-    size_t status, nchunks, doc_off, chunk_tab;
+    size_t status, nchunks, doc_off, doc_order, chunk_tab;
     size_t dS1, dDelta, dR, P, dQg, dKb, dAqk, dM, rsum;              // backward intermediates
     size_t pdA, pddt;                                                 // parameter partials
     size_t replay;    // replay copy of the saved set
@@ -106,6 +106,7 @@ inline Layout make_layout(int64_t T, int N, int H) {
     L.status = take(256);
     L.nchunks = take(sizeof(int));
     L.doc_off = take(sizeof(int) * size_t(N + 1));
+    L.doc_order = take(sizeof(int) * size_t(N));
     L.chunk_tab = take(sizeof(int4) * size_t(L.maxC));
     L.intra_ws = o;
     L.ws_fwd = o + R.bytes;
@@ -142,6 +143,7 @@ struct Params {
     int* status;
     int* nchunks;
     int* doc_off;
+    int* doc_order;   // documents by decreasing chunk count (ties: index order)
     int4* chunk_tab;  // {doc, first token, length, chunk index within the doc}
     __nv_bfloat16 *Wh, *Wl, *Qh, *Ql, *Kh, *Kl, *Ah, *Al, *Mh, *Ml;
     float *U, *Akk, *gam, *eGL;

@@ -145,7 +145,7 @@ def alg_bytes_per_token_head(kernel):
         "k_intra_fwd": qkv + beta + gate,                    # reads the chunk inputs
         "k_chain_fwd_tc": o,                                 # writes o
         "k_chain_bwd_tc": dO,                                # reads dO
-        "k_bwd_gemms": dO,                                   # reads dO
+        "k_bwd_gemms_tc": dO,                                # reads dO
         "k_bwd_intra": qkv + beta + gate + dqkv + dbeta + dg,  # reads inputs, writes grads
     }
     return table.get(kernel)

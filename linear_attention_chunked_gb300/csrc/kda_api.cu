@@ -12,7 +12,7 @@ namespace {
 const size_t SMEM_INTRA_FWD = intra_smem_bytes();
 const size_t SMEM_CHAIN_FWD_TC = chain_fwd_tc_smem_bytes();
 const size_t SMEM_CHAIN_BWD_TC = chain_bwd_tc_smem_bytes();
-const size_t SMEM_BWD_GEMMS = bwd_gemm_smem_bytes();
+const size_t SMEM_BWD_GEMMS_TC = bwd_gemm_tc_smem_bytes();
 const size_t SMEM_BWD_INTRA = bwd_intra_smem_bytes();
 constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
 
@@ -37,7 +37,7 @@ kda_status setup_device() {
         return KDA_ERR_CUDA;
     struct { const void* f; size_t smem; } attrs[] = {
         {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd_tc, SMEM_CHAIN_FWD_TC},
-        {(const void*)k_chain_bwd_tc, SMEM_CHAIN_BWD_TC}, {(const void*)k_bwd_gemms, SMEM_BWD_GEMMS},
+        {(const void*)k_chain_bwd_tc, SMEM_CHAIN_BWD_TC}, {(const void*)k_bwd_gemms_tc, SMEM_BWD_GEMMS_TC},
         {(const void*)k_bwd_intra, SMEM_BWD_INTRA}, {(const void*)k_walk, SMEM_WALK},
     };
     for (auto& a : attrs)
@@ -177,7 +177,7 @@ kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
     if (6 * CHd > size_t(INT32_MAX)) return KDA_ERR_UNSUPPORTED;
     const IntraRecord R = make_intra_record(CHd);
     const size_t t128 = size_t(CH) * D * 2, t64 = size_t(CH) * CH * 2;
-    if (R.Kl + CHd * t128 - R.Wh != 6 * CHd * t128 || R.Al + CHd * t64 - R.Ah != 2 * CHd * t64)
+    if (R.Kl + CHd * t128 - R.Wh != 6 * CHd * t128 || R.Ml + CHd * t64 - R.Ah != 4 * CHd * t64)
         return KDA_ERR_UNSUPPORTED;  // planes not contiguous (layout changed)
     tm->zWh = 0;
     tm->zWl = int((R.Wl - R.Wh) / t128);
@@ -187,9 +187,11 @@ kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
     tm->zKl = int((R.Kl - R.Wh) / t128);
     tm->zAh = 0;
     tm->zAl = int((R.Al - R.Ah) / t64);
+    tm->zMh = int((R.Mh - R.Ah) / t64);
+    tm->zMl = int((R.Ml - R.Ah) / t64);
     const cuuint32_t box[3] = {64, 64, 1}, es[3] = {1, 1, 1};
     const cuuint64_t d128[3] = {D, CH, 6 * CHd}, s128[2] = {D * 2, t128};
-    const cuuint64_t d64[3] = {CH, CH, 2 * CHd}, s64[2] = {CH * 2, t64};
+    const cuuint64_t d64[3] = {CH, CH, 4 * CHd}, s64[2] = {CH * 2, t64};
     if (enc(&tm->m128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.Wh, d128, s128, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
@@ -213,6 +215,31 @@ kda_status make_dO_map(const void* dO, int64_t T, int H, TcMaps* tm) {
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+// Tensor maps of the backward per-chunk operands (p's saved set and backward regions set).
+kda_status make_bwd_maps(const Params& p, const Layout& L, TcMaps* tm) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return KDA_ERR_CUDA;
+    const size_t CHd = size_t(L.maxC) * L.H;
+    const cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t b64[3] = {64, 64, 1}, b128[3] = {64, 128, 1};
+    const cuuint64_t d64[3] = {D, CH, 2 * CHd}, s64[2] = {D * 2, size_t(CH) * D * 2};
+    const cuuint64_t d128[3] = {D, D, 2 * CHd}, s128[2] = {D * 2, size_t(D) * D * 2};
+    struct {
+        CUtensorMap* m;
+        const void* base;
+        const cuuint64_t* dims;
+        const cuuint64_t* st;
+        const cuuint32_t* box;
+    } v[4] = {{&tm->mDD, p.dDelta, d64, s64, b64}, {&tm->mDl, p.sDelta, d64, s64, b64},
+              {&tm->mS, p.sS, d128, s128, b128}, {&tm->mdS, p.dS1, d128, s128, b128}};
+    for (auto& x : v)
+        if (enc(x.m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x.base), x.dims, x.st,
+                x.box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return KDA_ERR_CUDA;
     return KDA_OK;
 }
 
@@ -369,6 +396,7 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
     TcMaps tm{};
     if (kda_status s = make_tc_maps(p, L, &tm)) return s;
     if (kda_status s = make_dO_map(dO, pr->T, pr->H, &tm)) return s;
+    if (kda_status s = make_bwd_maps(p, L, &tm)) return s;
     if (saved) {
         // the saved set already holds the intra products and states: only the chunk plan
         ProfScope ps(KK_PLAN, st);
@@ -392,7 +420,7 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         const dim3 grid(unsigned(L.maxC), pr->H);
         {
             ProfScope ps(KK_BWD_GEMMS, st);
-            k_bwd_gemms<<<grid, NTHR, SMEM_BWD_GEMMS, st>>>(p);
+            k_bwd_gemms_tc<<<grid, NTHR, SMEM_BWD_GEMMS_TC, st>>>(p, tm);
         }
         ProfScope ps(KK_BWD_INTRA, st);
         k_bwd_intra<<<grid, BI_THREADS, SMEM_BWD_INTRA, st>>>(p);

@@ -1,5 +1,6 @@
-// Backward-side per-chunk kernels: gradient products, intra-chunk gradients, deterministic
-// parameter reduction (the reverse state recurrence is in the tcgen05 recurrence file).
+// Backward-side per-chunk kernels: intra-chunk gradients and the deterministic parameter
+// reduction (the reverse state recurrence and the per-chunk gradient products run on tcgen05 in
+// their own files).
 //
 // Per chunk (adjoint of the forward lines in kda_internal.cuh), with dS1 the gradient at the
 // chunk-end state and dO already multiplied by the output scale:
@@ -14,228 +15,9 @@
 
 namespace kda {
 
-
 namespace {
 
-constexpr int LB = 136;   // row stride (bf16) of [rows][128] tiles
-constexpr int LB64 = 72;  // row stride (bf16) of [rows][64] tiles
-
-struct BwdGemmSmem {
-    __nv_bfloat16 M[2][CH * LB64];   // Minv (hi, lo)
-    __nv_bfloat16 X[2][CH * LB];     // dDelta (hi, lo)
-    __nv_bfloat16 R[2][CH * LB];     // dR (hi, lo)
-    __nv_bfloat16 S[2][D * LB];      // S_c, later dS1 [key][value] (hi, lo)
-    __nv_bfloat16 O[CH * LB];        // dO (exact bf16)
-    __nv_bfloat16 Dl[2][CH * LB];    // Delta (hi, lo)
-};
-
-static_assert(sizeof(BwdGemmSmem) <= 232448, "backward GEMM shared memory above the opt-in limit");
-
-}  // namespace
-
-size_t bwd_gemm_smem_bytes() { return sizeof(BwdGemmSmem); }
-
-// Per-chunk gradient products that need the chunk's states (tensor cores, 8 warps):
-//   dR = Minv^T dDelta, P = dR S0^T, dQg = dO S0^T, dAqk = tril(dO Delta^T),
-//   dM = -strict_tril(dR Delta^T), dKb = Delta dS1^T, rsum = rowsum(S0 * dS1).
-__global__ void __launch_bounds__(NTHR) k_bwd_gemms(Params p) {
-    const int ci = blockIdx.x, h = blockIdx.y;
-    if (ci >= *p.nchunks) return;
-    const int4 info = p.chunk_tab[ci];
-    const int t0 = info.y, L = info.z;
-    extern __shared__ __align__(16) unsigned char smraw[];
-    BwdGemmSmem& sm = *reinterpret_cast<BwdGemmSmem*>(smraw);
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const size_t chd = size_t(ci) * p.H + h;
-    const __nv_bfloat16* S0 = p.sS + chd * 2 * D * D;
-    const __nv_bfloat16* dS1 = p.dS1 + chd * 2 * D * D;
-    const __nv_bfloat16* Dl = p.sDelta + chd * 2 * CH * D;
-    const __nv_bfloat16* dDl = p.dDelta + chd * 2 * CH * D;
-    const int mt = w & 3, nh = w >> 2;
-
-    // every operand arrives as bf16 (hi / lo planes): one batch of cp.async
-    cp_tile_bf16(sm.M[0], LB64, p.Mh + chd * CH * CH, CH, CH, CH, tid, NTHR);
-    cp_tile_bf16(sm.M[1], LB64, p.Ml + chd * CH * CH, CH, CH, CH, tid, NTHR);
-    cp_tile_bf16(sm.X[0], LB, dDl, D, CH, D, tid, NTHR);
-    cp_tile_bf16(sm.X[1], LB, dDl + CH * D, D, CH, D, tid, NTHR);
-    cp_tile_bf16(sm.S[0], LB, S0, D, D, D, tid, NTHR);
-    cp_tile_bf16(sm.S[1], LB, S0 + D * D, D, D, D, tid, NTHR);
-    cp_tile_bf16(sm.Dl[0], LB, Dl, D, CH, D, tid, NTHR);
-    cp_tile_bf16(sm.Dl[1], LB, Dl + CH * D, D, CH, D, tid, NTHR);
-    for (int i = tid; i < CH * 16; i += NTHR) {
-        const int r = i >> 4, c = (i & 15) * 8;
-        const bool ok = r < L;
-        const size_t row = size_t(t0 + (ok ? r : 0));
-        cp16z(sm.O + r * LB + c, p.dO + (row * p.H + h) * D + c, ok);
-    }
-    cp_commit();
-    cp_wait<0>();
-    __syncthreads();
-
-    // dR = Minv^T dDelta  [64 tok x 128 val]; warp: tokens 16mt.., values 64nh..
-    {
-        float acc[8][4] = {};
-        for (int ks = mt; ks < 4; ++ks) {  // Minv^T is upper triangular
-            uint32_t ah[4], al[4];
-            ldsm4t(ah, at_addr(sm.M[0], LB64, 16 * mt, 16 * ks, lane));
-            ldsm4t(al, at_addr(sm.M[1], LB64, 16 * mt, 16 * ks, lane));
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bh[4], bl[4];
-                ldsm4t(bh, bk_addr(sm.X[0], LB, 16 * ks, 64 * nh + 16 * np, lane));
-                ldsm4t(bl, bk_addr(sm.X[1], LB, 16 * ks, 64 * nh + 16 * np, lane));
-                mma_x3(acc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                mma_x3(acc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
-            }
-        }
-        float* dR = p.dR + chd * CH * D;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int row = 16 * mt + g + 8 * hf, col = 64 * nh + 8 * nt + 2 * t;
-                *reinterpret_cast<float2*>(dR + row * D + col) =
-                    make_float2(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
-                uint32_t hi, lo;
-                split2(acc[nt][2 * hf], acc[nt][2 * hf + 1], hi, lo);
-                *reinterpret_cast<uint32_t*>(&sm.R[0][row * LB + col]) = hi;
-                *reinterpret_cast<uint32_t*>(&sm.R[1][row * LB + col]) = lo;
-            }
-    }
-    __syncthreads();
-    // P = dR S0^T and dQg = dO S0^T  [64 tok x 128 key], contraction over values
-    {
-        float aP[8][4] = {}, aQ[8][4] = {};
-#pragma unroll 2
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t rh[4], rl[4], o[4];
-            ldsm4(rh, a_addr(sm.R[0], LB, 16 * mt, 16 * ks, lane));
-            ldsm4(rl, a_addr(sm.R[1], LB, 16 * mt, 16 * ks, lane));
-            ldsm4(o, a_addr(sm.O, LB, 16 * mt, 16 * ks, lane));
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bh[4], bl[4];
-                ldsm4(bh, bn_addr(sm.S[0], LB, 16 * ks, 64 * nh + 16 * np, lane));
-                ldsm4(bl, bn_addr(sm.S[1], LB, 16 * ks, 64 * nh + 16 * np, lane));
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    mma_x3(aP[2 * np + hh], rh, rl, bh[2 * hh], bh[2 * hh + 1], bl[2 * hh], bl[2 * hh + 1]);
-                    mma_x2b(aQ[2 * np + hh], o, bh[2 * hh], bh[2 * hh + 1], bl[2 * hh], bl[2 * hh + 1]);
-                }
-            }
-        }
-        float* P = p.P + chd * CH * D;
-        float* dQg = p.dQg + chd * CH * D;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int row = 16 * mt + g + 8 * hf, col = 64 * nh + 8 * nt + 2 * t;
-                *reinterpret_cast<float2*>(P + row * D + col) = make_float2(aP[nt][2 * hf], aP[nt][2 * hf + 1]);
-                *reinterpret_cast<float2*>(dQg + row * D + col) =
-                    make_float2(p.scale * aQ[nt][2 * hf], p.scale * aQ[nt][2 * hf + 1]);
-            }
-    }
-    // dAqk = tril(dO Delta^T), dM = -strict_tril(dR Delta^T)  [64 x 64]; warp: rows 16mt, cols 32nh
-    {
-        float aA[4][4] = {}, aM[4][4] = {};
-#pragma unroll 2
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t rh[4], rl[4], o[4];
-            ldsm4(rh, a_addr(sm.R[0], LB, 16 * mt, 16 * ks, lane));
-            ldsm4(rl, a_addr(sm.R[1], LB, 16 * mt, 16 * ks, lane));
-            ldsm4(o, a_addr(sm.O, LB, 16 * mt, 16 * ks, lane));
-#pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                uint32_t bh[4], bl[4];
-                ldsm4(bh, bn_addr(sm.Dl[0], LB, 16 * ks, 32 * nh + 16 * np, lane));
-                ldsm4(bl, bn_addr(sm.Dl[1], LB, 16 * ks, 32 * nh + 16 * np, lane));
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    mma_x2b(aA[2 * np + hh], o, bh[2 * hh], bh[2 * hh + 1], bl[2 * hh], bl[2 * hh + 1]);
-                    mma_x3(aM[2 * np + hh], rh, rl, bh[2 * hh], bh[2 * hh + 1], bl[2 * hh], bl[2 * hh + 1]);
-                }
-            }
-        }
-        float* dAqk = p.dAqk + chd * CH * CH;
-        float* dM = p.dM + chd * CH * CH;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 16 * mt + g + 8 * (e >> 1), s = 32 * nh + 8 * nt + 2 * t + (e & 1);
-                dAqk[r * CH + s] = s <= r ? p.scale * aA[nt][e] : 0.f;
-                dM[r * CH + s] = s < r ? -aM[nt][e] : 0.f;
-            }
-    }
-    __syncthreads();
-    // dKb = Delta dS1^T  [64 tok x 128 key]; rsum = rowsum(S0 * dS1) from the hi + lo parts of
-    // both (16 significant bits), taken before the staged S0 is replaced by dS1
-    {
-        uint4 vh[8], vl[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
-            vh[k] = *reinterpret_cast<const uint4*>(dS1 + r * D + c8);
-            vl[k] = *reinterpret_cast<const uint4*>(dS1 + D * D + r * D + c8);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;  // 16 lanes per row
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&vh[k]);
-            const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&vl[k]);
-            const __nv_bfloat162* sh = reinterpret_cast<const __nv_bfloat162*>(&sm.S[0][r * LB + c8]);
-            const __nv_bfloat162* sl = reinterpret_cast<const __nv_bfloat162*>(&sm.S[1][r * LB + c8]);
-            float a = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 d0 = __bfloat1622float2(h2[j]), d1 = __bfloat1622float2(l2[j]);
-                const float2 s0 = __bfloat1622float2(sh[j]), s1 = __bfloat1622float2(sl[j]);
-                a = fmaf(s0.x + s1.x, d0.x + d1.x, a);
-                a = fmaf(s0.y + s1.y, d0.y + d1.y, a);
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if ((lane & 15) == 0) p.rsum[chd * D + r] = a;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + NTHR * k, r = i >> 4, c8 = (i & 15) * 8;
-            *reinterpret_cast<uint4*>(&sm.S[0][r * LB + c8]) = vh[k];
-            *reinterpret_cast<uint4*>(&sm.S[1][r * LB + c8]) = vl[k];
-        }
-    }
-    __syncthreads();
-    {
-        float acc[8][4] = {};
-#pragma unroll 2
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t ah[4], al[4];
-            ldsm4(ah, a_addr(sm.Dl[0], LB, 16 * mt, 16 * ks, lane));
-            ldsm4(al, a_addr(sm.Dl[1], LB, 16 * mt, 16 * ks, lane));
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bh[4], bl[4];
-                ldsm4(bh, bn_addr(sm.S[0], LB, 16 * ks, 64 * nh + 16 * np, lane));
-                ldsm4(bl, bn_addr(sm.S[1], LB, 16 * ks, 64 * nh + 16 * np, lane));
-                mma_x3(acc[2 * np], ah, al, bh[0], bh[1], bl[0], bl[1]);
-                mma_x3(acc[2 * np + 1], ah, al, bh[2], bh[3], bl[2], bl[3]);
-            }
-        }
-        float* dKb = p.dKb + chd * CH * D;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int row = 16 * mt + g + 8 * hf, col = 64 * nh + 8 * nt + 2 * t;
-                *reinterpret_cast<float2*>(dKb + row * D + col) = make_float2(acc[nt][2 * hf], acc[nt][2 * hf + 1]);
-            }
-    }
-}
-
-namespace {
-
+constexpr int LB = 136;  // row stride (bf16) of [rows][128] tiles
 constexpr int LAS = 68;  // row stride (fp32) of the staged 64x64 gradient matrices
 
 struct BwdIntraSmem {
@@ -594,7 +376,8 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
         float part = 0.f;  // sum over the 16 warps' row sets, fixed order
 #pragma unroll
         for (int ww = 0; ww < NW; ++ww) part += S.kbp[ww * D + c];
-        const float dgl = __expf(gl) * p.rsum[chd * D + c] + part;
+        const float* rs = p.rsum + chd * 2 * D + c;  // rowsum(S_c * dS1): two partials, fixed order
+        const float dgl = __expf(gl) * (rs[0] + rs[D]) + part;
         float carry = 0.f;  // totals of the later quarters
         for (int q2 = qu + 1; q2 < 4; ++q2) carry += S.red[BT + q2 * D + c];
         for (int r = r0; r < r0 + 16; ++r) S.dG[r * LDP + c] += carry + dgl;

@@ -119,7 +119,7 @@ inline Layout make_layout(int64_t T, int N, int H) {
     L.dKb = take(tileD * 4);
     L.dAqk = take(tileC * 4);
     L.dM = take(tileC * 4);
-    L.rsum = take(CHd * D * 4);
+    L.rsum = take(CHd * 2 * D * 4);  // [chunk-head][2 partials][key]
     L.pdA = take(CHd * 4);
     L.pddt = take(CHd * D * 4);
     L.ws_bwd_saved = o;
@@ -299,16 +299,19 @@ constexpr int GEMM_SCRATCH = 16 * 256;
 // chunk * H + head.
 struct TcMaps {
     CUtensorMap m128;  // W, Qg, Kb hi / lo planes as [tile][64 rows][128 bf16]
-    CUtensorMap m64;   // Aqk hi / lo planes as [tile][64 rows][64 bf16]
+    CUtensorMap m64;   // Aqk and Minv hi / lo planes as [tile][64 rows][64 bf16]
     CUtensorMap mdO;   // dO [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens} (backward)
-    int zWh, zWl, zQh, zQl, zKh, zKl, zAh, zAl;  // first tile of each plane
+    // backward per-chunk operands, tile = 2 * (chunk * H + head) + plane: dDelta and Delta
+    // [tile][64][128] (64 x 64 boxes), S_c and dS1 [tile][128][128] (64 x 128 boxes)
+    CUtensorMap mDD, mDl, mS, mdS;
+    int zWh, zWl, zQh, zQl, zKh, zKl, zAh, zAl, zMh, zMl;  // first tile of each plane
 };
 
 // ---- kernels (defined in the .cu files) and their dynamic shared memory ----
 size_t intra_smem_bytes();
 size_t chain_fwd_tc_smem_bytes();
 size_t chain_bwd_tc_smem_bytes();
-size_t bwd_gemm_smem_bytes();
+size_t bwd_gemm_tc_smem_bytes();
 size_t bwd_intra_smem_bytes();
 constexpr int CHAIN_THREADS = 256;  // 8 warps per state-recurrence block
 constexpr int BI_THREADS = 512;     // threads of the backward intra-chunk kernel
@@ -318,7 +321,7 @@ __global__ void k_plan(Params p);
 __global__ void k_intra_fwd(Params p);
 __global__ void k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
 __global__ void k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
-__global__ void k_bwd_gemms(Params p);
+__global__ void k_bwd_gemms_tc(Params p, const __grid_constant__ TcMaps tm);
 __global__ void k_bwd_intra(Params p);
 __global__ void k_param_reduce(Params p);
 __global__ void k_walk(int N, const int* doc_frag, int F, int H, const float* M, const float* B,

@@ -17,7 +17,7 @@ struct Rec {
 };
 std::vector<Rec> g_recs;
 const char* const kNames[KK_COUNT] = {"k_plan",      "k_intra_fwd",    "k_chain_fwd_tc",
-                                      "k_chain_bwd_tc", "k_bwd_gemms",    "k_bwd_intra",
+                                      "k_chain_bwd_tc", "k_bwd_gemms_tc",    "k_bwd_intra",
                                       "k_param_reduce", "k_walk"};
 }  // namespace
 

@@ -420,7 +420,11 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         const dim3 grid(unsigned(L.maxC), pr->H);
         {
             ProfScope ps(KK_BWD_GEMMS, st);
-            k_bwd_gemms_tc<<<grid, NTHR, SMEM_BWD_GEMMS_TC, st>>>(p, tm);
+            int dev = 0;
+            cudaGetDevice(&dev);
+            const long long items = L.maxC * pr->H;
+            k_bwd_gemms_tc<<<unsigned(items < g_sms[dev] ? items : g_sms[dev]), NTHR,
+                             SMEM_BWD_GEMMS_TC, st>>>(p, tm);
         }
         ProfScope ps(KK_BWD_INTRA, st);
         k_bwd_intra<<<grid, BI_THREADS, SMEM_BWD_INTRA, st>>>(p);

@@ -53,25 +53,24 @@ __device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, int x, i
 
 size_t bwd_gemm_tc_smem_bytes() { return BWD_GEMM_TC_SMEM; }
 
+// Persistent: one block per SM walks the (chunk, head) items item = chunk * H + head.  As soon as
+// an item's MMAs and row sums are done, every operand tile is free and the next item's TMA loads
+// start, overlapping this item's TMEM -> global epilogues.
 __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid_constant__ TcMaps tm) {
-    const int ci = blockIdx.x, h = blockIdx.y;
-    if (ci >= *p.nchunks) return;
+    const int items = *p.nchunks * p.H;
+    if (int(blockIdx.x) >= items) return;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = align1024b(smraw);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G_BAR);  // 0 G1 in, 1 G2 in, 2 MMA1, 3 MMA2/3, 4 dS1 in, 5 MMA4
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + G_BAR + 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G_BAR + 68);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int qd = w & 3, half = w >> 2;
     const int row = 32 * qd + lane;  // accumulator row / TMEM lane of this thread
-    const int chd = ci * p.H + h;
-    const int t0 = p.chunk_tab[ci].y;
 
-    if (tid == 0) {
-#pragma unroll
-        for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
-        tc::fence_mbar_init();
-        // G1: Minv (hi, lo) and dDelta (hi, lo); G2: dO into rows 64..127 of the hi [dR; dO]
-        // operand, S0 and Delta
+    // G1: Minv (hi, lo) and dDelta (hi, lo); G2: dO into rows 64..127 of the hi [dR; dO] operand,
+    // S0 and Delta (thread 0; t0 = the item's first token)
+    auto issue_loads = [&](int chd, int hh, int t0) {
         tc::mbar_expect_tx(&bar[0], 49152u);
         tma3(sm + G_MN, &tm.m64, 0, 0, tm.zMh + chd, &bar[0]);
         tma3(sm + G_MN + 8192, &tm.m64, 0, 0, tm.zMl + chd, &bar[0]);
@@ -83,16 +82,26 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
         tc::mbar_expect_tx(&bar[1], 114688u);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            tma3(sm + G_A + 16384 * kb + 8192, &tm.mdO, 64 * kb, h, t0, &bar[1]);
+            tma3(sm + G_A + 16384 * kb + 8192, &tm.mdO, 64 * kb, hh, t0, &bar[1]);
 #pragma unroll
             for (int pl = 0; pl < 2; ++pl) {
                 tma3(sm + G_S0 + 32768 * pl + 16384 * kb, &tm.mS, 64 * kb, 0, 2 * chd + pl, &bar[1]);
                 tma3(sm + G_DL + 16384 * pl + 8192 * kb, &tm.mDl, 64 * kb, 0, 2 * chd + pl, &bar[1]);
             }
         }
+    };
+    int pend = -1;  // phase parity of the G1 / G2 loads in flight (thread 0), -1 = none
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&bar[i], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        const int first = blockIdx.x;
+        issue_loads(first, first % p.H, p.chunk_tab[first / p.H].y);
+        pend = 0;
     }
     if (w == 0) tc::tmem_alloc(tslot, 512);
-    // lo plane of the dO rows: zero
+    // lo plane of the dO rows: zero for good (nothing else writes there)
     for (int i = tid; i < 2 * 8192 / 16; i += NTHR) {
         const int kb = i / 512, o = (i % 512) * 16;
         *reinterpret_cast<uint4*>(sm + G_A + 32768 + 16384 * kb + 8192 + o) = make_uint4(0u, 0u, 0u, 0u);
@@ -103,196 +112,215 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
     tc::fence_after_sync();
     const uint32_t taddr = *tslot;
     const uint32_t tl = taddr + (uint32_t(32 * qd) << 16);
-    bool ok = true;
+    const int tpa[3] = {0, 1, 0}, tpb[3] = {1, 0, 0};  // (A plane, B plane) of the split terms
 
-    // ---- MMA1: DR = Minv^T dDelta ----
-    if (tid == 0) {
-        if (tc::mbar_wait(&bar[0], 0)) {
-            tc::fence_after_sync();
-            const uint32_t sMN = smem_u32(sm + G_MN), sDD = smem_u32(sm + G_DD);
-            const uint64_t mh = tc::sdesc(sMN, 8192, 1024), ml = tc::sdesc(sMN + 8192, 8192, 1024);
-            const uint64_t dh = tc::sdesc(sDD, 8192, 1024), dl = tc::sdesc(sDD + 16384, 8192, 1024);
-            const uint64_t ta[3] = {mh, ml, mh}, tb[3] = {dl, dh, dh};
-            const uint32_t id = tc::idesc_bf16(128, 128, true, true);
-            uint32_t acc = 0;
-#pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3)
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    tc::mma(taddr, ta[t3] + uint64_t((s * 2048) >> 4), tb[t3] + uint64_t((s * 2048) >> 4), id, acc);
-                    acc = 1;
-                }
-        } else {
-            p.status[0] = KDA_ERR_TIMEOUT;
+    int it = 0;
+    for (int item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+        const uint32_t ph = uint32_t(it) & 1u;
+        const int chd = item;  // chunk * H + head
+        const int next = item + int(gridDim.x);
+        int t0n = 0, hn = 0;
+        if (tid == 0 && next < items) {  // the next item's first token, read early
+            t0n = p.chunk_tab[next / p.H].y;
+            hn = next % p.H;
         }
-        tc::mma_commit(&bar[2]);
-    }
-    __syncwarp();
-    ok = tc::mbar_wait(&bar[2], 0) && ok;
-    tc::fence_after_sync();
-    if (tid == 0) {  // G3: dS1 into the Minv / dDelta space, free now
-        tc::mbar_expect_tx(&bar[4], 65536u);
-#pragma unroll
-        for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-                tma3(sm + ds1_tile(pl, kb), &tm.mdS, 64 * kb, 0, 2 * chd + pl, &bar[4]);
-    }
-    __syncwarp();
 
-    // ---- dR: fp32 to global, hi / lo split into rows 0..63 of the [dR; dO] operand ----
-    if (qd < 2) {
-        float* dst = p.dR + size_t(chd) * CH * D + size_t(row) * D + 64 * half;
+        // ---- MMA1: DR = Minv^T dDelta ----
+        if (tid == 0) {
+            if (tc::mbar_wait(&bar[0], ph)) {
+                tc::fence_after_sync();
+                const uint32_t sMN = smem_u32(sm + G_MN), sDD = smem_u32(sm + G_DD);
+                const uint64_t mh = tc::sdesc(sMN, 8192, 1024), ml = tc::sdesc(sMN + 8192, 8192, 1024);
+                const uint64_t dh = tc::sdesc(sDD, 8192, 1024), dl = tc::sdesc(sDD + 16384, 8192, 1024);
+                const uint64_t ta[3] = {mh, ml, mh}, tb[3] = {dl, dh, dh};
+                const uint32_t id = tc::idesc_bf16(128, 128, true, true);
+                uint32_t acc = 0;
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            float v[32];
-            tc::tmem_ld32(tl + 64 * half + 32 * q2, v);
+                for (int t3 = 0; t3 < 3; ++t3)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                reinterpret_cast<float4*>(dst + 32 * q2)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    for (int s = 0; s < 4; ++s) {
+                        tc::mma(taddr, ta[t3] + uint64_t((s * 2048) >> 4), tb[t3] + uint64_t((s * 2048) >> 4), id, acc);
+                        acc = 1;
+                    }
+            } else {
+                *abort_flag = 1;
+            }
+            tc::mma_commit(&bar[2]);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(&bar[2], ph)) *abort_flag = 1;
+        tc::fence_after_sync();
+        if (tid == 0) {  // G3: dS1 into the Minv / dDelta space, free now
+            tc::mbar_expect_tx(&bar[4], 65536u);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {  // 16-byte chunk 4 q2 + j of this row's 128-byte K-block row
-                uint32_t hi[4], lo[4];
+            for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) split2(v[8 * j + 2 * e], v[8 * j + 2 * e + 1], hi[e], lo[e]);
-                const int off = row * 128 + (((4 * q2 + j) ^ (row & 7)) * 16);
-                *reinterpret_cast<uint4*>(sm + G_A + 16384 * half + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(sm + G_A + 32768 + 16384 * half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                for (int kb = 0; kb < 2; ++kb)
+                    tma3(sm + ds1_tile(pl, kb), &tm.mdS, 64 * kb, 0, 2 * chd + pl, &bar[4]);
+        }
+        __syncwarp();
+
+        // ---- dR: fp32 to global, hi / lo split into rows 0..63 of the [dR; dO] operand ----
+        if (qd < 2) {
+            float* dst = p.dR + size_t(chd) * CH * D + size_t(row) * D + 64 * half;
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float v[32];
+                tc::tmem_ld32(tl + 64 * half + 32 * q2, v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    reinterpret_cast<float4*>(dst + 32 * q2)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // 16-byte chunk 4 q2 + j of this row's K-block row
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) split2(v[8 * j + 2 * e], v[8 * j + 2 * e + 1], hi[e], lo[e]);
+                    const int off = row * 128 + (((4 * q2 + j) ^ (row & 7)) * 16);
+                    *reinterpret_cast<uint4*>(sm + G_A + 16384 * half + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(sm + G_A + 32768 + 16384 * half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
             }
         }
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (*abort_flag) break;
 
-    // ---- MMA2 / MMA3 ([dR; dO] S0^T, [dR; dO] Delta^T), then MMA4 (Delta dS1^T) ----
-    if (tid == 0) {
-        const uint32_t sA = smem_u32(sm + G_A), sS = smem_u32(sm + G_S0), sL = smem_u32(sm + G_DL);
-        const int tpa[3] = {0, 1, 0}, tpb[3] = {1, 0, 0};  // (A plane, B plane) per term
-        if (tc::mbar_wait(&bar[1], 0)) {
-            tc::fence_after_sync();
-            const uint32_t i2 = tc::idesc_bf16(128, 128, false, false);
-            const uint32_t i3 = tc::idesc_bf16(128, 64, false, false);
-            uint32_t acc = 0;
+        // ---- MMA2 / MMA3 ([dR; dO] S0^T, [dR; dO] Delta^T), then MMA4 (Delta dS1^T) ----
+        if (tid == 0) {
+            const uint32_t sA = smem_u32(sm + G_A), sS = smem_u32(sm + G_S0), sL = smem_u32(sm + G_DL);
+            if (tc::mbar_wait(&bar[1], ph)) {
+                pend = -1;
+                tc::fence_after_sync();
+                const uint32_t i2 = tc::idesc_bf16(128, 128, false, false);
+                const uint32_t i3 = tc::idesc_bf16(128, 64, false, false);
+                uint32_t acc = 0;
 #pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3)
+                for (int t3 = 0; t3 < 3; ++t3)
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const int kb = s >> 2, ko = (s & 3) * 32;
-                    const uint64_t a = tc::sdesc(sA + 32768 * tpa[t3] + 16384 * kb + ko, 16, 1024);
-                    const uint64_t b2 = tc::sdesc(sS + 32768 * tpb[t3] + 16384 * kb + ko, 16, 1024);
-                    const uint64_t b3 = tc::sdesc(sL + 16384 * tpb[t3] + 8192 * kb + ko, 16, 1024);
-                    tc::mma(taddr + 128, a, b2, i2, acc);
-                    tc::mma(taddr + 256, a, b3, i3, acc);
-                    acc = 1;
-                }
-        } else {
-            p.status[0] = KDA_ERR_TIMEOUT;
-        }
-        tc::mma_commit(&bar[3]);
-        if (tc::mbar_wait(&bar[4], 0)) {
-            tc::fence_after_sync();
-            const uint32_t i4 = tc::idesc_bf16(128, 128, false, false);
-            uint32_t acc = 0;
-#pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3)
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const int kb = s >> 2, ko = (s & 3) * 32;
-                    const uint64_t a = tc::sdesc(sL + 16384 * tpa[t3] + 8192 * kb + ko, 16, 1024);
-                    const uint64_t b = tc::sdesc(smem_u32(sm + ds1_tile(tpb[t3], kb)) + ko, 16, 1024);
-                    tc::mma(taddr + 320, a, b, i4, acc);
-                    acc = 1;
-                }
-        } else {
-            p.status[0] = KDA_ERR_TIMEOUT;
-        }
-        tc::mma_commit(&bar[5]);
-    }
-    __syncwarp();
-
-    // ---- P / dQg and dM / dAqk epilogues (overlap MMA4) ----
-    ok = tc::mbar_wait(&bar[3], 0) && ok;
-    tc::fence_after_sync();
-    {
-        const bool top = qd < 2;  // lanes 0..63: P and dM rows; lanes 64..127: dQg and dAqk rows
-        const int r = top ? row : row - 64;
-        float* dst = (top ? p.P : p.dQg) + size_t(chd) * CH * D + size_t(r) * D + 64 * half;
-        const float sc = top ? 1.f : p.scale;
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            float v[32];
-            tc::tmem_ld32(tl + 128 + 64 * half + 32 * q2, v);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                reinterpret_cast<float4*>(dst + 32 * q2)[j] =
-                    make_float4(sc * v[4 * j], sc * v[4 * j + 1], sc * v[4 * j + 2], sc * v[4 * j + 3]);
-        }
-        float v[32];
-        tc::tmem_ld32(tl + 256 + 32 * half, v);
-        float* da = (top ? p.dM : p.dAqk) + size_t(chd) * CH * CH + size_t(r) * CH + 32 * half;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float o4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s = 32 * half + 4 * j + e;
-                o4[e] = top ? (s < r ? -v[4 * j + e] : 0.f) : (s <= r ? p.scale * v[4 * j + e] : 0.f);
+                    for (int s = 0; s < 8; ++s) {
+                        const int kb = s >> 2, ko = (s & 3) * 32;
+                        const uint64_t a = tc::sdesc(sA + 32768 * tpa[t3] + 16384 * kb + ko, 16, 1024);
+                        const uint64_t b2 = tc::sdesc(sS + 32768 * tpb[t3] + 16384 * kb + ko, 16, 1024);
+                        const uint64_t b3 = tc::sdesc(sL + 16384 * tpb[t3] + 8192 * kb + ko, 16, 1024);
+                        tc::mma(taddr + 128, a, b2, i2, acc);
+                        tc::mma(taddr + 256, a, b3, i3, acc);
+                        acc = 1;
+                    }
+            } else {
+                *abort_flag = 1;
             }
-            reinterpret_cast<float4*>(da)[j] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+            tc::mma_commit(&bar[3]);
+            if (tc::mbar_wait(&bar[4], ph)) {
+                tc::fence_after_sync();
+                const uint32_t i4 = tc::idesc_bf16(128, 128, false, false);
+                uint32_t acc = 0;
+#pragma unroll
+                for (int t3 = 0; t3 < 3; ++t3)
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const int kb = s >> 2, ko = (s & 3) * 32;
+                        const uint64_t a = tc::sdesc(sL + 16384 * tpa[t3] + 8192 * kb + ko, 16, 1024);
+                        const uint64_t b = tc::sdesc(smem_u32(sm + ds1_tile(tpb[t3], kb)) + ko, 16, 1024);
+                        tc::mma(taddr + 320, a, b, i4, acc);
+                        acc = 1;
+                    }
+            } else {
+                *abort_flag = 1;
+            }
+            tc::mma_commit(&bar[5]);
         }
-    }
+        __syncwarp();
 
-    // ---- dKb epilogue ----
-    ok = tc::mbar_wait(&bar[5], 0) && ok;
-    tc::fence_after_sync();
-    if (qd < 2) {
-        float* dst = p.dKb + size_t(chd) * CH * D + size_t(row) * D + 64 * half;
+        // ---- rowsum(S0 * dS1) of this thread's key over K block `half` (hi + lo of both) ----
+        bool ok = tc::mbar_wait(&bar[4], ph);  // makes the dS1 tiles visible to this thread
+        ok = tc::mbar_wait(&bar[3], ph) && ok;
+        ok = tc::mbar_wait(&bar[5], ph) && ok;  // every MMA of the item done: all tiles free after
+        if (!ok) *abort_flag = 1;
+        tc::fence_after_sync();
+        {
+            const unsigned char* s0h = sm + G_S0 + 16384 * half;
+            const unsigned char* d1h = sm + ds1_tile(0, half);
+            const unsigned char* d1l = sm + ds1_tile(1, half);
+            float part = 0.f;
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            float v[32];
-            tc::tmem_ld32(tl + 320 + 64 * half + 32 * q2, v);
+            for (int j = 0; j < 8; ++j) {  // 16-byte chunks in logical order
+                const int off = row * 128 + ((j ^ (row & 7)) * 16);
+                const uint4 a = *reinterpret_cast<const uint4*>(s0h + off);
+                const uint4 b = *reinterpret_cast<const uint4*>(s0h + 32768 + off);
+                const uint4 c = *reinterpret_cast<const uint4*>(d1h + off);
+                const uint4 d = *reinterpret_cast<const uint4*>(d1l + off);
+                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+                const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+                const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                reinterpret_cast<float4*>(dst + 32 * q2)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                for (int e = 0; e < 4; ++e) {
+                    const float2 s0 = __bfloat1622float2(a2[e]), s1 = __bfloat1622float2(b2[e]);
+                    const float2 g0 = __bfloat1622float2(c2[e]), g1 = __bfloat1622float2(d2[e]);
+                    part = fmaf(s0.x + s1.x, g0.x + g1.x, part);
+                    part = fmaf(s0.y + s1.y, g0.y + g1.y, part);
+                }
+            }
+            p.rsum[(size_t(chd) * 2 + half) * D + row] = part;
         }
-    }
-    // rowsum(S0 * dS1) of this thread's key over K block `half` (hi + lo of both): both tiles are
-    // still in shared memory; the (completed) wait makes the dS1 tiles visible to this thread
-    ok = tc::mbar_wait(&bar[4], 0) && ok;
-    {
-        const unsigned char* s0h = sm + G_S0 + 16384 * half;
-        const unsigned char* d1h = sm + ds1_tile(0, half);
-        const unsigned char* d1l = sm + ds1_tile(1, half);
-        float part = 0.f;
+        __syncthreads();  // every operand tile is free: the next item's loads start now
+        if (tid == 0 && next < items && !*abort_flag) {
+            issue_loads(next, hn, t0n);
+            pend = int(ph ^ 1u);
+        }
+
+        // ---- epilogues from TMEM (overlap the next item's loads) ----
+        {
+            const bool top = qd < 2;  // lanes 0..63: P and dM rows; lanes 64..127: dQg and dAqk rows
+            const int r = top ? row : row - 64;
+            float* dst = (top ? p.P : p.dQg) + size_t(chd) * CH * D + size_t(r) * D + 64 * half;
+            const float sc = top ? 1.f : p.scale;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {  // 16-byte chunks in logical order
-            const int off = row * 128 + ((j ^ (row & 7)) * 16);
-            const uint4 a = *reinterpret_cast<const uint4*>(s0h + off);
-            const uint4 b = *reinterpret_cast<const uint4*>(s0h + 32768 + off);
-            const uint4 c = *reinterpret_cast<const uint4*>(d1h + off);
-            const uint4 d = *reinterpret_cast<const uint4*>(d1l + off);
-            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-            const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
-            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d);
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float v[32];
+                tc::tmem_ld32(tl + 128 + 64 * half + 32 * q2, v);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 s0 = __bfloat1622float2(a2[e]), s1 = __bfloat1622float2(b2[e]);
-                const float2 g0 = __bfloat1622float2(c2[e]), g1 = __bfloat1622float2(d2[e]);
-                part = fmaf(s0.x + s1.x, g0.x + g1.x, part);
-                part = fmaf(s0.y + s1.y, g0.y + g1.y, part);
+                for (int j = 0; j < 8; ++j)
+                    reinterpret_cast<float4*>(dst + 32 * q2)[j] =
+                        make_float4(sc * v[4 * j], sc * v[4 * j + 1], sc * v[4 * j + 2], sc * v[4 * j + 3]);
+            }
+            float v[32];
+            tc::tmem_ld32(tl + 256 + 32 * half, v);
+            float* da = (top ? p.dM : p.dAqk) + size_t(chd) * CH * CH + size_t(r) * CH + 32 * half;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float o4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = 32 * half + 4 * j + e;
+                    o4[e] = top ? (s < r ? -v[4 * j + e] : 0.f) : (s <= r ? p.scale * v[4 * j + e] : 0.f);
+                }
+                reinterpret_cast<float4*>(da)[j] = make_float4(o4[0], o4[1], o4[2], o4[3]);
             }
         }
-        p.rsum[(size_t(chd) * 2 + half) * D + row] = part;
+        if (qd < 2) {
+            float* dst = p.dKb + size_t(chd) * CH * D + size_t(row) * D + 64 * half;
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                float v[32];
+                tc::tmem_ld32(tl + 320 + 64 * half + 32 * q2, v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    reinterpret_cast<float4*>(dst + 32 * q2)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+        }
+        tc::fence_before_sync();  // TMEM reads above come before the next item's MMAs
     }
-    if (!ok && tid == 0) p.status[0] = KDA_ERR_TIMEOUT;
-    if (tid == 0 && p.status[0] == KDA_ERR_TIMEOUT) {
-        // after a timed-out wait: let this block's TMA copies land (bounded) before it exits
-        tc::mbar_wait(&bar[0], 0, 100000000ull);
-        tc::mbar_wait(&bar[1], 0, 100000000ull);
-        tc::mbar_wait(&bar[4], 0, 100000000ull);
+
+    if (*abort_flag && tid == 0) {
+        // after a timed-out wait: let this block's TMA loads in flight land (bounded), report
+        if (pend >= 0) {
+            tc::mbar_wait(&bar[0], uint32_t(pend), 100000000ull);
+            tc::mbar_wait(&bar[1], uint32_t(pend), 100000000ull);
+        }
+        p.status[0] = KDA_ERR_TIMEOUT;
     }
     tc::fence_before_sync();
     __syncthreads();

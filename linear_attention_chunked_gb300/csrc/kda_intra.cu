@@ -51,7 +51,8 @@ static_assert(sizeof(IntraSmem) <= 232448, "intra shared memory above the opt-in
 size_t intra_smem_bytes() { return sizeof(IntraSmem); }
 
 // Persistent: one block per SM walks the (chunk, head) items item = chunk * H + head; the raw
-// inputs of its next item are loaded into registers while the current one is computed.
+// inputs of its next item are loaded into registers while the current one is computed, in three
+// bursts (q, k, then the gate) so that no burst fills the memory request queue of the SM.
 __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     constexpr int BT = INTRA_THREADS, NW = BT / 32;
     extern __shared__ __align__(16) unsigned char smraw[];
@@ -67,7 +68,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     float pb = 0.f, peA = 0.f;
     int nT0 = 0, nL = 0, nh = 0;  // first token, length and head of the next item
     int4 tab_ahead = make_int4(0, 0, 0, 0);  // chunk-table entry of the item after the next
-    auto fetch = [&](int item, int4 inf) {
+    // parts: bit 0 q, bit 1 k, bit 2 gate / beta / gate parameters / next chunk-table entry
+    auto fetch = [&](int item, int4 inf, int parts) {
         const int hh = item % p.H;
         const int T0 = inf.y, Ln = inf.z;
         nT0 = T0;
@@ -78,9 +80,10 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
             const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
             const size_t off = (size_t(T0 + r) * p.H + hh) * D + c8;
             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            pq[k] = r < Ln ? *reinterpret_cast<const uint4*>(p.q + off) : z;
-            pk[k] = r < Ln ? *reinterpret_cast<const uint4*>(p.k + off) : z;
+            if (parts & 1) pq[k] = r < Ln ? *reinterpret_cast<const uint4*>(p.q + off) : z;
+            if (parts & 2) pk[k] = r < Ln ? *reinterpret_cast<const uint4*>(p.k + off) : z;
         }
+        if (!(parts & 4)) return;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         cp_commit();
     };
     if (int(blockIdx.x) < items) {
-        fetch(blockIdx.x, p.chunk_tab[blockIdx.x / p.H]);
+        fetch(blockIdx.x, p.chunk_tab[blockIdx.x / p.H], 7);
         fetch_v();
     }
 
@@ -327,7 +330,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     }
     __syncthreads();
 
-    if (more) fetch(item + gridDim.x, tab_ahead);  // lands during Minv, W / U and the stores
+    int4 tab_next = tab_ahead;  // (the g part below overwrites tab_ahead)
+    if (more) fetch(item + gridDim.x, tab_next, 1);
 
     // 5. Minv = (I + diag(beta) Akk)^-1, blockwise: 16x16 diagonal inverses by substitution, then
     //    X_ij = -D_i sum_{l=j}^{i-1} diag(beta_i) Akk_il X_lj by increasing block distance
@@ -376,6 +380,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     }
 
     cp_wait<0>();  // this item's v tile (copied during the previous item's last phase)
+    if (more) fetch(item + gridDim.x, tab_next, 2);
 
     // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
     for (int i = tid; i < CH * D / 2; i += BT) {
@@ -434,8 +439,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
             }
     }
 
-    // 7. elementwise operands and the small matrices (eight consecutive elements per thread:
-    //    16-byte stores of every plane)
+    if (more) fetch(item + gridDim.x, tab_next, 4);
+
+    // 7. elementwise operands and the small matrices
     {
         __nv_bfloat16* Qh = p.Qh + chd * CH * D;
         __nv_bfloat16* Ql = p.Ql + chd * CH * D;

@@ -37,14 +37,53 @@ struct IntraSmem {
 // off-diagonal sub-chunk pairs (i, j), i > j, one per warp
 __constant__ int2 kPairs[6] = {{1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
 
-__device__ __forceinline__ int tri_row(int pi) {  // row of the pi-th entry of a lower triangle
-    int r = int((sqrtf(8.f * pi + 1.f) - 1.f) * 0.5f);
-    while ((r + 1) * (r + 2) / 2 <= pi) ++r;
-    while (r * (r + 1) / 2 > pi) --r;
-    return r;
-}
 
 static_assert(sizeof(IntraSmem) <= 232448, "intra shared memory above the opt-in limit");
+
+__device__ __forceinline__ float4 row4(const float* t, int r, int c4) {
+    return *reinterpret_cast<const float4*>(t + r * LDP + c4);
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
+}
+
+// Partial sums over this lane's channels (cbase + 32 j + 0..3, j = 0, 1) of the diagonal 8 x 8
+// block starting at row b0, for rows RB = 7 - RP (pairs s = RB..0, slots 0..RB) and RA = RP
+// (pairs s = RA..0, slots RB+1..8): akk = sum_c k_r E k_s, aqk = sum_c q_r E k_s with
+// E = exp(gam_r - gam_s) built as the running product of per-token decays (each <= 1).
+template <int RP>
+__device__ __forceinline__ void diag_pair_sums(const float* q, const float* k, const float* gam,
+                                               int b0, int cbase, float (&akk)[9], float (&aqk)[9]) {
+    constexpr int RB = 7 - RP, RA = RP;
+#pragma unroll
+    for (int j = 0; j < 9; ++j) akk[j] = aqk[j] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int c4 = cbase + 32 * j;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int R = pass == 0 ? RB : RA, slot0 = pass == 0 ? 0 : RB + 1;
+            const float4 kr = row4(k, b0 + R, c4), qr = row4(q, b0 + R, c4);
+            float4 gs = row4(gam, b0 + R, c4);
+            float4 E = make_float4(1.f, 1.f, 1.f, 1.f);
+#pragma unroll
+            for (int s = R; s >= 0; --s) {
+                const float4 ks = row4(k, b0 + s, c4);
+                const float4 x = make_float4(E.x * ks.x, E.y * ks.y, E.z * ks.z, E.w * ks.w);
+                akk[slot0 + R - s] = dot4(kr, x, akk[slot0 + R - s]);
+                aqk[slot0 + R - s] = dot4(qr, x, aqk[slot0 + R - s]);
+                if (s > 0) {
+                    const float4 gp = row4(gam, b0 + s - 1, c4);
+                    E.x *= __expf(gs.x - gp.x);
+                    E.y *= __expf(gs.y - gp.y);
+                    E.z *= __expf(gs.z - gp.z);
+                    E.w *= __expf(gs.w - gp.w);
+                    gs = gp;
+                }
+            }
+        }
+    }
+}
 
 }  // namespace
 
@@ -198,36 +237,47 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     }
     __syncthreads();
 
-    // 4a. diagonal 8x8 blocks, elementwise exact exponent differences (the lower-left 8x8
-    //     quadrant of each 16-row sub-chunk runs on tensor cores in 4c)
-    for (int idx = tid; idx < 8 * 36; idx += BT) {
-        const int b = idx / 36, pi = idx % 36;
-        const int rl = tri_row(pi), sl = pi - rl * (rl + 1) / 2;
-        const int r = 8 * b + rl, s = 8 * b + sl;
-        float akk = 0.f, aqk = 0.f, akk2 = 0.f, aqk2 = 0.f;
-        const float4* gr = reinterpret_cast<const float4*>(S.gam + r * LDP);
-        const float4* gs = reinterpret_cast<const float4*>(S.gam + s * LDP);
-        const float4* kr = reinterpret_cast<const float4*>(S.k + r * LDP);
-        const float4* ks = reinterpret_cast<const float4*>(S.k + s * LDP);
-        const float4* qr = reinterpret_cast<const float4*>(S.q + r * LDP);
-#pragma unroll 2
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-            const float4 a = gr[c4], b = gs[c4], ksv = ks[c4], krv = kr[c4], qrv = qr[c4];
-            const float e0 = ksv.x * __expf(a.x - b.x), e1 = ksv.y * __expf(a.y - b.y);
-            const float e2 = ksv.z * __expf(a.z - b.z), e3 = ksv.w * __expf(a.w - b.w);
-            akk = fmaf(krv.x, e0, akk);
-            aqk = fmaf(qrv.x, e0, aqk);
-            akk2 = fmaf(krv.y, e1, akk2);
-            aqk2 = fmaf(qrv.y, e1, aqk2);
-            akk = fmaf(krv.z, e2, akk);
-            aqk = fmaf(qrv.z, e2, aqk);
-            akk2 = fmaf(krv.w, e3, akk2);
-            aqk2 = fmaf(qrv.w, e3, aqk2);
+    // 4a. diagonal 8x8 blocks (the lower-left 8x8 quadrant of each 16-row sub-chunk runs on tensor
+    //     cores in 4c).  Warp = (row pair rp: rows 7 - rp and rp, blocks 4 bq..4 bq + 3, channel
+    //     half chh), lane = (block, 8-channel group): every lane of a warp runs the same rows, so
+    //     the running products need no divergent control flow.  Channel groups are summed with
+    //     shuffles, the two channel halves through shared scratch, both in a fixed order.
+    {
+        const int rp = warp & 3, bq = (warp >> 2) & 1, chh = warp >> 3;
+        const int b = 4 * bq + (lane >> 3), cg = lane & 7;
+        float akk[9], aqk[9];
+        switch (rp) {
+            case 0: diag_pair_sums<0>(S.q, S.k, S.gam, 8 * b, 64 * chh + 4 * cg, akk, aqk); break;
+            case 1: diag_pair_sums<1>(S.q, S.k, S.gam, 8 * b, 64 * chh + 4 * cg, akk, aqk); break;
+            case 2: diag_pair_sums<2>(S.q, S.k, S.gam, 8 * b, 64 * chh + 4 * cg, akk, aqk); break;
+            default: diag_pair_sums<3>(S.q, S.k, S.gam, 8 * b, 64 * chh + 4 * cg, akk, aqk); break;
         }
-        akk += akk2;
-        aqk += aqk2;
-        if (s < r) S.Akk[r * LDA + s] = akk;
-        S.Aqk[r * LDA + s] = aqk;
+#pragma unroll
+        for (int j = 0; j < 9; ++j)
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                akk[j] += __shfl_xor_sync(0xffffffffu, akk[j], o);
+                aqk[j] += __shfl_xor_sync(0xffffffffu, aqk[j], o);
+            }
+        float* part = &S.u.a.P[0][0];  // [channel half][block][row pair][9 akk | 9 aqk]
+        if (cg == 0) {
+#pragma unroll
+            for (int j = 0; j < 9; ++j) {
+                part[((chh * 8 + b) * 4 + rp) * 18 + j] = akk[j];
+                part[((chh * 8 + b) * 4 + rp) * 18 + 9 + j] = aqk[j];
+            }
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < 8 * 4 * 9; idx += BT) {
+        const int b = idx / 36, rp = (idx / 9) % 4, j = idx % 9;
+        const int rB = 7 - rp, rA = rp;
+        const bool rowB = j <= rB;
+        const int r = 8 * b + (rowB ? rB : rA), sc = 8 * b + (rowB ? rB - j : rA - (j - rB - 1));
+        const float* p0 = &S.u.a.P[0][0] + (b * 4 + rp) * 18;
+        const float* p1 = p0 + 8 * 4 * 18;
+        if (sc < r) S.Akk[r * LDA + sc] = p0[j] + p1[j];
+        S.Aqk[r * LDA + sc] = p0[9 + j] + p1[9 + j];
     }
     // 4b. B operands Ks_j[sl][c] = k[16j+sl][c] exp(gam[16j+15][c] - gam[16j+sl][c]), j = 0..2
     for (int idx = tid; idx < 3 * 16 * D; idx += BT) {

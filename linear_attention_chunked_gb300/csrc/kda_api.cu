@@ -243,6 +243,35 @@ kda_status make_bwd_maps(const Params& p, const Layout& L, TcMaps* tm) {
     return KDA_OK;
 }
 
+// Tensor maps of the backward intra-chunk kernel's inputs: q and k (64 x 64 boxes like dO) and
+// the dAqk / dM regions (3-D [chunk-head][64][64] fp32, 32 x 64 boxes).
+kda_status make_bwd_intra_maps(const Params& p, const Layout& L, int64_t T, TcMaps* tm) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return KDA_ERR_CUDA;
+    const size_t CHd = size_t(L.maxC) * L.H;
+    const cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t bq[3] = {64, 1, 64}, ba[3] = {32, 64, 1};
+    const cuuint64_t dq[3] = {D, cuuint64_t(L.H), cuuint64_t(T)}, sq[2] = {D * 2, cuuint64_t(L.H) * D * 2};
+    const cuuint64_t da[3] = {CH, CH, CHd}, sa[2] = {CH * 4, size_t(CH) * CH * 4};
+    struct {
+        CUtensorMap* m;
+        CUtensorMapDataType ty;
+        const void* base;
+        const cuuint64_t* dims;
+        const cuuint64_t* st;
+        const cuuint32_t* box;
+    } v[4] = {{&tm->mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, dq, sq, bq},
+              {&tm->mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, dq, sq, bq},
+              {&tm->mdA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dAqk, da, sa, ba},
+              {&tm->mdM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dM, da, sa, ba}};
+    for (auto& x : v)
+        if (enc(x.m, x.ty, 3, const_cast<void*>(x.base), x.dims, x.st, x.box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status launched() {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -397,6 +426,8 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
     if (kda_status s = make_tc_maps(p, L, &tm)) return s;
     if (kda_status s = make_dO_map(dO, pr->T, pr->H, &tm)) return s;
     if (kda_status s = make_bwd_maps(p, L, &tm)) return s;
+    if (L.maxC > 0)
+        if (kda_status s = make_bwd_intra_maps(p, L, pr->T, &tm)) return s;
     if (saved) {
         // the saved set already holds the intra products and states: only the chunk plan
         ProfScope ps(KK_PLAN, st);
@@ -417,17 +448,16 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
             p, CHAIN_BWD, tm);
     }
     if (L.maxC > 0) {
-        const dim3 grid(unsigned(L.maxC), pr->H);
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const long long items = L.maxC * pr->H;
+        const unsigned grid = unsigned(items < g_sms[dev] ? items : g_sms[dev]);  // persistent
         {
             ProfScope ps(KK_BWD_GEMMS, st);
-            int dev = 0;
-            cudaGetDevice(&dev);
-            const long long items = L.maxC * pr->H;
-            k_bwd_gemms_tc<<<unsigned(items < g_sms[dev] ? items : g_sms[dev]), NTHR,
-                             SMEM_BWD_GEMMS_TC, st>>>(p, tm);
+            k_bwd_gemms_tc<<<grid, NTHR, SMEM_BWD_GEMMS_TC, st>>>(p, tm);
         }
         ProfScope ps(KK_BWD_INTRA, st);
-        k_bwd_intra<<<grid, BI_THREADS, SMEM_BWD_INTRA, st>>>(p);
+        k_bwd_intra<<<grid, BI_THREADS, SMEM_BWD_INTRA, st>>>(p, tm);
     }
     if (p.gate_raw) {
         ProfScope ps(KK_PARAM_REDUCE, st);

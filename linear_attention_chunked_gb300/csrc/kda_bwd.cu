@@ -12,34 +12,51 @@
 // and through the exponent differences of Aqk / Akk into q, k and gam.  The r == s terms of Aqk
 // carry no gate dependence; they are left out of dgam symbolically so that they cancel exactly.
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
 namespace {
 
-constexpr int LB = 136;  // row stride (bf16) of [rows][128] tiles
-constexpr int LAS = 68;  // row stride (fp32) of the staged 64x64 gradient matrices
+// Shared tiles filled by the TMA unit keep its 128-byte swizzle (1024-byte aligned blocks of 8 rows
+// x 128 bytes; the 16-byte chunk j of row r sits at chunk position j ^ (r % 8)), which also keeps
+// the column-wise reads below free of bank conflicts:
+//   q, k:      two blocks [64 tokens][64 channels] bf16 (channels 0..63, 64..127), element qk_at
+//   dAqk, dM:  two blocks [64 rows][32 columns] fp32 (columns 0..31, 32..63), element a_at
+__device__ __forceinline__ int qk_at(int r, int c) {
+    return (c >> 6) * (CH * 64) + r * 64 + ((((c >> 3) & 7) ^ (r & 7)) << 3) + (c & 7);
+}
+__device__ __forceinline__ int a_at(int r, int c) {
+    return (c >> 5) * (CH * 32) + r * 32 + ((((c >> 2) & 7) ^ (r & 7)) << 2) + (c & 3);
+}
 
 struct BwdIntraSmem {
+    __nv_bfloat16 qb[2 * CH * 64], kb[2 * CH * 64];  // q, k as given (bf16); q^ = q * rq
+    float dA[2 * CH * 32], dAk[2 * CH * 32];         // dAqk and dAkk = beta_r dM
     float gam[CH * LDP];                             // in-chunk cumsum of g
-    float dQ[CH * LDP], dK[CH * LDP], dG[CH * LDP];  // accumulators of dq^, dk^, dgam
-    __nv_bfloat16 qb[CH * LB], kb[CH * LB];          // q, k as given (bf16); q^ = q * rq
-    float dA[CH * LAS], dAk[CH * LAS];               // dAqk and dAkk = beta_r dM
+    // accumulators of dq^, dk^, dgam; until step 2 the dQ / dK tiles hold, densely, rows 0..31 of
+    // dQg then P (dQ tile) and of dKb then dR (dK tile), copied during the previous item
+    float dQ[CH * LDP], dK[CH * LDP], dG[CH * LDP];
     float beta[CH], rq[CH], rk[CH];
     float dbp[CH];  // per-row dbeta, accumulated in steps 1-2 in a fixed order
+    float fin[32];  // last-level partials of step 7
     union {
         uint4 Af[24][2][32];  // split A fragments of dAqk / dAkk (fragment order), step 3
         struct {
-            float red[2 * BI_THREADS + 32];  // reduction scratch, steps 5 and 7
-            float kbp[16 * D];               // per-warp partials of sum_r dKb * Kb (step 2 -> 5)
+            float red[BI_THREADS];  // quarter totals of the reverse cumsum, step 5
+            float kbp[16 * D];      // per-warp partials of sum_r dKb * Kb (step 2 -> 5)
         };
+        float wsum[2][16][D];  // per-warp column partials of step 7
     };
+    uint64_t bar[2];  // TMA completion of the next item's inputs: 0 dAqk / dM, 1 q / k / staged rows
+    int abort;        // a wait timed out
 };
-static_assert(sizeof(BwdIntraSmem) <= 232448, "backward intra shared memory above the opt-in limit");
+constexpr size_t BWD_INTRA_SMEM = sizeof(BwdIntraSmem) + 1024;  // + alignment slack of the base
+static_assert(BWD_INTRA_SMEM <= 232448, "backward intra shared memory above the opt-in limit");
 
 }  // namespace
 
-size_t bwd_intra_smem_bytes() { return sizeof(BwdIntraSmem); }
+size_t bwd_intra_smem_bytes() { return BWD_INTRA_SMEM; }
 
 // Intra-chunk gradients of one (chunk, head): dq, dk, dv, dbeta, dg / da and the partials of
 // dA_log / ddt_bias.  The contractions through the exponent differences,
@@ -49,85 +66,152 @@ size_t bwd_intra_smem_bytes() { return sizeof(BwdIntraSmem); }
 // cores: for destination rows of sub-chunk i the factor is split at the first row of i (both parts
 // <= 1), for destination columns of sub-chunk j at its last row.  Inside a sub-chunk they are formed
 // elementwise.  The r == s terms of Aqk (no gate dependence) enter dq and dk only.  512 threads.
-__global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
+//
+// Persistent: one block per SM walks the items item = chunk * H + head.  The inputs of its next
+// item are fetched while the current one is computed, in two parts that land in tiles the current
+// item no longer reads.  Shared-memory tiles are copied row by row by the TMA unit (issued by warp 0,
+// completion on an mbarrier), so no other warp waits on the issue: once step 4 is done, dAqk and dM;
+// once step 6 is done, q, k and the first half of dQg, P, dKb, dR.  Akk, gam, v and beta of the next
+// item go to registers.  Every wait is bounded; after a timeout the block stops and reports.
+__global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __grid_constant__ TcMaps tm) {
     constexpr int BT = BI_THREADS, NW = BT / 32;
-    const int ci = blockIdx.x, h = blockIdx.y;
-    if (ci >= *p.nchunks) return;
-    const int4 info = p.chunk_tab[ci];
-    const int t0 = info.y, L = info.z;
     extern __shared__ __align__(16) unsigned char smraw[];
-    BwdIntraSmem& S = *reinterpret_cast<BwdIntraSmem*>(smraw);
+    // 1024-byte aligned base (offset arithmetic on the shared array keeps its address space known)
+    BwdIntraSmem& S = *reinterpret_cast<BwdIntraSmem*>(smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    auto Qv = [&](int r, int c) { return __bfloat162float(S.qb[r * LB + c]) * S.rq[r]; };
-    auto Kv = [&](int r, int c) { return __bfloat162float(S.kb[r * LB + c]) * S.rk[r]; };
-    const size_t chd = size_t(ci) * p.H + h;
+    const int items = *p.nchunks * p.H;
+    if (int(blockIdx.x) >= items) return;
+    auto Qv = [&](int r, int c) { return __bfloat162float(S.qb[qk_at(r, c)]) * S.rq[r]; };
+    auto Kv = [&](int r, int c) { return __bfloat162float(S.kb[qk_at(r, c)]) * S.rk[r]; };
+
+    float4 pA[2], pgm[4];  // Akk and gam of the next item
+    uint2 pv[2];           // v, first half, of the next item
+    float pb = 0.f;        // beta of the next item (threads < 64)
+    int4 ntab = make_int4(0, 0, 0, 0);
+    int nT0 = 0, nL = 0, nh = 0;  // first token, length and head of the next item
+    // part A: dAqk, dM by TMA (thread 0); Akk, gam, the chunk-table entry to registers
+    auto fetchA = [&](int item) {
+        const size_t nchd = size_t(item);
+        if (tid == 0) {
+            tc::fence_async_smem();  // the tiles' earlier generic accesses come first
+            tc::mbar_expect_tx(&S.bar[0], 2u * CH * CH * 4u);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                tc::tma3(S.dA + hb * CH * 32, &tm.mdA, 32 * hb, 0, item, &S.bar[0]);
+                tc::tma3(S.dAk + hb * CH * 32, &tm.mdM, 32 * hb, 0, item, &S.bar[0]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) pA[k] = reinterpret_cast<const float4*>(p.Akk + nchd * CH * CH)[tid + BT * k];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pgm[k] = reinterpret_cast<const float4*>(p.gam + nchd * CH * D)[tid + BT * k];
+        ntab = p.chunk_tab[item / p.H];
+    };
+    // part B: the item's 64 token rows of q and k (rows past the document end are cleared once
+    // they land) and rows 0..31 of dQg, P, dKb, dR by TMA (thread 0); v and beta to registers
+    auto fetchB = [&](int item) {
+        const int T0 = ntab.y, Ln = ntab.z, hh = item % p.H;
+        nT0 = T0;
+        nL = Ln;
+        nh = hh;
+        const size_t nchd = size_t(item);
+        if (tid == 0) {
+            tc::fence_async_smem();
+            tc::mbar_expect_tx(&S.bar[1], 4u * CH * 64u * 2u + 4u * 32u * D * 4u);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                tc::tma3(S.qb + hb * CH * 64, &tm.mq, 64 * hb, hh, T0, &S.bar[1]);
+                tc::tma3(S.kb + hb * CH * 64, &tm.mk, 64 * hb, hh, T0, &S.bar[1]);
+            }
+            tc::bulk_g2s(S.dQ, p.dQg + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
+            tc::bulk_g2s(S.dQ + 32 * D, p.P + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
+            tc::bulk_g2s(S.dK, p.dKb + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
+            tc::bulk_g2s(S.dK + 32 * D, p.dR + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = (tid + BT * k) >> 5, c0 = (tid & 31) * 4;
+            pv[k] = r < Ln ? *reinterpret_cast<const uint2*>(p.v + (size_t(T0 + r) * p.H + hh) * D + c0)
+                           : make_uint2(0u, 0u);
+        }
+        if (tid < CH) pb = tid < Ln ? bf2f(p.beta[size_t(T0 + tid) * p.H + hh]) : 0.f;
+    };
+    if (tid == 0) {
+        tc::mbar_init(&S.bar[0], 1);
+        tc::mbar_init(&S.bar[1], 1);
+        S.abort = 0;
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    fetchA(blockIdx.x);
+    fetchB(blockIdx.x);
+    uint32_t ph = 0;  // phase parity of this item's two barriers
+
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int t0 = nT0, L = nL, h = nh;  // this item (its fetch was the latest one)
+    const size_t chd = size_t(item);
+    const bool more = item + int(gridDim.x) < items;
     const float* dQg = p.dQg + chd * CH * D;
     const float* Pp = p.P + chd * CH * D;
     const float* dKb = p.dKb + chd * CH * D;
     const float* dR = p.dR + chd * CH * D;
-    const float* dAqk = p.dAqk + chd * CH * CH;
-    const float* dM = p.dM + chd * CH * CH;
-    const float* Akk = p.Akk + chd * CH * CH;
 
-    // 1. inputs: q, k (bf16 rows, zero past the end), gam, beta, dAqk, dAkk; per-row L2 scales
-    {
-        uint4 vq[2], vk[2];
+    // 1. inputs: the second half of the step-2 inputs from global memory; the prefetched tiles and
+    //    registers to shared memory; dAkk = beta_r dM; per-row L2 scales
+    float4 vq1[2], vp1[2], vb1[2], vr1[2];
+    uint2 vv1[2];
 #pragma unroll
-        for (int k4 = 0; k4 < 2; ++k4) {
-            const int i = tid + BT * k4, r = i >> 4, c8 = (i & 15) * 8;
-            const size_t off = (size_t(t0 + r) * p.H + h) * D + c8;
-            vq[k4] = r < L ? *reinterpret_cast<const uint4*>(p.q + off) : make_uint4(0u, 0u, 0u, 0u);
-            vk[k4] = r < L ? *reinterpret_cast<const uint4*>(p.k + off) : make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + BT * (2 + k), r = i >> 5, c0 = (i & 31) * 4;
+        vq1[k] = reinterpret_cast<const float4*>(dQg)[i];
+        vp1[k] = reinterpret_cast<const float4*>(Pp)[i];
+        vb1[k] = reinterpret_cast<const float4*>(dKb)[i];
+        vr1[k] = reinterpret_cast<const float4*>(dR)[i];
+        vv1[k] = r < L ? *reinterpret_cast<const uint2*>(p.v + (size_t(t0 + r) * p.H + h) * D + c0)
+                       : make_uint2(0u, 0u);
+    }
+    if (!(tc::mbar_wait(&S.bar[0], ph) && tc::mbar_wait(&S.bar[1], ph))) S.abort = 1;
+    ph ^= 1u;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // q, k rows past the document end read as zero
+        const int i = tid + BT * k, r = i >> 4, j = i & 15;
+        if (r >= L) {
+            *reinterpret_cast<uint4*>(&S.qb[(j >> 3) * CH * 64 + r * 64 + (j & 7) * 8]) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(&S.kb[(j >> 3) * CH * 64 + r * 64 + (j & 7) * 8]) = make_uint4(0u, 0u, 0u, 0u);
         }
-        float4 v[4], va[2], vm[2], vak[2];
+    }
+    // dbeta_r <- sum_{s<r} Akk[r,s] dM[r,s] (dM is zero for s >= r): 16 lanes per row
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) v[k4] = reinterpret_cast<const float4*>(p.gam + chd * CH * D)[tid + BT * k4];
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + BT * k, r = i >> 4, c = (i & 15) * 4;
+        const float4 m4 = *reinterpret_cast<const float4*>(&S.dAk[a_at(r, c)]);
+        float a = pA[k].x * m4.x + pA[k].y * m4.y + pA[k].z * m4.z + pA[k].w * m4.w;
 #pragma unroll
-        for (int k4 = 0; k4 < 2; ++k4) {
-            va[k4] = reinterpret_cast<const float4*>(dAqk)[tid + BT * k4];
-            vm[k4] = reinterpret_cast<const float4*>(dM)[tid + BT * k4];
-            vak[k4] = reinterpret_cast<const float4*>(Akk)[tid + BT * k4];
-        }
-        // dbeta_r <- sum_{s<r} Akk[r,s] dM[r,s] (dM is zero for s >= r): 16 lanes per row
+        for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if ((i & 15) == 0) S.dbp[r] = a;
+    }
+    if (tid < CH) S.beta[tid] = pb;
 #pragma unroll
-        for (int k4 = 0; k4 < 2; ++k4) {
-            const int i = tid + BT * k4, r = i >> 4;
-            float a = vak[k4].x * vm[k4].x + vak[k4].y * vm[k4].y + vak[k4].z * vm[k4].z + vak[k4].w * vm[k4].w;
+    for (int k = 0; k < 4; ++k) {
+        const int i = tid + BT * k, r = i >> 5, c = (i & 31) * 4;
+        *reinterpret_cast<float4*>(&S.gam[r * LDP + c]) = pgm[k];
+    }
+    __syncthreads();  // beta, gam, the zero rows of q / k
+    if (*reinterpret_cast<volatile int*>(&S.abort)) break;
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if ((i & 15) == 0) S.dbp[r] = a;
-        }
-        if (tid < CH) S.beta[tid] = tid < L ? bf2f(p.beta[size_t(t0 + tid) * p.H + h]) : 0.f;
-#pragma unroll
-        for (int k4 = 0; k4 < 2; ++k4) {
-            const int i = tid + BT * k4, r = i >> 4, c8 = (i & 15) * 8;
-            *reinterpret_cast<uint4*>(&S.qb[r * LB + c8]) = vq[k4];
-            *reinterpret_cast<uint4*>(&S.kb[r * LB + c8]) = vk[k4];
-        }
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const int i = tid + BT * k4, r = i >> 5, c = (i & 31) * 4;
-            S.gam[r * LDP + c] = v[k4].x;
-            S.gam[r * LDP + c + 1] = v[k4].y;
-            S.gam[r * LDP + c + 2] = v[k4].z;
-            S.gam[r * LDP + c + 3] = v[k4].w;
-        }
-        __syncthreads();  // beta
-#pragma unroll
-        for (int k4 = 0; k4 < 2; ++k4) {
-            const int i = tid + BT * k4, r = i >> 4, c = (i & 15) * 4;
-            *reinterpret_cast<float4*>(&S.dA[r * LAS + c]) = va[k4];
-            const float br = S.beta[r];
-            *reinterpret_cast<float4*>(&S.dAk[r * LAS + c]) =
-                make_float4(br * vm[k4].x, br * vm[k4].y, br * vm[k4].z, br * vm[k4].w);
-        }
+    for (int k = 0; k < 2; ++k) {
+        const int i = tid + BT * k, r = i >> 4, c = (i & 15) * 4;
+        float4* m4 = reinterpret_cast<float4*>(&S.dAk[a_at(r, c)]);
+        const float br = S.beta[r];
+        const float4 m = *m4;
+        *m4 = make_float4(br * m.x, br * m.y, br * m.z, br * m.w);
     }
     for (int r = w; r < CH; r += NW) {
         float ra = 1.f, rb = 1.f;
         if (p.l2n) {
             float a = 0.f, b = 0.f;
             for (int c = lane; c < D; c += 32) {
-                const float x = __bfloat162float(S.qb[r * LB + c]), y = __bfloat162float(S.kb[r * LB + c]);
+                const float x = __bfloat162float(S.qb[qk_at(r, c)]), y = __bfloat162float(S.kb[qk_at(r, c)]);
                 a = fmaf(x, x, a);
                 b = fmaf(y, y, b);
             }
@@ -152,22 +236,30 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
         uint2 vv[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const int i = tid + BT * (2 * half + k), r = i >> 5, c0 = (i & 31) * 4;
-            vq[k] = reinterpret_cast<const float4*>(dQg)[i];
-            vp[k] = reinterpret_cast<const float4*>(Pp)[i];
-            vb[k] = reinterpret_cast<const float4*>(dKb)[i];
-            vr[k] = reinterpret_cast<const float4*>(dR)[i];
-            vv[k] = r < L ? *reinterpret_cast<const uint2*>(p.v + (size_t(t0 + r) * p.H + h) * D + c0)
-                          : make_uint2(0u, 0u);
+            if (half == 0) {  // staged densely in the accumulator tiles
+                const int i = (tid + BT * k) * 4;
+                vq[k] = *reinterpret_cast<const float4*>(&S.dQ[i]);
+                vp[k] = *reinterpret_cast<const float4*>(&S.dQ[32 * D + i]);
+                vb[k] = *reinterpret_cast<const float4*>(&S.dK[i]);
+                vr[k] = *reinterpret_cast<const float4*>(&S.dK[32 * D + i]);
+                vv[k] = pv[k];
+            } else {
+                vq[k] = vq1[k];
+                vp[k] = vp1[k];
+                vb[k] = vb1[k];
+                vr[k] = vr1[k];
+                vv[k] = vv1[k];
+            }
         }
+        if (half == 0) __syncthreads();  // every staged value is read before the tiles are written
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int i = tid + BT * (2 * half + k), r = i >> 5, c0 = (i & 31) * 4;
-            const float dgn = S.dA[r * LAS + r], br = S.beta[r], rqr = S.rq[r], rkr = S.rk[r];
+            const float dgn = S.dA[a_at(r, r)], br = S.beta[r], rqr = S.rq[r], rkr = S.rk[r];
             const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LDP + c0]);
             const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LDP + c0]);
-            const uint2 qb2 = *reinterpret_cast<const uint2*>(&S.qb[r * LB + c0]);
-            const uint2 kb2 = *reinterpret_cast<const uint2*>(&S.kb[r * LB + c0]);
+            const uint2 qb2 = *reinterpret_cast<const uint2*>(&S.qb[qk_at(r, c0)]);
+            const uint2 kb2 = *reinterpret_cast<const uint2*>(&S.kb[qk_at(r, c0)]);
             __nv_bfloat162 qa, qb_, ka, kb_, va_, vb_;
             memcpy(&qa, &qb2.x, 4);
             memcpy(&qb_, &qb2.y, 4);
@@ -224,8 +316,8 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const int m = m0 + g + 8 * (rr & 1), kx = k0 + 2 * t + 8 * (rr >> 1);
-                const float x0 = col ? A[kx * LAS + m] : A[m * LAS + kx];
-                const float x1 = col ? A[(kx + 1) * LAS + m] : A[m * LAS + kx + 1];
+                const float x0 = col ? A[a_at(kx, m)] : A[a_at(m, kx)];
+                const float x1 = col ? A[a_at(kx + 1, m)] : A[a_at(m, kx + 1)];
                 split2(x0, x1, hi[rr], lo[rr]);
             }
             S.Af[f][0][lane] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -332,7 +424,7 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
             for (int rl = sl + 1; rl < 16; ++rl) {
                 E *= ed[rl];
                 const int r = base + rl;
-                const float da = S.dA[r * LAS + base + sl], dk = S.dAk[r * LAS + base + sl];
+                const float da = S.dA[a_at(r, base + sl)], dk = S.dAk[a_at(r, base + sl)];
                 const float ks = kv[sl] * E;
                 aq[rl] = fmaf(da, ks, aq[rl]);
                 ak[rl] = fmaf(dk, ks, ak[rl]);
@@ -349,15 +441,16 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
     }
     __syncthreads();
 
-    // raw gate input of step 7, loaded here so its latency hides behind steps 5 and 6
-    float4 av[4];
-    if (p.gate_raw) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
-            av[k] = r < L ? *reinterpret_cast<const float4*>(p.g + (size_t(t0 + r) * p.H + h) * D + c4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+    // this item's inputs of steps 5 and 7 (their latency hides behind steps 5 and 6), then the first
+    // part of the next item's inputs
+    const float aLog = p.gate_raw ? p.A_log[h] : 0.f;
+    const float rs0 = p.rsum[chd * 2 * D + (tid & (D - 1))];  // rowsum(S_c * dS1): two partials
+    const float rs1 = p.rsum[chd * 2 * D + D + (tid & (D - 1))];
+    if (more) {
+        fetchA(item + gridDim.x);
+    } else {  // defined on every path, so nothing fetched stays live across steps 2-4
+        pA[0] = pA[1] = pgm[0] = pgm[1] = pgm[2] = pgm[3] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ntab = make_int4(0, 0, 0, 0);
     }
 
     // 5. chunk-end gate term dgL = e^gL rowsum(S0 * dS1) + sum_r dKb * Kb, then the reverse
@@ -371,15 +464,14 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
             suf += S.dG[r * LDP + c];
             S.dG[r * LDP + c] = suf;
         }
-        S.red[BT + tid] = suf;  // quarter total
+        S.red[tid] = suf;  // quarter total
         __syncthreads();
         float part = 0.f;  // sum over the 16 warps' row sets, fixed order
 #pragma unroll
         for (int ww = 0; ww < NW; ++ww) part += S.kbp[ww * D + c];
-        const float* rs = p.rsum + chd * 2 * D + c;  // rowsum(S_c * dS1): two partials, fixed order
-        const float dgl = __expf(gl) * (rs[0] + rs[D]) + part;
+        const float dgl = __expf(gl) * (rs0 + rs1) + part;
         float carry = 0.f;  // totals of the later quarters
-        for (int q2 = qu + 1; q2 < 4; ++q2) carry += S.red[BT + q2 * D + c];
+        for (int q2 = qu + 1; q2 < 4; ++q2) carry += S.red[q2 * D + c];
         for (int r = r0; r < r0 + 16; ++r) S.dG[r * LDP + c] += carry + dgl;
     }
     __syncthreads();
@@ -412,70 +504,78 @@ __global__ void __launch_bounds__(BI_THREADS) k_bwd_intra(Params p) {
         store_out4(p.dk, base + c0, make_float4(dk[0], dk[1], dk[2], dk[3]), p.out_fp32);
         if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, S.dbp[r], p.out_fp32);
     }
-    __syncthreads();  // step 7 reuses dQ / dK as scratch
+    __syncthreads();  // q, k and the accumulator tiles are free: the next item's second part
+    if (more) {
+        fetchB(item + gridDim.x);
+    } else {
+        pv[0] = pv[1] = make_uint2(0u, 0u);
+        pb = 0.f;
+        nT0 = nL = nh = 0;
+    }
 
     // 7. gate gradient: g form writes dg; raw form writes da and the parameter partials.
     //    In raw form the token's gate g_r is recovered from the stored cumsum, g_r = gam_r -
-    //    gam_{r-1}, and dg/da = -exp(A_log) sigmoid(a + dt_bias).
+    //    gam_{r-1}, and dg/da = -exp(A_log) sigmoid(a + dt_bias), where sigmoid(a + dt_bias) =
+    //    1 - exp(-softplus(a + dt_bias)) = -expm1(g_r / exp(A_log)).  Thread: rows w + 16 k, four
+    //    channels; per-warp column partials, then fixed-order sums over the warps.
     if (!p.gate_raw) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
             if (r < L)
                 *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
-                    make_float4(S.dG[r * LDP + c4], S.dG[r * LDP + c4 + 1], S.dG[r * LDP + c4 + 2],
-                                S.dG[r * LDP + c4 + 3]);
+                    *reinterpret_cast<const float4*>(&S.dG[r * LDP + c4]);
         }
-        return;
-    }
-    const float eA = expf(p.A_log[h]);
-    {
+    } else {
+        const float eA = expf(aLog), ieA = 1.f / eA;
         const int c4 = (tid & 31) * 4;
-        const float4 dtb = *reinterpret_cast<const float4*>(p.dt_bias + h * D + c4);
-        const float b4[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
+        float pd[4] = {0.f, 0.f, 0.f, 0.f}, pa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
-            const float a4[4] = {av[k].x, av[k].y, av[k].z, av[k].w};
+            const bool ok = r < L;
+            const float4 dg4 = *reinterpret_cast<const float4*>(&S.dG[r * LDP + c4]);
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LDP + c4]);
+            const float4 gp4 = r > 0 ? *reinterpret_cast<const float4*>(&S.gam[(r - 1) * LDP + c4])
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
+            const float gv[4] = {g4.x - gp4.x, g4.y - gp4.y, g4.z - gp4.z, g4.w - gp4.w};
             float da4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int c = c4 + j;
-                const bool ok = r < L;
-                const float x = a4[j] + b4[j], dg = S.dG[r * LDP + c];
-                const float gv = S.gam[r * LDP + c] - (r > 0 ? S.gam[(r - 1) * LDP + c] : 0.f);
-                da4[j] = ok ? dg * (-eA) * __frcp_rn(1.f + __expf(-x)) : 0.f;
-                S.dQ[r * LDP + c] = ok ? dg * gv : 0.f;
-                S.dK[r * LDP + c] = da4[j];
+                da4[j] = ok ? dgv[j] * eA * expm1f(gv[j] * ieA) : 0.f;
+                pd[j] += da4[j];
+                pa[j] += ok ? dgv[j] * gv[j] : 0.f;
             }
-            if (r < L)
+            if (ok)
                 *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
                     make_float4(da4[0], da4[1], da4[2], da4[3]);
         }
-    }
-    __syncthreads();
-    {
-        // column sums over the 64 rows: four threads per channel (16 rows each), fixed order
-        const int c = tid & (D - 1), qu = tid >> 7;
-        float pd = 0.f, pa = 0.f;
-        for (int r = 16 * qu; r < 16 * qu + 16; ++r) {
-            pd += S.dK[r * LDP + c];
-            pa += S.dQ[r * LDP + c];
+        *reinterpret_cast<float4*>(&S.wsum[0][w][c4]) = make_float4(pd[0], pd[1], pd[2], pd[3]);
+        *reinterpret_cast<float4*>(&S.wsum[1][w][c4]) = make_float4(pa[0], pa[1], pa[2], pa[3]);
+        __syncthreads();
+        if (tid < D) {  // warps 0..3: one channel per thread, then a fixed-order sum of the channels
+            float sd = 0.f, sa = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) {
+                sd += S.wsum[0][ww][tid];
+                sa += S.wsum[1][ww][tid];
+            }
+            p.pddt[chd * D + tid] = sd;
+            sa = warp_sum(sa);
+            if (lane == 0) S.fin[w] = sa;
         }
-        S.red[tid] = pd;
-        S.red[BT + tid] = pa;
+        __syncthreads();
+        if (tid == 0) p.pdA[chd] = (S.fin[0] + S.fin[1]) + (S.fin[2] + S.fin[3]);
     }
-    __syncthreads();
-    if (tid < D) {  // warps 0..3: one channel per thread, then a fixed-order sum of the channels
-        const int c = tid;
-        p.pddt[chd * D + c] = (S.red[c] + S.red[D + c]) + (S.red[2 * D + c] + S.red[3 * D + c]);
-        float pa = (S.red[BT + c] + S.red[BT + D + c]) + (S.red[BT + 2 * D + c] + S.red[BT + 3 * D + c]);
-        pa = warp_sum(pa);
-        if (lane == 0) S.red[2 * BT + w] = pa;
+    __syncthreads();  // the next item overwrites gam, beta, dbp and the union
+    }  // items
+    if (tid == 0 && S.abort) {
+        // after a timed-out wait: let the copies in flight land (bounded), report
+        tc::mbar_wait(&S.bar[0], ph ^ 1u, 100000000ull);
+        tc::mbar_wait(&S.bar[1], ph ^ 1u, 100000000ull);
+        p.status[0] = KDA_ERR_TIMEOUT;
     }
-    __syncthreads();
-    if (tid == 0)
-        p.pdA[chd] = (S.red[2 * BT] + S.red[2 * BT + 1]) + (S.red[2 * BT + 2] + S.red[2 * BT + 3]);
 }
 
 // Fixed-order sums of the per-chunk partials: dA_log[h], ddt_bias[h, :].

@@ -35,20 +35,6 @@ __host__ __device__ constexpr int ds1_tile(int pl, int kb) {
     return pl == 0 ? 16384 * kb : (kb == 0 ? 32768 : G_X);
 }
 
-__device__ __forceinline__ unsigned char* align1024b(unsigned char* p) {
-    return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                            ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                     uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
 }  // namespace
 
 size_t bwd_gemm_tc_smem_bytes() { return BWD_GEMM_TC_SMEM; }
@@ -60,7 +46,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
     const int items = *p.nchunks * p.H;
     if (int(blockIdx.x) >= items) return;
     extern __shared__ unsigned char smraw[];
-    unsigned char* sm = align1024b(smraw);
+    unsigned char* sm = tc::align1024(smraw);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G_BAR);  // 0 G1 in, 1 G2 in, 2 MMA1, 3 MMA2/3, 4 dS1 in, 5 MMA4
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + G_BAR + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G_BAR + 68);
@@ -72,21 +58,21 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
     // S0 and Delta (thread 0; t0 = the item's first token)
     auto issue_loads = [&](int chd, int hh, int t0) {
         tc::mbar_expect_tx(&bar[0], 49152u);
-        tma3(sm + G_MN, &tm.m64, 0, 0, tm.zMh + chd, &bar[0]);
-        tma3(sm + G_MN + 8192, &tm.m64, 0, 0, tm.zMl + chd, &bar[0]);
+        tc::tma3(sm + G_MN, &tm.m64, 0, 0, tm.zMh + chd, &bar[0]);
+        tc::tma3(sm + G_MN + 8192, &tm.m64, 0, 0, tm.zMl + chd, &bar[0]);
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
             for (int vb = 0; vb < 2; ++vb)
-                tma3(sm + G_DD + 16384 * pl + 8192 * vb, &tm.mDD, 64 * vb, 0, 2 * chd + pl, &bar[0]);
+                tc::tma3(sm + G_DD + 16384 * pl + 8192 * vb, &tm.mDD, 64 * vb, 0, 2 * chd + pl, &bar[0]);
         tc::mbar_expect_tx(&bar[1], 114688u);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            tma3(sm + G_A + 16384 * kb + 8192, &tm.mdO, 64 * kb, hh, t0, &bar[1]);
+            tc::tma3(sm + G_A + 16384 * kb + 8192, &tm.mdO, 64 * kb, hh, t0, &bar[1]);
 #pragma unroll
             for (int pl = 0; pl < 2; ++pl) {
-                tma3(sm + G_S0 + 32768 * pl + 16384 * kb, &tm.mS, 64 * kb, 0, 2 * chd + pl, &bar[1]);
-                tma3(sm + G_DL + 16384 * pl + 8192 * kb, &tm.mDl, 64 * kb, 0, 2 * chd + pl, &bar[1]);
+                tc::tma3(sm + G_S0 + 32768 * pl + 16384 * kb, &tm.mS, 64 * kb, 0, 2 * chd + pl, &bar[1]);
+                tc::tma3(sm + G_DL + 16384 * pl + 8192 * kb, &tm.mDl, 64 * kb, 0, 2 * chd + pl, &bar[1]);
             }
         }
     };
@@ -156,7 +142,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
             for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb)
-                    tma3(sm + ds1_tile(pl, kb), &tm.mdS, 64 * kb, 0, 2 * chd + pl, &bar[4]);
+                    tc::tma3(sm + ds1_tile(pl, kb), &tm.mdS, 64 * kb, 0, 2 * chd + pl, &bar[4]);
         }
         __syncwarp();
 

@@ -30,20 +30,6 @@ constexpr size_t CHAIN_TC_SMEM = OFF_BAR + 128 + 1024;  // + alignment slack of 
 
 static_assert(CHAIN_TC_SMEM <= 232448, "tcgen05 chain shared memory above the opt-in limit");
 
-__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
-    return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                            ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // 32 values -> packed bf16 hi / lo pairs
 __device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&h)[16],
                                         uint32_t (&l)[16]) {
@@ -88,7 +74,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const bool want_o = fwd && p.o != nullptr;
     const int col0 = (hv & 1) * 64;
     extern __shared__ unsigned char smraw[];
-    unsigned char* sm = align1024(smraw);
+    unsigned char* sm = tc::align1024(smraw);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // A1 in, K in, MMA1 done, MMA2 done
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + 36);
@@ -139,11 +125,11 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         tc::mbar_expect_tx(&bar[0], bytesA1);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            tma_load_3d(sm + OFF_A1 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWh + chd, &bar[0]);
-            tma_load_3d(sm + OFF_A1 + 32768 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWl + chd, &bar[0]);
+            tc::tma3(sm + OFF_A1 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWh + chd, &bar[0]);
+            tc::tma3(sm + OFF_A1 + 32768 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWl + chd, &bar[0]);
             if (want_o) {
-                tma_load_3d(sm + OFF_A1 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0, tm.zQh + chd, &bar[0]);
-                tma_load_3d(sm + OFF_A1 + 32768 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0,
+                tc::tma3(sm + OFF_A1 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0, tm.zQh + chd, &bar[0]);
+                tc::tma3(sm + OFF_A1 + 32768 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0,
                             tm.zQl + chd, &bar[0]);
             }
         }
@@ -153,12 +139,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         tc::mbar_expect_tx(&bar[1], bytesK);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_3d(sm + OFF_KT + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[1]);
-            tma_load_3d(sm + OFF_KT + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[1]);
+            tc::tma3(sm + OFF_KT + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[1]);
+            tc::tma3(sm + OFF_KT + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[1]);
         }
         if (want_o) {
-            tma_load_3d(sm + OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[1]);
-            tma_load_3d(sm + OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[1]);
+            tc::tma3(sm + OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[1]);
+            tc::tma3(sm + OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[1]);
         }
     };
     // per-thread operands of the next chunk, fetched one chunk ahead: its U row (lanes 0..63),
@@ -400,7 +386,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const bool bwd = mode == CHAIN_BWD;
     const int col0 = hv * 64;
     extern __shared__ unsigned char smraw[];
-    unsigned char* sm = align1024(smraw);
+    unsigned char* sm = tc::align1024(smraw);
     // barriers: 0 Kb+Aqk in, 1 dO in, 2 Qg+W in, 3 MMA-A done, 4 MMA-D done
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + B_OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_OFF_BAR + 48);
@@ -447,25 +433,25 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         tc::mbar_expect_tx(&bar[0], 49152u);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_3d(sm + B_OFF_KB + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[0]);
-            tma_load_3d(sm + B_OFF_KB + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[0]);
+            tc::tma3(sm + B_OFF_KB + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[0]);
+            tc::tma3(sm + B_OFF_KB + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[0]);
         }
-        tma_load_3d(sm + B_OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[0]);
-        tma_load_3d(sm + B_OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[0]);
+        tc::tma3(sm + B_OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[0]);
+        tc::tma3(sm + B_OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[0]);
     };
     auto load_O = [&](int t0) {
         tc::mbar_expect_tx(&bar[1], 8192u);
-        tma_load_3d(sm + B_OFF_DO, &tm.mdO, col0, h, t0, &bar[1]);
+        tc::tma3(sm + B_OFF_DO, &tm.mdO, col0, h, t0, &bar[1]);
     };
     auto load_QW = [&](int ci) {
         const int chd = ci * p.H + h;
         tc::mbar_expect_tx(&bar[2], 65536u);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_3d(sm + B_OFF_QG + b * 8192, &tm.m128, 64 * b, 0, tm.zQh + chd, &bar[2]);
-            tma_load_3d(sm + B_OFF_QG + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zQl + chd, &bar[2]);
-            tma_load_3d(sm + B_OFF_W + b * 8192, &tm.m128, 64 * b, 0, tm.zWh + chd, &bar[2]);
-            tma_load_3d(sm + B_OFF_W + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zWl + chd, &bar[2]);
+            tc::tma3(sm + B_OFF_QG + b * 8192, &tm.m128, 64 * b, 0, tm.zQh + chd, &bar[2]);
+            tc::tma3(sm + B_OFF_QG + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zQl + chd, &bar[2]);
+            tc::tma3(sm + B_OFF_W + b * 8192, &tm.m128, 64 * b, 0, tm.zWh + chd, &bar[2]);
+            tc::tma3(sm + B_OFF_W + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zWl + chd, &bar[2]);
         }
     };
     // next chunk's e^gL of this thread's key and first token, fetched one chunk ahead

@@ -304,6 +304,9 @@ struct TcMaps {
     // backward per-chunk operands, tile = 2 * (chunk * H + head) + plane: dDelta and Delta
     // [tile][64][128] (64 x 64 boxes), S_c and dS1 [tile][128][128] (64 x 128 boxes)
     CUtensorMap mDD, mDl, mS, mdS;
+    // backward intra-chunk inputs: q, k [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens};
+    // dAqk, dM [chunk * H + head][64][64] fp32 as 32 x 64 boxes (128-byte swizzle)
+    CUtensorMap mq, mk, mdA, mdM;
     int zWh, zWl, zQh, zQl, zKh, zKl, zAh, zAl, zMh, zMl;  // first tile of each plane
 };
 
@@ -322,7 +325,7 @@ __global__ void k_intra_fwd(Params p);
 __global__ void k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
 __global__ void k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
 __global__ void k_bwd_gemms_tc(Params p, const __grid_constant__ TcMaps tm);
-__global__ void k_bwd_intra(Params p);
+__global__ void k_bwd_intra(Params p, const __grid_constant__ TcMaps tm);
 __global__ void k_param_reduce(Params p);
 __global__ void k_walk(int N, const int* doc_frag, int F, int H, const float* M, const float* B,
                        const float* S0, int reverse, float* S_in, float* S_final);

@@ -417,18 +417,28 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
                 prev = cur;
             }
         }
+        // row rl of the block: columns sl = rl-1 down to 0, read four at a time (warp-wide broadcast)
 #pragma unroll
-        for (int sl = 0; sl < 15; ++sl) {
+        for (int rl = 1; rl < 16; ++rl) {
+            const int r = base + rl;
             float E = 1.f;
 #pragma unroll
-            for (int rl = sl + 1; rl < 16; ++rl) {
-                E *= ed[rl];
-                const int r = base + rl;
-                const float da = S.dA[a_at(r, base + sl)], dk = S.dAk[a_at(r, base + sl)];
-                const float ks = kv[sl] * E;
-                aq[rl] = fmaf(da, ks, aq[rl]);
-                ak[rl] = fmaf(dk, ks, ak[rl]);
-                bb[sl] = fmaf(fmaf(da, qv[rl], dk * kv[rl]), E, bb[sl]);
+            for (int q4 = (rl - 1) >> 2; q4 >= 0; --q4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(&S.dA[a_at(r, base + 4 * q4)]);
+                const float4 m4 = *reinterpret_cast<const float4*>(&S.dAk[a_at(r, base + 4 * q4)]);
+                const float av4[4] = {a4.x, a4.y, a4.z, a4.w}, mv4[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int e = 3; e >= 0; --e) {
+                    const int sl = 4 * q4 + e;
+                    if (sl < rl) {
+                        E *= ed[sl + 1];
+                        const float da = av4[e], dk = mv4[e];
+                        const float ks = kv[sl] * E;
+                        aq[rl] = fmaf(da, ks, aq[rl]);
+                        ak[rl] = fmaf(dk, ks, ak[rl]);
+                        bb[sl] = fmaf(fmaf(da, qv[rl], dk * kv[rl]), E, bb[sl]);
+                    }
+                }
             }
         }
 #pragma unroll

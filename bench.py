@@ -223,7 +223,7 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
             def fwd():
                 M, B = kda.kda_fragment_summary(*a, mode=kda.KDA_FRAG_FWD, ws=ws, **kw)
                 S_in, S_fin = kda.kda_transfer_walk(dfr, M, B)
-                o, _, _ = kda.kda_fwd(*a, h0=S_in, saved=saved, ws=ws, **kw)
+                o, _, _ = kda.kda_fwd(*a, h0=S_in, saved=saved, ws=ws, out_dtype=torch.bfloat16, **kw)
                 st.update(M=M, S_in=S_in)
 
             def fwd_bwd():
@@ -231,7 +231,7 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
                 C = kda.kda_fragment_summary(*a, mode=kda.KDA_FRAG_BWD, dO=x["dO"], ws=ws, **kw)
                 dS_end, dh0 = kda.kda_transfer_walk(dfr, st["M"], C, reverse=True)
                 kda.kda_bwd(*a, x["dO"], saved=saved, h0=st["S_in"], dht=dS_end, want_dh0=False,
-                            ws=ws, **kw)
+                            ws=ws, out_dtype=torch.bfloat16, **kw)
         else:
             a = (x["q"], x["k"], x["v"], x["beta"], x["g"], x["cu_seqlens"])
             T, N, H = w.T, w.N, w.H
@@ -243,11 +243,12 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
             saved = None if replay else torch.empty(svb, dtype=torch.uint8, device=dev)
 
             def fwd():
-                kda.kda_fwd(*a, saved=saved, save=not replay, ws=ws, **kw)
+                kda.kda_fwd(*a, saved=saved, save=not replay, ws=ws, out_dtype=torch.bfloat16, **kw)
 
             def fwd_bwd():
                 fwd()
-                kda.kda_bwd(*a, x["dO"], saved=saved, want_dh0=False, ws=ws, **kw)
+                kda.kda_bwd(*a, x["dO"], saved=saved, want_dh0=False, ws=ws, out_dtype=torch.bfloat16,
+                            **kw)
         f_ms = _time_calls(fwd)
         fb_ms = _time_calls(fwd_bwd)
         # roofline position of the row: algorithmic bytes and FLOPs per token-head (method I/O and
@@ -347,13 +348,15 @@ def main():
     wsb, _ = kda.kda_workspace_size(T, N, H, kda.KDA_OP_BWD_SAVED)
     ws = torch.empty(max(wsf, wsb), dtype=torch.uint8, device=dev)
     saved = torch.empty(svb, dtype=torch.uint8, device=dev)
-    f32 = torch.float32
-    o = torch.empty((T, H, 128), dtype=f32, device=dev)
+    # outputs in the inputs' dtype (o, dq, dk, dv, dbeta bf16), gate gradients and states fp32:
+    # the dtypes the algorithmic byte model counts and the pages' kernels return
+    f32, bf = torch.float32, torch.bfloat16
+    o = torch.empty((T, H, 128), dtype=bf, device=dev)
     ht = torch.empty((N, H, 128, 128), dtype=f32, device=dev)
-    grads = dict(dq=torch.empty((T, H, 128), dtype=f32, device=dev),
-                 dk=torch.empty((T, H, 128), dtype=f32, device=dev),
-                 dv=torch.empty((T, H, 128), dtype=f32, device=dev),
-                 dbeta=torch.empty((T, H), dtype=f32, device=dev),
+    grads = dict(dq=torch.empty((T, H, 128), dtype=bf, device=dev),
+                 dk=torch.empty((T, H, 128), dtype=bf, device=dev),
+                 dv=torch.empty((T, H, 128), dtype=bf, device=dev),
+                 dbeta=torch.empty((T, H), dtype=bf, device=dev),
                  dg=torch.empty((T, H, 128), dtype=f32, device=dev))
     if w.gate == "raw":
         grads["dA_log"] = torch.empty((H,), dtype=f32, device=dev)
@@ -363,9 +366,9 @@ def main():
     def step(x):
         a = (x["q"], x["k"], x["v"], x["beta"], x["g"], x["cu_seqlens"])
         kda.kda_fwd(*a, A_log=x["A_log"], dt_bias=x["dt_bias"], o=o, ht=ht, saved=saved, ws=ws,
-                    **kw)
+                    out_dtype=bf, **kw)
         kda.kda_bwd(*a, x["dO"], saved=saved, A_log=x["A_log"], dt_bias=x["dt_bias"],
-                    want_dh0=False, out=grads, ws=ws, **kw)
+                    want_dh0=False, out=grads, ws=ws, out_dtype=bf, **kw)
 
     def barrier():
         if world > 1:
@@ -467,7 +470,8 @@ def main():
                             if args.workload == "4doc" else None),
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"{w.row}:saved", "T": T, "H": H, "docs": list(w.lens),
-                       "d": 128, "chunk": 64, "outputs": "fp32",
+                       "d": 128, "chunk": 64,
+                       "outputs": "o, dq, dk, dv, dbeta bf16; dg / da, dA_log, dt_bias, states fp32",
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
             "clocks": ck,

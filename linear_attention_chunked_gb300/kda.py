@@ -132,6 +132,13 @@ def kda_workspace_size(T, N, H, op, **kw):
     return ws.value, sv.value
 
 
+def _check_dtypes(tensors, dtype):
+    """The library writes outputs in the dtype the problem declares: a caller's tensor must match."""
+    for name, t in tensors.items():
+        if t.dtype != dtype:
+            raise ValueError(f"{name} is {t.dtype}, the call writes {dtype}")
+
+
 def _empty_bytes(n, device):
     return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
 
@@ -158,6 +165,7 @@ def kda_fwd(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=
         saved = None
     if o is None:
         o = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    _check_dtypes({"o": o}, out_dtype)
     if ht is None:
         ht = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -180,6 +188,7 @@ def kda_fwd_static_ws(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None
                       out_dtype=out_dtype)
     if o is None:
         o = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    _check_dtypes({"o": o}, out_dtype)
     if ht is None:
         ht = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -213,6 +222,9 @@ def kda_bwd(q, k, v, beta, g_or_a, cu_seqlens, dO, *, saved=None, gate="g", A_lo
             out["ddt_bias"] = torch.empty((H, d), dtype=torch.float32, device=dev)
         if want_dh0:
             out["dh0"] = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    _check_dtypes({k: out[k] for k in ("dq", "dk", "dv", "dbeta")}, out_dtype)
+    _check_dtypes({k: out[k] for k in ("dg", "dA_log", "ddt_bias", "dh0") if out.get(k) is not None},
+                  torch.float32)
     with torch.cuda.device(dev):
         st = lib().kda_bwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_or_a),
                            _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(dO), _ptr(dht), _ptr(saved),

@@ -104,3 +104,10 @@ def test_pointer_validation(lib):
     pf.cu_seqlens = 256
     assert lib.kda_fragment_summary(ctypes.byref(pf), 5, *([a] * 10), a, 1 << 40, z) == \
         kda.KDA_ERR_INVALID_ARG
+
+
+def test_output_dtype_must_match_the_declared_one():
+    import torch
+    kda._check_dtypes({"o": torch.empty(2, dtype=torch.bfloat16)}, torch.bfloat16)
+    with pytest.raises(ValueError, match="dq is torch.float32"):
+        kda._check_dtypes({"dq": torch.empty(2, dtype=torch.float32)}, torch.bfloat16)

@@ -199,6 +199,26 @@ kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return KDA_ERR_CUDA;
+    // multi-block images: the extra dimensions step through column blocks (128 B), planes (CHd
+    // tiles) and W -> Qg (2 CHd tiles) inside the same record
+    const cuuint32_t es5[5] = {1, 1, 1, 1, 1};
+    const cuuint32_t b5[5] = {64, 64, 2, 2, 1}, b4[4] = {64, 64, 2, 1};
+    const cuuint64_t dA1[5] = {64, CH, 2, 2, 6 * CHd};
+    const cuuint64_t sA1[4] = {D * 2, 2 * CHd * t128, 128, t128};
+    const cuuint64_t dKb[5] = {64, CH, 2, 2, 6 * CHd};
+    const cuuint64_t sKb[4] = {D * 2, 128, CHd * t128, t128};
+    const cuuint64_t dAq[4] = {CH, CH, 2, 4 * CHd};
+    const cuuint64_t sAq[3] = {CH * 2, CHd * t64, t64};
+    if (enc(&tm->mA1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, p.Wh, dA1, sA1, b5, es5,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&tm->mKb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, p.Wh, dKb, sKb, b5, es5,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&tm->mAq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.Ah, dAq, sAq, b4, es5,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KDA_ERR_CUDA;
     return KDA_OK;
 }
 
@@ -238,6 +258,24 @@ kda_status make_bwd_maps(const Params& p, const Layout& L, TcMaps* tm) {
     for (auto& x : v)
         if (enc(x.m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x.base), x.dims, x.st,
                 x.box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return KDA_ERR_CUDA;
+    // both planes and both value blocks of one chunk in a single load
+    const cuuint32_t es5[5] = {1, 1, 1, 1, 1};
+    const cuuint32_t b5d[5] = {64, 64, 2, 2, 1}, b5s[5] = {64, 128, 2, 2, 1};
+    const cuuint64_t dd5[5] = {64, CH, 2, 2, CHd}, sd5[4] = {D * 2, 128, size_t(CH) * D * 2, 2 * size_t(CH) * D * 2};
+    const cuuint64_t ds5[5] = {64, D, 2, 2, CHd}, ss5[4] = {D * 2, 128, size_t(D) * D * 2, 2 * size_t(D) * D * 2};
+    struct {
+        CUtensorMap* m;
+        const void* base;
+        const cuuint64_t* dims;
+        const cuuint64_t* st;
+        const cuuint32_t* box;
+    } v5[3] = {{&tm->mDD5, p.dDelta, dd5, sd5, b5d}, {&tm->mDl5, p.sDelta, dd5, sd5, b5d},
+               {&tm->mS5, p.sS, ds5, ss5, b5s}};
+    for (auto& x : v5)
+        if (enc(x.m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x.base), x.dims, x.st,
+                x.box, es5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return KDA_ERR_CUDA;
     return KDA_OK;

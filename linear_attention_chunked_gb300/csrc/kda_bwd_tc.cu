@@ -58,23 +58,13 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
     // S0 and Delta (thread 0; t0 = the item's first token)
     auto issue_loads = [&](int chd, int hh, int t0) {
         tc::mbar_expect_tx(&bar[0], 49152u);
-        tc::tma3(sm + G_MN, &tm.m64, 0, 0, tm.zMh + chd, &bar[0]);
-        tc::tma3(sm + G_MN + 8192, &tm.m64, 0, 0, tm.zMl + chd, &bar[0]);
-#pragma unroll
-        for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-            for (int vb = 0; vb < 2; ++vb)
-                tc::tma3(sm + G_DD + 16384 * pl + 8192 * vb, &tm.mDD, 64 * vb, 0, 2 * chd + pl, &bar[0]);
+        tc::tma4(sm + G_MN, &tm.mAq, 0, 0, 0, tm.zMh + chd, &bar[0]);         // Minv, both planes
+        tc::tma5(sm + G_DD, &tm.mDD5, 0, 0, 0, 0, chd, &bar[0]);              // dDelta, both planes
         tc::mbar_expect_tx(&bar[1], 114688u);
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tc::tma3(sm + G_A + 16384 * kb + 8192, &tm.mdO, 64 * kb, hh, t0, &bar[1]);
-#pragma unroll
-            for (int pl = 0; pl < 2; ++pl) {
-                tc::tma3(sm + G_S0 + 32768 * pl + 16384 * kb, &tm.mS, 64 * kb, 0, 2 * chd + pl, &bar[1]);
-                tc::tma3(sm + G_DL + 16384 * pl + 8192 * kb, &tm.mDl, 64 * kb, 0, 2 * chd + pl, &bar[1]);
-            }
-        }
+        for (int kb = 0; kb < 2; ++kb) tc::tma3(sm + G_A + 16384 * kb + 8192, &tm.mdO, 64 * kb, hh, t0, &bar[1]);
+        tc::tma5(sm + G_S0, &tm.mS5, 0, 0, 0, 0, chd, &bar[1]);               // S0, both planes
+        tc::tma5(sm + G_DL, &tm.mDl5, 0, 0, 0, 0, chd, &bar[1]);              // Delta, both planes
     };
     int pend = -1;  // phase parity of the G1 / G2 loads in flight (thread 0), -1 = none
     if (tid == 0) {

@@ -120,32 +120,26 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const uint32_t sDl = smem_u32(sm + OFF_DL);
 
     const uint32_t bytesA1 = want_o ? 65536u : 32768u, bytesK = want_o ? 49152u : 32768u;
+    // one TMA operation per operand image (each costs the issuing thread ~100+ cycles)
     auto load_A1 = [&](int ci) {
         const int chd = ci * p.H + h;
         tc::mbar_expect_tx(&bar[0], bytesA1);
+        if (want_o) {  // [W; Qg] per plane: {columns, rows, W / Qg, column block}
+            tc::tma5(sm + OFF_A1, &tm.mA1, 0, 0, 0, 0, tm.zWh + chd, &bar[0]);
+            tc::tma5(sm + OFF_A1 + 32768, &tm.mA1, 0, 0, 0, 0, tm.zWl + chd, &bar[0]);
+        } else {  // W rows only (rows 64..127 of the operand are not read back)
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tc::tma3(sm + OFF_A1 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWh + chd, &bar[0]);
-            tc::tma3(sm + OFF_A1 + 32768 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWl + chd, &bar[0]);
-            if (want_o) {
-                tc::tma3(sm + OFF_A1 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0, tm.zQh + chd, &bar[0]);
-                tc::tma3(sm + OFF_A1 + 32768 + kb * 16384 + 8192, &tm.m128, 64 * kb, 0,
-                            tm.zQl + chd, &bar[0]);
+            for (int kb = 0; kb < 2; ++kb) {
+                tc::tma3(sm + OFF_A1 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWh + chd, &bar[0]);
+                tc::tma3(sm + OFF_A1 + 32768 + kb * 16384, &tm.m128, 64 * kb, 0, tm.zWl + chd, &bar[0]);
             }
         }
     };
     auto load_K = [&](int ci) {
         const int chd = ci * p.H + h;
         tc::mbar_expect_tx(&bar[1], bytesK);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            tc::tma3(sm + OFF_KT + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[1]);
-            tc::tma3(sm + OFF_KT + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[1]);
-        }
-        if (want_o) {
-            tc::tma3(sm + OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[1]);
-            tc::tma3(sm + OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[1]);
-        }
+        tc::tma5(sm + OFF_KT, &tm.mKb, 0, 0, 0, 0, tm.zKh + chd, &bar[1]);
+        if (want_o) tc::tma4(sm + OFF_AQ, &tm.mAq, 0, 0, 0, tm.zAh + chd, &bar[1]);
     };
     // per-thread operands of the next chunk, fetched one chunk ahead: its U row (lanes 0..63),
     // e^gL of this thread's key, its chunk-table entry
@@ -428,16 +422,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const uint32_t sdO = smem_u32(sm + B_OFF_DO), sdS = smem_u32(sm + B_OFF_DS);
     const uint32_t sdD = smem_u32(sm + B_OFF_DD);
 
+    // one TMA operation per operand image, both planes and both key blocks
     auto load_KA = [&](int ci) {
         const int chd = ci * p.H + h;
         tc::mbar_expect_tx(&bar[0], 49152u);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            tc::tma3(sm + B_OFF_KB + b * 8192, &tm.m128, 64 * b, 0, tm.zKh + chd, &bar[0]);
-            tc::tma3(sm + B_OFF_KB + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zKl + chd, &bar[0]);
-        }
-        tc::tma3(sm + B_OFF_AQ, &tm.m64, 0, 0, tm.zAh + chd, &bar[0]);
-        tc::tma3(sm + B_OFF_AQ + 8192, &tm.m64, 0, 0, tm.zAl + chd, &bar[0]);
+        tc::tma5(sm + B_OFF_KB, &tm.mKb, 0, 0, 0, 0, tm.zKh + chd, &bar[0]);
+        tc::tma4(sm + B_OFF_AQ, &tm.mAq, 0, 0, 0, tm.zAh + chd, &bar[0]);
     };
     auto load_O = [&](int t0) {
         tc::mbar_expect_tx(&bar[1], 8192u);
@@ -446,13 +436,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     auto load_QW = [&](int ci) {
         const int chd = ci * p.H + h;
         tc::mbar_expect_tx(&bar[2], 65536u);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            tc::tma3(sm + B_OFF_QG + b * 8192, &tm.m128, 64 * b, 0, tm.zQh + chd, &bar[2]);
-            tc::tma3(sm + B_OFF_QG + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zQl + chd, &bar[2]);
-            tc::tma3(sm + B_OFF_W + b * 8192, &tm.m128, 64 * b, 0, tm.zWh + chd, &bar[2]);
-            tc::tma3(sm + B_OFF_W + 16384 + b * 8192, &tm.m128, 64 * b, 0, tm.zWl + chd, &bar[2]);
-        }
+        tc::tma5(sm + B_OFF_QG, &tm.mKb, 0, 0, 0, 0, tm.zQh + chd, &bar[2]);
+        tc::tma5(sm + B_OFF_W, &tm.mKb, 0, 0, 0, 0, tm.zWh + chd, &bar[2]);
     };
     // next chunk's e^gL of this thread's key and first token, fetched one chunk ahead
     float egn = 0.f;

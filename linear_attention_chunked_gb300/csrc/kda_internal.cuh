@@ -304,6 +304,13 @@ struct TcMaps {
     // backward per-chunk operands, tile = 2 * (chunk * H + head) + plane: dDelta and Delta
     // [tile][64][128] (64 x 64 boxes), S_c and dS1 [tile][128][128] (64 x 128 boxes)
     CUtensorMap mDD, mDl, mS, mdS;
+    // whole operand images in one load (dimension order = shared-memory order, innermost first):
+    //   mA1  [W; Qg] of one plane: {64 columns, 64 rows, type W / Qg, column block, tile}
+    //   mKb  Kb, Qg or W, both planes: {64 columns, 64 rows, column block, plane, tile}
+    //   mAq  Aqk or Minv, both planes: {64 columns, 64 rows, plane, tile}
+    //   mDD5, mDl5  dDelta / Delta, both planes: {64 values, 64 tokens, value block, plane, chunk}
+    //   mS5  saved S, both planes: {64 values, 128 keys, value block, plane, chunk}
+    CUtensorMap mA1, mKb, mAq, mDD5, mDl5, mS5;
     // backward intra-chunk inputs: q, k [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens};
     // dAqk, dM [chunk * H + head][64][64] fp32 as 32 x 64 boxes (128-byte swizzle)
     CUtensorMap mq, mk, mdA, mdM;

@@ -98,6 +98,24 @@ __device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, int x, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
+// 4-D and 5-D tiled tensor loads (one operation fills a whole multi-block operand image).
+__device__ __forceinline__ void tma4(void* dst, const CUtensorMap* map, int x, int y, int z, int u,
+                                     uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(u), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma5(void* dst, const CUtensorMap* map, int x, int y, int z, int u,
+                                     int v, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(u), "r"(v),
+        "r"(smem_u32(bar))
+        : "memory");
+}
 // First 1024-byte boundary at or after p (128-byte-swizzled tiles need it).
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
     return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &

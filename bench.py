@@ -134,17 +134,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------------------------
 # algorithmic bytes per kernel launch (method inputs and outputs a kernel must touch; workspace
-# intermediates excluded), per token-head, with this library's I/O formats: q, k, v, dO bf16;
-# beta bf16; gate fp32; o, dq, dk, dv, dbeta fp32 (parity-grade outputs)
+# intermediates excluded), per token-head, in the bench's I/O formats: q, k, v, beta, dO and the
+# outputs o, dq, dk, dv, dbeta bf16; gate and dg fp32
 
 
 def alg_bytes_per_token_head(kernel):
     qkv, beta, gate, dO = 3 * 256, 2, 512, 256
-    o, dqkv, dbeta, dg = 512, 3 * 512, 4, 512
+    o, dqkv, dbeta, dg = 256, 3 * 256, 2, 512
     table = {
         "k_intra_fwd": qkv + beta + gate,                    # reads the chunk inputs
-        "k_chain_fwd_tc": o,                                 # writes o
-        "k_chain_bwd_tc": dO,                                # reads dO
+        "k_chain_fwd": o,                                    # writes o
+        "k_chain_bwd": dO,                                   # reads dO
         "k_bwd_gemms_tc": dO,                                # reads dO
         "k_bwd_intra": qkv + beta + gate + dqkv + dbeta + dg,  # reads inputs, writes grads
     }

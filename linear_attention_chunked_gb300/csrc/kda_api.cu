@@ -310,6 +310,17 @@ kda_status make_bwd_intra_maps(const Params& p, const Layout& L, int64_t T, TcMa
     return KDA_OK;
 }
 
+// The state recurrences of the forward (o, ht, saved set) and of the backward: one block per
+// (document, head, value half), longest documents first.
+void launch_chain_fwd(const Params& p, const kda_problem* pr, const TcMaps& tm, cudaStream_t st) {
+    const unsigned pairs = unsigned(pr->N) * unsigned(pr->H);
+    k_chain_fwd_tc<<<pairs * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(p, CHAIN_FWD_OUT, tm);
+}
+void launch_chain_bwd(const Params& p, const kda_problem* pr, const TcMaps& tm, cudaStream_t st) {
+    const unsigned pairs = unsigned(pr->N) * unsigned(pr->H);
+    k_chain_bwd_tc<<<pairs * NHALF, CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(p, CHAIN_BWD, tm);
+}
+
 kda_status launched() {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -397,8 +408,7 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     if (kda_status s = run_prologue(p, st)) return s;
     {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
-            p, CHAIN_FWD_OUT, tm);
+        launch_chain_fwd(p, pr, tm, st);
     }
     return launched();
 }
@@ -477,13 +487,11 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         r.o = nullptr;
         r.ht = nullptr;
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
-            r, CHAIN_FWD_OUT, tm);
+        launch_chain_fwd(r, pr, tm, st);
     }
     {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
-            p, CHAIN_BWD, tm);
+        launch_chain_bwd(p, pr, tm, st);
     }
     if (L.maxC > 0) {
         int dev = 0;

@@ -50,6 +50,9 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G_BAR);  // 0 G1 in, 1 G2 in, 2 MMA1, 3 MMA2/3, 4 dS1 in, 5 MMA4
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + G_BAR + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G_BAR + 68);
+    // leave-the-loop decision: thread 0 copies the abort flag into the item's slot (parity) before
+    // the barrier and every thread reads that slot after it, so all warps leave together
+    volatile int* stopf = reinterpret_cast<volatile int*>(sm + G_BAR + 72);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int qd = w & 3, half = w >> 2;
     const int row = 32 * qd + lane;  // accumulator row / TMEM lane of this thread
@@ -159,9 +162,10 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
+        if (tid == 0) stopf[it & 1] = *abort_flag;
         __syncthreads();
         tc::fence_after_sync();
-        if (*abort_flag) break;
+        if (stopf[it & 1]) break;
 
         // ---- MMA2 / MMA3 ([dR; dO] S0^T, [dR; dO] Delta^T), then MMA4 (Delta dS1^T) ----
         if (tid == 0) {

@@ -30,29 +30,6 @@ constexpr size_t CHAIN_TC_SMEM = OFF_BAR + 128 + 1024;  // + alignment slack of 
 
 static_assert(CHAIN_TC_SMEM <= 232448, "tcgen05 chain shared memory above the opt-in limit");
 
-// 32 values -> packed bf16 hi / lo pairs
-__device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&h)[16],
-                                        uint32_t (&l)[16]) {
-#pragma unroll
-    for (int e = 0; e < 16; ++e) split2(v[2 * e], v[2 * e + 1], h[e], l[e]);
-}
-// 128-byte-swizzled tile row `row`, 32 values starting at column c0 (multiple of 8)
-__device__ __forceinline__ void st_sw128(unsigned char* tile, int row, int c0,
-                                         const uint32_t (&x)[16]) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int chunk = ((c0 >> 3) + j) ^ (row & 7);
-        *reinterpret_cast<uint4*>(tile + row * 128 + chunk * 16) =
-            make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-    }
-}
-// 32 consecutive bf16 in global memory (64 bytes, 16-byte aligned)
-__device__ __forceinline__ void st_g32(__nv_bfloat16* dst, const uint32_t (&x)[16]) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        reinterpret_cast<uint4*>(dst)[j] = make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-}
-
 }  // namespace
 
 size_t chain_fwd_tc_smem_bytes() { return CHAIN_TC_SMEM; }
@@ -78,6 +55,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // A1 in, K in, MMA1 done, MMA2 done
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + 36);
+    // leave-the-loop decision per barrier of a step: thread 0 copies the abort flag into slot 0 / 1
+    // after its wait that precedes the barrier and every thread reads that slot after the barrier,
+    // so all warps leave together (a flag raised later is seen at the next barrier)
+    volatile int* stopf = reinterpret_cast<volatile int*>(sm + OFF_BAR + 40);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int qd = w & 3, cc = 32 * (w >> 2);
     const int row = 32 * qd + lane;  // accumulator row (key for S / D2, token for D1)
@@ -88,6 +69,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) tc::mbar_init(&bar[i], 1);
         *abort_flag = 0;
+        stopf[0] = stopf[1] = 0;
         tc::fence_mbar_init();
         if (c0 < c1) {
             tc::tma_prefetch_map(&tm.m128);
@@ -179,14 +161,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         const uint32_t ph = uint32_t(ci - c0) & 1u;
         const size_t chd = size_t(ci) * p.H + h;
         uint32_t sh[16], sl[16];
-        split32(Sr, sh, sl);
-        st_sw128(sm + OFF_S, row, cc, sh);
-        st_sw128(sm + OFF_S + 16384, row, cc, sl);
+        tc::split32(Sr, sh, sl);
+        tc::st_sw128(sm + OFF_S, row, cc, sh);
+        tc::st_sw128(sm + OFF_S + 16384, row, cc, sl);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (*abort_flag) break;
+        if (stopf[0]) break;
 
         // ---- MMA1: D1 = [W; Qg] S ----
         if (tid == 0) {
@@ -214,12 +196,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // while MMA1 runs: the saved start state, this chunk's U row and e^gL
         if (fwd && p.sS) {
             __nv_bfloat16* dst = p.sS + chd * 2 * D * D + size_t(row) * D + col0 + cc;
-            st_g32(dst, sh);
-            st_g32(dst + D * D, sl);
+            tc::st_g32(dst, sh);
+            tc::st_g32(dst + D * D, sl);
         }
         const float eg = egn;
         const int4 info = infon;
         if (!tc::mbar_wait(&bar[2], ph)) *abort_flag = 1;
+        if (tid == 0) stopf[1] = *abort_flag;  // decision at the next barrier
         tc::fence_after_sync();
         if (tid == 0 && ci + 1 < c1 && !*abort_flag) {
             load_A1(ci + 1);
@@ -234,15 +217,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::tmem_ld32(tD1 + cc, v);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = Un[j] - v[j];
-            split32(v, dhh, dll);
-            st_sw128(sm + OFF_DL, row, cc, dhh);
-            st_sw128(sm + OFF_DL + 8192, row, cc, dll);
+            tc::split32(v, dhh, dll);
+            tc::st_sw128(sm + OFF_DL, row, cc, dhh);
+            tc::st_sw128(sm + OFF_DL + 8192, row, cc, dll);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (*abort_flag) break;
+        if (stopf[1]) break;
 
         // ---- MMA2: D2 = Kb^T Delta;  MMA3: D1 += [*; Aqk] Delta ----
         if (tid == 0) {
@@ -280,11 +263,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // while MMA2 / MMA3 run: the saved write vectors and the next chunk's per-thread operands
         if (qd < 2 && fwd && p.sDelta) {
             __nv_bfloat16* dst = p.sDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
-            st_g32(dst, dhh);
-            st_g32(dst + CH * D, dll);
+            tc::st_g32(dst, dhh);
+            tc::st_g32(dst + CH * D, dll);
         }
         fetch_next(ci + 1);
         if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
+        if (tid == 0) stopf[0] = *abort_flag;  // decision at the next step's first barrier
         tc::fence_after_sync();
         if (tid == 0 && ci + 1 < c1 && !*abort_flag) {
             load_K(ci + 1);
@@ -385,6 +369,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + B_OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_OFF_BAR + 48);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 52);
+    volatile int* stopf = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 56);  // as in the forward
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int qd = w & 3, cc = 32 * (w >> 2);
     const int row = 32 * qd + lane;
@@ -395,6 +380,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
         *abort_flag = 0;
+        stopf[0] = stopf[1] = 0;
         tc::fence_mbar_init();
         if (c0 < c1) {
             tc::tma_prefetch_map(&tm.m128);
@@ -461,14 +447,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         const uint32_t ph = uint32_t(c1 - 1 - ci) & 1u;
         const size_t chd = size_t(ci) * p.H + h;
         uint32_t sh_[16], sl_[16];  // dS1 operand split (its saved planes are written below)
-        split32(dSr, sh_, sl_);
-        st_sw128(sm + B_OFF_DS, row, cc, sh_);
-        st_sw128(sm + B_OFF_DS + 16384, row, cc, sl_);
+        tc::split32(dSr, sh_, sl_);
+        tc::st_sw128(sm + B_OFF_DS, row, cc, sh_);
+        tc::st_sw128(sm + B_OFF_DS + 16384, row, cc, sl_);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (*abort_flag) break;
+        if (stopf[0]) break;
 
         // ---- MMA-A: DA = Kb dS1, DT = Aqk^T dO ----
         if (tid == 0) {
@@ -506,11 +492,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         __syncwarp();
         if (bwd) {  // while MMA-A runs: the saved gradient at the chunk end
             __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + size_t(row) * D + col0 + cc;
-            st_g32(dst, sh_);
-            st_g32(dst + D * D, sl_);
+            tc::st_g32(dst, sh_);
+            tc::st_g32(dst + D * D, sl_);
         }
         const float eg = egn;
         if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
+        if (tid == 0) stopf[1] = *abort_flag;  // decision at the next barrier
         tc::fence_after_sync();
         if (tid == 0 && ci > c0 && !*abort_flag) {
             load_KA(ci - 1);
@@ -526,15 +513,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::tmem_ld32(tDT + cc, t);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] = fmaf(p.scale, t[j], a[j]);
-            split32(a, xh, xl);
-            st_sw128(sm + B_OFF_DD, row, cc, xh);
-            st_sw128(sm + B_OFF_DD + 8192, row, cc, xl);
+            tc::split32(a, xh, xl);
+            tc::st_sw128(sm + B_OFF_DD, row, cc, xh);
+            tc::st_sw128(sm + B_OFF_DD + 8192, row, cc, xl);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        if (*abort_flag) break;
+        if (stopf[1]) break;
 
         // ---- MMA-D: DQ = Qg^T dO, DW = W^T dDelta ----
         if (tid == 0) {
@@ -573,11 +560,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // while MMA-D runs: the saved write-vector gradient and the next chunk's per-thread operands
         if (qd < 2 && bwd) {
             __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
-            st_g32(dst, xh);
-            st_g32(dst + CH * D, xl);
+            tc::st_g32(dst, xh);
+            tc::st_g32(dst + CH * D, xl);
         }
         fetch_next(ci - 1);
         if (!tc::mbar_wait(&bar[4], ph)) *abort_flag = 1;
+        if (tid == 0) stopf[0] = *abort_flag;  // decision at the next step's first barrier
         tc::fence_after_sync();
         if (tid == 0 && ci > c0 && !*abort_flag) {
             load_O(t0n);

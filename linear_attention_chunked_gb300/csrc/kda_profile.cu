@@ -16,8 +16,8 @@ struct Rec {
     cudaEvent_t a, b;
 };
 std::vector<Rec> g_recs;
-const char* const kNames[KK_COUNT] = {"k_plan",      "k_intra_fwd",    "k_chain_fwd_tc",
-                                      "k_chain_bwd_tc", "k_bwd_gemms_tc",    "k_bwd_intra",
+const char* const kNames[KK_COUNT] = {"k_plan",      "k_intra_fwd",    "k_chain_fwd",
+                                      "k_chain_bwd",    "k_bwd_gemms_tc",    "k_bwd_intra",
                                       "k_param_reduce", "k_walk"};
 }  // namespace
 

@@ -168,6 +168,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 }
 
+// Stores 32 consecutive FP32 columns of this warp's 32 lanes (thread i writes lane base + i) and
+// waits for the store to complete.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+        "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+        "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
 // ---- MMA ----
 // Instruction descriptor of kind::f16 with bf16 A and B, FP32 accumulation; a_mn / b_mn select
 // MN-major operand tiles (else K-major).
@@ -216,6 +231,30 @@ __device__ __forceinline__ void st_sw128_split32(unsigned char* hi_tile, unsigne
         *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
     }
 }
+
+// 32 values -> packed bf16 hi / lo pairs
+__device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&h)[16],
+                                        uint32_t (&l)[16]) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) split2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+}
+// 128-byte-swizzled tile row `row`, 32 values starting at column c0 (multiple of 8)
+__device__ __forceinline__ void st_sw128(unsigned char* tile, int row, int c0,
+                                         const uint32_t (&x)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int chunk = ((c0 >> 3) + j) ^ (row & 7);
+        *reinterpret_cast<uint4*>(tile + row * 128 + chunk * 16) =
+            make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    }
+}
+// 32 consecutive bf16 in global memory (64 bytes, 16-byte aligned)
+__device__ __forceinline__ void st_g32(__nv_bfloat16* dst, const uint32_t (&x)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        reinterpret_cast<uint4*>(dst)[j] = make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+}
+
 
 }  // namespace tc
 }  // namespace kda

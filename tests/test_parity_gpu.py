@@ -72,6 +72,46 @@ def test_full_workloads_sampled_heads(name, saved_mode):
     assert_within(errs, label=name)
 
 
+def _many_docs(seed):
+    # 48 short ragged documents x 4 heads: a pack with more recurrence blocks than SMs
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(1, 200, size=48)]
+    lens[:6] = [1, 63, 64, 65, 128, 0]
+    return inputs.make_inputs(lens, 4, seed=seed, gate="raw", l2norm=True, A_log_range=(LN8, LN32))
+
+
+@pytest.mark.parametrize("saved_mode", [True, False])
+def test_many_documents(saved_mode):
+    inp = _many_docs(11)
+    N, H = inp["cu_seqlens"].numel() - 1, inp["q"].shape[1]
+    rng = np.random.default_rng(12)
+    h0 = rng.standard_normal((N, H, 128, 128)).astype(np.float32) * 0.1
+    dht = rng.standard_normal((N, H, 128, 128)).astype(np.float32) * 0.1
+    gpu = gpu_fwd_bwd(inp, gate="raw", l2norm=True, h0=h0, dht=dht, saved_mode=saved_mode)
+    ref = oracle_fwd_bwd(inp, gate="raw", l2norm=True, h0=h0, dht=dht)
+    errs = compare(gpu, ref)
+    print("many documents", saved_mode, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert_within(errs, label="many documents")
+
+
+def test_many_documents_isolation_bitwise():
+    inp = _many_docs(13)
+    pack = gpu_fwd_bwd(inp, gate="raw", l2norm=True)
+    cu = inp["cu_seqlens"].tolist()
+    for n in range(len(cu) - 1):
+        a, b = cu[n], cu[n + 1]
+        if a == b:
+            continue
+        one = {k: (v[a:b] if k in ("q", "k", "v", "beta", "g", "dO") else v)
+               for k, v in inp.items()}
+        one["cu_seqlens"] = torch.tensor([0, b - a], dtype=torch.int32)
+        alone = gpu_fwd_bwd(one, gate="raw", l2norm=True)
+        for k in ("o", "dq", "dk", "dv", "dbeta", "dg"):
+            assert np.array_equal(alone[k], pack[k][a:b]), (n, k)
+        for k in ("ht", "dh0"):
+            assert np.array_equal(alone[k][0], pack[k][n]), (n, k)
+
+
 def test_bitwise_deterministic():
     inp, gate, l2n = _small("raw_empty_doc", seed=3)
     a = gpu_fwd_bwd(inp, gate=gate, l2norm=l2n)

@@ -13,7 +13,6 @@ const size_t SMEM_INTRA_FWD = intra_smem_bytes();
 const size_t SMEM_CHAIN_FWD_TC = chain_fwd_tc_smem_bytes();
 const size_t SMEM_CHAIN_BWD_TC = chain_bwd_tc_smem_bytes();
 const size_t SMEM_BWD_GEMMS_TC = bwd_gemm_tc_smem_bytes();
-const size_t SMEM_BWD_INTRA = bwd_intra_smem_bytes();
 constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
 
 std::mutex g_mu;
@@ -38,12 +37,13 @@ kda_status setup_device() {
     struct { const void* f; size_t smem; } attrs[] = {
         {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd_tc, SMEM_CHAIN_FWD_TC},
         {(const void*)k_chain_bwd_tc, SMEM_CHAIN_BWD_TC}, {(const void*)k_bwd_gemms_tc, SMEM_BWD_GEMMS_TC},
-        {(const void*)k_bwd_intra, SMEM_BWD_INTRA}, {(const void*)k_walk, SMEM_WALK},
+        {(const void*)k_walk, SMEM_WALK},
     };
     for (auto& a : attrs)
         if (cudaFuncSetAttribute(a.f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(a.smem)) !=
             cudaSuccess)
             return KDA_ERR_CUDA;
+    if (bwd_intra_setup() != cudaSuccess) return KDA_ERR_CUDA;
     g_ready[dev] = true;
     return KDA_OK;
 }
@@ -503,7 +503,7 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
             k_bwd_gemms_tc<<<grid, NTHR, SMEM_BWD_GEMMS_TC, st>>>(p, tm);
         }
         ProfScope ps(KK_BWD_INTRA, st);
-        k_bwd_intra<<<grid, BI_THREADS, SMEM_BWD_INTRA, st>>>(p, tm);
+        launch_bwd_intra(p, tm, grid, st);
     }
     if (p.gate_raw) {
         ProfScope ps(KK_PARAM_REDUCE, st);

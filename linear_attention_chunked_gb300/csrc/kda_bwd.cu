@@ -56,7 +56,6 @@ static_assert(BWD_INTRA_SMEM <= 232448, "backward intra shared memory above the 
 
 }  // namespace
 
-size_t bwd_intra_smem_bytes() { return BWD_INTRA_SMEM; }
 
 // Intra-chunk gradients of one (chunk, head): dq, dk, dv, dbeta, dg / da and the partials of
 // dA_log / ddt_bias.  The contractions through the exponent differences,
@@ -73,6 +72,9 @@ size_t bwd_intra_smem_bytes() { return BWD_INTRA_SMEM; }
 // completion on an mbarrier), so no other warp waits on the issue: once step 4 is done, dAqk and dM;
 // once step 6 is done, q, k and the first half of dQg, P, dKb, dR.  Akk, gam, v and beta of the next
 // item go to registers.  Every wait is bounded; after a timeout the block stops and reports.
+// L2N: the fused L2 norm of q and k is on (row scales rq, rk and their backward); off, the scales
+// are 1 and every multiply by them is compiled out.
+template <bool L2N>
 __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __grid_constant__ TcMaps tm) {
     constexpr int BT = BI_THREADS, NW = BT / 32;
     extern __shared__ __align__(16) unsigned char smraw[];
@@ -81,8 +83,10 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int items = *p.nchunks * p.H;
     if (int(blockIdx.x) >= items) return;
-    auto Qv = [&](int r, int c) { return __bfloat162float(S.qb[qk_at(r, c)]) * S.rq[r]; };
-    auto Kv = [&](int r, int c) { return __bfloat162float(S.kb[qk_at(r, c)]) * S.rk[r]; };
+    auto rqs = [&](int r) { return L2N ? S.rq[r] : 1.f; };  // row scales of q^ = q rq, k^ = k rk
+    auto rks = [&](int r) { return L2N ? S.rk[r] : 1.f; };
+    auto Qv = [&](int r, int c) { return __bfloat162float(S.qb[qk_at(r, c)]) * rqs(r); };
+    auto Kv = [&](int r, int c) { return __bfloat162float(S.kb[qk_at(r, c)]) * rks(r); };
 
     float4 pA[2], pgm[4];  // Akk and gam of the next item
     uint2 pv[2];           // v, first half, of the next item
@@ -206,23 +210,18 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         const float4 m = *m4;
         *m4 = make_float4(br * m.x, br * m.y, br * m.z, br * m.w);
     }
-    for (int r = w; r < CH; r += NW) {
-        float ra = 1.f, rb = 1.f;
-        if (p.l2n) {
-            float a = 0.f, b = 0.f;
-            for (int c = lane; c < D; c += 32) {
-                const float x = __bfloat162float(S.qb[qk_at(r, c)]), y = __bfloat162float(S.kb[qk_at(r, c)]);
-                a = fmaf(x, x, a);
-                b = fmaf(y, y, b);
-            }
-            a = warp_sum(a);
-            b = warp_sum(b);
-            ra = 1.f / sqrtf(a + p.eps);
-            rb = 1.f / sqrtf(b + p.eps);
+    for (int r = w; L2N && r < CH; r += NW) {  // per-row L2 scales (warp per row)
+        float a = 0.f, b = 0.f;
+        for (int c = lane; c < D; c += 32) {
+            const float x = __bfloat162float(S.qb[qk_at(r, c)]), y = __bfloat162float(S.kb[qk_at(r, c)]);
+            a = fmaf(x, x, a);
+            b = fmaf(y, y, b);
         }
+        a = warp_sum(a);
+        b = warp_sum(b);
         if (lane == 0) {
-            S.rq[r] = ra;
-            S.rk[r] = rb;
+            S.rq[r] = 1.f / sqrtf(a + p.eps);
+            S.rk[r] = 1.f / sqrtf(b + p.eps);
         }
     }
     __syncthreads();
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int i = tid + BT * (2 * half + k), r = i >> 5, c0 = (i & 31) * 4;
-            const float dgn = S.dA[a_at(r, r)], br = S.beta[r], rqr = S.rq[r], rkr = S.rk[r];
+            const float dgn = S.dA[a_at(r, r)], br = S.beta[r], rqr = rqs(r), rkr = rks(r);
             const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LDP + c0]);
             const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LDP + c0]);
             const uint2 qb2 = *reinterpret_cast<const uint2*>(&S.qb[qk_at(r, c0)]);
@@ -335,8 +334,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         const int cb = (w >> 3) * (CH * 64);
         const int kx0 = cb + (((w & 7) ^ (2 * t)) << 3) + g, kx1 = cb + (((w & 7) ^ (2 * t + 1)) << 3) + g;
         const int ex = cb + (((w & 7) ^ g) << 3) + 2 * t;
-        auto ldq = [&](int off, int r) { return __bfloat162float(S.qb[off + 64 * r]) * S.rq[r]; };
-        auto ldk = [&](int off, int r) { return __bfloat162float(S.kb[off + 64 * r]) * S.rk[r]; };
+        auto ldq = [&](int off, int r) { return __bfloat162float(S.qb[off + 64 * r]) * rqs(r); };
+        auto ldk = [&](int off, int r) { return __bfloat162float(S.kb[off + 64 * r]) * rks(r); };
         auto afrag = [&](int f, uint32_t (&hi)[4], uint32_t (&lo)[4]) {
             const uint4 h4 = S.Af[f][0][lane], l4 = S.Af[f][1][lane];
             hi[0] = h4.x; hi[1] = h4.y; hi[2] = h4.z; hi[3] = h4.w;
@@ -501,7 +500,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         const float4 dq4 = *reinterpret_cast<const float4*>(&S.dQ[r * LDP + c0]);
         const float4 dk4 = *reinterpret_cast<const float4*>(&S.dK[r * LDP + c0]);
         float dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w}, dk[4] = {dk4.x, dk4.y, dk4.z, dk4.w};
-        if (p.l2n) {
+        if (L2N) {
             float qv[4], kv[4], pq = 0.f, pk = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -514,8 +513,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             pk = warp_sum(pk);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                dq[j] = (dq[j] - qv[j] * pq) * S.rq[r];
-                dk[j] = (dk[j] - kv[j] * pk) * S.rk[r];
+                dq[j] = (dq[j] - qv[j] * pq) * rqs(r);
+                dk[j] = (dk[j] - kv[j] * pk) * rks(r);
             }
         }
         store_out4(p.dq, base + c0, make_float4(dq[0], dq[1], dq[2], dq[3]), p.out_fp32);
@@ -595,6 +594,21 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         tc::mbar_wait(&S.bar[1], ph ^ 1u, 100000000ull);
         p.status[0] = KDA_ERR_TIMEOUT;
     }
+}
+
+// Raises the dynamic shared-memory limit of both instantiations (once per device).
+cudaError_t bwd_intra_setup() {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_intra<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(BWD_INTRA_SMEM));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_bwd_intra<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(BWD_INTRA_SMEM));
+}
+void launch_bwd_intra(const Params& p, const TcMaps& tm, unsigned grid, cudaStream_t st) {
+    if (p.l2n)
+        k_bwd_intra<true><<<grid, BI_THREADS, BWD_INTRA_SMEM, st>>>(p, tm);
+    else
+        k_bwd_intra<false><<<grid, BI_THREADS, BWD_INTRA_SMEM, st>>>(p, tm);
 }
 
 // Fixed-order sums of the per-chunk partials: dA_log[h], ddt_bias[h, :].

@@ -322,7 +322,6 @@ size_t intra_smem_bytes();
 size_t chain_fwd_tc_smem_bytes();
 size_t chain_bwd_tc_smem_bytes();
 size_t bwd_gemm_tc_smem_bytes();
-size_t bwd_intra_smem_bytes();
 constexpr int CHAIN_THREADS = 256;  // 8 warps per state-recurrence block
 constexpr int BI_THREADS = 512;     // threads of the backward intra-chunk kernel
 constexpr int INTRA_THREADS = 512;  // threads of the forward intra-chunk kernel
@@ -332,7 +331,8 @@ __global__ void k_intra_fwd(Params p);
 __global__ void k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
 __global__ void k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
 __global__ void k_bwd_gemms_tc(Params p, const __grid_constant__ TcMaps tm);
-__global__ void k_bwd_intra(Params p, const __grid_constant__ TcMaps tm);
+cudaError_t bwd_intra_setup();  // shared-memory limits of the backward intra kernel
+void launch_bwd_intra(const Params& p, const TcMaps& tm, unsigned grid, cudaStream_t st);
 __global__ void k_param_reduce(Params p);
 __global__ void k_walk(int N, const int* doc_frag, int F, int H, const float* M, const float* B,
                        const float* S0, int reverse, float* S_in, float* S_final);

@@ -341,63 +341,95 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             hi[0] = h4.x; hi[1] = h4.y; hi[2] = h4.z; hi[3] = h4.w;
             lo[0] = l4.x; lo[1] = l4.y; lo[2] = l4.z; lo[3] = l4.w;
         };
-        // "as row": destination sub-chunk i = 1..3, reference row 16 i
-        int pair = 0;
-        for (int i = 1; i < 4; ++i) {
-            const int ref = 16 * i;
-            const float gr = S.gam[ref * LDP + c];
-            float aq[4] = {}, ak[4] = {};
-            for (int ks = 0; ks < i; ++ks, ++pair) {
-                uint32_t qh[4], ql[4], kh[4], kl[4], bh[2], bl[2];
-                afrag(2 * pair, qh, ql);
-                afrag(2 * pair + 1, kh, kl);
+        // "as row": destination sub-chunk i = 1..3, reference row 16 i.  The B operand of source
+        // sub-chunk ks is built once at reference row 16 (ks + 1); for a later destination i its
+        // reference moves to row 16 i by the per-channel factor exp(gam_16i - gam_16(ks+1)) <= 1
+        // (a column scaling of B, applied before the hi / lo split).  Pair (i, ks) = i (i-1) / 2 + ks.
+        {
+            float aq[3][4] = {}, ak[3][4] = {};
+#pragma unroll
+            for (int ks = 0; ks < 3; ++ks) {
+                const float g1 = S.gam[16 * (ks + 1) * LDP + c];
+                float xb[2][2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int s0 = 16 * ks + 2 * t + 8 * hf;
-                    const float x0 = ldk(kx0, s0) * __expf(gr - S.gam[s0 * LDP + c]);
-                    const float x1 = ldk(kx1, s0 + 1) * __expf(gr - S.gam[(s0 + 1) * LDP + c]);
-                    split2(x0, x1, bh[hf], bl[hf]);
+                    xb[hf][0] = ldk(kx0, s0) * __expf(g1 - S.gam[s0 * LDP + c]);
+                    xb[hf][1] = ldk(kx1, s0 + 1) * __expf(g1 - S.gam[(s0 + 1) * LDP + c]);
                 }
-                mma_x3(aq, qh, ql, bh[0], bh[1], bl[0], bl[1]);
-                mma_x3(ak, kh, kl, bh[0], bh[1], bl[0], bl[1]);
+#pragma unroll
+                for (int i = ks + 1; i < 4; ++i) {
+                    const int pair = i * (i - 1) / 2 + ks;
+                    const float R = i == ks + 1 ? 1.f : __expf(S.gam[16 * i * LDP + c] - g1);
+                    uint32_t qh[4], ql[4], kh[4], kl[4], bh[2], bl[2];
+                    afrag(2 * pair, qh, ql);
+                    afrag(2 * pair + 1, kh, kl);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) split2(xb[hf][0] * R, xb[hf][1] * R, bh[hf], bl[hf]);
+                    mma_x3(aq[i - 1], qh, ql, bh[0], bh[1], bl[0], bl[1]);
+                    mma_x3(ak[i - 1], kh, kl, bh[0], bh[1], bl[0], bl[1]);
+                }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 16 * i + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
-                const float sc = __expf(S.gam[r * LDP + cc] - S.gam[ref * LDP + cc]);
-                const float vq = aq[e] * sc, vk = ak[e] * sc;
-                S.dQ[r * LDP + cc] += vq;
-                S.dK[r * LDP + cc] += vk;
-                S.dG[r * LDP + cc] += ldq(ex + (e & 1), r) * vq + ldk(ex + (e & 1), r) * vk;
+            for (int i = 1; i < 4; ++i) {
+                const int ref = 16 * i;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 16 * i + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
+                    const float sc = __expf(S.gam[r * LDP + cc] - S.gam[ref * LDP + cc]);
+                    const float vq = aq[i - 1][e] * sc, vk = ak[i - 1][e] * sc;
+                    S.dQ[r * LDP + cc] += vq;
+                    S.dK[r * LDP + cc] += vk;
+                    S.dG[r * LDP + cc] += ldq(ex + (e & 1), r) * vq + ldk(ex + (e & 1), r) * vk;
+                }
             }
         }
-        // "as column": destination sub-chunk j = 0..2, reference row 16 j + 15
-        pair = 6;
-        for (int j = 0; j < 3; ++j) {
-            const int ref = 16 * j + 15;
-            const float gr = S.gam[ref * LDP + c];
-            float bacc[4] = {};
-            for (int ks = j + 1; ks < 4; ++ks, ++pair) {
-                uint32_t qh[4], ql[4], kh[4], kl[4], qbh[2], qbl[2], kbh[2], kbl[2];
-                afrag(2 * pair, qh, ql);
-                afrag(2 * pair + 1, kh, kl);
+        // "as column": destination sub-chunk j = 0..2, reference row 16 j + 15.  The B operands of
+        // source sub-chunk ks are built once at reference row 16 (ks - 1) + 15; for an earlier
+        // destination j the reference moves by the factor exp(gam_e(ks-1) - gam_e(j)) <= 1.
+        // Pair (j, ks) = 6 + base(j) + ks - j - 1 with base = 0, 3, 5.
+        {
+            float bacc[3][4] = {};
+#pragma unroll
+            for (int ks = 1; ks < 4; ++ks) {
+                const float g1 = S.gam[(16 * ks - 1) * LDP + c];
+                float xq[2][2], xk[2][2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int r0 = 16 * ks + 2 * t + 8 * hf;
-                    const float e0 = __expf(S.gam[r0 * LDP + c] - gr);
-                    const float e1 = __expf(S.gam[(r0 + 1) * LDP + c] - gr);
-                    split2(ldq(kx0, r0) * e0, ldq(kx1, r0 + 1) * e1, qbh[hf], qbl[hf]);
-                    split2(ldk(kx0, r0) * e0, ldk(kx1, r0 + 1) * e1, kbh[hf], kbl[hf]);
+                    const float e0 = __expf(S.gam[r0 * LDP + c] - g1);
+                    const float e1 = __expf(S.gam[(r0 + 1) * LDP + c] - g1);
+                    xq[hf][0] = ldq(kx0, r0) * e0;
+                    xq[hf][1] = ldq(kx1, r0 + 1) * e1;
+                    xk[hf][0] = ldk(kx0, r0) * e0;
+                    xk[hf][1] = ldk(kx1, r0 + 1) * e1;
                 }
-                mma_x3(bacc, qh, ql, qbh[0], qbh[1], qbl[0], qbl[1]);
-                mma_x3(bacc, kh, kl, kbh[0], kbh[1], kbl[0], kbl[1]);
+#pragma unroll
+                for (int j = 0; j < ks; ++j) {
+                    const int pair = 6 + (j == 0 ? 0 : j == 1 ? 3 : 5) + ks - j - 1;
+                    const float R = j == ks - 1 ? 1.f : __expf(g1 - S.gam[(16 * j + 15) * LDP + c]);
+                    uint32_t qh[4], ql[4], kh[4], kl[4], qbh[2], qbl[2], kbh[2], kbl[2];
+                    afrag(2 * pair, qh, ql);
+                    afrag(2 * pair + 1, kh, kl);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        split2(xq[hf][0] * R, xq[hf][1] * R, qbh[hf], qbl[hf]);
+                        split2(xk[hf][0] * R, xk[hf][1] * R, kbh[hf], kbl[hf]);
+                    }
+                    mma_x3(bacc[j], qh, ql, qbh[0], qbh[1], qbl[0], qbl[1]);
+                    mma_x3(bacc[j], kh, kl, kbh[0], kbh[1], kbl[0], kbl[1]);
+                }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int sr = 16 * j + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
-                const float vb = bacc[e] * __expf(S.gam[ref * LDP + cc] - S.gam[sr * LDP + cc]);
-                S.dK[sr * LDP + cc] += vb;
-                S.dG[sr * LDP + cc] -= ldk(ex + (e & 1), sr) * vb;
+            for (int j = 0; j < 3; ++j) {
+                const int ref = 16 * j + 15;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int sr = 16 * j + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
+                    const float vb = bacc[j][e] * __expf(S.gam[ref * LDP + cc] - S.gam[sr * LDP + cc]);
+                    S.dK[sr * LDP + cc] += vb;
+                    S.dG[sr * LDP + cc] -= ldk(ex + (e & 1), sr) * vb;
+                }
             }
         }
     }

@@ -21,14 +21,14 @@ struct IntraSmem {
     float q[CH * LDP], k[CH * LDP], gam[CH * LDP];
     float Akk[CH * LDA], Aqk[CH * LDA], Mi[CH * LDA];
     float beta[CH];
+    float T[3][16 * 17];  // blockwise inverse scratch (step 5)
     union {
         struct {
             __nv_bfloat16 Ks[3][2][16 * LB];  // B operands of the off-diagonal blocks (hi, lo)
-            float T[3][16 * 17];              // blockwise inverse scratch
             float P[6][16 * 32];              // partial off-diagonal sums of the K-split warps
         } a;
         struct {
-            __nv_bfloat16 bKg[2][CH * LB];  // beta K e^gam (hi, lo)
+            __nv_bfloat16 bKg[2][CH * LB];  // beta K e^gam (hi, lo), written during step 5
         } b;
     } u;
     __nv_bfloat16 v[CH * LB];  // V (exact in bf16)
@@ -385,7 +385,44 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
 
     // 5. Minv = (I + diag(beta) Akk)^-1, blockwise: 16x16 diagonal inverses by substitution, then
     //    X_ij = -D_i sum_{l=j}^{i-1} diag(beta_i) Akk_il X_lj by increasing block distance
-    if (tid < 64) {
+    if (tid >= 64) {
+        // meanwhile, the other warps form step 6's operand beta K e^gam (hi, lo) (Ks and the
+        // partial sums it overwrites were consumed in step 4)
+        for (int i = tid - 64; i < CH * D / 2; i += BT - 64) {
+            const int r = (2 * i) / D, c = (2 * i) % D;
+            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
+            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
+            const float x0 = S.beta[r] * kv.x * __expf(gv.x);
+            const float x1 = S.beta[r] * kv.y * __expf(gv.y);
+            uint32_t hi, lo;
+            split2(x0, x1, hi, lo);
+            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
+            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
+        }
+        // and the elementwise outputs of the recurrence: Qg = Q e^gam, Kb = K e^(gL - gam) (hi, lo)
+        // and gam
+        __nv_bfloat16* Qh = p.Qh + chd * CH * D;
+        __nv_bfloat16* Ql = p.Ql + chd * CH * D;
+        __nv_bfloat16* Kh = p.Kh + chd * CH * D;
+        __nv_bfloat16* Kl = p.Kl + chd * CH * D;
+        float* gam = p.gam + chd * CH * D;
+        for (int i = tid - 64; i < CH * D / 2; i += BT - 64) {
+            const int r = (2 * i) / D, c = (2 * i) % D;
+            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
+            const float2 gl = *reinterpret_cast<const float2*>(&S.gam[(CH - 1) * LDP + c]);
+            const float2 qv = *reinterpret_cast<const float2*>(&S.q[r * LDP + c]);
+            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
+            const float g0 = gv.x, g1 = gv.y;
+            uint32_t hi, lo;
+            split2(qv.x * __expf(g0), qv.y * __expf(g1), hi, lo);
+            reinterpret_cast<uint32_t*>(Qh)[i] = hi;
+            reinterpret_cast<uint32_t*>(Ql)[i] = lo;
+            split2(kv.x * __expf(gl.x - g0), kv.y * __expf(gl.y - g1), hi, lo);
+            reinterpret_cast<uint32_t*>(Kh)[i] = hi;
+            reinterpret_cast<uint32_t*>(Kl)[i] = lo;
+            reinterpret_cast<float2*>(gam)[i] = make_float2(g0, g1);
+        }
+    } else {
         const int b = tid >> 4, cl = tid & 15, c = 16 * b + cl;
         float x[16];
 #pragma unroll
@@ -412,7 +449,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
                 a0 = fmaf(S.Akk[r * LDA + 16 * jb + l], S.Mi[(16 * jb + l) * LDA + c], a0);
                 a1 = fmaf(S.Akk[r * LDA + 16 * jb + l + 1], S.Mi[(16 * jb + l + 1) * LDA + c], a1);
             }
-            S.u.a.T[b][rl * 17 + cl] = S.beta[r] * (a0 + a1);
+            S.T[b][rl * 17 + cl] = S.beta[r] * (a0 + a1);
         }
         __syncthreads();
         for (int idx = tid; idx < nb * 256; idx += BT) {
@@ -421,8 +458,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int sl = 0; sl < 16; sl += 2) {
-                a0 = fmaf(S.Mi[r * LDA + 16 * ib + sl], S.u.a.T[b][sl * 17 + cl], a0);
-                a1 = fmaf(S.Mi[r * LDA + 16 * ib + sl + 1], S.u.a.T[b][(sl + 1) * 17 + cl], a1);
+                a0 = fmaf(S.Mi[r * LDA + 16 * ib + sl], S.T[b][sl * 17 + cl], a0);
+                a1 = fmaf(S.Mi[r * LDA + 16 * ib + sl + 1], S.T[b][(sl + 1) * 17 + cl], a1);
             }
             S.Mi[r * LDA + c] = -(a0 + a1);
         }
@@ -431,20 +468,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
 
     cp_wait<0>();  // this item's v tile (copied during the previous item's last phase)
     if (more) fetch(item + gridDim.x, tab_next, 2);
+    __syncthreads();  // every thread's part of the v tile
 
     // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
-    for (int i = tid; i < CH * D / 2; i += BT) {
-        const int r = (2 * i) / D, c = (2 * i) % D;
-        const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
-        const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
-        const float x0 = S.beta[r] * kv.x * __expf(gv.x);
-        const float x1 = S.beta[r] * kv.y * __expf(gv.y);
-        uint32_t hi, lo;
-        split2(x0, x1, hi, lo);
-        *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
-        *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
-    }
-    __syncthreads();
     {
         const int mt = warp & 3, nq = warp >> 2;  // rows 16 mt.., columns 32 nq..
         float accW[4][4] = {}, accU[4][4] = {};
@@ -491,29 +517,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
 
     if (more) fetch(item + gridDim.x, tab_next, 4);
 
-    // 7. elementwise operands and the small matrices
+    // 7. the small matrices (the elementwise outputs were written during step 5)
     {
-        __nv_bfloat16* Qh = p.Qh + chd * CH * D;
-        __nv_bfloat16* Ql = p.Ql + chd * CH * D;
-        __nv_bfloat16* Kh = p.Kh + chd * CH * D;
-        __nv_bfloat16* Kl = p.Kl + chd * CH * D;
-        float* gam = p.gam + chd * CH * D;
-        for (int i = tid; i < CH * D / 2; i += BT) {
-            const int r = (2 * i) / D, c = (2 * i) % D;
-            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
-            const float2 gl = *reinterpret_cast<const float2*>(&S.gam[(CH - 1) * LDP + c]);
-            const float2 qv = *reinterpret_cast<const float2*>(&S.q[r * LDP + c]);
-            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
-            const float g0 = gv.x, g1 = gv.y;
-            uint32_t hi, lo;
-            split2(qv.x * __expf(g0), qv.y * __expf(g1), hi, lo);
-            reinterpret_cast<uint32_t*>(Qh)[i] = hi;
-            reinterpret_cast<uint32_t*>(Ql)[i] = lo;
-            split2(kv.x * __expf(gl.x - g0), kv.y * __expf(gl.y - g1), hi, lo);
-            reinterpret_cast<uint32_t*>(Kh)[i] = hi;
-            reinterpret_cast<uint32_t*>(Kl)[i] = lo;
-            reinterpret_cast<float2*>(gam)[i] = make_float2(g0, g1);
-        }
         __nv_bfloat16* Ah = p.Ah + chd * CH * CH;
         __nv_bfloat16* Al = p.Al + chd * CH * CH;
         __nv_bfloat16* Mh = p.Mh + chd * CH * CH;

@@ -70,8 +70,9 @@ static_assert(BWD_INTRA_SMEM <= 232448, "backward intra shared memory above the 
 // item are fetched while the current one is computed, in two parts that land in tiles the current
 // item no longer reads.  Shared-memory tiles are copied row by row by the TMA unit (issued by warp 0,
 // completion on an mbarrier), so no other warp waits on the issue: once step 4 is done, dAqk and dM;
-// once step 6 is done, q, k and the first half of dQg, P, dKb, dR.  Akk, gam, v and beta of the next
-// item go to registers.  Every wait is bounded; after a timeout the block stops and reports.
+// once step 6 is done, q, k and the first half of dQg, P, dKb, dR.  Akk, gam, v, beta and the second
+// half of dQg, P, dKb, dR of the next item go to registers (issued before the current item's output
+// stores, which would otherwise hold them up at the item boundary).  Every wait is bounded; after a timeout the block stops and reports.
 // L2N: the fused L2 norm of q and k is on (row scales rq, rk and their backward); off, the scales
 // are 1 and every multiply by them is compiled out.
 template <bool L2N>
@@ -89,6 +90,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     auto Kv = [&](int r, int c) { return __bfloat162float(S.kb[qk_at(r, c)]) * rks(r); };
 
     float4 pA[2], pgm[4];  // Akk and gam of the next item
+    float4 hq[2], hp[2], hb[2], hr[2];  // second half (rows 32..63) of its dQg, P, dKb, dR
+    uint2 hv[2];                        // and of its v
     uint2 pv[2];           // v, first half, of the next item
     float pb = 0.f;        // beta of the next item (threads < 64)
     int4 ntab = make_int4(0, 0, 0, 0);
@@ -110,6 +113,15 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
         for (int k = 0; k < 4; ++k) pgm[k] = reinterpret_cast<const float4*>(p.gam + nchd * CH * D)[tid + BT * k];
         ntab = p.chunk_tab[item / p.H];
+        // issued here, before the current item's output stores fill the memory queues
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const size_t i = nchd * CH * D / 4 + tid + BT * (2 + k);
+            hq[k] = reinterpret_cast<const float4*>(p.dQg)[i];
+            hp[k] = reinterpret_cast<const float4*>(p.P)[i];
+            hb[k] = reinterpret_cast<const float4*>(p.dKb)[i];
+            hr[k] = reinterpret_cast<const float4*>(p.dR)[i];
+        }
     };
     // part B: the item's 64 token rows of q and k (rows past the document end are cleared once
     // they land) and rows 0..31 of dQg, P, dKb, dR by TMA (thread 0); v and beta to registers
@@ -139,6 +151,12 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
                            : make_uint2(0u, 0u);
         }
         if (tid < CH) pb = tid < Ln ? bf2f(p.beta[size_t(T0 + tid) * p.H + hh]) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = (tid + BT * (2 + k)) >> 5, c0 = (tid & 31) * 4;
+            hv[k] = r < Ln ? *reinterpret_cast<const uint2*>(p.v + (size_t(T0 + r) * p.H + hh) * D + c0)
+                           : make_uint2(0u, 0u);
+        }
     };
     if (tid == 0) {
         tc::mbar_init(&S.bar[0], 1);
@@ -155,25 +173,9 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     const int t0 = nT0, L = nL, h = nh;  // this item (its fetch was the latest one)
     const size_t chd = size_t(item);
     const bool more = item + int(gridDim.x) < items;
-    const float* dQg = p.dQg + chd * CH * D;
-    const float* Pp = p.P + chd * CH * D;
-    const float* dKb = p.dKb + chd * CH * D;
-    const float* dR = p.dR + chd * CH * D;
 
-    // 1. inputs: the second half of the step-2 inputs from global memory; the prefetched tiles and
-    //    registers to shared memory; dAkk = beta_r dM; per-row L2 scales
-    float4 vq1[2], vp1[2], vb1[2], vr1[2];
-    uint2 vv1[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int i = tid + BT * (2 + k), r = i >> 5, c0 = (i & 31) * 4;
-        vq1[k] = reinterpret_cast<const float4*>(dQg)[i];
-        vp1[k] = reinterpret_cast<const float4*>(Pp)[i];
-        vb1[k] = reinterpret_cast<const float4*>(dKb)[i];
-        vr1[k] = reinterpret_cast<const float4*>(dR)[i];
-        vv1[k] = r < L ? *reinterpret_cast<const uint2*>(p.v + (size_t(t0 + r) * p.H + h) * D + c0)
-                       : make_uint2(0u, 0u);
-    }
+    // 1. inputs: the prefetched tiles and registers to shared memory; dAkk = beta_r dM; per-row
+    //    L2 scales
     if (!(tc::mbar_wait(&S.bar[0], ph) && tc::mbar_wait(&S.bar[1], ph))) S.abort = 1;
     ph ^= 1u;
 #pragma unroll
@@ -243,11 +245,11 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
                 vr[k] = *reinterpret_cast<const float4*>(&S.dK[32 * D + i]);
                 vv[k] = pv[k];
             } else {
-                vq[k] = vq1[k];
-                vp[k] = vp1[k];
-                vb[k] = vb1[k];
-                vr[k] = vr1[k];
-                vv[k] = vv1[k];
+                vq[k] = hq[k];
+                vp[k] = hp[k];
+                vb[k] = hb[k];
+                vr[k] = hr[k];
+                vv[k] = hv[k];
             }
         }
         if (half == 0) __syncthreads();  // every staged value is read before the tiles are written
@@ -499,6 +501,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         fetchA(item + gridDim.x);
     } else {  // defined on every path, so nothing fetched stays live across steps 2-4
         pA[0] = pA[1] = pgm[0] = pgm[1] = pgm[2] = pgm[3] = make_float4(0.f, 0.f, 0.f, 0.f);
+        hq[0] = hq[1] = hp[0] = hp[1] = hb[0] = hb[1] = hr[0] = hr[1] = pA[0];
         ntab = make_int4(0, 0, 0, 0);
     }
 
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     if (more) {
         fetchB(item + gridDim.x);
     } else {
-        pv[0] = pv[1] = make_uint2(0u, 0u);
+        pv[0] = pv[1] = hv[0] = hv[1] = make_uint2(0u, 0u);
         pb = 0.f;
         nT0 = nL = nh = 0;
     }

@@ -430,21 +430,46 @@ def main():
         h2d = sum(v.numel() * v.element_size() for v in host.values() if torch.is_tensor(v))
         d2h = sum(v.numel() * v.element_size() for v in res_host.values())
 
-        def e2e_step():
-            for k_, v_ in host.items():
-                if torch.is_tensor(v_):
-                    inp[k_].copy_(v_, non_blocking=True)
-            step(inp)
+        # double-buffered inputs, as an input pipeline runs: step i+1's host-to-device copies
+        # run on a copy stream while step i computes; every step's copies lie inside the timed
+        # region (the copy stream starts after its first event) and share HBM with the kernels
+        bufs = [inp, {k_: (v_.clone() if torch.is_tensor(v_) else v_) for k_, v_ in inp.items()}]
+        copy_stream = torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        freed = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def copy_in(b):
+            copy_stream.wait_event(freed[b])  # the step that last read buffer b is done
+            with torch.cuda.stream(copy_stream):
+                for k_, v_ in host.items():
+                    if torch.is_tensor(v_):
+                        bufs[b][k_].copy_(v_, non_blocking=True)
+                copied[b].record(copy_stream)
+
+        def run(i):
+            b = i % 2
+            stream.wait_event(copied[b])
+            step(bufs[b])
+            freed[b].record(stream)
             for k_, v_ in res_host.items():
                 v_.copy_(grads[k_] if k_ in grads else ht, non_blocking=True)
 
-        e2e_step()
+        def e2e_steps(n, start):
+            copy_stream.wait_event(start)
+            copy_in(0)
+            for i in range(n):
+                if i + 1 < n:
+                    copy_in((i + 1) % 2)
+                run(i)
+
+        s0 = torch.cuda.Event()
+        s0.record(stream)
+        e2e_steps(2, s0)  # warm-up
         torch.cuda.synchronize()
         barrier()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_steps(args.steps, a0)
         a1.record(stream)
         torch.cuda.synchronize()
         barrier()

@@ -192,6 +192,15 @@ kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int3
  * *device_status receives a kda_status value (KDA_OK when no device-side error happened). */
 kda_status kda_read_device_status(void* ws, int* device_status, kda_stream_t stream);
 
+/* Diagnostic (the pages have no counterpart): launches one kernel whose bounded device-side wait
+ * cannot complete (an mbarrier nothing arrives on).  After limit_us microseconds of GPU global
+ * time (1 .. 1,000,000) the wait gives up and the kernel writes KDA_ERR_TIMEOUT into the status
+ * word at the start of `ws` and returns, exactly as the library's kernels report a timed-out
+ * wait; the context stays usable.  ws: >= 256 bytes of 16-byte aligned device memory (any
+ * workspace), read with kda_read_device_status.  Returns KDA_ERR_INVALID_ARG for a null or
+ * misaligned ws or a limit out of range; does not synchronise `stream`. */
+kda_status kda_selftest_wait_timeout(void* ws, uint32_t limit_us, kda_stream_t stream);
+
 /* Instrumentation (no effect on results).  Every kernel launch is counted; while profiling is
  * enabled each launch is also bracketed by CUDA events recorded on its stream.
  * kda_profile_collect waits for the recorded events and returns, per kernel kind (index <

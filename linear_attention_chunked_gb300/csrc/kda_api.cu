@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 using namespace kda;
 
@@ -565,6 +566,29 @@ kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int3
         k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, F, H, M, B, S0, reverse,
                                                              S_in, S_final);
     }
+    return launched();
+}
+
+namespace kda {
+// Self-test of the bounded device-side waits: an mbarrier that nothing completes; the wait gives
+// up after limit_ns of global time and the kernel reports KDA_ERR_TIMEOUT in the status word, as
+// every kernel's timed-out wait does, and returns (no trap, the context stays usable).
+__global__ void k_selftest_wait(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0, limit_ns)) status[0] = KDA_ERR_TIMEOUT;
+}
+}  // namespace kda
+
+kda_status kda_selftest_wait_timeout(void* ws, uint32_t limit_us, kda_stream_t stream) {
+    if (!req(ws) || limit_us == 0 || limit_us > 1000000u) return KDA_ERR_INVALID_ARG;
+    if (kda_status s = setup_device()) return s;
+    k_selftest_wait<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<int*>(ws),
+                                                                        uint64_t(limit_us) * 1000u);
     return launched();
 }
 

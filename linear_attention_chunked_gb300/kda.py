@@ -70,6 +70,7 @@ def lib():
             L.kda_transfer_walk.argtypes = [ctypes.c_int32, V, ctypes.c_int32, ctypes.c_int32,
                                             V, V, V, I, V, V, V]
             L.kda_read_device_status.argtypes = [V, ctypes.POINTER(I), V]
+            L.kda_selftest_wait_timeout.argtypes = [V, ctypes.c_uint32, V]
             L.kda_profile_enable.argtypes = [I]
             L.kda_profile_collect.argtypes = [V, V]
             L.kda_kernel_count.argtypes = []
@@ -80,7 +81,8 @@ def lib():
             L.kda_status_string.argtypes = [I]
             L.kda_status_string.restype = ctypes.c_char_p
             for name in ("kda_workspace_size", "kda_fwd", "kda_fwd_static_ws", "kda_bwd", "kda_fragment_summary",
-                         "kda_transfer_walk", "kda_read_device_status", "kda_profile_enable",
+                         "kda_transfer_walk", "kda_read_device_status", "kda_selftest_wait_timeout",
+                         "kda_profile_enable",
                          "kda_profile_collect", "kda_kernel_count"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -280,6 +282,13 @@ def kda_read_device_status(ws) -> int:
         _check("kda_read_device_status",
                lib().kda_read_device_status(_ptr(ws), ctypes.byref(v), _stream(ws.device)))
     return v.value
+
+
+def kda_selftest_wait_timeout(ws, limit_us=20000):
+    """Runs a kernel whose bounded wait must time out; its KDA_ERR_TIMEOUT lands in ws's status."""
+    with torch.cuda.device(ws.device):
+        _check("kda_selftest_wait_timeout",
+               lib().kda_selftest_wait_timeout(_ptr(ws), ctypes.c_uint32(int(limit_us)), _stream(ws.device)))
 
 
 def kda_profile_enable(enable=True):

@@ -111,3 +111,14 @@ def test_output_dtype_must_match_the_declared_one():
     kda._check_dtypes({"o": torch.empty(2, dtype=torch.bfloat16)}, torch.bfloat16)
     with pytest.raises(ValueError, match="dq is torch.float32"):
         kda._check_dtypes({"dq": torch.empty(2, dtype=torch.float32)}, torch.bfloat16)
+
+
+def test_selftest_wait_timeout_validation(lib):
+    # argument checks come before any CUDA call (a null workspace, a limit out of range)
+    assert lib.kda_selftest_wait_timeout(None, ctypes.c_uint32(1000), None) == kda.KDA_ERR_INVALID_ARG
+    buf = (ctypes.c_char * 64)()
+    aligned = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    assert lib.kda_selftest_wait_timeout(ctypes.c_void_p(aligned), ctypes.c_uint32(0), None) == \
+        kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_selftest_wait_timeout(ctypes.c_void_p(aligned), ctypes.c_uint32(2000000), None) == \
+        kda.KDA_ERR_INVALID_ARG

@@ -148,6 +148,18 @@ def test_document_isolation_bitwise(case):
             assert np.array_equal(alone[k][0], pack[k][n]), (n, k)
 
 
+def test_bounded_wait_times_out_and_reports():
+    # a kernel whose mbarrier wait cannot complete gives up after 20 ms, reports KDA_ERR_TIMEOUT
+    # in the status word and returns; the context stays usable for the next call
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    kda.kda_selftest_wait_timeout(ws, limit_us=20000)
+    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_TIMEOUT
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK  # read clears it
+    inp, gate, l2n = _small("g_edges", seed=9)
+    assert_within(compare(gpu_fwd_bwd(inp, gate=gate, l2norm=l2n),
+                          oracle_fwd_bwd(inp, gate=gate, l2norm=l2n)), label="after timeout")
+
+
 def test_malformed_cu_seqlens_reports_device_status():
     inp, gate, l2n = _small("g_edges")
     d = to_dev(inp)

@@ -26,6 +26,7 @@ SMALL = {
     "raw_fast": dict(lens=[150, 99], H=2, gate="raw", l2norm=False, A_log_range=(LN8, LN32)),
     "g_l2n": dict(lens=[96, 33], H=3, gate="g", l2norm=True, gdiv=8.0),
     "raw_l2n_fast": dict(lens=[70, 129], H=2, gate="raw", l2norm=True, A_log_range=(LN8, LN32)),
+    "raw_one_head": dict(lens=[70, 64, 193], H=1, gate="raw", l2norm=False),
 }
 
 

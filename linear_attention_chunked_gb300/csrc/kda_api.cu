@@ -11,8 +11,6 @@ using namespace kda;
 namespace {
 
 const size_t SMEM_INTRA_FWD = intra_smem_bytes();
-const size_t SMEM_CHAIN_FWD_TC = chain_fwd_tc_smem_bytes();
-const size_t SMEM_CHAIN_BWD_TC = chain_bwd_tc_smem_bytes();
 const size_t SMEM_BWD_GEMMS_TC = bwd_gemm_tc_smem_bytes();
 constexpr size_t SMEM_WALK = (D * (SLICE + 1) + GEMM_SCRATCH) * 4;
 
@@ -36,15 +34,14 @@ kda_status setup_device() {
         g_sms[dev] < 1)
         return KDA_ERR_CUDA;
     struct { const void* f; size_t smem; } attrs[] = {
-        {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_chain_fwd_tc, SMEM_CHAIN_FWD_TC},
-        {(const void*)k_chain_bwd_tc, SMEM_CHAIN_BWD_TC}, {(const void*)k_bwd_gemms_tc, SMEM_BWD_GEMMS_TC},
+        {(const void*)k_intra_fwd, SMEM_INTRA_FWD}, {(const void*)k_bwd_gemms_tc, SMEM_BWD_GEMMS_TC},
         {(const void*)k_walk, SMEM_WALK},
     };
     for (auto& a : attrs)
         if (cudaFuncSetAttribute(a.f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(a.smem)) !=
             cudaSuccess)
             return KDA_ERR_CUDA;
-    if (bwd_intra_setup() != cudaSuccess) return KDA_ERR_CUDA;
+    if (bwd_intra_setup() != cudaSuccess || chain_tc_setup() != cudaSuccess) return KDA_ERR_CUDA;
     g_ready[dev] = true;
     return KDA_OK;
 }
@@ -312,14 +309,17 @@ kda_status make_bwd_intra_maps(const Params& p, const Layout& L, int64_t T, TcMa
 }
 
 // The state recurrences of the forward (o, ht, saved set) and of the backward: one block per
-// (document, head, value half), longest documents first.
+// (document, head, value part), longest documents first.
+int device_sms() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return g_sms[dev];
+}
 void launch_chain_fwd(const Params& p, const kda_problem* pr, const TcMaps& tm, cudaStream_t st) {
-    const unsigned pairs = unsigned(pr->N) * unsigned(pr->H);
-    k_chain_fwd_tc<<<pairs * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(p, CHAIN_FWD_OUT, tm);
+    launch_chain_fwd_tc(p, CHAIN_FWD_OUT, tm, unsigned(pr->N) * unsigned(pr->H), device_sms(), st);
 }
 void launch_chain_bwd(const Params& p, const kda_problem* pr, const TcMaps& tm, cudaStream_t st) {
-    const unsigned pairs = unsigned(pr->N) * unsigned(pr->H);
-    k_chain_bwd_tc<<<pairs * NHALF, CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(p, CHAIN_BWD, tm);
+    launch_chain_bwd_tc(p, CHAIN_BWD, tm, unsigned(pr->N) * unsigned(pr->H), device_sms(), st);
 }
 
 kda_status launched() {
@@ -541,12 +541,10 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     if (kda_status s = run_prologue(p, st)) return s;
     if (mode == KDA_FRAG_FWD) {
         ProfScope ps(KK_CHAIN_FWD, st);
-        k_chain_fwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * 2 * NHALF, CHAIN_THREADS, SMEM_CHAIN_FWD_TC, st>>>(
-            p, CHAIN_FRAG_MB, tm);
+        launch_chain_fwd_tc(p, CHAIN_FRAG_MB, tm, unsigned(pr->N) * unsigned(pr->H), device_sms(), st);
     } else {
         ProfScope ps(KK_CHAIN_BWD, st);
-        k_chain_bwd_tc<<<unsigned(pr->N) * unsigned(pr->H) * NHALF, CHAIN_THREADS, SMEM_CHAIN_BWD_TC, st>>>(
-            p, CHAIN_FRAG_C, tm);
+        launch_chain_bwd_tc(p, CHAIN_FRAG_C, tm, unsigned(pr->N) * unsigned(pr->H), device_sms(), st);
     }
     return launched();
 }

@@ -32,24 +32,27 @@ static_assert(CHAIN_TC_SMEM <= 232448, "tcgen05 chain shared memory above the op
 
 }  // namespace
 
-size_t chain_fwd_tc_smem_bytes() { return CHAIN_TC_SMEM; }
 
-// Grid N x H x 2 value halves for CHAIN_FWD_OUT; N x H x 4 parts for CHAIN_FRAG_MB (parts 0, 1:
-// X = I with zero values -> M; parts 2, 3: Y = 0 with the values -> B).
-// 256 threads: warp w reads TMEM lanes 32 (w % 4).. and value columns 32 (w / 4).. of the half.
+// Grid N x H x (128 / VW) value parts of VW = 64 or 32 columns for CHAIN_FWD_OUT; N x H x 4 parts
+// for CHAIN_FRAG_MB (VW = 64; parts 0, 1: X = I with zero values -> M; parts 2, 3: Y = 0 with the
+// values -> B).  256 threads: warp w reads TMEM lanes 32 (w % 4).. and VW / 2 value columns from
+// VW / 2 (w / 4) of its part.  The per-chunk latency scales with VW, so runs with few (document,
+// head) pairs use VW = 32 (more blocks on the critical path), the others VW = 64.
 // Thread 0 issues the TMA loads and the MMAs.  Operands of chunk c+1 are loaded as soon as the
 // MMA that reads their buffer has completed.
+template <int VW>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm) {
+    constexpr int VPT = VW / 2;  // value columns per thread
     // block = (document rank, head, value part): longest documents first, the parts of one
     // (document, head) adjacent so their shared operand tiles are read from L2 together
-    const int nparts = mode == CHAIN_FWD_OUT ? NHALF : 2 * NHALF;
+    const int nparts = mode == CHAIN_FWD_OUT ? D / VW : 2 * NHALF;
     const int hv = int(blockIdx.x % unsigned(nparts)), rest = int(blockIdx.x / unsigned(nparts));
     const int h = rest % p.H, n = p.doc_order[rest / p.H];
     const bool fwd = mode == CHAIN_FWD_OUT;
     const bool fragX = !fwd && hv < 2;
     const bool want_o = fwd && p.o != nullptr;
-    const int col0 = (hv & 1) * 64;
+    const int col0 = (hv % (D / VW)) * VW;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = tc::align1024(smraw);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // A1 in, K in, MMA1 done, MMA2 done
@@ -60,7 +63,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     // so all warps leave together (a flag raised later is seen at the next barrier)
     volatile int* stopf = reinterpret_cast<volatile int*>(sm + OFF_BAR + 40);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int qd = w & 3, cc = 32 * (w >> 2);
+    const int qd = w & 3, cc = VPT * (w >> 2);
     const int row = 32 * qd + lane;  // accumulator row (key for S / D2, token for D1)
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
@@ -80,9 +83,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     for (int i = tid; i < 8192 / 16; i += CHAIN_THREADS)
         reinterpret_cast<uint4*>(sm + OFF_PAD)[i] = make_uint4(0u, 0u, 0u, 0u);
 
-    float Sr[32];
+    float Sr[VPT];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < VPT; ++j) {
         const int val = col0 + cc + j;
         float v0 = 0.f;
         if (!fwd) v0 = (fragX && row == val) ? 1.f : 0.f;
@@ -95,8 +98,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const uint32_t taddr = *tslot;
     const uint32_t tD1 = taddr + (uint32_t(32 * qd) << 16), tD2 = tD1 + 64;
 
-    const uint32_t ID1 = tc::idesc_bf16(128, 64, false, true);  // K-major A, MN-major B
-    const uint32_t ID2 = tc::idesc_bf16(128, 64, true, true);   // MN-major A and B
+    const uint32_t ID1 = tc::idesc_bf16(128, VW, false, true);  // K-major A, MN-major B
+    const uint32_t ID2 = tc::idesc_bf16(128, VW, true, true);   // MN-major A and B
     const uint32_t sA1 = smem_u32(sm + OFF_A1), sS = smem_u32(sm + OFF_S);
     const uint32_t sKt = smem_u32(sm + OFF_KT), sPad = smem_u32(sm + OFF_PAD);
     const uint32_t sDl = smem_u32(sm + OFF_DL);
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     };
     // per-thread operands of the next chunk, fetched one chunk ahead: its U row (lanes 0..63),
     // e^gL of this thread's key, its chunk-table entry
-    float Un[32];
+    float Un[VPT];
     float egn = 0.f;
     int4 infon = make_int4(0, 0, 0, 0);
     auto fetch_next = [&](int ci) {
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (qd < 2 && !fragX) {
             const float4* src = reinterpret_cast<const float4*>(p.U + chd * CH * D + size_t(row) * D + col0 + cc);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < VPT / 4; ++j) {
                 const float4 u4 = src[j];
                 Un[4 * j] = u4.x;
                 Un[4 * j + 1] = u4.y;
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         infon = p.chunk_tab[ci];
     };
 #pragma unroll
-    for (int j = 0; j < 32; ++j) Un[j] = 0.f;
+    for (int j = 0; j < VPT; ++j) Un[j] = 0.f;
     fetch_next(c0);
 
     // phase parity of the loads in flight, -1 = none (thread 0's bookkeeping for an early exit)
@@ -160,10 +163,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     for (int ci = c0; ci < c1; ++ci) {
         const uint32_t ph = uint32_t(ci - c0) & 1u;
         const size_t chd = size_t(ci) * p.H + h;
-        uint32_t sh[16], sl[16];
-        tc::split32(Sr, sh, sl);
-        tc::st_sw128(sm + OFF_S, row, cc, sh);
-        tc::st_sw128(sm + OFF_S + 16384, row, cc, sl);
+        uint32_t sh[VPT / 2], sl[VPT / 2];
+        tc::split_n<VPT>(Sr, sh, sl);
+        tc::st_sw128_n<VPT>(sm + OFF_S, row, cc, sh);
+        tc::st_sw128_n<VPT>(sm + OFF_S + 16384, row, cc, sl);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
@@ -196,8 +199,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // while MMA1 runs: the saved start state, this chunk's U row and e^gL
         if (fwd && p.sS) {
             __nv_bfloat16* dst = p.sS + chd * 2 * D * D + size_t(row) * D + col0 + cc;
-            tc::st_g32(dst, sh);
-            tc::st_g32(dst + D * D, sl);
+            tc::st_g_n<VPT>(dst, sh);
+            tc::st_g_n<VPT>(dst + D * D, sl);
         }
         const float eg = egn;
         const int4 info = infon;
@@ -211,15 +214,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         __syncwarp();
 
         // ---- Delta = U - W S (lanes 0..63) ----
-        uint32_t dhh[16], dll[16];
+        uint32_t dhh[VPT / 2], dll[VPT / 2];
         if (qd < 2) {
-            float v[32];
-            tc::tmem_ld32(tD1 + cc, v);
+            float v[VPT];
+            tc::tmem_ld<VPT>(tD1 + cc, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = Un[j] - v[j];
-            tc::split32(v, dhh, dll);
-            tc::st_sw128(sm + OFF_DL, row, cc, dhh);
-            tc::st_sw128(sm + OFF_DL + 8192, row, cc, dll);
+            for (int j = 0; j < VPT; ++j) v[j] = Un[j] - v[j];
+            tc::split_n<VPT>(v, dhh, dll);
+            tc::st_sw128_n<VPT>(sm + OFF_DL, row, cc, dhh);
+            tc::st_sw128_n<VPT>(sm + OFF_DL + 8192, row, cc, dll);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -263,8 +266,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // while MMA2 / MMA3 run: the saved write vectors and the next chunk's per-thread operands
         if (qd < 2 && fwd && p.sDelta) {
             __nv_bfloat16* dst = p.sDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
-            tc::st_g32(dst, dhh);
-            tc::st_g32(dst + CH * D, dll);
+            tc::st_g_n<VPT>(dst, dhh);
+            tc::st_g_n<VPT>(dst + CH * D, dll);
         }
         fetch_next(ci + 1);
         if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
@@ -278,27 +281,27 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 
         // ---- S = e^gL * S + Kb^T Delta;  O rows (lanes 64..127) ----
         {
-            float v[32];
-            tc::tmem_ld32(tD2 + cc, v);
+            float v[VPT];
+            tc::tmem_ld<VPT>(tD2 + cc, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Sr[j] = fmaf(eg, Sr[j], v[j]);
+            for (int j = 0; j < VPT; ++j) Sr[j] = fmaf(eg, Sr[j], v[j]);
         }
         if (want_o && qd >= 2) {
-            float v[32];
-            tc::tmem_ld32(tD1 + cc, v);
+            float v[VPT];
+            tc::tmem_ld<VPT>(tD1 + cc, v);
             const int t = row - 64;
             if (t < info.z) {
                 const size_t off = (size_t(info.y + t) * p.H + h) * D + col0 + cc;
                 if (p.out_fp32) {
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + off);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < VPT / 4; ++j)
                         dst[j] = make_float4(p.scale * v[4 * j], p.scale * v[4 * j + 1],
                                              p.scale * v[4 * j + 2], p.scale * v[4 * j + 3]);
                 } else {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + off);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+                    for (int j = 0; j < VPT / 8; ++j)
                         dst[j] = make_uint4(pack2(p.scale * v[8 * j], p.scale * v[8 * j + 1]),
                                             pack2(p.scale * v[8 * j + 2], p.scale * v[8 * j + 3]),
                                             pack2(p.scale * v[8 * j + 4], p.scale * v[8 * j + 5]),
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (out) {
             float4* dst = reinterpret_cast<float4*>(out + dh + size_t(row) * D + col0 + cc);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < VPT / 4; ++j)
                 dst[j] = make_float4(Sr[4 * j], Sr[4 * j + 1], Sr[4 * j + 2], Sr[4 * j + 3]);
         }
     }
@@ -355,14 +358,15 @@ static_assert(CHAIN_BWD_TC_SMEM <= 232448, "tcgen05 chain shared memory above th
 
 }  // namespace
 
-size_t chain_bwd_tc_smem_bytes() { return CHAIN_BWD_TC_SMEM; }
 
+template <int VW>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm) {
-    const int hv = int(blockIdx.x % unsigned(NHALF)), rest = int(blockIdx.x / unsigned(NHALF));
+    constexpr int VPT = VW / 2, NP = D / VW;  // value columns per thread, value parts
+    const int hv = int(blockIdx.x % unsigned(NP)), rest = int(blockIdx.x / unsigned(NP));
     const int h = rest % p.H, n = p.doc_order[rest / p.H];
     const bool bwd = mode == CHAIN_BWD;
-    const int col0 = hv * 64;
+    const int col0 = hv * VW;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = tc::align1024(smraw);
     // barriers: 0 Kb+Aqk in, 1 dO in, 2 Qg+W in, 3 MMA-A done, 4 MMA-D done
@@ -371,7 +375,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 52);
     volatile int* stopf = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 56);  // as in the forward
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int qd = w & 3, cc = 32 * (w >> 2);
+    const int qd = w & 3, cc = VPT * (w >> 2);
     const int row = 32 * qd + lane;
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
@@ -390,9 +394,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     }
     if (w == 0) tc::tmem_alloc(tslot, 256);
 
-    float dSr[32];
+    float dSr[VPT];
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+    for (int j = 0; j < VPT; ++j)
         dSr[j] = (bwd && p.dht) ? p.dht[dh + size_t(row) * D + col0 + cc + j] : 0.f;
     tc::fence_before_sync();
     __syncthreads();
@@ -401,8 +405,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const uint32_t tl = taddr + (uint32_t(32 * qd) << 16);
     const uint32_t tDA = tl, tDT = tl + 64, tDQ = tl + 128, tDW = tl + 192;
 
-    const uint32_t IDA1 = tc::idesc_bf16(128, 64, false, true);  // Kb K-major, dS1 MN-major
-    const uint32_t IDMN = tc::idesc_bf16(128, 64, true, true);   // MN-major A and B
+    const uint32_t IDA1 = tc::idesc_bf16(128, VW, false, true);  // Kb K-major, dS1 MN-major
+    const uint32_t IDMN = tc::idesc_bf16(128, VW, true, true);   // MN-major A and B
     const uint32_t sKb = smem_u32(sm + B_OFF_KB), sQg = smem_u32(sm + B_OFF_QG);
     const uint32_t sW = smem_u32(sm + B_OFF_W), sAq = smem_u32(sm + B_OFF_AQ);
     const uint32_t sdO = smem_u32(sm + B_OFF_DO), sdS = smem_u32(sm + B_OFF_DS);
@@ -446,10 +450,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     for (int ci = c1 - 1; ci >= c0; --ci) {
         const uint32_t ph = uint32_t(c1 - 1 - ci) & 1u;
         const size_t chd = size_t(ci) * p.H + h;
-        uint32_t sh_[16], sl_[16];  // dS1 operand split (its saved planes are written below)
-        tc::split32(dSr, sh_, sl_);
-        tc::st_sw128(sm + B_OFF_DS, row, cc, sh_);
-        tc::st_sw128(sm + B_OFF_DS + 16384, row, cc, sl_);
+        uint32_t sh_[VPT / 2], sl_[VPT / 2];  // dS1 operand split (its saved planes are written below)
+        tc::split_n<VPT>(dSr, sh_, sl_);
+        tc::st_sw128_n<VPT>(sm + B_OFF_DS, row, cc, sh_);
+        tc::st_sw128_n<VPT>(sm + B_OFF_DS + 16384, row, cc, sl_);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
@@ -492,8 +496,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         __syncwarp();
         if (bwd) {  // while MMA-A runs: the saved gradient at the chunk end
             __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + size_t(row) * D + col0 + cc;
-            tc::st_g32(dst, sh_);
-            tc::st_g32(dst + D * D, sl_);
+            tc::st_g_n<VPT>(dst, sh_);
+            tc::st_g_n<VPT>(dst + D * D, sl_);
         }
         const float eg = egn;
         if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
@@ -506,16 +510,16 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         __syncwarp();
 
         // ---- dDelta = scale DT + DA (lanes 0..63) ----
-        uint32_t xh[16], xl[16];
+        uint32_t xh[VPT / 2], xl[VPT / 2];
         if (qd < 2) {
-            float a[32], t[32];
-            tc::tmem_ld32(tDA + cc, a);
-            tc::tmem_ld32(tDT + cc, t);
+            float a[VPT], t[VPT];
+            tc::tmem_ld<VPT>(tDA + cc, a);
+            tc::tmem_ld<VPT>(tDT + cc, t);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = fmaf(p.scale, t[j], a[j]);
-            tc::split32(a, xh, xl);
-            tc::st_sw128(sm + B_OFF_DD, row, cc, xh);
-            tc::st_sw128(sm + B_OFF_DD + 8192, row, cc, xl);
+            for (int j = 0; j < VPT; ++j) a[j] = fmaf(p.scale, t[j], a[j]);
+            tc::split_n<VPT>(a, xh, xl);
+            tc::st_sw128_n<VPT>(sm + B_OFF_DD, row, cc, xh);
+            tc::st_sw128_n<VPT>(sm + B_OFF_DD + 8192, row, cc, xl);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -560,8 +564,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // while MMA-D runs: the saved write-vector gradient and the next chunk's per-thread operands
         if (qd < 2 && bwd) {
             __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
-            tc::st_g32(dst, xh);
-            tc::st_g32(dst + CH * D, xl);
+            tc::st_g_n<VPT>(dst, xh);
+            tc::st_g_n<VPT>(dst + CH * D, xl);
         }
         fetch_next(ci - 1);
         if (!tc::mbar_wait(&bar[4], ph)) *abort_flag = 1;
@@ -576,11 +580,11 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 
         // ---- dS0 = e^gL * dS1 + scale DQ - DW ----
         {
-            float q[32], x[32];
-            tc::tmem_ld32(tDQ + cc, q);
-            tc::tmem_ld32(tDW + cc, x);
+            float q[VPT], x[VPT];
+            tc::tmem_ld<VPT>(tDQ + cc, q);
+            tc::tmem_ld<VPT>(tDW + cc, x);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dSr[j] = fmaf(eg, dSr[j], fmaf(p.scale, q[j], -x[j]));
+            for (int j = 0; j < VPT; ++j) dSr[j] = fmaf(eg, dSr[j], fmaf(p.scale, q[j], -x[j]));
         }
     }
 
@@ -596,13 +600,41 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (out) {
             float4* dst = reinterpret_cast<float4*>(out + dh + size_t(row) * D + col0 + cc);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < VPT / 4; ++j)
                 dst[j] = make_float4(dSr[4 * j], dSr[4 * j + 1], dSr[4 * j + 2], dSr[4 * j + 3]);
         }
     }
     tc::fence_before_sync();
     __syncthreads();
     if (w == 0) tc::tmem_dealloc(taddr, 256);
+}
+
+// Launchers (the kernels are templates on the value width): VW = 32 when four blocks per
+// (document, head) still fit on the SMs at once, else VW = 64; the fragment modes use VW = 64.
+cudaError_t chain_tc_setup() {
+    const void* fs[4] = {(const void*)k_chain_fwd_tc<64>, (const void*)k_chain_fwd_tc<32>,
+                         (const void*)k_chain_bwd_tc<64>, (const void*)k_chain_bwd_tc<32>};
+    for (int i = 0; i < 4; ++i) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            fs[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(i < 2 ? CHAIN_TC_SMEM : CHAIN_BWD_TC_SMEM));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+void launch_chain_fwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned pairs, int sms,
+                         cudaStream_t st) {
+    if (mode == CHAIN_FWD_OUT && long(pairs) * (D / 32) <= sms)
+        k_chain_fwd_tc<32><<<pairs * (D / 32), CHAIN_THREADS, CHAIN_TC_SMEM, st>>>(p, mode, tm);
+    else
+        k_chain_fwd_tc<64><<<pairs * (mode == CHAIN_FWD_OUT ? NHALF : 2 * NHALF), CHAIN_THREADS,
+                             CHAIN_TC_SMEM, st>>>(p, mode, tm);
+}
+void launch_chain_bwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned pairs, int sms,
+                         cudaStream_t st) {
+    if (long(pairs) * (D / 32) <= sms)
+        k_chain_bwd_tc<32><<<pairs * (D / 32), CHAIN_THREADS, CHAIN_BWD_TC_SMEM, st>>>(p, mode, tm);
+    else
+        k_chain_bwd_tc<64><<<pairs * NHALF, CHAIN_THREADS, CHAIN_BWD_TC_SMEM, st>>>(p, mode, tm);
 }
 
 }  // namespace kda

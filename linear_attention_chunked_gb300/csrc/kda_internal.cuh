@@ -319,8 +319,6 @@ struct TcMaps {
 
 // ---- kernels (defined in the .cu files) and their dynamic shared memory ----
 size_t intra_smem_bytes();
-size_t chain_fwd_tc_smem_bytes();
-size_t chain_bwd_tc_smem_bytes();
 size_t bwd_gemm_tc_smem_bytes();
 constexpr int CHAIN_THREADS = 256;  // 8 warps per state-recurrence block
 constexpr int BI_THREADS = 512;     // threads of the backward intra-chunk kernel
@@ -328,8 +326,12 @@ constexpr int INTRA_THREADS = 512;  // threads of the forward intra-chunk kernel
 constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences
 __global__ void k_plan(Params p);
 __global__ void k_intra_fwd(Params p);
-__global__ void k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
-__global__ void k_chain_bwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm);
+// state recurrences (value-width templates, launched through these; sms = the device's SMs)
+cudaError_t chain_tc_setup();
+void launch_chain_fwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned pairs, int sms,
+                         cudaStream_t st);
+void launch_chain_bwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned pairs, int sms,
+                         cudaStream_t st);
 __global__ void k_bwd_gemms_tc(Params p, const __grid_constant__ TcMaps tm);
 cudaError_t bwd_intra_setup();  // shared-memory limits of the backward intra kernel
 void launch_bwd_intra(const Params& p, const TcMaps& tm, unsigned grid, cudaStream_t st);

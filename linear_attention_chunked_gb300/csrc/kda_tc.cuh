@@ -232,6 +232,50 @@ __device__ __forceinline__ void st_sw128_split32(unsigned char* hi_tile, unsigne
     }
 }
 
+// N values (N a multiple of 8) -> packed bf16 hi / lo pairs
+template <int N>
+__device__ __forceinline__ void split_n(const float (&v)[N], uint32_t (&h)[N / 2], uint32_t (&l)[N / 2]) {
+#pragma unroll
+    for (int e = 0; e < N / 2; ++e) split2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+}
+// 128-byte-swizzled tile row `row`: N values (packed pairs) starting at column c0 (multiple of 8)
+template <int N>
+__device__ __forceinline__ void st_sw128_n(unsigned char* tile, int row, int c0,
+                                           const uint32_t (&x)[N / 2]) {
+#pragma unroll
+    for (int j = 0; j < N / 8; ++j) {
+        const int chunk = ((c0 >> 3) + j) ^ (row & 7);
+        *reinterpret_cast<uint4*>(tile + row * 128 + chunk * 16) =
+            make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    }
+}
+// N consecutive bf16 in global memory (16-byte aligned)
+template <int N>
+__device__ __forceinline__ void st_g_n(__nv_bfloat16* dst, const uint32_t (&x)[N / 2]) {
+#pragma unroll
+    for (int j = 0; j < N / 8; ++j)
+        reinterpret_cast<uint4*>(dst)[j] = make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+}
+// N = 32 or 16 consecutive FP32 TMEM columns of this warp's 32 lanes (as tmem_ld32)
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
+    tmem_ld32(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+          "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]),
+          "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // 32 values -> packed bf16 hi / lo pairs
 __device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&h)[16],
                                         uint32_t (&l)[16]) {

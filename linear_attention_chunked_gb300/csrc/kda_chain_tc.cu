@@ -33,11 +33,11 @@ static_assert(CHAIN_TC_SMEM <= 232448, "tcgen05 chain shared memory above the op
 }  // namespace
 
 
-// Grid N x H x (128 / VW) value parts of VW = 64 or 32 columns for CHAIN_FWD_OUT; N x H x 4 parts
+// Grid N x H x (128 / VW) value parts of VW = 64, 32 or 16 columns for CHAIN_FWD_OUT; N x H x 4 parts
 // for CHAIN_FRAG_MB (VW = 64; parts 0, 1: X = I with zero values -> M; parts 2, 3: Y = 0 with the
 // values -> B).  256 threads: warp w reads TMEM lanes 32 (w % 4).. and VW / 2 value columns from
 // VW / 2 (w / 4) of its part.  The per-chunk latency scales with VW, so runs with few (document,
-// head) pairs use VW = 32 (more blocks on the critical path), the others VW = 64.
+// head) pairs use VW = 16 or 32 (more blocks on the critical path), the others VW = 64.
 // Thread 0 issues the TMA loads and the MMAs.  Operands of chunk c+1 are loaded as soon as the
 // MMA that reads their buffer has completed.
 template <int VW>
@@ -609,21 +609,29 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     if (w == 0) tc::tmem_dealloc(taddr, 256);
 }
 
-// Launchers (the kernels are templates on the value width): VW = 32 when four blocks per
-// (document, head) still fit on the SMs at once, else VW = 64; the fragment modes use VW = 64.
+// Launchers (the kernels are templates on the value width): the narrowest of VW = 16, 32 whose
+// blocks (128 / VW per (document, head)) all fit on the SMs at once, else VW = 64; the fragment
+// modes use VW = 64.
 cudaError_t chain_tc_setup() {
-    const void* fs[4] = {(const void*)k_chain_fwd_tc<64>, (const void*)k_chain_fwd_tc<32>,
-                         (const void*)k_chain_bwd_tc<64>, (const void*)k_chain_bwd_tc<32>};
-    for (int i = 0; i < 4; ++i) {
+    const void* fs[6] = {(const void*)k_chain_fwd_tc<64>, (const void*)k_chain_fwd_tc<32>,
+                         (const void*)k_chain_fwd_tc<16>, (const void*)k_chain_bwd_tc<64>,
+                         (const void*)k_chain_bwd_tc<32>, (const void*)k_chain_bwd_tc<16>};
+    for (int i = 0; i < 6; ++i) {
         const cudaError_t e = cudaFuncSetAttribute(
-            fs[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(i < 2 ? CHAIN_TC_SMEM : CHAIN_BWD_TC_SMEM));
+            fs[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(i < 3 ? CHAIN_TC_SMEM : CHAIN_BWD_TC_SMEM));
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
+static int chain_width(unsigned pairs, int sms) {
+    return long(pairs) * (D / 16) <= sms ? 16 : long(pairs) * (D / 32) <= sms ? 32 : 64;
+}
 void launch_chain_fwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned pairs, int sms,
                          cudaStream_t st) {
-    if (mode == CHAIN_FWD_OUT && long(pairs) * (D / 32) <= sms)
+    const int vw = mode == CHAIN_FWD_OUT ? chain_width(pairs, sms) : 64;
+    if (vw == 16)
+        k_chain_fwd_tc<16><<<pairs * (D / 16), CHAIN_THREADS, CHAIN_TC_SMEM, st>>>(p, mode, tm);
+    else if (vw == 32)
         k_chain_fwd_tc<32><<<pairs * (D / 32), CHAIN_THREADS, CHAIN_TC_SMEM, st>>>(p, mode, tm);
     else
         k_chain_fwd_tc<64><<<pairs * (mode == CHAIN_FWD_OUT ? NHALF : 2 * NHALF), CHAIN_THREADS,
@@ -631,7 +639,10 @@ void launch_chain_fwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned p
 }
 void launch_chain_bwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned pairs, int sms,
                          cudaStream_t st) {
-    if (long(pairs) * (D / 32) <= sms)
+    const int vw = chain_width(pairs, sms);
+    if (vw == 16)
+        k_chain_bwd_tc<16><<<pairs * (D / 16), CHAIN_THREADS, CHAIN_BWD_TC_SMEM, st>>>(p, mode, tm);
+    else if (vw == 32)
         k_chain_bwd_tc<32><<<pairs * (D / 32), CHAIN_THREADS, CHAIN_BWD_TC_SMEM, st>>>(p, mode, tm);
     else
         k_chain_bwd_tc<64><<<pairs * NHALF, CHAIN_THREADS, CHAIN_BWD_TC_SMEM, st>>>(p, mode, tm);

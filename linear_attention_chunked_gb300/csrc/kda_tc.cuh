@@ -256,7 +256,7 @@ __device__ __forceinline__ void st_g_n(__nv_bfloat16* dst, const uint32_t (&x)[N
     for (int j = 0; j < N / 8; ++j)
         reinterpret_cast<uint4*>(dst)[j] = make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
 }
-// N = 32 or 16 consecutive FP32 TMEM columns of this warp's 32 lanes (as tmem_ld32)
+// N = 32, 16 or 8 consecutive FP32 TMEM columns of this warp's 32 lanes (as tmem_ld32)
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);
 template <>
@@ -272,6 +272,17 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16]) {
         : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
           "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]),
           "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&v)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+          "=f"(v[7])
         : "r"(taddr)
         : "memory");
 }

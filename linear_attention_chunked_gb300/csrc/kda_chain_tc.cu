@@ -336,10 +336,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 // ------------------------------------------------------------------------------------------------
 // Backward state recurrence (reverse over the chunks of a document), same machinery.  Per chunk,
 // with dS = dS1 (gradient at the chunk end) in registers:
-//   MMA-A  DA = Kb dS1 (M = 128: rows 64..127 unused), DT = Aqk^T dO (dO exact bf16: two terms)
-//          dDelta = scale DT + DA                           (lanes 0..63)
-//   MMA-D  DQ = Qg^T dO,  DW = W^T dDelta                   (M = 128 keys)
-//          dS0 = e^gL * dS1 + scale DQ - DW                 (every thread, its own key row)
+//   DA = Kb dS1 (M = 128: rows 64..127 unused),  DT = Aqk^T dO (dO exact bf16: two terms)
+//   dDelta = scale DT + DA                                  (lanes 0..63)
+//   DQ = Qg^T dO,  DW = W^T dDelta                          (M = 128 keys)
+//   dS0 = e^gL * dS1 + scale DQ - DW                        (every thread, its own key row)
+// Only DA and DW lie on the serial path from one gradient to the next.  DT and DQ do not depend
+// on it: DQ is issued right behind DA (it runs while dDelta is formed), DT of the next chunk right
+// behind DW (it runs while dS0 is formed), on a double-buffered Aqk / dO tile pair.
 // mode CHAIN_BWD: dS from dht; writes the dS1 and dDelta planes of every chunk and dh0.
 // mode CHAIN_FRAG_C: dS from zero; writes only the fragment-start gradient C (into p.fragB).
 namespace {
@@ -347,11 +350,13 @@ namespace {
 constexpr int B_OFF_KB = 0;        // Kb K-major [plane][2 key blocks][64 tokens][128 B]     32 KB
 constexpr int B_OFF_QG = 32768;    // Qg MN-major [plane][2 key blocks][64 tokens][128 B]    32 KB
 constexpr int B_OFF_W = 65536;     // W MN-major, same layout                                32 KB
-constexpr int B_OFF_AQ = 98304;    // Aqk as MN-major A of Aqk^T: [plane][64 t][128 B]       16 KB
-constexpr int B_OFF_DO = 114688;   // dO MN-major B: [64 tokens][128 B]                        8 KB
+constexpr int B_OFF_AQ0 = 98304;   // Aqk as MN-major A of Aqk^T: [plane][64 t][128 B]       16 KB
+constexpr int B_OFF_DO0 = 114688;  // dO MN-major B: [64 tokens][128 B]                        8 KB
 constexpr int B_OFF_DS = 122880;   // dS1 MN-major B: [plane][128 keys][128 B]               32 KB
 constexpr int B_OFF_DD = 155648;   // dDelta MN-major B: [plane][64 tokens][128 B]           16 KB
-constexpr int B_OFF_BAR = 172032;  // mbarriers, TMEM base address, abort flag
+constexpr int B_OFF_AQ1 = 172032;  // second Aqk buffer                                      16 KB
+constexpr int B_OFF_DO1 = 188416;  // second dO buffer                                        8 KB
+constexpr int B_OFF_BAR = 196608;  // mbarriers, TMEM base address, abort flag
 constexpr size_t CHAIN_BWD_TC_SMEM = B_OFF_BAR + 128 + 1024;
 
 static_assert(CHAIN_BWD_TC_SMEM <= 232448, "tcgen05 chain shared memory above the opt-in limit");
@@ -369,11 +374,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int col0 = hv * VW;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = tc::align1024(smraw);
-    // barriers: 0 Kb+Aqk in, 1 dO in, 2 Qg+W in, 3 MMA-A done, 4 MMA-D done
+    // barriers: 0 Kb in, 1 / 2 Aqk + dO in (buffer 0 / 1), 3 Qg in, 4 W in, 5 DA done, 6 DW done,
+    // 7 DQ done
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + B_OFF_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_OFF_BAR + 48);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 52);
-    volatile int* stopf = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 56);  // as in the forward
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_OFF_BAR + 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 68);
+    volatile int* stopf = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 72);  // as in the forward
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int qd = w & 3, cc = VPT * (w >> 2);
     const int row = 32 * qd + lane;
@@ -382,13 +388,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 
     if (tid == 0) {
 #pragma unroll
-        for (int i = 0; i < 5; ++i) tc::mbar_init(&bar[i], 1);
+        for (int i = 0; i < 8; ++i) tc::mbar_init(&bar[i], 1);
         *abort_flag = 0;
         stopf[0] = stopf[1] = 0;
         tc::fence_mbar_init();
         if (c0 < c1) {
-            tc::tma_prefetch_map(&tm.m128);
-            tc::tma_prefetch_map(&tm.m64);
+            tc::tma_prefetch_map(&tm.mKb);
+            tc::tma_prefetch_map(&tm.mAq);
             tc::tma_prefetch_map(&tm.mdO);
         }
     }
@@ -402,53 +408,84 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t taddr = *tslot;
+    // TMEM columns: DA 0..63, DT 64..127, DQ 128..191, DW 192..255
     const uint32_t tl = taddr + (uint32_t(32 * qd) << 16);
     const uint32_t tDA = tl, tDT = tl + 64, tDQ = tl + 128, tDW = tl + 192;
 
     const uint32_t IDA1 = tc::idesc_bf16(128, VW, false, true);  // Kb K-major, dS1 MN-major
     const uint32_t IDMN = tc::idesc_bf16(128, VW, true, true);   // MN-major A and B
     const uint32_t sKb = smem_u32(sm + B_OFF_KB), sQg = smem_u32(sm + B_OFF_QG);
-    const uint32_t sW = smem_u32(sm + B_OFF_W), sAq = smem_u32(sm + B_OFF_AQ);
-    const uint32_t sdO = smem_u32(sm + B_OFF_DO), sdS = smem_u32(sm + B_OFF_DS);
+    const uint32_t sW = smem_u32(sm + B_OFF_W), sdS = smem_u32(sm + B_OFF_DS);
     const uint32_t sdD = smem_u32(sm + B_OFF_DD);
+    auto aq_buf = [&](int b) { return b ? B_OFF_AQ1 : B_OFF_AQ0; };
+    auto do_buf = [&](int b) { return b ? B_OFF_DO1 : B_OFF_DO0; };
+    // the Aqk / dO buffer of chunk c is (c1 - 1 - c) & 1; its n-th load completes phase n & 1 of
+    // that buffer's barrier
+    const int tok0 = (tid == 0 && c0 < c1) ? p.chunk_tab[c0].y : 0;  // first token of the document
 
     // one TMA operation per operand image, both planes and both key blocks
-    auto load_KA = [&](int ci) {
-        const int chd = ci * p.H + h;
-        tc::mbar_expect_tx(&bar[0], 49152u);
-        tc::tma5(sm + B_OFF_KB, &tm.mKb, 0, 0, 0, 0, tm.zKh + chd, &bar[0]);
-        tc::tma4(sm + B_OFF_AQ, &tm.mAq, 0, 0, 0, tm.zAh + chd, &bar[0]);
+    auto load_Kb = [&](int ci) {
+        tc::mbar_expect_tx(&bar[0], 32768u);
+        tc::tma5(sm + B_OFF_KB, &tm.mKb, 0, 0, 0, 0, tm.zKh + ci * p.H + h, &bar[0]);
     };
-    auto load_O = [&](int t0) {
-        tc::mbar_expect_tx(&bar[1], 8192u);
-        tc::tma3(sm + B_OFF_DO, &tm.mdO, col0, h, t0, &bar[1]);
+    auto load_AO = [&](int ci) {
+        const int b = (c1 - 1 - ci) & 1;
+        tc::mbar_expect_tx(&bar[1 + b], 16384u + 8192u);
+        tc::tma4(sm + aq_buf(b), &tm.mAq, 0, 0, 0, tm.zAh + ci * p.H + h, &bar[1 + b]);
+        tc::tma3(sm + do_buf(b), &tm.mdO, col0, h, tok0 + CH * (ci - c0), &bar[1 + b]);
     };
-    auto load_QW = [&](int ci) {
-        const int chd = ci * p.H + h;
-        tc::mbar_expect_tx(&bar[2], 65536u);
-        tc::tma5(sm + B_OFF_QG, &tm.mKb, 0, 0, 0, 0, tm.zQh + chd, &bar[2]);
-        tc::tma5(sm + B_OFF_W, &tm.mKb, 0, 0, 0, 0, tm.zWh + chd, &bar[2]);
+    auto load_Qg = [&](int ci) {
+        tc::mbar_expect_tx(&bar[3], 32768u);
+        tc::tma5(sm + B_OFF_QG, &tm.mKb, 0, 0, 0, 0, tm.zQh + ci * p.H + h, &bar[3]);
     };
-    // next chunk's e^gL of this thread's key and first token, fetched one chunk ahead
+    auto load_W = [&](int ci) {
+        tc::mbar_expect_tx(&bar[4], 32768u);
+        tc::tma5(sm + B_OFF_W, &tm.mKb, 0, 0, 0, 0, tm.zWh + ci * p.H + h, &bar[4]);
+    };
+    // DT = Aqk^T dO of chunk ci into its TMEM columns (thread 0), once its Aqk / dO buffer landed
+    auto issue_DT = [&](int ci) -> bool {
+        const int k = c1 - 1 - ci, b = k & 1;
+        if (!tc::mbar_wait(&bar[1 + b], uint32_t(k >> 1) & 1u)) return false;
+        tc::fence_after_sync();
+        const uint32_t sAq = smem_u32(sm + aq_buf(b)), sdO = smem_u32(sm + do_buf(b));
+        const uint64_t ah = tc::sdesc(sAq, 8192, 1024), al = tc::sdesc(sAq + 8192, 8192, 1024);
+        const uint64_t bo = tc::sdesc(sdO, 1024, 1024);
+        uint32_t acc = 0;
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                tc::mma(taddr + 64, (t2 ? ah : al) + uint64_t((s * 2048) >> 4),
+                        bo + uint64_t((s * 2048) >> 4), IDMN, acc);
+                acc = 1;
+            }
+        return true;
+    };
+    // next chunk's e^gL of this thread's key, fetched one chunk ahead
     float egn = 0.f;
-    int t0n = 0;
     auto fetch_next = [&](int ci) {
-        if (ci >= c0) {
-            egn = p.eGL[(size_t(ci) * p.H + h) * D + row];
-            if (tid == 0) t0n = p.chunk_tab[ci].y;
-        }
+        if (ci >= c0) egn = p.eGL[(size_t(ci) * p.H + h) * D + row];
     };
     fetch_next(c1 - 1);
-    int pend[3] = {-1, -1, -1};  // phase parity of the loads in flight per barrier (thread 0)
+    // phase parity of the loads in flight per barrier 0..4 (thread 0), -1 = none
+    int pend[5] = {-1, -1, -1, -1, -1};
     if (tid == 0 && c0 < c1) {
-        load_KA(c1 - 1);
-        load_O(t0n);
-        load_QW(c1 - 1);
-        pend[0] = pend[1] = pend[2] = 0;
+        load_Kb(c1 - 1);
+        load_AO(c1 - 1);
+        load_Qg(c1 - 1);
+        load_W(c1 - 1);
+        pend[0] = pend[1] = pend[3] = pend[4] = 0;
+        if (c1 - 2 >= c0) {
+            load_AO(c1 - 2);
+            pend[2] = 0;
+        }
+        if (issue_DT(c1 - 1)) pend[1] = -1;
+        else *abort_flag = stopf[0] = 1;
     }
 
     for (int ci = c1 - 1; ci >= c0; --ci) {
-        const uint32_t ph = uint32_t(c1 - 1 - ci) & 1u;
+        const int k = c1 - 1 - ci;
+        const uint32_t ph = uint32_t(k) & 1u;
         const size_t chd = size_t(ci) * p.H + h;
         uint32_t sh_[VPT / 2], sl_[VPT / 2];  // dS1 operand split (its saved planes are written below)
         tc::split_n<VPT>(dSr, sh_, sl_);
@@ -460,10 +497,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         tc::fence_after_sync();
         if (stopf[0]) break;
 
-        // ---- MMA-A: DA = Kb dS1, DT = Aqk^T dO ----
+        // ---- DA = Kb dS1, then DQ = Qg^T dO ----
         if (tid == 0) {
-            if (tc::mbar_wait(&bar[0], ph) && tc::mbar_wait(&bar[1], ph)) {
-                pend[0] = pend[1] = -1;
+            if (tc::mbar_wait(&bar[0], ph)) {
+                pend[0] = -1;
                 tc::fence_after_sync();
                 const uint64_t kh = tc::sdesc(sKb, 16, 1024), kl = tc::sdesc(sKb + 16384, 16, 1024);
                 const uint64_t dh_ = tc::sdesc(sdS, 1024, 1024), dl_ = tc::sdesc(sdS + 16384, 1024, 1024);
@@ -477,34 +514,40 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                                 tb[t3] + uint64_t((s * 2048) >> 4), IDA1, acc);
                         acc = 1;
                     }
-                const uint64_t ah = tc::sdesc(sAq, 8192, 1024), al = tc::sdesc(sAq + 8192, 8192, 1024);
-                const uint64_t bo = tc::sdesc(sdO, 1024, 1024);
-                acc = 0;
+            } else {
+                *abort_flag = 1;
+            }
+            tc::mma_commit(&bar[5]);
+            if (tc::mbar_wait(&bar[3], ph)) {
+                pend[3] = -1;
+                tc::fence_after_sync();
+                const uint64_t qh = tc::sdesc(sQg, 8192, 1024), ql = tc::sdesc(sQg + 16384, 8192, 1024);
+                const uint64_t bo = tc::sdesc(smem_u32(sm + do_buf(int(ph))), 1024, 1024);
+                uint32_t acc = 0;
 #pragma unroll
                 for (int t2 = 0; t2 < 2; ++t2)
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        tc::mma(taddr + 64, (t2 ? ah : al) + uint64_t((s * 2048) >> 4),
+                        tc::mma(taddr + 128, (t2 ? qh : ql) + uint64_t((s * 2048) >> 4),
                                 bo + uint64_t((s * 2048) >> 4), IDMN, acc);
                         acc = 1;
                     }
             } else {
                 *abort_flag = 1;
             }
-            tc::mma_commit(&bar[3]);
+            tc::mma_commit(&bar[7]);
         }
         __syncwarp();
-        if (bwd) {  // while MMA-A runs: the saved gradient at the chunk end
+        if (bwd) {  // while DA runs: the saved gradient at the chunk end
             __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + size_t(row) * D + col0 + cc;
             tc::st_g_n<VPT>(dst, sh_);
             tc::st_g_n<VPT>(dst + D * D, sl_);
         }
         const float eg = egn;
-        if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
-        if (tid == 0) stopf[1] = *abort_flag;  // decision at the next barrier
+        if (!tc::mbar_wait(&bar[5], ph)) *abort_flag = 1;  // DA (and this chunk's DT) done
         tc::fence_after_sync();
         if (tid == 0 && ci > c0 && !*abort_flag) {
-            load_KA(ci - 1);
+            load_Kb(ci - 1);
             pend[0] = int(ph ^ 1u);
         }
         __syncwarp();
@@ -521,32 +564,30 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::st_sw128_n<VPT>(sm + B_OFF_DD, row, cc, xh);
             tc::st_sw128_n<VPT>(sm + B_OFF_DD + 8192, row, cc, xl);
         }
+        if (tid == 0) {
+            if (!tc::mbar_wait(&bar[7], ph)) *abort_flag = 1;  // DQ done: the Qg buffer is free
+            tc::fence_after_sync();
+            if (ci > c0 && !*abort_flag) {
+                load_Qg(ci - 1);
+                pend[3] = int(ph ^ 1u);
+            }
+            stopf[1] = *abort_flag;  // decision at the next barrier
+        }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
         if (stopf[1]) break;
 
-        // ---- MMA-D: DQ = Qg^T dO, DW = W^T dDelta ----
+        // ---- DW = W^T dDelta, then DT of the next chunk ----
         if (tid == 0) {
-            if (tc::mbar_wait(&bar[2], ph)) {
-                pend[2] = -1;
+            if (tc::mbar_wait(&bar[4], ph)) {
+                pend[4] = -1;
                 tc::fence_after_sync();
-                const uint64_t qh = tc::sdesc(sQg, 8192, 1024), ql = tc::sdesc(sQg + 16384, 8192, 1024);
-                const uint64_t bo = tc::sdesc(sdO, 1024, 1024);
-                uint32_t acc = 0;
-#pragma unroll
-                for (int t2 = 0; t2 < 2; ++t2)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        tc::mma(taddr + 128, (t2 ? qh : ql) + uint64_t((s * 2048) >> 4),
-                                bo + uint64_t((s * 2048) >> 4), IDMN, acc);
-                        acc = 1;
-                    }
                 const uint64_t wh = tc::sdesc(sW, 8192, 1024), wl = tc::sdesc(sW + 16384, 8192, 1024);
                 const uint64_t dxh = tc::sdesc(sdD, 1024, 1024), dxl = tc::sdesc(sdD + 8192, 1024, 1024);
                 const uint64_t ta[3] = {wh, wl, wh}, tb[3] = {dxl, dxh, dxh};
-                acc = 0;
+                uint32_t acc = 0;
 #pragma unroll
                 for (int t3 = 0; t3 < 3; ++t3)
 #pragma unroll
@@ -558,23 +599,35 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             } else {
                 *abort_flag = 1;
             }
-            tc::mma_commit(&bar[4]);
+            tc::mma_commit(&bar[6]);
+            if (ci > c0 && !*abort_flag) {
+                if (!issue_DT(ci - 1)) *abort_flag = 1;
+                else if (ph) pend[1] = -1;
+                else pend[2] = -1;
+            }
         }
         __syncwarp();
-        // while MMA-D runs: the saved write-vector gradient and the next chunk's per-thread operands
+        // while DW runs: the saved write-vector gradient and the next chunk's per-thread operands
         if (qd < 2 && bwd) {
             __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
             tc::st_g_n<VPT>(dst, xh);
             tc::st_g_n<VPT>(dst + CH * D, xl);
         }
         fetch_next(ci - 1);
-        if (!tc::mbar_wait(&bar[4], ph)) *abort_flag = 1;
+        if (!tc::mbar_wait(&bar[6], ph)) *abort_flag = 1;  // DW (and DQ) done
         if (tid == 0) stopf[0] = *abort_flag;  // decision at the next step's first barrier
         tc::fence_after_sync();
-        if (tid == 0 && ci > c0 && !*abort_flag) {
-            load_O(t0n);
-            load_QW(ci - 1);
-            pend[1] = pend[2] = int(ph ^ 1u);
+        if (tid == 0 && !*abort_flag) {
+            if (ci > c0) {
+                load_W(ci - 1);
+                pend[4] = int(ph ^ 1u);
+            }
+            if (ci - 2 >= c0) {  // into this chunk's Aqk / dO buffer, now read by nothing
+                load_AO(ci - 2);
+                const int par = int(uint32_t((k + 2) >> 1) & 1u);
+                if (ph) pend[2] = par;
+                else pend[1] = par;
+            }
         }
         __syncwarp();
 
@@ -591,7 +644,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     if (*abort_flag) {
         if (tid == 0) {
 #pragma unroll
-            for (int i = 0; i < 3; ++i)
+            for (int i = 0; i < 5; ++i)
                 if (pend[i] >= 0) tc::mbar_wait(&bar[i], uint32_t(pend[i]), 100000000ull);
             p.status[0] = KDA_ERR_TIMEOUT;
         }

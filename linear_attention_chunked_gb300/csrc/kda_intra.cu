@@ -387,20 +387,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     //    X_ij = -D_i sum_{l=j}^{i-1} diag(beta_i) Akk_il X_lj by increasing block distance
     if (tid >= 64) {
         // meanwhile, the other warps form step 6's operand beta K e^gam (hi, lo) (Ks and the
-        // partial sums it overwrites were consumed in step 4)
-        for (int i = tid - 64; i < CH * D / 2; i += BT - 64) {
-            const int r = (2 * i) / D, c = (2 * i) % D;
-            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
-            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
-            const float x0 = S.beta[r] * kv.x * __expf(gv.x);
-            const float x1 = S.beta[r] * kv.y * __expf(gv.y);
-            uint32_t hi, lo;
-            split2(x0, x1, hi, lo);
-            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
-            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
-        }
-        // and the elementwise outputs of the recurrence: Qg = Q e^gam, Kb = K e^(gL - gam) (hi, lo)
-        // and gam
+        // partial sums it overwrites were consumed in step 4) and the elementwise outputs of the
+        // recurrence: Qg = Q e^gam, Kb = K e^(gL - gam) (hi, lo) and gam
         __nv_bfloat16* Qh = p.Qh + chd * CH * D;
         __nv_bfloat16* Ql = p.Ql + chd * CH * D;
         __nv_bfloat16* Kh = p.Kh + chd * CH * D;
@@ -408,19 +396,22 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         float* gam = p.gam + chd * CH * D;
         for (int i = tid - 64; i < CH * D / 2; i += BT - 64) {
             const int r = (2 * i) / D, c = (2 * i) % D;
+            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
             const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
             const float2 gl = *reinterpret_cast<const float2*>(&S.gam[(CH - 1) * LDP + c]);
             const float2 qv = *reinterpret_cast<const float2*>(&S.q[r * LDP + c]);
-            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
-            const float g0 = gv.x, g1 = gv.y;
+            const float e0 = __expf(gv.x), e1 = __expf(gv.y);
             uint32_t hi, lo;
-            split2(qv.x * __expf(g0), qv.y * __expf(g1), hi, lo);
+            split2(S.beta[r] * kv.x * e0, S.beta[r] * kv.y * e1, hi, lo);
+            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
+            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
+            split2(qv.x * e0, qv.y * e1, hi, lo);
             reinterpret_cast<uint32_t*>(Qh)[i] = hi;
             reinterpret_cast<uint32_t*>(Ql)[i] = lo;
-            split2(kv.x * __expf(gl.x - g0), kv.y * __expf(gl.y - g1), hi, lo);
+            split2(kv.x * __expf(gl.x - gv.x), kv.y * __expf(gl.y - gv.y), hi, lo);
             reinterpret_cast<uint32_t*>(Kh)[i] = hi;
             reinterpret_cast<uint32_t*>(Kl)[i] = lo;
-            reinterpret_cast<float2*>(gam)[i] = make_float2(g0, g1);
+            reinterpret_cast<float2*>(gam)[i] = gv;
         }
     } else {
         const int b = tid >> 4, cl = tid & 15, c = 16 * b + cl;

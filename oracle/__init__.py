@@ -16,9 +16,12 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
   * fragment_summary   -- explicit matrix product of the per-token transitions at small d, and
                           S_out = M S_in + B against the token run; C against the token backward.
   * transfer_walk      -- associativity of the affine maps, and the walk against the unfragmented run.
+tests/test_oracle_mutants.py plants one plausible mistake at a time into a copy of kda_oracle.c
+(``compile_source`` + ``using_build``) and checks that every such build fails at least one pin.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -34,40 +37,65 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_source(src: str, out: str) -> str:
+    """gcc, plain -O2, no fast-math: the one way every build of the oracle is made."""
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-std=c11", "-Wall", "-Wno-unused-result",
+           "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile kda_oracle.c into a shared library (gcc, plain -O2, no fast-math)."""
+    """Compile kda_oracle.c into a shared library."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-std=c11", "-Wall", "-Wno-unused-result",
-           "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_source(_SRC, tmp)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def _bind(path):
+    """Loads a build of kda_oracle.c and declares its entry points."""
+    lib = ctypes.CDLL(path)
+    i64, i32, dbl, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p
+    lib.oracle_kda_fwd.argtypes = [i64, i32, i32, i32, p, p, p, p, p, p, p, p, p,
+                                   ctypes.c_int, ctypes.c_int, dbl, dbl, p, p, ctypes.c_int]
+    lib.oracle_kda_bwd.argtypes = [i64, i32, i32, i32, p, p, p, p, p, p, p, p, p,
+                                   ctypes.c_int, ctypes.c_int, dbl, dbl, p, p,
+                                   p, p, p, p, p, p, p, p, ctypes.c_int]
+    lib.oracle_fragment_summary.argtypes = [i64, i32, i32, i32, p, p, p, p, p, p, p, p,
+                                            ctypes.c_int, ctypes.c_int, dbl, dbl,
+                                            ctypes.c_int, p, p, p, ctypes.c_int]
+    lib.oracle_transfer_walk.argtypes = [i32, p, i32, i32, p, p, p, ctypes.c_int, p, p]
+    for f in (lib.oracle_kda_fwd, lib.oracle_kda_bwd, lib.oracle_fragment_summary,
+              lib.oracle_transfer_walk):
+        f.restype = ctypes.c_int
+    return lib
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            i64, i32, dbl, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p
-            lib.oracle_kda_fwd.argtypes = [i64, i32, i32, i32, p, p, p, p, p, p, p, p, p,
-                                           ctypes.c_int, ctypes.c_int, dbl, dbl, p, p, ctypes.c_int]
-            lib.oracle_kda_bwd.argtypes = [i64, i32, i32, i32, p, p, p, p, p, p, p, p, p,
-                                           ctypes.c_int, ctypes.c_int, dbl, dbl, p, p,
-                                           p, p, p, p, p, p, p, p, ctypes.c_int]
-            lib.oracle_fragment_summary.argtypes = [i64, i32, i32, i32, p, p, p, p, p, p, p, p,
-                                                    ctypes.c_int, ctypes.c_int, dbl, dbl,
-                                                    ctypes.c_int, p, p, p, ctypes.c_int]
-            lib.oracle_transfer_walk.argtypes = [i32, p, i32, i32, p, p, p, ctypes.c_int, p, p]
-            for f in (lib.oracle_kda_fwd, lib.oracle_kda_bwd, lib.oracle_fragment_summary,
-                      lib.oracle_transfer_walk):
-                f.restype = ctypes.c_int
-            _lib = lib
+            _lib = _bind(build())
     return _lib
+
+
+@contextlib.contextmanager
+def using_build(path):
+    """Runs the functions below on another build of kda_oracle.c (the planted-mistake tests)."""
+    global _lib
+    lib = _bind(path)
+    with _lock:
+        saved, _lib = _lib, lib
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
 
 
 def _nthreads(n):

@@ -65,14 +65,40 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
 
 
+def _code_only(text: str) -> str:
+    """C / C++ / CUDA source without its comments, trailing blanks and empty lines (string and
+    character literals are kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # literal: copy through the closing quote, honouring escapes
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_digest() -> str:
-    """Short digest of the CUDA sources and the ABI header (ties profiles to the code they measured)."""
+    """Short digest of the code of the CUDA sources and the ABI header, comments left out (ties
+    profiles to the code they measured; a comment-only edit keeps the digest)."""
     import hashlib
     h = hashlib.sha256()
     for path in sorted(_deps()):
         h.update(os.path.basename(path).encode())
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

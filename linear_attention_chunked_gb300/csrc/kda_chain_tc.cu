@@ -1,9 +1,9 @@
 // Inter-chunk state recurrence of the forward pass on tcgen05 tensor cores (TMEM accumulators,
-// TMA-fed operands).  Per (document, head, 64-column value half) and chunk, with the FP32 state S
-// held in registers (thread = one key row x 32 value columns):
-//   MMA1  D1 = [W; Qg] S                 M = 128 (64 W rows, 64 Qg rows), N = 64, K = 128 keys
+// TMA-fed operands).  Per (document, head, block of VW value columns) and chunk, with the FP32
+// state S held in registers (thread = one key row x VW / 2 value columns; VW = 16, 32 or 64):
+//   MMA1  D1 = [W; Qg] S                 M = 128 (64 W rows, 64 Qg rows), N = VW, K = 128 keys
 //         Delta = U - D1[0:64]           (threads of TMEM lanes 0..63)
-//   MMA2  D2 = Kb^T Delta                M = 128 keys, N = 64, K = 64 tokens
+//   MMA2  D2 = Kb^T Delta                M = 128 keys, N = VW, K = 64 tokens
 //   MMA3  D1 += [*; Aqk] Delta           rows 64..127: O = Qg S + Aqk Delta
 //         S  = e^gL * S + D2             (every thread, its own row)
 // Every product is split into bf16 hi/lo terms (a_hi b_lo + a_lo b_hi + a_hi b_hi, FP32 accumulate

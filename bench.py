@@ -152,12 +152,12 @@ def alg_bytes_per_token_head(kernel):
 
 
 def traffic_for(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it is for the current source."""
+    """DRAM bytes per launch from the committed ncu summary, if it is for the kernel's current code."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     from linear_attention_chunked_gb300 import build as b
-    sha = b.source_digest()
+    sha = b.source_digest(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#"):

@@ -90,12 +90,28 @@ def _code_only(text: str) -> str:
     return "\n".join(line for line in lines if line)
 
 
-def source_digest() -> str:
+# the translation unit of each profiled kernel (bench.py stage labels)
+KERNEL_SOURCES = {
+    "k_intra_fwd": "kda_intra.cu",
+    "k_chain_fwd": "kda_chain_tc.cu",
+    "k_chain_bwd": "kda_chain_tc.cu",
+    "k_bwd_gemms_tc": "kda_bwd_tc.cu",
+    "k_bwd_intra": "kda_bwd.cu",
+}
+
+
+def source_digest(kernel: str = None) -> str:
     """Short digest of the code of the CUDA sources and the ABI header, comments left out (ties
-    profiles to the code they measured; a comment-only edit keeps the digest)."""
+    profiles to the code they measured; a comment-only edit keeps the digest).  With a kernel
+    label: only that kernel's translation unit, the launch code (kda_api.cu), the shared headers
+    and the ABI header, so a change to another kernel keeps this one's measurements."""
     import hashlib
+    deps = _deps()
+    if kernel is not None:
+        own = {KERNEL_SOURCES[kernel], "kda_api.cu"}
+        deps = [d for d in deps if not d.endswith(".cu") or os.path.basename(d) in own]
     h = hashlib.sha256()
-    for path in sorted(_deps()):
+    for path in sorted(deps):
         h.update(os.path.basename(path).encode())
         with open(path, encoding="utf-8") as f:
             h.update(_code_only(f.read()).encode())

@@ -457,23 +457,40 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         __syncthreads();
     }
 
+    // split A fragments of Minv and Minv diag(beta), built once per lower 16 x 16 block (mt, ks)
+    // by warp mt (mt + 1) / 2 + ks (four warps of step 6 share each block), into the q tile,
+    // which nothing reads after step 5: [block][Minv hi, lo, Minv diag(beta) hi, lo][lane]
+    uint4* mfrag = reinterpret_cast<uint4*>(S.q);
+    if (warp < 10) {
+        const int mt = warp < 1 ? 0 : warp < 3 ? 1 : warp < 6 ? 2 : 3;
+        const int ks = warp - mt * (mt + 1) / 2;
+        uint32_t mh[4], ml[4], bh_[4], bl_[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int row = 16 * mt + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
+            const float m0 = S.Mi[row * LDA + col], m1 = S.Mi[row * LDA + col + 1];
+            split2(m0, m1, mh[rr], ml[rr]);
+            split2(m0 * S.beta[col], m1 * S.beta[col + 1], bh_[rr], bl_[rr]);
+        }
+        uint4* f = mfrag + warp * 4 * 32 + lane;
+        f[0] = make_uint4(mh[0], mh[1], mh[2], mh[3]);
+        f[32] = make_uint4(ml[0], ml[1], ml[2], ml[3]);
+        f[64] = make_uint4(bh_[0], bh_[1], bh_[2], bh_[3]);
+        f[96] = make_uint4(bl_[0], bl_[1], bl_[2], bl_[3]);
+    }
     cp_wait<0>();  // this item's v tile (copied during the previous item's last phase)
     if (more) fetch(item + gridDim.x, tab_next, 2);
-    __syncthreads();  // every thread's part of the v tile
+    __syncthreads();  // every thread's part of the v tile, the Minv fragments
 
     // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
     {
         const int mt = warp & 3, nq = warp >> 2;  // rows 16 mt.., columns 32 nq..
         float accW[4][4] = {}, accU[4][4] = {};
         for (int ks = 0; ks <= mt; ++ks) {  // Minv is lower triangular
-            uint32_t mh[4], ml[4], bh_[4], bl_[4];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const int row = 16 * mt + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
-                const float m0 = S.Mi[row * LDA + col], m1 = S.Mi[row * LDA + col + 1];
-                split2(m0, m1, mh[rr], ml[rr]);
-                split2(m0 * S.beta[col], m1 * S.beta[col + 1], bh_[rr], bl_[rr]);
-            }
+            const uint4* f = mfrag + (mt * (mt + 1) / 2 + ks) * 4 * 32 + lane;
+            const uint4 a0 = f[0], a1 = f[32], a2 = f[64], a3 = f[96];
+            const uint32_t mh[4] = {a0.x, a0.y, a0.z, a0.w}, ml[4] = {a1.x, a1.y, a1.z, a1.w};
+            const uint32_t bh_[4] = {a2.x, a2.y, a2.z, a2.w}, bl_[4] = {a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
             for (int np = 0; np < 2; ++np) {
                 uint32_t kh[4], kl[4], vv[4];

@@ -3,8 +3,9 @@
 Bounds (max|err| / rms(ref) per tensor): o 2e-2, final state 1e-3, dq/dk/dv/dbeta 3e-2,
 dg/dA_log/dt_bias 5e-2 (also on fast-decay inputs).  Small cases span several chunks, ragged
 tails (lengths 1, 63, 64, 65), an empty document, nonzero h0 / dht, both gate forms, the fused L2
-norm and fast decay; the full workloads run in the same launch configuration the bench times,
-with heads sampled where the oracle would take too long on every head.
+norm and fast decay, and packs that select each value-block width of the recurrences (16, 32
+and 64 columns); the full workloads run in the same launch configuration the bench times, with
+heads sampled where the oracle would take too long on every head.
 """
 import math
 
@@ -27,6 +28,10 @@ SMALL = {
     "g_l2n": dict(lens=[96, 33], H=3, gate="g", l2norm=True, gdiv=8.0),
     "raw_l2n_fast": dict(lens=[70, 129], H=2, gate="raw", l2norm=True, A_log_range=(LN8, LN32)),
     "raw_one_head": dict(lens=[70, 64, 193], H=1, gate="raw", l2norm=False),
+    # 30 (document, head) pairs: the recurrences run 32-column value blocks (16-column blocks
+    # would not all fit on the SMs at once); the other small cases run 16-column blocks and the
+    # many-document pack and the full workloads 64-column blocks
+    "raw_30_pairs": dict(lens=[70, 1, 64, 130, 33], H=6, gate="raw", l2norm=False),
 }
 
 
@@ -129,7 +134,7 @@ def test_saved_equals_replay_bitwise():
         assert np.array_equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("case", ["g_edges", "raw_empty_doc", "raw_l2n_fast"])
+@pytest.mark.parametrize("case", ["g_edges", "raw_empty_doc", "raw_l2n_fast", "raw_30_pairs"])
 def test_document_isolation_bitwise(case):
     inp, gate, l2n = _small(case, seed=5)
     pack = gpu_fwd_bwd(inp, gate=gate, l2norm=l2n)

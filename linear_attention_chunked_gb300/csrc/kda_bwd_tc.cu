@@ -1,5 +1,5 @@
 // Per-chunk gradient products of the backward on tcgen05 tensor cores (TMEM accumulators,
-// TMA-fed operands), one block per (chunk, head):
+// TMA-fed operands), per (chunk, head) item of a persistent block:
 //   MMA1  DR  = Minv^T dDelta                      M = 128 (rows 0..63), N = 128 values, K = 64
 //   MMA2  DPQ = [dR; dO] S0^T                      rows 0..63: P, rows 64..127: dQg / scale
 //   MMA3  DAM = [dR; dO] Delta^T                   rows 0..63: -dM, rows 64..127: dAqk / scale

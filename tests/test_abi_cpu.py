@@ -122,3 +122,14 @@ def test_selftest_wait_timeout_validation(lib):
         kda.KDA_ERR_INVALID_ARG
     assert lib.kda_selftest_wait_timeout(ctypes.c_void_p(aligned), ctypes.c_uint32(2000000), None) == \
         kda.KDA_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no fallback of any kind: without the built library every entry point raises
+    from linear_attention_chunked_gb300 import build, kda
+    monkeypatch.setattr(kda, "_lib", None)
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "libkda_gb300.so"))
+    with pytest.raises(RuntimeError, match="is missing"):
+        kda.lib()
+    with pytest.raises(RuntimeError, match="is missing"):
+        kda.kda_status_string(0)

@@ -153,7 +153,7 @@ def alg_bytes_per_token_head(kernel):
 
 def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it is for the kernel's current code."""
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    path = os.path.join(ROOT, "profiles", "traffic_4doc.txt")
     if not os.path.exists(path):
         return None
     from linear_attention_chunked_gb300 import build as b

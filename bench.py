@@ -138,9 +138,11 @@ class ClockSampler:
 # gate fp32; outputs o, dq, dk, dv, dbeta, dg fp32 (parity-grade outputs)
 
 
-def alg_bytes_per_token_head(kernel):
+def alg_bytes_per_token_head(kernel, out_bytes=4):
+    """Method inputs and outputs the kernel must touch, per token-head; out_bytes = bytes of one
+    o / dq / dk / dv / dbeta element (4: fp32 outputs, 2: bf16 outputs as SURVEY 8(d) counts)."""
     qkv, beta, gate, dO = 3 * 256, 2, 512, 256
-    o, dqkv, dbeta, dg = 512, 3 * 512, 4, 512
+    o, dqkv, dbeta, dg = 128 * out_bytes, 3 * 128 * out_bytes, out_bytes, 512
     table = {
         "k_intra_fwd": qkv + beta + gate,                    # reads the chunk inputs
         "k_chain_fwd": o,                                    # writes o
@@ -149,6 +151,16 @@ def alg_bytes_per_token_head(kernel):
         "k_bwd_intra": qkv + beta + gate + dqkv + dbeta + dg,  # reads inputs, writes grads
     }
     return table.get(kernel)
+
+
+def step_bytes_per_token_head(out_bytes):
+    """Algorithmic bytes of a whole fwd (and fwd+bwd) per token-head: q, k, v, beta, gate in,
+    o out; the backward reads them and dO again and writes dq, dk, dv, dbeta, dg.  out_bytes = 2
+    gives SURVEY 8(d)'s 1,538 / 4,358 B; 4 (the library's fp32 outputs) 1,794 / 5,384 B."""
+    inputs = 3 * 256 + 2 + 512
+    fwd = inputs + 128 * out_bytes
+    bwd = inputs + 256 + 3 * 128 * out_bytes + out_bytes + 512
+    return fwd, fwd + bwd
 
 
 def traffic_for(kernel, workload):
@@ -168,13 +180,14 @@ def traffic_for(kernel, workload):
 
 
 # ---------------------------------------------------------------------------------------------
-# per-configuration rows: fwd and fwd+bwd ms (median of 5 samples, each 5 back-to-back calls / 5)
+# per-configuration rows: fwd and fwd+bwd ms with the pages' protocol (median of 15 samples, each
+# 20 back-to-back calls / 20)
 
 ROWS = [("m2", "saved"), ("R2", "saved"), ("R2fast", "saved"), ("1doc", "saved"),
         ("4doc", "saved"), ("4doc", "replay"), ("longpack", "saved")]
 
 
-def _time_calls(fn, samples=5, calls=5):
+def _time_calls(fn, samples=15, calls=20):
     import torch
     fn()
     torch.cuda.synchronize()
@@ -191,8 +204,10 @@ def _time_calls(fn, samples=5, calls=5):
 
 
 # per token-head: method inputs and outputs (q, k, v, beta, gate, o; + dO, dq, dk, dv, dbeta, dg)
-# and FLOPs of the chunked method with 64-token chunks, head dim 128
-BYTES_FWD, BYTES_FWD_BWD = 1538, 4358
+# with bf16 outputs and with the fp32 outputs every bench run writes, and FLOPs of
+# the chunked method with 64-token chunks, head dim 128
+BYTES_FWD, BYTES_FWD_BWD = step_bytes_per_token_head(2)        # 1,538 / 4,358
+BYTES_FWD_F32, BYTES_FWD_BWD_F32 = step_bytes_per_token_head(4)  # 1,794 / 5,384
 FLOP_FWD, FLOP_FWD_BWD = 180224, 540672
 
 
@@ -259,6 +274,8 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
             "fwd_bwd_tokens_per_s": round(w.T / (fb_ms / 1e3)),
             "fwd_byte_frac": round(th * BYTES_FWD / (f_ms * 1e6) / hbm_gbs, 4),
             "fwd_bwd_byte_frac": round(th * BYTES_FWD_BWD / (fb_ms * 1e6) / hbm_gbs, 4),
+            "fwd_byte_frac_fp32_out": round(th * BYTES_FWD_F32 / (f_ms * 1e6) / hbm_gbs, 4),
+            "fwd_bwd_byte_frac_fp32_out": round(th * BYTES_FWD_BWD_F32 / (fb_ms * 1e6) / hbm_gbs, 4),
             "fwd_bwd_flop_frac": round(th * fb_flop / (fb_ms * 1e9) / bf16_tflops, 4)}
         del x, ws, saved
         torch.cuda.empty_cache()
@@ -268,8 +285,25 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
 # ---------------------------------------------------------------------------------------------
 
 
+def bench_config(w, world):
+    """The `config` object of both arms' JSON lines (same keys, same values)."""
+    return {"workload": f"{w.row}:saved", "T": w.T, "H": w.H, "docs": list(w.lens), "d": 128,
+            "chunk": 64, "gate": w.gate, "l2norm": bool(w.l2norm),
+            "outputs": "fp32 (o, dq, dk, dv, dbeta, dg / da, dA_log, dt_bias, states)",
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+
+
+def oracle_sample(w):
+    """Heads of the workload the FP64 oracle runs per sample: one head per host core, so the
+    N x heads (document, head) chains keep every core busy (the oracle schedules chains over
+    os.cpu_count() threads, longest documents first)."""
+    cores = os.cpu_count() or 1
+    heads = list(range(max(1, min(w.H, cores))))
+    return heads, cores
+
+
 def run_reference(args, rank, world):
-    """The reference arm: the FP64 oracle on the host cores, bounded sample per step."""
+    """The reference arm: the FP64 oracle on all host cores, a bounded sample per step."""
     if rank != 0:
         return
     import numpy as np  # noqa: F401
@@ -281,8 +315,7 @@ def run_reference(args, rank, world):
     w = inputs.WORKLOADS[args.workload]
     inp = inputs.workload_inputs(args.workload)
     oracle.build()
-    heads = [0]
-    cores = min(os.cpu_count() or 1, w.N * len(heads))
+    heads, cores = oracle_sample(w)
     for _ in range(args.warmup):
         oracle_fwd_bwd(inp, gate=w.gate, l2norm=w.l2norm, heads=heads)
     t0 = time.perf_counter()
@@ -296,9 +329,11 @@ def run_reference(args, rank, world):
         "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": full_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.row}:saved", "T": w.T, "H": w.H, "docs": list(w.lens)},
+        "config": bench_config(w, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"head {heads} of {w.H} per step, fwd+bwd token by token, "
+                         "sample": f"heads 0..{len(heads) - 1} of {w.H} per step "
+                                   f"({w.N * len(heads)} (document, head) chains on {cores} "
+                                   f"threads), fwd+bwd token by token, {dt:.2f} s per sample, "
                                    f"scaled by {w.H}/{len(heads)}"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -311,14 +346,14 @@ def cpu_baseline(w, inp):
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from harness import oracle_fwd_bwd
     oracle.build()
-    heads = list(range(4))
-    cores = min(os.cpu_count() or 1, w.N * len(heads))
+    heads, cores = oracle_sample(w)
     t0 = time.perf_counter()
     oracle_fwd_bwd(inp, gate=w.gate, l2norm=w.l2norm, heads=heads)
     dt = time.perf_counter() - t0
     value = w.T * len(heads) / w.H / dt
     return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"heads {heads} of {w.H} (fwd+bwd, FP64 token by token), {dt:.1f} s, "
+            "sample": f"heads 0..{len(heads) - 1} of {w.H} ({w.N * len(heads)} (document, head) "
+                      f"chains on {cores} threads; fwd+bwd, FP64 token by token), {dt:.1f} s, "
                       f"scaled to {w.H} heads"}
 
 
@@ -350,117 +385,161 @@ def main():
     # fp32 outputs (the library's parity-grade default: rounding o / dq to bf16 alone exceeds the
     # error bounds on the heavy-tailed raw-gate workloads)
     f32 = torch.float32
-    o = torch.empty((T, H, 128), dtype=f32, device=dev)
-    ht = torch.empty((N, H, 128, 128), dtype=f32, device=dev)
-    grads = dict(dq=torch.empty((T, H, 128), dtype=f32, device=dev),
-                 dk=torch.empty((T, H, 128), dtype=f32, device=dev),
-                 dv=torch.empty((T, H, 128), dtype=f32, device=dev),
-                 dbeta=torch.empty((T, H), dtype=f32, device=dev),
-                 dg=torch.empty((T, H, 128), dtype=f32, device=dev))
-    if w.gate == "raw":
-        grads["dA_log"] = torch.empty((H,), dtype=f32, device=dev)
-        grads["ddt_bias"] = torch.empty((H, 128), dtype=f32, device=dev)
+
+    def make_outputs():
+        out = dict(o=torch.empty((T, H, 128), dtype=f32, device=dev),
+                   ht=torch.empty((N, H, 128, 128), dtype=f32, device=dev),
+                   dq=torch.empty((T, H, 128), dtype=f32, device=dev),
+                   dk=torch.empty((T, H, 128), dtype=f32, device=dev),
+                   dv=torch.empty((T, H, 128), dtype=f32, device=dev),
+                   dbeta=torch.empty((T, H), dtype=f32, device=dev),
+                   dg=torch.empty((T, H, 128), dtype=f32, device=dev))
+        if w.gate == "raw":
+            out["dA_log"] = torch.empty((H,), dtype=f32, device=dev)
+            out["ddt_bias"] = torch.empty((H, 128), dtype=f32, device=dev)
+        return out
+
+    outs = make_outputs()
+    grad_keys = [k for k in outs if k not in ("o", "ht")]
     kw = dict(gate=w.gate, l2norm=w.l2norm)
 
-    def step(x):
+    def step(x, out):
         a = (x["q"], x["k"], x["v"], x["beta"], x["g"], x["cu_seqlens"])
-        kda.kda_fwd(*a, A_log=x["A_log"], dt_bias=x["dt_bias"], o=o, ht=ht, saved=saved, ws=ws,
-                    **kw)
+        kda.kda_fwd(*a, A_log=x["A_log"], dt_bias=x["dt_bias"], o=out["o"], ht=out["ht"],
+                    saved=saved, ws=ws, **kw)
         kda.kda_bwd(*a, x["dO"], saved=saved, A_log=x["A_log"], dt_bias=x["dt_bias"],
-                    want_dh0=False, out=grads, ws=ws, **kw)
+                    want_dh0=False, out={k: out[k] for k in grad_keys}, ws=ws, **kw)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
     for _ in range(max(args.warmup, 3)):
-        step(inp)
+        step(inp, outs)
     torch.cuda.synchronize()
 
-    # ---- timed region ----
+    # ---- timed region: exactly K steps; an event every 20 steps gives the pages' samples ----
     stream = torch.cuda.current_stream(dev)
     clocks = ClockSampler(local)
     clocks.start()
     launches0 = kda.kda_launch_counter()
     barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step(inp)
-    e1.record(stream)
+    evs = [torch.cuda.Event(enable_timing=True)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        step(inp, outs)
+        if (i + 1) % 20 == 0 or i + 1 == args.steps:
+            evs.append(torch.cuda.Event(enable_timing=True))
+            evs[-1].record(stream)
     torch.cuda.synchronize()
     barrier()
     ck = clocks.stop()
     launches = kda.kda_launch_counter() - launches0
-    ms = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dev)
+    ms = reduce_max_ms(evs[0].elapsed_time(evs[-1]) / args.steps, world, dev)
     value = job_throughput(T, world, ms)
+
+    # ---- the pages' protocol: median of 15 samples, each 20 back-to-back steps / 20 ----
+    proto_ms = _time_calls(lambda: step(inp, outs), samples=15, calls=20)
+    proto_ms = reduce_max_ms(proto_ms, world, dev)
+    protocol = {"samples": 15, "calls_per_sample": 20, "median_ms_per_step": proto_ms,
+                "value": job_throughput(T, world, proto_ms), "unit": "tokens/s"}
+
+    hbm, bf16, src = load_peaks()
+    step_roof = {
+        "bound": "hbm", "peak": hbm, "unit": "GB/s", "peak_source": src,
+        "survey_bytes_per_token_head": BYTES_FWD_BWD,
+        "frac": T * H * BYTES_FWD_BWD / (ms * 1e6) / hbm,
+        "fp32_out_bytes_per_token_head": BYTES_FWD_BWD_F32,
+        "frac_fp32_out": T * H * BYTES_FWD_BWD_F32 / (ms * 1e6) / hbm,
+        "flop_per_token_head": FLOP_FWD_BWD,
+        "flop_frac": T * H * FLOP_FWD_BWD / (ms * 1e9) / bf16,
+    }
 
     # ---- per-kernel device time (second pass, CUDA events around every launch) ----
     kernels, roof = {}, None
-    hbm, bf16, src = load_peaks()
     if not args.no_profile:
         kda.kda_profile_enable(True)
         for _ in range(args.steps):
-            step(inp)
+            step(inp, outs)
         torch.cuda.synchronize()
         kda.kda_profile_enable(False)
         prof = kda.kda_profile_collect()
         kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                    for k, v in prof.items() if v[1]}
         dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
-        per_th = alg_bytes_per_token_head(dom)
+        per_th = alg_bytes_per_token_head(dom, out_bytes=4)
         if per_th is not None:
             launch_ms = kernels[dom]["ms_per_step"] / kernels[dom]["launches_per_step"]
             byts = per_th * T * H
             achieved = byts / (launch_ms / 1e3) / 1e9
-            roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
+            byts2 = alg_bytes_per_token_head(dom, out_bytes=2) * T * H
+            roof = {"kernel": dom, "scope": "dominant kernel alone (the step's fraction is "
+                                             "step_roofline)",
+                    "bound": "hbm", "achieved": achieved, "peak": hbm,
                     "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
-                    "alg_bytes_per_launch": byts, "launch_ms": launch_ms,
+                    "alg_bytes_per_launch": byts, "alg_bytes_model": "fp32 outputs (as written)",
+                    "achieved_bf16_out_model": byts2 / (launch_ms / 1e3) / 1e9,
+                    "frac_bf16_out_model": byts2 / (launch_ms / 1e3) / 1e9 / hbm,
+                    "launch_ms": launch_ms,
                     "traffic": traffic_for(dom, args.workload)}
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
         host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in cpu_inp.items()}
-        res_host = {k: torch.empty(grads[k].shape, dtype=f32).pin_memory()
-                    for k in ("dA_log", "ddt_bias") if k in grads}
-        if not res_host:
-            res_host = {"ht": torch.empty(ht.shape, dtype=f32).pin_memory()}
+        res_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
         h2d = sum(v.numel() * v.element_size() for v in host.values() if torch.is_tensor(v))
         d2h = sum(v.numel() * v.element_size() for v in res_host.values())
 
-        # double-buffered inputs, as an input pipeline runs: step i+1's host-to-device copies
-        # run on a copy stream while step i computes; every step's copies lie inside the timed
-        # region (the copy stream starts after its first event) and share HBM with the kernels
-        bufs = [inp, {k_: (v_.clone() if torch.is_tensor(v_) else v_) for k_, v_ in inp.items()}]
-        copy_stream = torch.cuda.Stream(dev)
-        copied = [torch.cuda.Event(), torch.cuda.Event()]
-        freed = [torch.cuda.Event(), torch.cuda.Event()]
+        # an input / output pipeline: inputs and outputs double-buffered on the device; step i+1's
+        # host-to-device copies (copy stream) and step i-1's device-to-host copies of every result
+        # (o, ht, dq, dk, dv, dbeta, dg and the parameter gradients; a second copy stream) run
+        # while step i computes.  Every step's copies lie inside the timed region.
+        ibufs = [inp, {k_: (v_.clone() if torch.is_tensor(v_) else v_) for k_, v_ in inp.items()}]
+        obufs = [outs, make_outputs()]
+        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event(), torch.cuda.Event()]     # inputs of buffer b landed
+        in_free = [torch.cuda.Event(), torch.cuda.Event()]    # the step reading buffer b is done
+        computed = [torch.cuda.Event(), torch.cuda.Event()]   # outputs of buffer b written
+        out_free = [torch.cuda.Event(), torch.cuda.Event()]   # outputs of buffer b copied out
 
         def copy_in(b):
-            copy_stream.wait_event(freed[b])  # the step that last read buffer b is done
-            with torch.cuda.stream(copy_stream):
+            h2d_stream.wait_event(in_free[b])
+            with torch.cuda.stream(h2d_stream):
                 for k_, v_ in host.items():
                     if torch.is_tensor(v_):
-                        bufs[b][k_].copy_(v_, non_blocking=True)
-                copied[b].record(copy_stream)
+                        ibufs[b][k_].copy_(v_, non_blocking=True)
+                copied[b].record(h2d_stream)
+
+        def copy_out(b):
+            d2h_stream.wait_event(computed[b])
+            with torch.cuda.stream(d2h_stream):
+                for k_, v_ in res_host.items():
+                    v_.copy_(obufs[b][k_], non_blocking=True)
+                out_free[b].record(d2h_stream)
 
         def run(i):
             b = i % 2
             stream.wait_event(copied[b])
-            step(bufs[b])
-            freed[b].record(stream)
-            for k_, v_ in res_host.items():
-                v_.copy_(grads[k_] if k_ in grads else ht, non_blocking=True)
+            stream.wait_event(out_free[b])  # step i-2's results have left this buffer
+            step(ibufs[b], obufs[b])
+            in_free[b].record(stream)
+            computed[b].record(stream)
+            copy_out(b)
 
         def e2e_steps(n, start):
-            copy_stream.wait_event(start)
+            h2d_stream.wait_event(start)
+            d2h_stream.wait_event(start)
+            for b in (0, 1):  # nothing pending on the buffers at the start
+                in_free[b].record(stream)
+                out_free[b].record(stream)
             copy_in(0)
             for i in range(n):
                 if i + 1 < n:
                     copy_in((i + 1) % 2)
                 run(i)
+            stream.wait_stream(d2h_stream)  # the last results are on the host before the end
 
         s0 = torch.cuda.Event()
         s0.record(stream)
@@ -475,7 +554,9 @@ def main():
         barrier()
         ems = reduce_max_ms(a0.elapsed_time(a1) / args.steps, world, dev)
         e2e = {"value": job_throughput(T, world, ems), "unit": "tokens/s", "ms_per_step": ems,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "returned": sorted(res_host)}
+        del ibufs, obufs, host, res_host
 
     rows = None
     if rank == 0 and not args.no_rows:
@@ -493,11 +574,9 @@ def main():
             "vs_baseline": ((value / world) / (T / (PAGES_MS / 1e3))
                             if args.workload == "4doc" else None),
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"{w.row}:saved", "T": T, "H": H, "docs": list(w.lens),
-                       "d": 128, "chunk": 64,
-                       "outputs": "fp32 (o, dq, dk, dv, dbeta, dg / da, dA_log, dt_bias, states)",
-                       "l2": "inputs larger than L2 (no flush)",
-                       "parallelism": f"replicas x{world}"},
+            "config": bench_config(w, world),
+            "pages_protocol": protocol,
+            "step_roofline": step_roof,
             "clocks": ck,
             "gpu_launches": launches,
             "kernels": kernels,

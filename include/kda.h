@@ -40,8 +40,8 @@
  *    non-decreasing, cu_seqlens[N] = T.  Empty documents are allowed (their ht = h0).
  *  - Every pointer must be 16-byte aligned.  Outputs are fully overwritten, never accumulated.
  *  - Errors found on the host are returned as a status and nothing is launched.  Errors found on
- *    the device (malformed cu_seqlens) set a status word inside the workspace and make the kernels
- *    skip their work; read it with kda_read_device_status.  The library never aborts and never
+ *    the device (malformed cu_seqlens; in g form a gate value above 0) set a status word inside the
+ *    workspace and make the kernels skip their work; read it with kda_read_device_status.  The library never aborts and never
  *    traps on the device.
  *  - Results are bitwise reproducible run to run (no floating-point atomics; every reduction has
  *    a fixed order), and a document's outputs do not depend on the other documents of the pack
@@ -67,12 +67,14 @@ typedef enum kda_status {
     KDA_ERR_WORKSPACE = 3,    /* workspace (or saved buffer) smaller than the size query says */
     KDA_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch error) */
     KDA_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (reported via device status) */
-    KDA_ERR_DEVICE_CHECK = 6, /* device-side validation failed (e.g. malformed cu_seqlens) */
+    KDA_ERR_DEVICE_CHECK = 6, /* device-side validation failed (malformed cu_seqlens, g > 0) */
     KDA_ERR_TOO_LARGE = 7     /* problem needs more scratch than kda_fwd_static_ws holds */
 } kda_status;
 
 typedef enum kda_gate_form {
-    KDA_GATE_G = 0,   /* g_or_a holds the per-channel fp32 log gate g (expected <= 0) */
+    KDA_GATE_G = 0,   /* g_or_a holds the per-channel fp32 log gate g, which must be <= 0 (a
+                         decaying gate): a g > 0 or NaN inside a document sets the device status
+                         KDA_ERR_DEVICE_CHECK and the call's later kernels write nothing */
     KDA_GATE_RAW = 1  /* g_or_a holds a; g = -exp(A_log[h]) * softplus(a + dt_bias[h]) */
 } kda_gate_form;
 
@@ -130,9 +132,11 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
  *  - Problems whose kda_fwd workspace (kda_workspace_size, KDA_OP_FWD) exceeds
  *    KDA_STATIC_WS_BYTES are rejected with KDA_ERR_TOO_LARGE before anything is launched
  *    (roughly: (ceil(T/64) + N) * H <= 300 (chunk, head) pairs, e.g. 4096 tokens x 4 heads).
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- *    that device current; make that first call before any stream capture.  It allocates nothing:
- *    no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - Every call looks up the array's device address (cudaGetSymbolAddress) on the calling
+ *    thread's current device, so a device reset in between is harmless.  The first call on a
+ *    device also sets the device up (and may load the library's device code): make that first
+ *    call before any stream capture.  It allocates nothing: no cudaMalloc, no cudaFree, no
+ *    allocating library routine.
  *  - Every call shares the one array, which keeps the previous call's contents (nothing in it
  *    needs to start at zero).  Calls that may overlap on the GPU -- on different streams, or from
  *    several host threads -- race on it; serialise them on one stream.

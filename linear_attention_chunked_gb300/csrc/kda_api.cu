@@ -344,10 +344,11 @@ kda_status run_prologue(const Params& p, cudaStream_t st) {
 }
 
 // Scratch of the allocation-free forward (kda_fwd_static_ws): one static array per device that
-// loads this library.  Host code must not use the symbol as an address; the device address is
-// looked up once per device with cudaGetSymbolAddress.
+// loads this library.  In host code the symbol is a host-side stand-in, not a device address: the
+// device address is looked up with cudaGetSymbolAddress, with the calling device current, on
+// every call (a cheap table lookup), so a device reset that reloads the module and moves the
+// array never leaves a stale address behind.
 __device__ __align__(256) unsigned char g_static_ws[KDA_STATIC_WS_BYTES];
-void* g_static_ws_ptr[128];
 
 }  // namespace
 
@@ -361,7 +362,8 @@ const char* kda_status_string(kda_status s) {
         case KDA_ERR_WORKSPACE: return "workspace or saved buffer too small";
         case KDA_ERR_CUDA: return "CUDA runtime error";
         case KDA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
-        case KDA_ERR_DEVICE_CHECK: return "device-side validation failed (malformed cu_seqlens)";
+        case KDA_ERR_DEVICE_CHECK:
+            return "device-side validation failed (malformed cu_seqlens, or a g-form gate above 0)";
         case KDA_ERR_TOO_LARGE:
             return "problem needs more scratch than the allocation-free forward holds (KDA_STATIC_WS_BYTES)";
     }
@@ -421,19 +423,9 @@ kda_status kda_fwd_static_ws(const kda_problem* pr, const void* q, const void* k
     if (kda_status s = check_problem(pr)) return s;
     const Layout L = make_layout(pr->T, pr->N, pr->H);
     if (L.ws_fwd > KDA_STATIC_WS_BYTES) return KDA_ERR_TOO_LARGE;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
-    if (dev < 0 || dev >= 128) return KDA_ERR_UNSUPPORTED;
+    if (kda_status s = setup_device()) return s;  // the calling thread's device, sm_103 only
     void* ws = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_static_ws_ptr[dev]) {
-            void* ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return KDA_ERR_CUDA;
-            g_static_ws_ptr[dev] = ptr;
-        }
-        ws = g_static_ws_ptr[dev];
-    }
+    if (cudaGetSymbolAddress(&ws, g_static_ws) != cudaSuccess || !ws) return KDA_ERR_CUDA;
     return kda_fwd(pr, q, k, v, beta, g_or_a, A_log, dt_bias, h0, o, ht, nullptr, ws,
                    KDA_STATIC_WS_BYTES, stream);
 }

@@ -82,7 +82,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     // 1024-byte aligned base (offset arithmetic on the shared array keeps its address space known)
     BwdIntraSmem& S = *reinterpret_cast<BwdIntraSmem*>(smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int items = *p.nchunks * p.H;
+    // no work after a failed device-side check of this call (the outputs stay unwritten)
+    const int items = *p.status == KDA_ERR_DEVICE_CHECK ? 0 : *p.nchunks * p.H;
     if (int(blockIdx.x) >= items) return;
     auto rqs = [&](int r) { return L2N ? S.rq[r] : 1.f; };  // row scales of q^ = q rq, k^ = k rk
     auto rks = [&](int r) { return L2N ? S.rk[r] : 1.f; };

@@ -43,11 +43,13 @@ size_t bwd_gemm_tc_smem_bytes() { return BWD_GEMM_TC_SMEM; }
 // an item's MMAs and row sums are done, every operand tile is free and the next item's TMA loads
 // start, overlapping this item's TMEM -> global epilogues.
 __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid_constant__ TcMaps tm) {
-    const int items = *p.nchunks * p.H;
+    // no work after a failed device-side check of this call (the outputs stay unwritten)
+    const int items = *p.status == KDA_ERR_DEVICE_CHECK ? 0 : *p.nchunks * p.H;
     if (int(blockIdx.x) >= items) return;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = tc::align1024(smraw);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G_BAR);  // 0 G1 in, 1 G2 in, 2 MMA1, 3 MMA2/3, 4 dS1 in, 5 MMA4
+    // 0 G1 in, 1 G2 in, 2 MMA1, 3 MMA2/3, 4 dS1 in, 5 MMA4 (+80: spare barrier of the abort path)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + G_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + G_BAR + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G_BAR + 68);
     // leave-the-loop decision: thread 0 copies the abort flag into the item's slot (parity) before
@@ -295,7 +297,9 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
     }
 
     if (*abort_flag && tid == 0) {
-        // after a timed-out wait: let this block's TMA loads in flight land (bounded), report
+        // after a timed-out wait: let this block's MMAs and TMA loads in flight finish (bounded),
+        // report
+        tc::drain_mmas(reinterpret_cast<uint64_t*>(sm + G_BAR + 80), 100000000ull);
         if (pend >= 0) {
             tc::mbar_wait(&bar[0], uint32_t(pend), 100000000ull);
             tc::mbar_wait(&bar[1], uint32_t(pend), 100000000ull);

@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int col0 = (hv % (D / VW)) * VW;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = tc::align1024(smraw);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // A1 in, K in, MMA1 done, MMA2 done
+    // A1 in, K in, MMA1 done, MMA2 done (+48: spare barrier of the abort path)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + 36);
     // leave-the-loop decision per barrier of a step: thread 0 copies the abort flag into slot 0 / 1
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int row = 32 * qd + lane;  // accumulator row (key for S / D2, token for D1)
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
+    if (*p.status == KDA_ERR_DEVICE_CHECK) return;  // a failed device-side check of this call
 
     if (tid == 0) {
 #pragma unroll
@@ -312,8 +314,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     }
 
     if (*abort_flag) {
-        // after a timed-out wait: let the loads still in flight land (bounded), report, stop
+        // after a timed-out wait: let the MMAs and loads still in flight finish (bounded), report,
+        // stop
         if (tid == 0) {
+            tc::drain_mmas(reinterpret_cast<uint64_t*>(sm + OFF_BAR + 48), 100000000ull);
             if (pendA >= 0) tc::mbar_wait(&bar[0], uint32_t(pendA), 100000000ull);
             if (pendK >= 0) tc::mbar_wait(&bar[1], uint32_t(pendK), 100000000ull);
             p.status[0] = KDA_ERR_TIMEOUT;
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = tc::align1024(smraw);
     // barriers: 0 Kb in, 1 / 2 Aqk + dO in (buffer 0 / 1), 3 Qg in, 4 W in, 5 DA done, 6 DW done,
-    // 7 DQ done
+    // 7 DQ done (+80: spare barrier of the abort path)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + B_OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + B_OFF_BAR + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + B_OFF_BAR + 68);
@@ -385,6 +389,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int row = 32 * qd + lane;
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
+    if (*p.status == KDA_ERR_DEVICE_CHECK) return;  // a failed device-side check of this call
 
     if (tid == 0) {
 #pragma unroll
@@ -643,6 +648,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 
     if (*abort_flag) {
         if (tid == 0) {
+            tc::drain_mmas(reinterpret_cast<uint64_t*>(sm + B_OFF_BAR + 80), 100000000ull);
 #pragma unroll
             for (int i = 0; i < 5; ++i)
                 if (pend[i] >= 0) tc::mbar_wait(&bar[i], uint32_t(pend[i]), 100000000ull);

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
             dk[1] = make_float4(fk[4], fk[5], fk[6], fk[7]);
         }
         const float eA = p.gate_raw ? expf(peA) : 0.f;
+        bool bad_gate = false;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
@@ -188,9 +189,16 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
             if (p.gate_raw) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) x[j] = r < L ? -eA * softplus_f(x[j] + b4[j]) : 0.f;
+            } else {
+                // the exponent-difference factorisation needs a decaying gate: g <= 0 (NaN fails)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bad_gate |= !(x[j] <= 0.f);
             }
             *reinterpret_cast<float4*>(&S.gam[r * LDP + c4t]) = make_float4(x[0], x[1], x[2], x[3]);
         }
+        // reported in the status word; the state recurrences and backward kernels of this call
+        // then do nothing
+        if (bad_gate) p.status[0] = KDA_ERR_DEVICE_CHECK;
     }
     for (int i = tid; i < CH * LDA; i += BT) {
         S.Akk[i] = 0.f;

@@ -1,4 +1,4 @@
-// Chunk plan of a call (the forward intra-chunk and state-recurrence kernels have their own files).
+// Chunk plan of a call: the chunk table, per-document chunk offsets and the recurrence launch order.
 #include "kda_internal.cuh"
 
 namespace kda {

@@ -215,6 +215,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
             smem_u32(bar))
         : "memory");
 }
+// Abort path of a block whose wait timed out (reached only when the device is already in a bad
+// state): one more commit, on a spare barrier initialised here, arrives once every MMA this
+// thread issued before it has completed; wait for it (bounded) so that no MMA still writes TMEM
+// or reads shared memory when the block frees its TMEM and exits.
+__device__ __forceinline__ void drain_mmas(uint64_t* spare, uint64_t limit_ns) {
+    mbar_init(spare, 1);
+    fence_mbar_init();
+    mma_commit(spare);
+    mbar_wait(spare, 0, limit_ns);
+}
 
 // Writes 32 consecutive values (columns c0..c0+31 of row `row`) of a 128-byte-swizzled bf16 tile
 // whose rows hold 64 values, as hi and lo planes; c0 is a multiple of 8.

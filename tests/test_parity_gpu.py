@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from harness import TOL, assert_within, compare, gpu_fwd_bwd, oracle_fwd_bwd, to_dev
+from harness import TOL, assert_within, compare, gpu_fwd_bwd, oracle_fwd_bwd, rel_err, to_dev
 from linear_attention_chunked_gb300 import inputs, kda
 
 pytestmark = pytest.mark.gpu
@@ -178,6 +178,28 @@ def test_malformed_cu_seqlens_reports_device_status():
     assert kda.kda_read_device_status(ws) == kda.KDA_OK  # read clears it
     kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["cu_seqlens"], save=False, ws=ws)
     assert kda.kda_read_device_status(ws) == kda.KDA_OK
+
+
+def test_positive_g_gate_reports_device_status():
+    # g form needs a decaying gate (g <= 0): one positive value inside a document is reported as
+    # KDA_ERR_DEVICE_CHECK, the recurrences write nothing (o keeps its NaN prefill), and the next
+    # valid call on the same workspace reports OK and matches the oracle
+    inp, gate, l2n = _small("g_edges")
+    d = to_dev(inp)
+    g_bad = d["g"].clone()
+    g_bad[3, 1, 17] = 0.25
+    ws_b, _ = kda.kda_workspace_size(inp["q"].shape[0], d["cu_seqlens"].numel() - 1, 2,
+                                     kda.KDA_OP_FWD)
+    ws = torch.zeros(ws_b, dtype=torch.uint8, device="cuda")
+    o = torch.full(d["q"].shape, float("nan"), dtype=torch.float32, device="cuda")
+    kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], g_bad, d["cu_seqlens"], save=False, ws=ws, o=o)
+    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_DEVICE_CHECK
+    assert torch.isnan(o).all()
+    o, ht, _ = kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["cu_seqlens"], save=False,
+                           ws=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    ref = oracle_fwd_bwd(inp, gate=gate, l2norm=l2n, want_bwd=False)
+    assert rel_err(o.cpu().numpy(), ref["o"]) <= TOL["o"]
 
 
 def test_host_validation_on_device():

@@ -16,6 +16,10 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
   * fragment_summary   -- explicit matrix product of the per-token transitions at small d, and
                           S_out = M S_in + B against the token run; C against the token backward.
   * transfer_walk      -- associativity of the affine maps, and the walk against the unfragmented run.
+  * conv1d.conv_fwd / conv1d.conv_bwd (the width-4 causal conv1d + SiLU ahead of q / k / v, plain
+    numpy in FP64) -- a hand-worked example, SiLU and pure-shift closed forms, numpy.convolve,
+    halo split invariance, central finite differences (tests/test_conv_pins.py; planted mistakes
+    in tests/test_conv_mutants.py).
 tests/test_oracle_mutants.py plants one plausible mistake at a time into a copy of kda_oracle.c
 (``compile_source`` + ``using_build``) and checks that every such build fails at least one pin.
 """

@@ -177,6 +177,29 @@ kda_status kda_fragment_summary(const kda_problem* p, int mode, const void* q, c
                                 float* M, float* B_or_C, void* ws, size_t ws_bytes,
                                 kda_stream_t stream);
 
+/* Product format of the transfer walk.  M, B (or C) and the states stay FP32 in memory; each
+ * format differs only in how the FP32 products M S are formed:
+ *   KDA_WALK_FP32       CUDA-core FP32 multiply-add (one block per 32 state columns).
+ *   KDA_WALK_TF32       tensor cores (tcgen05 kind::tf32), operands rounded to TF32 (11
+ *                       significant bits), one product; full width (one block per document-head).
+ *   KDA_WALK_TF32_HILO  tensor cores, each operand split into a TF32 hi and lo part, three
+ *                       products (hi hi + hi lo + lo hi); full width.
+ *   KDA_WALK_BF16X3     tensor cores (kind::f16), each operand split into three bf16 parts, the
+ *                       six part products of combined order < 3; full width.
+ *   KDA_WALK_BF16X3_HW  as KDA_WALK_BF16X3, half width: two blocks per (document, head), each
+ *                       covering 64 of the state's 128 columns.
+ * Source: the KCP transfer-walk page (flashinfer PR #7176), PR description (the half-width BF16x3
+ * walk, each FP32 operand split into three BF16 parts with FP32 accumulation, two CTAs per
+ * (segment, head); the full-width TF32 hi/lo walk it replaced) and the commit note listing the
+ * TF32 hi/lo, static precision-mode and full-width BF16x3 forms. */
+typedef enum kda_walk_precision {
+    KDA_WALK_FP32 = 0,
+    KDA_WALK_TF32 = 1,
+    KDA_WALK_TF32_HILO = 2,
+    KDA_WALK_BF16X3 = 3,
+    KDA_WALK_BF16X3_HW = 4
+} kda_walk_precision;
+
 /* Transfer walk over the fragments of N documents.  doc_frag: device int32 [N+1]; the fragments
  * of document n are doc_frag[n] .. doc_frag[n+1]-1 (in token order) and doc_frag[N] = F.
  *   reverse = 0:  S_in[first] = S0[n] (NULL: zero);  S_in[f+1] = M_f S_in[f] + B_f;
@@ -185,12 +208,47 @@ kda_status kda_fragment_summary(const kda_problem* p, int mode, const void* q, c
  *                 dS_end[last] = S0[n];  dS_end[f-1] = M_f^T dS_end[f] + C_f;
  *                 S_final[n] = M_first^T dS_end[first] + C_first  (the document's dh0).
  * S_in fp32 [F,H,128,128] receives S_in[f] (forward) or dS_end[f] (backward); S_final fp32
- * [N,H,128,128] nullable.  Products are FP32-accurate.  Needs no workspace.
+ * [N,H,128,128] nullable.  precision: a kda_walk_precision (all but KDA_WALK_TF32 are accurate
+ * to FP32 rounding).  Needs no workspace; `ws` (nullable, >= 256 bytes, 16-byte aligned) only
+ * receives a device-side status in its first word (KDA_ERR_TIMEOUT if a bounded wait of the
+ * tensor-core walk gave up, S_in / S_final then unspecified), read with kda_read_device_status.
  * Source: the KCP transfer-walk page (PR #7176), PR description (the walk carries the FP32 state
  * across fragment boundaries as S_out = M * S_in + B). */
 kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int32_t H,
                              const float* M, const float* B, const float* S0, int reverse,
-                             float* S_in, float* S_final, kda_stream_t stream);
+                             int precision, float* S_in, float* S_final, void* ws,
+                             kda_stream_t stream);
+
+/* Width-4 causal depthwise conv1d + SiLU, the step ahead of KDA's q, k and v.  Per document of
+ * the pack (cu_seqlens) and channel c:
+ *     z[t, c] = bias[c] + sum_{j=0..3} w[c, j] * x[t - 3 + j, c],    y[t, c] = silu(z[t, c])
+ * (activation = 0: y = z).  A read before a document's first token takes the document's halo
+ * row -- halo[n, 3 + (t - 3 + j - start), c], the three tokens that precede the document, e.g.
+ * the end of the previous fragment of the same long document -- or zero when halo is NULL.
+ * Layouts: x, halo bf16 [T, C] and [N, 3, C]; w fp32 [C, 4] (tap j multiplies x[t - 3 + j]);
+ * bias fp32 [C] (nullable); y, dy, dx and dhalo are fp32 when out_fp32 = 1, else bf16; dw fp32
+ * [C, 4], dbias fp32 [C].  C is a multiple of 8 (q, k or v of H heads: C = 128 H; or the three
+ * together).  cu_seqlens as for kda_fwd (a malformed one gives unspecified values, never an
+ * out-of-bounds access).  The backward (of L = sum(y * dy)) recomputes z, needs the workspace of
+ * kda_conv_workspace_size (partial sums of dw and dbias, reduced in a fixed order: results are
+ * bitwise reproducible) and writes dhalo (nullable; requires halo) with the gradient flowing into
+ * the halo rows.  Source: the KCP transfer-walk page (flashinfer PR #7176), PR description: the
+ * module forward runs the conv halo exchange and the conv ahead of the KDA recurrence, and the
+ * family ships a width-4 causal conv1d + SiLU training backend with a halo variant. */
+typedef struct kda_conv_problem {
+    int64_t T;                  /* tokens, >= 0 */
+    int32_t N;                  /* documents (or fragments), >= 1 */
+    int32_t C;                  /* channels, a positive multiple of 8 */
+    int32_t activation;         /* 1: SiLU; 0: none */
+    int32_t out_fp32;           /* 1: y, dy, dx, dhalo fp32; 0: bf16 */
+    const int32_t* cu_seqlens;  /* device int32 [N+1] */
+} kda_conv_problem;
+kda_status kda_conv_workspace_size(const kda_conv_problem* p, size_t* ws_bytes);
+kda_status kda_conv_fwd(const kda_conv_problem* p, const void* x, const float* w,
+                        const float* bias, const void* halo, void* y, kda_stream_t stream);
+kda_status kda_conv_bwd(const kda_conv_problem* p, const void* x, const float* w,
+                        const float* bias, const void* halo, const void* dy, void* dx, float* dw,
+                        float* dbias, void* dhalo, void* ws, size_t ws_bytes, kda_stream_t stream);
 
 /* Copies the device status word of `ws` to the host (synchronises `stream`) and clears it.
  * *device_status receives a kda_status value (KDA_OK when no device-side error happened). */

@@ -41,7 +41,9 @@ kda_status setup_device() {
         if (cudaFuncSetAttribute(a.f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(a.smem)) !=
             cudaSuccess)
             return KDA_ERR_CUDA;
-    if (bwd_intra_setup() != cudaSuccess || chain_tc_setup() != cudaSuccess) return KDA_ERR_CUDA;
+    if (bwd_intra_setup() != cudaSuccess || chain_tc_setup() != cudaSuccess ||
+        walk_tc_setup() != cudaSuccess)
+        return KDA_ERR_CUDA;
     g_ready[dev] = true;
     return KDA_OK;
 }
@@ -543,18 +545,25 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
 
 kda_status kda_transfer_walk(int32_t N, const int32_t* doc_frag, int32_t F, int32_t H,
                              const float* M, const float* B, const float* S0, int reverse,
-                             float* S_in, float* S_final, kda_stream_t stream) {
-    if (N < 1 || H < 1 || F < 0 || !doc_frag || (reinterpret_cast<uintptr_t>(doc_frag) & 3u))
+                             int precision, float* S_in, float* S_final, void* ws,
+                             kda_stream_t stream) {
+    if (N < 1 || N > 65535 || H < 1 || H > 65535 || F < 0 || !doc_frag ||
+        (reinterpret_cast<uintptr_t>(doc_frag) & 3u))
         return KDA_ERR_INVALID_ARG;
     if (reverse != 0 && reverse != 1) return KDA_ERR_INVALID_ARG;
+    if (precision < KDA_WALK_FP32 || precision > KDA_WALK_BF16X3_HW) return KDA_ERR_INVALID_ARG;
     if (F > 0 && !(req(M) && req(B) && req(S_in))) return KDA_ERR_INVALID_ARG;
-    if (!opt(S0) || !opt(S_final)) return KDA_ERR_INVALID_ARG;
+    if (!opt(S0) || !opt(S_final) || !opt(ws)) return KDA_ERR_INVALID_ARG;
     if (kda_status s = setup_device()) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     {
         ProfScope ps(KK_WALK, st);
-        k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, F, H, M, B, S0, reverse,
-                                                             S_in, S_final);
+        if (precision == KDA_WALK_FP32)
+            k_walk<<<dim3(N, H, NSLICE), NTHR, SMEM_WALK, st>>>(N, doc_frag, F, H, M, B, S0,
+                                                                 reverse, S_in, S_final);
+        else
+            launch_walk_tc(precision, N, doc_frag, F, H, M, B, S0, reverse, S_in, S_final,
+                           static_cast<int*>(ws), st);
     }
     return launched();
 }

@@ -338,12 +338,17 @@ void launch_bwd_intra(const Params& p, const TcMaps& tm, unsigned grid, cudaStre
 __global__ void k_param_reduce(Params p);
 __global__ void k_walk(int N, const int* doc_frag, int F, int H, const float* M, const float* B,
                        const float* S0, int reverse, float* S_in, float* S_final);
+// tensor-core transfer walks (kda_walk_precision other than KDA_WALK_FP32)
+cudaError_t walk_tc_setup();
+void launch_walk_tc(int precision, int N, const int* doc_frag, int F, int H, const float* M,
+                    const float* B, const float* S0, int reverse, float* S_in, float* S_final,
+                    int* status, cudaStream_t st);
 
 // Launch accounting: every kernel launch of the library sits inside a ProfScope, which counts it
 // and, while profiling is enabled (kda_profile_enable), brackets it with CUDA events on its stream.
 enum KernelKind {
     KK_PLAN, KK_INTRA_FWD, KK_CHAIN_FWD, KK_CHAIN_BWD, KK_BWD_GEMMS, KK_BWD_INTRA,
-    KK_PARAM_REDUCE, KK_WALK, KK_COUNT
+    KK_PARAM_REDUCE, KK_WALK, KK_CONV_FWD, KK_CONV_BWD, KK_CONV_REDUCE, KK_COUNT
 };
 const char* kernel_name(int kind);
 class ProfScope {

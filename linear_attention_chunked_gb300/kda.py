@@ -23,9 +23,14 @@ KDA_STATIC_WS_BYTES = 64 << 20
 KDA_GATE_G, KDA_GATE_RAW = 0, 1
 KDA_OP_FWD, KDA_OP_BWD_SAVED, KDA_OP_BWD_REPLAY, KDA_OP_FRAGMENT, KDA_OP_WALK = 0, 1, 2, 3, 4
 KDA_FRAG_FWD, KDA_FRAG_BWD = 0, 1
+KDA_WALK_FP32, KDA_WALK_TF32, KDA_WALK_TF32_HILO, KDA_WALK_BF16X3, KDA_WALK_BF16X3_HW = 0, 1, 2, 3, 4
+WALK_PRECISIONS = {"fp32": KDA_WALK_FP32, "tf32": KDA_WALK_TF32, "tf32_hilo": KDA_WALK_TF32_HILO,
+                   "bf16x3": KDA_WALK_BF16X3, "bf16x3_hw": KDA_WALK_BF16X3_HW}
+WALK_DEFAULT = KDA_WALK_BF16X3_HW  # the format the pages ship as the default walk
 
 EXPORTS = ("kda_workspace_size", "kda_fwd", "kda_fwd_static_ws", "kda_bwd", "kda_fragment_summary",
-           "kda_transfer_walk", "kda_read_device_status", "kda_profile_enable",
+           "kda_transfer_walk", "kda_conv_workspace_size", "kda_conv_fwd", "kda_conv_bwd",
+           "kda_read_device_status", "kda_profile_enable",
            "kda_profile_collect", "kda_kernel_count", "kda_kernel_name", "kda_launch_counter",
            "kda_status_string")
 
@@ -34,6 +39,12 @@ class KdaError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
         super().__init__(f"{fn}: {kda_status_string(status)} (status {status})")
+
+
+class kda_conv_problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("C", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("out_fp32", ctypes.c_int32),
+                ("cu_seqlens", ctypes.c_void_p)]
 
 
 class kda_problem(ctypes.Structure):
@@ -68,7 +79,11 @@ def lib():
             L.kda_bwd.argtypes = [P] + [V] * 19 + [V, S, V]
             L.kda_fragment_summary.argtypes = [P, I] + [V] * 10 + [V, S, V]
             L.kda_transfer_walk.argtypes = [ctypes.c_int32, V, ctypes.c_int32, ctypes.c_int32,
-                                            V, V, V, I, V, V, V]
+                                            V, V, V, I, I, V, V, V, V]
+            CP = ctypes.POINTER(kda_conv_problem)
+            L.kda_conv_workspace_size.argtypes = [CP, ctypes.POINTER(S)]
+            L.kda_conv_fwd.argtypes = [CP, V, V, V, V, V, V]
+            L.kda_conv_bwd.argtypes = [CP] + [V] * 9 + [V, S, V]
             L.kda_read_device_status.argtypes = [V, ctypes.POINTER(I), V]
             L.kda_selftest_wait_timeout.argtypes = [V, ctypes.c_uint32, V]
             L.kda_profile_enable.argtypes = [I]
@@ -81,7 +96,8 @@ def lib():
             L.kda_status_string.argtypes = [I]
             L.kda_status_string.restype = ctypes.c_char_p
             for name in ("kda_workspace_size", "kda_fwd", "kda_fwd_static_ws", "kda_bwd", "kda_fragment_summary",
-                         "kda_transfer_walk", "kda_read_device_status", "kda_selftest_wait_timeout",
+                         "kda_transfer_walk", "kda_conv_workspace_size", "kda_conv_fwd",
+                         "kda_conv_bwd", "kda_read_device_status", "kda_selftest_wait_timeout",
                          "kda_profile_enable",
                          "kda_profile_collect", "kda_kernel_count"):
                 getattr(L, name).restype = ctypes.c_int
@@ -260,20 +276,87 @@ def kda_fragment_summary(q, k, v, beta, g_or_a, frag_cu, *, mode=KDA_FRAG_FWD, d
     return (M, B_or_C) if mode == KDA_FRAG_FWD else B_or_C
 
 
-def kda_transfer_walk(doc_frag, M, B, S0=None, *, reverse=False, S_in=None, S_final=None):
-    """Returns (S_in [F,H,d,d], S_final [N,H,d,d])."""
+def kda_transfer_walk(doc_frag, M, B, S0=None, *, reverse=False, precision=None, S_in=None,
+                      S_final=None, ws=None):
+    """Returns (S_in [F,H,d,d], S_final [N,H,d,d]).  precision: a KDA_WALK_* product format
+    (default WALK_DEFAULT); ws (optional, >= 256 bytes) receives the device status."""
     F, H, d, _ = M.shape
     N = doc_frag.numel() - 1
     dev = M.device
+    if precision is None:
+        precision = WALK_DEFAULT
     if S_in is None:
         S_in = torch.empty_like(M)
     if S_final is None:
         S_final = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         st = lib().kda_transfer_walk(N, _ptr(doc_frag), F, H, _ptr(M), _ptr(B), _ptr(S0),
-                                     int(bool(reverse)), _ptr(S_in), _ptr(S_final), _stream(dev))
+                                     int(bool(reverse)), int(precision), _ptr(S_in),
+                                     _ptr(S_final), _ptr(ws), _stream(dev))
     _check("kda_transfer_walk", st)
     return S_in, S_final
+
+
+def make_conv_problem(T, N, C, cu_seqlens=None, *, activation=True, out_dtype=torch.bfloat16):
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    return kda_conv_problem(int(T), int(N), int(C), int(bool(activation)),
+                            int(out_dtype == torch.float32),
+                            None if cu_seqlens is None else cu_seqlens.data_ptr())
+
+
+def kda_conv_workspace_size(T, N, C):
+    pr = make_conv_problem(T, N, C)
+    pr.cu_seqlens = 16  # size queries never read it
+    ws = ctypes.c_size_t(0)
+    _check("kda_conv_workspace_size", lib().kda_conv_workspace_size(ctypes.byref(pr), ctypes.byref(ws)))
+    return ws.value
+
+
+def _conv_shape(x, cu_seqlens):
+    T = x.shape[0]
+    C = x.numel() // max(T, 1) if T else int(torch.tensor(x.shape[1:]).prod())
+    return T, cu_seqlens.numel() - 1, C
+
+
+def kda_conv_fwd(x, w, cu_seqlens, *, bias=None, halo=None, activation=True,
+                 out_dtype=torch.bfloat16, y=None):
+    """Width-4 causal conv1d (+ SiLU) of x [T, ...] (bf16, C channels per token) with taps w
+    [C, 4] fp32; halo [N, 3, C] bf16 or None.  Returns y with x's shape in out_dtype."""
+    T, N, C = _conv_shape(x, cu_seqlens)
+    pr = make_conv_problem(T, N, C, cu_seqlens, activation=activation, out_dtype=out_dtype)
+    if y is None:
+        y = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    _check_dtypes({"y": y}, out_dtype)
+    with torch.cuda.device(x.device):
+        st = lib().kda_conv_fwd(ctypes.byref(pr), _ptr(x), _ptr(w), _ptr(bias), _ptr(halo), _ptr(y),
+                                _stream(x.device))
+    _check("kda_conv_fwd", st)
+    return y
+
+
+def kda_conv_bwd(x, w, cu_seqlens, dy, *, bias=None, halo=None, activation=True, want_dhalo=None,
+                 ws=None):
+    """Backward of L = sum(y * dy) (dy in y's dtype).  Returns dict dx (dy's dtype, x's shape),
+    dw [C, 4], dbias [C] (when bias is given), dhalo [N, 3, C] (when halo is given)."""
+    T, N, C = _conv_shape(x, cu_seqlens)
+    out_dtype = dy.dtype
+    pr = make_conv_problem(T, N, C, cu_seqlens, activation=activation, out_dtype=out_dtype)
+    dev = x.device
+    if ws is None:
+        ws = _empty_bytes(kda_conv_workspace_size(T, N, C), dev)
+    out = dict(dx=torch.empty(x.shape, dtype=out_dtype, device=dev),
+               dw=torch.empty((C, 4), dtype=torch.float32, device=dev))
+    if bias is not None:
+        out["dbias"] = torch.empty((C,), dtype=torch.float32, device=dev)
+    if halo is not None and want_dhalo is not False:
+        out["dhalo"] = torch.empty((N, 3, C), dtype=out_dtype, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().kda_conv_bwd(ctypes.byref(pr), _ptr(x), _ptr(w), _ptr(bias), _ptr(halo),
+                                _ptr(dy), _ptr(out["dx"]), _ptr(out["dw"]), _ptr(out.get("dbias")),
+                                _ptr(out.get("dhalo")), _ptr(ws), ws.numel(), _stream(dev))
+    _check("kda_conv_bwd", st)
+    return out
 
 
 def kda_read_device_status(ws) -> int:

@@ -95,10 +95,14 @@ def test_pointer_validation(lib):
     pr.cu_seqlens = None
     assert lib.kda_fwd(ctypes.byref(pr), a, a, a, a, a, z, z, z, a, z, z, a, 1 << 40, z) == \
         kda.KDA_ERR_INVALID_ARG
-    # walk: N < 1, H < 1, bad reverse flag
-    assert lib.kda_transfer_walk(0, a, 1, 1, a, a, z, 0, a, z, z) == kda.KDA_ERR_INVALID_ARG
-    assert lib.kda_transfer_walk(1, a, 1, 0, a, a, z, 0, a, z, z) == kda.KDA_ERR_INVALID_ARG
-    assert lib.kda_transfer_walk(1, a, 1, 1, a, a, z, 2, a, z, z) == kda.KDA_ERR_INVALID_ARG
+    # walk: N < 1, H < 1, bad reverse flag, unknown product format, misaligned status pointer
+    assert lib.kda_transfer_walk(0, a, 1, 1, a, a, z, 0, 0, a, z, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_transfer_walk(1, a, 1, 0, a, a, z, 0, 0, a, z, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_transfer_walk(1, a, 1, 1, a, a, z, 2, 0, a, z, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_transfer_walk(1, a, 1, 1, a, a, z, 0, 5, a, z, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_transfer_walk(1, a, 1, 1, a, a, z, 0, -1, a, z, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_transfer_walk(1, a, 1, 1, a, a, z, 0, 0, a, z, ctypes.c_void_p(258), z) == \
+        kda.KDA_ERR_INVALID_ARG
     # fragment summary: bad mode
     pf = kda.make_problem(128, 1, 2)
     pf.cu_seqlens = 256

@@ -70,23 +70,57 @@ def test_fragment_path_small(gate, l2norm):
     assert errs["B"] < TOL["ht"] and errs["C"] < TOL["ht"] and errs["M"] < 1e-4, errs
 
 
-def test_walk_covers_every_column_slice():
-    # every column of every S_in must be written: prefill with NaN and check none is left
-    F, H = 5, 3
-    gen = torch.Generator("cpu").manual_seed(0)
+# max|err| / rms(ref) of each walk product format against the FP64 oracle walk on the same FP32
+# M, B, S0: every format but plain TF32 is accurate to FP32 rounding; plain TF32 keeps 11
+# significant bits per operand (unit roundoff 2^-11 ~ 4.9e-4 per product term)
+WALK_TOL = {"fp32": 1e-5, "tf32": 2e-2, "tf32_hilo": 1e-5, "bf16x3": 1e-5, "bf16x3_hw": 1e-5}
+
+
+def _walk_case(F=7, H=3, seed=0):
+    gen = torch.Generator("cpu").manual_seed(seed)
     M = (torch.randn((F, H, 128, 128), generator=gen) * 0.05).cuda()
     B = torch.randn((F, H, 128, 128), generator=gen).cuda()
-    dfr = torch.tensor([0, 2, 5], dtype=torch.int32, device="cuda")
+    S0 = torch.randn((4, H, 128, 128), generator=gen).cuda()
+    doc_frag = [0, 2, 2, 6, 7]  # fragments per document: 2, 0 (empty), 4, 1
+    return M, B, S0, doc_frag
+
+
+@pytest.mark.parametrize("prec", list(WALK_TOL))
+def test_walk_formats_against_oracle(prec):
+    # every column of every S_in must be written (NaN prefill), the values must match the oracle
+    # walk within the format's bound, both directions, with and without a start state, and a
+    # second run must be bitwise equal
+    M, B, S0, doc_frag = _walk_case()
+    F, H = M.shape[:2]
+    dfr = torch.tensor(doc_frag, dtype=torch.int32, device="cuda")
+    p = kda.WALK_PRECISIONS[prec]
     for rev in (False, True):
-        S_in = torch.full((F, H, 128, 128), float("nan"), device="cuda")
-        S_fin = torch.full((2, H, 128, 128), float("nan"), device="cuda")
-        kda.kda_transfer_walk(dfr, M, B, None, reverse=rev, S_in=S_in, S_final=S_fin)
-        torch.cuda.synchronize()
-        assert not torch.isnan(S_in).any() and not torch.isnan(S_fin).any()
-        S_ref, fin_ref = oracle.transfer_walk([0, 2, 5], M.double().cpu().numpy(),
-                                              B.double().cpu().numpy(), None, reverse=rev)
-        assert rel_err(S_in.cpu().numpy(), S_ref) < 1e-5
-        assert rel_err(S_fin.cpu().numpy(), fin_ref) < 1e-5
+        for s0 in (None, S0):
+            S_in = torch.full((F, H, 128, 128), float("nan"), device="cuda")
+            S_fin = torch.full((4, H, 128, 128), float("nan"), device="cuda")
+            kda.kda_transfer_walk(dfr, M, B, s0, reverse=rev, precision=p, S_in=S_in,
+                                  S_final=S_fin)
+            again = kda.kda_transfer_walk(dfr, M, B, s0, reverse=rev, precision=p)
+            torch.cuda.synchronize()
+            assert not torch.isnan(S_in).any() and not torch.isnan(S_fin).any()
+            assert torch.equal(again[0], S_in) and torch.equal(again[1], S_fin)
+            S_ref, fin_ref = oracle.transfer_walk(
+                doc_frag, M.double().cpu().numpy(), B.double().cpu().numpy(),
+                None if s0 is None else s0.double().cpu().numpy(), reverse=rev)
+            e_in, e_fin = rel_err(S_in.cpu().numpy(), S_ref), rel_err(S_fin.cpu().numpy(), fin_ref)
+            print(prec, "reverse" if rev else "forward", "S0" if s0 is not None else "zero",
+                  f"S_in {e_in:.2e} S_final {e_fin:.2e}")
+            assert e_in < WALK_TOL[prec] and e_fin < WALK_TOL[prec], (e_in, e_fin)
+
+
+def test_walk_half_width_matches_full_width():
+    M, B, S0, doc_frag = _walk_case(seed=1)
+    dfr = torch.tensor(doc_frag, dtype=torch.int32, device="cuda")
+    full = kda.kda_transfer_walk(dfr, M, B, S0, precision=kda.KDA_WALK_BF16X3)
+    half = kda.kda_transfer_walk(dfr, M, B, S0, precision=kda.KDA_WALK_BF16X3_HW)
+    torch.cuda.synchronize()
+    for a, b in zip(full, half):
+        assert rel_err(b.cpu().numpy(), a.cpu().numpy()) < 1e-6
 
 
 @pytest.mark.slow

@@ -239,7 +239,7 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
                 M, B = kda.kda_fragment_summary(*a, mode=kda.KDA_FRAG_FWD, ws=ws, **kw)
                 S_in, S_fin = kda.kda_transfer_walk(dfr, M, B)
                 o, _, _ = kda.kda_fwd(*a, h0=S_in, saved=saved, ws=ws, **kw)
-                st.update(M=M, S_in=S_in)
+                st.update(M=M, B=B, S_in=S_in)
 
             def fwd_bwd():
                 fwd()
@@ -277,9 +277,59 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
             "fwd_byte_frac_fp32_out": round(th * BYTES_FWD_F32 / (f_ms * 1e6) / hbm_gbs, 4),
             "fwd_bwd_byte_frac_fp32_out": round(th * BYTES_FWD_BWD_F32 / (fb_ms * 1e6) / hbm_gbs, 4),
             "fwd_bwd_flop_frac": round(th * fb_flop / (fb_ms * 1e9) / bf16_tflops, 4)}
+        if w.fragments:
+            rows[f"{w.row}:walk"] = walk_formats(st["M"], st["B"], dfr)
         del x, ws, saved
         torch.cuda.empty_cache()
+    rows["conv:qkv"] = conv_row(dev, hbm_gbs)
     return rows
+
+
+def walk_formats(M, B, dfr):
+    """Each transfer-walk product format on the long-pack summaries: forward-walk ms (pages'
+    protocol) and max|S_in - S_in(FP32 FMA walk)| / rms."""
+    import torch
+    from linear_attention_chunked_gb300 import kda
+    ref, _ = kda.kda_transfer_walk(dfr, M, B, precision=kda.KDA_WALK_FP32)
+    out = {}
+    for name, prec in kda.WALK_PRECISIONS.items():
+        S_in, _ = kda.kda_transfer_walk(dfr, M, B, precision=prec)
+        torch.cuda.synchronize()
+        diff = float((S_in - ref).abs().max() / ref.pow(2).mean().sqrt().clamp_min(1e-30))
+        ms = _time_calls(lambda: kda.kda_transfer_walk(dfr, M, B, precision=prec))
+        out[name] = {"ms": round(ms, 4), "vs_fp32_walk": diff}
+    return out
+
+
+def conv_row(dev, hbm_gbs):
+    """The width-4 causal conv1d + SiLU over q, k and v together (C = 3 x 64 heads x 128) of the
+    4doc pack, bf16 in and out: fwd and fwd+bwd ms and the HBM fraction of their algorithmic bytes
+    (fwd: x in, y out; bwd: x and dy in, dx out; 2 bytes each per channel-token)."""
+    import torch
+    from linear_attention_chunked_gb300 import inputs, kda
+    w_ = inputs.WORKLOADS["4doc"]
+    T, C = w_.T, 3 * w_.H * 128
+    gen = torch.Generator("cpu").manual_seed(0)
+    x = torch.randn((T, C), generator=gen).bfloat16().to(dev)
+    wt = (torch.randn((C, 4), generator=gen) * 0.5).to(dev)
+    b = (torch.randn((C,), generator=gen) * 0.1).to(dev)
+    dy = torch.randn((T, C), generator=gen).bfloat16().to(dev)
+    cu = inputs.cu_from_lens(w_.lens).to(dev)
+    ws = torch.empty(max(kda.kda_conv_workspace_size(T, len(w_.lens), C), 256), dtype=torch.uint8,
+                     device=dev)
+    y = torch.empty_like(x)
+
+    def fwd():
+        kda.kda_conv_fwd(x, wt, cu, bias=b, y=y)
+
+    def fwd_bwd():
+        fwd()
+        kda.kda_conv_bwd(x, wt, cu, dy, bias=b, ws=ws)
+    f_ms, fb_ms = _time_calls(fwd), _time_calls(fwd_bwd)
+    fb, bb = T * C * 4, T * C * 6
+    return {"T": T, "C": C, "fwd_ms": round(f_ms, 4), "fwd_bwd_ms": round(fb_ms, 4),
+            "fwd_byte_frac": round(fb / (f_ms * 1e6) / hbm_gbs, 4),
+            "fwd_bwd_byte_frac": round((fb + bb) / (fb_ms * 1e6) / hbm_gbs, 4)}
 
 
 # ---------------------------------------------------------------------------------------------

@@ -18,7 +18,8 @@ struct Rec {
 std::vector<Rec> g_recs;
 const char* const kNames[KK_COUNT] = {"k_plan",      "k_intra_fwd",    "k_chain_fwd",
                                       "k_chain_bwd",    "k_bwd_gemms_tc",    "k_bwd_intra",
-                                      "k_param_reduce", "k_walk"};
+                                      "k_param_reduce", "k_walk",         "k_conv_fwd",
+                                      "k_conv_bwd",     "k_conv_reduce"};
 }  // namespace
 
 const char* kernel_name(int kind) { return (kind >= 0 && kind < KK_COUNT) ? kNames[kind] : "?"; }

@@ -183,8 +183,10 @@ def traffic_for(kernel, workload):
 # per-configuration rows: fwd and fwd+bwd ms with the pages' protocol (median of 15 samples, each
 # 20 back-to-back calls / 20)
 
-ROWS = [("m2", "saved"), ("R2", "saved"), ("R2fast", "saved"), ("1doc", "saved"),
-        ("4doc", "saved"), ("4doc", "replay"), ("longpack", "saved")]
+# (workload, backward mode, chunk groups per document: 0 = one serial chain per document)
+ROWS = [("m2", "saved", 0), ("R2", "saved", 0), ("R2", "saved", 48), ("R2fast", "saved", 0),
+        ("1doc", "saved", 0), ("1doc", "saved", 64), ("4doc", "saved", 0), ("4doc", "replay", 0),
+        ("longpack", "saved", 0)]
 
 
 def _time_calls(fn, samples=15, calls=20):
@@ -215,7 +217,7 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
     import torch
     from linear_attention_chunked_gb300 import inputs, kda
     rows = {}
-    for name, mode in ROWS:
+    for name, mode, G in ROWS:
         w = inputs.WORKLOADS[name]
         x = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inputs.workload_inputs(name).items()}
         kw = dict(gate=w.gate, A_log=x["A_log"], dt_bias=x["dt_bias"], l2norm=w.l2norm)
@@ -251,9 +253,10 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
             a = (x["q"], x["k"], x["v"], x["beta"], x["g"], x["cu_seqlens"])
             T, N, H = w.T, w.N, w.H
             replay = mode == "replay"
-            wsf, svb = kda.kda_workspace_size(T, N, H, kda.KDA_OP_FWD)
+            kw["group_chunks"] = G
+            wsf, svb = kda.kda_workspace_size(T, N, H, kda.KDA_OP_FWD, group_chunks=G)
             wsb, _ = kda.kda_workspace_size(T, N, H, kda.KDA_OP_BWD_REPLAY if replay else
-                                            kda.KDA_OP_BWD_SAVED)
+                                            kda.KDA_OP_BWD_SAVED, group_chunks=G)
             ws = torch.empty(max(wsf, wsb), dtype=torch.uint8, device=dev)
             saved = None if replay else torch.empty(svb, dtype=torch.uint8, device=dev)
 
@@ -269,7 +272,7 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
         # chunked-method FLOPs; replay adds one forward's FLOPs) against the measured peaks
         th = w.T * w.H
         fb_flop = FLOP_FWD_BWD + (FLOP_FWD if mode == "replay" else 0)
-        rows[f"{w.row}:{mode}"] = {
+        rows[f"{w.row}:{mode}" + (f":groups{G}" if G else "")] = {
             "T": w.T, "H": w.H, "fwd_ms": round(f_ms, 4), "fwd_bwd_ms": round(fb_ms, 4),
             "fwd_bwd_tokens_per_s": round(w.T / (fb_ms / 1e3)),
             "fwd_byte_frac": round(th * BYTES_FWD / (f_ms * 1e6) / hbm_gbs, 4),

@@ -101,6 +101,18 @@ typedef struct kda_problem {
     int32_t gate;               /* kda_gate_form */
     int32_t l2norm;             /* 0: q, k used as given; 1: fused q/sqrt(|q|^2+eps), same for k */
     int32_t out_fp32;           /* 1: o, dq, dk, dv, dbeta are fp32; 0: they are bf16 */
+    int32_t group_chunks;       /* 0: each document's state recurrence runs over its chunks in one
+                                   serial chain.  G > 0: documents are cut into groups of G chunks
+                                   (64 G tokens; the last group of a document may be shorter); the
+                                   groups' affine state summaries (M, B) -- and in the backward the
+                                   gradient summaries C -- are computed in parallel, the transfer
+                                   walk (BF16x3, full width) composes them into each group's start
+                                   state (start gradient), and the groups are finished in parallel.
+                                   The serial chain shrinks from a document's chunks to G chunks
+                                   plus a walk step per group.  Results equal the G = 0 ones up to
+                                   rounding (not bitwise); for a given G they are bitwise
+                                   reproducible and each document stays independent of the others.
+                                   kda_fragment_summary and kda_fwd_static_ws take G = 0 only. */
     float scale;                /* output scale (1 for the plain recurrence) */
     float l2_eps;               /* eps of the fused L2 norm (1e-6) */
     const int32_t* cu_seqlens;  /* device int32 [N+1] */

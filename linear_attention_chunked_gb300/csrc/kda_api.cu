@@ -61,6 +61,11 @@ kda_status check_problem(const kda_problem* p) {
     if (p->out_fp32 != 0 && p->out_fp32 != 1) return KDA_ERR_INVALID_ARG;
     if (!p->cu_seqlens || (reinterpret_cast<uintptr_t>(p->cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
     if (!(p->l2_eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+    if (p->group_chunks < 0 || p->group_chunks > (1 << 20)) return KDA_ERR_INVALID_ARG;
+    if (p->group_chunks > 0) {  // the group launches' one-dimensional grids
+        const Layout L = make_layout(p->T, p->N, p->H, p->group_chunks);
+        if (L.Gmax * p->H * 2 * NHALF > INT32_MAX || L.Gmax > INT32_MAX / 2) return KDA_ERR_UNSUPPORTED;
+    }
     return KDA_OK;
 }
 
@@ -119,6 +124,34 @@ void set_saved(Params& p, const Layout& L, char* base, bool states) {
     p.eGL = f(R.eGL);
     p.sS = states ? b(L.sv_S) : nullptr;
     p.sDelta = states ? b(L.sv_Delta) : nullptr;
+    p.gM = states && L.G > 0 ? f(L.sv_gM) : nullptr;
+}
+
+// Chunk groups: the group plan and per-group arrays in the group region at `gbase`, and the
+// parameters of a launch over groups (groups take the place of documents: their chunk offsets,
+// their launch order, Gmax "documents").
+struct Groups {
+    GroupPlan gp;
+    float *M, *B, *S;  // [Gmax][H][D][D]: summaries M, B or C, start states / end gradients
+    Params pg;
+};
+Groups make_groups(const Params& p, const Layout& L, char* gbase) {
+    Groups g{};
+    int* plan = reinterpret_cast<int*>(gbase + L.g_plan);
+    g.gp.ngroups = plan;
+    g.gp.gdoc_off = plan + 1;
+    g.gp.gdoc_order = plan + 1 + (L.Gmax + 1);
+    g.gp.doc_frag = plan + 1 + (L.Gmax + 1) + L.Gmax;
+    g.gp.G = L.G;
+    g.gp.Gmax = int(L.Gmax);
+    g.M = reinterpret_cast<float*>(gbase + L.g_M);
+    g.B = reinterpret_cast<float*>(gbase + L.g_B);
+    g.S = reinterpret_cast<float*>(gbase + L.g_S);
+    g.pg = p;
+    g.pg.N = int(L.Gmax);
+    g.pg.doc_off = g.gp.gdoc_off;
+    g.pg.doc_order = g.gp.gdoc_order;
+    return g;
 }
 
 void set_bwd_regions(Params& p, const Layout& L, void* ws) {
@@ -328,6 +361,71 @@ kda_status launched() {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Forward state recurrence over chunk groups: the group plan, the groups' summaries (M into
+// Mdst, B) in parallel, the transfer walk into every group's start state (and every document's
+// final state, ht), then the groups finished as documents from those start states (o and the
+// saved states when p asks for them).
+void grouped_chain_fwd(const Params& p, const kda_problem* pr, const Layout& L, char* gbase,
+                       float* Mdst, const TcMaps& tm, cudaStream_t st) {
+    Groups g = make_groups(p, L, gbase);
+    const unsigned gpairs = unsigned(L.Gmax) * unsigned(pr->H);
+    {
+        ProfScope ps(KK_PLAN, st);
+        k_group_plan<<<1, NTHR, 0, st>>>(p, g.gp);
+    }
+    {
+        Params sm = g.pg;
+        sm.fragM = Mdst;
+        sm.fragB = g.B;
+        ProfScope ps(KK_CHAIN_FWD, st);
+        launch_chain_fwd_tc(sm, CHAIN_FRAG_MB, tm, gpairs, device_sms(), st);
+    }
+    {
+        ProfScope ps(KK_WALK, st);
+        launch_walk_tc(KDA_WALK_BF16X3, pr->N, g.gp.doc_frag, int(L.Gmax), pr->H, Mdst, g.B, p.h0,
+                       0, g.S, p.ht, p.status, st);
+    }
+    {
+        Params f = g.pg;
+        f.h0 = g.S;
+        f.ht = nullptr;
+        ProfScope ps(KK_CHAIN_FWD, st);
+        launch_chain_fwd_tc(f, CHAIN_FWD_OUT, tm, gpairs, device_sms(), st);
+    }
+}
+
+// Backward state recurrence over chunk groups: the groups' gradient summaries C in parallel, the
+// reverse walk (transposed M from the forward) into every group's end gradient (and every
+// document's dh0), then the groups finished as documents from those end gradients (the per-chunk
+// gradients dS1 and dDelta).
+void grouped_chain_bwd(const Params& p, const kda_problem* pr, const Layout& L, char* gbase,
+                       const float* Msrc, const TcMaps& tm, cudaStream_t st) {
+    Groups g = make_groups(p, L, gbase);
+    const unsigned gpairs = unsigned(L.Gmax) * unsigned(pr->H);
+    {
+        ProfScope ps(KK_PLAN, st);
+        k_group_plan<<<1, NTHR, 0, st>>>(p, g.gp);
+    }
+    {
+        Params c = g.pg;
+        c.fragB = g.B;
+        ProfScope ps(KK_CHAIN_BWD, st);
+        launch_chain_bwd_tc(c, CHAIN_FRAG_C, tm, gpairs, device_sms(), st);
+    }
+    {
+        ProfScope ps(KK_WALK, st);
+        launch_walk_tc(KDA_WALK_BF16X3, pr->N, g.gp.doc_frag, int(L.Gmax), pr->H, Msrc, g.B, p.dht,
+                       1, g.S, p.dh0, p.status, st);
+    }
+    {
+        Params b = g.pg;
+        b.dht = g.S;
+        b.dh0 = nullptr;
+        ProfScope ps(KK_CHAIN_BWD, st);
+        launch_chain_bwd_tc(b, CHAIN_BWD, tm, gpairs, device_sms(), st);
+    }
+}
+
 // plan + intra-chunk products (shared by every op)
 kda_status run_prologue(const Params& p, cudaStream_t st) {
     {
@@ -374,7 +472,7 @@ const char* kda_status_string(kda_status s) {
 
 kda_status kda_workspace_size(const kda_problem* p, int op, size_t* ws_bytes, size_t* saved_bytes) {
     if (kda_status s = check_problem(p)) return s;
-    const Layout L = make_layout(p->T, p->N, p->H);
+    const Layout L = make_layout(p->T, p->N, p->H, p->group_chunks);
     size_t ws = 0;
     switch (op) {
         case KDA_OP_FWD: ws = L.ws_fwd; break;
@@ -397,7 +495,7 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     if (kda_status s = check_inputs(pr, q, k, v, beta, g_or_a, A_log, dt_bias)) return s;
     if ((pr->T > 0 && !req(o)) || !opt(h0) || !opt(ht) || !opt(saved) || !req(ws))
         return KDA_ERR_INVALID_ARG;
-    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    const Layout L = make_layout(pr->T, pr->N, pr->H, pr->group_chunks);
     if (ws_bytes < L.ws_fwd) return KDA_ERR_WORKSPACE;
     if (kda_status s = setup_device()) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -411,7 +509,11 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     TcMaps tm{};
     if (kda_status s = make_tc_maps(p, L, &tm)) return s;
     if (kda_status s = run_prologue(p, st)) return s;
-    {
+    if (L.G > 0) {
+        char* gbase = static_cast<char*>(ws) + L.g_fwd;
+        grouped_chain_fwd(p, pr, L, gbase, saved ? p.gM : reinterpret_cast<float*>(gbase + L.g_M),
+                          tm, st);
+    } else {
         ProfScope ps(KK_CHAIN_FWD, st);
         launch_chain_fwd(p, pr, tm, st);
     }
@@ -423,7 +525,8 @@ kda_status kda_fwd_static_ws(const kda_problem* pr, const void* q, const void* k
                              const float* dt_bias, const float* h0, void* o, float* ht,
                              kda_stream_t stream) {
     if (kda_status s = check_problem(pr)) return s;
-    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    if (pr->group_chunks != 0) return KDA_ERR_UNSUPPORTED;
+    const Layout L = make_layout(pr->T, pr->N, pr->H, pr->group_chunks);
     if (L.ws_fwd > KDA_STATIC_WS_BYTES) return KDA_ERR_TOO_LARGE;
     if (kda_status s = setup_device()) return s;  // the calling thread's device, sm_103 only
     void* ws = nullptr;
@@ -444,7 +547,7 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         return KDA_ERR_INVALID_ARG;
     if (pr->gate == KDA_GATE_RAW && !(req(dA_log) && req(ddt_bias))) return KDA_ERR_INVALID_ARG;
     if (!opt(h0) || !opt(dht) || !opt(dh0) || !opt(saved) || !req(ws)) return KDA_ERR_INVALID_ARG;
-    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    const Layout L = make_layout(pr->T, pr->N, pr->H, pr->group_chunks);
     if (ws_bytes < (saved ? L.ws_bwd_saved : L.ws_bwd_replay)) return KDA_ERR_WORKSPACE;
     if (kda_status s = setup_device()) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -481,10 +584,17 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         Params r = p;
         r.o = nullptr;
         r.ht = nullptr;
-        ProfScope ps(KK_CHAIN_FWD, st);
-        launch_chain_fwd(r, pr, tm, st);
+        if (L.G > 0) {
+            grouped_chain_fwd(r, pr, L, static_cast<char*>(ws) + L.g_bwd_replay, p.gM, tm, st);
+        } else {
+            ProfScope ps(KK_CHAIN_FWD, st);
+            launch_chain_fwd(r, pr, tm, st);
+        }
     }
-    {
+    if (L.G > 0) {
+        grouped_chain_bwd(p, pr, L, static_cast<char*>(ws) + (saved ? L.g_bwd_saved : L.g_bwd_replay),
+                          p.gM, tm, st);
+    } else {
         ProfScope ps(KK_CHAIN_BWD, st);
         launch_chain_bwd(p, pr, tm, st);
     }
@@ -513,12 +623,13 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
                                 float* M, float* B_or_C, void* ws, size_t ws_bytes,
                                 kda_stream_t stream) {
     if (kda_status s = check_problem(pr)) return s;
+    if (pr->group_chunks != 0) return KDA_ERR_UNSUPPORTED;
     if (kda_status s = check_inputs(pr, q, k, v, beta, g_or_a, A_log, dt_bias)) return s;
     if (mode != KDA_FRAG_FWD && mode != KDA_FRAG_BWD) return KDA_ERR_INVALID_ARG;
     if (!req(B_or_C) || !req(ws)) return KDA_ERR_INVALID_ARG;
     if (mode == KDA_FRAG_FWD && !req(M)) return KDA_ERR_INVALID_ARG;
     if (mode == KDA_FRAG_BWD && pr->T > 0 && !req(dO)) return KDA_ERR_INVALID_ARG;
-    const Layout L = make_layout(pr->T, pr->N, pr->H);
+    const Layout L = make_layout(pr->T, pr->N, pr->H, pr->group_chunks);
     if (ws_bytes < L.ws_frag) return KDA_ERR_WORKSPACE;
     if (kda_status s = setup_device()) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

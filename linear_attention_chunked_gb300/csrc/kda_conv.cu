@@ -24,7 +24,8 @@ namespace {
 
 constexpr int CV_TX = 32, CV_TY = 8;  // block: 32 channel groups x 8 token runs
 constexpr int CV_TT = 64;             // tokens per run
-constexpr int CV_UNR = 4;             // rows loaded per batch
+constexpr int CV_UNR = 8;             // rows of x loaded per batch (forward)
+constexpr int CV_UNR_B = 4;           // rows of x and dy loaded per batch (backward)
 constexpr int CV_ROWS = CV_TY * CV_TT;  // tokens per block row
 
 struct ConvArgs {
@@ -224,10 +225,28 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                     store_row(a.dx, size_t(rc), a.C, c0, acc[i], a.out_fp32);
             }
         };
-        int64_t t = t0;
-        for (; t < tl; ++t) {
+        int64_t t = t0;  // first token not processed
+        bool stop = false;
+        for (int64_t tb = t0; tb < tl && !stop; tb += CV_UNR_B) {
+          float xb[CV_UNR_B][CPT], gb[CV_UNR_B][CPT];  // rows tb .. tb + UNR - 1, loaded together
+#pragma unroll
+          for (int u = 0; u < CV_UNR_B; ++u)
+              if (tb + u < tl) {
+                  load_row(a.x, size_t(tb + u), a.C, c0, xb[u]);
+                  load_any(a.dy, size_t(tb + u), a.C, c0, a.out_fp32, gb[u]);
+              }
+#pragma unroll
+          for (int u = 0; u < CV_UNR_B; ++u) {
+            t = tb + u;
+            if (t >= tl) {
+                stop = true;
+                break;
+            }
             if (t >= e) {  // next document: rows of the old one are complete, its halo too
-                if (t >= t1) break;  // lookahead stops at the end of the document
+                if (t >= t1) {  // lookahead stops at the end of the document
+                    stop = true;
+                    break;
+                }
                 emit(t, 3);
                 flush_halo();
 #pragma unroll
@@ -244,9 +263,8 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                     for (int k = 0; k < CPT; ++k) dh[i][k] = 0.f;
                 window_at(a, n, s, t, c0, xm);
             }
-            float xr[CPT], g[CPT];
-            load_row(a.x, size_t(t), a.C, c0, xr);
-            load_any(a.dy, size_t(t), a.C, c0, a.out_fp32, g);
+            const float(&xr)[CPT] = xb[u];
+            const float(&g)[CPT] = gb[u];
             float dz[CPT];
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
@@ -296,6 +314,8 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                 xm[1][k] = xm[2][k];
                 xm[2][k] = xr[k];
             }
+            t = tb + u + 1;
+          }
         }
         // rows t - 3 .. t - 1 are still held when the loop stops (end of the lookahead, of the
         // document or of the sequence); they are complete

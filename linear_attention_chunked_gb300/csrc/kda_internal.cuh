@@ -47,8 +47,16 @@ struct Layout {
     size_t replay;    // replay copy of the saved set
     size_t intra_ws;  // intra products of a forward without saved set / of fragment summaries
     size_t ws_fwd, ws_bwd_saved, ws_bwd_replay, ws_frag;
+    // chunk groups (group_chunks = G > 0): at most Gmax groups; per op a region of g_bytes at
+    // g_fwd / g_bwd_saved / g_bwd_replay holding the group plan (g_plan: group count, group chunk
+    // offsets [Gmax + 1], launch order [Gmax], first group of each document [N + 1]) and the
+    // per-group summaries M, B (or C) and start states S_in (or end gradients) [Gmax][H][D][D]
+    int G;
+    int64_t Gmax;
+    size_t g_plan, g_M, g_B, g_S, g_bytes;
+    size_t g_fwd, g_bwd_saved, g_bwd_replay;
     // saved set
-    size_t sv_S, sv_Delta, saved_bytes;
+    size_t sv_S, sv_Delta, sv_gM, saved_bytes;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -85,19 +93,24 @@ inline IntraRecord make_intra_record(size_t CHd) {
 // Delta_c].  The workspace holds the chunk plan, the backward intermediates, and a private copy of
 // the intra products (forward without a saved set, fragment summaries) or of the whole saved set
 // (checkpoint replay).
-inline Layout make_layout(int64_t T, int N, int H) {
+inline Layout make_layout(int64_t T, int N, int H, int G = 0) {
     Layout L{};
     L.T = T;
     L.N = N;
     L.H = H;
     L.maxC = (T + CH - 1) / CH + N;
+    L.G = G;
+    // a document of c chunks has max(1, ceil(c / G)) groups: at most N + ceil(maxC / G) in all
+    L.Gmax = G > 0 ? N + (L.maxC + G - 1) / G : 0;
     const size_t CHd = size_t(L.maxC) * H;  // chunk-head pairs
     const size_t tileD = CHd * CH * D, tileC = CHd * CH * CH;
+    const size_t gstate = size_t(L.Gmax) * H * D * D * 4;  // one [Gmax][H][D][D] fp32 array
     const IntraRecord R = make_intra_record(CHd);
-    // saved set
+    // saved set (+ the groups' transition summaries M for the backward's reverse walk)
     L.sv_S = R.bytes;
     L.sv_Delta = align256(L.sv_S + CHd * D * D * 4);
-    L.saved_bytes = align256(L.sv_Delta + tileD * 4);
+    L.sv_gM = align256(L.sv_Delta + tileD * 4);
+    L.saved_bytes = align256(L.sv_gM + gstate);
     // workspace: header | backward intermediates | replay copy of the saved set.  The forward
     // without a saved set and the fragment summaries keep their intra products right after the
     // header instead (they need no backward intermediates).
@@ -125,8 +138,32 @@ inline Layout make_layout(int64_t T, int N, int H) {
     L.ws_bwd_saved = o;
     L.replay = take(L.saved_bytes);
     L.ws_bwd_replay = o;
+    if (G > 0) {  // group region appended to each op's workspace
+        size_t g = 0;
+        auto gtake = [&](size_t bytes) { size_t at = g; g = align256(g + bytes); return at; };
+        L.g_plan = gtake(sizeof(int) * size_t(1 + (L.Gmax + 1) + L.Gmax + (N + 1)));
+        L.g_M = gtake(gstate);
+        L.g_B = gtake(gstate);
+        L.g_S = gtake(gstate);
+        L.g_bytes = g;
+        L.g_fwd = align256(L.ws_fwd);
+        L.ws_fwd = L.g_fwd + g;
+        L.g_bwd_saved = align256(L.ws_bwd_saved);
+        L.ws_bwd_saved = L.g_bwd_saved + g;
+        L.g_bwd_replay = align256(L.ws_bwd_replay);
+        L.ws_bwd_replay = L.g_bwd_replay + g;
+    }
     return L;
 }
+
+// The group plan of a call with chunk groups (device arrays inside the group region).
+struct GroupPlan {
+    int* ngroups;     // [1]
+    int* gdoc_off;    // [Gmax + 1] first chunk of each group (empty groups after the last)
+    int* gdoc_order;  // [Gmax] groups by decreasing chunk count
+    int* doc_frag;    // [N + 1] first group of each document
+    int G, Gmax;
+};
 
 // Everything a kernel needs, passed by value.
 struct Params {
@@ -156,6 +193,8 @@ struct Params {
     __nv_bfloat16 *sS, *sDelta;
     // fragment summary outputs
     float *fragM, *fragB;
+    // saved transition summaries of the chunk groups [Gmax][H][D][D] (group_chunks > 0)
+    float* gM;
     int64_t maxC;
 };
 
@@ -325,6 +364,7 @@ constexpr int BI_THREADS = 512;     // threads of the backward intra-chunk kerne
 constexpr int INTRA_THREADS = 512;  // threads of the forward intra-chunk kernel
 constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences
 __global__ void k_plan(Params p);
+__global__ void k_group_plan(Params p, GroupPlan gp);
 __global__ void k_intra_fwd(Params p);
 // state recurrences (value-width templates, launched through these; sms = the device's SMs)
 cudaError_t chain_tc_setup();

@@ -54,4 +54,41 @@ __global__ void k_plan(Params p) {
     }
 }
 
+// Group plan of a call with chunk groups (one block, after k_plan): document n's chunks
+// [doc_off[n], doc_off[n + 1]) are cut into groups of G chunks (the last one shorter; an empty
+// document keeps one empty group, so every document has at least one group and its walk yields
+// its final state).  Groups are numbered document by document; unused group slots up to Gmax are
+// empty.  The launch order puts longer groups first (ties in index order; above MAX_SORT groups
+// the order stays the identity).
+__global__ void k_group_plan(Params p, GroupPlan gp) {
+    if (threadIdx.x == 0) {
+        int g = 0;
+        for (int n = 0; n < p.N; ++n) {
+            gp.doc_frag[n] = g;
+            const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
+            const int ng = c1 > c0 ? (c1 - c0 + gp.G - 1) / gp.G : 1;
+            for (int i = 0; i < ng && g < gp.Gmax; ++i) gp.gdoc_off[g++] = min(c0 + i * gp.G, c1);
+        }
+        gp.doc_frag[p.N] = g;
+        *gp.ngroups = g;
+        const int total = p.doc_off[p.N];
+        for (int i = g; i <= gp.Gmax; ++i) gp.gdoc_off[i] = total;
+    }
+    __syncthreads();
+    constexpr int MAX_SORT = 1024;
+    __shared__ int ncs[MAX_SORT];
+    if (gp.Gmax > MAX_SORT) {
+        for (int i = threadIdx.x; i < gp.Gmax; i += blockDim.x) gp.gdoc_order[i] = i;
+        return;
+    }
+    for (int i = threadIdx.x; i < gp.Gmax; i += blockDim.x) ncs[i] = gp.gdoc_off[i + 1] - gp.gdoc_off[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < gp.Gmax; i += blockDim.x) {
+        const int ni = ncs[i];
+        int rank = 0;
+        for (int j = 0; j < gp.Gmax; ++j) rank += (ncs[j] > ni) || (ncs[j] == ni && j < i);
+        gp.gdoc_order[rank] = i;
+    }
+}
+
 }  // namespace kda

@@ -50,7 +50,8 @@ class kda_conv_problem(ctypes.Structure):
 class kda_problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("N", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("d", ctypes.c_int32), ("gate", ctypes.c_int32), ("l2norm", ctypes.c_int32),
-                ("out_fp32", ctypes.c_int32), ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
+                ("out_fp32", ctypes.c_int32), ("group_chunks", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("l2_eps", ctypes.c_float),
                 ("cu_seqlens", ctypes.c_void_p)]
 
 
@@ -131,11 +132,11 @@ def _gate(gate):
 
 
 def make_problem(T, N, H, cu_seqlens=None, *, gate="g", l2norm=False, scale=1.0, eps=1e-6,
-                 d=D, out_dtype=torch.float32):
+                 d=D, out_dtype=torch.float32, group_chunks=0):
     if out_dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     return kda_problem(int(T), int(N), int(H), int(d), _gate(gate), int(bool(l2norm)),
-                       int(out_dtype == torch.float32), float(scale), float(eps),
+                       int(out_dtype == torch.float32), int(group_chunks), float(scale), float(eps),
                        None if cu_seqlens is None else cu_seqlens.data_ptr())
 
 
@@ -168,13 +169,14 @@ def _shape(q, cu_seqlens):
 
 def kda_fwd(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None, dt_bias=None, h0=None,
             l2norm=False, scale=1.0, eps=1e-6, save=True, out_dtype=torch.float32, o=None, ht=None,
-            saved=None, ws=None):
-    """Forward.  Returns (o, ht, saved) -- saved is None when save=False."""
+            saved=None, ws=None, group_chunks=0):
+    """Forward.  Returns (o, ht, saved) -- saved is None when save=False.  group_chunks > 0 cuts
+    documents into groups of that many chunks whose summaries are composed by the walk."""
     T, N, H, d = _shape(q, cu_seqlens)
     dev = q.device
     pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d,
-                      out_dtype=out_dtype)
-    ws_b, sv_b = kda_workspace_size(T, N, H, KDA_OP_FWD)
+                      out_dtype=out_dtype, group_chunks=group_chunks)
+    ws_b, sv_b = kda_workspace_size(T, N, H, KDA_OP_FWD, group_chunks=group_chunks)
     if ws is None:
         ws = _empty_bytes(ws_b, dev)
     if save and saved is None:
@@ -219,15 +221,16 @@ def kda_fwd_static_ws(q, k, v, beta, g_or_a, cu_seqlens, *, gate="g", A_log=None
 
 def kda_bwd(q, k, v, beta, g_or_a, cu_seqlens, dO, *, saved=None, gate="g", A_log=None,
             dt_bias=None, h0=None, dht=None, l2norm=False, scale=1.0, eps=1e-6, want_dh0=True,
-            out_dtype=torch.float32, out=None, ws=None):
-    """Backward (saved=None: checkpoint replay).  Returns a dict of gradients."""
+            out_dtype=torch.float32, out=None, ws=None, group_chunks=0):
+    """Backward (saved=None: checkpoint replay).  Returns a dict of gradients.  group_chunks must
+    be the forward's."""
     T, N, H, d = _shape(q, cu_seqlens)
     dev = q.device
     g_ = _gate(gate)
     pr = make_problem(T, N, H, cu_seqlens, gate=gate, l2norm=l2norm, scale=scale, eps=eps, d=d,
-                      out_dtype=out_dtype)
+                      out_dtype=out_dtype, group_chunks=group_chunks)
     op = KDA_OP_BWD_SAVED if saved is not None else KDA_OP_BWD_REPLAY
-    ws_b, _ = kda_workspace_size(T, N, H, op)
+    ws_b, _ = kda_workspace_size(T, N, H, op, group_chunks=group_chunks)
     if ws is None:
         ws = _empty_bytes(ws_b, dev)
     if out is None:

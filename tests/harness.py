@@ -27,19 +27,20 @@ def to_dev(inp, device="cuda"):
 
 
 def gpu_fwd_bwd(inp, *, gate, l2norm, h0=None, dht=None, saved_mode=True, want_bwd=True,
-                out_dtype=torch.float32):
+                out_dtype=torch.float32, group_chunks=0):
     d = to_dev(inp)
     h0d = None if h0 is None else torch.as_tensor(h0, dtype=torch.float32).cuda()
     dhtd = None if dht is None else torch.as_tensor(dht, dtype=torch.float32).cuda()
     o, ht, saved = kda.kda_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["cu_seqlens"],
                                gate=gate, A_log=d["A_log"], dt_bias=d["dt_bias"], h0=h0d,
-                               l2norm=l2norm, save=saved_mode, out_dtype=out_dtype)
+                               l2norm=l2norm, save=saved_mode, out_dtype=out_dtype,
+                               group_chunks=group_chunks)
     out = dict(o=o, ht=ht)
     if want_bwd:
         g = kda.kda_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["cu_seqlens"], d["dO"],
                         saved=saved if saved_mode else None, gate=gate, A_log=d["A_log"],
                         dt_bias=d["dt_bias"], h0=h0d, dht=dhtd, l2norm=l2norm,
-                        out_dtype=out_dtype)
+                        out_dtype=out_dtype, group_chunks=group_chunks)
         out.update(g)
     torch.cuda.synchronize()
     return {k: v.float().cpu().numpy() for k, v in out.items()}

@@ -13,8 +13,11 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkda_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-         "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
+# -ftz=true: single-precision results below 2^-126 flush to zero.  The kernels' exponentials of
+# gate differences then compile to a multiply and one ex2 (no subnormal rescaling around it); the
+# only values affected lie below 1.2e-38, far under every error bound.
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-ftz=true", "-Xcompiler", "-fPIC", "-Xcompiler",
+         "-Wall", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
 
 def _sources():

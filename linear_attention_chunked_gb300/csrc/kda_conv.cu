@@ -24,7 +24,7 @@ namespace {
 
 constexpr int CV_TX = 32, CV_TY = 8;  // block: 32 channel groups x 8 token runs
 constexpr int CV_TT = 64;             // tokens per run
-constexpr int CV_UNR = 8;             // rows of x loaded per batch (forward)
+constexpr int CV_UNR = 4;             // rows of x loaded per batch (forward)
 constexpr int CV_UNR_B = 4;           // rows of x and dy loaded per batch (backward)
 constexpr int CV_ROWS = CV_TY * CV_TT;  // tokens per block row
 
@@ -86,7 +86,9 @@ __device__ __forceinline__ void load_any(const void* base, size_t row, int C, in
     }
 }
 
-__device__ __forceinline__ float sigm(float z) { return 1.f / (1.f + expf(-z)); }
+// logistic function; the fast reciprocal returns 0 once 1 + e^-z exceeds 2^126 (z < -87), the
+// limit the exact value has there
+__device__ __forceinline__ float sigm(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
 // Document of token t: the last n with cu[n] <= t among documents that are not empty before t
 // (binary search; indices stay inside [0, N - 1] for any cu_seqlens).
@@ -123,7 +125,7 @@ __device__ __forceinline__ void window_at(const ConvArgs& a, int n, int64_t s, i
     }
 }
 
-__global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_fwd(ConvArgs a) {
+__global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
     const int cg = blockIdx.x * CV_TX + threadIdx.x, c0 = CPT * cg;
     const int64_t t0 = (int64_t(blockIdx.y) * CV_TY + threadIdx.y) * CV_TT;
     if (c0 >= a.C || t0 >= a.T) return;
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_fwd(ConvArgs a) {
             for (int k = 0; k < CPT; ++k) {
                 const float z = b[k] + w[0][k] * xm[0][k] + w[1][k] * xm[1][k] +
                                 w[2][k] * xm[2][k] + w[3][k] * xr[u][k];
-                out[k] = a.act ? z * sigm(z) : z;
+                out[k] = a.act ? __fdividef(z, 1.f + __expf(-z)) : z;
                 xm[0][k] = xm[1][k];
                 xm[1][k] = xm[2][k];
                 xm[2][k] = xr[u][k];

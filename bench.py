@@ -289,14 +289,18 @@ def run_rows(dev, hbm_gbs, bf16_tflops):
 
 
 def walk_formats(M, B, dfr):
-    """Each transfer-walk product format on the long-pack summaries: forward-walk ms (pages'
-    protocol) and max|S_in - S_in(FP32 FMA walk)| / rms."""
+    """Each transfer-walk product format: forward-walk ms on the long-pack summaries (pages'
+    protocol), and max|S_in - S_in(FP32 FMA walk)| / rms on the same shapes with a contractive
+    random M (the long-pack M has decayed to ~0 over 15,000 tokens, which would make every
+    format agree)."""
     import torch
     from linear_attention_chunked_gb300 import kda
-    ref, _ = kda.kda_transfer_walk(dfr, M, B, precision=kda.KDA_WALK_FP32)
+    gen = torch.Generator("cpu").manual_seed(0)
+    Mr = (torch.randn(M.shape, generator=gen) * 0.05).to(M.device)
+    ref, _ = kda.kda_transfer_walk(dfr, Mr, B, precision=kda.KDA_WALK_FP32)
     out = {}
     for name, prec in kda.WALK_PRECISIONS.items():
-        S_in, _ = kda.kda_transfer_walk(dfr, M, B, precision=prec)
+        S_in, _ = kda.kda_transfer_walk(dfr, Mr, B, precision=prec)
         torch.cuda.synchronize()
         diff = float((S_in - ref).abs().max() / ref.pow(2).mean().sqrt().clamp_min(1e-30))
         ms = _time_calls(lambda: kda.kda_transfer_walk(dfr, M, B, precision=prec))
@@ -312,12 +316,9 @@ def conv_row(dev, hbm_gbs):
     from linear_attention_chunked_gb300 import inputs, kda
     w_ = inputs.WORKLOADS["4doc"]
     T, C = w_.T, 3 * w_.H * 128
-    gen = torch.Generator("cpu").manual_seed(0)
-    x = torch.randn((T, C), generator=gen).bfloat16().to(dev)
-    wt = (torch.randn((C, 4), generator=gen) * 0.5).to(dev)
-    b = (torch.randn((C,), generator=gen) * 0.1).to(dev)
-    dy = torch.randn((T, C), generator=gen).bfloat16().to(dev)
-    cu = inputs.cu_from_lens(w_.lens).to(dev)
+    c = inputs.conv_inputs(w_.lens, C, seed=0)
+    x, wt, b, cu = (c[k].to(dev) for k in ("x", "w", "bias", "cu_seqlens"))
+    dy = c["dy"].bfloat16().to(dev)
     ws = torch.empty(max(kda.kda_conv_workspace_size(T, len(w_.lens), C), 256), dtype=torch.uint8,
                      device=dev)
     y = torch.empty_like(x)

@@ -200,9 +200,9 @@ kda_status kda_fragment_summary(const kda_problem* p, int mode, const void* q, c
  *                       six part products of combined order < 3; full width.
  *   KDA_WALK_BF16X3_HW  as KDA_WALK_BF16X3, half width: two blocks per (document, head), each
  *                       covering 64 of the state's 128 columns.
- * Source: the KCP transfer-walk page (flashinfer PR #7176), PR description (the half-width BF16x3
- * walk, each FP32 operand split into three BF16 parts with FP32 accumulation, two CTAs per
- * (segment, head); the full-width TF32 hi/lo walk it replaced) and the commit note listing the
+ * Source: the KCP transfer-walk page (flashinfer PR #7176), PR description (the shipped walk uses
+ * three bf16 pieces per FP32 operand on the tensor cores, FP32 accumulation, two CTAs per
+ * (segment, head); the full-width TF32 hi/lo walk it replaced) and the commit note that lists the
  * TF32 hi/lo, static precision-mode and full-width BF16x3 forms. */
 typedef enum kda_walk_precision {
     KDA_WALK_FP32 = 0,

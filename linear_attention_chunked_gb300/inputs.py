@@ -16,6 +16,10 @@ Workloads (documents packed back to back, head dim 128, chunk 64):
   4doc-h16  the same with 16 heads (profiling case)
   longpack  120000/70000/40000/19856 tokens, 16 heads, g form /16, unit q,k; 8 fragments per doc
 In every workload v, dO ~ N(0,1), beta = sigmoid(N(0,1)), zero initial state.
+
+Conv inputs (the width-4 causal conv1d + SiLU ahead of q / k / v; conv_inputs): draw order x
+~ N(0,1) [T, C] (bf16), taps w ~ N(0,1)/2 [C, 4], bias ~ N(0,1)/10 [C], halo ~ N(0,1) [N, 3, C]
+(bf16, when asked for), dy ~ N(0,1) [T, C].
 """
 from __future__ import annotations
 
@@ -111,3 +115,16 @@ def workload_inputs(name, seed=0, with_dO=True):
     w = WORKLOADS[name]
     return make_inputs(w.lens, w.H, gate=w.gate, l2norm=w.l2norm, gdiv=w.gdiv,
                        A_log_range=w.A_log_range, seed=seed, with_dO=with_dO)
+
+
+def conv_inputs(lens, C, *, seed=0, halo=False, bias=True):
+    """Inputs of the conv1d + SiLU on the CPU: dict x, w, bias, halo (or None), dy (fp32),
+    cu_seqlens."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    T = int(sum(lens))
+    x = torch.randn((T, C), generator=gen).bfloat16()
+    w = torch.randn((C, 4), generator=gen) * 0.5
+    b = torch.randn((C,), generator=gen) * 0.1 if bias else None
+    h = torch.randn((len(lens), 3, C), generator=gen).bfloat16() if halo else None
+    dy = torch.randn((T, C), generator=gen)
+    return dict(x=x, w=w, bias=b, halo=h, dy=dy, cu_seqlens=cu_from_lens(lens))

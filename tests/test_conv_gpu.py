@@ -23,15 +23,8 @@ TOL = 1e-5
 
 
 def _make(lens, C, seed, halo=False, bias=True):
-    gen = torch.Generator("cpu").manual_seed(seed)
-    T = int(sum(lens))
-    x = torch.randn((T, C), generator=gen).bfloat16()
-    w = (torch.randn((C, 4), generator=gen) * 0.5).float()
-    b = (torch.randn((C,), generator=gen) * 0.1).float() if bias else None
-    h = torch.randn((len(lens), 3, C), generator=gen).bfloat16() if halo else None
-    dy = torch.randn((T, C), generator=gen)
-    cu = inputs.cu_from_lens(lens)
-    return x, w, b, h, dy, cu
+    c = inputs.conv_inputs(lens, C, seed=seed, halo=halo, bias=bias)
+    return c["x"], c["w"], c["bias"], c["halo"], c["dy"], c["cu_seqlens"]
 
 
 def _np(t):

@@ -16,8 +16,9 @@ NVCC = os.environ.get("NVCC", "nvcc")
 # -ftz=true: single-precision results below 2^-126 flush to zero.  The kernels' exponentials of
 # gate differences then compile to a multiply and one ex2 (no subnormal rescaling around it); the
 # only values affected lie below 1.2e-38, far under every error bound.
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-ftz=true", "-Xcompiler", "-fPIC", "-Xcompiler",
-         "-Wall", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
+CODEGEN = ["-O3", "-lineinfo", "-std=c++17", "-ftz=true"]
+FLAGS = CODEGEN + ["-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "--expt-relaxed-constexpr", "-I",
+                   os.path.join(ROOT, "include")]
 
 
 def _sources():
@@ -104,8 +105,9 @@ KERNEL_SOURCES = {
 
 
 def source_digest(kernel: str = None) -> str:
-    """Short digest of the code of the CUDA sources and the ABI header, comments left out (ties
-    profiles to the code they measured; a comment-only edit keeps the digest).  With a kernel
+    """Short digest of the code of the CUDA sources and the ABI header, comments left out, and of
+    the code generation flags (ties profiles to the code they measured; a comment-only edit keeps
+    the digest).  With a kernel
     label: only that kernel's translation unit, the launch code (kda_api.cu), the shared headers
     and the ABI header, so a change to another kernel keeps this one's measurements."""
     import hashlib
@@ -114,6 +116,7 @@ def source_digest(kernel: str = None) -> str:
         own = {KERNEL_SOURCES[kernel], "kda_api.cu"}
         deps = [d for d in deps if not d.endswith(".cu") or os.path.basename(d) in own]
     h = hashlib.sha256()
+    h.update(" ".join(ARCH + CODEGEN).encode())
     for path in sorted(deps):
         h.update(os.path.basename(path).encode())
         with open(path, encoding="utf-8") as f:

@@ -92,11 +92,11 @@ __device__ __forceinline__ float sigm(float z) { return __fdividef(1.f, 1.f + __
 
 // Document of token t: the last n with cu[n] <= t among documents that are not empty before t
 // (binary search; indices stay inside [0, N - 1] for any cu_seqlens).
-__device__ __forceinline__ int doc_of(const int* cu, int N, int64_t t) {
+__device__ __forceinline__ int doc_of(const int* cu, int N, int t) {
     int lo = 0, hi = N - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (int64_t(cu[mid]) <= t) lo = mid;
+        if (int(cu[mid]) <= t) lo = mid;
         else hi = mid - 1;
     }
     return lo;
@@ -104,11 +104,11 @@ __device__ __forceinline__ int doc_of(const int* cu, int N, int64_t t) {
 
 // The three rows before token t of document n (start s): x rows inside the document, halo rows
 // (or zeros) before it.
-__device__ __forceinline__ void window_at(const ConvArgs& a, int n, int64_t s, int64_t t, int c0,
+__device__ __forceinline__ void window_at(const ConvArgs& a, int n, int s, int t, int c0,
                                           float (&xm)[3][CPT]) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
-        const int64_t r = t - 3 + i;  // xm[i] = x[t - 3 + i]
+        const int r = t - 3 + i;  // xm[i] = x[t - 3 + i]
         if (r >= s && r >= 0) {
             load_row(a.x, size_t(r), a.C, c0, xm[i]);
         } else if (a.halo) {
@@ -127,9 +127,9 @@ __device__ __forceinline__ void window_at(const ConvArgs& a, int n, int64_t s, i
 
 __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
     const int cg = blockIdx.x * CV_TX + threadIdx.x, c0 = CPT * cg;
-    const int64_t t0 = (int64_t(blockIdx.y) * CV_TY + threadIdx.y) * CV_TT;
+    const int t0 = (int(blockIdx.y) * CV_TY + int(threadIdx.y)) * CV_TT;
     if (c0 >= a.C || t0 >= a.T) return;
-    const int64_t t1 = min(t0 + CV_TT, a.T);
+    const int t1 = min(t0 + CV_TT, int(a.T));
     float w[4][CPT], b[CPT];
 #pragma unroll
     for (int k = 0; k < CPT; ++k) {
@@ -138,20 +138,20 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
         b[k] = a.bias ? a.bias[c0 + k] : 0.f;
     }
     int n = doc_of(a.cu, a.N, t0);
-    int64_t s = a.cu[n], e = a.cu[n + 1];
+    int s = a.cu[n], e = a.cu[n + 1];
     float xm[3][CPT];
     window_at(a, n, s, t0, c0, xm);
-    for (int64_t tb = t0; tb < t1; tb += CV_UNR) {
+    for (int tb = t0; tb < t1; tb += CV_UNR) {
         float xr[CV_UNR][CPT];
 #pragma unroll
         for (int u = 0; u < CV_UNR; ++u)
             if (tb + u < t1) load_row(a.x, size_t(tb + u), a.C, c0, xr[u]);
 #pragma unroll
         for (int u = 0; u < CV_UNR; ++u) {
-            const int64_t t = tb + u;
+            const int t = tb + u;
             if (t >= t1) break;
             if (t >= e) {  // next document (skipping empty ones): its halo rows or zeros
-                while (n + 1 < a.N && int64_t(a.cu[n + 1]) <= t) ++n;
+                while (n + 1 < a.N && int(a.cu[n + 1]) <= t) ++n;
                 s = a.cu[n];
                 e = a.cu[n + 1];
                 window_at(a, n, s, t, c0, xm);
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
     __shared__ float red[CV_TY][5][CPT][CV_TX + 1];
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int cg = blockIdx.x * CV_TX + tx, c0 = CPT * cg;
-    const int64_t t0 = (int64_t(blockIdx.y) * CV_TY + ty) * CV_TT;
+    const int t0 = (int(blockIdx.y) * CV_TY + ty) * CV_TT;
     const bool active = c0 < a.C && t0 < a.T;
     float pw[4][CPT], pb[CPT];
 #pragma unroll
@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
         for (int j = 0; j < 4; ++j) pw[j][k] = 0.f;
     }
     if (active) {
-        const int64_t t1 = min(t0 + CV_TT, a.T);
-        const int64_t tl = min(t1 + 3, a.T);  // last token (exclusive) whose dz is needed
+        const int t1 = min(t0 + CV_TT, int(a.T));
+        const int tl = min(t1 + 3, int(a.T));  // last token (exclusive) whose dz is needed
         float w[4][CPT], b[CPT];
 #pragma unroll
         for (int k = 0; k < CPT; ++k) {
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
             b[k] = a.bias ? a.bias[c0 + k] : 0.f;
         }
         int n = doc_of(a.cu, a.N, t0);
-        int64_t s = a.cu[n], e = a.cu[n + 1];
+        int s = a.cu[n], e = a.cu[n + 1];
         float xm[3][CPT];
         window_at(a, n, s, t0, c0, xm);
         float acc[4][CPT];  // dx of rows t - 3 .. t (acc[j] = row t - 3 + j), shifted per token
@@ -219,17 +219,17 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
         };
         // rows t - 3 .. t - 3 + cnt - 1 (acc[0 .. cnt-1]) of the current document that this thread
         // owns are complete: store them
-        auto emit = [&](int64_t t, int cnt) {
+        auto emit = [&](int t, int cnt) {
 #pragma unroll
             for (int i = 0; i < 3; ++i) {
-                const int64_t rc = t - 3 + i;
+                const int rc = t - 3 + i;
                 if (i < cnt && rc >= t0 && rc < t1 && rc >= s)
                     store_row(a.dx, size_t(rc), a.C, c0, acc[i], a.out_fp32);
             }
         };
-        int64_t t = t0;  // first token not processed
+        int t = t0;  // first token not processed
         bool stop = false;
-        for (int64_t tb = t0; tb < tl && !stop; tb += CV_UNR_B) {
+        for (int tb = t0; tb < tl && !stop; tb += CV_UNR_B) {
           float xb[CV_UNR_B][CPT], gb[CV_UNR_B][CPT];  // rows tb .. tb + UNR - 1, loaded together
 #pragma unroll
           for (int u = 0; u < CV_UNR_B; ++u)
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int k = 0; k < CPT; ++k) acc[i][k] = 0.f;
-                while (n + 1 < a.N && int64_t(a.cu[n + 1]) <= t) ++n;
+                while (n + 1 < a.N && int(a.cu[n + 1]) <= t) ++n;
                 s = a.cu[n];
                 e = a.cu[n + 1];
                 own_start = s >= t0 && s < t1;
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
             // (row t - 3 + j is before the start for j < s - t + 3, i.e. halo row j + t - s)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int64_t hr = int64_t(j) + t - s;  // halo row when < 3
+                const int hr = int(j) + t - s;  // halo row when < 3
                 if (hr >= 3) {
 #pragma unroll
                     for (int k = 0; k < CPT; ++k) acc[j][k] = fmaf(w[j][k], dz[k], acc[j][k]);
@@ -367,7 +367,9 @@ __global__ void k_conv_reduce(ConvArgs a, int rows) {
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 kda_status check_conv(const kda_conv_problem* p) {
-    if (!p || p->T < 0 || p->T > INT32_MAX || p->N < 1 || p->N > (1 << 24) || p->C < 8 ||
+    // token indices stay 32-bit inside the kernels (a thread's run reads up to 67 tokens past its
+    // start)
+    if (!p || p->T < 0 || p->T > INT32_MAX - 1024 || p->N < 1 || p->N > (1 << 24) || p->C < 8 ||
         p->C % 8 || p->C > (1 << 24))
         return KDA_ERR_INVALID_ARG;
     if ((p->activation != 0 && p->activation != 1) || (p->out_fp32 != 0 && p->out_fp32 != 1))

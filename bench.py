@@ -547,53 +547,70 @@ def main():
         d2h = sum(v.numel() * v.element_size() for v in res_host.values())
 
         # an input / output pipeline: inputs and outputs double-buffered on the device; step i+1's
-        # host-to-device copies (copy stream) and step i-1's device-to-host copies of every result
-        # (o, ht, dq, dk, dv, dbeta, dg and the parameter gradients; a second copy stream) run
-        # while step i computes.  Every step's copies lie inside the timed region.
+        # host-to-device copies and step i-1's device-to-host copies of every result (o, ht, dq,
+        # dk, dv, dbeta, dg and the parameter gradients) run while step i computes, each
+        # direction spread over NCOPY streams (every tensor cut into NCOPY contiguous pieces) so
+        # that several copy engines share it.  Every step's copies lie inside the timed region.
+        NCOPY = 4
         ibufs = [inp, {k_: (v_.clone() if torch.is_tensor(v_) else v_) for k_, v_ in inp.items()}]
         obufs = [outs, make_outputs()]
-        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        copied = [torch.cuda.Event(), torch.cuda.Event()]     # inputs of buffer b landed
-        in_free = [torch.cuda.Event(), torch.cuda.Event()]    # the step reading buffer b is done
-        computed = [torch.cuda.Event(), torch.cuda.Event()]   # outputs of buffer b written
-        out_free = [torch.cuda.Event(), torch.cuda.Event()]   # outputs of buffer b copied out
+        h2d_streams = [torch.cuda.Stream(dev) for _ in range(NCOPY)]
+        d2h_streams = [torch.cuda.Stream(dev) for _ in range(NCOPY)]
+        ev = lambda: [[torch.cuda.Event() for _ in range(NCOPY)] for _ in range(2)]  # noqa: E731
+        copied, out_free = ev(), ev()  # per buffer and copy stream
+        in_free = [torch.cuda.Event(), torch.cuda.Event()]   # the step reading buffer b is done
+        computed = [torch.cuda.Event(), torch.cuda.Event()]  # outputs of buffer b written
+
+        def pieces(t):
+            flat = t.view(-1)
+            n = flat.numel()
+            return [flat[i * n // NCOPY:(i + 1) * n // NCOPY] for i in range(NCOPY)]
+
+        pin_in = {k_: pieces(v_) for k_, v_ in host.items() if torch.is_tensor(v_)}
+        pin_out = {k_: pieces(v_) for k_, v_ in res_host.items()}
+        dev_in = [{k_: pieces(bf[k_]) for k_ in pin_in} for bf in ibufs]
+        dev_out = [{k_: pieces(bf[k_]) for k_ in pin_out} for bf in obufs]
 
         def copy_in(b):
-            h2d_stream.wait_event(in_free[b])
-            with torch.cuda.stream(h2d_stream):
-                for k_, v_ in host.items():
-                    if torch.is_tensor(v_):
-                        ibufs[b][k_].copy_(v_, non_blocking=True)
-                copied[b].record(h2d_stream)
+            for i, cs in enumerate(h2d_streams):
+                cs.wait_event(in_free[b])
+                with torch.cuda.stream(cs):
+                    for k_ in pin_in:
+                        dev_in[b][k_][i].copy_(pin_in[k_][i], non_blocking=True)
+                    copied[b][i].record(cs)
 
         def copy_out(b):
-            d2h_stream.wait_event(computed[b])
-            with torch.cuda.stream(d2h_stream):
-                for k_, v_ in res_host.items():
-                    v_.copy_(obufs[b][k_], non_blocking=True)
-                out_free[b].record(d2h_stream)
+            for i, cs in enumerate(d2h_streams):
+                cs.wait_event(computed[b])
+                with torch.cuda.stream(cs):
+                    for k_ in pin_out:
+                        pin_out[k_][i].copy_(dev_out[b][k_][i], non_blocking=True)
+                    out_free[b][i].record(cs)
 
         def run(i):
             b = i % 2
-            stream.wait_event(copied[b])
-            stream.wait_event(out_free[b])  # step i-2's results have left this buffer
+            for j in range(NCOPY):
+                stream.wait_event(copied[b][j])
+                stream.wait_event(out_free[b][j])  # step i-2's results have left this buffer
             step(ibufs[b], obufs[b])
             in_free[b].record(stream)
             computed[b].record(stream)
             copy_out(b)
 
         def e2e_steps(n, start):
-            h2d_stream.wait_event(start)
-            d2h_stream.wait_event(start)
+            for cs in h2d_streams + d2h_streams:
+                cs.wait_event(start)
             for b in (0, 1):  # nothing pending on the buffers at the start
                 in_free[b].record(stream)
-                out_free[b].record(stream)
+                for j in range(NCOPY):
+                    out_free[b][j].record(stream)
             copy_in(0)
             for i in range(n):
                 if i + 1 < n:
                     copy_in((i + 1) % 2)
                 run(i)
-            stream.wait_stream(d2h_stream)  # the last results are on the host before the end
+            for cs in d2h_streams:  # the last results are on the host before the end
+                stream.wait_stream(cs)
 
         s0 = torch.cuda.Event()
         s0.record(stream)
@@ -609,7 +626,7 @@ def main():
         ems = reduce_max_ms(a0.elapsed_time(a1) / args.steps, world, dev)
         e2e = {"value": job_throughput(T, world, ems), "unit": "tokens/s", "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "returned": sorted(res_host)}
+               "returned": sorted(res_host), "copy_streams_per_direction": NCOPY}
         del ibufs, obufs, host, res_host
 
     rows = None

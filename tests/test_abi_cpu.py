@@ -59,6 +59,8 @@ def test_workspace_sizes_depend_on_T_N_H_only(lib):
     ("gate", 7, kda.KDA_ERR_INVALID_ARG),
     ("l2norm", 2, kda.KDA_ERR_INVALID_ARG),
     ("out_fp32", 3, kda.KDA_ERR_INVALID_ARG),
+    ("group_chunks", -1, kda.KDA_ERR_INVALID_ARG),
+    ("group_chunks", (1 << 20) + 1, kda.KDA_ERR_INVALID_ARG),
 ])
 def test_problem_validation(lib, field, value, status):
     pr = kda.make_problem(128, 1, 2)
@@ -137,3 +139,51 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         kda.lib()
     with pytest.raises(RuntimeError, match="is missing"):
         kda.kda_status_string(0)
+
+
+def test_chunk_group_sizes_and_entry_points(lib):
+    # the group region grows every op's workspace and the saved set (the groups' M); sizes still
+    # depend on (T, N, H, group_chunks) only
+    base = {op: kda.kda_workspace_size(16384, 4, 64, op) for op in
+            (kda.KDA_OP_FWD, kda.KDA_OP_BWD_SAVED, kda.KDA_OP_BWD_REPLAY)}
+    grp = {op: kda.kda_workspace_size(16384, 4, 64, op, group_chunks=48) for op in base}
+    for op in base:
+        assert grp[op][0] > base[op][0] and grp[op][1] > base[op][1]
+    # Gmax = N + ceil((ceil(T / 64) + N) / G) = 4 + ceil(260 / 48) = 10 groups: three
+    # [Gmax][H][128][128] fp32 arrays in the workspace, one in the saved set
+    g_state = 10 * 64 * 128 * 128 * 4
+    assert 3 * g_state <= grp[kda.KDA_OP_FWD][0] - base[kda.KDA_OP_FWD][0] < 3 * g_state + 4096
+    assert g_state <= grp[kda.KDA_OP_FWD][1] - base[kda.KDA_OP_FWD][1] < g_state + 512
+    # the fragment summaries and the allocation-free forward take group_chunks = 0 only
+    pr = kda.make_problem(128, 1, 2, group_chunks=2)
+    pr.cu_seqlens = 256
+    z = ctypes.c_void_p(0)
+    assert lib.kda_fragment_summary(ctypes.byref(pr), 0, *([z] * 10), z, 0, z) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_fwd_static_ws(ctypes.byref(pr), *([z] * 10), z) == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_conv_validation(lib):
+    ws = ctypes.c_size_t(0)
+    pr = kda.make_conv_problem(1000, 2, 64)
+    pr.cu_seqlens = 256
+    assert lib.kda_conv_workspace_size(ctypes.byref(pr), ctypes.byref(ws)) == kda.KDA_OK
+    # partial sums of dw (4) and dbias (1) per channel for every 512-token block row
+    assert ws.value >= 2 * 5 * 64 * 4
+    for field, value in (("C", 12), ("C", 0), ("N", 0), ("T", -1), ("T", (1 << 31) - 1),
+                         ("activation", 2), ("out_fp32", 5)):
+        bad = kda.make_conv_problem(1000, 2, 64)
+        bad.cu_seqlens = 256
+        setattr(bad, field, value)
+        assert lib.kda_conv_workspace_size(ctypes.byref(bad), ctypes.byref(ws)) == \
+            kda.KDA_ERR_INVALID_ARG, (field, value)
+    z = ctypes.c_void_p(0)
+    a = ctypes.c_void_p(4096)
+    mis = ctypes.c_void_p(4104)
+    # null x / y, misaligned w, a halo gradient without a halo, workspace too small
+    assert lib.kda_conv_fwd(ctypes.byref(pr), z, a, z, z, a, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_conv_fwd(ctypes.byref(pr), a, a, z, z, z, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_conv_fwd(ctypes.byref(pr), a, mis, z, z, a, z) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_conv_bwd(ctypes.byref(pr), a, a, z, z, a, a, a, z, a, a, 1 << 30, z) == \
+        kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_conv_bwd(ctypes.byref(pr), a, a, z, z, a, a, a, z, z, a, 16, z) == \
+        kda.KDA_ERR_WORKSPACE

@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-profile", action="store_true", help="skip the per-kernel event pass")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-configuration rows")
+    ap.add_argument("--no-protocol", action="store_true",
+                    help="skip the pages' protocol pass (15 samples of 20 steps)")
     return ap.parse_args()
 
 
@@ -494,10 +496,12 @@ def main():
     value = job_throughput(T, world, ms)
 
     # ---- the pages' protocol: median of 15 samples, each 20 back-to-back steps / 20 ----
-    proto_ms = _time_calls(lambda: step(inp, outs), samples=15, calls=20)
-    proto_ms = reduce_max_ms(proto_ms, world, dev)
-    protocol = {"samples": 15, "calls_per_sample": 20, "median_ms_per_step": proto_ms,
-                "value": job_throughput(T, world, proto_ms), "unit": "tokens/s"}
+    protocol = None
+    if not args.no_protocol:
+        proto_ms = _time_calls(lambda: step(inp, outs), samples=15, calls=20)
+        proto_ms = reduce_max_ms(proto_ms, world, dev)
+        protocol = {"samples": 15, "calls_per_sample": 20, "median_ms_per_step": proto_ms,
+                    "value": job_throughput(T, world, proto_ms), "unit": "tokens/s"}
 
     hbm, bf16, src = load_peaks()
     step_roof = {

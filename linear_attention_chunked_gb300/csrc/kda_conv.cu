@@ -25,7 +25,7 @@ namespace {
 constexpr int CV_TX = 32, CV_TY = 8;  // block: 32 channel groups x 8 token runs
 constexpr int CV_TT = 64;             // tokens per run
 constexpr int CV_UNR = 4;             // rows of x loaded per batch (forward)
-constexpr int CV_UNR_B = 4;           // rows of x and dy loaded per batch (backward)
+constexpr int CV_UNR_B = 2;           // rows of x and dy loaded per batch (backward)
 constexpr int CV_ROWS = CV_TY * CV_TT;  // tokens per block row
 
 struct ConvArgs {
@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
 
 // Backward: per thread, tokens t0 .. t1 - 1 own their dx rows and their dw / db terms; dz of the
 // three tokens after t1 (same document) completes the last rows.  The owner of a document's
-// first token also owns the document's halo gradient.
+// first token also owns the document's halo gradient.  Every branch below depends only on token
+// positions, which all lanes of a warp share (lanes differ in channels), so none diverges.
 __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
     __shared__ float red[CV_TY][5][CPT][CV_TX + 1];
     const int tx = threadIdx.x, ty = threadIdx.y;
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
         for (int j = 0; j < 4; ++j) pw[j][k] = 0.f;
     }
     if (active) {
+        const int C = a.C, fp32 = a.out_fp32, act = a.act;
         const int t1 = min(t0 + CV_TT, int(a.T));
         const int tl = min(t1 + 3, int(a.T));  // last token (exclusive) whose dz is needed
         float w[4][CPT], b[CPT];
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
         auto flush_halo = [&]() {
             if (own_start && a.dhalo)
 #pragma unroll
-                for (int i = 0; i < 3; ++i) store_row(a.dhalo, size_t(n) * 3 + i, a.C, c0, dh[i], a.out_fp32);
+                for (int i = 0; i < 3; ++i) store_row(a.dhalo, size_t(n) * 3 + i, C, c0, dh[i], fp32);
         };
         // rows t - 3 .. t - 3 + cnt - 1 (acc[0 .. cnt-1]) of the current document that this thread
         // owns are complete: store them
@@ -224,18 +226,20 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
             for (int i = 0; i < 3; ++i) {
                 const int rc = t - 3 + i;
                 if (i < cnt && rc >= t0 && rc < t1 && rc >= s)
-                    store_row(a.dx, size_t(rc), a.C, c0, acc[i], a.out_fp32);
+                    store_row(a.dx, size_t(rc), C, c0, acc[i], fp32);
             }
         };
+        const __nv_bfloat16* xcol = a.x + c0;  // row t at xcol + t C
         int t = t0;  // first token not processed
         bool stop = false;
         for (int tb = t0; tb < tl && !stop; tb += CV_UNR_B) {
           float xb[CV_UNR_B][CPT], gb[CV_UNR_B][CPT];  // rows tb .. tb + UNR - 1, loaded together
+          const __nv_bfloat16* xp = xcol + size_t(tb) * C;
 #pragma unroll
           for (int u = 0; u < CV_UNR_B; ++u)
               if (tb + u < tl) {
-                  load_row(a.x, size_t(tb + u), a.C, c0, xb[u]);
-                  load_any(a.dy, size_t(tb + u), a.C, c0, a.out_fp32, gb[u]);
+                  bf4_to_f(*reinterpret_cast<const uint2*>(xp + size_t(u) * C), xb[u]);
+                  load_any(a.dy, size_t(tb + u), C, c0, fp32, gb[u]);
               }
 #pragma unroll
           for (int u = 0; u < CV_UNR_B; ++u) {
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int k = 0; k < CPT; ++k) acc[i][k] = 0.f;
-                while (n + 1 < a.N && int(a.cu[n + 1]) <= t) ++n;
+                while (n + 1 < a.N && a.cu[n + 1] <= t) ++n;
                 s = a.cu[n];
                 e = a.cu[n + 1];
                 own_start = s >= t0 && s < t1;
@@ -266,17 +270,16 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                 window_at(a, n, s, t, c0, xm);
             }
             const float(&xr)[CPT] = xb[u];
-            const float(&g)[CPT] = gb[u];
             float dz[CPT];
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
                 const float z = b[k] + w[0][k] * xm[0][k] + w[1][k] * xm[1][k] +
                                 w[2][k] * xm[2][k] + w[3][k] * xr[k];
-                if (a.act) {
+                if (act) {
                     const float sg = sigm(z);
-                    dz[k] = g[k] * sg * (1.f + z * (1.f - sg));
+                    dz[k] = gb[u][k] * sg * (1.f + z * (1.f - sg));
                 } else {
-                    dz[k] = g[k];
+                    dz[k] = gb[u][k];
                 }
             }
             if (t < t1) {  // this thread's dw / db terms
@@ -289,20 +292,31 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                     pb[k] += dz[k];
                 }
             }
-            // dz[t] reaches rows t - 3 + j: inside the document into dx, before it into the halo
-            // (row t - 3 + j is before the start for j < s - t + 3, i.e. halo row j + t - s)
+            // dz[t] reaches rows t - 3 + j: inside the document into dx, before it (the first
+            // three tokens of a document, tt = t - s < 3) into halo row j + tt
+            const int tt = t - s;
+            if (tt >= 3) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int hr = int(j) + t - s;  // halo row when < 3
-                if (hr >= 3) {
+                for (int j = 0; j < 4; ++j)
 #pragma unroll
                     for (int k = 0; k < CPT; ++k) acc[j][k] = fmaf(w[j][k], dz[k], acc[j][k]);
-                } else {
+            } else {
 #pragma unroll
-                    for (int i = 0; i < 3; ++i)
-                        if (hr == i)
-#pragma unroll
-                            for (int k = 0; k < CPT; ++k) dh[i][k] = fmaf(w[j][k], dz[k], dh[i][k]);
+                for (int k = 0; k < CPT; ++k) {
+                    acc[3][k] = fmaf(w[3][k], dz[k], acc[3][k]);
+                    if (tt == 0) {
+                        dh[0][k] = fmaf(w[0][k], dz[k], dh[0][k]);
+                        dh[1][k] = fmaf(w[1][k], dz[k], dh[1][k]);
+                        dh[2][k] = fmaf(w[2][k], dz[k], dh[2][k]);
+                    } else if (tt == 1) {
+                        dh[1][k] = fmaf(w[0][k], dz[k], dh[1][k]);
+                        dh[2][k] = fmaf(w[1][k], dz[k], dh[2][k]);
+                        acc[2][k] = fmaf(w[2][k], dz[k], acc[2][k]);
+                    } else {
+                        dh[2][k] = fmaf(w[0][k], dz[k], dh[2][k]);
+                        acc[1][k] = fmaf(w[1][k], dz[k], acc[1][k]);
+                        acc[2][k] = fmaf(w[2][k], dz[k], acc[2][k]);
+                    }
                 }
             }
             emit(t, 1);  // row t - 3 is complete

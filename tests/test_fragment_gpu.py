@@ -98,8 +98,10 @@ def test_walk_formats_against_oracle(prec):
         for s0 in (None, S0):
             S_in = torch.full((F, H, 128, 128), float("nan"), device="cuda")
             S_fin = torch.full((4, H, 128, 128), float("nan"), device="cuda")
+            ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
             kda.kda_transfer_walk(dfr, M, B, s0, reverse=rev, precision=p, S_in=S_in,
-                                  S_final=S_fin)
+                                  S_final=S_fin, ws=ws)
+            assert kda.kda_read_device_status(ws) == kda.KDA_OK
             again = kda.kda_transfer_walk(dfr, M, B, s0, reverse=rev, precision=p)
             torch.cuda.synchronize()
             assert not torch.isnan(S_in).any() and not torch.isnan(S_fin).any()

@@ -49,6 +49,10 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-configuration rows")
     ap.add_argument("--no-protocol", action="store_true",
                     help="skip the pages' protocol pass (15 samples of 20 steps)")
+    ap.add_argument("--only", choices=["conv", "walk"], default=None,
+                    help="run only the conv (16384 x 8192, fwd + bwd) or the transfer-walk "
+                         "formats (4 documents x 8 fragments x 16 heads) a few times and print "
+                         "their times (profiling targets)")
     return ap.parse_args()
 
 
@@ -413,11 +417,53 @@ def cpu_baseline(w, inp):
                       f"scaled to {w.H} heads"}
 
 
+def run_only(what):
+    """Small fixed workloads of the conv or the walk formats (targets for ncu captures)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from linear_attention_chunked_gb300 import inputs, kda
+    dev = torch.device("cuda", 0)
+    out = {"only": what}
+    if what == "conv":
+        lens, C = [8192, 4096, 3072, 1024], 8192
+        c = inputs.conv_inputs(lens, C, seed=0)
+        x, w, b, cu = (c[k].to(dev) for k in ("x", "w", "bias", "cu_seqlens"))
+        dy = c["dy"].bfloat16().to(dev)
+        ws = torch.empty(kda.kda_conv_workspace_size(sum(lens), len(lens), C), dtype=torch.uint8,
+                         device=dev)
+        y = torch.empty_like(x)
+        f = lambda: kda.kda_conv_fwd(x, w, cu, bias=b, y=y)  # noqa: E731
+        g = lambda: kda.kda_conv_bwd(x, w, cu, dy, bias=b, ws=ws)  # noqa: E731
+        for _ in range(3):  # launch order fwd, bwd (+ reduce) x 3, then the timing loops
+            f()
+            g()
+        n = sum(lens) * C
+        f_ms, g_ms = _time_calls(f, 5, 20), _time_calls(g, 5, 20)
+        out.update(fwd_ms=f_ms, bwd_ms=g_ms, fwd_gbs=n * 4 / f_ms / 1e6, bwd_gbs=n * 6 / g_ms / 1e6)
+    else:
+        gen = torch.Generator("cpu").manual_seed(0)
+        M = (torch.randn((32, 16, 128, 128), generator=gen) * 0.05).to(dev)
+        B = torch.randn((32, 16, 128, 128), generator=gen).to(dev)
+        dfr = torch.tensor([0, 8, 16, 24, 32], dtype=torch.int32, device=dev)
+        for _ in range(2):  # launch order: every format forward then reverse, twice; then timing
+            for name, prec in kda.WALK_PRECISIONS.items():
+                for rev in (False, True):
+                    kda.kda_transfer_walk(dfr, M, B, precision=prec, reverse=rev)
+        for name, prec in kda.WALK_PRECISIONS.items():
+            out[name] = _time_calls(lambda: kda.kda_transfer_walk(dfr, M, B, precision=prec), 5, 20)
+    torch.cuda.synchronize()
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.only:
+        run_only(args.only)
         return
     import torch
     import torch.distributed as dist

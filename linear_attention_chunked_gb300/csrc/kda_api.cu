@@ -252,6 +252,18 @@ kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return KDA_ERR_CUDA;
+    if (p.sS) {  // the saved states and write vectors, stored from the recurrence's shared tiles
+        const cuuint32_t bS[3] = {64, 128, 2}, bD[3] = {64, 64, 2};
+        const cuuint64_t dS[3] = {D, D, 2 * CHd}, sSt[2] = {D * 2, size_t(D) * D * 2};
+        const cuuint64_t dD[3] = {D, CH, 2 * CHd}, sDt[2] = {D * 2, size_t(CH) * D * 2};
+        if (enc(&tm->mSst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.sS, dS, sSt, bS, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            enc(&tm->mDst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.sDelta, dD, sDt, bD, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return KDA_ERR_CUDA;
+    }
     return KDA_OK;
 }
 

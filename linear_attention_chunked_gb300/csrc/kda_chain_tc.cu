@@ -69,6 +69,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
     if (*p.status == KDA_ERR_DEVICE_CHECK) return;  // a failed device-side check of this call
+    // 64-column blocks store the saved S_c and Delta_c straight from their shared operand tiles
+    // (one TMA store per tile, issued by thread 0) instead of one row per thread
+    const bool tsave = VW == 64 && fwd && p.sS != nullptr;
 
     if (tid == 0) {
 #pragma unroll
@@ -170,6 +173,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         tc::st_sw128_n<VPT>(sm + OFF_S, row, cc, sh);
         tc::st_sw128_n<VPT>(sm + OFF_S + 16384, row, cc, sl);
         tc::fence_async_smem();
+        // the previous chunk's Delta store has read its tile (rewritten below this barrier)
+        if (tsave && tid == 0) tc::bulk_wait_read0();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -196,10 +201,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 *abort_flag = 1;
             }
             tc::mma_commit(&bar[2]);
+            if (tsave) {  // the saved start state, both planes, from the S tile
+                tc::tma_store3(&tm.mSst, col0, 0, int(2 * chd), sm + OFF_S);
+                tc::bulk_commit();
+            }
         }
         __syncwarp();
         // while MMA1 runs: the saved start state, this chunk's U row and e^gL
-        if (fwd && p.sS) {
+        if (fwd && p.sS && !tsave) {
             __nv_bfloat16* dst = p.sS + chd * 2 * D * D + size_t(row) * D + col0 + cc;
             tc::st_g_n<VPT>(dst, sh);
             tc::st_g_n<VPT>(dst + D * D, sl);
@@ -227,6 +236,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::st_sw128_n<VPT>(sm + OFF_DL + 8192, row, cc, dll);
         }
         tc::fence_async_smem();
+        // this chunk's state store has read the S tile (rewritten before the next barrier)
+        if (tsave && tid == 0) tc::bulk_wait_read0();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -263,10 +274,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 *abort_flag = 1;
             }
             tc::mma_commit(&bar[3]);
+            if (tsave) {  // the saved write vectors, both planes, from the Delta tile
+                tc::tma_store3(&tm.mDst, col0, 0, int(2 * chd), sm + OFF_DL);
+                tc::bulk_commit();
+            }
         }
         __syncwarp();
         // while MMA2 / MMA3 run: the saved write vectors and the next chunk's per-thread operands
-        if (qd < 2 && fwd && p.sDelta) {
+        if (qd < 2 && fwd && p.sDelta && !tsave) {
             __nv_bfloat16* dst = p.sDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
             tc::st_g_n<VPT>(dst, dhh);
             tc::st_g_n<VPT>(dst + CH * D, dll);
@@ -313,6 +328,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         }
     }
 
+    if (tsave && tid == 0) tc::bulk_wait0();  // saved-set stores complete before the block ends
     if (*abort_flag) {
         // after a timed-out wait: let the MMAs and loads still in flight finish (bounded), report,
         // stop

@@ -350,6 +350,9 @@ struct TcMaps {
     //   mDD5, mDl5  dDelta / Delta, both planes: {64 values, 64 tokens, value block, plane, chunk}
     //   mS5  saved S, both planes: {64 values, 128 keys, value block, plane, chunk}
     CUtensorMap mA1, mKb, mAq, mDD5, mDl5, mS5;
+    // stores of the saved set by the 64-column forward recurrence: S_c and Delta_c, both planes of
+    // one 64-value block, {64 values, 128 keys or 64 tokens, plane-chunk = 2 chunk-head + plane}
+    CUtensorMap mSst, mDst;
     // backward intra-chunk inputs: q, k [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens};
     // dAqk, dM [chunk * H + head][64][64] fp32 as 32 x 64 boxes (128-byte swizzle)
     CUtensorMap mq, mk, mdA, mdM;

@@ -116,6 +116,26 @@ __device__ __forceinline__ void tma5(void* dst, const CUtensorMap* map, int x, i
         "r"(smem_u32(bar))
         : "memory");
 }
+// 3-D tiled tensor store from shared memory (the map's swizzle describes the shared image),
+// tracked as a bulk async-group of the issuing thread: commit it with bulk_commit, then
+// bulk_wait_read0 before the shared tile is rewritten and bulk_wait0 before the block exits.
+__device__ __forceinline__ void tma_store3(const CUtensorMap* map, int x, int y, int z,
+                                           const void* src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 // First 1024-byte boundary at or after p (128-byte-swizzled tiles need it).
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
     return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &

@@ -323,6 +323,15 @@ kda_status make_bwd_maps(const Params& p, const Layout& L, TcMaps* tm) {
                 x.box, es5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return KDA_ERR_CUDA;
+    // stores of dS1 / dDelta by the backward recurrence: one 64-value block, both planes
+    const cuuint32_t bS[3] = {64, 128, 2}, bD[3] = {64, 64, 2};
+    if (enc(&tm->mdSst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.dS1, d128, s128, bS, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&tm->mdDst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.dDelta, d64, s64, bD, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

@@ -406,6 +406,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
     if (*p.status == KDA_ERR_DEVICE_CHECK) return;  // a failed device-side check of this call
+    // 64-column blocks store dS1 and dDelta straight from their shared operand tiles (one TMA
+    // store per tile, issued by thread 0) instead of one row per thread
+    const bool tsave = VW == 64 && bwd;
 
     if (tid == 0) {
 #pragma unroll
@@ -513,6 +516,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         tc::st_sw128_n<VPT>(sm + B_OFF_DS, row, cc, sh_);
         tc::st_sw128_n<VPT>(sm + B_OFF_DS + 16384, row, cc, sl_);
         tc::fence_async_smem();
+        // the previous chunk's dDelta store has read its tile (rewritten below this barrier)
+        if (tsave && tid == 0) tc::bulk_wait_read0();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -557,9 +562,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 *abort_flag = 1;
             }
             tc::mma_commit(&bar[7]);
+            if (tsave) {  // the gradient at the chunk end, both planes, from the dS1 tile
+                tc::tma_store3(&tm.mdSst, col0, 0, int(2 * chd), sm + B_OFF_DS);
+                tc::bulk_commit();
+            }
         }
         __syncwarp();
-        if (bwd) {  // while DA runs: the saved gradient at the chunk end
+        if (bwd && !tsave) {  // while DA runs: the saved gradient at the chunk end
             __nv_bfloat16* dst = p.dS1 + chd * 2 * D * D + size_t(row) * D + col0 + cc;
             tc::st_g_n<VPT>(dst, sh_);
             tc::st_g_n<VPT>(dst + D * D, sl_);
@@ -593,6 +602,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 pend[3] = int(ph ^ 1u);
             }
             stopf[1] = *abort_flag;  // decision at the next barrier
+            if (tsave) tc::bulk_wait_read0();  // this chunk's dS1 store has read its tile
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
@@ -621,6 +631,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 *abort_flag = 1;
             }
             tc::mma_commit(&bar[6]);
+            if (tsave) {  // the write-vector gradient, both planes, from the dDelta tile
+                tc::tma_store3(&tm.mdDst, col0, 0, int(2 * chd), sm + B_OFF_DD);
+                tc::bulk_commit();
+            }
             if (ci > c0 && !*abort_flag) {
                 if (!issue_DT(ci - 1)) *abort_flag = 1;
                 else if (ph) pend[1] = -1;
@@ -629,7 +643,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         }
         __syncwarp();
         // while DW runs: the saved write-vector gradient and the next chunk's per-thread operands
-        if (qd < 2 && bwd) {
+        if (qd < 2 && bwd && !tsave) {
             __nv_bfloat16* dst = p.dDelta + chd * 2 * CH * D + size_t(row) * D + col0 + cc;
             tc::st_g_n<VPT>(dst, xh);
             tc::st_g_n<VPT>(dst + CH * D, xl);
@@ -662,6 +676,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         }
     }
 
+    if (tsave && tid == 0) tc::bulk_wait0();  // gradient stores complete before the block ends
     if (*abort_flag) {
         if (tid == 0) {
             tc::drain_mmas(reinterpret_cast<uint64_t*>(sm + B_OFF_BAR + 80), 100000000ull);

@@ -353,6 +353,8 @@ struct TcMaps {
     // stores of the saved set by the 64-column forward recurrence: S_c and Delta_c, both planes of
     // one 64-value block, {64 values, 128 keys or 64 tokens, plane-chunk = 2 chunk-head + plane}
     CUtensorMap mSst, mDst;
+    // the same stores of the backward recurrence's dS1 and dDelta planes (workspace)
+    CUtensorMap mdSst, mdDst;
     // backward intra-chunk inputs: q, k [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens};
     // dAqk, dM [chunk * H + head][64][64] fp32 as 32 x 64 boxes (128-byte swizzle)
     CUtensorMap mq, mk, mdA, mdM;

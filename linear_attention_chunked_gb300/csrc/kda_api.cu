@@ -252,6 +252,18 @@ kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return KDA_ERR_CUDA;
+    {  // fp32 products of the forward intra kernel (TMA stores)
+        const cuuint32_t bF[3] = {32, 64, 1};
+        const cuuint64_t dU[3] = {D, CH, CHd}, sU[2] = {D * 4, size_t(CH) * D * 4};
+        const cuuint64_t dK[3] = {CH, CH, CHd}, sK[2] = {CH * 4, size_t(CH) * CH * 4};
+        if (enc(&tm->mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.U, dU, sU, bF, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            enc(&tm->mAkk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.Akk, dK, sK, bF, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return KDA_ERR_CUDA;
+    }
     if (p.sS) {  // the saved states and write vectors, stored from the recurrence's shared tiles
         const cuuint32_t bS[3] = {64, 128, 2}, bD[3] = {64, 64, 2};
         const cuuint64_t dS[3] = {D, D, 2 * CHd}, sSt[2] = {D * 2, size_t(D) * D * 2};
@@ -448,7 +460,7 @@ void grouped_chain_bwd(const Params& p, const kda_problem* pr, const Layout& L, 
 }
 
 // plan + intra-chunk products (shared by every op)
-kda_status run_prologue(const Params& p, cudaStream_t st) {
+kda_status run_prologue(const Params& p, const TcMaps& tm, cudaStream_t st) {
     {
         ProfScope ps(KK_PLAN, st);
         k_plan<<<1, NTHR, 0, st>>>(p);
@@ -459,7 +471,7 @@ kda_status run_prologue(const Params& p, cudaStream_t st) {
         cudaGetDevice(&dev);
         const long long items = p.maxC * p.H;
         const unsigned grid = unsigned(items < g_sms[dev] ? items : g_sms[dev]);
-        k_intra_fwd<<<grid, INTRA_THREADS, SMEM_INTRA_FWD, st>>>(p);
+        k_intra_fwd<<<grid, INTRA_THREADS, SMEM_INTRA_FWD, st>>>(p, tm);
     }
     return launched();
 }
@@ -529,7 +541,7 @@ kda_status kda_fwd(const kda_problem* pr, const void* q, const void* k, const vo
     else set_saved(p, L, static_cast<char*>(ws) + L.intra_ws, false);
     TcMaps tm{};
     if (kda_status s = make_tc_maps(p, L, &tm)) return s;
-    if (kda_status s = run_prologue(p, st)) return s;
+    if (kda_status s = run_prologue(p, tm, st)) return s;
     if (L.G > 0) {
         char* gbase = static_cast<char*>(ws) + L.g_fwd;
         grouped_chain_fwd(p, pr, L, gbase, saved ? p.gM : reinterpret_cast<float*>(gbase + L.g_M),
@@ -601,7 +613,7 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
         k_plan<<<1, NTHR, 0, st>>>(p);
     } else {
         // checkpoint replay: recompute the intra products, the states and the write vectors
-        if (kda_status s = run_prologue(p, st)) return s;
+        if (kda_status s = run_prologue(p, tm, st)) return s;
         Params r = p;
         r.o = nullptr;
         r.ht = nullptr;
@@ -664,7 +676,7 @@ kda_status kda_fragment_summary(const kda_problem* pr, int mode, const void* q, 
     if (kda_status s = make_tc_maps(p, L, &tm)) return s;
     if (mode == KDA_FRAG_BWD)
         if (kda_status s = make_dO_map(dO, pr->T, pr->H, &tm)) return s;
-    if (kda_status s = run_prologue(p, st)) return s;
+    if (kda_status s = run_prologue(p, tm, st)) return s;
     if (mode == KDA_FRAG_FWD) {
         ProfScope ps(KK_CHAIN_FWD, st);
         launch_chain_fwd_tc(p, CHAIN_FRAG_MB, tm, unsigned(pr->N) * unsigned(pr->H), device_sms(), st);

@@ -355,6 +355,9 @@ struct TcMaps {
     CUtensorMap mSst, mDst;
     // the same stores of the backward recurrence's dS1 and dDelta planes (workspace)
     CUtensorMap mdSst, mdDst;
+    // stores of the forward intra kernel's fp32 products: U [tile][64][128] and Akk [tile][64][64]
+    // as 32 x 64 boxes (128-byte swizzle); its bf16 planes go through m128 / m64
+    CUtensorMap mU, mAkk;
     // backward intra-chunk inputs: q, k [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens};
     // dAqk, dM [chunk * H + head][64][64] fp32 as 32 x 64 boxes (128-byte swizzle)
     CUtensorMap mq, mk, mdA, mdM;
@@ -370,7 +373,7 @@ constexpr int INTRA_THREADS = 512;  // threads of the forward intra-chunk kernel
 constexpr int NHALF = 2;            // value halves (64 columns) per head in the recurrences
 __global__ void k_plan(Params p);
 __global__ void k_group_plan(Params p, GroupPlan gp);
-__global__ void k_intra_fwd(Params p);
+__global__ void k_intra_fwd(Params p, const __grid_constant__ TcMaps tm);
 // state recurrences (value-width templates, launched through these; sms = the device's SMs)
 cudaError_t chain_tc_setup();
 void launch_chain_fwd_tc(const Params& p, int mode, const TcMaps& tm, unsigned pairs, int sms,

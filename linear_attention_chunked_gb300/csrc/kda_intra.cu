@@ -10,27 +10,38 @@
 // without overflow at any decay rate.  Inside a sub-chunk (the diagonal 16x16 blocks) the factor
 // is formed elementwise in FP32.
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
 namespace {
 
 constexpr int LB = 136;  // row stride (bf16 elements) of [rows][128] MMA operand tiles
+// row stride (floats) of the q, k, gam tiles: 8 words of bank offset per row, so the 8-byte
+// fragment reads of step 4c (rows g, columns 2t of a quad-lane layout) meet no bank conflict
+constexpr int LQ = D + 8;
 
+// The base is 1024-byte aligned; so are k, akk_st and u, which double as 128-byte-swizzled
+// staging tiles of the TMA stores of the products: Aqk / Minv hi / lo in k and Akk in akk_st
+// (after step 5), W hi / lo in u (after step 6, until the next item's step 4a).
 struct IntraSmem {
-    float q[CH * LDP], k[CH * LDP], gam[CH * LDP];
-    float Akk[CH * LDA], Aqk[CH * LDA], Mi[CH * LDA];
-    float beta[CH];
-    float T[3][16 * 17];  // blockwise inverse scratch (step 5)
+    float q[CH * LQ], k[CH * LQ], gam[CH * LQ];
+    union {
+        unsigned char akk_st[2 * 8192];  // Akk staged for its TMA store: boxes [64 rows][32 fp32]
+        float P[6][16 * 32];             // partial sums of step 4 (dead before the staging)
+    } x;
     union {
         struct {
             __nv_bfloat16 Ks[3][2][16 * LB];  // B operands of the off-diagonal blocks (hi, lo)
-            float P[6][16 * 32];              // partial off-diagonal sums of the K-split warps
         } a;
         struct {
             __nv_bfloat16 bKg[2][CH * LB];  // beta K e^gam (hi, lo), written during step 5
         } b;
+        unsigned char wst[4 * 8192];  // W staged: boxes [plane][column block] of 64 rows x 64 bf16
     } u;
+    float Akk[CH * LDA], Aqk[CH * LDA], Mi[CH * LDA];
+    float beta[CH];
+    uint4 gfrag[6 * 2 * 32];  // split A fragments of G_il (step 5): [pair][hi, lo][lane]
     __nv_bfloat16 v[CH * LB];  // V (exact in bf16)
 };
 
@@ -38,10 +49,19 @@ struct IntraSmem {
 __constant__ int2 kPairs[6] = {{1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
 
 
-static_assert(sizeof(IntraSmem) <= 232448, "intra shared memory above the opt-in limit");
+static_assert(sizeof(IntraSmem) + 1024 <= 232448, "intra shared memory above the opt-in limit");
+static_assert(offsetof(IntraSmem, k) % 1024 == 0 && offsetof(IntraSmem, x) % 1024 == 0 &&
+                  offsetof(IntraSmem, u) % 1024 == 0 && CH * LQ * 4 >= 4 * 8192,
+              "staging tiles of the TMA stores must be 1024-byte aligned and hold four boxes");
+
+// Byte offset of (row, byte) inside a box of 64 rows x 128 bytes in the TMA unit's 128-byte
+// swizzle: the 16-byte chunk j of row r sits at chunk position j ^ (r % 8).
+__device__ __forceinline__ int sw128(int row, int byte) {
+    return row * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
+}
 
 __device__ __forceinline__ float4 row4(const float* t, int r, int c4) {
-    return *reinterpret_cast<const float4*>(t + r * LDP + c4);
+    return *reinterpret_cast<const float4*>(t + r * LQ + c4);
 }
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
@@ -87,27 +107,33 @@ __device__ __forceinline__ void diag_pair_sums(const float* q, const float* k, c
 
 }  // namespace
 
-size_t intra_smem_bytes() { return sizeof(IntraSmem); }
+size_t intra_smem_bytes() { return sizeof(IntraSmem) + 1024; }  // + alignment slack of the base
 
 // Persistent: one block per SM walks the (chunk, head) items item = chunk * H + head; the raw
 // inputs of its next item are loaded into registers while the current one is computed, in three
-// bursts (q, k, then the gate) so that no burst fills the memory request queue of the SM.
-__global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
+// bursts (q, k, then the gate) so that no burst fills the memory request queue of the SM.  The
+// hi / lo planes of Aqk, Minv and W and Akk leave through TMA stores from staging tiles (thread 0
+// issues them and waits for their reads of shared memory before the tiles are rewritten): the
+// small matrices' stores run during step 6, W's during the next item's first steps.
+__global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const __grid_constant__ TcMaps tm) {
     constexpr int BT = INTRA_THREADS, NW = BT / 32;
     extern __shared__ __align__(16) unsigned char smraw[];
-    IntraSmem& S = *reinterpret_cast<IntraSmem*>(smraw);
+    // 1024-byte aligned base (offset arithmetic on the shared array keeps its address space known)
+    IntraSmem& S = *reinterpret_cast<IntraSmem*>(smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const int items = *p.nchunks * p.H;
     const int c4t = (tid & 31) * 4;  // the gate channels of this thread (every k below)
 
-    // raw inputs of the next item (rows past the document end read as zero): q, k, gate, beta in
-    // registers; v goes to its shared tile with cp.async once the current item no longer needs it
+    // raw inputs of the next item (rows past the document end read as zero): q, k, beta in
+    // registers; the gate and v go to their shared tiles with cp.async once the current item no
+    // longer needs them (gam after step 5, v after step 6)
     uint4 pq[2], pk[2];
-    float4 pg[4], pdb = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 pdb = make_float4(0.f, 0.f, 0.f, 0.f);
     float pb = 0.f, peA = 0.f;
     int nT0 = 0, nL = 0, nh = 0;  // first token, length and head of the next item
     int4 tab_ahead = make_int4(0, 0, 0, 0);  // chunk-table entry of the item after the next
-    // parts: bit 0 q, bit 1 k, bit 2 gate / beta / gate parameters / next chunk-table entry
+    // parts: bit 0 q, bit 1 k, bit 2 gate (cp.async into gam, one commit group) / beta / gate
+    // parameters / next chunk-table entry
     auto fetch = [&](int item, int4 inf, int parts) {
         const int hh = item % p.H;
         const int T0 = inf.y, Ln = inf.z;
@@ -124,11 +150,12 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         }
         if (!(parts & 4)) return;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 4; ++k) {  // the thread's own rows of step 1 (no barrier needed there)
             const int r = (tid + BT * k) >> 5;
-            pg[k] = r < Ln ? *reinterpret_cast<const float4*>(p.g + (size_t(T0 + r) * p.H + hh) * D + c4t)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool ok = r < Ln;
+            cp16z(&S.gam[r * LQ + c4t], p.g + (size_t(T0 + (ok ? r : 0)) * p.H + hh) * D + c4t, ok);
         }
+        cp_commit();
         if (tid < CH) pb = tid < Ln ? bf2f(p.beta[size_t(T0 + tid) * p.H + hh]) : 0.f;
         if (p.gate_raw) {
             pdb = *reinterpret_cast<const float4*>(p.dt_bias + hh * D + c4t);
@@ -172,8 +199,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
                 fk[2 * j] = b.x;
                 fk[2 * j + 1] = b.y;
             }
-            float4* dq = reinterpret_cast<float4*>(&S.q[r * LDP + c8]);
-            float4* dk = reinterpret_cast<float4*>(&S.k[r * LDP + c8]);
+            float4* dq = reinterpret_cast<float4*>(&S.q[r * LQ + c8]);
+            float4* dk = reinterpret_cast<float4*>(&S.k[r * LQ + c8]);
             dq[0] = make_float4(fq[0], fq[1], fq[2], fq[3]);
             dq[1] = make_float4(fq[4], fq[5], fq[6], fq[7]);
             dk[0] = make_float4(fk[0], fk[1], fk[2], fk[3]);
@@ -181,10 +208,12 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         }
         const float eA = p.gate_raw ? expf(peA) : 0.f;
         bool bad_gate = false;
+        cp_wait<1>();  // this item's gate rows (this thread's copies; the v tile may still be in flight)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
-            float x[4] = {pg[k].x, pg[k].y, pg[k].z, pg[k].w};
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LQ + c4t]);
+            float x[4] = {g4.x, g4.y, g4.z, g4.w};
             const float b4[4] = {pdb.x, pdb.y, pdb.z, pdb.w};
             if (p.gate_raw) {
 #pragma unroll
@@ -194,7 +223,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) bad_gate |= !(x[j] <= 0.f);
             }
-            *reinterpret_cast<float4*>(&S.gam[r * LDP + c4t]) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(&S.gam[r * LQ + c4t]) = make_float4(x[0], x[1], x[2], x[3]);
         }
         // reported in the status word; the state recurrences and backward kernels of this call
         // then do nothing
@@ -213,7 +242,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         for (int r = warp; r < CH; r += NW) {
             float a = 0.f, b = 0.f;
             for (int c = lane; c < D; c += 32) {
-                const float x = S.q[r * LDP + c], y = S.k[r * LDP + c];
+                const float x = S.q[r * LQ + c], y = S.k[r * LQ + c];
                 a = fmaf(x, x, a);
                 b = fmaf(y, y, b);
             }
@@ -221,8 +250,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
             b = warp_sum(b);
             const float ra = 1.f / sqrtf(a + p.eps), rb = 1.f / sqrtf(b + p.eps);
             for (int c = lane; c < D; c += 32) {
-                S.q[r * LDP + c] *= ra;
-                S.k[r * LDP + c] *= rb;
+                S.q[r * LQ + c] *= ra;
+                S.k[r * LQ + c] *= rb;
             }
         }
     }
@@ -232,17 +261,18 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         float run = 0.f;
 #pragma unroll
         for (int r = r0; r < r0 + 16; ++r) {
-            run += S.gam[r * LDP + c];
-            S.gam[r * LDP + c] = run;
+            run += S.gam[r * LQ + c];
+            S.gam[r * LQ + c] = run;
         }
         __syncthreads();
         float carry = 0.f;
-        for (int q2 = 0; q2 < qu; ++q2) carry += S.gam[(16 * q2 + 15) * LDP + c];
+        for (int q2 = 0; q2 < qu; ++q2) carry += S.gam[(16 * q2 + 15) * LQ + c];
         __syncthreads();
         if (qu > 0)
 #pragma unroll
-            for (int r = r0; r < r0 + 16; ++r) S.gam[r * LDP + c] += carry;
+            for (int r = r0; r < r0 + 16; ++r) S.gam[r * LQ + c] += carry;
     }
+    if (tid == 0) tc::bulk_wait_read0();  // the previous item's W store has read u (written in 4a)
     __syncthreads();
 
     // 4a. diagonal 8x8 blocks (the lower-left 8x8 quadrant of each 16-row sub-chunk runs on tensor
@@ -267,7 +297,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
                 akk[j] += __shfl_xor_sync(0xffffffffu, akk[j], o);
                 aqk[j] += __shfl_xor_sync(0xffffffffu, aqk[j], o);
             }
-        float* part = &S.u.a.P[0][0];  // [channel half][block][row pair][9 akk | 9 aqk]
+        float* part = &S.x.P[0][0];  // [channel half][block][row pair][9 akk | 9 aqk]
         if (cg == 0) {
 #pragma unroll
             for (int j = 0; j < 9; ++j) {
@@ -282,7 +312,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         const int rB = 7 - rp, rA = rp;
         const bool rowB = j <= rB;
         const int r = 8 * b + (rowB ? rB : rA), sc = 8 * b + (rowB ? rB - j : rA - (j - rB - 1));
-        const float* p0 = &S.u.a.P[0][0] + (b * 4 + rp) * 18;
+        const float* p0 = &S.x.P[0][0] + (b * 4 + rp) * 18;
         const float* p1 = p0 + 8 * 4 * 18;
         if (sc < r) S.Akk[r * LDA + sc] = p0[j] + p1[j];
         S.Aqk[r * LDA + sc] = p0[9 + j] + p1[9 + j];
@@ -291,7 +321,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     for (int idx = tid; idx < 3 * 16 * D; idx += BT) {
         const int j = idx / (16 * D), rem = idx % (16 * D), sl = rem / D, c = rem % D;
         const int s = 16 * j + sl, e = 16 * j + 15;
-        const float x = S.k[s * LDP + c] * __expf(S.gam[e * LDP + c] - S.gam[s * LDP + c]);
+        const float x = S.k[s * LQ + c] * __expf(S.gam[e * LQ + c] - S.gam[s * LQ + c]);
         const __nv_bfloat16 hi = __float2bfloat16_rn(x);
         S.u.a.Ks[j][0][sl * LB + c] = hi;
         S.u.a.Ks[j][1][sl * LB + c] = __float2bfloat16_rn(x - __bfloat162float(hi));
@@ -310,10 +340,10 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
 #pragma unroll
             for (int rr = 1; rr < 4; rr += 2) {  // rows 16b + 8 + g; rows 16b + g stay zero
                 const int row = 16 * b + 8 + g, col = 16 * ks + 2 * t + 8 * (rr >> 1);
-                const float2 gr = *reinterpret_cast<const float2*>(&S.gam[row * LDP + col]);
-                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LDP + col]);
-                const float2 qv = *reinterpret_cast<const float2*>(&S.q[row * LDP + col]);
-                const float2 kv = *reinterpret_cast<const float2*>(&S.k[row * LDP + col]);
+                const float2 gr = *reinterpret_cast<const float2*>(&S.gam[row * LQ + col]);
+                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LQ + col]);
+                const float2 qv = *reinterpret_cast<const float2*>(&S.q[row * LQ + col]);
+                const float2 kv = *reinterpret_cast<const float2*>(&S.k[row * LQ + col]);
                 const float e0 = __expf(gr.x - ge.x), e1 = __expf(gr.y - ge.y);
                 split2(qv.x * e0, qv.y * e1, qh[rr], ql[rr]);
                 split2(kv.x * e0, kv.y * e1, kh4[rr], kl[rr]);
@@ -322,9 +352,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {  // B[k = channel][n = s]: k[s][c] exp(gam_e - gam_s)
                 const int sr = 16 * b + g, c = 16 * ks + 2 * t + 8 * hf;
-                const float2 gs = *reinterpret_cast<const float2*>(&S.gam[sr * LDP + c]);
-                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LDP + c]);
-                const float2 kv = *reinterpret_cast<const float2*>(&S.k[sr * LDP + c]);
+                const float2 gs = *reinterpret_cast<const float2*>(&S.gam[sr * LQ + c]);
+                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LQ + c]);
+                const float2 kv = *reinterpret_cast<const float2*>(&S.k[sr * LQ + c]);
                 split2(kv.x * __expf(ge.x - gs.x), kv.y * __expf(ge.y - gs.y), bh[hf], bl[hf]);
             }
             mma_x3(accQ, qh, ql, bh[0], bh[1], bl[0], bl[1]);
@@ -346,10 +376,10 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const int row = 16 * i + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
-                const float2 gr = *reinterpret_cast<const float2*>(&S.gam[row * LDP + col]);
-                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LDP + col]);
-                const float2 qv = *reinterpret_cast<const float2*>(&S.q[row * LDP + col]);
-                const float2 kv = *reinterpret_cast<const float2*>(&S.k[row * LDP + col]);
+                const float2 gr = *reinterpret_cast<const float2*>(&S.gam[row * LQ + col]);
+                const float2 ge = *reinterpret_cast<const float2*>(&S.gam[e * LQ + col]);
+                const float2 qv = *reinterpret_cast<const float2*>(&S.q[row * LQ + col]);
+                const float2 kv = *reinterpret_cast<const float2*>(&S.k[row * LQ + col]);
                 const float e0 = __expf(gr.x - ge.x), e1 = __expf(gr.y - ge.y);
                 split2(qv.x * e0, qv.y * e1, qh[rr], ql[rr]);
                 split2(kv.x * e0, kv.y * e1, kh4[rr], kl[rr]);
@@ -363,7 +393,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
                 mma_x3(accK[nt], kh4, kl, bh[2 * nt], bh[2 * nt + 1], bl[2 * nt], bl[2 * nt + 1]);
             }
         }
-        float* part = S.u.a.P[pr];  // upper half's partial [2 n-tiles][2 (Q, K)][4] per lane
+        float* part = S.x.P[pr];  // upper half's partial [2 n-tiles][2 (Q, K)][4] per lane
         if (kh == 1) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -391,8 +421,10 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
     int4 tab_next = tab_ahead;  // (the g part below overwrites tab_ahead)
     if (more) fetch(item + gridDim.x, tab_next, 1);
 
-    // 5. Minv = (I + diag(beta) Akk)^-1, blockwise: 16x16 diagonal inverses by substitution, then
-    //    X_ij = -D_i sum_{l=j}^{i-1} diag(beta_i) Akk_il X_lj by increasing block distance
+    // 5. Minv = (I + diag(beta) Akk)^-1, blockwise: 16x16 diagonal inverses D_i by substitution,
+    //    then on tensor cores (split-bf16 products) G_il = -D_i diag(beta_i) Akk_il for i > l and
+    //    the blocks off the diagonal X_ij = sum_{l=j}^{i-1} G_il X_lj (X_jj = D_j) by increasing
+    //    block distance
     if (tid >= 64) {
         // meanwhile, the other warps form step 6's operand beta K e^gam (hi, lo) (Ks and the
         // partial sums it overwrites were consumed in step 4) and the elementwise outputs of the
@@ -402,12 +434,13 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         __nv_bfloat16* Kh = p.Kh + chd * CH * D;
         __nv_bfloat16* Kl = p.Kl + chd * CH * D;
         float* gam = p.gam + chd * CH * D;
+        if (tid - 64 < D) p.eGL[chd * D + tid - 64] = __expf(S.gam[(CH - 1) * LQ + tid - 64]);
         for (int i = tid - 64; i < CH * D / 2; i += BT - 64) {
             const int r = (2 * i) / D, c = (2 * i) % D;
-            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LDP + c]);
-            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LDP + c]);
-            const float2 gl = *reinterpret_cast<const float2*>(&S.gam[(CH - 1) * LDP + c]);
-            const float2 qv = *reinterpret_cast<const float2*>(&S.q[r * LDP + c]);
+            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LQ + c]);
+            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LQ + c]);
+            const float2 gl = *reinterpret_cast<const float2*>(&S.gam[(CH - 1) * LQ + c]);
+            const float2 qv = *reinterpret_cast<const float2*>(&S.q[r * LQ + c]);
             const float e0 = __expf(gv.x), e1 = __expf(gv.y);
             uint32_t hi, lo;
             split2(S.beta[r] * kv.x * e0, S.beta[r] * kv.y * e1, hi, lo);
@@ -436,35 +469,82 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         for (int rl = 0; rl < 16; ++rl) S.Mi[(16 * b + rl) * LDA + c] = x[rl];
     }
     __syncthreads();
+    // G_il, pair w = i (i - 1) / 2 + l on warp w < 6: A = D_i, B = diag(beta_i) Akk_il (both
+    // n-tiles, so the accumulator is already G's A fragment)
+    if (warp < 6) {
+        const int i = warp < 1 ? 1 : warp < 3 ? 2 : 3, l = warp - i * (i - 1) / 2;
+        uint32_t dh[4], dl[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int row = 16 * i + g + 8 * (rr & 1), col = 16 * i + 2 * t + 8 * (rr >> 1);
+            split2(S.Mi[row * LDA + col], S.Mi[row * LDA + col + 1], dh[rr], dl[rr]);
+        }
+        float acc[2][4] = {};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t bh[2], bl[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int kr = 16 * i + 2 * t + 8 * hf, n = 16 * l + 8 * nt + g;
+                split2(S.beta[kr] * S.Akk[kr * LDA + n], S.beta[kr + 1] * S.Akk[(kr + 1) * LDA + n],
+                       bh[hf], bl[hf]);
+            }
+            mma_x3(acc[nt], dh, dl, bh[0], bh[1], bl[0], bl[1]);
+        }
+        uint32_t h[4], lo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) split2(-acc[q >> 1][2 * (q & 1)], -acc[q >> 1][2 * (q & 1) + 1], h[q], lo[q]);
+        S.gfrag[(2 * warp) * 32 + lane] = make_uint4(h[0], h[1], h[2], h[3]);
+        S.gfrag[(2 * warp + 1) * 32 + lane] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    __syncthreads();
+    // X_ij for j = 0 .. 3 - dist, i = j + dist: warp = (j, 8-column n-tile)
 #pragma unroll
     for (int dist = 1; dist < 4; ++dist) {
-        const int nb = 4 - dist;
-        for (int idx = tid; idx < nb * 256; idx += BT) {
-            const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
-            const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
-            float a0 = 0.f, a1 = 0.f;
+        if (warp < 2 * (4 - dist)) {
+            const int j = warp >> 1, i = j + dist, n = 16 * j + 8 * (warp & 1) + g;
+            float acc[4] = {};
 #pragma unroll
-            for (int l = 0; l < 16 * dist; l += 2) {
-                a0 = fmaf(S.Akk[r * LDA + 16 * jb + l], S.Mi[(16 * jb + l) * LDA + c], a0);
-                a1 = fmaf(S.Akk[r * LDA + 16 * jb + l + 1], S.Mi[(16 * jb + l + 1) * LDA + c], a1);
-            }
-            S.T[b][rl * 17 + cl] = S.beta[r] * (a0 + a1);
-        }
-        __syncthreads();
-        for (int idx = tid; idx < nb * 256; idx += BT) {
-            const int b = idx >> 8, e = idx & 255, rl = e >> 4, cl = e & 15;
-            const int jb = b, ib = b + dist, r = 16 * ib + rl, c = 16 * jb + cl;
-            float a0 = 0.f, a1 = 0.f;
+            for (int l = j; l < i; ++l) {
+                const int pr = i * (i - 1) / 2 + l;
+                const uint4 fh = S.gfrag[(2 * pr) * 32 + lane], fl = S.gfrag[(2 * pr + 1) * 32 + lane];
+                const uint32_t ah[4] = {fh.x, fh.y, fh.z, fh.w}, al[4] = {fl.x, fl.y, fl.z, fl.w};
+                uint32_t bh[2], bl[2];
 #pragma unroll
-            for (int sl = 0; sl < 16; sl += 2) {
-                a0 = fmaf(S.Mi[r * LDA + 16 * ib + sl], S.T[b][sl * 17 + cl], a0);
-                a1 = fmaf(S.Mi[r * LDA + 16 * ib + sl + 1], S.T[b][(sl + 1) * 17 + cl], a1);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int kr = 16 * l + 2 * t + 8 * hf;
+                    split2(S.Mi[kr * LDA + n], S.Mi[(kr + 1) * LDA + n], bh[hf], bl[hf]);
+                }
+                mma_x3(acc, ah, al, bh[0], bh[1], bl[0], bl[1]);
             }
-            S.Mi[r * LDA + c] = -(a0 + a1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                S.Mi[(16 * i + g + 8 * (e >> 1)) * LDA + 16 * j + 8 * (warp & 1) + 2 * t + (e & 1)] = acc[e];
         }
         __syncthreads();
     }
 
+    if (more) fetch(item + gridDim.x, tab_next, 4);  // gam is free: the next item's gate
+
+    // 7 (ahead of step 6). The small matrices, staged for TMA stores whose reads of shared memory
+    //    overlap step 6: Aqk and Minv hi / lo in the k tile (boxes Ah, Al, Mh, Ml of 64 rows x 64
+    //    bf16; k is not read after step 5), Akk in akk_st (the elementwise outputs were written
+    //    during step 5)
+    {
+        unsigned char* ast = reinterpret_cast<unsigned char*>(S.k);
+        for (int i = tid; i < CH * CH / 2; i += BT) {
+            const int r = (2 * i) / CH, s = (2 * i) % CH, o = sw128(r, 2 * s);
+            uint32_t hi, lo;
+            split2(S.Aqk[r * LDA + s], S.Aqk[r * LDA + s + 1], hi, lo);
+            *reinterpret_cast<uint32_t*>(ast + o) = hi;
+            *reinterpret_cast<uint32_t*>(ast + 8192 + o) = lo;
+            split2(S.Mi[r * LDA + s], S.Mi[r * LDA + s + 1], hi, lo);
+            *reinterpret_cast<uint32_t*>(ast + 2 * 8192 + o) = hi;
+            *reinterpret_cast<uint32_t*>(ast + 3 * 8192 + o) = lo;
+            *reinterpret_cast<float2*>(S.x.akk_st + (s >> 5) * 8192 + sw128(r, (s & 31) * 4)) =
+                make_float2(S.Akk[r * LDA + s], S.Akk[r * LDA + s + 1]);
+        }
+    }
     // split A fragments of Minv and Minv diag(beta), built once per lower 16 x 16 block (mt, ks)
     // by warp mt (mt + 1) / 2 + ks (four warps of step 6 share each block), into the q tile,
     // which nothing reads after step 5: [block][Minv hi, lo, Minv diag(beta) hi, lo][lane]
@@ -486,76 +566,92 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p) {
         f[64] = make_uint4(bh_[0], bh_[1], bh_[2], bh_[3]);
         f[96] = make_uint4(bl_[0], bl_[1], bl_[2], bl_[3]);
     }
-    cp_wait<0>();  // this item's v tile (copied during the previous item's last phase)
+    // this item's v tile (copied during the previous item's last phase; the next gate may stay in
+    // flight)
+    if (more)
+        cp_wait<1>();
+    else
+        cp_wait<0>();
     if (more) fetch(item + gridDim.x, tab_next, 2);
-    __syncthreads();  // every thread's part of the v tile, the Minv fragments
-
-    // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores
-    {
-        const int mt = warp & 3, nq = warp >> 2;  // rows 16 mt.., columns 32 nq..
-        float accW[4][4] = {}, accU[4][4] = {};
-        for (int ks = 0; ks <= mt; ++ks) {  // Minv is lower triangular
-            const uint4* f = mfrag + (mt * (mt + 1) / 2 + ks) * 4 * 32 + lane;
-            const uint4 a0 = f[0], a1 = f[32], a2 = f[64], a3 = f[96];
-            const uint32_t mh[4] = {a0.x, a0.y, a0.z, a0.w}, ml[4] = {a1.x, a1.y, a1.z, a1.w};
-            const uint32_t bh_[4] = {a2.x, a2.y, a2.z, a2.w}, bl_[4] = {a3.x, a3.y, a3.z, a3.w};
+    tc::fence_async_smem();  // this thread's staged values, before the TMA unit reads them
+    __syncthreads();  // every thread's part of the v tile, the Minv fragments, the staged matrices
+    if (tid == 0) {
+        const int z[4] = {tm.zAh, tm.zAl, tm.zMh, tm.zMl};
 #pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                uint32_t kh[4], kl[4], vv[4];
-                const int n0 = 32 * nq + 16 * np;
-                ldsm4t(kh, bk_addr(S.u.b.bKg[0], LB, 16 * ks, n0, lane));
-                ldsm4t(kl, bk_addr(S.u.b.bKg[1], LB, 16 * ks, n0, lane));
-                ldsm4t(vv, bk_addr(S.v, LB, 16 * ks, n0, lane));
+        for (int b = 0; b < 4; ++b)
+            tc::tma_store3(&tm.m64, 0, 0, z[b] + int(chd), reinterpret_cast<unsigned char*>(S.k) + b * 8192);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) tc::tma_store3(&tm.mAkk, 32 * b, 0, int(chd), S.x.akk_st + b * 8192);
+        tc::bulk_commit();
+    }
+
+    // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores.  Minv is lower
+    //    triangular, so row block mt takes mt + 1 k-steps; a warp takes the row blocks {0, 3} or
+    //    {1, 2} (five k-steps either way) over 16 columns.
+    {
+        const int m0 = (warp & 1) ? 1 : 0, m1 = 3 - m0, n0 = 16 * (warp >> 1);
+        float accW[2][2][4] = {}, accU[2][2][4] = {};  // [row block m0 / m1][n-tile][fragment]
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            if (ks > m1) break;
+            uint32_t kh[4], kl[4], vv[4];
+            ldsm4t(kh, bk_addr(S.u.b.bKg[0], LB, 16 * ks, n0, lane));
+            ldsm4t(kl, bk_addr(S.u.b.bKg[1], LB, 16 * ks, n0, lane));
+            ldsm4t(vv, bk_addr(S.v, LB, 16 * ks, n0, lane));
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                const int mt = bi ? m1 : m0;
+                if (ks > mt) continue;
+                const uint4* f = mfrag + (mt * (mt + 1) / 2 + ks) * 4 * 32 + lane;
+                const uint4 a0 = f[0], a1 = f[32], a2 = f[64], a3 = f[96];
+                const uint32_t mh[4] = {a0.x, a0.y, a0.z, a0.w}, ml[4] = {a1.x, a1.y, a1.z, a1.w};
+                const uint32_t bh_[4] = {a2.x, a2.y, a2.z, a2.w}, bl_[4] = {a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    mma_x3(accW[2 * np + hh], mh, ml, kh[2 * hh], kh[2 * hh + 1], kl[2 * hh],
-                           kl[2 * hh + 1]);
-                    mma_x2(accU[2 * np + hh], bh_, bl_, vv[2 * hh], vv[2 * hh + 1]);
+                    mma_x3(accW[bi][hh], mh, ml, kh[2 * hh], kh[2 * hh + 1], kl[2 * hh], kl[2 * hh + 1]);
+                    mma_x2(accU[bi][hh], bh_, bl_, vv[2 * hh], vv[2 * hh + 1]);
                 }
             }
         }
-        __nv_bfloat16* Wh = p.Wh + chd * CH * D;
-        __nv_bfloat16* Wl = p.Wl + chd * CH * D;
         float* U = p.U + chd * CH * D;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int bi = 0; bi < 2; ++bi)
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int row = 16 * mt + g + 8 * hf, col = 32 * nq + 8 * nt + 2 * t;
-                uint32_t hi, lo;
-                split2(accW[nt][2 * hf], accW[nt][2 * hf + 1], hi, lo);
-                *reinterpret_cast<uint32_t*>(Wh + row * D + col) = hi;
-                *reinterpret_cast<uint32_t*>(Wl + row * D + col) = lo;
-                *reinterpret_cast<float2*>(U + row * D + col) =
-                    make_float2(accU[nt][2 * hf], accU[nt][2 * hf + 1]);
-            }
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int row = 16 * (bi ? m1 : m0) + g + 8 * hf, col = n0 + 8 * hh + 2 * t;
+                    *reinterpret_cast<float2*>(U + row * D + col) =
+                        make_float2(accU[bi][hh][2 * hf], accU[bi][hh][2 * hf + 1]);
+                }
+        __syncthreads();  // every warp's reads of bKg are done: u becomes W's staging tile
+#pragma unroll
+        for (int bi = 0; bi < 2; ++bi)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int row = 16 * (bi ? m1 : m0) + g + 8 * hf, col = n0 + 8 * hh + 2 * t;
+                    uint32_t hi, lo;
+                    split2(accW[bi][hh][2 * hf], accW[bi][hh][2 * hf + 1], hi, lo);
+                    const int wo = (col >> 6) * 8192 + sw128(row, (col & 63) * 2);
+                    *reinterpret_cast<uint32_t*>(S.u.wst + wo) = hi;
+                    *reinterpret_cast<uint32_t*>(S.u.wst + 2 * 8192 + wo) = lo;
+                }
     }
-
-    if (more) fetch(item + gridDim.x, tab_next, 4);
-
-    // 7. the small matrices (the elementwise outputs were written during step 5)
-    {
-        __nv_bfloat16* Ah = p.Ah + chd * CH * CH;
-        __nv_bfloat16* Al = p.Al + chd * CH * CH;
-        __nv_bfloat16* Mh = p.Mh + chd * CH * CH;
-        __nv_bfloat16* Ml = p.Ml + chd * CH * CH;
-        float* Akk = p.Akk + chd * CH * CH;
-        for (int i = tid; i < CH * CH / 2; i += BT) {
-            const int r = (2 * i) / CH, s = (2 * i) % CH;
-            uint32_t hi, lo;
-            split2(S.Aqk[r * LDA + s], S.Aqk[r * LDA + s + 1], hi, lo);
-            reinterpret_cast<uint32_t*>(Ah)[i] = hi;
-            reinterpret_cast<uint32_t*>(Al)[i] = lo;
-            split2(S.Mi[r * LDA + s], S.Mi[r * LDA + s + 1], hi, lo);
-            reinterpret_cast<uint32_t*>(Mh)[i] = hi;
-            reinterpret_cast<uint32_t*>(Ml)[i] = lo;
-            reinterpret_cast<float2*>(Akk)[i] = make_float2(S.Akk[r * LDA + s], S.Akk[r * LDA + s + 1]);
-        }
-        if (tid < D) p.eGL[chd * D + tid] = __expf(S.gam[(CH - 1) * LDP + tid]);
+    tc::fence_async_smem();
+    if (tid == 0) tc::bulk_wait_read0();  // the small matrices' stores have read k and akk_st
+    __syncthreads();  // W staged; every thread is done with this item's shared tiles
+    if (tid == 0) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            tc::tma_store3(&tm.m128, 64 * (b & 1), 0, ((b >> 1) ? tm.zWl : tm.zWh) + int(chd),
+                           S.u.wst + b * 8192);
+        tc::bulk_commit();
     }
-    __syncthreads();  // the next item overwrites the shared tiles
     if (more) fetch_v();
     }
+    if (tid == 0) tc::bulk_wait0();  // the stores are complete before the block ends
 }
 
 }  // namespace kda

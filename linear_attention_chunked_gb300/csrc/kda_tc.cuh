@@ -146,7 +146,7 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
-// (tensor-core operand fetches).
+// (tensor-core operand fetches, TMA stores).
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -35,29 +35,6 @@ __host__ __device__ constexpr int ds1_tile(int pl, int kb) {
     return pl == 0 ? 16384 * kb : (kb == 0 ? 32768 : G_X);
 }
 
-// Stores v, columns 0..31 of this thread's row at dst (row stride ld floats), so that every warp
-// store fills whole 32-byte sectors: the lanes 2k, 2k + 1 (rows r, r + 1) swap 16-byte chunks and
-// each store writes 32 contiguous bytes of one row per lane pair (one row per thread would fill
-// half a sector per lane and take twice the sector writes).
-__device__ __forceinline__ void st_row32_pairs(float* dst, int ld, const float (&v)[32], int lane) {
-    const bool odd = lane & 1;
-    float* d0 = odd ? dst - ld + 4 : dst;  // row r (even lane's), this lane's chunk of each pair
-    float* d1 = odd ? dst + 4 : dst + ld;  // row r + 1
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 ce = make_float4(v[8 * i], v[8 * i + 1], v[8 * i + 2], v[8 * i + 3]);
-        const float4 co = make_float4(v[8 * i + 4], v[8 * i + 5], v[8 * i + 6], v[8 * i + 7]);
-        const float4 snd = odd ? ce : co;
-        float4 rcv;
-        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, 1);
-        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, 1);
-        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, 1);
-        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, 1);
-        reinterpret_cast<float4*>(d0 + 8 * i)[0] = odd ? rcv : ce;
-        reinterpret_cast<float4*>(d1 + 8 * i)[0] = odd ? co : rcv;
-    }
-}
-
 }  // namespace
 
 size_t bwd_gemm_tc_smem_bytes() { return BWD_GEMM_TC_SMEM; }
@@ -171,7 +148,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
             for (int q2 = 0; q2 < 2; ++q2) {
                 float v[32];
                 tc::tmem_ld32(tl + 64 * half + 32 * q2, v);
-                st_row32_pairs(dst + 32 * q2, D, v, lane);
+                tc::st_rows_paired_f32<32>(dst + 32 * q2, D, v, lane, true, true);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {  // 16-byte chunk 4 q2 + j of this row's K-block row
                     uint32_t hi[4], lo[4];
@@ -286,7 +263,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
                 tc::tmem_ld32(tl + 128 + 64 * half + 32 * q2, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] *= sc;
-                st_row32_pairs(dst + 32 * q2, D, v, lane);
+                tc::st_rows_paired_f32<32>(dst + 32 * q2, D, v, lane, true, true);
             }
             float v[32];
             tc::tmem_ld32(tl + 256 + 32 * half, v);
@@ -296,7 +273,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
                 const int s = 32 * half + j;
                 v[j] = top ? (s < r ? -v[j] : 0.f) : (s <= r ? p.scale * v[j] : 0.f);
             }
-            st_row32_pairs(da, CH, v, lane);
+            tc::st_rows_paired_f32<32>(da, CH, v, lane, true, true);
         }
         if (qd < 2) {
             float* dst = p.dKb + size_t(chd) * CH * D + size_t(row) * D + 64 * half;
@@ -304,7 +281,7 @@ __global__ void __launch_bounds__(NTHR, 1) k_bwd_gemms_tc(Params p, const __grid
             for (int q2 = 0; q2 < 2; ++q2) {
                 float v[32];
                 tc::tmem_ld32(tl + 320 + 64 * half + 32 * q2, v);
-                st_row32_pairs(dst + 32 * q2, D, v, lane);
+                tc::st_rows_paired_f32<32>(dst + 32 * q2, D, v, lane, true, true);
             }
         }
         tc::fence_before_sync();  // TMEM reads above come before the next item's MMAs

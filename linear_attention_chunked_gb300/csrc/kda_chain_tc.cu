@@ -306,23 +306,27 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (want_o && qd >= 2) {
             float v[VPT];
             tc::tmem_ld<VPT>(tD1 + cc, v);
-            const int t = row - 64;
-            if (t < info.z) {
-                const size_t off = (size_t(info.y + t) * p.H + h) * D + col0 + cc;
-                if (p.out_fp32) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + off);
 #pragma unroll
-                    for (int j = 0; j < VPT / 4; ++j)
-                        dst[j] = make_float4(p.scale * v[4 * j], p.scale * v[4 * j + 1],
-                                             p.scale * v[4 * j + 2], p.scale * v[4 * j + 3]);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + off);
+            for (int j = 0; j < VPT; ++j) v[j] *= p.scale;
+            // token rows of this lane and of its pair (lanes 2k, 2k + 1 store together)
+            const int t = row - 64, te = t & ~1;
+            const size_t off = (size_t(info.y + t) * p.H + h) * D + col0 + cc;
+            const size_t ldt = size_t(p.H) * D;  // token stride in elements
+            if (p.out_fp32) {
+                tc::st_rows_paired_f32<VPT>(static_cast<float*>(p.o) + off, ldt, v, lane,
+                                            te < info.z, te + 1 < info.z);
+            } else {
+                uint4 c[VPT / 8];
 #pragma unroll
-                    for (int j = 0; j < VPT / 8; ++j)
-                        dst[j] = make_uint4(pack2(p.scale * v[8 * j], p.scale * v[8 * j + 1]),
-                                            pack2(p.scale * v[8 * j + 2], p.scale * v[8 * j + 3]),
-                                            pack2(p.scale * v[8 * j + 4], p.scale * v[8 * j + 5]),
-                                            pack2(p.scale * v[8 * j + 6], p.scale * v[8 * j + 7]));
+                for (int j = 0; j < VPT / 8; ++j)
+                    c[j] = make_uint4(pack2(v[8 * j], v[8 * j + 1]), pack2(v[8 * j + 2], v[8 * j + 3]),
+                                      pack2(v[8 * j + 4], v[8 * j + 5]), pack2(v[8 * j + 6], v[8 * j + 7]));
+                if constexpr (VPT >= 16) {
+                    tc::st_rows_paired<VPT / 8>(
+                        reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.o) + off), ldt / 2, c,
+                        lane, te < info.z, te + 1 < info.z);
+                } else if (t < info.z) {
+                    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + off)[0] = c[0];
                 }
             }
         }

@@ -286,6 +286,43 @@ __device__ __forceinline__ void st_g_n(__nv_bfloat16* dst, const uint32_t (&x)[N
     for (int j = 0; j < N / 8; ++j)
         reinterpret_cast<uint4*>(dst)[j] = make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
 }
+// Row stores from a warp whose lane i holds row r0 + i (as after a 32x32b tcgen05.ld): the lane
+// pairs (2k, 2k + 1) swap 16-byte chunks so that every warp store writes 32 contiguous bytes of
+// one row per pair -- whole 32-byte sectors, where one row per lane fills half a sector per
+// lane and takes twice the sector writes.  `own` points at this lane's row segment of NC chunks
+// (NC even), `ld` is the row stride in 32-bit words; ok0 / ok1 gate the stores of the pair's
+// even / odd row.  Every lane of the warp takes part (shuffles).
+template <int NC>
+__device__ __forceinline__ void st_rows_paired(uint32_t* own, size_t ld, const uint4 (&c)[NC],
+                                               int lane, bool ok0, bool ok1) {
+    static_assert(NC % 2 == 0, "chunks are exchanged in pairs");
+    const bool odd = lane & 1;
+    uint32_t* d0 = odd ? own - ld + 4 : own;  // the even row, this lane's chunk of each pair
+    uint32_t* d1 = odd ? own + 4 : own + ld;  // the odd row
+#pragma unroll
+    for (int i = 0; i < NC / 2; ++i) {
+        const uint4 ce = c[2 * i], co = c[2 * i + 1];
+        const uint4 snd = odd ? ce : co;
+        uint4 rcv;
+        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, 1);
+        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, 1);
+        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, 1);
+        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, 1);
+        if (ok0) reinterpret_cast<uint4*>(d0 + 8 * i)[0] = odd ? rcv : ce;
+        if (ok1) reinterpret_cast<uint4*>(d1 + 8 * i)[0] = odd ? co : rcv;
+    }
+}
+// The same for N consecutive FP32 values of this lane's row (N a multiple of 8).
+template <int N>
+__device__ __forceinline__ void st_rows_paired_f32(float* own, size_t ld, const float (&v)[N],
+                                                   int lane, bool ok0, bool ok1) {
+    uint4 c[N / 4];
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j)
+        c[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                          __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+    st_rows_paired<N / 4>(reinterpret_cast<uint32_t*>(own), ld, c, lane, ok0, ok1);
+}
 // N = 32, 16 or 8 consecutive FP32 TMEM columns of this warp's 32 lanes (as tmem_ld32)
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);

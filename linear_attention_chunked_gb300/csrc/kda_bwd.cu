@@ -439,33 +439,74 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     __syncthreads();
 
     // 4. inside each sub-chunk, elementwise: one thread per (sub-chunk, channel); the column's 16
-    //    values of gam, q^, k^ are held in registers, and exp(gam_r - gam_s) is the running product
-    //    of the per-token decay factors exp(gam_x - gam_{x-1}), s < x <= r (each <= 1)
+    //    values of q^, k^ are held in registers.  Rows 8..15 against columns 0..7 (the lower-left
+    //    8 x 8 quadrant) factor as e^(gam_r - gam_s) = F_r G_s with F_r = e^(gam_r - gam_7) and
+    //    G_s = e^(gam_7 - gam_s), both <= 1 (row 7 lies between s and r), so each pair there costs
+    //    four FMAs; inside the two diagonal 8 x 8 blocks e^(gam_r - gam_s) is the running product
+    //    of the per-token decays e^(gam_x - gam_{x-1}), s < x <= r (each <= 1)
     {
         const int b = tid / D, c = tid % D, base = 16 * b;
-        float qv[16], kv[16], ed[16], aq[16], ak[16], bb[16];
+        float qv[16], kv[16], aq[16], ak[16], bb[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
             qv[x] = Qv(base + x, c);
             kv[x] = Kv(base + x, c);
-            aq[x] = ak[x] = bb[x] = 0.f;
         }
+        {
+            const float g7 = S.gam[(base + 7) * LDP + c];
+            float F[8], G[8], Y[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                F[j] = __expf(S.gam[(base + 8 + j) * LDP + c] - g7);
+                G[j] = __expf(g7 - S.gam[(base + j) * LDP + c]);
+                Y[j] = G[j] * kv[j];
+                bb[j] = 0.f;
+            }
+#pragma unroll
+            for (int rj = 0; rj < 8; ++rj) {
+                const int r = base + 8 + rj;
+                const float qF = qv[8 + rj] * F[rj], kF = kv[8 + rj] * F[rj];
+                float tq = 0.f, tk = 0.f;
+#pragma unroll
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(&S.dA[a_at(r, base + 4 * q4)]);
+                    const float4 m4 = *reinterpret_cast<const float4*>(&S.dAk[a_at(r, base + 4 * q4)]);
+                    const float av4[4] = {a4.x, a4.y, a4.z, a4.w}, mv4[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int sq = 4 * q4 + e;
+                        tq = fmaf(av4[e], Y[sq], tq);
+                        tk = fmaf(mv4[e], Y[sq], tk);
+                        bb[sq] = fmaf(av4[e], qF, fmaf(mv4[e], kF, bb[sq]));
+                    }
+                }
+                aq[8 + rj] = F[rj] * tq;
+                ak[8 + rj] = F[rj] * tk;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                bb[j] *= G[j];
+                aq[j] = ak[j] = bb[8 + j] = 0.f;
+            }
+        }
+        float ed[16];  // ed[x] = e^(gam_x - gam_{x-1}) (x = 8 starts a block: unused)
         {
             float prev = S.gam[base * LDP + c];
 #pragma unroll
             for (int x = 1; x < 16; ++x) {
                 const float cur = S.gam[(base + x) * LDP + c];
-                ed[x] = __expf(cur - prev);
+                ed[x] = x == 8 ? 1.f : __expf(cur - prev);
                 prev = cur;
             }
         }
-        // row rl of the block: columns sl = rl-1 down to 0, read four at a time (warp-wide broadcast)
+        // row rl of a diagonal block: columns sl = rl-1 down to the block's first row, read four at
+        // a time (warp-wide broadcast)
 #pragma unroll
         for (int rl = 1; rl < 16; ++rl) {
-            const int r = base + rl;
+            const int r = base + rl, lo = rl < 8 ? 0 : 8;
             float E = 1.f;
 #pragma unroll
-            for (int q4 = (rl - 1) >> 2; q4 >= 0; --q4) {
+            for (int q4 = (rl - 1) >> 2; q4 >= (lo >> 2); --q4) {
                 const float4 a4 = *reinterpret_cast<const float4*>(&S.dA[a_at(r, base + 4 * q4)]);
                 const float4 m4 = *reinterpret_cast<const float4*>(&S.dAk[a_at(r, base + 4 * q4)]);
                 const float av4[4] = {a4.x, a4.y, a4.z, a4.w}, mv4[4] = {m4.x, m4.y, m4.z, m4.w};

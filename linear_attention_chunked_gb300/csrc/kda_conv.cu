@@ -11,8 +11,9 @@
 // Both kernels are bound by HBM traffic (2 bytes of x per channel and token in, as much out),
 // so they are plain streaming kernels: a thread owns 4 consecutive channels (an 8-byte bf16 row
 // segment; a warp covers 128 channels, 256 contiguous bytes of a row) and a run of TT tokens,
-// keeps the three previous rows in registers, and loads UNR rows per batch so that enough bytes
-// are in flight per SM.  The backward recomputes z, takes dz = dy silu'(z) for its tokens and the
+// keeps the three previous rows in registers, and streams its rows through a ring of shared
+// memory slots filled by cp.async RING - 1 rows ahead, so that enough bytes are in flight per SM
+// without holding them in registers.  The backward recomputes z, takes dz = dy silu'(z) for its tokens and the
 // three after them (their dz also reaches its last rows), and writes dx of its own rows only;
 // dw and db are summed per block in a fixed order and then over blocks by a second kernel, so
 // every result is bitwise reproducible (no atomics).
@@ -24,8 +25,8 @@ namespace {
 
 constexpr int CV_TX = 32, CV_TY = 8;  // block: 32 channel groups x 8 token runs
 constexpr int CV_TT = 64;             // tokens per run
-constexpr int CV_UNR = 4;             // rows of x loaded per batch (forward)
-constexpr int CV_UNR_B = 2;           // rows of x and dy loaded per batch (backward)
+constexpr int CV_RING = 16;           // ring slots per thread (forward): 15 rows in flight
+constexpr int CV_RING_B = 8;          // ring slots per thread (backward, x and dy)
 constexpr int CV_ROWS = CV_TY * CV_TT;  // tokens per block row
 
 struct ConvArgs {
@@ -45,6 +46,19 @@ struct ConvArgs {
 };
 
 constexpr int CPT = 4;  // channels per thread (8-byte bf16 / 16-byte fp32 row segments)
+
+// 8- and 16-byte cp.async with zero fill (nothing is read when !valid); the source pointer stays
+// inside the tensor either way
+__device__ __forceinline__ void cp8z(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 8 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp16zm(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
 
 __device__ __forceinline__ void bf4_to_f(const uint2& u, float (&f)[CPT]) {
     const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -69,20 +83,6 @@ __device__ __forceinline__ void store_row(void* base, size_t row, int C, int c0,
     } else {
         *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(base) + i) =
             make_uint2(pack2(f[0], f[1]), pack2(f[2], f[3]));
-    }
-}
-
-__device__ __forceinline__ void load_any(const void* base, size_t row, int C, int c0, int fp32,
-                                         float (&f)[CPT]) {
-    const size_t i = row * size_t(C) + c0;
-    if (fp32) {
-        const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
-        f[0] = a.x;
-        f[1] = a.y;
-        f[2] = a.z;
-        f[3] = a.w;
-    } else {
-        bf4_to_f(*reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + i), f);
     }
 }
 
@@ -126,10 +126,21 @@ __device__ __forceinline__ void window_at(const ConvArgs& a, int n, int s, int t
 }
 
 __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
-    const int cg = blockIdx.x * CV_TX + threadIdx.x, c0 = CPT * cg;
-    const int t0 = (int(blockIdx.y) * CV_TY + int(threadIdx.y)) * CV_TT;
-    if (c0 >= a.C || t0 >= a.T) return;
+    __shared__ uint2 ring[CV_TY][CV_RING][CV_TX];  // [token run][slot][channel group]: one x row each
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int cg = blockIdx.x * CV_TX + tx, c0 = CPT * cg;
+    const int t0 = (int(blockIdx.y) * CV_TY + ty) * CV_TT;
+    if (c0 >= a.C || t0 >= a.T) return;  // (no block-wide barrier in this kernel)
     const int t1 = min(t0 + CV_TT, int(a.T));
+    const __nv_bfloat16* xcol = a.x + c0;  // row t at xcol + t C
+    // row t into its slot, (t - t0) mod RING; rows past the run are zero-filled and never read
+    auto fill = [&](int t) {
+        const bool ok = t < t1;
+        cp8z(&ring[ty][(t - t0) & (CV_RING - 1)][tx], xcol + size_t(ok ? t : t0) * a.C, ok);
+        cp_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < CV_RING - 1; ++i) fill(t0 + i);
     float w[4][CPT], b[CPT];
 #pragma unroll
     for (int k = 0; k < CPT; ++k) {
@@ -141,34 +152,30 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
     int s = a.cu[n], e = a.cu[n + 1];
     float xm[3][CPT];
     window_at(a, n, s, t0, c0, xm);
-    for (int tb = t0; tb < t1; tb += CV_UNR) {
-        float xr[CV_UNR][CPT];
-#pragma unroll
-        for (int u = 0; u < CV_UNR; ++u)
-            if (tb + u < t1) load_row(a.x, size_t(tb + u), a.C, c0, xr[u]);
-#pragma unroll
-        for (int u = 0; u < CV_UNR; ++u) {
-            const int t = tb + u;
-            if (t >= t1) break;
-            if (t >= e) {  // next document (skipping empty ones): its halo rows or zeros
-                while (n + 1 < a.N && int(a.cu[n + 1]) <= t) ++n;
-                s = a.cu[n];
-                e = a.cu[n + 1];
-                window_at(a, n, s, t, c0, xm);
-            }
-            float out[CPT];
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) {
-                const float z = b[k] + w[0][k] * xm[0][k] + w[1][k] * xm[1][k] +
-                                w[2][k] * xm[2][k] + w[3][k] * xr[u][k];
-                out[k] = a.act ? __fdividef(z, 1.f + __expf(-z)) : z;
-                xm[0][k] = xm[1][k];
-                xm[1][k] = xm[2][k];
-                xm[2][k] = xr[u][k];
-            }
-            store_row(a.y, size_t(t), a.C, c0, out, a.out_fp32);
+    for (int t = t0; t < t1; ++t) {
+        cp_wait<CV_RING - 2>();  // row t has landed (the RING - 2 later rows may be in flight)
+        float xr[CPT];
+        bf4_to_f(ring[ty][(t - t0) & (CV_RING - 1)][tx], xr);
+        fill(t + CV_RING - 1);  // into the slot of row t - 1, read in the previous iteration
+        if (t >= e) {  // next document (skipping empty ones): its halo rows or zeros
+            while (n + 1 < a.N && int(a.cu[n + 1]) <= t) ++n;
+            s = a.cu[n];
+            e = a.cu[n + 1];
+            window_at(a, n, s, t, c0, xm);
         }
+        float out[CPT];
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const float z = b[k] + w[0][k] * xm[0][k] + w[1][k] * xm[1][k] +
+                            w[2][k] * xm[2][k] + w[3][k] * xr[k];
+            out[k] = a.act ? __fdividef(z, 1.f + __expf(-z)) : z;
+            xm[0][k] = xm[1][k];
+            xm[1][k] = xm[2][k];
+            xm[2][k] = xr[k];
+        }
+        store_row(a.y, size_t(t), a.C, c0, out, a.out_fp32);
     }
+    cp_wait<0>();  // no copy into the ring is in flight when the thread leaves
 }
 
 // Backward: per thread, tokens t0 .. t1 - 1 own their dx rows and their dw / db terms; dz of the
@@ -176,7 +183,15 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
 // first token also owns the document's halo gradient.  Every branch below depends only on token
 // positions, which all lanes of a warp share (lanes differ in channels), so none diverges.
 __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
-    __shared__ float red[CV_TY][5][CPT][CV_TX + 1];
+    // rings of x and dy rows during the token loop; the dw / db reduction scratch afterwards
+    __shared__ union {
+        struct {
+            uint2 x[CV_TY][CV_RING_B][CV_TX];
+            uint4 g[CV_TY][CV_RING_B][CV_TX];  // dy: fp32 (16 bytes) or bf16 (the first 8)
+        } ring;
+        float red[CV_TY][5][CPT][CV_TX + 1];
+    } sh;
+    auto& red = sh.red;
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int cg = blockIdx.x * CV_TX + tx, c0 = CPT * cg;
     const int t0 = (int(blockIdx.y) * CV_TY + ty) * CV_TT;
@@ -230,29 +245,38 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
             }
         };
         const __nv_bfloat16* xcol = a.x + c0;  // row t at xcol + t C
+        // rows t0 .. tl - 1 of x and dy through the ring, RING - 1 rows ahead; rows past tl are
+        // zero-filled and never read
+        auto fill = [&](int tr) {
+            const bool ok = tr < tl;
+            const size_t row = size_t(ok ? tr : t0);
+            const int slot = (tr - t0) & (CV_RING_B - 1);
+            cp8z(&sh.ring.x[ty][slot][tx], xcol + row * C, ok);
+            if (fp32) cp16zm(&sh.ring.g[ty][slot][tx], static_cast<const float*>(a.dy) + row * C + c0, ok);
+            else cp8z(&sh.ring.g[ty][slot][tx], static_cast<const __nv_bfloat16*>(a.dy) + row * C + c0, ok);
+            cp_commit();
+        };
+#pragma unroll
+        for (int i = 0; i < CV_RING_B - 1; ++i) fill(t0 + i);
         int t = t0;  // first token not processed
-        bool stop = false;
-        for (int tb = t0; tb < tl && !stop; tb += CV_UNR_B) {
-          float xb[CV_UNR_B][CPT], gb[CV_UNR_B][CPT];  // rows tb .. tb + UNR - 1, loaded together
-          const __nv_bfloat16* xp = xcol + size_t(tb) * C;
-#pragma unroll
-          for (int u = 0; u < CV_UNR_B; ++u)
-              if (tb + u < tl) {
-                  bf4_to_f(*reinterpret_cast<const uint2*>(xp + size_t(u) * C), xb[u]);
-                  load_any(a.dy, size_t(tb + u), C, c0, fp32, gb[u]);
-              }
-#pragma unroll
-          for (int u = 0; u < CV_UNR_B; ++u) {
-            t = tb + u;
-            if (t >= tl) {
-                stop = true;
-                break;
+        for (; t < tl; ++t) {
+            cp_wait<CV_RING_B - 2>();  // row t has landed
+            const int slot = (t - t0) & (CV_RING_B - 1);
+            float xr[CPT], gr[CPT];
+            bf4_to_f(sh.ring.x[ty][slot][tx], xr);
+            if (fp32) {
+                const uint4 u = sh.ring.g[ty][slot][tx];
+                gr[0] = __uint_as_float(u.x);
+                gr[1] = __uint_as_float(u.y);
+                gr[2] = __uint_as_float(u.z);
+                gr[3] = __uint_as_float(u.w);
+            } else {
+                const uint4 u = sh.ring.g[ty][slot][tx];
+                bf4_to_f(make_uint2(u.x, u.y), gr);
             }
+            fill(t + CV_RING_B - 1);  // into the slot of row t - 1, read in the previous iteration
             if (t >= e) {  // next document: rows of the old one are complete, its halo too
-                if (t >= t1) {  // lookahead stops at the end of the document
-                    stop = true;
-                    break;
-                }
+                if (t >= t1) break;  // lookahead stops at the end of the document
                 emit(t, 3);
                 flush_halo();
 #pragma unroll
@@ -269,7 +293,6 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                     for (int k = 0; k < CPT; ++k) dh[i][k] = 0.f;
                 window_at(a, n, s, t, c0, xm);
             }
-            const float(&xr)[CPT] = xb[u];
             float dz[CPT];
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
@@ -277,9 +300,9 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                                 w[2][k] * xm[2][k] + w[3][k] * xr[k];
                 if (act) {
                     const float sg = sigm(z);
-                    dz[k] = gb[u][k] * sg * (1.f + z * (1.f - sg));
+                    dz[k] = gr[k] * sg * (1.f + z * (1.f - sg));
                 } else {
-                    dz[k] = gb[u][k];
+                    dz[k] = gr[k];
                 }
             }
             if (t < t1) {  // this thread's dw / db terms
@@ -330,15 +353,16 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 2) k_conv_bwd(ConvArgs a) {
                 xm[1][k] = xm[2][k];
                 xm[2][k] = xr[k];
             }
-            t = tb + u + 1;
-          }
         }
+        cp_wait<0>();  // no copy into the ring is in flight past the loop
         // rows t - 3 .. t - 1 are still held when the loop stops (end of the lookahead, of the
         // document or of the sequence); they are complete
         emit(t, 3);
         flush_halo();
     }
-    // dw / db partials: the 8 token runs of the block summed in order, one row per block row
+    // dw / db partials: the 8 token runs of the block summed in order, one row per block row (the
+    // scratch overlays the rings: every thread is past its loop and its copies)
+    __syncthreads();
 #pragma unroll
     for (int k = 0; k < CPT; ++k) {
 #pragma unroll

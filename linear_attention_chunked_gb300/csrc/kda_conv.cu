@@ -25,7 +25,8 @@ namespace {
 
 constexpr int CV_TX = 32, CV_TY = 8;  // block: 32 channel groups x 8 token runs
 constexpr int CV_TT = 64;             // tokens per run
-constexpr int CV_RING = 16;           // ring slots per thread (forward): 15 rows in flight
+constexpr int CV_RING = 16;           // ring slots per thread (forward): four groups of four rows
+constexpr int CV_GR = 4;              // rows per copy group (forward)
 constexpr int CV_RING_B = 8;          // ring slots per thread (backward, x and dy)
 constexpr int CV_ROWS = CV_TY * CV_TT;  // tokens per block row
 
@@ -132,15 +133,23 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
     const int t0 = (int(blockIdx.y) * CV_TY + ty) * CV_TT;
     if (c0 >= a.C || t0 >= a.T) return;  // (no block-wide barrier in this kernel)
     const int t1 = min(t0 + CV_TT, int(a.T));
+    const size_t C = size_t(a.C);
     const __nv_bfloat16* xcol = a.x + c0;  // row t at xcol + t C
-    // row t into its slot, (t - t0) mod RING; rows past the run are zero-filled and never read
-    auto fill = [&](int t) {
-        const bool ok = t < t1;
-        cp8z(&ring[ty][(t - t0) & (CV_RING - 1)][tx], xcol + size_t(ok ? t : t0) * a.C, ok);
+    // group q = rows t0 + 4 q .. t0 + 4 q + 3 into slots 4 (q mod 4) ..; rows past the run are
+    // zero-filled and never read
+    auto fill = [&](int q) {
+        const int tq = t0 + CV_GR * q;
+        const __nv_bfloat16* src = xcol + size_t(tq) * C;
+#pragma unroll
+        for (int j = 0; j < CV_GR; ++j) {
+            const bool ok = tq + j < t1;
+            cp8z(&ring[ty][(q & 3) * CV_GR + j][tx], ok ? src + j * C : xcol + size_t(t0) * C, ok);
+        }
         cp_commit();
     };
-#pragma unroll
-    for (int i = 0; i < CV_RING - 1; ++i) fill(t0 + i);
+    fill(0);
+    fill(1);
+    fill(2);
     float w[4][CPT], b[CPT];
 #pragma unroll
     for (int k = 0; k < CPT; ++k) {
@@ -152,28 +161,36 @@ __global__ void __launch_bounds__(CV_TX * CV_TY, 3) k_conv_fwd(ConvArgs a) {
     int s = a.cu[n], e = a.cu[n + 1];
     float xm[3][CPT];
     window_at(a, n, s, t0, c0, xm);
-    for (int t = t0; t < t1; ++t) {
-        cp_wait<CV_RING - 2>();  // row t has landed (the RING - 2 later rows may be in flight)
-        float xr[CPT];
-        bf4_to_f(ring[ty][(t - t0) & (CV_RING - 1)][tx], xr);
-        fill(t + CV_RING - 1);  // into the slot of row t - 1, read in the previous iteration
-        if (t >= e) {  // next document (skipping empty ones): its halo rows or zeros
-            while (n + 1 < a.N && int(a.cu[n + 1]) <= t) ++n;
-            s = a.cu[n];
-            e = a.cu[n + 1];
-            window_at(a, n, s, t, c0, xm);
-        }
-        float out[CPT];
+    for (int q = 0; t0 + CV_GR * q < t1; ++q) {
+        cp_wait<2>();  // group q has landed (groups q + 1, q + 2 may be in flight)
+        uint2 raw[CV_GR];
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const float z = b[k] + w[0][k] * xm[0][k] + w[1][k] * xm[1][k] +
-                            w[2][k] * xm[2][k] + w[3][k] * xr[k];
-            out[k] = a.act ? __fdividef(z, 1.f + __expf(-z)) : z;
-            xm[0][k] = xm[1][k];
-            xm[1][k] = xm[2][k];
-            xm[2][k] = xr[k];
+        for (int j = 0; j < CV_GR; ++j) raw[j] = ring[ty][(q & 3) * CV_GR + j][tx];
+        fill(q + 3);  // into the slots of group q - 1, read in the previous iteration
+#pragma unroll
+        for (int j = 0; j < CV_GR; ++j) {
+            const int t = t0 + CV_GR * q + j;
+            if (t >= t1) break;
+            float xr[CPT];
+            bf4_to_f(raw[j], xr);
+            if (t >= e) {  // next document (skipping empty ones): its halo rows or zeros
+                while (n + 1 < a.N && int(a.cu[n + 1]) <= t) ++n;
+                s = a.cu[n];
+                e = a.cu[n + 1];
+                window_at(a, n, s, t, c0, xm);
+            }
+            float out[CPT];
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const float z = b[k] + w[0][k] * xm[0][k] + w[1][k] * xm[1][k] +
+                                w[2][k] * xm[2][k] + w[3][k] * xr[k];
+                out[k] = a.act ? __fdividef(z, 1.f + __expf(-z)) : z;
+                xm[0][k] = xm[1][k];
+                xm[1][k] = xm[2][k];
+                xm[2][k] = xr[k];
+            }
+            store_row(a.y, size_t(t), a.C, c0, out, a.out_fp32);
         }
-        store_row(a.y, size_t(t), a.C, c0, out, a.out_fp32);
     }
     cp_wait<0>();  // no copy into the ring is in flight when the thread leaves
 }

@@ -50,6 +50,8 @@ __constant__ int2 kPairs[6] = {{1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
 
 
 static_assert(sizeof(IntraSmem) + 1024 <= 232448, "intra shared memory above the opt-in limit");
+static_assert(offsetof(IntraSmem, Akk) % 16 == 0 && (CH * LDA) % 4 == 0,
+              "the 64 x 64 tiles are cleared with 16-byte stores");
 static_assert(offsetof(IntraSmem, k) % 1024 == 0 && offsetof(IntraSmem, x) % 1024 == 0 &&
                   offsetof(IntraSmem, u) % 1024 == 0 && CH * LQ * 4 >= 4 * 8192,
               "staging tiles of the TMA stores must be 1024-byte aligned and hold four boxes");
@@ -229,10 +231,11 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         // then do nothing
         if (bad_gate) p.status[0] = KDA_ERR_DEVICE_CHECK;
     }
-    for (int i = tid; i < CH * LDA; i += BT) {
-        S.Akk[i] = 0.f;
-        S.Aqk[i] = 0.f;
-        S.Mi[i] = 0.f;
+    for (int i = tid; i < CH * LDA / 4; i += BT) {  // (each tile is 16-byte aligned, 4160 floats)
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<float4*>(S.Akk)[i] = z;
+        reinterpret_cast<float4*>(S.Aqk)[i] = z;
+        reinterpret_cast<float4*>(S.Mi)[i] = z;
     }
     __syncthreads();
     const bool more = item + int(gridDim.x) < items;
@@ -318,13 +321,15 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         S.Aqk[r * LDA + sc] = p0[9 + j] + p1[9 + j];
     }
     // 4b. B operands Ks_j[sl][c] = k[16j+sl][c] exp(gam[16j+15][c] - gam[16j+sl][c]), j = 0..2
-    for (int idx = tid; idx < 3 * 16 * D; idx += BT) {
-        const int j = idx / (16 * D), rem = idx % (16 * D), sl = rem / D, c = rem % D;
+    for (int idx = tid; idx < 3 * 16 * D / 4; idx += BT) {  // four channels per pass
+        const int j = idx / (4 * D), rem = idx % (4 * D), sl = rem / (D / 4), c = (rem % (D / 4)) * 4;
         const int s = 16 * j + sl, e = 16 * j + 15;
-        const float x = S.k[s * LQ + c] * __expf(S.gam[e * LQ + c] - S.gam[s * LQ + c]);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-        S.u.a.Ks[j][0][sl * LB + c] = hi;
-        S.u.a.Ks[j][1][sl * LB + c] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        const float4 kv = row4(S.k, s, c), ge = row4(S.gam, e, c), gs = row4(S.gam, s, c);
+        uint32_t h0, l0, h1, l1;
+        split2(kv.x * __expf(ge.x - gs.x), kv.y * __expf(ge.y - gs.y), h0, l0);
+        split2(kv.z * __expf(ge.z - gs.z), kv.w * __expf(ge.w - gs.w), h1, l1);
+        *reinterpret_cast<uint2*>(&S.u.a.Ks[j][0][sl * LB + c]) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(&S.u.a.Ks[j][1][sl * LB + c]) = make_uint2(l0, l1);
     }
     __syncthreads();
     // 4c. off-diagonal blocks on tensor cores: warp w < 12 takes pair w / 2 and half w % 2 of the
@@ -435,24 +440,28 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         __nv_bfloat16* Kl = p.Kl + chd * CH * D;
         float* gam = p.gam + chd * CH * D;
         if (tid - 64 < D) p.eGL[chd * D + tid - 64] = __expf(S.gam[(CH - 1) * LQ + tid - 64]);
-        for (int i = tid - 64; i < CH * D / 2; i += BT - 64) {
-            const int r = (2 * i) / D, c = (2 * i) % D;
-            const float2 kv = *reinterpret_cast<const float2*>(&S.k[r * LQ + c]);
-            const float2 gv = *reinterpret_cast<const float2*>(&S.gam[r * LQ + c]);
-            const float2 gl = *reinterpret_cast<const float2*>(&S.gam[(CH - 1) * LQ + c]);
-            const float2 qv = *reinterpret_cast<const float2*>(&S.q[r * LQ + c]);
-            const float e0 = __expf(gv.x), e1 = __expf(gv.y);
-            uint32_t hi, lo;
-            split2(S.beta[r] * kv.x * e0, S.beta[r] * kv.y * e1, hi, lo);
-            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[0][r * LB + c]) = hi;
-            *reinterpret_cast<uint32_t*>(&S.u.b.bKg[1][r * LB + c]) = lo;
-            split2(qv.x * e0, qv.y * e1, hi, lo);
-            reinterpret_cast<uint32_t*>(Qh)[i] = hi;
-            reinterpret_cast<uint32_t*>(Ql)[i] = lo;
-            split2(kv.x * __expf(gl.x - gv.x), kv.y * __expf(gl.y - gv.y), hi, lo);
-            reinterpret_cast<uint32_t*>(Kh)[i] = hi;
-            reinterpret_cast<uint32_t*>(Kl)[i] = lo;
-            reinterpret_cast<float2*>(gam)[i] = gv;
+        for (int i = tid - 64; i < CH * D / 4; i += BT - 64) {  // four channels of a row per pass
+            const int r = (4 * i) / D, c = (4 * i) % D;
+            const float4 kv = *reinterpret_cast<const float4*>(&S.k[r * LQ + c]);
+            const float4 gv = *reinterpret_cast<const float4*>(&S.gam[r * LQ + c]);
+            const float4 gl = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LQ + c]);
+            const float4 qv = *reinterpret_cast<const float4*>(&S.q[r * LQ + c]);
+            const float br = S.beta[r];
+            const float e0 = __expf(gv.x), e1 = __expf(gv.y), e2 = __expf(gv.z), e3 = __expf(gv.w);
+            uint32_t h0, l0, h1, l1;
+            split2(br * kv.x * e0, br * kv.y * e1, h0, l0);
+            split2(br * kv.z * e2, br * kv.w * e3, h1, l1);
+            *reinterpret_cast<uint2*>(&S.u.b.bKg[0][r * LB + c]) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(&S.u.b.bKg[1][r * LB + c]) = make_uint2(l0, l1);
+            split2(qv.x * e0, qv.y * e1, h0, l0);
+            split2(qv.z * e2, qv.w * e3, h1, l1);
+            reinterpret_cast<uint2*>(Qh)[i] = make_uint2(h0, h1);
+            reinterpret_cast<uint2*>(Ql)[i] = make_uint2(l0, l1);
+            split2(kv.x * __expf(gl.x - gv.x), kv.y * __expf(gl.y - gv.y), h0, l0);
+            split2(kv.z * __expf(gl.z - gv.z), kv.w * __expf(gl.w - gv.w), h1, l1);
+            reinterpret_cast<uint2*>(Kh)[i] = make_uint2(h0, h1);
+            reinterpret_cast<uint2*>(Kl)[i] = make_uint2(l0, l1);
+            reinterpret_cast<float4*>(gam)[i] = gv;
         }
     } else {
         const int b = tid >> 4, cl = tid & 15, c = 16 * b + cl;

@@ -20,6 +20,9 @@ constexpr int LB = 136;  // row stride (bf16 elements) of [rows][128] MMA operan
 // row stride (floats) of the q, k, gam tiles: 8 words of bank offset per row, so the 8-byte
 // fragment reads of step 4c (rows g, columns 2t of a quad-lane layout) meet no bank conflict
 constexpr int LQ = D + 8;
+// row stride (floats) of the 64 x 64 tiles Akk, Aqk, Minv: 16-byte aligned rows (8-byte fragment
+// and staging reads) and 4 banks per row (the G and X phases' column-wise B reads meet no conflict)
+constexpr int LA = CH + 4;
 
 // The base is 1024-byte aligned; so are k, akk_st and u, which double as 128-byte-swizzled
 // staging tiles of the TMA stores of the products: Aqk / Minv hi / lo in k and Akk in akk_st
@@ -28,7 +31,8 @@ struct IntraSmem {
     float q[CH * LQ], k[CH * LQ], gam[CH * LQ];
     union {
         unsigned char akk_st[2 * 8192];  // Akk staged for its TMA store: boxes [64 rows][32 fp32]
-        float P[6][16 * 32];             // partial sums of step 4 (dead before the staging)
+        float P[6][16 * 32];             // partial sums of step 4 (dead before step 5)
+        uint4 gfrag[6 * 2 * 32];         // split A fragments of G_il (step 5): [pair][hi, lo][lane]
     } x;
     union {
         struct {
@@ -39,9 +43,8 @@ struct IntraSmem {
         } b;
         unsigned char wst[4 * 8192];  // W staged: boxes [plane][column block] of 64 rows x 64 bf16
     } u;
-    float Akk[CH * LDA], Aqk[CH * LDA], Mi[CH * LDA];
+    float Akk[CH * LA], Aqk[CH * LA], Mi[CH * LA];
     float beta[CH];
-    uint4 gfrag[6 * 2 * 32];  // split A fragments of G_il (step 5): [pair][hi, lo][lane]
     __nv_bfloat16 v[CH * LB];  // V (exact in bf16)
 };
 
@@ -50,7 +53,7 @@ __constant__ int2 kPairs[6] = {{1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
 
 
 static_assert(sizeof(IntraSmem) + 1024 <= 232448, "intra shared memory above the opt-in limit");
-static_assert(offsetof(IntraSmem, Akk) % 16 == 0 && (CH * LDA) % 4 == 0,
+static_assert(offsetof(IntraSmem, Akk) % 16 == 0 && (CH * LA) % 4 == 0,
               "the 64 x 64 tiles are cleared with 16-byte stores");
 static_assert(offsetof(IntraSmem, k) % 1024 == 0 && offsetof(IntraSmem, x) % 1024 == 0 &&
                   offsetof(IntraSmem, u) % 1024 == 0 && CH * LQ * 4 >= 4 * 8192,
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         // then do nothing
         if (bad_gate) p.status[0] = KDA_ERR_DEVICE_CHECK;
     }
-    for (int i = tid; i < CH * LDA / 4; i += BT) {  // (each tile is 16-byte aligned, 4160 floats)
+    for (int i = tid; i < CH * LA / 4; i += BT) {  // (each tile is 16-byte aligned, 4352 floats)
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         reinterpret_cast<float4*>(S.Akk)[i] = z;
         reinterpret_cast<float4*>(S.Aqk)[i] = z;
@@ -317,8 +320,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         const int r = 8 * b + (rowB ? rB : rA), sc = 8 * b + (rowB ? rB - j : rA - (j - rB - 1));
         const float* p0 = &S.x.P[0][0] + (b * 4 + rp) * 18;
         const float* p1 = p0 + 8 * 4 * 18;
-        if (sc < r) S.Akk[r * LDA + sc] = p0[j] + p1[j];
-        S.Aqk[r * LDA + sc] = p0[9 + j] + p1[9 + j];
+        if (sc < r) S.Akk[r * LA + sc] = p0[j] + p1[j];
+        S.Aqk[r * LA + sc] = p0[9 + j] + p1[9 + j];
     }
     // 4b. B operands Ks_j[sl][c] = k[16j+sl][c] exp(gam[16j+15][c] - gam[16j+sl][c]), j = 0..2
     for (int idx = tid; idx < 3 * 16 * D / 4; idx += BT) {  // four channels per pass
@@ -368,8 +371,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
         for (int e4 = 2; e4 < 4; ++e4) {
             const int row = 16 * b + 8 + g, col = 16 * b + 2 * t + (e4 & 1);
-            S.Aqk[row * LDA + col] = accQ[e4];
-            S.Akk[row * LDA + col] = accK[e4];
+            S.Aqk[row * LA + col] = accQ[e4];
+            S.Akk[row * LA + col] = accK[e4];
         }
     } else {
         const int pr = warp >> 1, kh = warp & 1;
@@ -416,8 +419,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
                 for (int e4 = 0; e4 < 4; ++e4) {
                     const int row = 16 * i + g + 8 * (e4 >> 1), col = 16 * j + 8 * nt + 2 * t + (e4 & 1);
-                    S.Aqk[row * LDA + col] = accQ[nt][e4] + part[((nt * 2 + 0) * 4 + e4) * 32 + lane];
-                    S.Akk[row * LDA + col] = accK[nt][e4] + part[((nt * 2 + 1) * 4 + e4) * 32 + lane];
+                    S.Aqk[row * LA + col] = accQ[nt][e4] + part[((nt * 2 + 0) * 4 + e4) * 32 + lane];
+                    S.Akk[row * LA + col] = accK[nt][e4] + part[((nt * 2 + 1) * 4 + e4) * 32 + lane];
                 }
         }
     }
@@ -471,11 +474,11 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             const int r = 16 * b + rl;
             float acc = 0.f;
 #pragma unroll
-            for (int sl = 0; sl < rl; ++sl) acc = fmaf(S.Akk[r * LDA + 16 * b + sl], x[sl], acc);
+            for (int sl = 0; sl < rl; ++sl) acc = fmaf(S.Akk[r * LA + 16 * b + sl], x[sl], acc);
             x[rl] = (rl == cl) ? 1.f : -S.beta[r] * acc;
         }
 #pragma unroll
-        for (int rl = 0; rl < 16; ++rl) S.Mi[(16 * b + rl) * LDA + c] = x[rl];
+        for (int rl = 0; rl < 16; ++rl) S.Mi[(16 * b + rl) * LA + c] = x[rl];
     }
     __syncthreads();
     // G_il, pair w = i (i - 1) / 2 + l on warp w < 6: A = D_i, B = diag(beta_i) Akk_il (both
@@ -486,7 +489,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
             const int row = 16 * i + g + 8 * (rr & 1), col = 16 * i + 2 * t + 8 * (rr >> 1);
-            split2(S.Mi[row * LDA + col], S.Mi[row * LDA + col + 1], dh[rr], dl[rr]);
+            const float2 m = *reinterpret_cast<const float2*>(&S.Mi[row * LA + col]);
+            split2(m.x, m.y, dh[rr], dl[rr]);
         }
         float acc[2][4] = {};
 #pragma unroll
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int kr = 16 * i + 2 * t + 8 * hf, n = 16 * l + 8 * nt + g;
-                split2(S.beta[kr] * S.Akk[kr * LDA + n], S.beta[kr + 1] * S.Akk[(kr + 1) * LDA + n],
+                split2(S.beta[kr] * S.Akk[kr * LA + n], S.beta[kr + 1] * S.Akk[(kr + 1) * LA + n],
                        bh[hf], bl[hf]);
             }
             mma_x3(acc[nt], dh, dl, bh[0], bh[1], bl[0], bl[1]);
@@ -503,8 +507,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         uint32_t h[4], lo[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) split2(-acc[q >> 1][2 * (q & 1)], -acc[q >> 1][2 * (q & 1) + 1], h[q], lo[q]);
-        S.gfrag[(2 * warp) * 32 + lane] = make_uint4(h[0], h[1], h[2], h[3]);
-        S.gfrag[(2 * warp + 1) * 32 + lane] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        S.x.gfrag[(2 * warp) * 32 + lane] = make_uint4(h[0], h[1], h[2], h[3]);
+        S.x.gfrag[(2 * warp + 1) * 32 + lane] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     __syncthreads();
     // X_ij for j = 0 .. 3 - dist, i = j + dist: warp = (j, 8-column n-tile)
@@ -516,19 +520,19 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
             for (int l = j; l < i; ++l) {
                 const int pr = i * (i - 1) / 2 + l;
-                const uint4 fh = S.gfrag[(2 * pr) * 32 + lane], fl = S.gfrag[(2 * pr + 1) * 32 + lane];
+                const uint4 fh = S.x.gfrag[(2 * pr) * 32 + lane], fl = S.x.gfrag[(2 * pr + 1) * 32 + lane];
                 const uint32_t ah[4] = {fh.x, fh.y, fh.z, fh.w}, al[4] = {fl.x, fl.y, fl.z, fl.w};
                 uint32_t bh[2], bl[2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int kr = 16 * l + 2 * t + 8 * hf;
-                    split2(S.Mi[kr * LDA + n], S.Mi[(kr + 1) * LDA + n], bh[hf], bl[hf]);
+                    split2(S.Mi[kr * LA + n], S.Mi[(kr + 1) * LA + n], bh[hf], bl[hf]);
                 }
                 mma_x3(acc, ah, al, bh[0], bh[1], bl[0], bl[1]);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                S.Mi[(16 * i + g + 8 * (e >> 1)) * LDA + 16 * j + 8 * (warp & 1) + 2 * t + (e & 1)] = acc[e];
+                S.Mi[(16 * i + g + 8 * (e >> 1)) * LA + 16 * j + 8 * (warp & 1) + 2 * t + (e & 1)] = acc[e];
         }
         __syncthreads();
     }
@@ -544,14 +548,16 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         for (int i = tid; i < CH * CH / 2; i += BT) {
             const int r = (2 * i) / CH, s = (2 * i) % CH, o = sw128(r, 2 * s);
             uint32_t hi, lo;
-            split2(S.Aqk[r * LDA + s], S.Aqk[r * LDA + s + 1], hi, lo);
+            const float2 aq = *reinterpret_cast<const float2*>(&S.Aqk[r * LA + s]);
+            const float2 mi = *reinterpret_cast<const float2*>(&S.Mi[r * LA + s]);
+            const float2 ak = *reinterpret_cast<const float2*>(&S.Akk[r * LA + s]);
+            split2(aq.x, aq.y, hi, lo);
             *reinterpret_cast<uint32_t*>(ast + o) = hi;
             *reinterpret_cast<uint32_t*>(ast + 8192 + o) = lo;
-            split2(S.Mi[r * LDA + s], S.Mi[r * LDA + s + 1], hi, lo);
+            split2(mi.x, mi.y, hi, lo);
             *reinterpret_cast<uint32_t*>(ast + 2 * 8192 + o) = hi;
             *reinterpret_cast<uint32_t*>(ast + 3 * 8192 + o) = lo;
-            *reinterpret_cast<float2*>(S.x.akk_st + (s >> 5) * 8192 + sw128(r, (s & 31) * 4)) =
-                make_float2(S.Akk[r * LDA + s], S.Akk[r * LDA + s + 1]);
+            *reinterpret_cast<float2*>(S.x.akk_st + (s >> 5) * 8192 + sw128(r, (s & 31) * 4)) = ak;
         }
     }
     // split A fragments of Minv and Minv diag(beta), built once per lower 16 x 16 block (mt, ks)
@@ -565,7 +571,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
             const int row = 16 * mt + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
-            const float m0 = S.Mi[row * LDA + col], m1 = S.Mi[row * LDA + col + 1];
+            const float2 m2 = *reinterpret_cast<const float2*>(&S.Mi[row * LA + col]);
+            const float m0 = m2.x, m1 = m2.y;
             split2(m0, m1, mh[rr], ml[rr]);
             split2(m0 * S.beta[col], m1 * S.beta[col + 1], bh_[rr], bl_[rr]);
         }

@@ -23,6 +23,11 @@ namespace {
 // the column-wise reads below free of bank conflicts:
 //   q, k:      two blocks [64 tokens][64 channels] bf16 (channels 0..63, 64..127), element qk_at
 //   dAqk, dM:  two blocks [64 rows][32 columns] fp32 (columns 0..31, 32..63), element a_at
+// row stride (floats) of the gam, dQ, dK, dG tiles: 8 banks per row, so the paired (8-byte)
+// accesses of step 3's epilogues (rows g, g + 8, columns 2t, 2t + 1 of a quad-lane layout) meet
+// no bank conflict
+constexpr int LG = D + 8;
+
 __device__ __forceinline__ int qk_at(int r, int c) {
     return (c >> 6) * (CH * 64) + r * 64 + ((((c >> 3) & 7) ^ (r & 7)) << 3) + (c & 7);
 }
@@ -33,10 +38,10 @@ __device__ __forceinline__ int a_at(int r, int c) {
 struct BwdIntraSmem {
     __nv_bfloat16 qb[2 * CH * 64], kb[2 * CH * 64];  // q, k as given (bf16); q^ = q * rq
     float dA[2 * CH * 32], dAk[2 * CH * 32];         // dAqk and dAkk = beta_r dM
-    float gam[CH * LDP];                             // in-chunk cumsum of g
+    float gam[CH * LG];                             // in-chunk cumsum of g
     // accumulators of dq^, dk^, dgam; until step 2 the dQ / dK tiles hold, densely, rows 0..31 of
     // dQg then P (dQ tile) and of dKb then dR (dK tile), copied during the previous item
-    float dQ[CH * LDP], dK[CH * LDP], dG[CH * LDP];
+    float dQ[CH * LG], dK[CH * LG], dG[CH * LG];
     float beta[CH], rq[CH], rk[CH];
     float dbp[CH];  // per-row dbeta, accumulated in steps 1-2 in a fixed order
     float fin[32];  // last-level partials of step 7
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int i = tid + BT * k, r = i >> 5, c = (i & 31) * 4;
-        *reinterpret_cast<float4*>(&S.gam[r * LDP + c]) = pgm[k];
+        *reinterpret_cast<float4*>(&S.gam[r * LG + c]) = pgm[k];
     }
     __syncthreads();  // beta, gam, the zero rows of q / k
     if (*reinterpret_cast<volatile int*>(&S.abort)) break;
@@ -258,8 +263,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         for (int k = 0; k < 2; ++k) {
             const int i = tid + BT * (2 * half + k), r = i >> 5, c0 = (i & 31) * 4;
             const float dgn = S.dA[a_at(r, r)], br = S.beta[r], rqr = rqs(r), rkr = rks(r);
-            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LDP + c0]);
-            const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LDP + c0]);
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LG + c0]);
+            const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LG + c0]);
             const uint2 qb2 = *reinterpret_cast<const uint2*>(&S.qb[qk_at(r, c0)]);
             const uint2 kb2 = *reinterpret_cast<const uint2*>(&S.kb[qk_at(r, c0)]);
             __nv_bfloat162 qa, qb_, ka, kb_, va_, vb_;
@@ -293,9 +298,9 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
                 db = fmaf(ar[j], vvv[j], db);
                 db = fmaf(-kv * er, ap[j], db);
             }
-            *reinterpret_cast<float4*>(&S.dQ[r * LDP + c0]) = make_float4(oq[0], oq[1], oq[2], oq[3]);
-            *reinterpret_cast<float4*>(&S.dK[r * LDP + c0]) = make_float4(ok[0], ok[1], ok[2], ok[3]);
-            *reinterpret_cast<float4*>(&S.dG[r * LDP + c0]) = make_float4(og[0], og[1], og[2], og[3]);
+            *reinterpret_cast<float4*>(&S.dQ[r * LG + c0]) = make_float4(oq[0], oq[1], oq[2], oq[3]);
+            *reinterpret_cast<float4*>(&S.dK[r * LG + c0]) = make_float4(ok[0], ok[1], ok[2], ok[3]);
+            *reinterpret_cast<float4*>(&S.dG[r * LG + c0]) = make_float4(og[0], og[1], og[2], og[3]);
             if (r < L)
                 store_out4(p.dv, (size_t(t0 + r) * p.H + h) * D + c0,
                            make_float4(br * ar[0], br * ar[1], br * ar[2], br * ar[3]), p.out_fp32);
@@ -352,18 +357,18 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             float aq[3][4] = {}, ak[3][4] = {};
 #pragma unroll
             for (int ks = 0; ks < 3; ++ks) {
-                const float g1 = S.gam[16 * (ks + 1) * LDP + c];
+                const float g1 = S.gam[16 * (ks + 1) * LG + c];
                 float xb[2][2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int s0 = 16 * ks + 2 * t + 8 * hf;
-                    xb[hf][0] = ldk(kx0, s0) * __expf(g1 - S.gam[s0 * LDP + c]);
-                    xb[hf][1] = ldk(kx1, s0 + 1) * __expf(g1 - S.gam[(s0 + 1) * LDP + c]);
+                    xb[hf][0] = ldk(kx0, s0) * __expf(g1 - S.gam[s0 * LG + c]);
+                    xb[hf][1] = ldk(kx1, s0 + 1) * __expf(g1 - S.gam[(s0 + 1) * LG + c]);
                 }
 #pragma unroll
                 for (int i = ks + 1; i < 4; ++i) {
                     const int pair = i * (i - 1) / 2 + ks;
-                    const float R = i == ks + 1 ? 1.f : __expf(S.gam[16 * i * LDP + c] - g1);
+                    const float R = i == ks + 1 ? 1.f : __expf(S.gam[16 * i * LG + c] - g1);
                     uint32_t qh[4], ql[4], kh[4], kl[4], bh[2], bl[2];
                     afrag(2 * pair, qh, ql);
                     afrag(2 * pair + 1, kh, kl);
@@ -375,15 +380,23 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             }
 #pragma unroll
             for (int i = 1; i < 4; ++i) {
-                const int ref = 16 * i;
+                const int ref = 16 * i, cc = 8 * w + 2 * t;  // columns cc, cc + 1 (paired accesses)
+                const float2 gref = *reinterpret_cast<const float2*>(&S.gam[ref * LG + cc]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = 16 * i + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
-                    const float sc = __expf(S.gam[r * LDP + cc] - S.gam[ref * LDP + cc]);
-                    const float vq = aq[i - 1][e] * sc, vk = ak[i - 1][e] * sc;
-                    S.dQ[r * LDP + cc] += vq;
-                    S.dK[r * LDP + cc] += vk;
-                    S.dG[r * LDP + cc] += ldq(ex + (e & 1), r) * vq + ldk(ex + (e & 1), r) * vk;
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int r = 16 * i + g + 8 * hf;
+                    const float2 gr = *reinterpret_cast<const float2*>(&S.gam[r * LG + cc]);
+                    const float s0 = __expf(gr.x - gref.x), s1 = __expf(gr.y - gref.y);
+                    const float vq0 = aq[i - 1][2 * hf] * s0, vq1 = aq[i - 1][2 * hf + 1] * s1;
+                    const float vk0 = ak[i - 1][2 * hf] * s0, vk1 = ak[i - 1][2 * hf + 1] * s1;
+                    float2* pq = reinterpret_cast<float2*>(&S.dQ[r * LG + cc]);
+                    float2* pk = reinterpret_cast<float2*>(&S.dK[r * LG + cc]);
+                    float2* pg = reinterpret_cast<float2*>(&S.dG[r * LG + cc]);
+                    const float2 oq = *pq, ok = *pk, og = *pg;
+                    *pq = make_float2(oq.x + vq0, oq.y + vq1);
+                    *pk = make_float2(ok.x + vk0, ok.y + vk1);
+                    *pg = make_float2(og.x + (ldq(ex, r) * vq0 + ldk(ex, r) * vk0),
+                                      og.y + (ldq(ex + 1, r) * vq1 + ldk(ex + 1, r) * vk1));
                 }
             }
         }
@@ -395,13 +408,13 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             float bacc[3][4] = {};
 #pragma unroll
             for (int ks = 1; ks < 4; ++ks) {
-                const float g1 = S.gam[(16 * ks - 1) * LDP + c];
+                const float g1 = S.gam[(16 * ks - 1) * LG + c];
                 float xq[2][2], xk[2][2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int r0 = 16 * ks + 2 * t + 8 * hf;
-                    const float e0 = __expf(S.gam[r0 * LDP + c] - g1);
-                    const float e1 = __expf(S.gam[(r0 + 1) * LDP + c] - g1);
+                    const float e0 = __expf(S.gam[r0 * LG + c] - g1);
+                    const float e1 = __expf(S.gam[(r0 + 1) * LG + c] - g1);
                     xq[hf][0] = ldq(kx0, r0) * e0;
                     xq[hf][1] = ldq(kx1, r0 + 1) * e1;
                     xk[hf][0] = ldk(kx0, r0) * e0;
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
                 for (int j = 0; j < ks; ++j) {
                     const int pair = 6 + (j == 0 ? 0 : j == 1 ? 3 : 5) + ks - j - 1;
-                    const float R = j == ks - 1 ? 1.f : __expf(g1 - S.gam[(16 * j + 15) * LDP + c]);
+                    const float R = j == ks - 1 ? 1.f : __expf(g1 - S.gam[(16 * j + 15) * LG + c]);
                     uint32_t qh[4], ql[4], kh[4], kl[4], qbh[2], qbl[2], kbh[2], kbl[2];
                     afrag(2 * pair, qh, ql);
                     afrag(2 * pair + 1, kh, kl);
@@ -425,13 +438,19 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             }
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
-                const int ref = 16 * j + 15;
+                const int ref = 16 * j + 15, cc = 8 * w + 2 * t;  // columns cc, cc + 1 (paired)
+                const float2 gref = *reinterpret_cast<const float2*>(&S.gam[ref * LG + cc]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int sr = 16 * j + g + 8 * (e >> 1), cc = 8 * w + 2 * t + (e & 1);
-                    const float vb = bacc[j][e] * __expf(S.gam[ref * LDP + cc] - S.gam[sr * LDP + cc]);
-                    S.dK[sr * LDP + cc] += vb;
-                    S.dG[sr * LDP + cc] -= ldk(ex + (e & 1), sr) * vb;
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int sr = 16 * j + g + 8 * hf;
+                    const float2 gs = *reinterpret_cast<const float2*>(&S.gam[sr * LG + cc]);
+                    const float vb0 = bacc[j][2 * hf] * __expf(gref.x - gs.x);
+                    const float vb1 = bacc[j][2 * hf + 1] * __expf(gref.y - gs.y);
+                    float2* pk = reinterpret_cast<float2*>(&S.dK[sr * LG + cc]);
+                    float2* pg = reinterpret_cast<float2*>(&S.dG[sr * LG + cc]);
+                    const float2 ok = *pk, og = *pg;
+                    *pk = make_float2(ok.x + vb0, ok.y + vb1);
+                    *pg = make_float2(og.x - ldk(ex, sr) * vb0, og.y - ldk(ex + 1, sr) * vb1);
                 }
             }
         }
@@ -453,12 +472,12 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             kv[x] = Kv(base + x, c);
         }
         {
-            const float g7 = S.gam[(base + 7) * LDP + c];
+            const float g7 = S.gam[(base + 7) * LG + c];
             float F[8], G[8], Y[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                F[j] = __expf(S.gam[(base + 8 + j) * LDP + c] - g7);
-                G[j] = __expf(g7 - S.gam[(base + j) * LDP + c]);
+                F[j] = __expf(S.gam[(base + 8 + j) * LG + c] - g7);
+                G[j] = __expf(g7 - S.gam[(base + j) * LG + c]);
                 Y[j] = G[j] * kv[j];
                 bb[j] = 0.f;
             }
@@ -491,10 +510,10 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         }
         float ed[16];  // ed[x] = e^(gam_x - gam_{x-1}) (x = 8 starts a block: unused)
         {
-            float prev = S.gam[base * LDP + c];
+            float prev = S.gam[base * LG + c];
 #pragma unroll
             for (int x = 1; x < 16; ++x) {
-                const float cur = S.gam[(base + x) * LDP + c];
+                const float cur = S.gam[(base + x) * LG + c];
                 ed[x] = x == 8 ? 1.f : __expf(cur - prev);
                 prev = cur;
             }
@@ -527,9 +546,9 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
             const int r = base + x;
-            S.dQ[r * LDP + c] += aq[x];
-            S.dK[r * LDP + c] += ak[x] + bb[x];
-            S.dG[r * LDP + c] += qv[x] * aq[x] + kv[x] * (ak[x] - bb[x]);
+            S.dQ[r * LG + c] += aq[x];
+            S.dK[r * LG + c] += ak[x] + bb[x];
+            S.dG[r * LG + c] += qv[x] * aq[x] + kv[x] * (ak[x] - bb[x]);
         }
     }
     __syncthreads();
@@ -551,12 +570,12 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     //    cumsum over the chunk; four threads per channel (16 rows each), fixed order
     {
         const int c = tid & (D - 1), qu = tid >> 7, r0 = 16 * qu;
-        const float gl = S.gam[(CH - 1) * LDP + c];
+        const float gl = S.gam[(CH - 1) * LG + c];
         *reinterpret_cast<float4*>(&S.kbp[w * D + 4 * lane]) = make_float4(kbp[0], kbp[1], kbp[2], kbp[3]);
         float suf = 0.f;  // suffix sums inside the quarter
         for (int r = r0 + 15; r >= r0; --r) {
-            suf += S.dG[r * LDP + c];
-            S.dG[r * LDP + c] = suf;
+            suf += S.dG[r * LG + c];
+            S.dG[r * LG + c] = suf;
         }
         S.red[tid] = suf;  // quarter total
         __syncthreads();
@@ -566,7 +585,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         const float dgl = __expf(gl) * (rs0 + rs1) + part;
         float carry = 0.f;  // totals of the later quarters
         for (int q2 = qu + 1; q2 < 4; ++q2) carry += S.red[q2 * D + c];
-        for (int r = r0; r < r0 + 16; ++r) S.dG[r * LDP + c] += carry + dgl;
+        for (int r = r0; r < r0 + 16; ++r) S.dG[r * LG + c] += carry + dgl;
     }
     __syncthreads();
 
@@ -574,8 +593,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     for (int r = w; r < L; r += NW) {
         const size_t base = (size_t(t0 + r) * p.H + h) * D;
         const int c0 = 4 * lane;
-        const float4 dq4 = *reinterpret_cast<const float4*>(&S.dQ[r * LDP + c0]);
-        const float4 dk4 = *reinterpret_cast<const float4*>(&S.dK[r * LDP + c0]);
+        const float4 dq4 = *reinterpret_cast<const float4*>(&S.dQ[r * LG + c0]);
+        const float4 dk4 = *reinterpret_cast<const float4*>(&S.dK[r * LG + c0]);
         float dq[4] = {dq4.x, dq4.y, dq4.z, dq4.w}, dk[4] = {dk4.x, dk4.y, dk4.z, dk4.w};
         if (L2N) {
             float qv[4], kv[4], pq = 0.f, pk = 0.f;
@@ -619,7 +638,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
             if (r < L)
                 *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
-                    *reinterpret_cast<const float4*>(&S.dG[r * LDP + c4]);
+                    *reinterpret_cast<const float4*>(&S.dG[r * LG + c4]);
         }
     } else {
         const float eA = expf(aLog), ieA = 1.f / eA;
@@ -629,9 +648,9 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
             const bool ok = r < L;
-            const float4 dg4 = *reinterpret_cast<const float4*>(&S.dG[r * LDP + c4]);
-            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LDP + c4]);
-            const float4 gp4 = r > 0 ? *reinterpret_cast<const float4*>(&S.gam[(r - 1) * LDP + c4])
+            const float4 dg4 = *reinterpret_cast<const float4*>(&S.dG[r * LG + c4]);
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LG + c4]);
+            const float4 gp4 = r > 0 ? *reinterpret_cast<const float4*>(&S.gam[(r - 1) * LG + c4])
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
             const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
             const float gv[4] = {g4.x - gp4.x, g4.y - gp4.y, g4.z - gp4.z, g4.w - gp4.w};

@@ -323,8 +323,15 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const int m = m0 + g + 8 * (rr & 1), kx = k0 + 2 * t + 8 * (rr >> 1);
-                const float x0 = col ? A[a_at(kx, m)] : A[a_at(m, kx)];
-                const float x1 = col ? A[a_at(kx + 1, m)] : A[a_at(m, kx + 1)];
+                float x0, x1;
+                if (col) {
+                    x0 = A[a_at(kx, m)];
+                    x1 = A[a_at(kx + 1, m)];
+                } else {  // columns kx, kx + 1 share a 16-byte chunk (kx even): one paired load
+                    const float2 v = *reinterpret_cast<const float2*>(&A[a_at(m, kx)]);
+                    x0 = v.x;
+                    x1 = v.y;
+                }
                 split2(x0, x1, hi[rr], lo[rr]);
             }
             S.Af[f][0][lane] = make_uint4(hi[0], hi[1], hi[2], hi[3]);

@@ -24,9 +24,11 @@ constexpr int LQ = D + 8;
 // and staging reads) and 4 banks per row (the G and X phases' column-wise B reads meet no conflict)
 constexpr int LA = CH + 4;
 
-// The base is 1024-byte aligned; so are k, akk_st and u, which double as 128-byte-swizzled
-// staging tiles of the TMA stores of the products: Aqk / Minv hi / lo in k and Akk in akk_st
-// (after step 5), W hi / lo in u (after step 6, until the next item's step 4a).
+// The base is 1024-byte aligned; so are q, k, x, u and v, which double as 128-byte-swizzled tiles
+// of the tensor-memory accelerator: after step 5 Aqk / Minv hi / lo in k (TMA store sources; Minv
+// also the A operand of W) and Akk in x.akk_st, Minv diag(beta) hi / lo in q (A operand of U),
+// beta K e^gam hi / lo in u and V in v (B operands of W and U); after step 6 W hi / lo in u (TMA
+// store source until the next item's step 4a).
 struct IntraSmem {
     float q[CH * LQ], k[CH * LQ], gam[CH * LQ];
     union {
@@ -38,14 +40,17 @@ struct IntraSmem {
         struct {
             __nv_bfloat16 Ks[3][2][16 * LB];  // B operands of the off-diagonal blocks (hi, lo)
         } a;
-        struct {
-            __nv_bfloat16 bKg[2][CH * LB];  // beta K e^gam (hi, lo), written during step 5
-        } b;
+        // beta K e^gam (hi, lo) as the MN-major B operand of W: [plane][column block of 64][64
+        // token rows][128 bytes], written during step 5
+        unsigned char bkg[2 * 16384];
         unsigned char wst[4 * 8192];  // W staged: boxes [plane][column block] of 64 rows x 64 bf16
     } u;
+    unsigned char v[2 * 8192];  // V (exact in bf16), MN-major B of U: [column block][64 rows][128 B]
     float Akk[CH * LA], Aqk[CH * LA], Mi[CH * LA];
     float beta[CH];
-    __nv_bfloat16 v[CH * LB];  // V (exact in bf16)
+    uint64_t mbar[2];  // 0: completion of step 6's MMAs; 1: spare of the abort path
+    uint32_t tslot;    // TMEM base address
+    int abort;         // a bounded wait timed out
 };
 
 // off-diagonal sub-chunk pairs (i, j), i > j, one per warp
@@ -56,8 +61,11 @@ static_assert(sizeof(IntraSmem) + 1024 <= 232448, "intra shared memory above the
 static_assert(offsetof(IntraSmem, Akk) % 16 == 0 && (CH * LA) % 4 == 0,
               "the 64 x 64 tiles are cleared with 16-byte stores");
 static_assert(offsetof(IntraSmem, k) % 1024 == 0 && offsetof(IntraSmem, x) % 1024 == 0 &&
-                  offsetof(IntraSmem, u) % 1024 == 0 && CH * LQ * 4 >= 4 * 8192,
-              "staging tiles of the TMA stores must be 1024-byte aligned and hold four boxes");
+                  offsetof(IntraSmem, u) % 1024 == 0 && offsetof(IntraSmem, v) % 1024 == 0 &&
+                  CH * LQ * 4 >= 4 * 8192,
+              "operand / staging tiles must be 1024-byte aligned and hold four boxes");
+// (rows 64..127 of step 6's M = 128 A operands read the 8 KB after each 64-row tile: the next
+// tile or the next member of this image, never past it; those accumulator rows are not read)
 
 // Byte offset of (row, byte) inside a box of 64 rows x 128 bytes in the TMA unit's 128-byte
 // swizzle: the 16-byte chunk j of row r sits at chunk position j ^ (r % 8).
@@ -119,7 +127,10 @@ size_t intra_smem_bytes() { return sizeof(IntraSmem) + 1024; }  // + alignment s
 // bursts (q, k, then the gate) so that no burst fills the memory request queue of the SM.  The
 // hi / lo planes of Aqk, Minv and W and Akk leave through TMA stores from staging tiles (thread 0
 // issues them and waits for their reads of shared memory before the tiles are rewritten): the
-// small matrices' stores run during step 6, W's during the next item's first steps.
+// small matrices' stores run during step 6, W's during the next item's first steps.  Step 6 (W
+// and U) runs as tcgen05 MMAs issued by thread 0 into 256 TMEM columns held for the whole kernel;
+// every wait on their completion is bounded (on expiry the block reports KDA_ERR_TIMEOUT, lets
+// its MMAs drain, frees its TMEM and stops).
 __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const __grid_constant__ TcMaps tm) {
     constexpr int BT = INTRA_THREADS, NW = BT / 32;
     extern __shared__ __align__(16) unsigned char smraw[];
@@ -174,10 +185,22 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         for (int k = 0; k < 2; ++k) {
             const int i = tid + BT * k, r = i >> 4, c8 = (i & 15) * 8;
             const bool ok = r < nL;
-            cp16z(&S.v[r * LB + c8], p.v + (size_t(nT0 + (ok ? r : 0)) * p.H + nh) * D + c8, ok);
+            cp16z(S.v + (c8 >> 6) * 8192 + sw128(r, (c8 & 63) * 2),
+                  p.v + (size_t(nT0 + (ok ? r : 0)) * p.H + nh) * D + c8, ok);
         }
         cp_commit();
     };
+    if (tid == 0) {
+        tc::mbar_init(&S.mbar[0], 1);
+        S.abort = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) tc::tmem_alloc(&S.tslot, 256);  // W in columns 0..127, U in 128..255
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t taddr = S.tslot;
+    uint32_t mph = 0;  // phase parity of the MMA barrier
     if (int(blockIdx.x) < items) {
         fetch(blockIdx.x, p.chunk_tab[blockIdx.x / p.H], 7);
         fetch_v();
@@ -434,9 +457,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     //    the blocks off the diagonal X_ij = sum_{l=j}^{i-1} G_il X_lj (X_jj = D_j) by increasing
     //    block distance
     if (tid >= 64) {
-        // meanwhile, the other warps form step 6's operand beta K e^gam (hi, lo) (Ks and the
-        // partial sums it overwrites were consumed in step 4) and the elementwise outputs of the
-        // recurrence: Qg = Q e^gam, Kb = K e^(gL - gam) (hi, lo) and gam
+        // meanwhile, the other warps form step 6's operand beta K e^gam (hi, lo) (Ks, which it
+        // overwrites, was consumed in step 4) and the elementwise outputs of the recurrence:
+        // Qg = Q e^gam, Kb = K e^(gL - gam) (hi, lo) and gam
         __nv_bfloat16* Qh = p.Qh + chd * CH * D;
         __nv_bfloat16* Ql = p.Ql + chd * CH * D;
         __nv_bfloat16* Kh = p.Kh + chd * CH * D;
@@ -454,8 +477,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             uint32_t h0, l0, h1, l1;
             split2(br * kv.x * e0, br * kv.y * e1, h0, l0);
             split2(br * kv.z * e2, br * kv.w * e3, h1, l1);
-            *reinterpret_cast<uint2*>(&S.u.b.bKg[0][r * LB + c]) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2*>(&S.u.b.bKg[1][r * LB + c]) = make_uint2(l0, l1);
+            const int bo = (c >> 6) * 8192 + sw128(r, (c & 63) * 2);
+            *reinterpret_cast<uint2*>(S.u.bkg + bo) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(S.u.bkg + 16384 + bo) = make_uint2(l0, l1);
             split2(qv.x * e0, qv.y * e1, h0, l0);
             split2(qv.z * e2, qv.w * e3, h1, l1);
             reinterpret_cast<uint2*>(Qh)[i] = make_uint2(h0, h1);
@@ -542,45 +566,29 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     // 7 (ahead of step 6). The small matrices, staged for TMA stores whose reads of shared memory
     //    overlap step 6: Aqk and Minv hi / lo in the k tile (boxes Ah, Al, Mh, Ml of 64 rows x 64
     //    bf16; k is not read after step 5), Akk in akk_st (the elementwise outputs were written
-    //    during step 5)
+    //    during step 5).  Minv's planes double as the K-major A operand of W; Minv diag(beta)
+    //    hi / lo, the A operand of U, go to the q tile (not read after step 5).
     {
         unsigned char* ast = reinterpret_cast<unsigned char*>(S.k);
+        unsigned char* mbt = reinterpret_cast<unsigned char*>(S.q);
         for (int i = tid; i < CH * CH / 2; i += BT) {
             const int r = (2 * i) / CH, s = (2 * i) % CH, o = sw128(r, 2 * s);
             uint32_t hi, lo;
             const float2 aq = *reinterpret_cast<const float2*>(&S.Aqk[r * LA + s]);
             const float2 mi = *reinterpret_cast<const float2*>(&S.Mi[r * LA + s]);
             const float2 ak = *reinterpret_cast<const float2*>(&S.Akk[r * LA + s]);
+            const float2 bs = *reinterpret_cast<const float2*>(&S.beta[s]);
             split2(aq.x, aq.y, hi, lo);
             *reinterpret_cast<uint32_t*>(ast + o) = hi;
             *reinterpret_cast<uint32_t*>(ast + 8192 + o) = lo;
             split2(mi.x, mi.y, hi, lo);
             *reinterpret_cast<uint32_t*>(ast + 2 * 8192 + o) = hi;
             *reinterpret_cast<uint32_t*>(ast + 3 * 8192 + o) = lo;
+            split2(mi.x * bs.x, mi.y * bs.y, hi, lo);
+            *reinterpret_cast<uint32_t*>(mbt + o) = hi;
+            *reinterpret_cast<uint32_t*>(mbt + 8192 + o) = lo;
             *reinterpret_cast<float2*>(S.x.akk_st + (s >> 5) * 8192 + sw128(r, (s & 31) * 4)) = ak;
         }
-    }
-    // split A fragments of Minv and Minv diag(beta), built once per lower 16 x 16 block (mt, ks)
-    // by warp mt (mt + 1) / 2 + ks (four warps of step 6 share each block), into the q tile,
-    // which nothing reads after step 5: [block][Minv hi, lo, Minv diag(beta) hi, lo][lane]
-    uint4* mfrag = reinterpret_cast<uint4*>(S.q);
-    if (warp < 10) {
-        const int mt = warp < 1 ? 0 : warp < 3 ? 1 : warp < 6 ? 2 : 3;
-        const int ks = warp - mt * (mt + 1) / 2;
-        uint32_t mh[4], ml[4], bh_[4], bl_[4];
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int row = 16 * mt + g + 8 * (rr & 1), col = 16 * ks + 2 * t + 8 * (rr >> 1);
-            const float2 m2 = *reinterpret_cast<const float2*>(&S.Mi[row * LA + col]);
-            const float m0 = m2.x, m1 = m2.y;
-            split2(m0, m1, mh[rr], ml[rr]);
-            split2(m0 * S.beta[col], m1 * S.beta[col + 1], bh_[rr], bl_[rr]);
-        }
-        uint4* f = mfrag + warp * 4 * 32 + lane;
-        f[0] = make_uint4(mh[0], mh[1], mh[2], mh[3]);
-        f[32] = make_uint4(ml[0], ml[1], ml[2], ml[3]);
-        f[64] = make_uint4(bh_[0], bh_[1], bh_[2], bh_[3]);
-        f[96] = make_uint4(bl_[0], bl_[1], bl_[2], bl_[3]);
     }
     // this item's v tile (copied during the previous item's last phase; the next gate may stay in
     // flight)
@@ -589,8 +597,10 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     else
         cp_wait<0>();
     if (more) fetch(item + gridDim.x, tab_next, 2);
-    tc::fence_async_smem();  // this thread's staged values, before the TMA unit reads them
-    __syncthreads();  // every thread's part of the v tile, the Minv fragments, the staged matrices
+    tc::fence_async_smem();  // this thread's staged values and operands, before the async proxy reads
+    tc::fence_before_sync();
+    __syncthreads();  // every thread's part of the v tile, the operands, the staged matrices
+    tc::fence_after_sync();
     if (tid == 0) {
         const int z[4] = {tm.zAh, tm.zAl, tm.zMh, tm.zMl};
 #pragma unroll
@@ -599,65 +609,62 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
         for (int b = 0; b < 2; ++b) tc::tma_store3(&tm.mAkk, 32 * b, 0, int(chd), S.x.akk_st + b * 8192);
         tc::bulk_commit();
-    }
-
-    // 6. W = Minv (beta K e^gam) and U = (Minv diag(beta)) V on tensor cores.  Minv is lower
-    //    triangular, so row block mt takes mt + 1 k-steps; a warp takes the row blocks {0, 3} or
-    //    {1, 2} (five k-steps either way) over 16 columns.
-    {
-        const int m0 = (warp & 1) ? 1 : 0, m1 = 3 - m0, n0 = 16 * (warp >> 1);
-        float accW[2][2][4] = {}, accU[2][2][4] = {};  // [row block m0 / m1][n-tile][fragment]
+        // 6. W = Minv (beta K e^gam) (TMEM columns 0..127) and U = (Minv diag(beta)) V (columns
+        //    128..255): M = 128 (rows 0..63 are the chunk's tokens, rows 64..127 are not read), N =
+        //    128 channels, K = 64 tokens in four steps; A K-major (64 tokens = one 128-byte swizzle
+        //    atom per row), B MN-major (two 64-channel atoms, LBO 8 KB).  W takes the split terms
+        //    Minv_hi Kg_lo + Minv_lo Kg_hi + Minv_hi Kg_hi, U the terms of the two Minv diag(beta)
+        //    planes against V (exact in bf16).
+        const uint32_t sK = smem_u32(S.k), sQ = smem_u32(S.q), sB = smem_u32(S.u.bkg), sV = smem_u32(S.v);
+        const uint64_t aMh = tc::sdesc(sK + 2 * 8192, 16, 1024), aMl = tc::sdesc(sK + 3 * 8192, 16, 1024);
+        const uint64_t aBh = tc::sdesc(sQ, 16, 1024), aBl = tc::sdesc(sQ + 8192, 16, 1024);
+        const uint64_t bKh = tc::sdesc(sB, 8192, 1024), bKl = tc::sdesc(sB + 16384, 8192, 1024);
+        const uint64_t bV = tc::sdesc(sV, 8192, 1024);
+        const uint32_t id = tc::idesc_bf16(128, 128, false, true);
+        const uint64_t wa[3] = {aMh, aMl, aMh}, wb[3] = {bKl, bKh, bKh};
+        uint32_t acc = 0;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            if (ks > m1) break;
-            uint32_t kh[4], kl[4], vv[4];
-            ldsm4t(kh, bk_addr(S.u.b.bKg[0], LB, 16 * ks, n0, lane));
-            ldsm4t(kl, bk_addr(S.u.b.bKg[1], LB, 16 * ks, n0, lane));
-            ldsm4t(vv, bk_addr(S.v, LB, 16 * ks, n0, lane));
+        for (int t3 = 0; t3 < 3; ++t3)
 #pragma unroll
-            for (int bi = 0; bi < 2; ++bi) {
-                const int mt = bi ? m1 : m0;
-                if (ks > mt) continue;
-                const uint4* f = mfrag + (mt * (mt + 1) / 2 + ks) * 4 * 32 + lane;
-                const uint4 a0 = f[0], a1 = f[32], a2 = f[64], a3 = f[96];
-                const uint32_t mh[4] = {a0.x, a0.y, a0.z, a0.w}, ml[4] = {a1.x, a1.y, a1.z, a1.w};
-                const uint32_t bh_[4] = {a2.x, a2.y, a2.z, a2.w}, bl_[4] = {a3.x, a3.y, a3.z, a3.w};
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    mma_x3(accW[bi][hh], mh, ml, kh[2 * hh], kh[2 * hh + 1], kl[2 * hh], kl[2 * hh + 1]);
-                    mma_x2(accU[bi][hh], bh_, bl_, vv[2 * hh], vv[2 * hh + 1]);
-                }
+            for (int ks = 0; ks < 4; ++ks) {
+                tc::mma(taddr, wa[t3] + uint64_t((ks * 32) >> 4), wb[t3] + uint64_t((ks * 2048) >> 4), id, acc);
+                acc = 1;
             }
-        }
-        float* U = p.U + chd * CH * D;
+        acc = 0;
 #pragma unroll
-        for (int bi = 0; bi < 2; ++bi)
+        for (int t2 = 0; t2 < 2; ++t2)
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int row = 16 * (bi ? m1 : m0) + g + 8 * hf, col = n0 + 8 * hh + 2 * t;
-                    *reinterpret_cast<float2*>(U + row * D + col) =
-                        make_float2(accU[bi][hh][2 * hf], accU[bi][hh][2 * hf + 1]);
-                }
-        __syncthreads();  // every warp's reads of bKg are done: u becomes W's staging tile
-#pragma unroll
-        for (int bi = 0; bi < 2; ++bi)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int row = 16 * (bi ? m1 : m0) + g + 8 * hf, col = n0 + 8 * hh + 2 * t;
-                    uint32_t hi, lo;
-                    split2(accW[bi][hh][2 * hf], accW[bi][hh][2 * hf + 1], hi, lo);
-                    const int wo = (col >> 6) * 8192 + sw128(row, (col & 63) * 2);
-                    *reinterpret_cast<uint32_t*>(S.u.wst + wo) = hi;
-                    *reinterpret_cast<uint32_t*>(S.u.wst + 2 * 8192 + wo) = lo;
-                }
+            for (int ks = 0; ks < 4; ++ks) {
+                tc::mma(taddr + 128, (t2 ? aBh : aBl) + uint64_t((ks * 32) >> 4),
+                        bV + uint64_t((ks * 2048) >> 4), id, acc);
+                acc = 1;
+            }
+        tc::mma_commit(&S.mbar[0]);
     }
+    // epilogue: warps w % 4 < 2 hold the token rows (TMEM lanes 0..63), 32 columns each (w / 4):
+    // U straight to global memory, W split into its staging tile (u: the MMAs have read beta K
+    // e^gam by then)
+    if (!tc::mbar_wait(&S.mbar[0], mph)) S.abort = 1;
+    mph ^= 1u;
+    tc::fence_after_sync();
+    {
+        const int qd = warp & 3, cq = warp >> 2;
+        if (qd < 2) {
+            const int r = 32 * qd + lane;
+            const uint32_t tl = taddr + (uint32_t(32 * qd) << 16);
+            float v[32];
+            tc::tmem_ld32(tl + 128 + 32 * cq, v);
+            tc::st_rows_paired_f32<32>(p.U + chd * CH * D + size_t(r) * D + 32 * cq, D, v, lane, true, true);
+            tc::tmem_ld32(tl + 32 * cq, v);
+            tc::st_sw128_split32(S.u.wst + (cq >> 1) * 8192, S.u.wst + 16384 + (cq >> 1) * 8192, r,
+                                 32 * (cq & 1), v);
+        }
+    }
+    tc::fence_before_sync();
     tc::fence_async_smem();
     if (tid == 0) tc::bulk_wait_read0();  // the small matrices' stores have read k and akk_st
-    __syncthreads();  // W staged; every thread is done with this item's shared tiles
+    __syncthreads();  // W staged; every thread is done with this item's shared tiles and TMEM
+    if (*reinterpret_cast<volatile int*>(&S.abort)) break;
     if (tid == 0) {
 #pragma unroll
         for (int b = 0; b < 4; ++b)
@@ -667,7 +674,17 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     }
     if (more) fetch_v();
     }
+    if (tid == 0 && S.abort) {
+        // after a timed-out wait (the device is already in a bad state): let this block's MMAs
+        // finish (bounded) before its TMEM is freed, report
+        tc::drain_mmas(&S.mbar[1], 100000000ull);
+        p.status[0] = KDA_ERR_TIMEOUT;
+    }
+    cp_wait<0>();                    // no cp.async into the tiles is in flight past this point
     if (tid == 0) tc::bulk_wait0();  // the stores are complete before the block ends
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(taddr, 256);
 }
 
 }  // namespace kda

@@ -76,8 +76,9 @@ static_assert(BWD_INTRA_SMEM <= 232448, "backward intra shared memory above the 
 // item no longer reads.  Shared-memory tiles are copied row by row by the TMA unit (issued by warp 0,
 // completion on an mbarrier), so no other warp waits on the issue: once step 4 is done, dAqk and dM;
 // once step 6 is done, q, k and the first half of dQg, P, dKb, dR.  Akk, gam, v, beta and the second
-// half of dQg, P, dKb, dR of the next item go to registers (issued before the current item's output
-// stores, which would otherwise hold them up at the item boundary).  Every wait is bounded; after a timeout the block stops and reports.
+// half of dQg, P, dKb, dR of the next item go to registers, dQg and P issued before the current
+// item's output stores (which would otherwise hold them up at the item boundary), dKb and dR after
+// step 5.  Every wait is bounded; after a timeout the block stops and reports.
 // L2N: the fused L2 norm of q and k is on (row scales rq, rk and their backward); off, the scales
 // are 1 and every multiply by them is compiled out.
 template <bool L2N>
@@ -125,6 +126,13 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             const size_t i = nchd * CH * D / 4 + tid + BT * (2 + k);
             hq[k] = reinterpret_cast<const float4*>(p.dQg)[i];
             hp[k] = reinterpret_cast<const float4*>(p.P)[i];
+        }
+    };
+    // rows 32..63 of dKb, dR: a second, later burst (after step 5)
+    auto fetchA2 = [&](int item) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const size_t i = size_t(item) * CH * D / 4 + tid + BT * (2 + k);
             hb[k] = reinterpret_cast<const float4*>(p.dKb)[i];
             hr[k] = reinterpret_cast<const float4*>(p.dR)[i];
         }
@@ -172,6 +180,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     }
     __syncthreads();
     fetchA(blockIdx.x);
+    fetchA2(blockIdx.x);
     fetchB(blockIdx.x);
     uint32_t ph = 0;  // phase parity of this item's two barriers
 
@@ -569,7 +578,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         fetchA(item + gridDim.x);
     } else {  // defined on every path, so nothing fetched stays live across steps 2-4
         pA[0] = pA[1] = pgm[0] = pgm[1] = pgm[2] = pgm[3] = make_float4(0.f, 0.f, 0.f, 0.f);
-        hq[0] = hq[1] = hp[0] = hp[1] = hb[0] = hb[1] = hr[0] = hr[1] = pA[0];
+        hq[0] = hq[1] = hp[0] = hp[1] = pA[0];
         ntab = make_int4(0, 0, 0, 0);
     }
 
@@ -595,6 +604,10 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         for (int r = r0; r < r0 + 16; ++r) S.dG[r * LG + c] += carry + dgl;
     }
     __syncthreads();
+    if (more)
+        fetchA2(item + gridDim.x);
+    else
+        hb[0] = hb[1] = hr[0] = hr[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 
     // 6. per row: L2-norm backward and the dq, dk, dbeta outputs (warp per row, 4 channels per lane)
     for (int r = w; r < L; r += NW) {

@@ -38,8 +38,9 @@ static_assert(CHAIN_TC_SMEM <= 232448, "tcgen05 chain shared memory above the op
 // values -> B).  256 threads: warp w reads TMEM lanes 32 (w % 4).. and VW / 2 value columns from
 // VW / 2 (w / 4) of its part.  The per-chunk latency scales with VW, so runs with few (document,
 // head) pairs use VW = 16 or 32 (more blocks on the critical path), the others VW = 64.
-// Thread 0 issues the TMA loads and the MMAs.  Operands of chunk c+1 are loaded as soon as the
-// MMA that reads their buffer has completed.
+// Thread 0 issues the MMAs and the TMA stores; thread 96 (warp 3: no Delta rows, and its O rows
+// cost more than a TMA issue) issues the TMA loads, so their issue cost stays off thread 0.
+// Operands of chunk c+1 are loaded as soon as the MMA that reads their buffer has completed.
 template <int VW>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     k_chain_fwd_tc(Params p, int mode, const __grid_constant__ TcMaps tm) {
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int col0 = (hv % (D / VW)) * VW;
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = tc::align1024(smraw);
-    // A1 in, K in, MMA1 done, MMA2 done (+48: spare barrier of the abort path)
+    // A1 in, K in, MMA1 done, MMA2 / MMA3 done (+48: spare barrier of the abort path)
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_BAR + 36);
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int qd = w & 3, cc = VPT * (w >> 2);
     const int row = 32 * qd + lane;  // accumulator row (key for S / D2, token for D1)
+    constexpr int LD = 96;           // the thread that issues the TMA loads
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
     if (*p.status == KDA_ERR_DEVICE_CHECK) return;  // a failed device-side check of this call
@@ -157,9 +159,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     for (int j = 0; j < VPT; ++j) Un[j] = 0.f;
     fetch_next(c0);
 
-    // phase parity of the loads in flight, -1 = none (thread 0's bookkeeping for an early exit)
+    // phase parity of the latest loads (the loader thread's bookkeeping for an early exit: a wait
+    // on it returns at once when they have landed), -1 = none
     int pendA = -1, pendK = -1;
-    if (tid == 0 && c0 < c1) {
+    if (tid == LD && c0 < c1) {
         load_A1(c0);
         load_K(c0);
         pendA = pendK = 0;
@@ -183,7 +186,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // ---- MMA1: D1 = [W; Qg] S ----
         if (tid == 0) {
             if (tc::mbar_wait(&bar[0], ph)) {
-                pendA = -1;
                 tc::fence_after_sync();
                 const uint64_t dAh = tc::sdesc(sA1, 16, 1024), dAl = tc::sdesc(sA1 + 32768, 16, 1024);
                 const uint64_t dSh = tc::sdesc(sS, 1024, 1024), dSl = tc::sdesc(sS + 16384, 1024, 1024);
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (!tc::mbar_wait(&bar[2], ph)) *abort_flag = 1;
         if (tid == 0) stopf[1] = *abort_flag;  // decision at the next barrier
         tc::fence_after_sync();
-        if (tid == 0 && ci + 1 < c1 && !*abort_flag) {
+        if (tid == LD && ci + 1 < c1 && !*abort_flag) {
             load_A1(ci + 1);
             pendA = int(ph ^ 1u);
         }
@@ -246,7 +248,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // ---- MMA2: D2 = Kb^T Delta;  MMA3: D1 += [*; Aqk] Delta ----
         if (tid == 0) {
             if (tc::mbar_wait(&bar[1], ph)) {
-                pendK = -1;
                 tc::fence_after_sync();
                 const uint64_t dKh = tc::sdesc(sKt, 8192, 1024), dKl = tc::sdesc(sKt + 16384, 8192, 1024);
                 const uint64_t dDh = tc::sdesc(sDl, 1024, 1024), dDl = tc::sdesc(sDl + 8192, 1024, 1024);
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (!tc::mbar_wait(&bar[3], ph)) *abort_flag = 1;
         if (tid == 0) stopf[0] = *abort_flag;  // decision at the next step's first barrier
         tc::fence_after_sync();
-        if (tid == 0 && ci + 1 < c1 && !*abort_flag) {
+        if (tid == LD && ci + 1 < c1 && !*abort_flag) {
             load_K(ci + 1);
             pendK = int(ph ^ 1u);
         }
@@ -338,9 +339,11 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // stop
         if (tid == 0) {
             tc::drain_mmas(reinterpret_cast<uint64_t*>(sm + OFF_BAR + 48), 100000000ull);
+            p.status[0] = KDA_ERR_TIMEOUT;
+        }
+        if (tid == LD) {
             if (pendA >= 0) tc::mbar_wait(&bar[0], uint32_t(pendA), 100000000ull);
             if (pendK >= 0) tc::mbar_wait(&bar[1], uint32_t(pendK), 100000000ull);
-            p.status[0] = KDA_ERR_TIMEOUT;
         }
     } else {
         float* out = fwd ? p.ht : (fragX ? p.fragM : p.fragB);
@@ -407,6 +410,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int qd = w & 3, cc = VPT * (w >> 2);
     const int row = 32 * qd + lane;
+    constexpr int LD = 96;  // the thread that issues the TMA loads (warp 3: no dDelta rows)
     const int c0 = p.doc_off[n], c1 = p.doc_off[n + 1];
     const size_t dh = (size_t(n) * p.H + h) * D * D;
     if (*p.status == KDA_ERR_DEVICE_CHECK) return;  // a failed device-side check of this call
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     auto do_buf = [&](int b) { return b ? B_OFF_DO1 : B_OFF_DO0; };
     // the Aqk / dO buffer of chunk c is (c1 - 1 - c) & 1; its n-th load completes phase n & 1 of
     // that buffer's barrier
-    const int tok0 = (tid == 0 && c0 < c1) ? p.chunk_tab[c0].y : 0;  // first token of the document
+    const int tok0 = (tid == LD && c0 < c1) ? p.chunk_tab[c0].y : 0;  // first token (loader thread)
 
     // one TMA operation per operand image, both planes and both key blocks
     auto load_Kb = [&](int ci) {
@@ -495,9 +499,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (ci >= c0) egn = p.eGL[(size_t(ci) * p.H + h) * D + row];
     };
     fetch_next(c1 - 1);
-    // phase parity of the loads in flight per barrier 0..4 (thread 0), -1 = none
+    // phase parity of the latest load per barrier 0..4 (the loader thread's bookkeeping for an
+    // early exit: a wait on it returns at once when it has landed), -1 = none
     int pend[5] = {-1, -1, -1, -1, -1};
-    if (tid == 0 && c0 < c1) {
+    if (tid == LD && c0 < c1) {
         load_Kb(c1 - 1);
         load_AO(c1 - 1);
         load_Qg(c1 - 1);
@@ -507,9 +512,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             load_AO(c1 - 2);
             pend[2] = 0;
         }
-        if (issue_DT(c1 - 1)) pend[1] = -1;
-        else *abort_flag = stopf[0] = 1;
     }
+    if (tid == 0 && c0 < c1 && !issue_DT(c1 - 1)) *abort_flag = stopf[0] = 1;
 
     for (int ci = c1 - 1; ci >= c0; --ci) {
         const int k = c1 - 1 - ci;
@@ -530,7 +534,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // ---- DA = Kb dS1, then DQ = Qg^T dO ----
         if (tid == 0) {
             if (tc::mbar_wait(&bar[0], ph)) {
-                pend[0] = -1;
                 tc::fence_after_sync();
                 const uint64_t kh = tc::sdesc(sKb, 16, 1024), kl = tc::sdesc(sKb + 16384, 16, 1024);
                 const uint64_t dh_ = tc::sdesc(sdS, 1024, 1024), dl_ = tc::sdesc(sdS + 16384, 1024, 1024);
@@ -549,7 +552,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             }
             tc::mma_commit(&bar[5]);
             if (tc::mbar_wait(&bar[3], ph)) {
-                pend[3] = -1;
                 tc::fence_after_sync();
                 const uint64_t qh = tc::sdesc(sQg, 8192, 1024), ql = tc::sdesc(sQg + 16384, 8192, 1024);
                 const uint64_t bo = tc::sdesc(smem_u32(sm + do_buf(int(ph))), 1024, 1024);
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         const float eg = egn;
         if (!tc::mbar_wait(&bar[5], ph)) *abort_flag = 1;  // DA (and this chunk's DT) done
         tc::fence_after_sync();
-        if (tid == 0 && ci > c0 && !*abort_flag) {
+        if (tid == LD && ci > c0 && !*abort_flag) {
             load_Kb(ci - 1);
             pend[0] = int(ph ^ 1u);
         }
@@ -598,13 +600,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::st_sw128_n<VPT>(sm + B_OFF_DD, row, cc, xh);
             tc::st_sw128_n<VPT>(sm + B_OFF_DD + 8192, row, cc, xl);
         }
-        if (tid == 0) {
+        if (tid == LD) {
             if (!tc::mbar_wait(&bar[7], ph)) *abort_flag = 1;  // DQ done: the Qg buffer is free
             tc::fence_after_sync();
             if (ci > c0 && !*abort_flag) {
                 load_Qg(ci - 1);
                 pend[3] = int(ph ^ 1u);
             }
+        }
+        if (tid == 0) {
             stopf[1] = *abort_flag;  // decision at the next barrier
             if (tsave) tc::bulk_wait_read0();  // this chunk's dS1 store has read its tile
         }
@@ -617,7 +621,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // ---- DW = W^T dDelta, then DT of the next chunk ----
         if (tid == 0) {
             if (tc::mbar_wait(&bar[4], ph)) {
-                pend[4] = -1;
                 tc::fence_after_sync();
                 const uint64_t wh = tc::sdesc(sW, 8192, 1024), wl = tc::sdesc(sW + 16384, 8192, 1024);
                 const uint64_t dxh = tc::sdesc(sdD, 1024, 1024), dxl = tc::sdesc(sdD + 8192, 1024, 1024);
@@ -639,11 +642,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 tc::tma_store3(&tm.mdDst, col0, 0, int(2 * chd), sm + B_OFF_DD);
                 tc::bulk_commit();
             }
-            if (ci > c0 && !*abort_flag) {
-                if (!issue_DT(ci - 1)) *abort_flag = 1;
-                else if (ph) pend[1] = -1;
-                else pend[2] = -1;
-            }
+            if (ci > c0 && !*abort_flag && !issue_DT(ci - 1)) *abort_flag = 1;
         }
         __syncwarp();
         // while DW runs: the saved write-vector gradient and the next chunk's per-thread operands
@@ -656,7 +655,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         if (!tc::mbar_wait(&bar[6], ph)) *abort_flag = 1;  // DW (and DQ) done
         if (tid == 0) stopf[0] = *abort_flag;  // decision at the next step's first barrier
         tc::fence_after_sync();
-        if (tid == 0 && !*abort_flag) {
+        if (tid == LD && !*abort_flag) {
             if (ci > c0) {
                 load_W(ci - 1);
                 pend[4] = int(ph ^ 1u);
@@ -684,10 +683,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     if (*abort_flag) {
         if (tid == 0) {
             tc::drain_mmas(reinterpret_cast<uint64_t*>(sm + B_OFF_BAR + 80), 100000000ull);
+            p.status[0] = KDA_ERR_TIMEOUT;
+        }
+        if (tid == LD) {
 #pragma unroll
             for (int i = 0; i < 5; ++i)
                 if (pend[i] >= 0) tc::mbar_wait(&bar[i], uint32_t(pend[i]), 100000000ull);
-            p.status[0] = KDA_ERR_TIMEOUT;
         }
     } else {
         float* out = bwd ? p.dh0 : p.fragB;

@@ -73,8 +73,8 @@ static_assert(BWD_INTRA_SMEM <= 232448, "backward intra shared memory above the 
 //
 // Persistent: one block per SM walks the items item = chunk * H + head.  The inputs of its next
 // item are fetched while the current one is computed, in two parts that land in tiles the current
-// item no longer reads.  Shared-memory tiles are copied row by row by the TMA unit (issued by warp 0,
-// completion on an mbarrier), so no other warp waits on the issue: once step 4 is done, dAqk and dM;
+// item no longer reads.  Shared-memory tiles are copied row by row by the TMA unit (one copy issued by
+// lane 0 of each of several warps, completion on an mbarrier): once step 4 is done, dAqk and dM;
 // once step 6 is done, q, k and the first half of dQg, P, dKb, dR.  Akk, gam, v, beta and the second
 // half of dQg, P, dKb, dR of the next item go to registers, dQg and P issued before the current
 // item's output stores (which would otherwise hold them up at the item boundary), dKb and dR after
@@ -103,17 +103,19 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     float pb = 0.f;        // beta of the next item (threads < 64)
     int4 ntab = make_int4(0, 0, 0, 0);
     int nT0 = 0, nL = 0, nh = 0;  // first token, length and head of the next item
-    // part A: dAqk, dM by TMA (thread 0); Akk, gam, the chunk-table entry to registers
+    // The copies of each part are issued by lane 0 of different warps, one each, so their issue
+    // costs (hundreds of cycles per copy) overlap; thread 0 sets the part's expected bytes before a
+    // barrier that precedes every issue.
+    auto expectA = [&]() { tc::mbar_expect_tx(&S.bar[0], 2u * CH * CH * 4u); };
+    auto expectB = [&]() { tc::mbar_expect_tx(&S.bar[1], 4u * CH * 64u * 2u + 4u * 32u * D * 4u); };
+    // part A: dAqk, dM by TMA (warps 0..3); Akk, gam, the chunk-table entry to registers
     auto fetchA = [&](int item) {
         const size_t nchd = size_t(item);
-        if (tid == 0) {
+        if (w < 4 && lane == 0) {
             tc::fence_async_smem();  // the tiles' earlier generic accesses come first
-            tc::mbar_expect_tx(&S.bar[0], 2u * CH * CH * 4u);
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                tc::tma3(S.dA + hb * CH * 32, &tm.mdA, 32 * hb, 0, item, &S.bar[0]);
-                tc::tma3(S.dAk + hb * CH * 32, &tm.mdM, 32 * hb, 0, item, &S.bar[0]);
-            }
+            const int hb = w & 1;
+            if (w < 2) tc::tma3(S.dA + hb * CH * 32, &tm.mdA, 32 * hb, 0, item, &S.bar[0]);
+            else tc::tma3(S.dAk + hb * CH * 32, &tm.mdM, 32 * hb, 0, item, &S.bar[0]);
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) pA[k] = reinterpret_cast<const float4*>(p.Akk + nchd * CH * CH)[tid + BT * k];
@@ -138,25 +140,25 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         }
     };
     // part B: the item's 64 token rows of q and k (rows past the document end are cleared once
-    // they land) and rows 0..31 of dQg, P, dKb, dR by TMA (thread 0); v and beta to registers
+    // they land) and rows 0..31 of dQg, P, dKb, dR by TMA (warps 0..7); v and beta to registers
     auto fetchB = [&](int item) {
         const int T0 = ntab.y, Ln = ntab.z, hh = item % p.H;
         nT0 = T0;
         nL = Ln;
         nh = hh;
         const size_t nchd = size_t(item);
-        if (tid == 0) {
+        if (w < 8 && lane == 0) {
             tc::fence_async_smem();
-            tc::mbar_expect_tx(&S.bar[1], 4u * CH * 64u * 2u + 4u * 32u * D * 4u);
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
+            const int hb = w & 1;
+            if (w < 2) {
                 tc::tma3(S.qb + hb * CH * 64, &tm.mq, 64 * hb, hh, T0, &S.bar[1]);
+            } else if (w < 4) {
                 tc::tma3(S.kb + hb * CH * 64, &tm.mk, 64 * hb, hh, T0, &S.bar[1]);
+            } else {
+                const float* src = w == 4 ? p.dQg : w == 5 ? p.P : w == 6 ? p.dKb : p.dR;
+                float* dst = (w < 6 ? S.dQ : S.dK) + (w & 1) * 32 * D;
+                tc::bulk_g2s(dst, src + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
             }
-            tc::bulk_g2s(S.dQ, p.dQg + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
-            tc::bulk_g2s(S.dQ + 32 * D, p.P + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
-            tc::bulk_g2s(S.dK, p.dKb + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
-            tc::bulk_g2s(S.dK + 32 * D, p.dR + nchd * CH * D, 32u * D * 4u, &S.bar[1]);
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -177,6 +179,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         tc::mbar_init(&S.bar[1], 1);
         S.abort = 0;
         tc::fence_mbar_init();
+        expectA();
+        expectB();
     }
     __syncthreads();
     fetchA(blockIdx.x);
@@ -567,6 +571,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             S.dG[r * LG + c] += qv[x] * aq[x] + kv[x] * (ak[x] - bb[x]);
         }
     }
+    if (tid == 0 && more) expectA();  // the next item's part A, issued after this barrier
     __syncthreads();
 
     // this item's inputs of steps 5 and 7 (their latency hides behind steps 5 and 6), then the first
@@ -637,6 +642,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         store_out4(p.dk, base + c0, make_float4(dk[0], dk[1], dk[2], dk[3]), p.out_fp32);
         if (lane == 0) store_out(p.dbeta, size_t(t0 + r) * p.H + h, S.dbp[r], p.out_fp32);
     }
+    if (tid == 0 && more) expectB();
     __syncthreads();  // q, k and the accumulator tiles are free: the next item's second part
     if (more) {
         fetchB(item + gridDim.x);

@@ -125,9 +125,10 @@ size_t intra_smem_bytes() { return sizeof(IntraSmem) + 1024; }  // + alignment s
 // Persistent: one block per SM walks the (chunk, head) items item = chunk * H + head; the raw
 // inputs of its next item are loaded into registers while the current one is computed, in three
 // bursts (q, k, then the gate) so that no burst fills the memory request queue of the SM.  The
-// hi / lo planes of Aqk, Minv and W and Akk leave through TMA stores from staging tiles (thread 0
-// issues them and waits for their reads of shared memory before the tiles are rewritten): the
-// small matrices' stores run during step 6, W's during the next item's first steps.  Step 6 (W
+// hi / lo planes of Aqk, Minv and W and Akk leave through TMA stores from staging tiles (lane 0 of
+// one warp per store issues it and waits for its reads of shared memory before the tile is
+// rewritten, so the issue costs overlap): the small matrices' stores run during step 6, W's during
+// the next item's first steps.  Step 6 (W
 // and U) runs as tcgen05 MMAs issued by thread 0 into 256 TMEM columns held for the whole kernel;
 // every wait on their completion is bounded (on expiry the block reports KDA_ERR_TIMEOUT, lets
 // its MMAs drain, frees its TMEM and stops).
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
 #pragma unroll
             for (int r = r0; r < r0 + 16; ++r) S.gam[r * LQ + c] += carry;
     }
-    if (tid == 0) tc::bulk_wait_read0();  // the previous item's W store has read u (written in 4a)
+    if (warp >= NW - 4 && lane == 0) tc::bulk_wait_read0();  // the previous item's W stores have read u (written in 4a)
     __syncthreads();
 
     // 4a. diagonal 8x8 blocks (the lower-left 8x8 quadrant of each 16-row sub-chunk runs on tensor
@@ -601,14 +602,17 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     tc::fence_before_sync();
     __syncthreads();  // every thread's part of the v tile, the operands, the staged matrices
     tc::fence_after_sync();
-    if (tid == 0) {
-        const int z[4] = {tm.zAh, tm.zAl, tm.zMh, tm.zMl};
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            tc::tma_store3(&tm.m64, 0, 0, z[b] + int(chd), reinterpret_cast<unsigned char*>(S.k) + b * 8192);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) tc::tma_store3(&tm.mAkk, 32 * b, 0, int(chd), S.x.akk_st + b * 8192);
+    if (warp >= 1 && warp <= 6 && lane == 0) {  // one small-matrix store per warp, beside the MMAs
+        const int b = warp - 1;
+        if (b < 4) {
+            const int z = b == 0 ? tm.zAh : b == 1 ? tm.zAl : b == 2 ? tm.zMh : tm.zMl;
+            tc::tma_store3(&tm.m64, 0, 0, z + int(chd), reinterpret_cast<unsigned char*>(S.k) + b * 8192);
+        } else {
+            tc::tma_store3(&tm.mAkk, 32 * (b - 4), 0, int(chd), S.x.akk_st + (b - 4) * 8192);
+        }
         tc::bulk_commit();
+    }
+    if (tid == 0) {
         // 6. W = Minv (beta K e^gam) (TMEM columns 0..127) and U = (Minv diag(beta)) V (columns
         //    128..255): M = 128 (rows 0..63 are the chunk's tokens, rows 64..127 are not read), N =
         //    128 channels, K = 64 tokens in four steps; A K-major (64 tokens = one 128-byte swizzle
@@ -662,14 +666,12 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     }
     tc::fence_before_sync();
     tc::fence_async_smem();
-    if (tid == 0) tc::bulk_wait_read0();  // the small matrices' stores have read k and akk_st
+    if (warp >= 1 && warp <= 6 && lane == 0) tc::bulk_wait_read0();  // the small matrices' stores have read k, akk_st
     __syncthreads();  // W staged; every thread is done with this item's shared tiles and TMEM
     if (*reinterpret_cast<volatile int*>(&S.abort)) break;
-    if (tid == 0) {
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            tc::tma_store3(&tm.m128, 64 * (b & 1), 0, ((b >> 1) ? tm.zWl : tm.zWh) + int(chd),
-                           S.u.wst + b * 8192);
+    if (warp >= NW - 4 && lane == 0) {  // W: one store per warp
+        const int b = warp - (NW - 4);
+        tc::tma_store3(&tm.m128, 64 * (b & 1), 0, ((b >> 1) ? tm.zWl : tm.zWh) + int(chd), S.u.wst + b * 8192);
         tc::bulk_commit();
     }
     if (more) fetch_v();
@@ -681,7 +683,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         p.status[0] = KDA_ERR_TIMEOUT;
     }
     cp_wait<0>();                    // no cp.async into the tiles is in flight past this point
-    if (tid == 0) tc::bulk_wait0();  // the stores are complete before the block ends
+    if (lane == 0) tc::bulk_wait0();  // every warp's stores are complete before the block ends
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(taddr, 256);

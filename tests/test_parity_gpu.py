@@ -100,6 +100,21 @@ def test_many_documents(saved_mode):
     assert_within(errs, label="many documents")
 
 
+def test_thousands_of_documents():
+    # 1500 short ragged documents (empty ones included), one head: the chunk plan's block-wide
+    # scan over documents (several documents per thread) and its identity launch order above
+    # 1024 documents
+    rng = np.random.default_rng(21)
+    lens = [int(x) for x in rng.integers(0, 25, size=1500)]
+    lens[:5] = [64, 0, 65, 1, 63]
+    inp = inputs.make_inputs(lens, 1, seed=21, gate="raw", l2norm=False, A_log_range=(LN8, LN32))
+    gpu = gpu_fwd_bwd(inp, gate="raw", l2norm=False)
+    ref = oracle_fwd_bwd(inp, gate="raw", l2norm=False)
+    errs = compare(gpu, ref)
+    print("thousands of documents", {k: f"{v:.2e}" for k, v in errs.items()})
+    assert_within(errs, label="thousands of documents")
+
+
 def test_many_documents_isolation_bitwise():
     inp = _many_docs(13)
     pack = gpu_fwd_bwd(inp, gate="raw", l2norm=True)

@@ -357,6 +357,7 @@ kda_status make_bwd_intra_maps(const Params& p, const Layout& L, int64_t T, TcMa
     const cuuint32_t bq[3] = {64, 1, 64}, ba[3] = {32, 64, 1};
     const cuuint64_t dq[3] = {D, cuuint64_t(L.H), cuuint64_t(T)}, sq[2] = {D * 2, cuuint64_t(L.H) * D * 2};
     const cuuint64_t da[3] = {CH, CH, CHd}, sa[2] = {CH * 4, size_t(CH) * CH * 4};
+    const cuuint64_t dg[3] = {D, CH, CHd}, sg[2] = {D * 4, size_t(CH) * D * 4};
     struct {
         CUtensorMap* m;
         CUtensorMapDataType ty;
@@ -364,10 +365,11 @@ kda_status make_bwd_intra_maps(const Params& p, const Layout& L, int64_t T, TcMa
         const cuuint64_t* dims;
         const cuuint64_t* st;
         const cuuint32_t* box;
-    } v[4] = {{&tm->mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, dq, sq, bq},
+    } v[5] = {{&tm->mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, dq, sq, bq},
               {&tm->mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, dq, sq, bq},
               {&tm->mdA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dAqk, da, sa, ba},
-              {&tm->mdM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dM, da, sa, ba}};
+              {&tm->mdM, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dM, da, sa, ba},
+              {&tm->mgam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.gam, dg, sg, ba}};
     for (auto& x : v)
         if (enc(x.m, x.ty, 3, const_cast<void*>(x.base), x.dims, x.st, x.box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -23,6 +23,7 @@ namespace {
 // the column-wise reads below free of bank conflicts:
 //   q, k:      two blocks [64 tokens][64 channels] bf16 (channels 0..63, 64..127), element qk_at
 //   dAqk, dM:  two blocks [64 rows][32 columns] fp32 (columns 0..31, 32..63), element a_at
+//   gam:       four such blocks (columns 0..31, ..., 96..127), element a_at as well
 // row stride (floats) of the gam, dQ, dK, dG tiles: 8 banks per row, so the paired (8-byte)
 // accesses of step 3's epilogues (rows g, g + 8, columns 2t, 2t + 1 of a quad-lane layout) meet
 // no bank conflict
@@ -38,9 +39,10 @@ __device__ __forceinline__ int a_at(int r, int c) {
 struct BwdIntraSmem {
     __nv_bfloat16 qb[2 * CH * 64], kb[2 * CH * 64];  // q, k as given (bf16); q^ = q * rq
     float dA[2 * CH * 32], dAk[2 * CH * 32];         // dAqk and dAkk = beta_r dM
-    float gam[CH * LG];                             // in-chunk cumsum of g
+    float gam[CH * D];                              // in-chunk cumsum of g (swizzled, a_at)
     // accumulators of dq^, dk^, dgam; until step 2 the dQ / dK tiles hold, densely, rows 0..31 of
-    // dQg then P (dQ tile) and of dKb then dR (dK tile), copied during the previous item
+    // dQg then P (dQ tile) and of dKb then dR (dK tile), and the dG tile rows 32..63 of dQg then P,
+    // copied during the previous item
     float dQ[CH * LG], dK[CH * LG], dG[CH * LG];
     float beta[CH], rq[CH], rk[CH];
     float dbp[CH];  // per-row dbeta, accumulated in steps 1-2 in a fixed order
@@ -52,12 +54,22 @@ struct BwdIntraSmem {
             float kbp[16 * D];      // per-warp partials of sum_r dKb * Kb (step 2 -> 5)
         };
         float wsum[2][16][D];  // per-warp column partials of step 7
+        float akk[CH * CH];    // Akk (dense), copied during the previous item, read in step 1
     };
-    uint64_t bar[2];  // TMA completion of the next item's inputs: 0 dAqk / dM, 1 q / k / staged rows
-    int abort;        // a wait timed out
+    // TMA completion of the next item's inputs: 0 dAqk / dM, 1 q / k / rows 0..31 of dQg, P, dKb,
+    // dR, 2 gam / Akk / rows 32..63 of dQg, P
+    uint64_t bar[3];
+    int abort;  // a wait timed out
 };
 constexpr size_t BWD_INTRA_SMEM = sizeof(BwdIntraSmem) + 1024;  // + alignment slack of the base
 static_assert(BWD_INTRA_SMEM <= 232448, "backward intra shared memory above the opt-in limit");
+static_assert(offsetof(BwdIntraSmem, gam) % 1024 == 0 && offsetof(BwdIntraSmem, dA) % 1024 == 0 &&
+                  offsetof(BwdIntraSmem, dAk) % 1024 == 0 && offsetof(BwdIntraSmem, qb) % 1024 == 0 &&
+                  offsetof(BwdIntraSmem, kb) % 1024 == 0,
+              "128-byte-swizzled TMA destinations must be 1024-byte aligned");
+static_assert(offsetof(BwdIntraSmem, akk) % 16 == 0 && offsetof(BwdIntraSmem, dG) % 16 == 0 &&
+                  offsetof(BwdIntraSmem, dQ) % 16 == 0 && offsetof(BwdIntraSmem, dK) % 16 == 0,
+              "bulk-copy destinations must be 16-byte aligned");
 
 }  // namespace
 
@@ -72,13 +84,14 @@ static_assert(BWD_INTRA_SMEM <= 232448, "backward intra shared memory above the 
 // elementwise.  The r == s terms of Aqk (no gate dependence) enter dq and dk only.  512 threads.
 //
 // Persistent: one block per SM walks the items item = chunk * H + head.  The inputs of its next
-// item are fetched while the current one is computed, in two parts that land in tiles the current
-// item no longer reads.  Shared-memory tiles are copied row by row by the TMA unit (one copy issued by
-// lane 0 of each of several warps, completion on an mbarrier): once step 4 is done, dAqk and dM;
-// once step 6 is done, q, k and the first half of dQg, P, dKb, dR.  Akk, gam, v, beta and the second
-// half of dQg, P, dKb, dR of the next item go to registers, dQg and P issued before the current
-// item's output stores (which would otherwise hold them up at the item boundary), dKb and dR after
-// step 5.  Every wait is bounded; after a timeout the block stops and reports.
+// item are fetched while the current one is computed, in three parts that land in tiles the
+// current item no longer reads (each copy issued by lane 0 of its own warp, completion on an
+// mbarrier per part): once step 4 is done, dAqk and dM (TMA); once step 7 is done (it runs ahead
+// of step 6), gam (TMA, into its swizzled tile), Akk (into the union) and rows 32..63 of dQg and P
+// (into the dG tile); once step 6 is done, q, k (TMA) and rows 0..31 of dQg, P, dKb, dR (into the
+// dQ / dK tiles).  Only rows 32..63 of dKb and dR (after step 5), v and beta go to registers.  The
+// register loads of the rest filled the SM's outstanding-request capacity and stalled the warps
+// issuing them.  Every wait is bounded; after a timeout the block stops and reports.
 // L2N: the fused L2 norm of q and k is on (row scales rq, rk and their backward); off, the scales
 // are 1 and every multiply by them is compiled out.
 template <bool L2N>
@@ -96,9 +109,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     auto Qv = [&](int r, int c) { return __bfloat162float(S.qb[qk_at(r, c)]) * rqs(r); };
     auto Kv = [&](int r, int c) { return __bfloat162float(S.kb[qk_at(r, c)]) * rks(r); };
 
-    float4 pA[2], pgm[4];  // Akk and gam of the next item
-    float4 hq[2], hp[2], hb[2], hr[2];  // second half (rows 32..63) of its dQg, P, dKb, dR
-    uint2 hv[2];                        // and of its v
+    float4 hb[2], hr[2];  // second half (rows 32..63) of the next item's dKb, dR
+    uint2 hv[2];          // and of its v
     uint2 pv[2];           // v, first half, of the next item
     float pb = 0.f;        // beta of the next item (threads < 64)
     int4 ntab = make_int4(0, 0, 0, 0);
@@ -108,26 +120,30 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     // barrier that precedes every issue.
     auto expectA = [&]() { tc::mbar_expect_tx(&S.bar[0], 2u * CH * CH * 4u); };
     auto expectB = [&]() { tc::mbar_expect_tx(&S.bar[1], 4u * CH * 64u * 2u + 4u * 32u * D * 4u); };
-    // part A: dAqk, dM by TMA (warps 0..3); Akk, gam, the chunk-table entry to registers
+    auto expectC = [&]() { tc::mbar_expect_tx(&S.bar[2], CH * D * 4u + CH * CH * 4u + 2u * 32u * D * 4u); };
+    // part A: dAqk, dM by TMA (warps 0..3); the chunk-table entry to registers
     auto fetchA = [&](int item) {
-        const size_t nchd = size_t(item);
         if (w < 4 && lane == 0) {
             tc::fence_async_smem();  // the tiles' earlier generic accesses come first
             const int hb = w & 1;
             if (w < 2) tc::tma3(S.dA + hb * CH * 32, &tm.mdA, 32 * hb, 0, item, &S.bar[0]);
             else tc::tma3(S.dAk + hb * CH * 32, &tm.mdM, 32 * hb, 0, item, &S.bar[0]);
         }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) pA[k] = reinterpret_cast<const float4*>(p.Akk + nchd * CH * CH)[tid + BT * k];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pgm[k] = reinterpret_cast<const float4*>(p.gam + nchd * CH * D)[tid + BT * k];
         ntab = p.chunk_tab[item / p.H];
-        // issued here, before the current item's output stores fill the memory queues
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const size_t i = nchd * CH * D / 4 + tid + BT * (2 + k);
-            hq[k] = reinterpret_cast<const float4*>(p.dQg)[i];
-            hp[k] = reinterpret_cast<const float4*>(p.P)[i];
+    };
+    // part C: gam by TMA (warps 0..3), Akk and rows 32..63 of dQg, P by bulk copies (warps 4..6)
+    auto fetchC = [&](int item) {
+        const size_t nchd = size_t(item);
+        if (w < 7 && lane == 0) {
+            tc::fence_async_smem();
+            if (w < 4) {
+                tc::tma3(S.gam + w * CH * 32, &tm.mgam, 32 * w, 0, item, &S.bar[2]);
+            } else if (w == 4) {
+                tc::bulk_g2s(S.akk, p.Akk + nchd * CH * CH, CH * CH * 4u, &S.bar[2]);
+            } else {
+                const float* src = (w == 5 ? p.dQg : p.P) + nchd * CH * D + 32 * D;
+                tc::bulk_g2s(S.dG + (w - 5) * 32 * D, src, 32u * D * 4u, &S.bar[2]);
+            }
         }
     };
     // rows 32..63 of dKb, dR: a second, later burst (after step 5)
@@ -177,15 +193,18 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     if (tid == 0) {
         tc::mbar_init(&S.bar[0], 1);
         tc::mbar_init(&S.bar[1], 1);
+        tc::mbar_init(&S.bar[2], 1);
         S.abort = 0;
         tc::fence_mbar_init();
         expectA();
         expectB();
+        expectC();
     }
     __syncthreads();
     fetchA(blockIdx.x);
     fetchA2(blockIdx.x);
     fetchB(blockIdx.x);
+    fetchC(blockIdx.x);
     uint32_t ph = 0;  // phase parity of this item's two barriers
 
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
@@ -195,7 +214,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 
     // 1. inputs: the prefetched tiles and registers to shared memory; dAkk = beta_r dM; per-row
     //    L2 scales
-    if (!(tc::mbar_wait(&S.bar[0], ph) && tc::mbar_wait(&S.bar[1], ph))) S.abort = 1;
+    if (!(tc::mbar_wait(&S.bar[0], ph) && tc::mbar_wait(&S.bar[1], ph) && tc::mbar_wait(&S.bar[2], ph))) S.abort = 1;
     ph ^= 1u;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {  // q, k rows past the document end read as zero
@@ -210,18 +229,14 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     for (int k = 0; k < 2; ++k) {
         const int i = tid + BT * k, r = i >> 4, c = (i & 15) * 4;
         const float4 m4 = *reinterpret_cast<const float4*>(&S.dAk[a_at(r, c)]);
-        float a = pA[k].x * m4.x + pA[k].y * m4.y + pA[k].z * m4.z + pA[k].w * m4.w;
+        const float4 a4 = *reinterpret_cast<const float4*>(&S.akk[r * CH + c]);
+        float a = a4.x * m4.x + a4.y * m4.y + a4.z * m4.z + a4.w * m4.w;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
         if ((i & 15) == 0) S.dbp[r] = a;
     }
     if (tid < CH) S.beta[tid] = pb;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int i = tid + BT * k, r = i >> 5, c = (i & 31) * 4;
-        *reinterpret_cast<float4*>(&S.gam[r * LG + c]) = pgm[k];
-    }
-    __syncthreads();  // beta, gam, the zero rows of q / k
+    __syncthreads();  // beta, the zero rows of q / k
     if (*reinterpret_cast<volatile int*>(&S.abort)) break;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -250,6 +265,13 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     // 2. elementwise terms through Qg, Kg, Kb and the diagonal of Aqk; dv = beta dR; dbeta_r +=
     //    dR_r . v_r - Kg_r . P_r (one warp per row, fixed-order warp sums)
     float kbp[4] = {0.f, 0.f, 0.f, 0.f};  // sum over this thread's rows of dKb * Kb, its 4 channels
+    float4 hq[2], hp[2];  // rows 32..63 of dQg, P, staged densely in the dG tile (read before the
+#pragma unroll            // first barrier below, after which step 2 writes that tile)
+    for (int k = 0; k < 2; ++k) {
+        const int i = (tid + BT * k) * 4;
+        hq[k] = *reinterpret_cast<const float4*>(&S.dG[i]);
+        hp[k] = *reinterpret_cast<const float4*>(&S.dG[32 * D + i]);
+    }
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
         float4 vq[2], vp[2], vb[2], vr[2];
@@ -276,8 +298,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         for (int k = 0; k < 2; ++k) {
             const int i = tid + BT * (2 * half + k), r = i >> 5, c0 = (i & 31) * 4;
             const float dgn = S.dA[a_at(r, r)], br = S.beta[r], rqr = rqs(r), rkr = rks(r);
-            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LG + c0]);
-            const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[(CH - 1) * LG + c0]);
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[a_at(r, c0)]);
+            const float4 l4 = *reinterpret_cast<const float4*>(&S.gam[a_at(CH - 1, c0)]);
             const uint2 qb2 = *reinterpret_cast<const uint2*>(&S.qb[qk_at(r, c0)]);
             const uint2 kb2 = *reinterpret_cast<const uint2*>(&S.kb[qk_at(r, c0)]);
             __nv_bfloat162 qa, qb_, ka, kb_, va_, vb_;
@@ -377,18 +399,18 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             float aq[3][4] = {}, ak[3][4] = {};
 #pragma unroll
             for (int ks = 0; ks < 3; ++ks) {
-                const float g1 = S.gam[16 * (ks + 1) * LG + c];
+                const float g1 = S.gam[a_at(16 * (ks + 1), c)];
                 float xb[2][2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int s0 = 16 * ks + 2 * t + 8 * hf;
-                    xb[hf][0] = ldk(kx0, s0) * __expf(g1 - S.gam[s0 * LG + c]);
-                    xb[hf][1] = ldk(kx1, s0 + 1) * __expf(g1 - S.gam[(s0 + 1) * LG + c]);
+                    xb[hf][0] = ldk(kx0, s0) * __expf(g1 - S.gam[a_at(s0, c)]);
+                    xb[hf][1] = ldk(kx1, s0 + 1) * __expf(g1 - S.gam[a_at(s0 + 1, c)]);
                 }
 #pragma unroll
                 for (int i = ks + 1; i < 4; ++i) {
                     const int pair = i * (i - 1) / 2 + ks;
-                    const float R = i == ks + 1 ? 1.f : __expf(S.gam[16 * i * LG + c] - g1);
+                    const float R = i == ks + 1 ? 1.f : __expf(S.gam[a_at(16 * i, c)] - g1);
                     uint32_t qh[4], ql[4], kh[4], kl[4], bh[2], bl[2];
                     afrag(2 * pair, qh, ql);
                     afrag(2 * pair + 1, kh, kl);
@@ -401,11 +423,11 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
             for (int i = 1; i < 4; ++i) {
                 const int ref = 16 * i, cc = 8 * w + 2 * t;  // columns cc, cc + 1 (paired accesses)
-                const float2 gref = *reinterpret_cast<const float2*>(&S.gam[ref * LG + cc]);
+                const float2 gref = *reinterpret_cast<const float2*>(&S.gam[a_at(ref, cc)]);
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int r = 16 * i + g + 8 * hf;
-                    const float2 gr = *reinterpret_cast<const float2*>(&S.gam[r * LG + cc]);
+                    const float2 gr = *reinterpret_cast<const float2*>(&S.gam[a_at(r, cc)]);
                     const float s0 = __expf(gr.x - gref.x), s1 = __expf(gr.y - gref.y);
                     const float vq0 = aq[i - 1][2 * hf] * s0, vq1 = aq[i - 1][2 * hf + 1] * s1;
                     const float vk0 = ak[i - 1][2 * hf] * s0, vk1 = ak[i - 1][2 * hf + 1] * s1;
@@ -428,13 +450,13 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             float bacc[3][4] = {};
 #pragma unroll
             for (int ks = 1; ks < 4; ++ks) {
-                const float g1 = S.gam[(16 * ks - 1) * LG + c];
+                const float g1 = S.gam[a_at(16 * ks - 1, c)];
                 float xq[2][2], xk[2][2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int r0 = 16 * ks + 2 * t + 8 * hf;
-                    const float e0 = __expf(S.gam[r0 * LG + c] - g1);
-                    const float e1 = __expf(S.gam[(r0 + 1) * LG + c] - g1);
+                    const float e0 = __expf(S.gam[a_at(r0, c)] - g1);
+                    const float e1 = __expf(S.gam[a_at(r0 + 1, c)] - g1);
                     xq[hf][0] = ldq(kx0, r0) * e0;
                     xq[hf][1] = ldq(kx1, r0 + 1) * e1;
                     xk[hf][0] = ldk(kx0, r0) * e0;
@@ -443,7 +465,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
                 for (int j = 0; j < ks; ++j) {
                     const int pair = 6 + (j == 0 ? 0 : j == 1 ? 3 : 5) + ks - j - 1;
-                    const float R = j == ks - 1 ? 1.f : __expf(g1 - S.gam[(16 * j + 15) * LG + c]);
+                    const float R = j == ks - 1 ? 1.f : __expf(g1 - S.gam[a_at(16 * j + 15, c)]);
                     uint32_t qh[4], ql[4], kh[4], kl[4], qbh[2], qbl[2], kbh[2], kbl[2];
                     afrag(2 * pair, qh, ql);
                     afrag(2 * pair + 1, kh, kl);
@@ -459,11 +481,11 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
                 const int ref = 16 * j + 15, cc = 8 * w + 2 * t;  // columns cc, cc + 1 (paired)
-                const float2 gref = *reinterpret_cast<const float2*>(&S.gam[ref * LG + cc]);
+                const float2 gref = *reinterpret_cast<const float2*>(&S.gam[a_at(ref, cc)]);
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int sr = 16 * j + g + 8 * hf;
-                    const float2 gs = *reinterpret_cast<const float2*>(&S.gam[sr * LG + cc]);
+                    const float2 gs = *reinterpret_cast<const float2*>(&S.gam[a_at(sr, cc)]);
                     const float vb0 = bacc[j][2 * hf] * __expf(gref.x - gs.x);
                     const float vb1 = bacc[j][2 * hf + 1] * __expf(gref.y - gs.y);
                     float2* pk = reinterpret_cast<float2*>(&S.dK[sr * LG + cc]);
@@ -492,12 +514,12 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
             kv[x] = Kv(base + x, c);
         }
         {
-            const float g7 = S.gam[(base + 7) * LG + c];
+            const float g7 = S.gam[a_at(base + 7, c)];
             float F[8], G[8], Y[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                F[j] = __expf(S.gam[(base + 8 + j) * LG + c] - g7);
-                G[j] = __expf(g7 - S.gam[(base + j) * LG + c]);
+                F[j] = __expf(S.gam[a_at(base + 8 + j, c)] - g7);
+                G[j] = __expf(g7 - S.gam[a_at(base + j, c)]);
                 Y[j] = G[j] * kv[j];
                 bb[j] = 0.f;
             }
@@ -530,10 +552,10 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         }
         float ed[16];  // ed[x] = e^(gam_x - gam_{x-1}) (x = 8 starts a block: unused)
         {
-            float prev = S.gam[base * LG + c];
+            float prev = S.gam[a_at(base, c)];
 #pragma unroll
             for (int x = 1; x < 16; ++x) {
-                const float cur = S.gam[(base + x) * LG + c];
+                const float cur = S.gam[a_at(base + x, c)];
                 ed[x] = x == 8 ? 1.f : __expf(cur - prev);
                 prev = cur;
             }
@@ -581,9 +603,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     const float rs1 = p.rsum[chd * 2 * D + D + (tid & (D - 1))];
     if (more) {
         fetchA(item + gridDim.x);
-    } else {  // defined on every path, so nothing fetched stays live across steps 2-4
-        pA[0] = pA[1] = pgm[0] = pgm[1] = pgm[2] = pgm[3] = make_float4(0.f, 0.f, 0.f, 0.f);
-        hq[0] = hq[1] = hp[0] = hp[1] = pA[0];
+    } else {
         ntab = make_int4(0, 0, 0, 0);
     }
 
@@ -591,7 +611,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     //    cumsum over the chunk; four threads per channel (16 rows each), fixed order
     {
         const int c = tid & (D - 1), qu = tid >> 7, r0 = 16 * qu;
-        const float gl = S.gam[(CH - 1) * LG + c];
+        const float gl = S.gam[a_at(CH - 1, c)];
         *reinterpret_cast<float4*>(&S.kbp[w * D + 4 * lane]) = make_float4(kbp[0], kbp[1], kbp[2], kbp[3]);
         float suf = 0.f;  // suffix sums inside the quarter
         for (int r = r0 + 15; r >= r0; --r) {
@@ -613,6 +633,66 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         fetchA2(item + gridDim.x);
     else
         hb[0] = hb[1] = hr[0] = hr[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    // 7. gate gradient: g form writes dg; raw form writes da and the parameter partials.
+    //    In raw form the token's gate g_r is recovered from the stored cumsum, g_r = gam_r -
+    //    gam_{r-1}, and dg/da = -exp(A_log) sigmoid(a + dt_bias), where sigmoid(a + dt_bias) =
+    //    1 - exp(-softplus(a + dt_bias)) = 1 - exp(g_r / exp(A_log)) (absolute rounding error
+    //    ~1e-7: negligible where the difference is small).  Thread: rows w + 16 k, four channels;
+    //    per-warp column partials, then fixed-order sums over the warps.
+    if (!p.gate_raw) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
+            if (r < L)
+                *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
+                    *reinterpret_cast<const float4*>(&S.dG[r * LG + c4]);
+        }
+    } else {
+        const float eA = expf(aLog), ieA = 1.f / eA;
+        const int c4 = (tid & 31) * 4;
+        float pd[4] = {0.f, 0.f, 0.f, 0.f}, pa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = (tid + BT * k) >> 5;
+            const bool ok = r < L;
+            const float4 dg4 = *reinterpret_cast<const float4*>(&S.dG[r * LG + c4]);
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[a_at(r, c4)]);
+            const float4 gp4 = r > 0 ? *reinterpret_cast<const float4*>(&S.gam[a_at(r - 1, c4)])
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
+            const float gv[4] = {g4.x - gp4.x, g4.y - gp4.y, g4.z - gp4.z, g4.w - gp4.w};
+            float da4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                da4[j] = ok ? dgv[j] * eA * (__expf(gv[j] * ieA) - 1.f) : 0.f;
+                pd[j] += da4[j];
+                pa[j] += ok ? dgv[j] * gv[j] : 0.f;
+            }
+            if (ok)
+                *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
+                    make_float4(da4[0], da4[1], da4[2], da4[3]);
+        }
+        *reinterpret_cast<float4*>(&S.wsum[0][w][c4]) = make_float4(pd[0], pd[1], pd[2], pd[3]);
+        *reinterpret_cast<float4*>(&S.wsum[1][w][c4]) = make_float4(pa[0], pa[1], pa[2], pa[3]);
+        __syncthreads();
+        if (tid < D) {  // warps 0..3: one channel per thread, then a fixed-order sum of the channels
+            float sd = 0.f, sa = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) {
+                sd += S.wsum[0][ww][tid];
+                sa += S.wsum[1][ww][tid];
+            }
+            p.pddt[chd * D + tid] = sd;
+            sa = warp_sum(sa);
+            if (lane == 0) S.fin[w] = sa;
+        }
+        __syncthreads();
+        if (tid == 0) p.pdA[chd] = (S.fin[0] + S.fin[1]) + (S.fin[2] + S.fin[3]);
+    }
+    if (tid == 0 && more) expectC();
+    __syncthreads();  // gam, dG and the union are free: the next item's third part
+    if (more) fetchC(item + gridDim.x);
 
     // 6. per row: L2-norm backward and the dq, dk, dbeta outputs (warp per row, 4 channels per lane)
     for (int r = w; r < L; r += NW) {
@@ -651,69 +731,12 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         pb = 0.f;
         nT0 = nL = nh = 0;
     }
-
-    // 7. gate gradient: g form writes dg; raw form writes da and the parameter partials.
-    //    In raw form the token's gate g_r is recovered from the stored cumsum, g_r = gam_r -
-    //    gam_{r-1}, and dg/da = -exp(A_log) sigmoid(a + dt_bias), where sigmoid(a + dt_bias) =
-    //    1 - exp(-softplus(a + dt_bias)) = 1 - exp(g_r / exp(A_log)) (absolute rounding error
-    //    ~1e-7: negligible where the difference is small).  Thread: rows w + 16 k, four channels;
-    //    per-warp column partials, then fixed-order sums over the warps.
-    if (!p.gate_raw) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int i = tid + BT * k, r = i >> 5, c4 = (i & 31) * 4;
-            if (r < L)
-                *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
-                    *reinterpret_cast<const float4*>(&S.dG[r * LG + c4]);
-        }
-    } else {
-        const float eA = expf(aLog), ieA = 1.f / eA;
-        const int c4 = (tid & 31) * 4;
-        float pd[4] = {0.f, 0.f, 0.f, 0.f}, pa[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int r = (tid + BT * k) >> 5;
-            const bool ok = r < L;
-            const float4 dg4 = *reinterpret_cast<const float4*>(&S.dG[r * LG + c4]);
-            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LG + c4]);
-            const float4 gp4 = r > 0 ? *reinterpret_cast<const float4*>(&S.gam[(r - 1) * LG + c4])
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
-            const float gv[4] = {g4.x - gp4.x, g4.y - gp4.y, g4.z - gp4.z, g4.w - gp4.w};
-            float da4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                da4[j] = ok ? dgv[j] * eA * (__expf(gv[j] * ieA) - 1.f) : 0.f;
-                pd[j] += da4[j];
-                pa[j] += ok ? dgv[j] * gv[j] : 0.f;
-            }
-            if (ok)
-                *reinterpret_cast<float4*>(p.dg + (size_t(t0 + r) * p.H + h) * D + c4) =
-                    make_float4(da4[0], da4[1], da4[2], da4[3]);
-        }
-        *reinterpret_cast<float4*>(&S.wsum[0][w][c4]) = make_float4(pd[0], pd[1], pd[2], pd[3]);
-        *reinterpret_cast<float4*>(&S.wsum[1][w][c4]) = make_float4(pa[0], pa[1], pa[2], pa[3]);
-        __syncthreads();
-        if (tid < D) {  // warps 0..3: one channel per thread, then a fixed-order sum of the channels
-            float sd = 0.f, sa = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
-                sd += S.wsum[0][ww][tid];
-                sa += S.wsum[1][ww][tid];
-            }
-            p.pddt[chd * D + tid] = sd;
-            sa = warp_sum(sa);
-            if (lane == 0) S.fin[w] = sa;
-        }
-        __syncthreads();
-        if (tid == 0) p.pdA[chd] = (S.fin[0] + S.fin[1]) + (S.fin[2] + S.fin[3]);
-    }
-    __syncthreads();  // the next item overwrites gam, beta, dbp and the union
     }  // items
     if (tid == 0 && S.abort) {
         // after a timed-out wait: let the copies in flight land (bounded), report
         tc::mbar_wait(&S.bar[0], ph ^ 1u, 100000000ull);
         tc::mbar_wait(&S.bar[1], ph ^ 1u, 100000000ull);
+        tc::mbar_wait(&S.bar[2], ph ^ 1u, 100000000ull);
         p.status[0] = KDA_ERR_TIMEOUT;
     }
 }

@@ -361,6 +361,8 @@ struct TcMaps {
     // backward intra-chunk inputs: q, k [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens};
     // dAqk, dM [chunk * H + head][64][64] fp32 as 32 x 64 boxes (128-byte swizzle)
     CUtensorMap mq, mk, mdA, mdM;
+    // gam of the saved record [chunk * H + head][64][128] fp32 as 32 x 64 boxes (128-byte swizzle)
+    CUtensorMap mgam;
     int zWh, zWl, zQh, zQl, zKh, zKl, zAh, zAl, zMh, zMl;  // first tile of each plane
 };
 

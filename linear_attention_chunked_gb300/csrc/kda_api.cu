@@ -264,6 +264,15 @@ kda_status make_tc_maps(const Params& p, const Layout& L, TcMaps* tm) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return KDA_ERR_CUDA;
     }
+    if (L.T > 0) {  // the gate, loaded by the forward intra kernel
+        const cuuint32_t bg[3] = {D, 1, CH};
+        const cuuint64_t dg[3] = {D, cuuint64_t(L.H), cuuint64_t(L.T)};
+        const cuuint64_t sg[2] = {D * 4, cuuint64_t(L.H) * D * 4};
+        if (enc(&tm->mg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p.g), dg, sg, bg, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return KDA_ERR_CUDA;
+    }
     if (p.sS) {  // the saved states and write vectors, stored from the recurrence's shared tiles
         const cuuint32_t bS[3] = {64, 128, 2}, bD[3] = {64, 64, 2};
         const cuuint64_t dS[3] = {D, D, 2 * CHd}, sSt[2] = {D * 2, size_t(D) * D * 2};

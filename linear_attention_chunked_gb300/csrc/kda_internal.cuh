@@ -358,6 +358,9 @@ struct TcMaps {
     // stores of the forward intra kernel's fp32 products: U [tile][64][128] and Akk [tile][64][64]
     // as 32 x 64 boxes (128-byte swizzle); its bf16 planes go through m128 / m64
     CUtensorMap mU, mAkk;
+    // loads of the forward intra kernel: the gate g [T][H][128] fp32 as boxes of 128 channels x 1
+    // head x 64 tokens (no swizzle; tokens at or past T read as zero)
+    CUtensorMap mg;
     // backward intra-chunk inputs: q, k [T][H][128] bf16 as 64 x 64 boxes {values, head, tokens};
     // dAqk, dM [chunk * H + head][64][64] fp32 as 32 x 64 boxes (128-byte swizzle)
     CUtensorMap mq, mk, mdA, mdM;

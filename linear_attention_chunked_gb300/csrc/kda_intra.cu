@@ -48,7 +48,7 @@ struct IntraSmem {
     unsigned char v[2 * 8192];  // V (exact in bf16), MN-major B of U: [column block][64 rows][128 B]
     float Akk[CH * LA], Aqk[CH * LA], Mi[CH * LA];
     float beta[CH];
-    uint64_t mbar[2];  // 0: completion of step 6's MMAs; 1: spare of the abort path
+    uint64_t mbar[3];  // 0: completion of step 6's MMAs; 1: spare of the abort path; 2: gate tile loaded
     uint32_t tslot;    // TMEM base address
     int abort;         // a bounded wait timed out
 };
@@ -60,6 +60,7 @@ __constant__ int2 kPairs[6] = {{1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
 static_assert(sizeof(IntraSmem) + 1024 <= 232448, "intra shared memory above the opt-in limit");
 static_assert(offsetof(IntraSmem, Akk) % 16 == 0 && (CH * LA) % 4 == 0,
               "the 64 x 64 tiles are cleared with 16-byte stores");
+static_assert(offsetof(IntraSmem, gam) % 128 == 0, "the gate tile is a TMA destination");
 static_assert(offsetof(IntraSmem, k) % 1024 == 0 && offsetof(IntraSmem, x) % 1024 == 0 &&
                   offsetof(IntraSmem, u) % 1024 == 0 && offsetof(IntraSmem, v) % 1024 == 0 &&
                   CH * LQ * 4 >= 4 * 8192,
@@ -149,8 +150,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     float pb = 0.f, peA = 0.f;
     int nT0 = 0, nL = 0, nh = 0;  // first token, length and head of the next item
     int4 tab_ahead = make_int4(0, 0, 0, 0);  // chunk-table entry of the item after the next
-    // parts: bit 0 q, bit 1 k, bit 2 gate (cp.async into gam, one commit group) / beta / gate
-    // parameters / next chunk-table entry
+    // parts: bit 0 q, bit 1 k, bit 2 gate (one TMA copy into gam, rows dense, issued by thread 0) /
+    // beta / gate parameters / next chunk-table entry
     auto fetch = [&](int item, int4 inf, int parts) {
         const int hh = item % p.H;
         const int T0 = inf.y, Ln = inf.z;
@@ -166,13 +167,11 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             if (parts & 2) pk[k] = r < Ln ? *reinterpret_cast<const uint4*>(p.k + off) : z;
         }
         if (!(parts & 4)) return;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {  // the thread's own rows of step 1 (no barrier needed there)
-            const int r = (tid + BT * k) >> 5;
-            const bool ok = r < Ln;
-            cp16z(&S.gam[r * LQ + c4t], p.g + (size_t(T0 + (ok ? r : 0)) * p.H + hh) * D + c4t, ok);
+        if (tid == 0) {  // rows past the document end are zeroed in step 1
+            tc::fence_async_smem();  // the tile's earlier generic accesses come first
+            tc::mbar_expect_tx(&S.mbar[2], CH * D * 4u);
+            tc::tma3(S.gam, &tm.mg, 0, hh, T0, &S.mbar[2]);
         }
-        cp_commit();
         if (tid < CH) pb = tid < Ln ? bf2f(p.beta[size_t(T0 + tid) * p.H + hh]) : 0.f;
         if (p.gate_raw) {
             pdb = *reinterpret_cast<const float4*>(p.dt_bias + hh * D + c4t);
@@ -193,6 +192,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     };
     if (tid == 0) {
         tc::mbar_init(&S.mbar[0], 1);
+        tc::mbar_init(&S.mbar[2], 1);
         S.abort = 0;
         tc::fence_mbar_init();
     }
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t taddr = S.tslot;
-    uint32_t mph = 0;  // phase parity of the MMA barrier
+    uint32_t mph = 0, gph = 0;  // phase parities of the MMA and gate barriers
     if (int(blockIdx.x) < items) {
         fetch(blockIdx.x, p.chunk_tab[blockIdx.x / p.H], 7);
         fetch_v();
@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     const size_t chd = size_t(item);
 
     // 1. inputs (fetched one item ahead) to shared memory, gate, beta; clear the 64x64 accumulators
+    float4 gx[4];  // this thread's gate values (rows w + 16 k), written to the padded tile after
+                   // the barrier below (every dense row has been read by then)
     {
         if (tid < CH) S.beta[tid] = pb;
 #pragma unroll
@@ -237,11 +239,12 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
         }
         const float eA = p.gate_raw ? expf(peA) : 0.f;
         bool bad_gate = false;
-        cp_wait<1>();  // this item's gate rows (this thread's copies; the v tile may still be in flight)
+        if (!tc::mbar_wait(&S.mbar[2], gph)) S.abort = 1;  // this item's gate tile (dense rows)
+        gph ^= 1u;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = (tid + BT * k) >> 5;
-            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * LQ + c4t]);
+            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * D + c4t]);
             float x[4] = {g4.x, g4.y, g4.z, g4.w};
             const float b4[4] = {pdb.x, pdb.y, pdb.z, pdb.w};
             if (p.gate_raw) {
@@ -250,9 +253,12 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             } else {
                 // the exponent-difference factorisation needs a decaying gate: g <= 0 (NaN fails)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) bad_gate |= !(x[j] <= 0.f);
+                for (int j = 0; j < 4; ++j) {
+                    x[j] = r < L ? x[j] : 0.f;
+                    bad_gate |= !(x[j] <= 0.f);
+                }
             }
-            *reinterpret_cast<float4*>(&S.gam[r * LQ + c4t]) = make_float4(x[0], x[1], x[2], x[3]);
+            gx[k] = make_float4(x[0], x[1], x[2], x[3]);
         }
         // reported in the status word; the state recurrences and backward kernels of this call
         // then do nothing
@@ -266,6 +272,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     }
     __syncthreads();
     const bool more = item + int(gridDim.x) < items;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(&S.gam[((tid + BT * k) >> 5) * LQ + c4t]) = gx[k];
 
     // 2. fused L2 norm (warp per row)
     if (p.l2n) {
@@ -285,6 +293,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             }
         }
     }
+    __syncthreads();  // the gate rows in the padded tile
     // 3. in-chunk inclusive cumsum: four threads per channel (16 rows each), then carries
     {
         const int c = tid & (D - 1), qu = tid >> 7, r0 = 16 * qu;
@@ -591,12 +600,7 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             *reinterpret_cast<float2*>(S.x.akk_st + (s >> 5) * 8192 + sw128(r, (s & 31) * 4)) = ak;
         }
     }
-    // this item's v tile (copied during the previous item's last phase; the next gate may stay in
-    // flight)
-    if (more)
-        cp_wait<1>();
-    else
-        cp_wait<0>();
+    cp_wait<0>();  // this item's v tile (copied during the previous item's last phase)
     if (more) fetch(item + gridDim.x, tab_next, 2);
     tc::fence_async_smem();  // this thread's staged values and operands, before the async proxy reads
     tc::fence_before_sync();
@@ -678,8 +682,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     }
     if (tid == 0 && S.abort) {
         // after a timed-out wait (the device is already in a bad state): let this block's MMAs
-        // finish (bounded) before its TMEM is freed, report
+        // and its gate copy in flight finish (bounded) before its TMEM is freed, report
         tc::drain_mmas(&S.mbar[1], 100000000ull);
+        tc::mbar_wait(&S.mbar[2], gph, 100000000ull);
         p.status[0] = KDA_ERR_TIMEOUT;
     }
     cp_wait<0>();                    // no cp.async into the tiles is in flight past this point

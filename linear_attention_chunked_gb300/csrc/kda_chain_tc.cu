@@ -7,7 +7,12 @@
 //   MMA3  D1 += [*; Aqk] Delta           rows 64..127: O = Qg S + Aqk Delta
 //         S  = e^gL * S + D2             (every thread, its own row)
 // Every product is split into bf16 hi/lo terms (a_hi b_lo + a_lo b_hi + a_hi b_hi, FP32 accumulate
-// in TMEM), which keeps ~16 significant bits per operand.  Rows 0..63 of the MMA3 A operand are
+// in TMEM), which keeps ~16 significant bits per operand.  The B operand's hi and lo planes sit
+// side by side along N (64-column blocks: two 64-column atoms, the lo plane one plane stride away;
+// narrower blocks: the lo values at column VW of the hi tile): one N = 2 VW MMA gives a_hi b_hi
+// and a_hi b_lo in two TMEM column halves, a_lo b_hi adds onto the first, and the epilogues sum
+// the halves -- two MMAs per K step instead of three, A read twice instead of three times, and
+// the same arithmetic for every block width (bitwise equal results).  Rows 0..63 of the MMA3 A operand are
 // whatever precedes the hi / lo Aqk tiles (zeros / the hi tile): they only touch D1 rows whose W S
 // values were already consumed.
 #include "kda_internal.cuh"
@@ -86,7 +91,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::tma_prefetch_map(&tm.m64);
         }
     }
-    if (w == 0) tc::tmem_alloc(tslot, 128);
+    constexpr bool W64 = VW == 64;  // lo planes in their own tiles (else beside hi, at column VW)
+    constexpr uint32_t TCOLS = W64 ? 256 : 128;
+    if (w == 0) tc::tmem_alloc(tslot, TCOLS);
     for (int i = tid; i < 8192 / 16; i += CHAIN_THREADS)
         reinterpret_cast<uint4*>(sm + OFF_PAD)[i] = make_uint4(0u, 0u, 0u, 0u);
 
@@ -103,10 +110,20 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t taddr = *tslot;
-    const uint32_t tD1 = taddr + (uint32_t(32 * qd) << 16), tD2 = tD1 + 64;
+    // TMEM columns: D1 0..2 VW - 1 (two halves), D2 from 128 (64-column blocks) or 64
+    const uint32_t tD1 = taddr + (uint32_t(32 * qd) << 16), tD2 = tD1 + (W64 ? 128 : 64);
 
     const uint32_t ID1 = tc::idesc_bf16(128, VW, false, true);  // K-major A, MN-major B
     const uint32_t ID2 = tc::idesc_bf16(128, VW, true, true);   // MN-major A and B
+    const uint32_t ID1c = tc::idesc_bf16(128, 2 * VW, false, true), ID2c = tc::idesc_bf16(128, 2 * VW, true, true);
+    // sum of the two column halves of an accumulator
+    auto tld = [&](uint32_t tcol, float (&v)[VPT]) {
+        float v2[VPT];
+        tc::tmem_ld<VPT>(tcol, v);
+        tc::tmem_ld<VPT>(tcol + VW, v2);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) v[j] += v2[j];
+    };
     const uint32_t sA1 = smem_u32(sm + OFF_A1), sS = smem_u32(sm + OFF_S);
     const uint32_t sKt = smem_u32(sm + OFF_KT), sPad = smem_u32(sm + OFF_PAD);
     const uint32_t sDl = smem_u32(sm + OFF_DL);
@@ -174,7 +191,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         uint32_t sh[VPT / 2], sl[VPT / 2];
         tc::split_n<VPT>(Sr, sh, sl);
         tc::st_sw128_n<VPT>(sm + OFF_S, row, cc, sh);
-        tc::st_sw128_n<VPT>(sm + OFF_S + 16384, row, cc, sl);
+        tc::st_sw128_n<VPT>(sm + OFF_S + (W64 ? 16384 : 0), row, (W64 ? 0 : VW) + cc, sl);
         tc::fence_async_smem();
         // the previous chunk's Delta store has read its tile (rewritten below this barrier)
         if (tsave && tid == 0) tc::bulk_wait_read0();
@@ -188,17 +205,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             if (tc::mbar_wait(&bar[0], ph)) {
                 tc::fence_after_sync();
                 const uint64_t dAh = tc::sdesc(sA1, 16, 1024), dAl = tc::sdesc(sA1 + 32768, 16, 1024);
-                const uint64_t dSh = tc::sdesc(sS, 1024, 1024), dSl = tc::sdesc(sS + 16384, 1024, 1024);
-                const uint64_t ta[3] = {dAh, dAl, dAh}, tb[3] = {dSl, dSh, dSh};
-                uint32_t acc = 0;
+                const uint64_t dSh = tc::sdesc(sS, 1024, 1024);
+                const uint64_t dShl = tc::sdesc(sS, W64 ? 16384 : 1024, 1024);  // [hi | lo] along N
 #pragma unroll
-                for (int tm3 = 0; tm3 < 3; ++tm3)
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        tc::mma(taddr, ta[tm3] + uint64_t(((s >> 2) * 16384 + (s & 3) * 32) >> 4),
-                                tb[tm3] + uint64_t((s * 2048) >> 4), ID1, acc);
-                        acc = 1;
-                    }
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t ak = uint64_t(((s >> 2) * 16384 + (s & 3) * 32) >> 4);
+                    const uint64_t bk = uint64_t((s * 2048) >> 4);
+                    tc::mma(taddr, dAh + ak, dShl + bk, ID1c, s > 0 ? 1u : 0u);
+                    tc::mma(taddr, dAl + ak, dSh + bk, ID1, 1u);
+                }
             } else {
                 *abort_flag = 1;
             }
@@ -230,12 +245,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         uint32_t dhh[VPT / 2], dll[VPT / 2];
         if (qd < 2) {
             float v[VPT];
-            tc::tmem_ld<VPT>(tD1 + cc, v);
+            tld(tD1 + cc, v);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) v[j] = Un[j] - v[j];
             tc::split_n<VPT>(v, dhh, dll);
             tc::st_sw128_n<VPT>(sm + OFF_DL, row, cc, dhh);
-            tc::st_sw128_n<VPT>(sm + OFF_DL + 8192, row, cc, dll);
+            tc::st_sw128_n<VPT>(sm + OFF_DL + (W64 ? 8192 : 0), row, (W64 ? 0 : VW) + cc, dll);
         }
         tc::fence_async_smem();
         // this chunk's state store has read the S tile (rewritten before the next barrier)
@@ -250,26 +265,23 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             if (tc::mbar_wait(&bar[1], ph)) {
                 tc::fence_after_sync();
                 const uint64_t dKh = tc::sdesc(sKt, 8192, 1024), dKl = tc::sdesc(sKt + 16384, 8192, 1024);
-                const uint64_t dDh = tc::sdesc(sDl, 1024, 1024), dDl = tc::sdesc(sDl + 8192, 1024, 1024);
-                const uint64_t ka[3] = {dKh, dKl, dKh}, db[3] = {dDl, dDh, dDh};
-                uint32_t acc = 0;
+                const uint64_t dDh = tc::sdesc(sDl, 1024, 1024);
+                const uint64_t dDhl = tc::sdesc(sDl, W64 ? 8192 : 1024, 1024);  // [hi | lo] along N
+                const uint64_t dQh = tc::sdesc(sPad, 16, 1024), dQl = tc::sdesc(sPad + 8192, 16, 1024);
+                const uint32_t d2 = taddr + (W64 ? 128 : 64);
 #pragma unroll
-                for (int tm3 = 0; tm3 < 3; ++tm3)
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t kk = uint64_t((s * 2048) >> 4);
+                    tc::mma(d2, dKh + kk, dDhl + kk, ID2c, s > 0 ? 1u : 0u);
+                    tc::mma(d2, dKl + kk, dDh + kk, ID2, 1u);
+                }
+                if (want_o) {
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        tc::mma(taddr + 64, ka[tm3] + uint64_t((s * 2048) >> 4),
-                                db[tm3] + uint64_t((s * 2048) >> 4), ID2, acc);
-                        acc = 1;
+                        const uint64_t qk = uint64_t((s * 32) >> 4), kk = uint64_t((s * 2048) >> 4);
+                        tc::mma(taddr, dQh + qk, dDhl + kk, ID1c, 1u);
+                        tc::mma(taddr, dQl + qk, dDh + kk, ID1, 1u);
                     }
-                if (want_o) {
-                    const uint64_t dQh = tc::sdesc(sPad, 16, 1024), dQl = tc::sdesc(sPad + 8192, 16, 1024);
-                    const uint64_t qa[3] = {dQh, dQl, dQh};
-#pragma unroll
-                    for (int tm3 = 0; tm3 < 3; ++tm3)
-#pragma unroll
-                        for (int s = 0; s < 4; ++s)
-                            tc::mma(taddr, qa[tm3] + uint64_t((s * 32) >> 4),
-                                    db[tm3] + uint64_t((s * 2048) >> 4), ID1, 1u);
                 }
             } else {
                 *abort_flag = 1;
@@ -300,13 +312,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         // ---- S = e^gL * S + Kb^T Delta;  O rows (lanes 64..127) ----
         {
             float v[VPT];
-            tc::tmem_ld<VPT>(tD2 + cc, v);
+            tld(tD2 + cc, v);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) Sr[j] = fmaf(eg, Sr[j], v[j]);
         }
         if (want_o && qd >= 2) {
             float v[VPT];
-            tc::tmem_ld<VPT>(tD1 + cc, v);
+            tld(tD1 + cc, v);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) v[j] *= p.scale;
             // token rows of this lane and of its pair (lanes 2k, 2k + 1 store together)
@@ -356,7 +368,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (w == 0) tc::tmem_dealloc(taddr, 128);
+    if (w == 0) tc::tmem_dealloc(taddr, TCOLS);
 }
 
 
@@ -367,7 +379,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 //   dDelta = scale DT + DA                                  (lanes 0..63)
 //   DQ = Qg^T dO,  DW = W^T dDelta                          (M = 128 keys)
 //   dS0 = e^gL * dS1 + scale DQ - DW                        (every thread, its own key row)
-// Only DA and DW lie on the serial path from one gradient to the next.  DT and DQ do not depend
+// Only DA and DW lie on the serial path from one gradient to the next.  DA and DW take their B
+// operand's hi and lo planes side by side along N, as in the forward.  DT and DQ do not depend
 // on it: DQ is issued right behind DA (it runs while dDelta is formed), DT of the next chunk right
 // behind DW (it runs while dS0 is formed), on a double-buffered Aqk / dO tile pair.
 // mode CHAIN_BWD: dS from dht; writes the dS1 and dDelta planes of every chunk and dh0.
@@ -430,7 +443,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             tc::tma_prefetch_map(&tm.mdO);
         }
     }
-    if (w == 0) tc::tmem_alloc(tslot, 256);
+    constexpr bool W64 = VW == 64;  // lo planes in their own tiles (else beside hi, at column VW)
+    constexpr uint32_t TCOLS = W64 ? 512 : 256;
+    if (w == 0) tc::tmem_alloc(tslot, TCOLS);
 
     float dSr[VPT];
 #pragma unroll
@@ -440,12 +455,23 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t taddr = *tslot;
-    // TMEM columns: DA 0..63, DT 64..127, DQ 128..191, DW 192..255
+    // TMEM columns (DA and DW as two VW-column halves each): DA 0.., DT 64.., DQ 128.., DW 192..
+    // (64-column blocks: DA 0..127, DW 128..255, DT 256..319, DQ 320..383)
     const uint32_t tl = taddr + (uint32_t(32 * qd) << 16);
-    const uint32_t tDA = tl, tDT = tl + 64, tDQ = tl + 128, tDW = tl + 192;
+    constexpr uint32_t cDA = 0, cDT = W64 ? 256 : 64, cDQ = W64 ? 320 : 128, cDW = W64 ? 128 : 192;
+    const uint32_t tDA = tl + cDA, tDT = tl + cDT, tDQ = tl + cDQ, tDW = tl + cDW;
 
     const uint32_t IDA1 = tc::idesc_bf16(128, VW, false, true);  // Kb K-major, dS1 MN-major
     const uint32_t IDMN = tc::idesc_bf16(128, VW, true, true);   // MN-major A and B
+    const uint32_t IDA1c = tc::idesc_bf16(128, 2 * VW, false, true), IDMNc = tc::idesc_bf16(128, 2 * VW, true, true);
+    // sum of the two column halves of an accumulator
+    auto tld = [&](uint32_t tcol, float (&v)[VPT]) {
+        float v2[VPT];
+        tc::tmem_ld<VPT>(tcol, v);
+        tc::tmem_ld<VPT>(tcol + VW, v2);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) v[j] += v2[j];
+    };
     const uint32_t sKb = smem_u32(sm + B_OFF_KB), sQg = smem_u32(sm + B_OFF_QG);
     const uint32_t sW = smem_u32(sm + B_OFF_W), sdS = smem_u32(sm + B_OFF_DS);
     const uint32_t sdD = smem_u32(sm + B_OFF_DD);
@@ -487,7 +513,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         for (int t2 = 0; t2 < 2; ++t2)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                tc::mma(taddr + 64, (t2 ? ah : al) + uint64_t((s * 2048) >> 4),
+                tc::mma(taddr + cDT, (t2 ? ah : al) + uint64_t((s * 2048) >> 4),
                         bo + uint64_t((s * 2048) >> 4), IDMN, acc);
                 acc = 1;
             }
@@ -522,7 +548,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         uint32_t sh_[VPT / 2], sl_[VPT / 2];  // dS1 operand split (its saved planes are written below)
         tc::split_n<VPT>(dSr, sh_, sl_);
         tc::st_sw128_n<VPT>(sm + B_OFF_DS, row, cc, sh_);
-        tc::st_sw128_n<VPT>(sm + B_OFF_DS + 16384, row, cc, sl_);
+        tc::st_sw128_n<VPT>(sm + B_OFF_DS + (W64 ? 16384 : 0), row, (W64 ? 0 : VW) + cc, sl_);
         tc::fence_async_smem();
         // the previous chunk's dDelta store has read its tile (rewritten below this barrier)
         if (tsave && tid == 0) tc::bulk_wait_read0();
@@ -536,17 +562,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             if (tc::mbar_wait(&bar[0], ph)) {
                 tc::fence_after_sync();
                 const uint64_t kh = tc::sdesc(sKb, 16, 1024), kl = tc::sdesc(sKb + 16384, 16, 1024);
-                const uint64_t dh_ = tc::sdesc(sdS, 1024, 1024), dl_ = tc::sdesc(sdS + 16384, 1024, 1024);
-                const uint64_t ta[3] = {kh, kl, kh}, tb[3] = {dl_, dh_, dh_};
-                uint32_t acc = 0;
+                const uint64_t dh_ = tc::sdesc(sdS, 1024, 1024);
+                const uint64_t dhl = tc::sdesc(sdS, W64 ? 16384 : 1024, 1024);  // [hi | lo] along N
 #pragma unroll
-                for (int t3 = 0; t3 < 3; ++t3)
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        tc::mma(taddr, ta[t3] + uint64_t(((s >> 2) * 8192 + (s & 3) * 32) >> 4),
-                                tb[t3] + uint64_t((s * 2048) >> 4), IDA1, acc);
-                        acc = 1;
-                    }
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t ak = uint64_t(((s >> 2) * 8192 + (s & 3) * 32) >> 4);
+                    const uint64_t bk = uint64_t((s * 2048) >> 4);
+                    tc::mma(taddr + cDA, kh + ak, dhl + bk, IDA1c, s > 0 ? 1u : 0u);
+                    tc::mma(taddr + cDA, kl + ak, dh_ + bk, IDA1, 1u);
+                }
             } else {
                 *abort_flag = 1;
             }
@@ -560,7 +584,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
                 for (int t2 = 0; t2 < 2; ++t2)
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        tc::mma(taddr + 128, (t2 ? qh : ql) + uint64_t((s * 2048) >> 4),
+                        tc::mma(taddr + cDQ, (t2 ? qh : ql) + uint64_t((s * 2048) >> 4),
                                 bo + uint64_t((s * 2048) >> 4), IDMN, acc);
                         acc = 1;
                     }
@@ -592,13 +616,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         uint32_t xh[VPT / 2], xl[VPT / 2];
         if (qd < 2) {
             float a[VPT], t[VPT];
-            tc::tmem_ld<VPT>(tDA + cc, a);
+            tld(tDA + cc, a);
             tc::tmem_ld<VPT>(tDT + cc, t);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) a[j] = fmaf(p.scale, t[j], a[j]);
             tc::split_n<VPT>(a, xh, xl);
             tc::st_sw128_n<VPT>(sm + B_OFF_DD, row, cc, xh);
-            tc::st_sw128_n<VPT>(sm + B_OFF_DD + 8192, row, cc, xl);
+            tc::st_sw128_n<VPT>(sm + B_OFF_DD + (W64 ? 8192 : 0), row, (W64 ? 0 : VW) + cc, xl);
         }
         if (tid == LD) {
             if (!tc::mbar_wait(&bar[7], ph)) *abort_flag = 1;  // DQ done: the Qg buffer is free
@@ -623,17 +647,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             if (tc::mbar_wait(&bar[4], ph)) {
                 tc::fence_after_sync();
                 const uint64_t wh = tc::sdesc(sW, 8192, 1024), wl = tc::sdesc(sW + 16384, 8192, 1024);
-                const uint64_t dxh = tc::sdesc(sdD, 1024, 1024), dxl = tc::sdesc(sdD + 8192, 1024, 1024);
-                const uint64_t ta[3] = {wh, wl, wh}, tb[3] = {dxl, dxh, dxh};
-                uint32_t acc = 0;
+                const uint64_t dxh = tc::sdesc(sdD, 1024, 1024);
+                const uint64_t dxhl = tc::sdesc(sdD, W64 ? 8192 : 1024, 1024);  // [hi | lo] along N
 #pragma unroll
-                for (int t3 = 0; t3 < 3; ++t3)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        tc::mma(taddr + 192, ta[t3] + uint64_t((s * 2048) >> 4),
-                                tb[t3] + uint64_t((s * 2048) >> 4), IDMN, acc);
-                        acc = 1;
-                    }
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t kk = uint64_t((s * 2048) >> 4);
+                    tc::mma(taddr + cDW, wh + kk, dxhl + kk, IDMNc, s > 0 ? 1u : 0u);
+                    tc::mma(taddr + cDW, wl + kk, dxh + kk, IDMN, 1u);
+                }
             } else {
                 *abort_flag = 1;
             }
@@ -673,7 +694,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
         {
             float q[VPT], x[VPT];
             tc::tmem_ld<VPT>(tDQ + cc, q);
-            tc::tmem_ld<VPT>(tDW + cc, x);
+            tld(tDW + cc, x);
 #pragma unroll
             for (int j = 0; j < VPT; ++j) dSr[j] = fmaf(eg, dSr[j], fmaf(p.scale, q[j], -x[j]));
         }
@@ -701,7 +722,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (w == 0) tc::tmem_dealloc(taddr, 256);
+    if (w == 0) tc::tmem_dealloc(taddr, TCOLS);
 }
 
 // Launchers (the kernels are templates on the value width): the narrowest of VW = 16, 32 whose

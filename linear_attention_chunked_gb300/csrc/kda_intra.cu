@@ -202,16 +202,54 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
     tc::fence_after_sync();
     const uint32_t taddr = S.tslot;
     uint32_t mph = 0, gph = 0;  // phase parities of the MMA and gate barriers
+    // An item's gate rows in place (dense tile: g, or the raw form's -exp(A_log) softplus(a +
+    // dt_bias); zero past the document end) and its cleared 64 x 64 accumulators, done before its
+    // step 1 -- for every item but the first while the previous item's step-6 MMAs run.
+    auto prep = [&](int Ln) {
+        for (int i = tid; i < CH * LA / 4; i += BT) {  // (each tile is 16-byte aligned, 4352 floats)
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            reinterpret_cast<float4*>(S.Akk)[i] = z;
+            reinterpret_cast<float4*>(S.Aqk)[i] = z;
+            reinterpret_cast<float4*>(S.Mi)[i] = z;
+        }
+        const float eA = p.gate_raw ? expf(peA) : 0.f;
+        bool bad_gate = false;
+        if (!tc::mbar_wait(&S.mbar[2], gph)) S.abort = 1;  // the gate tile (dense rows)
+        gph ^= 1u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = (tid + BT * k) >> 5;
+            float4* g4p = reinterpret_cast<float4*>(&S.gam[r * D + c4t]);
+            const float4 g4 = *g4p;
+            float x[4] = {g4.x, g4.y, g4.z, g4.w};
+            const float b4[4] = {pdb.x, pdb.y, pdb.z, pdb.w};
+            if (p.gate_raw) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = r < Ln ? -eA * softplus_f(x[j] + b4[j]) : 0.f;
+            } else {
+                // the exponent-difference factorisation needs a decaying gate: g <= 0 (NaN fails)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    x[j] = r < Ln ? x[j] : 0.f;
+                    bad_gate |= !(x[j] <= 0.f);
+                }
+            }
+            *g4p = make_float4(x[0], x[1], x[2], x[3]);  // this thread's own elements
+        }
+        // reported in the status word; the state recurrences and backward kernels of this call
+        // then do nothing
+        if (bad_gate) p.status[0] = KDA_ERR_DEVICE_CHECK;
+    };
     if (int(blockIdx.x) < items) {
         fetch(blockIdx.x, p.chunk_tab[blockIdx.x / p.H], 7);
         fetch_v();
+        prep(nL);
     }
 
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int L = nL;  // this item's length (its fetch was the latest one)
     const size_t chd = size_t(item);
 
-    // 1. inputs (fetched one item ahead) to shared memory, gate, beta; clear the 64x64 accumulators
+    // 1. inputs (fetched one item ahead) to shared memory, gate, beta
     float4 gx[4];  // this thread's gate values (rows w + 16 k), written to the padded tile after
                    // the barrier below (every dense row has been read by then)
     {
@@ -237,38 +275,8 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             dk[0] = make_float4(fk[0], fk[1], fk[2], fk[3]);
             dk[1] = make_float4(fk[4], fk[5], fk[6], fk[7]);
         }
-        const float eA = p.gate_raw ? expf(peA) : 0.f;
-        bool bad_gate = false;
-        if (!tc::mbar_wait(&S.mbar[2], gph)) S.abort = 1;  // this item's gate tile (dense rows)
-        gph ^= 1u;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int r = (tid + BT * k) >> 5;
-            const float4 g4 = *reinterpret_cast<const float4*>(&S.gam[r * D + c4t]);
-            float x[4] = {g4.x, g4.y, g4.z, g4.w};
-            const float b4[4] = {pdb.x, pdb.y, pdb.z, pdb.w};
-            if (p.gate_raw) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) x[j] = r < L ? -eA * softplus_f(x[j] + b4[j]) : 0.f;
-            } else {
-                // the exponent-difference factorisation needs a decaying gate: g <= 0 (NaN fails)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    x[j] = r < L ? x[j] : 0.f;
-                    bad_gate |= !(x[j] <= 0.f);
-                }
-            }
-            gx[k] = make_float4(x[0], x[1], x[2], x[3]);
-        }
-        // reported in the status word; the state recurrences and backward kernels of this call
-        // then do nothing
-        if (bad_gate) p.status[0] = KDA_ERR_DEVICE_CHECK;
-    }
-    for (int i = tid; i < CH * LA / 4; i += BT) {  // (each tile is 16-byte aligned, 4352 floats)
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        reinterpret_cast<float4*>(S.Akk)[i] = z;
-        reinterpret_cast<float4*>(S.Aqk)[i] = z;
-        reinterpret_cast<float4*>(S.Mi)[i] = z;
+        for (int k = 0; k < 4; ++k) gx[k] = *reinterpret_cast<const float4*>(&S.gam[((tid + BT * k) >> 5) * D + c4t]);
     }
     __syncthreads();
     const bool more = item + int(gridDim.x) < items;
@@ -649,6 +657,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const 
             }
         tc::mma_commit(&S.mbar[0]);
     }
+    // while the MMAs run: the next item's gate rows (landed during steps 6-7) and clears; the
+    // small 64 x 64 tiles were last read by the staging pass above
+    if (more) prep(nL);
     // epilogue: warps w % 4 < 2 hold the token rows (TMEM lanes 0..63), 32 columns each (w / 4):
     // U straight to global memory, W split into its staging tile (u: the MMAs have read beta K
     // e^gam by then)

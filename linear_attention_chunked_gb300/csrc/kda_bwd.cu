@@ -59,6 +59,7 @@ struct BwdIntraSmem {
     // TMA completion of the next item's inputs: 0 dAqk / dM, 1 q / k / rows 0..31 of dQg, P, dKb,
     // dR, 2 gam / Akk / rows 32..63 of dQg, P
     uint64_t bar[3];
+    int2 ntab;  // first token and length of the next item (written by thread 0 after step 1)
     int abort;  // a wait timed out
 };
 constexpr size_t BWD_INTRA_SMEM = sizeof(BwdIntraSmem) + 1024;  // + alignment slack of the base
@@ -113,23 +114,27 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     uint2 hv[2];          // and of its v
     uint2 pv[2];           // v, first half, of the next item
     float pb = 0.f;        // beta of the next item (threads < 64)
-    int4 ntab = make_int4(0, 0, 0, 0);
     int nT0 = 0, nL = 0, nh = 0;  // first token, length and head of the next item
     // The copies of each part are issued by lane 0 of different warps, one each, so their issue
     // costs (hundreds of cycles per copy) overlap; thread 0 sets the part's expected bytes before a
     // barrier that precedes every issue.
-    auto expectA = [&]() { tc::mbar_expect_tx(&S.bar[0], 2u * CH * CH * 4u); };
-    auto expectB = [&]() { tc::mbar_expect_tx(&S.bar[1], 4u * CH * 64u * 2u + 4u * 32u * D * 4u); };
+    // Without the L2 norm q and k are not read after step 4, so they come with part A; the staged
+    // rows of part B are then first needed in step 2, and step 1 runs while they land.
+    constexpr bool QKE = !L2N;
+    auto expectA = [&]() { tc::mbar_expect_tx(&S.bar[0], 2u * CH * CH * 4u + (QKE ? 4u * CH * 64u * 2u : 0u)); };
+    auto expectB = [&]() { tc::mbar_expect_tx(&S.bar[1], (QKE ? 0u : 4u * CH * 64u * 2u) + 4u * 32u * D * 4u); };
     auto expectC = [&]() { tc::mbar_expect_tx(&S.bar[2], CH * D * 4u + CH * CH * 4u + 2u * 32u * D * 4u); };
-    // part A: dAqk, dM by TMA (warps 0..3); the chunk-table entry to registers
+    // part A: dAqk, dM by TMA (warps 0..3), and (QKE) q, k (warps 4..7); S.ntab holds the item's
+    // first token and length
     auto fetchA = [&](int item) {
-        if (w < 4 && lane == 0) {
+        if (w < (QKE ? 8 : 4) && lane == 0) {
             tc::fence_async_smem();  // the tiles' earlier generic accesses come first
             const int hb = w & 1;
             if (w < 2) tc::tma3(S.dA + hb * CH * 32, &tm.mdA, 32 * hb, 0, item, &S.bar[0]);
-            else tc::tma3(S.dAk + hb * CH * 32, &tm.mdM, 32 * hb, 0, item, &S.bar[0]);
+            else if (w < 4) tc::tma3(S.dAk + hb * CH * 32, &tm.mdM, 32 * hb, 0, item, &S.bar[0]);
+            else if (w < 6) tc::tma3(S.qb + hb * CH * 64, &tm.mq, 64 * hb, item % p.H, S.ntab.x, &S.bar[0]);
+            else tc::tma3(S.kb + hb * CH * 64, &tm.mk, 64 * hb, item % p.H, S.ntab.x, &S.bar[0]);
         }
-        ntab = p.chunk_tab[item / p.H];
     };
     // part C: gam by TMA (warps 0..3), Akk and rows 32..63 of dQg, P by bulk copies (warps 4..6)
     auto fetchC = [&](int item) {
@@ -158,12 +163,12 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     // part B: the item's 64 token rows of q and k (rows past the document end are cleared once
     // they land) and rows 0..31 of dQg, P, dKb, dR by TMA (warps 0..7); v and beta to registers
     auto fetchB = [&](int item) {
-        const int T0 = ntab.y, Ln = ntab.z, hh = item % p.H;
+        const int T0 = S.ntab.x, Ln = S.ntab.y, hh = item % p.H;
         nT0 = T0;
         nL = Ln;
         nh = hh;
         const size_t nchd = size_t(item);
-        if (w < 8 && lane == 0) {
+        if (w >= (QKE ? 4 : 0) && w < 8 && lane == 0) {
             tc::fence_async_smem();
             const int hb = w & 1;
             if (w < 2) {
@@ -191,6 +196,8 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         }
     };
     if (tid == 0) {
+        const int4 e = p.chunk_tab[blockIdx.x / p.H];
+        S.ntab = make_int2(e.y, e.z);
         tc::mbar_init(&S.bar[0], 1);
         tc::mbar_init(&S.bar[1], 1);
         tc::mbar_init(&S.bar[2], 1);
@@ -214,8 +221,12 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
 
     // 1. inputs: the prefetched tiles and registers to shared memory; dAkk = beta_r dM; per-row
     //    L2 scales
-    if (!(tc::mbar_wait(&S.bar[0], ph) && tc::mbar_wait(&S.bar[1], ph) && tc::mbar_wait(&S.bar[2], ph))) S.abort = 1;
+    if (!(tc::mbar_wait(&S.bar[0], ph) && (QKE || tc::mbar_wait(&S.bar[1], ph)) && tc::mbar_wait(&S.bar[2], ph)))
+        S.abort = 1;
+    const uint32_t phb = ph;  // (QKE: part B is waited for before step 2)
     ph ^= 1u;
+    int4 nxt = make_int4(0, 0, 0, 0);  // the next item's chunk-table entry (thread 0; to S.ntab below)
+    if (tid == 0 && more) nxt = p.chunk_tab[(item + gridDim.x) / p.H];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {  // q, k rows past the document end read as zero
         const int i = tid + BT * k, r = i >> 4, j = i & 15;
@@ -237,6 +248,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     }
     if (tid < CH) S.beta[tid] = pb;
     __syncthreads();  // beta, the zero rows of q / k
+    if (tid == 0) S.ntab = make_int2(nxt.y, nxt.z);  // every fetch of this item's entry is done
     if (*reinterpret_cast<volatile int*>(&S.abort)) break;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -261,6 +273,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
         }
     }
     __syncthreads();
+    if (QKE && !tc::mbar_wait(&S.bar[1], phb)) S.abort = 1;  // rows 0..31 of dQg, P, dKb, dR
 
     // 2. elementwise terms through Qg, Kg, Kb and the diagonal of Aqk; dv = beta dR; dbeta_r +=
     //    dR_r . v_r - Kg_r . P_r (one warp per row, fixed-order warp sums)
@@ -601,11 +614,7 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     const float aLog = p.gate_raw ? p.A_log[h] : 0.f;
     const float rs0 = p.rsum[chd * 2 * D + (tid & (D - 1))];  // rowsum(S_c * dS1): two partials
     const float rs1 = p.rsum[chd * 2 * D + D + (tid & (D - 1))];
-    if (more) {
-        fetchA(item + gridDim.x);
-    } else {
-        ntab = make_int4(0, 0, 0, 0);
-    }
+    if (more) fetchA(item + gridDim.x);
 
     // 5. chunk-end gate term dgL = e^gL rowsum(S0 * dS1) + sum_r dKb * Kb, then the reverse
     //    cumsum over the chunk; four threads per channel (16 rows each), fixed order

@@ -656,7 +656,7 @@ kda_status kda_bwd(const kda_problem* pr, const void* q, const void* k, const vo
     }
     if (p.gate_raw) {
         ProfScope ps(KK_PARAM_REDUCE, st);
-        k_param_reduce<<<pr->H, D, 0, st>>>(p);
+        k_param_reduce<<<pr->H, 4 * D, 0, st>>>(p);
     }
     return launched();
 }

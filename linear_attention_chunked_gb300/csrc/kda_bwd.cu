@@ -767,16 +767,26 @@ void launch_bwd_intra(const Params& p, const TcMaps& tm, unsigned grid, cudaStre
 
 // Fixed-order sums of the per-chunk partials: dA_log[h], ddt_bias[h, :].
 __global__ void k_param_reduce(Params p) {
-    const int h = blockIdx.x, c = threadIdx.x;
+    // 512 threads: channel c = tid % 128 of quarter q = tid / 128 sums the chunks ci = q (mod 4) in
+    // increasing order, then the four quarter sums are added in quarter order; warp 0 also sums the
+    // dA_log partials, lane l taking ci = l (mod 32), then a fixed-order warp reduction.  The order
+    // is fixed, so the results are bitwise reproducible.
+    __shared__ float part[4][D];
+    const int h = blockIdx.x, tid = threadIdx.x, c = tid & (D - 1), q = tid >> 7;
     const int nc = *p.nchunks;
     float s = 0.f;
-    for (int ci = 0; ci < nc; ++ci) s += p.pddt[(size_t(ci) * p.H + h) * D + c];
-    p.ddt_bias[h * D + c] = s;
-    if (c == 0) {
+#pragma unroll 8
+    for (int ci = q; ci < nc; ci += 4) s += p.pddt[(size_t(ci) * p.H + h) * D + c];
+    part[q][c] = s;
+    if (tid < 32) {
         float a = 0.f;
-        for (int ci = 0; ci < nc; ++ci) a += p.pdA[size_t(ci) * p.H + h];
-        p.dA_log[h] = a;
+#pragma unroll 4
+        for (int ci = tid; ci < nc; ci += 32) a += p.pdA[size_t(ci) * p.H + h];
+        a = warp_sum(a);
+        if (tid == 0) p.dA_log[h] = a;
     }
+    __syncthreads();
+    if (q == 0) p.ddt_bias[h * D + c] = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
 }
 
 }  // namespace kda

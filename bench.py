@@ -146,7 +146,7 @@ class ClockSampler:
 
 def alg_bytes_per_token_head(kernel, out_bytes=4):
     """Method inputs and outputs the kernel must touch, per token-head; out_bytes = bytes of one
-    o / dq / dk / dv / dbeta element (4: fp32 outputs, 2: bf16 outputs as SURVEY 8(d) counts)."""
+    o / dq / dk / dv / dbeta element (4: fp32 outputs, 2: bf16 outputs, the inputs' format)."""
     qkv, beta, gate, dO = 3 * 256, 2, 512, 256
     o, dqkv, dbeta, dg = 128 * out_bytes, 3 * 128 * out_bytes, out_bytes, 512
     table = {
@@ -162,7 +162,8 @@ def alg_bytes_per_token_head(kernel, out_bytes=4):
 def step_bytes_per_token_head(out_bytes):
     """Algorithmic bytes of a whole fwd (and fwd+bwd) per token-head: q, k, v, beta, gate in,
     o out; the backward reads them and dO again and writes dq, dk, dv, dbeta, dg.  out_bytes = 2
-    gives SURVEY 8(d)'s 1,538 / 4,358 B; 4 (the library's fp32 outputs) 1,794 / 5,384 B."""
+    (outputs in the inputs' bf16 format) gives 1,538 / 4,358 B; 4 (the library's fp32 outputs)
+    1,794 / 5,384 B."""
     inputs = 3 * 256 + 2 + 512
     fwd = inputs + 128 * out_bytes
     bwd = inputs + 256 + 3 * 128 * out_bytes + out_bytes + 512
@@ -212,7 +213,7 @@ def _time_calls(fn, samples=15, calls=20):
 
 
 # per token-head: method inputs and outputs (q, k, v, beta, gate, o; + dO, dq, dk, dv, dbeta, dg)
-# with bf16 outputs and with the fp32 outputs every bench run writes, and FLOPs of
+# with bf16 outputs (the inputs' format) and with the fp32 outputs every bench run writes, and FLOPs of
 # the chunked method with 64-token chunks, head dim 128
 BYTES_FWD, BYTES_FWD_BWD = step_bytes_per_token_head(2)        # 1,538 / 4,358
 BYTES_FWD_F32, BYTES_FWD_BWD_F32 = step_bytes_per_token_head(4)  # 1,794 / 5,384
@@ -552,7 +553,7 @@ def main():
     hbm, bf16, src = load_peaks()
     step_roof = {
         "bound": "hbm", "peak": hbm, "unit": "GB/s", "peak_source": src,
-        "survey_bytes_per_token_head": BYTES_FWD_BWD,
+        "bf16_out_bytes_per_token_head": BYTES_FWD_BWD,
         "frac": T * H * BYTES_FWD_BWD / (ms * 1e6) / hbm,
         "fp32_out_bytes_per_token_head": BYTES_FWD_BWD_F32,
         "frac_fp32_out": T * H * BYTES_FWD_BWD_F32 / (ms * 1e6) / hbm,

@@ -87,12 +87,13 @@ static_assert(offsetof(BwdIntraSmem, akk) % 16 == 0 && offsetof(BwdIntraSmem, dG
 // Persistent: one block per SM walks the items item = chunk * H + head.  The inputs of its next
 // item are fetched while the current one is computed, in three parts that land in tiles the
 // current item no longer reads (each copy issued by lane 0 of its own warp, completion on an
-// mbarrier per part): once step 4 is done, dAqk and dM (TMA); once step 7 is done (it runs ahead
-// of step 6), gam (TMA, into its swizzled tile), Akk (into the union) and rows 32..63 of dQg and P
-// (into the dG tile); once step 6 is done, q, k (TMA) and rows 0..31 of dQg, P, dKb, dR (into the
-// dQ / dK tiles).  Only rows 32..63 of dKb and dR (after step 5), v and beta go to registers.  The
-// register loads of the rest filled the SM's outstanding-request capacity and stalled the warps
-// issuing them.  Every wait is bounded; after a timeout the block stops and reports.
+// mbarrier per part): once step 4 is done, dAqk and dM (TMA), and q, k (TMA) when the L2 norm is
+// off; once step 7 is done (it runs ahead of step 6), gam (TMA, into its swizzled tile), Akk (into
+// the union) and rows 32..63 of dQg and P (into the dG tile); once step 6 is done, rows 0..31 of
+// dQg, P, dKb, dR (into the dQ / dK tiles) and, with the L2 norm (step 6 reads q, k), q and k.
+// Only rows 32..63 of dKb and dR (after step 5), v and beta go to registers.  The register loads
+// of the rest filled the SM's outstanding-request capacity and stalled the warps issuing them.
+// Every wait is bounded; after a timeout the block stops and reports.
 // L2N: the fused L2 norm of q and k is on (row scales rq, rk and their backward); off, the scales
 // are 1 and every multiply by them is compiled out.
 template <bool L2N>

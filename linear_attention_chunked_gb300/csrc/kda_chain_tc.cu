@@ -6,15 +6,15 @@
 //   MMA2  D2 = Kb^T Delta                M = 128 keys, N = VW, K = 64 tokens
 //   MMA3  D1 += [*; Aqk] Delta           rows 64..127: O = Qg S + Aqk Delta
 //         S  = e^gL * S + D2             (every thread, its own row)
-// Every product is split into bf16 hi/lo terms (a_hi b_lo + a_lo b_hi + a_hi b_hi, FP32 accumulate
-// in TMEM), which keeps ~16 significant bits per operand.  The B operand's hi and lo planes sit
-// side by side along N (64-column blocks: two 64-column atoms, the lo plane one plane stride away;
-// narrower blocks: the lo values at column VW of the hi tile): one N = 2 VW MMA gives a_hi b_hi
-// and a_hi b_lo in two TMEM column halves, a_lo b_hi adds onto the first, and the epilogues sum
-// the halves -- two MMAs per K step instead of three, A read twice instead of three times, and
-// the same arithmetic for every block width (bitwise equal results).  Rows 0..63 of the MMA3 A operand are
-// whatever precedes the hi / lo Aqk tiles (zeros / the hi tile): they only touch D1 rows whose W S
-// values were already consumed.
+// Every product is split into bf16 hi/lo terms (a_hi b_lo + a_lo b_hi + a_hi b_hi, FP32
+// accumulate in TMEM), which keeps ~16 significant bits per operand.  The B operand's hi and lo
+// planes sit side by side along N (64-column blocks: two 64-column atoms, the lo plane one plane
+// stride away; narrower blocks: the lo values at column VW of the hi tile): one N = 2 VW MMA gives
+// a_hi b_hi and a_hi b_lo in two TMEM column halves, a_lo b_hi adds onto the first, and the
+// epilogues sum the halves -- two MMAs per K step instead of three, A read twice instead of three
+// times, and the same arithmetic for every block width (bitwise equal results).  Rows 0..63 of
+// the MMA3 A operand are whatever precedes the hi / lo Aqk tiles (zeros / the hi tile): they only
+// touch D1 rows whose W S values were already consumed.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -26,10 +26,10 @@ namespace {
 // swizzled (see kda_tc.cuh); "plane" 0 = hi, 1 = lo.
 constexpr int OFF_KT = 0;        // Kb as MN-major A: [plane][2 key blocks][64 tokens][128 B]  32 KB
 constexpr int OFF_A1 = 32768;    // [W; Qg] K-major: [plane][2 key blocks][128 rows][128 B]    64 KB
-constexpr int OFF_S = 98304;     // S as MN-major B: [plane][128 keys][128 B]                  32 KB
+constexpr int OFF_S = 98304;     // S as MN-major B: [plane][128 keys][128 B] (VW < 64: one plane) 32 KB
 constexpr int OFF_PAD = 131072;  // 8 KB of zeros: rows 0..63 of the hi MMA3 operand
 constexpr int OFF_AQ = 139264;   // Aqk K-major: [plane][64 tokens][128 B]                     16 KB
-constexpr int OFF_DL = 155648;   // Delta as MN-major B: [plane][64 tokens][128 B]             16 KB
+constexpr int OFF_DL = 155648;   // Delta as MN-major B: [plane][64 tokens][128 B] (likewise)  16 KB
 constexpr int OFF_BAR = 172032;  // mbarriers, TMEM base address, abort flag
 constexpr size_t CHAIN_TC_SMEM = OFF_BAR + 128 + 1024;  // + alignment slack of the base
 

@@ -123,16 +123,17 @@ __device__ __forceinline__ void diag_pair_sums(const float* q, const float* k, c
 
 size_t intra_smem_bytes() { return sizeof(IntraSmem) + 1024; }  // + alignment slack of the base
 
-// Persistent: one block per SM walks the (chunk, head) items item = chunk * H + head; the raw
-// inputs of its next item are loaded into registers while the current one is computed, in three
-// bursts (q, k, then the gate) so that no burst fills the memory request queue of the SM.  The
-// hi / lo planes of Aqk, Minv and W and Akk leave through TMA stores from staging tiles (lane 0 of
-// one warp per store issues it and waits for its reads of shared memory before the tile is
-// rewritten, so the issue costs overlap): the small matrices' stores run during step 6, W's during
-// the next item's first steps.  Step 6 (W
-// and U) runs as tcgen05 MMAs issued by thread 0 into 256 TMEM columns held for the whole kernel;
-// every wait on their completion is bounded (on expiry the block reports KDA_ERR_TIMEOUT, lets
-// its MMAs drain, frees its TMEM and stops).
+// Persistent: one block per SM walks the (chunk, head) items item = chunk * H + head.  The next
+// item's q and k are loaded into registers in two bursts (so no burst fills the memory request
+// queue of the SM), its gate tile by one TMA copy and its v tile by cp.async while the current
+// item is computed; while the current item's step-6 MMAs run, the block prepares the next item's
+// gate rows and clears its 64 x 64 tiles.  The hi / lo planes of Aqk, Minv and W and Akk leave
+// through TMA stores from staging tiles (lane 0 of one warp per store issues it and waits for its
+// reads of shared memory before the tile is rewritten, so the issue costs overlap): the small
+// matrices' stores run during step 6, W's during the next item's first steps.  Step 6 (W and U)
+// runs as tcgen05 MMAs issued by thread 0 into 256 TMEM columns held for the whole kernel; every
+// wait on their completion is bounded (on expiry the block reports KDA_ERR_TIMEOUT, lets its MMAs
+// drain, frees its TMEM and stops).
 __global__ void __launch_bounds__(INTRA_THREADS, 1) k_intra_fwd(Params p, const __grid_constant__ TcMaps tm) {
     constexpr int BT = INTRA_THREADS, NW = BT / 32;
     extern __shared__ __align__(16) unsigned char smraw[];

@@ -360,14 +360,17 @@ __global__ void __launch_bounds__(BI_THREADS, 1) k_bwd_intra(Params p, const __g
     // split A fragments of dAqk and dAkk, built once: 12 "as row" (i, ks<i) and 12 "as column"
     // (j, ks>j) fragments, index = 2 * pair + (0: dAqk, 1: dAkk)
     {
-        constexpr int2 kRow[6] = {{1, 0}, {2, 0}, {2, 1}, {3, 0}, {3, 1}, {3, 2}};
-        constexpr int2 kCol[6] = {{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}, {2, 3}};
         for (int f = w; f < 24; f += NW) {
             const bool col = f >= 12;
             const int pi = (f % 12) >> 1, src = f & 1;
             const float* A = src ? S.dAk : S.dA;
-            const int m0 = 16 * (col ? kCol[pi].x : kRow[pi].x);
-            const int k0 = 16 * (col ? kCol[pi].y : kRow[pi].y);
+            // pair pi: as row (i, ks) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2); as column (j, ks) =
+            // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3) -- by arithmetic (an indexed table would live in
+            // local memory)
+            const int ri = pi < 1 ? 1 : pi < 3 ? 2 : 3, rk = pi - ri * (ri - 1) / 2;
+            const int cj = pi < 3 ? 0 : pi < 5 ? 1 : 2, ck = pi + 1 - (cj == 0 ? 0 : cj == 1 ? 2 : 3);
+            const int m0 = 16 * (col ? cj : ri);
+            const int k0 = 16 * (col ? ck : rk);
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
